@@ -1,0 +1,266 @@
+/*
+ * snip.h -- C ABI of the quantized linear layer for sub-byte mixed-precision
+ * LLM training on GB300 (sm_103a).
+ *
+ * What it computes (page title, section):
+ *  - "SNIP: An Adaptive Mixed Precision Framework for Subbyte Large Language
+ *    Model Training", Figure 5: a linear layer whose forward GEMM Y = X W^T,
+ *    dgrad dX = dY W and wgrad dW = dY^T X run in the layer's low precision,
+ *    each operand quantized along that GEMM's own contraction dimension;
+ *    Abstract / Figure 2: one format (FP8 or FP4) per layer, chosen by a plan;
+ *    periodic statistics on activations, weights and gradients.
+ *  - "FP4 all the way" (Chmiel, Fishman, Banner, Soudry), summary page,
+ *    Outline: the FP4 format is NVFP4 -- blocks of 16 E2M1 values sharing one
+ *    E4M3 scale -- with round-to-nearest in the forward pass and stochastic
+ *    rounding in the backpropagation and update passes; quantized training
+ *    loses efficiency once the gradient norm drops below about sqrt(3) times
+ *    the quantization noise.
+ *  - "Research on Mixed-Precision Training for LLMs", stochastic rounding
+ *    paragraph: round up or down with probabilities that keep the expected
+ *    value.
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory (except tensor memory inside its GEMM kernels,
+ *    which is freed before each kernel exits).  Host pointers are marked.
+ *  - Tensors are dense row-major.  bf16 inputs are passed as `const void*` to
+ *    2-byte IEEE bfloat16 values.  Device pointers must be 16-byte aligned
+ *    (SNIP_ERR_ALIGN otherwise).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are returned synchronously and launch
+ *    nothing.  Errors found on the device (non-finite input, a kernel wait
+ *    that timed out) are OR-ed into the status word of the caller's workspace
+ *    and read with snip_workspace_status().
+ *  - Workspace: a caller-owned device buffer of at least the size returned by
+ *    the matching *_workspace_size() call.  Its first SNIP_WS_HEADER_BYTES hold
+ *    the sticky device status word; initialise them once with
+ *    snip_workspace_init().  Calls that share a workspace must be ordered on
+ *    one stream.
+ *  - Random bits for stochastic rounding come from Philox4x32-10 (Salmon et
+ *    al., SC'11) keyed by `seed`; source element e (row-major index into the
+ *    tensor being quantized, whatever the output orientation) uses 16 bits of
+ *    the call with counter (e/8, stream_id): word (e/2) mod 4, low half for
+ *    even e.  A result is therefore a pure function of (input, seed,
+ *    stream_id).
+ */
+#ifndef SNIP_H
+#define SNIP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SNIP_OK = 0,
+    SNIP_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, negative size    */
+    SNIP_ERR_SHAPE = 2,             /* a dimension breaks the multiple-of-16 rule */
+    SNIP_ERR_ALIGN = 3,             /* a device pointer is not 16-byte aligned  */
+    SNIP_ERR_NONFINITE = 4,         /* (device) the input held an Inf or NaN     */
+    SNIP_ERR_TIMEOUT = 5,           /* (device) a kernel wait gave up            */
+    SNIP_ERR_CUDA = 6,              /* a CUDA runtime call failed                */
+    SNIP_ERR_UNSUPPORTED_DEVICE = 7,/* the current device is not sm_103          */
+    SNIP_ERR_WORKSPACE = 8          /* workspace missing or too small            */
+} snip_status;
+
+typedef enum { SNIP_FMT_FP8_E4M3 = 0, SNIP_FMT_NVFP4 = 1 } snip_format;
+typedef enum { SNIP_RTN = 0, SNIP_SR = 1 } snip_round;
+
+/* Orientation of a quantization of a rows x cols tensor.
+ * ALONG_COLS: blocks run along the last dim; the output has rows x cols.
+ * ALONG_ROWS: blocks run along the first dim; the output is the transpose,
+ *             cols x rows (output row i = input column i). */
+typedef enum { SNIP_BLOCKS_ALONG_COLS = 0, SNIP_BLOCKS_ALONG_ROWS = 1 } snip_orient;
+
+/* Output layout of a quantization (OR x OC = output rows x contraction).
+ * ROWMAJOR: NVFP4 codes OR x OC/2 bytes (element 2j in bits 0..3 of byte j,
+ *           bit 3 of each code the sign), E4M3 scales OR x OC/16 bytes;
+ *           FP8 codes OR x OC bytes.
+ * MMA:      the GEMM operand layout.  Rows are padded to ORp = roundup(OR,256)
+ *           and the contraction to OCp = roundup(OC,256) for NVFP4 (128 for
+ *           FP8), padding filled with zero codes and zero scales.  Codes are
+ *           row-major ORp x OCp/2 (NVFP4) or ORp x OCp (FP8).  NVFP4 scales
+ *           are stored in 512-byte chunks, one per (128-row group rg, group of
+ *           four 16-element blocks kc): chunk index rg*(OCp/64) + kc, and row
+ *           r, block kb at byte (r%32)*16 + ((r/32)%4)*4 + kb%4 of its chunk. */
+typedef enum { SNIP_LAYOUT_ROWMAJOR = 0, SNIP_LAYOUT_MMA = 1 } snip_layout;
+
+/* Index of each quantization inside a qlinear call; the Philox stream id of
+ * quantization `tag` of layer `l` is l*8 + tag. */
+typedef enum {
+    SNIP_TAG_X_FWD = 0,      /* X, blocks along K, forward            */
+    SNIP_TAG_W_FWD = 1,      /* W, blocks along K, forward            */
+    SNIP_TAG_DY_DGRAD = 2,   /* dY, blocks along N, dgrad             */
+    SNIP_TAG_WT_DGRAD = 3,   /* W^T, blocks along N, dgrad            */
+    SNIP_TAG_DYT_WGRAD = 4,  /* dY^T, blocks along T, wgrad           */
+    SNIP_TAG_XT_WGRAD = 5    /* X^T, blocks along T, wgrad            */
+} snip_tag;
+
+#define SNIP_WS_HEADER_BYTES 256
+#define SNIP_STATS_NVALS 8
+
+/* Slots of the raw statistics vector written by snip_quant_stats. */
+enum {
+    SNIP_ST_SUM_X2 = 0,       /* ||A||^2                                              */
+    SNIP_ST_NVFP4_ERR2 = 1,   /* ||Q_nvfp4(A) - A||^2 under the requested rounding     */
+    SNIP_ST_FP8_ERR2 = 2,     /* ||Q_fp8(A) - A||^2 under the requested rounding       */
+    SNIP_ST_NVFP4_SRVAR = 3,  /* sum (hi-|y|)(|y|-lo) q^2: expected SR error^2, NVFP4   */
+    SNIP_ST_FP8_SRVAR = 4,    /* the same on the FP8 grid                               */
+    SNIP_ST_AMAX = 5,         /* max |A|                                              */
+    SNIP_ST_COUNT = 6         /* number of elements                                   */
+};
+
+typedef struct {
+    double sum_x2, nvfp4_err2, fp8_err2, nvfp4_sr_var, fp8_sr_var, amax, count;
+    double ratio_nvfp4;        /* ||A|| / ||Q_nvfp4(A) - A|| (+inf when the error is 0) */
+    double ratio_fp8;
+    int below_sqrt3_nvfp4;     /* ratio < sqrt(3): the "FP4 all the way" threshold      */
+    int below_sqrt3_fp8;
+} snip_stats;
+
+typedef struct snip_plan snip_plan;
+
+/* ---------------------------------------------------------------- misc */
+
+/* Text of a status code (static storage). */
+const char* snip_status_string(snip_status s);
+
+/* ABI version (major*10000 + minor*100 + patch). */
+int snip_version(void);
+
+/* SNIP_OK if the current CUDA device can run the kernels (compute capability
+ * 10.3), else SNIP_ERR_UNSUPPORTED_DEVICE (or SNIP_ERR_CUDA). */
+snip_status snip_device_check(void);
+
+/* Zero the status word of a workspace (async on `stream`). */
+snip_status snip_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronize `stream`, read the workspace's device status word and return
+ * it as a status code in *device_status: SNIP_OK, SNIP_ERR_NONFINITE or
+ * SNIP_ERR_TIMEOUT (the first of those that any kernel raised since the last
+ * snip_workspace_init).  *device_status is host memory. */
+snip_status snip_workspace_status(const void* ws, void* stream, snip_status* device_status);
+
+/* ---------------------------------------------------------------- a1: amax */
+
+/* Workspace bytes for snip_amax / snip_quantize_* / snip_quant_stats. */
+size_t snip_quantize_workspace_size(int64_t rows, int64_t cols);
+
+/* amax_out[0] = max |x| over n bf16 elements (exact; the max of fp32 values
+ * widened from bf16).  A non-finite element raises SNIP_ERR_NONFINITE in the
+ * workspace status and writes NaN.  n may be 0 (result 0). */
+snip_status snip_amax(const void* x, int64_t n, float* amax_out, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- a2/a3: NVFP4 */
+
+/* NVFP4 quantization of a bf16 rows x cols tensor ("FP4 all the way",
+ * Outline: 16 E2M1 values share one E4M3 scale), with a per-tensor fp32 scale
+ * g above the block scales:
+ *   g   = amax / 2688 (2688 = 6 * 448; g = 1 for an all-zero tensor), or *g_in;
+ *   s_b = E4M3(amax_block / (6 g)), round to nearest even, saturating at 448;
+ *   p   = decode(s_b) * g; y = |x| * (1/p) in fp32;
+ *   code = sign(x) | E2M1(y): nearest with ties to the even code (rnd = RTN)
+ *          or stochastic with 16 Philox bits (rnd = SR), y >= 6 -> 6; a zero
+ *          element, or a block whose p is 0, encodes to magnitude 0.
+ * x          device, rows x cols bf16.  The blocked dim (cols for ALONG_COLS,
+ *            rows for ALONG_ROWS) must be a multiple of 16 (SNIP_ERR_SHAPE).
+ * g_in       device float or NULL (NULL: compute from amax).
+ * codes, scales   device outputs in `layout` (see snip_layout); sizes from
+ *            snip_quantized_bytes().
+ * g_out      device float: the g used.
+ * block_sqerr  device float OR x OC/16 (row-major, in output orientation) or
+ *            NULL: per-block sum of squared dequantization error.
+ * A non-finite input raises SNIP_ERR_NONFINITE in the workspace status; the
+ * outputs are then unspecified and *g_out is NaN. */
+snip_status snip_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, snip_orient orient,
+                                snip_round rnd, uint64_t seed, uint64_t stream_id, const float* g_in,
+                                snip_layout layout, uint8_t* codes, uint8_t* scales, float* g_out,
+                                float* block_sqerr, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- a4: FP8 */
+
+/* FP8 E4M3 quantization with one fp32 tensor scale s = amax / 448 (1 for an
+ * all-zero tensor) or *s_in: code = sign(x) | E4M3(|x| * (1/s)), nearest-even
+ * with saturation at 448 (RTN) or stochastic with 16 Philox bits (SR).
+ * Orientation, layout and errors as for snip_quantize_nvfp4 (no blocks, so
+ * no multiple-of-16 rule beyond the MMA layout's padding). */
+snip_status snip_quantize_fp8(const void* x, int64_t rows, int64_t cols, snip_orient orient,
+                              snip_round rnd, uint64_t seed, uint64_t stream_id, const float* s_in,
+                              snip_layout layout, uint8_t* codes, float* s_out,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes of the code and scale buffers of a quantization whose output has
+ * out_rows rows and contraction out_cols, in `layout`.  Host-only. */
+snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
+                                 size_t* codes_bytes, size_t* scales_bytes);
+
+/* ---------------------------------------------------------------- a5-a7: GEMM */
+
+/* D[m, n] = ga * gb * sum_k A[m, k] B[n, k] for m < M, n < N, fp32 output with
+ * row pitch ldd (elements).  A (M rows) and B (N rows) are quantized operands
+ * in the MMA layout with contraction K; ga/gb are device floats (NVFP4: the
+ * tensor scales g; FP8: the tensor scales s).  NVFP4 uses the tensor cores'
+ * block-scaled FP4 MMA with E4M3 block scales; FP8 the E4M3 x E4M3 MMA.
+ * Accumulation is fp32.  Needs K % 16 == 0 (SNIP_ERR_SHAPE).
+ * ws: at least SNIP_WS_HEADER_BYTES (status word; a timed-out wait raises
+ * SNIP_ERR_TIMEOUT there). */
+snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
+                      const uint8_t* b_codes, const uint8_t* b_scales, const float* gb,
+                      int64_t M, int64_t N, int64_t K, float* D, int64_t ldd,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- plan */
+
+/* A per-layer precision plan (SNIP, Abstract: one format per layer).  formats
+ * (host, n_layers entries) are snip_format values.  Every layer starts with
+ * the rounding of "FP4 all the way": RTN for the forward quantizations (tags
+ * X_FWD, W_FWD) and SR for the four backward ones.  *out is a host object
+ * owned by the caller (snip_plan_destroy). */
+snip_status snip_plan_create(int n_layers, const int* formats, uint64_t seed, snip_plan** out);
+snip_status snip_plan_set_rounding(snip_plan* plan, int layer, snip_tag tag, snip_round rnd);
+snip_status snip_plan_get(const snip_plan* plan, int layer, snip_format* fmt, uint64_t* seed);
+void snip_plan_destroy(snip_plan* plan);
+
+/* ---------------------------------------------------------------- qlinear */
+
+/* Workspace bytes for snip_qlinear_fwd / snip_qlinear_bwd of this layer. */
+size_t snip_qlinear_workspace_size(const snip_plan* plan, int layer, int64_t T, int64_t K, int64_t N);
+
+/* Forward (SNIP Figure 5): Y = Q(X) Q(W)^T.  X device T x K bf16, W device
+ * N x K bf16, Y device T x N fp32.  Both quantized along K in the layer's
+ * format with the plan's rounding (default RTN), stream ids layer*8+{0,1}.
+ * T, K, N multiples of 16. */
+snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, const void* W,
+                             int64_t T, int64_t K, int64_t N, float* Y,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Backward (SNIP Figure 5): dX = Q(dY) Q(W^T)^T (dY and W^T quantized along
+ * N) and dW = Q(dY^T) Q(X^T)^T (both quantized along T), stochastic rounding
+ * by default ("FP4 all the way", Outline), stream ids layer*8+{2,3,4,5}.
+ * dY device T x N bf16, dX device T x K fp32, dW device N x K fp32. */
+snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W,
+                             const void* dY, int64_t T, int64_t K, int64_t N, float* dX, float* dW,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- a8: statistics */
+
+/* SNIP's statistics pass over one bf16 rows x cols tensor (cols % 16 == 0),
+ * blocks along cols, under the tensor's rounding rnd (seed, stream_id for SR):
+ * raw_out (device, SNIP_STATS_NVALS doubles) receives the SNIP_ST_* sums;
+ * block_err_nvfp4 / block_err_fp8 (device, rows x cols/16 floats, nullable)
+ * receive per-block squared errors.  Non-finite input raises
+ * SNIP_ERR_NONFINITE in the workspace status. */
+snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_round rnd, uint64_t seed,
+                             uint64_t stream_id, double* raw_out, float* block_err_nvfp4,
+                             float* block_err_fp8, void* ws, size_t ws_bytes, void* stream);
+
+/* Host helper: derive ratios and sqrt(3) flags from a host copy of raw_out. */
+snip_status snip_stats_finalize(const double* raw_host, snip_stats* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SNIP_H */

@@ -1,0 +1,466 @@
+// api.cu -- the C ABI declared in include/snip.h: argument checks, workspace
+// layout, the per-layer precision plan and the launch sequence of each call.
+// Every compute step runs in the kernels of quant.cu and gemm.cu.
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/snip.h"
+#include "snip_kernels.cuh"
+
+using namespace snip;
+
+namespace {
+
+// ---------------------------------------------------------------- workspace header
+// Byte offsets inside the SNIP_WS_HEADER_BYTES header and the small-scratch
+// region that follows it.
+constexpr size_t kOffStatus = 0;        // uint32 sticky status bits
+constexpr size_t kOffAmaxCounter = 4;   // uint32, self-resetting
+constexpr size_t kOffStatsCounter = 8;  // uint32, self-resetting
+constexpr size_t kOffAmaxSlots = 16;    // 8 x uint32 published amax words
+constexpr size_t kOffScaleSlots = 64;   // 8 x float tensor scales (qlinear operands)
+constexpr size_t kOffAmaxPartials = SNIP_WS_HEADER_BYTES;                            // kMaxPartials x uint32
+constexpr size_t kOffStatsPartials = kOffAmaxPartials + 4 * kMaxPartials;            // kMaxPartials x 5 doubles
+constexpr size_t kSmallWorkspace = kOffStatsPartials + 8 * 5 * kMaxPartials;         // 45312
+constexpr size_t kSmallWorkspaceRounded = (kSmallWorkspace + 4095) / 4096 * 4096;   // 49152
+
+constexpr uint64_t kTimeoutNs = 4000000000ull;   // a GEMM wait that takes 4 s is a fault
+
+inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+inline T* ws_at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off); }
+
+// Per-device facts, cached for device ordinals < 64.
+struct DeviceInfo { int checked = 0; int ok = 0; int num_sms = 0; };
+DeviceInfo g_dev[64];
+
+snip_status current_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SNIP_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SNIP_ERR_UNSUPPORTED_DEVICE;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SNIP_ERR_CUDA;
+    d.ok = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    d.checked = 1;
+  }
+  if (!d.ok) return SNIP_ERR_UNSUPPORTED_DEVICE;
+  if (num_sms) *num_sms = d.num_sms;
+  return SNIP_OK;
+}
+
+inline snip_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SNIP_OK;
+  fprintf(stderr, "snip: CUDA error %s\n", cudaGetErrorString(e));
+  return SNIP_ERR_CUDA;
+}
+
+// Padded dims of the MMA operand layout.
+inline int64_t mma_rows(int64_t r) { return round_up(r, 256); }
+inline int64_t mma_cols(int snip_fmt, int64_t c) { return round_up(c, snip_fmt == SNIP_FMT_NVFP4 ? 256 : 128); }
+
+struct OperandBytes { size_t codes, scales; };
+OperandBytes operand_bytes(int fmt, int layout, int64_t orows, int64_t ocols) {
+  if (layout == SNIP_LAYOUT_ROWMAJOR) {
+    if (fmt == SNIP_FMT_NVFP4) return {(size_t)(orows * ocols / 2), (size_t)(orows * ocols / 16)};
+    return {(size_t)(orows * ocols), 0};
+  }
+  const int64_t r = mma_rows(orows), c = mma_cols(fmt, ocols);
+  if (fmt == SNIP_FMT_NVFP4) return {(size_t)(r * c / 2), (size_t)(r * c / 16)};
+  return {(size_t)(r * c), 0};
+}
+
+// ---------------------------------------------------------------- shared launch helpers
+snip_status run_amax(const void* x, int64_t n, int slot, float* result_float, void* ws, int num_sms, cudaStream_t st) {
+  return cuda_status(launch_amax(static_cast<const uint16_t*>(x), n, ws_at<uint32_t>(ws, kOffAmaxPartials),
+                                 ws_at<uint32_t>(ws, kOffAmaxCounter), ws_at<uint32_t>(ws, kOffAmaxSlots + 4 * slot),
+                                 result_float, ws_at<uint32_t>(ws, kOffStatus), num_sms, st));
+}
+
+// One quantization: amax (unless g_in) then the quantizer kernel.
+snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int orient, int rnd, uint64_t seed,
+                         uint64_t stream_id, const float* g_in, int layout, uint8_t* codes, uint8_t* scales,
+                         float* g_out, float* block_err, void* ws, int amax_slot, int num_sms, cudaStream_t st) {
+  if (!g_in) {
+    snip_status s = run_amax(x, rows * cols, amax_slot, nullptr, ws, num_sms, st);
+    if (s != SNIP_OK) return s;
+  }
+  QuantParams p;
+  p.x = static_cast<const uint16_t*>(x);
+  p.rows = rows;
+  p.cols = cols;
+  p.out_rows = orient == SNIP_BLOCKS_ALONG_COLS ? rows : cols;
+  p.out_cols = orient == SNIP_BLOCKS_ALONG_COLS ? cols : rows;
+  p.orp = layout == SNIP_LAYOUT_MMA ? mma_rows(p.out_rows) : p.out_rows;
+  p.ocp = layout == SNIP_LAYOUT_MMA ? mma_cols(fmt, p.out_cols) : p.out_cols;
+  p.seed = seed;
+  p.stream_id = stream_id;
+  p.g_in = g_in;
+  p.amax_bits = ws_at<uint32_t>(ws, kOffAmaxSlots + 4 * amax_slot);
+  p.codes = codes;
+  p.scales = scales;
+  p.g_out = g_out;
+  p.block_err = block_err;
+  // an empty output still publishes its tensor scale: the one-CTA row kernel does that
+  if (p.orp == 0 || p.ocp == 0) orient = SNIP_BLOCKS_ALONG_COLS;
+  if (fmt == SNIP_FMT_NVFP4)
+    return cuda_status(launch_quant_nvfp4(p, orient, layout, rnd, block_err != nullptr, num_sms, st));
+  return cuda_status(launch_quant_fp8(p, orient, layout, rnd, num_sms, st));
+}
+
+snip_status run_gemm(int fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga, const uint8_t* b_codes,
+                     const uint8_t* b_scales, const float* gb, int64_t M, int64_t N, int64_t K, float* D, int64_t ldd,
+                     void* ws, int num_sms, cudaStream_t st) {
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  p.a_scales = a_scales;
+  p.b_scales = b_scales;
+  p.ga = ga;
+  p.gb = gb;
+  p.D = D;
+  p.M = M;
+  p.N = N;
+  p.ldd = ldd;
+  p.kp = mma_cols(fmt, K);
+  p.status = ws_at<uint32_t>(ws, kOffStatus);
+  p.timeout_ns = kTimeoutNs;
+  return cuda_status(launch_gemm(fmt == SNIP_FMT_NVFP4 ? 1 : 0, a_codes, mma_rows(M), b_codes, mma_rows(N), p,
+                                 num_sms, st));
+}
+
+bool valid_enum(int v, int n) { return v >= 0 && v < n; }
+
+}  // namespace
+
+// ---------------------------------------------------------------- plan object
+struct snip_plan {
+  std::vector<int> fmt;
+  std::vector<int> rnd;   // 6 per layer, indexed by snip_tag
+  uint64_t seed;
+};
+
+extern "C" {
+
+const char* snip_status_string(snip_status s) {
+  switch (s) {
+    case SNIP_OK: return "ok";
+    case SNIP_ERR_INVALID_ARG: return "invalid argument";
+    case SNIP_ERR_SHAPE: return "shape not supported (dims must be multiples of 16)";
+    case SNIP_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case SNIP_ERR_NONFINITE: return "input holds a non-finite value";
+    case SNIP_ERR_TIMEOUT: return "a kernel wait timed out";
+    case SNIP_ERR_CUDA: return "CUDA runtime error";
+    case SNIP_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103)";
+    case SNIP_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+int snip_version(void) { return 100; }
+
+snip_status snip_device_check(void) { return current_device(nullptr); }
+
+snip_status snip_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < SNIP_WS_HEADER_BYTES) return SNIP_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, SNIP_WS_HEADER_BYTES, static_cast<cudaStream_t>(stream)));
+}
+
+snip_status snip_workspace_status(const void* ws, void* stream, snip_status* device_status) {
+  if (!ws || !device_status) return SNIP_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  *device_status = (word & kDevNonFinite) ? SNIP_ERR_NONFINITE : (word & kDevTimeout) ? SNIP_ERR_TIMEOUT : SNIP_OK;
+  return SNIP_OK;
+}
+
+size_t snip_quantize_workspace_size(int64_t rows, int64_t cols) {
+  (void)rows;
+  (void)cols;
+  return kSmallWorkspaceRounded;
+}
+
+snip_status snip_amax(const void* x, int64_t n, float* amax_out, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if ((!x && n > 0) || !amax_out || n < 0) return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(ws)) return SNIP_ERR_ALIGN;
+  return run_amax(x, n, 0, amax_out, ws, sms, static_cast<cudaStream_t>(stream));
+}
+
+snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
+                                 size_t* codes_bytes, size_t* scales_bytes) {
+  if (!valid_enum(fmt, 2) || !valid_enum(layout, 2) || out_rows < 0 || out_cols < 0) return SNIP_ERR_INVALID_ARG;
+  OperandBytes b = operand_bytes(fmt, layout, out_rows, out_cols);
+  if (codes_bytes) *codes_bytes = b.codes;
+  if (scales_bytes) *scales_bytes = b.scales;
+  return SNIP_OK;
+}
+
+static snip_status check_quantize_args(int fmt, const void* x, int64_t rows, int64_t cols, int orient, int rnd,
+                                       int layout, const void* codes, const void* scales, const void* g_out,
+                                       const void* ws, size_t ws_bytes) {
+  if (!valid_enum(orient, 2) || !valid_enum(rnd, 2) || !valid_enum(layout, 2)) return SNIP_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || !g_out || !codes || (rows * cols > 0 && !x)) return SNIP_ERR_INVALID_ARG;
+  if (fmt == SNIP_FMT_NVFP4 && !scales) return SNIP_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || (orient == SNIP_BLOCKS_ALONG_ROWS && rows % 16 != 0)) return SNIP_ERR_SHAPE;
+  if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(ws) || (scales && !aligned16(scales))) return SNIP_ERR_ALIGN;
+  return SNIP_OK;
+}
+
+snip_status snip_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, snip_orient orient, snip_round rnd,
+                                uint64_t seed, uint64_t stream_id, const float* g_in, snip_layout layout,
+                                uint8_t* codes, uint8_t* scales, float* g_out, float* block_sqerr, void* ws,
+                                size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  s = check_quantize_args(SNIP_FMT_NVFP4, x, rows, cols, orient, rnd, layout, codes, scales, g_out, ws, ws_bytes);
+  if (s != SNIP_OK) return s;
+  return run_quantize(SNIP_FMT_NVFP4, x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
+                      block_sqerr, ws, 0, sms, static_cast<cudaStream_t>(stream));
+}
+
+snip_status snip_quantize_fp8(const void* x, int64_t rows, int64_t cols, snip_orient orient, snip_round rnd,
+                              uint64_t seed, uint64_t stream_id, const float* s_in, snip_layout layout,
+                              uint8_t* codes, float* s_out, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  s = check_quantize_args(SNIP_FMT_FP8_E4M3, x, rows, cols, orient, rnd, layout, codes, nullptr, s_out, ws,
+                          ws_bytes);
+  if (s != SNIP_OK) return s;
+  return run_quantize(SNIP_FMT_FP8_E4M3, x, rows, cols, orient, rnd, seed, stream_id, s_in, layout, codes, nullptr,
+                      s_out, nullptr, ws, 0, sms, static_cast<cudaStream_t>(stream));
+}
+
+snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
+                      const uint8_t* b_codes, const uint8_t* b_scales, const float* gb, int64_t M, int64_t N,
+                      int64_t K, float* D, int64_t ldd, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if (!valid_enum(fmt, 2) || M < 0 || N < 0 || K < 0 || ldd < N) return SNIP_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return SNIP_OK;
+  if (!a_codes || !b_codes || !ga || !gb || !D) return SNIP_ERR_INVALID_ARG;
+  if (fmt == SNIP_FMT_NVFP4 && (!a_scales || !b_scales)) return SNIP_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K == 0 || ldd % 4 != 0) return SNIP_ERR_SHAPE;
+  if (!ws || ws_bytes < SNIP_WS_HEADER_BYTES) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(D) || !aligned16(ws) ||
+      (fmt == SNIP_FMT_NVFP4 && (!aligned16(a_scales) || !aligned16(b_scales))))
+    return SNIP_ERR_ALIGN;
+  return run_gemm(fmt, a_codes, a_scales, ga, b_codes, b_scales, gb, M, N, K, D, ldd, ws, sms,
+                  static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- plan
+snip_status snip_plan_create(int n_layers, const int* formats, uint64_t seed, snip_plan** out) {
+  if (n_layers <= 0 || !formats || !out) return SNIP_ERR_INVALID_ARG;
+  for (int i = 0; i < n_layers; ++i)
+    if (!valid_enum(formats[i], 2)) return SNIP_ERR_INVALID_ARG;
+  snip_plan* p = new (std::nothrow) snip_plan;
+  if (!p) return SNIP_ERR_INVALID_ARG;
+  p->fmt.assign(formats, formats + n_layers);
+  p->rnd.assign((size_t)n_layers * 6, SNIP_SR);
+  for (int i = 0; i < n_layers; ++i) {
+    p->rnd[(size_t)i * 6 + SNIP_TAG_X_FWD] = SNIP_RTN;
+    p->rnd[(size_t)i * 6 + SNIP_TAG_W_FWD] = SNIP_RTN;
+  }
+  p->seed = seed;
+  *out = p;
+  return SNIP_OK;
+}
+
+snip_status snip_plan_set_rounding(snip_plan* plan, int layer, snip_tag tag, snip_round rnd) {
+  if (!plan || layer < 0 || layer >= (int)plan->fmt.size() || !valid_enum(tag, 6) || !valid_enum(rnd, 2))
+    return SNIP_ERR_INVALID_ARG;
+  plan->rnd[(size_t)layer * 6 + tag] = rnd;
+  return SNIP_OK;
+}
+
+snip_status snip_plan_get(const snip_plan* plan, int layer, snip_format* fmt, uint64_t* seed) {
+  if (!plan || layer < 0 || layer >= (int)plan->fmt.size()) return SNIP_ERR_INVALID_ARG;
+  if (fmt) *fmt = (snip_format)plan->fmt[layer];
+  if (seed) *seed = plan->seed;
+  return SNIP_OK;
+}
+
+void snip_plan_destroy(snip_plan* plan) { delete plan; }
+
+// ---------------------------------------------------------------- qlinear
+namespace {
+struct QlOperand { size_t codes_off, scales_off; };
+struct QlLayout {
+  QlOperand op[4];
+  size_t total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// fwd: op0 = X (T x K), op1 = W (N x K); bwd: op0 = dY (T x N), op1 = W^T
+// (K x N), op2 = dY^T (N x T), op3 = X^T (K x T).  The two calls reuse the
+// same region, so the workspace is sized for the larger of the two.
+QlLayout ql_layout(int fmt, int64_t T, int64_t K, int64_t N, bool bwd) {
+  QlLayout L;
+  size_t off = kSmallWorkspaceRounded;
+  const int64_t shapes_fwd[2][2] = {{T, K}, {N, K}};
+  const int64_t shapes_bwd[4][2] = {{T, N}, {K, N}, {N, T}, {K, T}};
+  const int n = bwd ? 4 : 2;
+  for (int i = 0; i < n; ++i) {
+    const int64_t* sh = bwd ? shapes_bwd[i] : shapes_fwd[i];
+    OperandBytes b = operand_bytes(fmt, SNIP_LAYOUT_MMA, sh[0], sh[1]);
+    L.op[i].codes_off = off;
+    off = align_up(off + b.codes, 1024);
+    L.op[i].scales_off = off;
+    off = align_up(off + b.scales, 1024);
+  }
+  L.total = off;
+  return L;
+}
+
+snip_status check_ql(const snip_plan* plan, int layer, int64_t T, int64_t K, int64_t N) {
+  if (!plan || layer < 0 || layer >= (int)plan->fmt.size()) return SNIP_ERR_INVALID_ARG;
+  if (T <= 0 || K <= 0 || N <= 0) return SNIP_ERR_INVALID_ARG;
+  if (T % 16 || K % 16 || N % 16) return SNIP_ERR_SHAPE;
+  return SNIP_OK;
+}
+}  // namespace
+
+size_t snip_qlinear_workspace_size(const snip_plan* plan, int layer, int64_t T, int64_t K, int64_t N) {
+  if (check_ql(plan, layer, T, K, N) != SNIP_OK) return 0;
+  const int fmt = plan->fmt[layer];
+  size_t a = ql_layout(fmt, T, K, N, false).total, b = ql_layout(fmt, T, K, N, true).total;
+  return a > b ? a : b;
+}
+
+snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, const void* W, int64_t T, int64_t K,
+                             int64_t N, float* Y, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if ((s = check_ql(plan, layer, T, K, N)) != SNIP_OK) return s;
+  if (!X || !W || !Y) return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < snip_qlinear_workspace_size(plan, layer, T, K, N)) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(ws)) return SNIP_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int fmt = plan->fmt[layer];
+  const int* rnd = &plan->rnd[(size_t)layer * 6];
+  const uint64_t sid = (uint64_t)layer * 8;
+  QlLayout L = ql_layout(fmt, T, K, N, false);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  float* gs = ws_at<float>(ws, kOffScaleSlots);
+  if ((s = run_quantize(fmt, X, T, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_X_FWD], plan->seed, sid + SNIP_TAG_X_FWD,
+                        nullptr, SNIP_LAYOUT_MMA, b + L.op[0].codes_off, b + L.op[0].scales_off, gs + 0, nullptr, ws,
+                        0, sms, st)) != SNIP_OK)
+    return s;
+  if ((s = run_quantize(fmt, W, N, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_W_FWD], plan->seed, sid + SNIP_TAG_W_FWD,
+                        nullptr, SNIP_LAYOUT_MMA, b + L.op[1].codes_off, b + L.op[1].scales_off, gs + 1, nullptr, ws,
+                        1, sms, st)) != SNIP_OK)
+    return s;
+  return run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, gs + 0, b + L.op[1].codes_off,
+                  b + L.op[1].scales_off, gs + 1, T, N, K, Y, N, ws, sms, st);
+}
+
+snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W, const void* dY,
+                             int64_t T, int64_t K, int64_t N, float* dX, float* dW, void* ws, size_t ws_bytes,
+                             void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if ((s = check_ql(plan, layer, T, K, N)) != SNIP_OK) return s;
+  if (!X || !W || !dY || !dX || !dW) return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < snip_qlinear_workspace_size(plan, layer, T, K, N)) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(ws))
+    return SNIP_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int fmt = plan->fmt[layer];
+  const int* rnd = &plan->rnd[(size_t)layer * 6];
+  const uint64_t sid = (uint64_t)layer * 8;
+  QlLayout L = ql_layout(fmt, T, K, N, true);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  float* gs = ws_at<float>(ws, kOffScaleSlots);
+  // dgrad: dX = Q(dY) Q(W^T)^T, contraction N
+  if ((s = run_quantize(fmt, dY, T, N, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_DY_DGRAD], plan->seed,
+                        sid + SNIP_TAG_DY_DGRAD, nullptr, SNIP_LAYOUT_MMA, b + L.op[0].codes_off,
+                        b + L.op[0].scales_off, gs + 2, nullptr, ws, 2, sms, st)) != SNIP_OK)
+    return s;
+  if ((s = run_quantize(fmt, W, N, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_WT_DGRAD], plan->seed,
+                        sid + SNIP_TAG_WT_DGRAD, nullptr, SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
+                        b + L.op[1].scales_off, gs + 3, nullptr, ws, 1, sms, st)) != SNIP_OK)
+    return s;
+  if ((s = run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, gs + 2, b + L.op[1].codes_off,
+                    b + L.op[1].scales_off, gs + 3, T, K, N, dX, K, ws, sms, st)) != SNIP_OK)
+    return s;
+  // wgrad: dW = Q(dY^T) Q(X^T)^T, contraction T
+  if ((s = run_quantize(fmt, dY, T, N, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_DYT_WGRAD], plan->seed,
+                        sid + SNIP_TAG_DYT_WGRAD, nullptr, SNIP_LAYOUT_MMA, b + L.op[2].codes_off,
+                        b + L.op[2].scales_off, gs + 4, nullptr, ws, 2, sms, st)) != SNIP_OK)
+    return s;
+  if ((s = run_quantize(fmt, X, T, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_XT_WGRAD], plan->seed,
+                        sid + SNIP_TAG_XT_WGRAD, nullptr, SNIP_LAYOUT_MMA, b + L.op[3].codes_off,
+                        b + L.op[3].scales_off, gs + 5, nullptr, ws, 0, sms, st)) != SNIP_OK)
+    return s;
+  return run_gemm(fmt, b + L.op[2].codes_off, b + L.op[2].scales_off, gs + 4, b + L.op[3].codes_off,
+                  b + L.op[3].scales_off, gs + 5, N, K, T, dW, K, ws, sms, st);
+}
+
+// ---------------------------------------------------------------- statistics
+snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_round rnd, uint64_t seed,
+                             uint64_t stream_id, double* raw_out, float* block_err_nvfp4, float* block_err_fp8,
+                             void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if (!valid_enum(rnd, 2) || rows < 0 || cols < 0 || !raw_out || (rows * cols > 0 && !a)) return SNIP_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return SNIP_ERR_SHAPE;
+  if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(a) || !aligned16(ws)) return SNIP_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = run_amax(a, rows * cols, 3, nullptr, ws, sms, st)) != SNIP_OK) return s;
+  StatsParams p;
+  p.x = static_cast<const uint16_t*>(a);
+  p.rows = rows;
+  p.cols = cols;
+  p.seed = seed;
+  p.stream_id = stream_id;
+  p.amax_bits = ws_at<uint32_t>(ws, kOffAmaxSlots + 4 * 3);
+  p.partials = ws_at<double>(ws, kOffStatsPartials);
+  p.counter = ws_at<uint32_t>(ws, kOffStatsCounter);
+  p.raw_out = raw_out;
+  p.block_err4 = block_err_nvfp4;
+  p.block_err8 = block_err_fp8;
+  return cuda_status(launch_stats(p, rnd, sms, st));
+}
+
+snip_status snip_stats_finalize(const double* raw, snip_stats* out) {
+  if (!raw || !out) return SNIP_ERR_INVALID_ARG;
+  out->sum_x2 = raw[SNIP_ST_SUM_X2];
+  out->nvfp4_err2 = raw[SNIP_ST_NVFP4_ERR2];
+  out->fp8_err2 = raw[SNIP_ST_FP8_ERR2];
+  out->nvfp4_sr_var = raw[SNIP_ST_NVFP4_SRVAR];
+  out->fp8_sr_var = raw[SNIP_ST_FP8_SRVAR];
+  out->amax = raw[SNIP_ST_AMAX];
+  out->count = raw[SNIP_ST_COUNT];
+  const double inf = __builtin_huge_val();
+  out->ratio_nvfp4 = out->nvfp4_err2 == 0.0 ? inf : __builtin_sqrt(out->sum_x2 / out->nvfp4_err2);
+  out->ratio_fp8 = out->fp8_err2 == 0.0 ? inf : __builtin_sqrt(out->sum_x2 / out->fp8_err2);
+  out->below_sqrt3_nvfp4 = out->ratio_nvfp4 < 1.7320508075688772;
+  out->below_sqrt3_fp8 = out->ratio_fp8 < 1.7320508075688772;
+  return SNIP_OK;
+}
+
+}  // extern "C"

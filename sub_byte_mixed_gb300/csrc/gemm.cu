@@ -1,0 +1,279 @@
+// gemm.cu -- the three GEMMs of the quantized linear layer (SNIP, Figure 5:
+// forward Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X).  All three are "TN"
+// products D = ga*gb * A B^T of two operands quantized along the contraction
+// dim (K-major), so one kernel serves them.
+//
+// NVFP4 operands ("FP4 all the way" (Chmiel et al.), summary page, Outline:
+// 16 E2M1 values share one E4M3 scale) run on the block-scaled FP4 tensor-core
+// MMA (tcgen05.mma kind::mxf4nvf4, scale_vec::4X: one E4M3 scale per 16
+// elements of each operand row); FP8 E4M3 operands on kind::f8f6f4.  The fp32
+// tensor scales multiply the fp32 accumulator in the epilogue.
+//
+// Structure (one CTA per SM, persistent over output tiles, 6 warps):
+//   warp 0     TMA producer: 128B-swizzled code tiles via cp.async.bulk.tensor,
+//              block-scale chunks via cp.async.bulk, into a STAGES-deep ring;
+//   warp 1     allocates tensor memory and issues tcgen05.cp (scales smem ->
+//              TMEM) and tcgen05.mma (accumulator in TMEM) from one thread;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, scale by ga*gb, store
+//              fp32 rows.
+// Every wait is bounded (globaltimer); on expiry the CTA raises the timeout
+// bit of the status word, lets all roles fall through, drains in-flight
+// tensor-core work and frees its tensor memory before returning.
+#include <cuda.h>
+
+#include "snip_kernels.cuh"
+
+namespace snip {
+
+template <int FMT, int BN>
+struct GemmCfg {
+  static constexpr int BM = 128;
+  static constexpr int KB = 128;  // contraction bytes per stage and row (256 FP4 / 128 FP8 elements)
+  static constexpr int A_BYTES = BM * KB;
+  static constexpr int B_BYTES = BN * KB;
+  static constexpr int SFA_BYTES = FMT ? 2048 : 0;               // 4 chunks of 512 B
+  static constexpr int SFB_BYTES = FMT ? (BN / 128) * 2048 : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGES = 4;
+  static constexpr int ACC_STAGES = (FMT && BN == 256) ? 1 : 2;
+  // tensor-memory columns of one stage's scale factors: per MMA (K=64), A
+  // takes 4 columns (128 rows / 32 lanes) and B takes BN/32
+  static constexpr int SFA_COLS = 16;
+  static constexpr int SF_COLS = FMT ? SFA_COLS + 4 * (BN / 32) : 0;
+  static constexpr int SF_TMEM_BASE = ACC_STAGES * BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+  // Instruction descriptor.  Block-scaled FP4: A/B type E2M1 (1) in bits 7-9
+  // and 10-12, K-major, N>>3 in bits 17-22, scale type UE4M3 (0) in bit 23,
+  // M>>4 in bits 24-28.  FP8: D type f32 (1) in bits 4-5, A/B type E4M3 (0).
+  static constexpr uint32_t IDESC =
+      FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24))
+          : ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24));
+};
+
+template <int FMT, int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  using C = GemmCfg<FMT, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::ACC_STAGES + a); };
+  const uint32_t drain = bar0 + 8u * (2 * C::STAGES + 2 * C::ACC_STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+    for (int a = 0; a < C::ACC_STAGES; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 4); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); }
+  if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int64_t sf_chunks_per_group = p.kp >> 6;   // 512-byte scale chunks per 128-row group
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+        for (int kb = 0; kb < p.num_k_stages; ++kb) {
+          if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          uint8_t* sA = smem + stage * C::STAGE_BYTES;
+          uint8_t* sB = sA + C::A_BYTES;
+          mbar_arrive_expect_tx(full(stage), C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sA), &tmA, kb * C::KB, mt * C::BM, full(stage));
+          tma_load_2d(smem_u32(sB), &tmB, kb * C::KB, nt * BN, full(stage));
+          if (FMT) {
+            uint8_t* sSFA = sB + C::B_BYTES;
+            uint8_t* sSFB = sSFA + C::SFA_BYTES;
+            bulk_load(smem_u32(sSFA), p.a_scales + ((int64_t)mt * sf_chunks_per_group + kb * 4) * 512, 2048,
+                      full(stage));
+#pragma unroll
+            for (int nb = 0; nb < BN / 128; ++nb)
+              bulk_load(smem_u32(sSFB + nb * 2048),
+                        p.b_scales + ((int64_t)(nt * (BN / 128) + nb) * sf_chunks_per_group + kb * 4) * 512, 2048,
+                        full(stage));
+          }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // let copies already in flight land before the CTA leaves (bounded)
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait_bounded(tempty(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        for (int kb = 0; kb < p.num_k_stages; ++kb) {
+          if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t sB = sA + C::A_BYTES;
+          const uint32_t sf = tmem + C::SF_TMEM_BASE + stage * C::SF_COLS;
+          if (FMT) {
+            const uint32_t sSFA = sB + C::B_BYTES, sSFB = sSFA + C::SFA_BYTES;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) tc_cp_32x128b_x4(sf + 4 * k, smem_desc(sSFA + 512 * k, 0, 128, 0));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int nb = 0; nb < BN / 128; ++nb)
+                tc_cp_32x128b_x4(sf + C::SFA_COLS + k * (BN / 32) + 4 * nb,
+                                 smem_desc(sSFB + nb * 2048 + 512 * k, 0, 128, 0));
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t adesc = smem_desc(sA + 32 * k, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(sB + 32 * k, 16, 1024, 2);
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            if (FMT) tc_mma_nvf4(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * (BN / 32), accum);
+            else tc_mma_f8(d_tmem, adesc, bdesc, C::IDESC, accum);
+          }
+          tc_commit(empty(stage));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull(acc));
+        if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+      }
+      // all tensor-core work issued by this thread completes before TMEM is freed
+      tc_commit(drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const float alpha = __fmul_rn(*p.ga, *p.gb);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+      if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
+      tc_fence_after();
+      const int64_t row = (int64_t)mt * C::BM + q * 32 + lane;
+      float* drow = p.D + row * p.ldd;
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + ch * 32, r);
+        tmem_ld_wait();
+        if (ch == BN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty(acc));
+        }
+        const int64_t col0 = (int64_t)nt * BN + ch * 32;
+        if (row < p.M) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (col0 + 4 * j < p.N) {
+              float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * j])),
+                                     __fmul_rn(alpha, __uint_as_float(r[4 * j + 1])),
+                                     __fmul_rn(alpha, __uint_as_float(r[4 * j + 2])),
+                                     __fmul_rn(alpha, __uint_as_float(r[4 * j + 3])));
+              *reinterpret_cast<float4*>(drow + col0 + 4 * j) = v;
+            }
+          }
+        }
+      }
+      if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D byte tensor rows x row_bytes, loaded in boxes of box_rows x 128 bytes
+// with the 128-byte swizzle the MMA descriptors expect.
+static bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t row_bytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, int BN>
+static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
+                                   GemmParams p, int num_sms, cudaStream_t st) {
+  using C = GemmCfg<FMT, BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t row_bytes = FMT ? p.kp / 2 : p.kp;
+  CUtensorMap ta, tb;
+  if (!make_code_map(&ta, a_codes, a_rows, row_bytes, C::BM) || !make_code_map(&tb, b_codes, b_rows, row_bytes, BN))
+    return cudaErrorInvalidValue;
+  p.num_k_stages = (int)(row_bytes / C::KB);
+  p.num_m_tiles = (int)((p.M + C::BM - 1) / C::BM);
+  p.num_n_tiles = (int)((p.N + BN - 1) / BN);
+  const int tiles = p.num_m_tiles * p.num_n_tiles;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  gemm_tn_kernel<FMT, BN><<<grid, 192, C::SMEM_BYTES, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,
+                        int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st) {
+  if (fmt == 1) return launch_gemm_cfg<1, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  return launch_gemm_cfg<0, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+}
+
+}  // namespace snip

@@ -1,0 +1,267 @@
+// snip_device.cuh -- device primitives of the quantized linear layer:
+// element formats and rounding rules, Philox4x32-10, and thin inline-PTX
+// wrappers for mbarrier / TMA / tcgen05 on sm_103a.
+//
+// Format rules ("FP4 all the way" (Chmiel et al.), summary page, Outline):
+// NVFP4 is 16 E2M1 elements sharing one E4M3 scale; round-to-nearest forward,
+// stochastic rounding backward.  Stochastic rounding keeps the expected value
+// ("Research on Mixed-Precision Training for LLMs", stochastic rounding
+// paragraph).  Every fp32 step is a single IEEE round-to-nearest operation
+// (explicit __f*_rn intrinsics, no contraction), so results are bit-exact
+// functions of the input.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace snip {
+
+// Status bits OR-ed into the workspace status word by kernels.
+constexpr uint32_t kDevNonFinite = 1u;
+constexpr uint32_t kDevTimeout = 2u;
+
+// ------------------------------------------------------------------ bf16
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+
+// ------------------------------------------------------------------ E4M3
+// Round-to-nearest-even conversion of t >= 0 to E4M3 with saturation at 448
+// (hardware cvt with .satfinite).  Both halves get t, the low byte is used.
+__device__ __forceinline__ uint32_t e4m3_rn_sat(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(t), "f"(t));
+  return r & 0xffu;
+}
+// Two values at once: low byte <- lo, high byte <- hi.
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Value of a non-negative E4M3 code (0..0x7e): 2^(e-7)(1+m/8), or m 2^-9.
+__device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
+  uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
+}
+
+// Stochastic rounding of y >= 0 (finite) onto the finite E4M3 grid: lo is y
+// truncated to 3 mantissa bits, frac = (y - lo) / step is exact, go up iff
+// u16 < floor(frac * 2^16); y >= 448 gives 448.  Returns the magnitude code.
+__device__ __forceinline__ uint32_t e4m3_sr(float y, uint32_t u16) {
+  if (y >= 448.0f) return 0x7eu;
+  uint32_t code_lo, thr;
+  if (y >= 0.015625f) {                     // normal range: 2^-6 <= y < 448
+    uint32_t b = __float_as_uint(y);
+    code_lo = ((((b >> 23) & 0xffu) - 120u) << 3) | ((b >> 20) & 7u);
+    thr = (b >> 4) & 0xffffu;               // the 20 dropped mantissa bits, top 16
+  } else {                                  // subnormal range: steps of 2^-9
+    uint32_t t = (uint32_t)__fmul_rn(y, 33554432.0f);   // y * 2^25, exact, < 2^19
+    code_lo = t >> 16;
+    thr = t & 0xffffu;
+  }
+  return code_lo + (u16 < thr ? 1u : 0u);
+}
+
+// ------------------------------------------------------------------ E2M1
+// Round-to-nearest onto {0, .5, 1, 1.5, 2, 3, 4, 6} with ties to the even
+// code, saturating at 6: count the midpoints below y (a tie counts only when
+// the upper neighbour has the even code).  y >= 0 or NaN (-> 0).
+__device__ __forceinline__ uint32_t e2m1_rn(float y) {
+  return (uint32_t)(y > 0.25f) + (uint32_t)(y >= 0.75f) + (uint32_t)(y > 1.25f) +
+         (uint32_t)(y >= 1.75f) + (uint32_t)(y > 2.5f) + (uint32_t)(y >= 3.5f) +
+         (uint32_t)(y > 5.0f);
+}
+
+// Stochastic rounding onto the E2M1 grid with 16 random bits: lo = largest
+// grid value <= y, frac = (y - lo)/(hi - lo) (exact: the step is a power of
+// two), up iff u16 < floor(frac * 2^16); y >= 6 gives 6; NaN gives 0.
+__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t u16) {
+  if (y >= 6.0f) return 7u;
+  if (!(y > 0.0f)) return 0u;
+  uint32_t idx = (uint32_t)(y >= 0.5f) + (uint32_t)(y >= 1.0f) + (uint32_t)(y >= 1.5f) +
+                 (uint32_t)(y >= 2.0f) + (uint32_t)(y >= 3.0f) + (uint32_t)(y >= 4.0f);
+  float lo = idx <= 4u ? __fmul_rn((float)idx, 0.5f) : (idx == 5u ? 3.0f : 4.0f);
+  float inv_step = idx < 4u ? 2.0f : (idx < 6u ? 1.0f : 0.5f);
+  float frac = __fmul_rn(__fsub_rn(y, lo), inv_step);
+  uint32_t thr = (uint32_t)__fmul_rn(frac, 65536.0f);
+  return idx + (u16 < thr ? 1u : 0u);
+}
+
+// Value of an E2M1 magnitude code 0..7.
+__device__ __forceinline__ float e2m1_value(uint32_t m) {
+  return m <= 4u ? __fmul_rn((float)m, 0.5f) : (m == 5u ? 3.0f : (m == 6u ? 4.0f : 6.0f));
+}
+
+// ------------------------------------------------------------------ Philox4x32-10
+// Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
+// (SC'11): ten rounds of two 32x32->64-bit products on a 4-word counter, the
+// 2-word key bumped by the Weyl constants between rounds.
+struct U4 { uint32_t x, y, z, w; };
+
+__device__ __forceinline__ U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                            uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+  }
+  return U4{c0, c1, c2, c3};
+}
+
+// The 4 random words covering source elements 8*group .. 8*group+7: element
+// 8*group + i takes word i/2, low half for even i.
+__device__ __forceinline__ U4 sr_words(uint64_t group, uint64_t seed, uint64_t stream_id) {
+  return philox4x32_10((uint32_t)group, (uint32_t)(group >> 32), (uint32_t)stream_id,
+                       (uint32_t)(stream_id >> 32), (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+__device__ __forceinline__ uint32_t sr_half(const U4& w, int i) {
+  uint32_t v = (i >> 1) == 0 ? w.x : (i >> 1) == 1 ? w.y : (i >> 1) == 2 ? w.z : w.w;
+  return (i & 1) ? (v >> 16) : (v & 0xffffu);
+}
+
+// ------------------------------------------------------------------ misc
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: spins until the phase with `parity` completes, the shared
+// abort flag is raised by another role, or `limit_ns` elapse (then raises the
+// abort flag and the timeout bit of the status word).  Returns true when the
+// phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint32_t* status, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        if (status) atomicOr(status, kDevTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ TMA / bulk copies
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// Copy a 32-row x 16-byte matrix from shared memory into tensor memory,
+// replicated into all four 32-lane quadrants.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (16-byte units), version 1, layout type in bits 61..63
+// (0 = no swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3fffu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3fffu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3fffu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(layout & 7u) << 61;
+  return d;
+}
+
+}  // namespace snip

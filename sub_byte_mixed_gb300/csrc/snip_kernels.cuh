@@ -1,0 +1,115 @@
+// snip_kernels.cuh -- parameter blocks, block-level reductions and launcher
+// declarations shared by the kernels (quant.cu, gemm.cu) and the C ABI
+// (api.cu).  Internal to the library.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "snip_device.cuh"
+
+namespace snip {
+
+// One quantization launch (NVFP4 or FP8, either orientation, either layout).
+struct QuantParams {
+  const uint16_t* x;        // source bf16 rows x cols
+  int64_t rows, cols;
+  int64_t out_rows, out_cols;   // output orientation (out_cols = the blocked/contraction dim)
+  int64_t orp, ocp;             // padded output dims (== out_rows/out_cols for the row-major layout)
+  uint64_t seed, stream_id;
+  const float* g_in;            // tensor scale given by the caller, or null
+  const uint32_t* amax_bits;    // published amax word (bf16 magnitude bits) when g_in is null
+  uint8_t* codes;
+  uint8_t* scales;              // NVFP4 only
+  float* g_out;
+  float* block_err;             // NVFP4 only, nullable
+};
+
+struct StatsParams {
+  const uint16_t* x;
+  int64_t rows, cols;
+  uint64_t seed, stream_id;
+  const uint32_t* amax_bits;
+  double* partials;             // 5 doubles per CTA
+  uint32_t* counter;
+  double* raw_out;              // SNIP_STATS_NVALS doubles
+  float* block_err4;
+  float* block_err8;
+};
+
+struct GemmParams {
+  const uint8_t* a_scales;
+  const uint8_t* b_scales;
+  const float* ga;
+  const float* gb;
+  float* D;
+  int64_t M, N, ldd;
+  int64_t kp;                   // padded contraction (elements)
+  int num_k_stages;             // kp / elements-per-stage
+  int num_m_tiles, num_n_tiles;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+// ------------------------------------------------------------------ block reductions
+__device__ __forceinline__ uint32_t mag_max4(uint4 a) {
+  return __vmaxu2(__vmaxu2(a.x & 0x7fff7fffu, a.y & 0x7fff7fffu), __vmaxu2(a.z & 0x7fff7fffu, a.w & 0x7fff7fffu));
+}
+
+// Max over the CTA (blockDim.x a multiple of 32, <= 1024); result valid in
+// every thread.
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v) {
+  __shared__ uint32_t red[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = l < nw ? red[l] : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sum of N doubles over the CTA; result valid in thread 0.
+template <int N>
+__device__ __forceinline__ void block_sum_f64(double (&v)[N]) {
+  __shared__ double red[32][N];
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (l == 0)
+#pragma unroll
+    for (int k = 0; k < N; ++k) red[w][k] = v[k];
+  __syncthreads();
+  if (w == 0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      v[k] = l < nw ? red[l][k] : 0.0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_amax(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, uint32_t* result_bits,
+                        float* result_float, uint32_t* status, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_nvfp4(const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
+                               cudaStream_t st);
+cudaError_t launch_quant_fp8(const QuantParams& p, int orient, int layout, int rnd, int num_sms, cudaStream_t st);
+cudaError_t launch_stats(const StatsParams& p, int rnd, int num_sms, cudaStream_t st);
+
+// GEMM: D = ga*gb*A B^T on MMA-layout operands.  fmt 1 = NVFP4, 0 = FP8.
+// a_codes / b_codes are passed to the launcher, which builds the TMA tensor
+// maps.
+cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,
+                        int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st);
+
+// Upper bound on the number of amax / stats partial slots any launch uses.
+constexpr int kMaxPartials = 1024;
+
+}  // namespace snip

@@ -1,0 +1,357 @@
+"""ctypes binding of the C ABI in ``include/snip.h`` (library ``_build/libsnip.so``).
+
+The ``snip_*`` functions below take the same arguments as their C
+counterparts (device pointers as ints, sizes, enums, the CUDA stream handle)
+and raise :class:`SnipError` on a non-OK status.  The lower-case helpers
+(``quantize_nvfp4`` ...) only allocate the output tensors with PyTorch and
+marshal pointers: every step of the computation runs in the library's CUDA
+kernels.  There is no fallback: if the library is missing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsnip.so")
+
+SNIP_OK, SNIP_ERR_INVALID_ARG, SNIP_ERR_SHAPE, SNIP_ERR_ALIGN, SNIP_ERR_NONFINITE, SNIP_ERR_TIMEOUT, \
+    SNIP_ERR_CUDA, SNIP_ERR_UNSUPPORTED_DEVICE, SNIP_ERR_WORKSPACE = range(9)
+FP8, NVFP4 = 0, 1
+RTN, SR = 0, 1
+ALONG_COLS, ALONG_ROWS = 0, 1
+ROWMAJOR, MMA = 0, 1
+TAG_X_FWD, TAG_W_FWD, TAG_DY_DGRAD, TAG_WT_DGRAD, TAG_DYT_WGRAD, TAG_XT_WGRAD = range(6)
+WS_HEADER_BYTES = 256
+STATS_NVALS = 8
+
+# every symbol include/snip.h declares
+EXPORTS = (
+    "snip_status_string", "snip_version", "snip_device_check", "snip_workspace_init", "snip_workspace_status",
+    "snip_quantize_workspace_size", "snip_amax", "snip_quantize_nvfp4", "snip_quantize_fp8",
+    "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
+    "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
+    "snip_quant_stats", "snip_stats_finalize",
+)
+
+
+class SnipError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
+
+
+class SnipStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in
+                ("sum_x2", "nvfp4_err2", "fp8_err2", "nvfp4_sr_var", "fp8_sr_var", "amax", "count",
+                 "ratio_nvfp4", "ratio_fp8")] + [("below_sqrt3_nvfp4", ctypes.c_int), ("below_sqrt3_fp8", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libsnip not built ({path} missing): run sub_byte_mixed_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i64, u64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_size_t
+    szp = ctypes.POINTER(ctypes.c_size_t)
+    sig = {
+        "snip_status_string": (ctypes.c_char_p, [i32]),
+        "snip_version": (i32, []),
+        "snip_device_check": (i32, []),
+        "snip_workspace_init": (i32, [vp, sz, vp]),
+        "snip_workspace_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_int)]),
+        "snip_quantize_workspace_size": (sz, [i64, i64]),
+        "snip_amax": (i32, [vp, i64, vp, vp, sz, vp]),
+        "snip_quantize_nvfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
+        "snip_quantize_fp8": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, sz, vp]),
+        "snip_quantized_bytes": (i32, [i32, i32, i64, i64, szp, szp]),
+        "snip_gemm": (i32, [i32, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz, vp]),
+        "snip_plan_create": (i32, [i32, ctypes.POINTER(ctypes.c_int), u64, ctypes.POINTER(vp)]),
+        "snip_plan_set_rounding": (i32, [vp, i32, i32, i32]),
+        "snip_plan_get": (i32, [vp, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_uint64)]),
+        "snip_plan_destroy": (None, [vp]),
+        "snip_qlinear_workspace_size": (sz, [vp, i32, i64, i64, i64]),
+        "snip_qlinear_fwd": (i32, [vp, i32, vp, vp, i64, i64, i64, vp, vp, sz, vp]),
+        "snip_qlinear_bwd": (i32, [vp, i32, vp, vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]),
+        "snip_quant_stats": (i32, [vp, i64, i64, i32, u64, u64, vp, vp, vp, vp, sz, vp]),
+        "snip_stats_finalize": (i32, [vp, ctypes.POINTER(SnipStats)]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return load().snip_status_string(int(status)).decode()
+
+
+def check(status: int, what: str = "") -> None:
+    if status != SNIP_OK:
+        raise SnipError(status, what)
+
+
+# ----------------------------------------------------------------------------- raw ABI (same names)
+
+def _call(name, *args):
+    st = getattr(load(), name)(*args)
+    check(st, name)
+
+
+def snip_device_check():
+    _call("snip_device_check")
+
+
+def snip_workspace_init(ws, ws_bytes, stream):
+    _call("snip_workspace_init", ws, ws_bytes, stream)
+
+
+def snip_workspace_status(ws, stream) -> int:
+    out = ctypes.c_int(0)
+    _call("snip_workspace_status", ws, stream, ctypes.byref(out))
+    return out.value
+
+
+def snip_quantize_workspace_size(rows, cols) -> int:
+    return load().snip_quantize_workspace_size(rows, cols)
+
+
+def snip_amax(x, n, amax_out, ws, ws_bytes, stream):
+    _call("snip_amax", x, n, amax_out, ws, ws_bytes, stream)
+
+
+def snip_quantize_nvfp4(x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
+                        block_sqerr, ws, ws_bytes, stream):
+    _call("snip_quantize_nvfp4", x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
+          block_sqerr, ws, ws_bytes, stream)
+
+
+def snip_quantize_fp8(x, rows, cols, orient, rnd, seed, stream_id, s_in, layout, codes, s_out, ws, ws_bytes, stream):
+    _call("snip_quantize_fp8", x, rows, cols, orient, rnd, seed, stream_id, s_in, layout, codes, s_out, ws,
+          ws_bytes, stream)
+
+
+def snip_quantized_bytes(fmt, layout, out_rows, out_cols) -> tuple[int, int]:
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _call("snip_quantized_bytes", fmt, layout, out_rows, out_cols, ctypes.byref(c), ctypes.byref(s))
+    return c.value, s.value
+
+
+def snip_gemm(fmt, a_codes, a_scales, ga, b_codes, b_scales, gb, M, N, K, D, ldd, ws, ws_bytes, stream):
+    _call("snip_gemm", fmt, a_codes, a_scales, ga, b_codes, b_scales, gb, M, N, K, D, ldd, ws, ws_bytes, stream)
+
+
+def snip_qlinear_workspace_size(plan, layer, T, K, N) -> int:
+    return load().snip_qlinear_workspace_size(plan, layer, T, K, N)
+
+
+def snip_qlinear_fwd(plan, layer, X, W, T, K, N, Y, ws, ws_bytes, stream):
+    _call("snip_qlinear_fwd", plan, layer, X, W, T, K, N, Y, ws, ws_bytes, stream)
+
+
+def snip_qlinear_bwd(plan, layer, X, W, dY, T, K, N, dX, dW, ws, ws_bytes, stream):
+    _call("snip_qlinear_bwd", plan, layer, X, W, dY, T, K, N, dX, dW, ws, ws_bytes, stream)
+
+
+def snip_quant_stats(a, rows, cols, rnd, seed, stream_id, raw_out, block_err_nvfp4, block_err_fp8, ws, ws_bytes,
+                     stream):
+    _call("snip_quant_stats", a, rows, cols, rnd, seed, stream_id, raw_out, block_err_nvfp4, block_err_fp8, ws,
+          ws_bytes, stream)
+
+
+def snip_stats_finalize(raw_host) -> SnipStats:
+    arr = (ctypes.c_double * STATS_NVALS)(*[float(v) for v in raw_host])
+    out = SnipStats()
+    _call("snip_stats_finalize", arr, ctypes.byref(out))
+    return out
+
+
+# ----------------------------------------------------------------------------- torch conveniences
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    torch = _torch()
+    return (stream or torch.cuda.current_stream()).cuda_stream
+
+
+class Plan:
+    """Owns a snip_plan (per-layer formats, rounding per quantization, seed)."""
+
+    def __init__(self, formats, seed: int = 0):
+        self.formats = list(formats)
+        arr = (ctypes.c_int * len(self.formats))(*self.formats)
+        h = ctypes.c_void_p()
+        check(load().snip_plan_create(len(self.formats), arr, seed, ctypes.byref(h)), "snip_plan_create")
+        self.handle = h
+        self.seed = seed
+
+    def set_rounding(self, layer: int, tag: int, rnd: int):
+        check(load().snip_plan_set_rounding(self.handle, layer, tag, rnd), "snip_plan_set_rounding")
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.snip_plan_destroy(self.handle)
+            self.handle = None
+
+
+class Workspace:
+    """A caller-owned device workspace with an initialised status word."""
+
+    def __init__(self, nbytes: int, device="cuda"):
+        torch = _torch()
+        self.nbytes = max(int(nbytes), WS_HEADER_BYTES)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        snip_workspace_init(self.buf.data_ptr(), self.nbytes, _stream())
+
+    @property
+    def ptr(self):
+        return self.buf.data_ptr()
+
+    def status(self) -> int:
+        return snip_workspace_status(self.ptr, _stream())
+
+    def reset(self):
+        snip_workspace_init(self.ptr, self.nbytes, _stream())
+
+
+_small_ws = {}
+
+
+def small_workspace(device=None) -> Workspace:
+    """A shared small workspace per device for the standalone quantize/stats/GEMM calls."""
+    torch = _torch()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    key = str(dev)
+    if key not in _small_ws:
+        _small_ws[key] = Workspace(snip_quantize_workspace_size(0, 0), dev)
+    return _small_ws[key]
+
+
+@dataclass
+class QuantNVFP4:
+    codes: object
+    scales: object
+    g: object            # device float tensor (1,)
+    out_rows: int
+    out_cols: int
+    layout: int
+    block_err: object = None
+
+
+@dataclass
+class QuantFP8:
+    codes: object
+    s: object
+    out_rows: int
+    out_cols: int
+    layout: int
+
+
+def amax(x, ws: Workspace | None = None):
+    torch = _torch()
+    ws = ws or small_workspace()
+    out = torch.empty(1, dtype=torch.float32, device=x.device)
+    snip_amax(x.data_ptr(), x.numel(), out.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return out
+
+
+def quantize_nvfp4(x, orient=ALONG_COLS, rnd=RTN, seed=0, stream_id=0, g_in=None, layout=ROWMAJOR,
+                   want_block_err=False, ws: Workspace | None = None) -> QuantNVFP4:
+    torch = _torch()
+    ws = ws or small_workspace()
+    rows, cols = x.shape
+    orows, ocols = (rows, cols) if orient == ALONG_COLS else (cols, rows)
+    cb, sb = snip_quantized_bytes(NVFP4, layout, orows, ocols)
+    codes = torch.empty(max(cb, 16), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(max(sb, 16), dtype=torch.uint8, device=x.device)
+    g = torch.empty(1, dtype=torch.float32, device=x.device)
+    berr = torch.empty((orows, ocols // 16), dtype=torch.float32, device=x.device) if want_block_err else None
+    snip_quantize_nvfp4(x.data_ptr(), rows, cols, orient, rnd, seed, stream_id, _ptr(g_in), layout,
+                        codes.data_ptr(), scales.data_ptr(), g.data_ptr(), _ptr(berr), ws.ptr, ws.nbytes, _stream())
+    return QuantNVFP4(codes[:cb], scales[:sb], g, orows, ocols, layout, berr)
+
+
+def quantize_fp8(x, orient=ALONG_COLS, rnd=RTN, seed=0, stream_id=0, s_in=None, layout=ROWMAJOR,
+                 ws: Workspace | None = None) -> QuantFP8:
+    torch = _torch()
+    ws = ws or small_workspace()
+    rows, cols = x.shape
+    orows, ocols = (rows, cols) if orient == ALONG_COLS else (cols, rows)
+    cb, _ = snip_quantized_bytes(FP8, layout, orows, ocols)
+    codes = torch.empty(max(cb, 16), dtype=torch.uint8, device=x.device)
+    s = torch.empty(1, dtype=torch.float32, device=x.device)
+    snip_quantize_fp8(x.data_ptr(), rows, cols, orient, rnd, seed, stream_id, _ptr(s_in), layout,
+                      codes.data_ptr(), s.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return QuantFP8(codes[:cb], s, orows, ocols, layout)
+
+
+def gemm(fmt, a, b, M, N, K, out=None, ws: Workspace | None = None):
+    """D = A B^T on two MMA-layout quantized operands (QuantNVFP4 / QuantFP8)."""
+    torch = _torch()
+    ws = ws or small_workspace()
+    D = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=a.codes.device)
+    if fmt == NVFP4:
+        snip_gemm(NVFP4, a.codes.data_ptr(), a.scales.data_ptr(), a.g.data_ptr(), b.codes.data_ptr(),
+                  b.scales.data_ptr(), b.g.data_ptr(), M, N, K, D.data_ptr(), D.stride(0), ws.ptr, ws.nbytes,
+                  _stream())
+    else:
+        snip_gemm(FP8, a.codes.data_ptr(), None, a.s.data_ptr(), b.codes.data_ptr(), None, b.s.data_ptr(),
+                  M, N, K, D.data_ptr(), D.stride(0), ws.ptr, ws.nbytes, _stream())
+    return D
+
+
+def qlinear_workspace(plan: Plan, layer: int, T: int, K: int, N: int, device="cuda") -> Workspace:
+    return Workspace(snip_qlinear_workspace_size(plan.handle, layer, T, K, N), device)
+
+
+def qlinear_fwd(plan: Plan, layer: int, X, W, ws: Workspace, Y=None):
+    torch = _torch()
+    T, K = X.shape
+    N = W.shape[0]
+    Y = Y if Y is not None else torch.empty((T, N), dtype=torch.float32, device=X.device)
+    snip_qlinear_fwd(plan.handle, layer, X.data_ptr(), W.data_ptr(), T, K, N, Y.data_ptr(), ws.ptr, ws.nbytes,
+                     _stream())
+    return Y
+
+
+def qlinear_bwd(plan: Plan, layer: int, X, W, dY, ws: Workspace, dX=None, dW=None):
+    torch = _torch()
+    T, K = X.shape
+    N = W.shape[0]
+    dX = dX if dX is not None else torch.empty((T, K), dtype=torch.float32, device=X.device)
+    dW = dW if dW is not None else torch.empty((N, K), dtype=torch.float32, device=X.device)
+    snip_qlinear_bwd(plan.handle, layer, X.data_ptr(), W.data_ptr(), dY.data_ptr(), T, K, N, dX.data_ptr(),
+                     dW.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return dX, dW
+
+
+def quant_stats(a, rnd=RTN, seed=0, stream_id=0, want_block_err=False, ws: Workspace | None = None, raw=None):
+    """Launch the statistics pass; returns (raw device tensor, block errors or None)."""
+    torch = _torch()
+    ws = ws or small_workspace()
+    rows, cols = a.shape
+    raw = raw if raw is not None else torch.empty(STATS_NVALS, dtype=torch.float64, device=a.device)
+    b4 = b8 = None
+    if want_block_err:
+        b4 = torch.empty((rows, cols // 16), dtype=torch.float32, device=a.device)
+        b8 = torch.empty((rows, cols // 16), dtype=torch.float32, device=a.device)
+    snip_quant_stats(a.data_ptr(), rows, cols, rnd, seed, stream_id, raw.data_ptr(), _ptr(b4), _ptr(b8), ws.ptr,
+                     ws.nbytes, _stream())
+    return raw, (b4, b8)
