@@ -168,7 +168,7 @@ def test_argument_errors(snip):
     with pytest.raises(snip.SnipError) as e:
         snip.quantize_nvfp4(x)
     assert e.value.status == snip.SNIP_ERR_SHAPE
-    y = torch.zeros(16 * 32 + 8, dtype=torch.bfloat16, device="cuda")[8:].view(16, 32)
+    y = torch.zeros(16 * 32 + 4, dtype=torch.bfloat16, device="cuda")[4:].view(16, 32)
     with pytest.raises(snip.SnipError) as e:
         snip.quantize_nvfp4(y)
     assert e.value.status == snip.SNIP_ERR_ALIGN
