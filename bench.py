@@ -36,9 +36,10 @@ if ROOT not in sys.path:
 
 METRIC = "qlinear fwd+bwd TFLOP/s (NVFP4/FP8 mix) & quantizer GB/s, % of GB300 roofline"
 UNIT = "TFLOP/s"
-NVFP4_BYTES_PER_ELEM = 2 + 2 + 0.5 + 1 / 16      # amax read + read + codes + scales
-FP8_BYTES_PER_ELEM = 2 + 2 + 1                   # amax read + read + codes
-STATS_BYTES_PER_ELEM = 2 + 2                     # amax read + read
+SCALES_BYTES_PER_ELEM = 2                        # amax pass: read
+NVFP4_BYTES_PER_ELEM = 2 + 0.5 + 1 / 16          # read + codes + block scales
+FP8_BYTES_PER_ELEM = 2 + 1                       # read + codes
+STATS_BYTES_PER_ELEM = 2                         # read
 FP4_OVER_BF16, FP8_OVER_BF16 = 13.5 / 2.25, 4.5 / 2.25   # nominal dense ratios
 
 
@@ -231,7 +232,8 @@ class Step:
         self.dW = [torch.empty((l.N, l.K), dtype=torch.float32, device=device) for l in cfg.linears]
         self.raw = torch.empty((len(cfg.linears), 3, snip.STATS_NVALS), dtype=torch.float64, device=device)
         self.ws = snip.Workspace(snip.snip_quantize_workspace_size(0, 0), device)
-        self.gs = torch.empty(8, dtype=torch.float32, device=device)
+        # {amax, NVFP4 g, FP8 s} of X, W and dY of every linear (16-byte slots)
+        self.sc = torch.empty((len(cfg.linears), 3, 4), dtype=torch.float32, device=device)
         # operand roles: (source, orient, out_rows, out_cols) per linear; buffers sized for the largest
         roles = lambda l: [(l.x_id, 0, T, l.K), ("W", 0, l.N, l.K), ("dY", 0, T, l.N), ("W", 1, l.K, l.N),
                            ("dY", 1, l.N, T), (l.x_id, 1, l.K, T)]
@@ -252,21 +254,27 @@ class Step:
             X = self.inp.X[l.x_id]
             W, dY = self.inp.W[j], self.inp.dY[j]
             src = {l.x_id: X, "W": W, "dY": dY}
+            scp = {l.x_id: self.sc[j, 0].data_ptr(), "W": self.sc[j, 1].data_ptr(), "dY": self.sc[j, 2].data_ptr()}
             sid = 8 * j
             rnd = [0, 0, 1, 1, 1, 1]
             qcat = "quant_nvfp4" if f == snip.NVFP4 else "quant_fp8"
             gcat = "gemm_nvfp4" if f == snip.NVFP4 else "gemm_fp8"
             bpe = NVFP4_BYTES_PER_ELEM if f == snip.NVFP4 else FP8_BYTES_PER_ELEM
+            fo = 4 if f == snip.NVFP4 else 8          # byte offset of g (NVFP4) or s (FP8) in a slot
+            for name in (l.x_id, "W", "dY"):
+                t = src[name]
+                calls.append((L.snip_tensor_scales, (t.data_ptr(), t.numel(), scp[name], ws, wsb, stream), "scales",
+                              SCALES_BYTES_PER_ELEM * t.numel()))
             for r, (name, orient, orr, occ) in enumerate(roles(l)):
                 t = src[name]
                 rows, cols = t.shape
-                g = self.gs.data_ptr() + 4 * r
+                g = scp[name] + fo
                 if f == snip.NVFP4:
-                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, None, snip.MMA,
+                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, None, ws, wsb, stream)
                     calls.append((L.snip_quantize_nvfp4, args, qcat, bpe * t.numel()))
                 else:
-                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, None, snip.MMA,
+                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), g, ws, wsb, stream)
                     calls.append((L.snip_quantize_fp8, args, qcat, bpe * t.numel()))
                 if r in (1, 3, 5):   # both operands of a GEMM are ready
@@ -275,17 +283,20 @@ class Step:
                     D = {1: self.Y[j], 3: self.dX[j], 5: self.dW[j]}[r]
                     sa = self.scales[a].data_ptr() if f == snip.NVFP4 else None
                     sb = self.scales[b].data_ptr() if f == snip.NVFP4 else None
-                    args = (f, self.codes[a].data_ptr(), sa, self.gs.data_ptr() + 4 * a, self.codes[b].data_ptr(),
-                            sb, self.gs.data_ptr() + 4 * b, M, N, K, D.data_ptr(), D.stride(0), ws, wsb, stream)
+                    ga = scp[roles(l)[a][0]] + fo
+                    gb = scp[roles(l)[b][0]] + fo
+                    args = (f, self.codes[a].data_ptr(), sa, ga, self.codes[b].data_ptr(), sb, gb, M, N, K,
+                            D.data_ptr(), D.stride(0), ws, wsb, stream)
                     calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K))
-            for k, (t, rn, s_id) in enumerate(((X, 0, sid + 0), (W, 0, sid + 1), (dY, 1, sid + 2))):
+            for k, (name, rn, s_id) in enumerate(((l.x_id, 0, sid + 0), ("W", 0, sid + 1), ("dY", 1, sid + 2))):
+                t = src[name]
                 rows, cols = t.shape
-                args = (t.data_ptr(), rows, cols, rn, 0, s_id, self.raw[j, k].data_ptr(), None, None, ws, wsb,
-                        stream)
+                args = (t.data_ptr(), rows, cols, rn, 0, s_id, scp[name], self.raw[j, k].data_ptr(), None, None, ws,
+                        wsb, stream)
                 calls.append((L.snip_quant_stats, args, "stats", STATS_BYTES_PER_ELEM * t.numel()))
         self.calls = calls
-        # kernels per call: quantize/stats = amax + main kernel, GEMM = 1
-        self.launches_per_step = sum(1 if c[2].startswith("gemm") else 2 for c in calls)
+        # one kernel per call (the scales are computed once per tensor and passed in)
+        self.launches_per_step = len(calls)
 
     def run(self, events=None):
         for i, (fn, args, _, _) in enumerate(self.calls):
@@ -330,6 +341,7 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
             snip.qlinear_bwd(p, j, X, inp.W[j], inp.dY[j], ws, dX=step.dX[j], dW=step.dW[j])
             for k, (t, rn) in enumerate(((X, 0), (inp.W[j], 0), (inp.dY[j], 1))):
                 snip.quant_stats(t, rnd=rn, seed=0, stream_id=8 * j + k, ws=ws, raw=step.raw[j, k])
+        # (the layer API computes each tensor's scales inside the calls)
         for h, d in zip(hY + hdX + hdW, step.Y + step.dX + step.dW):
             h.copy_(d, non_blocking=True)
         hraw.copy_(step.raw, non_blocking=True)

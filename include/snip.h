@@ -153,6 +153,16 @@ size_t snip_quantize_workspace_size(int64_t rows, int64_t cols);
  * workspace status and writes NaN.  n may be 0 (result 0). */
 snip_status snip_amax(const void* x, int64_t n, float* amax_out, void* ws, size_t ws_bytes, void* stream);
 
+/* scales_out (device, 3 floats) = {amax, g, s}: amax = max |x| over n bf16
+ * elements, g = amax / 2688 the NVFP4 tensor scale and s = amax / 448 the FP8
+ * tensor scale (g = s = 1 when amax is 0), each a single fp32 division.
+ * Pass scales_out + 1 as g_in of snip_quantize_nvfp4, scales_out + 2 as s_in of
+ * snip_quantize_fp8, or scales_out as scales_in of snip_quant_stats, to reuse
+ * one amax pass for several quantizations of the same tensor.  A non-finite
+ * element raises SNIP_ERR_NONFINITE in the workspace status and writes NaN. */
+snip_status snip_tensor_scales(const void* x, int64_t n, float* scales_out, void* ws, size_t ws_bytes,
+                               void* stream);
+
 /* ---------------------------------------------------------------- a2/a3: NVFP4 */
 
 /* NVFP4 quantization of a bf16 rows x cols tensor ("FP4 all the way",
@@ -250,10 +260,11 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
  * blocks along cols, under the tensor's rounding rnd (seed, stream_id for SR):
  * raw_out (device, SNIP_STATS_NVALS doubles) receives the SNIP_ST_* sums;
  * block_err_nvfp4 / block_err_fp8 (device, rows x cols/16 floats, nullable)
- * receive per-block squared errors.  Non-finite input raises
- * SNIP_ERR_NONFINITE in the workspace status. */
+ * receive per-block squared errors.  scales_in (device, nullable) holds the
+ * tensor's {amax, g, s} from snip_tensor_scales; NULL computes them first.
+ * Non-finite input raises SNIP_ERR_NONFINITE in the workspace status. */
 snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_round rnd, uint64_t seed,
-                             uint64_t stream_id, double* raw_out, float* block_err_nvfp4,
+                             uint64_t stream_id, const float* scales_in, double* raw_out, float* block_err_nvfp4,
                              float* block_err_fp8, void* ws, size_t ws_bytes, void* stream);
 
 /* Host helper: derive ratios and sqrt(3) flags from a host copy of raw_out. */

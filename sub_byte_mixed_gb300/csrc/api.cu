@@ -19,8 +19,7 @@ namespace {
 constexpr size_t kOffStatus = 0;        // uint32 sticky status bits
 constexpr size_t kOffAmaxCounter = 4;   // uint32, self-resetting
 constexpr size_t kOffStatsCounter = 8;  // uint32, self-resetting
-constexpr size_t kOffAmaxSlots = 16;    // 8 x uint32 published amax words
-constexpr size_t kOffScaleSlots = 64;   // 8 x float tensor scales (qlinear operands)
+constexpr size_t kOffScaleSlots = 64;   // 8 slots x 4 floats {amax, NVFP4 g, FP8 s, -} (12 bytes used)
 constexpr size_t kOffAmaxPartials = SNIP_WS_HEADER_BYTES;                            // kMaxPartials x uint32
 constexpr size_t kOffStatsPartials = kOffAmaxPartials + 4 * kMaxPartials;            // kMaxPartials x 5 doubles
 constexpr size_t kSmallWorkspace = kOffStatsPartials + 8 * 5 * kMaxPartials;         // 45312
@@ -80,20 +79,19 @@ OperandBytes operand_bytes(int fmt, int layout, int64_t orows, int64_t ocols) {
 }
 
 // ---------------------------------------------------------------- shared launch helpers
-snip_status run_amax(const void* x, int64_t n, int slot, float* result_float, void* ws, int num_sms, cudaStream_t st) {
-  return cuda_status(launch_amax(static_cast<const uint16_t*>(x), n, ws_at<uint32_t>(ws, kOffAmaxPartials),
-                                 ws_at<uint32_t>(ws, kOffAmaxCounter), ws_at<uint32_t>(ws, kOffAmaxSlots + 4 * slot),
-                                 result_float, ws_at<uint32_t>(ws, kOffStatus), num_sms, st));
+float* scale_slot(void* ws, int slot) { return ws_at<float>(ws, kOffScaleSlots + 16 * slot); }
+
+// amax of a bf16 tensor and the two tensor scales derived from it -> out3
+snip_status run_scales(const void* x, int64_t n, float* out3, void* ws, int num_sms, cudaStream_t st) {
+  return cuda_status(launch_scales(static_cast<const uint16_t*>(x), n, ws_at<uint32_t>(ws, kOffAmaxPartials),
+                                   ws_at<uint32_t>(ws, kOffAmaxCounter), out3, ws_at<uint32_t>(ws, kOffStatus),
+                                   num_sms, st));
 }
 
-// One quantization: amax (unless g_in) then the quantizer kernel.
+// One quantization with the tensor scale `scale` (device float).
 snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int orient, int rnd, uint64_t seed,
-                         uint64_t stream_id, const float* g_in, int layout, uint8_t* codes, uint8_t* scales,
-                         float* g_out, float* block_err, void* ws, int amax_slot, int num_sms, cudaStream_t st) {
-  if (!g_in) {
-    snip_status s = run_amax(x, rows * cols, amax_slot, nullptr, ws, num_sms, st);
-    if (s != SNIP_OK) return s;
-  }
+                         uint64_t stream_id, const float* scale, int layout, uint8_t* codes, uint8_t* scales,
+                         float* g_out, float* block_err, int num_sms, cudaStream_t st) {
   QuantParams p;
   p.x = static_cast<const uint16_t*>(x);
   p.rows = rows;
@@ -104,17 +102,30 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   p.ocp = layout == SNIP_LAYOUT_MMA ? mma_cols(fmt, p.out_cols) : p.out_cols;
   p.seed = seed;
   p.stream_id = stream_id;
-  p.g_in = g_in;
-  p.amax_bits = ws_at<uint32_t>(ws, kOffAmaxSlots + 4 * amax_slot);
+  p.scale = scale;
   p.codes = codes;
   p.scales = scales;
   p.g_out = g_out;
   p.block_err = block_err;
   // an empty output still publishes its tensor scale: the one-CTA row kernel does that
   if (p.orp == 0 || p.ocp == 0) orient = SNIP_BLOCKS_ALONG_COLS;
-  if (fmt == SNIP_FMT_NVFP4)
-    return cuda_status(launch_quant_nvfp4(p, orient, layout, rnd, block_err != nullptr, num_sms, st));
-  return cuda_status(launch_quant_fp8(p, orient, layout, rnd, num_sms, st));
+  return cuda_status(launch_quant(fmt == SNIP_FMT_NVFP4 ? 1 : 0, p, orient, layout, rnd, block_err != nullptr,
+                                  num_sms, st));
+}
+
+// Standalone quantization: tensor scales (unless given) then the quantizer.
+snip_status run_quantize_api(int fmt, const void* x, int64_t rows, int64_t cols, int orient, int rnd, uint64_t seed,
+                             uint64_t stream_id, const float* g_in, int layout, uint8_t* codes, uint8_t* scales,
+                             float* g_out, float* block_err, void* ws, int num_sms, cudaStream_t st) {
+  const float* scale = g_in;
+  if (!scale) {
+    float* slot = scale_slot(ws, 0);
+    snip_status s = run_scales(x, rows * cols, slot, ws, num_sms, st);
+    if (s != SNIP_OK) return s;
+    scale = slot + (fmt == SNIP_FMT_NVFP4 ? 1 : 2);
+  }
+  return run_quantize(fmt, x, rows, cols, orient, rnd, seed, stream_id, scale, layout, codes, scales, g_out,
+                      block_err, num_sms, st);
 }
 
 snip_status run_gemm(int fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga, const uint8_t* b_codes,
@@ -198,7 +209,20 @@ snip_status snip_amax(const void* x, int64_t n, float* amax_out, void* ws, size_
   if ((!x && n > 0) || !amax_out || n < 0) return SNIP_ERR_INVALID_ARG;
   if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
   if (!aligned16(x) || !aligned16(ws)) return SNIP_ERR_ALIGN;
-  return run_amax(x, n, 0, amax_out, ws, sms, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* slot = scale_slot(ws, 0);
+  if ((s = run_scales(x, n, slot, ws, sms, st)) != SNIP_OK) return s;
+  return cuda_status(cudaMemcpyAsync(amax_out, slot, sizeof(float), cudaMemcpyDeviceToDevice, st));
+}
+
+snip_status snip_tensor_scales(const void* x, int64_t n, float* scales_out, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if ((!x && n > 0) || !scales_out || n < 0) return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(ws)) return SNIP_ERR_ALIGN;
+  return run_scales(x, n, scales_out, ws, sms, static_cast<cudaStream_t>(stream));
 }
 
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
@@ -231,8 +255,8 @@ snip_status snip_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, snip_
   if (s != SNIP_OK) return s;
   s = check_quantize_args(SNIP_FMT_NVFP4, x, rows, cols, orient, rnd, layout, codes, scales, g_out, ws, ws_bytes);
   if (s != SNIP_OK) return s;
-  return run_quantize(SNIP_FMT_NVFP4, x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
-                      block_sqerr, ws, 0, sms, static_cast<cudaStream_t>(stream));
+  return run_quantize_api(SNIP_FMT_NVFP4, x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales,
+                          g_out, block_sqerr, ws, sms, static_cast<cudaStream_t>(stream));
 }
 
 snip_status snip_quantize_fp8(const void* x, int64_t rows, int64_t cols, snip_orient orient, snip_round rnd,
@@ -244,8 +268,8 @@ snip_status snip_quantize_fp8(const void* x, int64_t rows, int64_t cols, snip_or
   s = check_quantize_args(SNIP_FMT_FP8_E4M3, x, rows, cols, orient, rnd, layout, codes, nullptr, s_out, ws,
                           ws_bytes);
   if (s != SNIP_OK) return s;
-  return run_quantize(SNIP_FMT_FP8_E4M3, x, rows, cols, orient, rnd, seed, stream_id, s_in, layout, codes, nullptr,
-                      s_out, nullptr, ws, 0, sms, static_cast<cudaStream_t>(stream));
+  return run_quantize_api(SNIP_FMT_FP8_E4M3, x, rows, cols, orient, rnd, seed, stream_id, s_in, layout, codes,
+                          nullptr, s_out, nullptr, ws, sms, static_cast<cudaStream_t>(stream));
 }
 
 snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
@@ -362,17 +386,21 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
   const uint64_t sid = (uint64_t)layer * 8;
   QlLayout L = ql_layout(fmt, T, K, N, false);
   uint8_t* b = static_cast<uint8_t*>(ws);
-  float* gs = ws_at<float>(ws, kOffScaleSlots);
+  const int si = fmt == SNIP_FMT_NVFP4 ? 1 : 2;   // which tensor scale the format uses
+  float* sx = scale_slot(ws, 0);
+  float* sw = scale_slot(ws, 1);
+  if ((s = run_scales(X, T * K, sx, ws, sms, st)) != SNIP_OK) return s;
+  if ((s = run_scales(W, N * K, sw, ws, sms, st)) != SNIP_OK) return s;
   if ((s = run_quantize(fmt, X, T, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_X_FWD], plan->seed, sid + SNIP_TAG_X_FWD,
-                        nullptr, SNIP_LAYOUT_MMA, b + L.op[0].codes_off, b + L.op[0].scales_off, gs + 0, nullptr, ws,
-                        0, sms, st)) != SNIP_OK)
+                        sx + si, SNIP_LAYOUT_MMA, b + L.op[0].codes_off, b + L.op[0].scales_off, nullptr, nullptr,
+                        sms, st)) != SNIP_OK)
     return s;
   if ((s = run_quantize(fmt, W, N, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_W_FWD], plan->seed, sid + SNIP_TAG_W_FWD,
-                        nullptr, SNIP_LAYOUT_MMA, b + L.op[1].codes_off, b + L.op[1].scales_off, gs + 1, nullptr, ws,
-                        1, sms, st)) != SNIP_OK)
+                        sw + si, SNIP_LAYOUT_MMA, b + L.op[1].codes_off, b + L.op[1].scales_off, nullptr, nullptr,
+                        sms, st)) != SNIP_OK)
     return s;
-  return run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, gs + 0, b + L.op[1].codes_off,
-                  b + L.op[1].scales_off, gs + 1, T, N, K, Y, N, ws, sms, st);
+  return run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, sx + si, b + L.op[1].codes_off,
+                  b + L.op[1].scales_off, sw + si, T, N, K, Y, N, ws, sms, st);
 }
 
 snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W, const void* dY,
@@ -392,36 +420,42 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
   const uint64_t sid = (uint64_t)layer * 8;
   QlLayout L = ql_layout(fmt, T, K, N, true);
   uint8_t* b = static_cast<uint8_t*>(ws);
-  float* gs = ws_at<float>(ws, kOffScaleSlots);
+  const int si = fmt == SNIP_FMT_NVFP4 ? 1 : 2;
+  float* sx = scale_slot(ws, 0);
+  float* sw = scale_slot(ws, 1);
+  float* sd = scale_slot(ws, 2);
+  if ((s = run_scales(dY, T * N, sd, ws, sms, st)) != SNIP_OK) return s;
+  if ((s = run_scales(W, N * K, sw, ws, sms, st)) != SNIP_OK) return s;
+  if ((s = run_scales(X, T * K, sx, ws, sms, st)) != SNIP_OK) return s;
   // dgrad: dX = Q(dY) Q(W^T)^T, contraction N
   if ((s = run_quantize(fmt, dY, T, N, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_DY_DGRAD], plan->seed,
-                        sid + SNIP_TAG_DY_DGRAD, nullptr, SNIP_LAYOUT_MMA, b + L.op[0].codes_off,
-                        b + L.op[0].scales_off, gs + 2, nullptr, ws, 2, sms, st)) != SNIP_OK)
+                        sid + SNIP_TAG_DY_DGRAD, sd + si, SNIP_LAYOUT_MMA, b + L.op[0].codes_off,
+                        b + L.op[0].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
     return s;
   if ((s = run_quantize(fmt, W, N, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_WT_DGRAD], plan->seed,
-                        sid + SNIP_TAG_WT_DGRAD, nullptr, SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
-                        b + L.op[1].scales_off, gs + 3, nullptr, ws, 1, sms, st)) != SNIP_OK)
+                        sid + SNIP_TAG_WT_DGRAD, sw + si, SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
+                        b + L.op[1].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
     return s;
-  if ((s = run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, gs + 2, b + L.op[1].codes_off,
-                    b + L.op[1].scales_off, gs + 3, T, K, N, dX, K, ws, sms, st)) != SNIP_OK)
+  if ((s = run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, sd + si, b + L.op[1].codes_off,
+                    b + L.op[1].scales_off, sw + si, T, K, N, dX, K, ws, sms, st)) != SNIP_OK)
     return s;
   // wgrad: dW = Q(dY^T) Q(X^T)^T, contraction T
   if ((s = run_quantize(fmt, dY, T, N, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_DYT_WGRAD], plan->seed,
-                        sid + SNIP_TAG_DYT_WGRAD, nullptr, SNIP_LAYOUT_MMA, b + L.op[2].codes_off,
-                        b + L.op[2].scales_off, gs + 4, nullptr, ws, 2, sms, st)) != SNIP_OK)
+                        sid + SNIP_TAG_DYT_WGRAD, sd + si, SNIP_LAYOUT_MMA, b + L.op[2].codes_off,
+                        b + L.op[2].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
     return s;
   if ((s = run_quantize(fmt, X, T, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_XT_WGRAD], plan->seed,
-                        sid + SNIP_TAG_XT_WGRAD, nullptr, SNIP_LAYOUT_MMA, b + L.op[3].codes_off,
-                        b + L.op[3].scales_off, gs + 5, nullptr, ws, 0, sms, st)) != SNIP_OK)
+                        sid + SNIP_TAG_XT_WGRAD, sx + si, SNIP_LAYOUT_MMA, b + L.op[3].codes_off,
+                        b + L.op[3].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
     return s;
-  return run_gemm(fmt, b + L.op[2].codes_off, b + L.op[2].scales_off, gs + 4, b + L.op[3].codes_off,
-                  b + L.op[3].scales_off, gs + 5, N, K, T, dW, K, ws, sms, st);
+  return run_gemm(fmt, b + L.op[2].codes_off, b + L.op[2].scales_off, sd + si, b + L.op[3].codes_off,
+                  b + L.op[3].scales_off, sx + si, N, K, T, dW, K, ws, sms, st);
 }
 
 // ---------------------------------------------------------------- statistics
 snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_round rnd, uint64_t seed,
-                             uint64_t stream_id, double* raw_out, float* block_err_nvfp4, float* block_err_fp8,
-                             void* ws, size_t ws_bytes, void* stream) {
+                             uint64_t stream_id, const float* scales_in, double* raw_out, float* block_err_nvfp4,
+                             float* block_err_fp8, void* ws, size_t ws_bytes, void* stream) {
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
@@ -430,14 +464,19 @@ snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_rou
   if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
   if (!aligned16(a) || !aligned16(ws)) return SNIP_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((s = run_amax(a, rows * cols, 3, nullptr, ws, sms, st)) != SNIP_OK) return s;
+  const float* sc = scales_in;
+  if (!sc) {
+    float* slot = scale_slot(ws, 3);
+    if ((s = run_scales(a, rows * cols, slot, ws, sms, st)) != SNIP_OK) return s;
+    sc = slot;
+  }
   StatsParams p;
   p.x = static_cast<const uint16_t*>(a);
   p.rows = rows;
   p.cols = cols;
   p.seed = seed;
   p.stream_id = stream_id;
-  p.amax_bits = ws_at<uint32_t>(ws, kOffAmaxSlots + 4 * 3);
+  p.scales3 = sc;
   p.partials = ws_at<double>(ws, kOffStatsPartials);
   p.counter = ws_at<uint32_t>(ws, kOffStatsCounter);
   p.raw_out = raw_out;

@@ -9,13 +9,15 @@
 // elements of each operand row); FP8 E4M3 operands on kind::f8f6f4.  The fp32
 // tensor scales multiply the fp32 accumulator in the epilogue.
 //
-// Structure (one CTA per SM, persistent over output tiles, 6 warps):
+// Structure (one CTA per SM, persistent over output tiles, 10 warps):
 //   warp 0     TMA producer: 128B-swizzled code tiles via cp.async.bulk.tensor,
 //              block-scale chunks via cp.async.bulk, into a STAGES-deep ring;
 //   warp 1     allocates tensor memory and issues tcgen05.cp (scales smem ->
 //              TMEM) and tcgen05.mma (accumulator in TMEM) from one thread;
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, scale by ga*gb, store
-//              fp32 rows.
+//   warps 2-9  epilogue: each warp drains 32 accumulator rows x BN/2 columns
+//              from TMEM into registers with back-to-back tcgen05.ld, hands
+//              the accumulator back to the MMA warp at once, then scales by
+//              ga*gb and stores fp32 rows while the next tile's MMAs run.
 // Every wait is bounded (globaltimer); on expiry the CTA raises the timeout
 // bit of the status word, lets all roles fall through, drains in-flight
 // tensor-core work and frees its tensor memory before returning.
@@ -46,6 +48,9 @@ struct GemmCfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_COLS = BN / 2;          // accumulator columns drained by one epilogue warp
+  static constexpr int THREADS = 32 * (2 + EPI_WARPS);
   // Instruction descriptor.  Block-scaled FP4: A/B type E2M1 (1) in bits 7-9
   // and 10-12, K-major, N>>3 in bits 17-22, scale type UE4M3 (0) in bit 23,
   // M>>4 in bits 24-28.  FP8: D type f32 (1) in bits 4-5, A/B type E4M3 (0).
@@ -55,7 +60,7 @@ struct GemmCfg {
 };
 
 template <int FMT, int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   using C = GemmCfg<FMT, BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -73,7 +78,7 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-    for (int a = 0; a < C::ACC_STAGES; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 4); }
+    for (int a = 0; a < C::ACC_STAGES; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), C::EPI_WARPS); }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -169,38 +174,39 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;       // which BN/2 columns it drains
     const float alpha = __fmul_rn(*p.ga, *p.gb);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
+      uint32_t r[C::EPI_COLS / 32][32];
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + half * C::EPI_COLS;
+#pragma unroll
+      for (int c = 0; c < C::EPI_COLS / 32; ++c) tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
       const int64_t row = (int64_t)mt * C::BM + q * 32 + lane;
-      float* drow = p.D + row * p.ldd;
-#pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + ch * 32, r);
-        tmem_ld_wait();
-        if (ch == BN / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty(acc));
-        }
-        const int64_t col0 = (int64_t)nt * BN + ch * 32;
-        if (row < p.M) {
+      if (row < p.M) {
+        float* drow = p.D + row * p.ldd;
+        const int64_t col0 = (int64_t)nt * BN + half * C::EPI_COLS;
+#pragma unroll
+        for (int c = 0; c < C::EPI_COLS / 32; ++c)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            if (col0 + 4 * j < p.N) {
-              float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * j])),
-                                     __fmul_rn(alpha, __uint_as_float(r[4 * j + 1])),
-                                     __fmul_rn(alpha, __uint_as_float(r[4 * j + 2])),
-                                     __fmul_rn(alpha, __uint_as_float(r[4 * j + 3])));
-              *reinterpret_cast<float4*>(drow + col0 + 4 * j) = v;
+            const int64_t col = col0 + c * 32 + 4 * j;
+            if (col < p.N) {
+              const float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[c][4 * j])),
+                                           __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 1])),
+                                           __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 2])),
+                                           __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 3])));
+              *reinterpret_cast<float4*>(drow + col) = v;
             }
           }
-        }
       }
       if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
     }
@@ -266,7 +272,7 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
   p.num_n_tiles = (int)((p.N + BN - 1) / BN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_tn_kernel<FMT, BN><<<grid, 192, C::SMEM_BYTES, st>>>(ta, tb, p);
+  gemm_tn_kernel<FMT, BN><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,7 @@
-// quant.cu -- HBM-bound kernels of the quantized linear layer: tensor amax
-// (a1), NVFP4 quantization with blocks along columns (a2) or rows (a3), FP8
-// E4M3 quantization (a4) and SNIP's statistics pass (a8).
+// quant.cu -- HBM-bound kernels of the quantized linear layer: tensor scales
+// (a1: amax, NVFP4 g, FP8 s), NVFP4 quantization with blocks along columns
+// (a2) or rows (a3), FP8 E4M3 quantization (a4) and SNIP's statistics pass
+// (a8).
 //
 // Sources: "FP4 all the way" (Chmiel et al.), summary page, Outline (NVFP4 =
 // 16 E2M1 values sharing an E4M3 scale; RTN forward, SR backward; the
@@ -8,28 +9,31 @@
 // activations, weights and gradients); "SNIP", Figure 5 (each GEMM operand
 // quantized along its own contraction dim).
 //
-// Design: every kernel streams its input once with 16-byte coalesced loads;
-// one thread owns 8 consecutive source elements (one Philox call supplies
-// their 8 x 16 random bits) and a lane pair owns one 16-element block, whose
-// amax is exchanged with one shuffle.  The transposed (column-block) kernels
-// stage a 128 x 64 tile in shared memory so that loads and stores both stay
-// coalesced.  The tensor scale comes from a two-stage amax reduction whose
-// last CTA publishes one word, so quantizer CTAs read a single value.
+// Design: every kernel streams its input once with 16-byte loads.  One thread
+// owns one 16-element block (32 source bytes), so the block's scale is
+// computed once and no shuffles are needed; a warp covers 32 consecutive
+// blocks of a row.  The transposed (column-block) kernels stage a 128 x 64
+// tile in shared memory so that loads and stores both stay coalesced.
+// Rounding to nearest uses the hardware E2M1/E4M3 conversions; stochastic
+// rounding uses the carry form of the 16-bit rule (snip_device.cuh), with one
+// Philox4x32-10 call per 8 source elements.
 #include "snip_kernels.cuh"
 
 namespace snip {
 
-// ------------------------------------------------------------------ amax
+constexpr float kInf = __builtin_huge_valf();
+
+// ------------------------------------------------------------------ a1: tensor scales
 // Magnitudes are compared as bf16 bit patterns (sign cleared): for finite
 // values the integer order is the float order, and any pattern >= 0x7f80 is
-// an infinity or NaN.
-__global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, int64_t n,
-                                                   uint32_t* __restrict__ partials,
-                                                   uint32_t* __restrict__ counter,
-                                                   uint32_t* __restrict__ result_bits,
-                                                   float* __restrict__ result_float,
-                                                   uint32_t* __restrict__ status) {
-  uint32_t m2 = 0;  // two 16-bit lanes of magnitudes (sign bits cleared before the max)
+// an infinity or NaN.  Each CTA publishes its max; the last CTA to finish
+// reduces them and writes out3 = {amax, g = amax/2688, s = amax/448} (g = s = 1
+// for an all-zero tensor; all NaN and the status bit for non-finite input).
+__global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                        uint32_t* __restrict__ partials,
+                                                        uint32_t* __restrict__ counter, float* __restrict__ out3,
+                                                        uint32_t* __restrict__ status) {
+  uint32_t m2 = 0;
   const int64_t nvec = n >> 3;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -40,7 +44,6 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
     m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(mag_max4(a), mag_max4(b)), __vmaxu2(mag_max4(c), mag_max4(d))));
   }
   for (; i < nvec; i += stride) m2 = __vmaxu2(m2, mag_max4(__ldg(xv + i)));
-  // tail (n % 8 elements)
   if (blockIdx.x == 0 && threadIdx.x < (n & 7)) m2 = __vmaxu2(m2, (uint32_t)(x[(nvec << 3) + threadIdx.x] & 0x7fffu));
   uint32_t m = max(m2 & 0xffffu, m2 >> 16);
   m = block_max_u32(m);
@@ -49,8 +52,7 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
     partials[blockIdx.x] = m;
     if (m >= 0x7f80u) atomicOr(status, kDevNonFinite);
     __threadfence();
-    uint32_t done = atomicAdd(counter, 1u);
-    s_last = (done == gridDim.x - 1);
+    s_last = atomicAdd(counter, 1u) == gridDim.x - 1;
   }
   __syncthreads();
   if (!s_last) return;
@@ -59,407 +61,448 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
   for (uint32_t j = threadIdx.x; j < gridDim.x; j += blockDim.x) mm = max(mm, ((volatile uint32_t*)partials)[j]);
   mm = block_max_u32(mm);
   if (threadIdx.x == 0) {
-    *result_bits = mm;
-    if (result_float) *result_float = mm >= 0x7f80u ? __int_as_float(0x7fc00000) : bf16_bits_to_float(mm);
+    if (mm >= 0x7f80u) {
+      const float nan = __int_as_float(0x7fc00000);
+      out3[0] = nan; out3[1] = nan; out3[2] = nan;
+    } else {
+      const float a = bf16_bits_to_float(mm);
+      out3[0] = a;
+      out3[1] = a == 0.0f ? 1.0f : __fdiv_rn(a, 2688.0f);   // 6 * 448: largest E2M1 x largest E4M3
+      out3[2] = a == 0.0f ? 1.0f : __fdiv_rn(a, 448.0f);
+    }
     *counter = 0;  // ready for the next reduction on this workspace
   }
 }
 
-// Tensor scale of an NVFP4 tensor (amax / (6*448), 1 for an all-zero tensor)
-// or of an FP8 tensor (amax / 448); NaN when the amax word flags non-finite.
-__device__ __forceinline__ float tensor_scale_from_bits(uint32_t mbits, float divisor) {
-  if (mbits >= 0x7f80u) return __int_as_float(0x7fc00000);
-  float m = bf16_bits_to_float(mbits);
-  return m == 0.0f ? 1.0f : __fdiv_rn(m, divisor);
-}
-
-__device__ __forceinline__ float load_scale(const QuantParams& p, float divisor) {
-  return p.g_in ? *p.g_in : tensor_scale_from_bits(*p.amax_bits, divisor);
-}
-
 // Byte offset of the E4M3 scale of (row r, block kb) in the MMA layout.
 __device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64_t ocp) {
-  int64_t chunk = (r >> 7) * (ocp >> 6) + (kb >> 2);
+  const int64_t chunk = (r >> 7) * (ocp >> 6) + (kb >> 2);
   return chunk * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
 }
 
-// ------------------------------------------------------------------ NVFP4 block encode
-// Encodes 8 elements (bf16 bits in w[0..3], element i in half i of w[i/2])
-// that are one half of a 16-element block whose partner half sits in the
-// lane with index ^1.  Returns the 8 packed codes; *scale gets the block's
-// E4M3 code, *err (if ERR) this half's squared dequantization error.
-template <int RND, bool ERR>
-__device__ __forceinline__ uint32_t nvfp4_encode_half(const uint32_t (&w)[4], float g, float six_g,
-                                                      const U4& rbits, uint32_t* scale, float* err) {
-  uint32_t m2 = __vmaxu2(__vmaxu2(w[0] & 0x7fff7fffu, w[1] & 0x7fff7fffu),
-                         __vmaxu2(w[2] & 0x7fff7fffu, w[3] & 0x7fff7fffu));
-  uint32_t mh = max(m2 & 0xffffu, m2 >> 16);
-  mh = max(mh, __shfl_xor_sync(0xffffffffu, mh, 1));
-  const float ab = bf16_bits_to_float(mh);
-  const uint32_t s = e4m3_rn_sat(__fdiv_rn(ab, six_g));
-  const float p = __fmul_rn(e4m3_decode_pos(s), g);
-  const float inv = __frcp_rn(p);
-  uint32_t packed = 0;
+// ------------------------------------------------------------------ per-block helpers
+// 16 bf16 values (two uint4) -> signed floats.
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&v)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ uint32_t amax16_bits(const uint4& a, const uint4& b) {
+  const uint32_t m2 = __vmaxu2(mag_max4(a), mag_max4(b));
+  return max(m2 & 0xffffu, m2 >> 16);
+}
+
+// Block scale of NVFP4: s_b = E4M3(amax_b / (6 g)) (nearest even, saturating),
+// p = decode(s_b) * g, inv = 1 / p.  `special` marks p == 0 or 1/p overflow,
+// where codes are decided without the product (zero -> 0, else 6).
+struct BlockScale {
+  uint32_t s;
+  float p, inv;
+  bool special;
+};
+__device__ __forceinline__ BlockScale nvfp4_block_scale(uint32_t amax_bits, float g, float six_g) {
+  BlockScale r;
+  r.s = e4m3_rn_sat(__fdiv_rn(bf16_bits_to_float(amax_bits), six_g));
+  r.p = __fmul_rn(e4m3_decode_pos(r.s), g);
+  r.inv = __frcp_rn(r.p);
+  r.special = !(r.inv < kInf);
+  return r;
+}
+
+// The 16 random halves of source elements e0 .. e0+15 (e0 % 8 == 0).
+__device__ __forceinline__ void sr_bits16(int64_t e0, uint64_t seed, uint64_t sid, uint32_t (&u)[8]) {
+  const U4 w0 = sr_words((uint64_t)e0 >> 3, seed, sid);
+  const U4 w1 = sr_words(((uint64_t)e0 >> 3) + 1, seed, sid);
+  u[0] = w0.x; u[1] = w0.y; u[2] = w0.z; u[3] = w0.w;
+  u[4] = w1.x; u[5] = w1.y; u[6] = w1.z; u[7] = w1.w;
+}
+// random half of element i from the packed words (element i in half i%2 of word i/2)
+__device__ __forceinline__ uint32_t uhalf(const uint32_t (&u)[8], int i) {
+  return (i & 1) ? (u[i >> 1] >> 16) : (u[i >> 1] & 0xffffu);
+}
+
+// Encode one NVFP4 block of 16 signed values into two words of packed codes
+// (element 2j in the low nibble of byte j).  RND: 0 nearest, 1 stochastic.
+template <int RND>
+__device__ __forceinline__ uint2 nvfp4_encode16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8]) {
+  uint32_t w[2] = {0u, 0u};
+  if (bs.special) {
+    // p == 0: every magnitude 0; 1/p overflowed: non-zero elements saturate to 6
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t sign = (__float_as_uint(v[i]) >> 28) & 8u;
+      const uint32_t mag = (bs.p == 0.0f || v[i] == 0.0f) ? 0u : 7u;
+      w[i >> 3] |= (sign | mag) << (4 * (i & 7));
+    }
+  } else if (RND == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i >> 2] |= e2m1x2_rn(__fmul_rn(v[2 * i], bs.inv), __fmul_rn(v[2 * i + 1], bs.inv)) << (8 * (i & 3));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t b = __float_as_uint(v[i]);
+      const float y = __fmul_rn(__uint_as_float(b & 0x7fffffffu), bs.inv);
+      w[i >> 3] |= (((b >> 28) & 8u) | e2m1_sr(y, uhalf(u, i))) << (4 * (i & 7));
+    }
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+// Squared dequantization error of an encoded block (x_hat = value(code) * p).
+__device__ __forceinline__ float nvfp4_block_err(const float (&v)[16], const uint2& c, float p) {
   float e = 0.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t h = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
-    const float ax = bf16_bits_to_float(h & 0x7fffu);
-    const float y = __fmul_rn(ax, inv);
-    uint32_t mag;
-    if (RND == 0) mag = e2m1_rn(y);
-    else mag = e2m1_sr(y, sr_half(rbits, i));
-    if (p == 0.0f || ax == 0.0f) mag = 0u;
-    packed |= (((h >> 12) & 8u) | mag) << (4 * i);
-    if (ERR) {
-      const float d = __fsub_rn(__fmul_rn(e2m1_value(mag), p), ax);
-      e = __fadd_rn(e, __fmul_rn(d, d));
-    }
+    const uint32_t byte = ((i < 4 ? c.x : c.y) >> (8 * (i & 3))) & 0xffu;
+    const float2 q = e2m1x2_decode(byte);
+    const float d0 = __fsub_rn(__fmul_rn(q.x, p), v[2 * i]);
+    const float d1 = __fsub_rn(__fmul_rn(q.y, p), v[2 * i + 1]);
+    e = __fadd_rn(e, __fadd_rn(__fmul_rn(d0, d0), __fmul_rn(d1, d1)));
   }
-  *scale = s;
-  if (ERR) *err = e;
-  return packed;
+  return e;
 }
 
-// ------------------------------------------------------------------ a2: NVFP4, blocks along columns
-template <int LAYOUT, int RND, bool ERR>
-__global__ void __launch_bounds__(256) quant_nvfp4_rows_kernel(QuantParams p) {
-  const float g = load_scale(p, 2688.0f);
-  if (isnan(g)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.g_out = g;
-    return;
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.g_out = g;
-  const float six_g = __fmul_rn(6.0f, g);
-  const int64_t hb_row = p.ocp >> 3;                  // half-blocks per output row
-  const int64_t total = p.orp * hb_row;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += stride) {
-    const int64_t hb = base + threadIdx.x;
-    const int64_t r = hb / hb_row, c8 = hb - r * hb_row;
-    const bool valid = hb < total && r < p.out_rows && (c8 << 3) < p.out_cols;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (valid) {
-      uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + r * p.cols + (c8 << 3)));
-      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+// Encode 16 signed values to E4M3 with the tensor scale's inverse.
+template <int RND>
+__device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, const uint32_t (&u)[8]) {
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  if (!(inv < kInf)) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t sign = (__float_as_uint(v[i]) >> 24) & 0x80u;
+      w[i >> 2] |= (sign | (v[i] == 0.0f ? 0u : 0x7eu)) << (8 * (i & 3));
     }
-    U4 rb{0u, 0u, 0u, 0u};
-    if (RND == 1 && valid) rb = sr_words((uint64_t)((r * p.cols + (c8 << 3)) >> 3), p.seed, p.stream_id);
-    uint32_t scale;
-    float err = 0.0f;
-    const uint32_t packed = nvfp4_encode_half<RND, ERR>(w, g, six_g, rb, &scale, &err);
-    if (ERR) err = __fadd_rn(err, __shfl_xor_sync(0xffffffffu, err, 1));
-    if (hb >= total) continue;
-    if (LAYOUT == 0) {
-      if (!valid) continue;
-      *reinterpret_cast<uint32_t*>(p.codes + r * (p.out_cols >> 1) + (c8 << 2)) = packed;
-      if ((c8 & 1) == 0) {
-        p.scales[r * (p.out_cols >> 4) + (c8 >> 1)] = (uint8_t)scale;
-        if (ERR && p.block_err) p.block_err[r * (p.out_cols >> 4) + (c8 >> 1)] = err;
+  } else if (RND == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i >> 1] |= e4m3x2_rn_sat(__fmul_rn(v[2 * i], inv), __fmul_rn(v[2 * i + 1], inv)) << (16 * (i & 1));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t b = __float_as_uint(v[i]);
+      const float y = __fmul_rn(__uint_as_float(b & 0x7fffffffu), inv);
+      w[i >> 2] |= (((b >> 24) & 0x80u) | e4m3_sr(y, uhalf(u, i))) << (8 * (i & 3));
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ------------------------------------------------------------------ a2 / a4: blocks along columns
+// One thread per 16-element block; a warp covers 32 consecutive blocks of one
+// output row.  Rows and blocks past the source tensor (MMA padding) encode as
+// zeros.
+template <int FMT, int LAYOUT, int RND, bool ERR>
+__global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
+  const float g = *p.scale;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = g;
+  if (isnan(g)) return;
+  const float six_g = __fmul_rn(6.0f, g);
+  const float inv8 = __frcp_rn(g);
+  const uint32_t bpr = (uint32_t)(p.ocp >> 4);   // blocks per output row (padded)
+  const uint32_t spr = (bpr + 31) >> 5;          // 32-block segments per row
+  const uint32_t total = (uint32_t)p.orp * spr;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
+  for (uint32_t seg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); seg < total; seg += wstride) {
+    const uint32_t r = seg / spr, kb = (seg - r * spr) * 32 + lane;
+    if (kb >= bpr) continue;
+    const bool real = r < p.out_rows && (int64_t)kb * 16 < p.out_cols;
+    uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+    const int64_t e0 = (int64_t)r * p.cols + (int64_t)kb * 16;
+    if (real) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + e0);
+      a = __ldg(src);
+      b = __ldg(src + 1);
+    }
+    float v[16];
+    unpack16(a, b, v);
+    uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (RND == 1 && real) sr_bits16(e0, p.seed, p.stream_id, u);
+    if (FMT == 1) {
+      const BlockScale bs = nvfp4_block_scale(amax16_bits(a, b), g, six_g);
+      const uint2 c = nvfp4_encode16<RND>(v, bs, u);
+      if (LAYOUT == 0) {
+        if (!real) continue;
+        *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.out_cols >> 1) + (int64_t)kb * 8) = c;
+        p.scales[(int64_t)r * (p.out_cols >> 4) + kb] = (uint8_t)bs.s;
+      } else {
+        *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.ocp >> 1) + (int64_t)kb * 8) = c;
+        p.scales[mma_scale_offset(r, kb, p.ocp)] = (uint8_t)bs.s;
       }
+      if (ERR && real && p.block_err) p.block_err[(int64_t)r * (p.out_cols >> 4) + kb] = nvfp4_block_err(v, c, bs.p);
     } else {
-      *reinterpret_cast<uint32_t*>(p.codes + r * (p.ocp >> 1) + (c8 << 2)) = packed;
-      if ((c8 & 1) == 0) {
-        p.scales[mma_scale_offset(r, c8 >> 1, p.ocp)] = (uint8_t)scale;
-        if (ERR && p.block_err && valid) p.block_err[r * (p.out_cols >> 4) + (c8 >> 1)] = err;
-      }
+      const uint4 c = fp8_encode16<RND>(v, inv8, u);
+      const int64_t pitch = LAYOUT == 0 ? p.out_cols : p.ocp;
+      if (LAYOUT == 0 && !real) continue;
+      *reinterpret_cast<uint4*>(p.codes + (int64_t)r * pitch + (int64_t)kb * 16) = c;
     }
   }
 }
 
-// ------------------------------------------------------------------ a3: NVFP4, blocks along rows (transposed output)
+// ------------------------------------------------------------------ a3 / a4: blocks along rows (transposed output)
 // Tile: 128 source rows (8 blocks of the output contraction) x 64 source
-// columns (64 output rows).
-constexpr int kTR = 128, kTC = 64, kXP = kTC + 8;  // bf16 pitch (halfwords)
+// columns (64 output rows).  Thread (column pair cp, block b) encodes the two
+// blocks of source columns 2cp and 2cp+1, rows 16b..16b+15.
+constexpr int kTR = 128, kTC = 64;
+constexpr int kXW = kTC / 2 + 4;   // words per staged source row (pairs of bf16), padded
 
-template <int LAYOUT, int RND, bool ERR>
-__global__ void __launch_bounds__(256) quant_nvfp4_cols_kernel(QuantParams p) {
-  __shared__ __align__(16) uint16_t xs[kTR][kXP];
-  __shared__ __align__(16) uint16_t rs[RND ? kTR : 1][RND ? kTC : 8];
-  __shared__ __align__(16) uint8_t oc[kTC][kTR / 2 + 16];
-  __shared__ uint8_t os[kTC][8];
+template <int FMT, int LAYOUT, int RND, bool ERR>
+__global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
+  constexpr int OB = FMT == 1 ? kTR / 2 : kTR;   // output bytes per row of the tile
+  constexpr int OW = OB / 4 + 1;                  // staged output row, words (odd: fewer conflicts)
+  __shared__ __align__(16) uint32_t xs[kTR][kXW];
+  __shared__ __align__(16) uint32_t rs[RND ? kTR : 1][RND ? kXW : 4];
+  __shared__ uint32_t oc[kTC][OW];
+  __shared__ uint8_t os[FMT == 1 ? kTC : 1][8];
   __shared__ float oe[ERR ? kTC : 1][8];
-  const float g = load_scale(p, 2688.0f);
-  if (isnan(g)) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.g_out = g;
-    return;
-  }
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.g_out = g;
+  const float g = *p.scale;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = g;
+  if (isnan(g)) return;
   const float six_g = __fmul_rn(6.0f, g);
+  const float inv8 = __frcp_rn(g);
   const int64_t r0 = (int64_t)blockIdx.x * kTR;   // source row = output contraction index
   const int64_t c0 = (int64_t)blockIdx.y * kTC;   // source col = output row
   const int t = threadIdx.x;
-  // load 128 x 64 bf16 (zero outside the source tensor) and the random bits
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int row = (t >> 3) + 32 * j, ch = t & 7;
     const int64_t gr = r0 + row, gc = c0 + ch * 8;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (gr < p.rows && gc < p.cols) v = __ldg(reinterpret_cast<const uint4*>(p.x + gr * p.cols + gc));
-    *reinterpret_cast<uint4*>(&xs[row][ch * 8]) = v;
+    const bool in = gr < p.rows && gc < p.cols;
+    if (in) v = __ldg(reinterpret_cast<const uint4*>(p.x + gr * p.cols + gc));
+    *reinterpret_cast<uint4*>(&xs[row][ch * 4]) = v;
     if (RND == 1) {
-      U4 w = sr_words((uint64_t)((gr * p.cols + gc) >> 3), p.seed, p.stream_id);
-      *reinterpret_cast<uint4*>(&rs[row][ch * 8]) = make_uint4(w.x, w.y, w.z, w.w);
+      U4 w = make_zero_u4();
+      if (in) w = sr_words((uint64_t)(gr * p.cols + gc) >> 3, p.seed, p.stream_id);
+      *reinterpret_cast<uint4*>(&rs[row][ch * 4]) = make_uint4(w.x, w.y, w.z, w.w);
     }
   }
   __syncthreads();
-  // encode: thread -> (output row c, block b); a warp covers 32 consecutive c
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int c = t & 63, b = (t >> 6) + 4 * j;
-    uint32_t mh = 0;
-    uint32_t hv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      hv[i] = xs[b * 16 + i][c];
-      mh = max(mh, hv[i] & 0x7fffu);
-    }
-    const float ab = bf16_bits_to_float(mh);
-    const uint32_t s = e4m3_rn_sat(__fdiv_rn(ab, six_g));
-    const float pq = __fmul_rn(e4m3_decode_pos(s), g);
-    const float inv = __frcp_rn(pq);
-    uint32_t lo = 0, hi = 0;
-    float e = 0.0f;
+  {
+    const int cp = t & 31, b = t >> 5;
+    float v0[16], v1[16];
+    uint32_t m0 = 0, m1 = 0;
+    uint32_t u0[8], u1[8];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float ax = bf16_bits_to_float(hv[i] & 0x7fffu);
-      const float y = __fmul_rn(ax, inv);
-      uint32_t mag;
-      if (RND == 0) mag = e2m1_rn(y);
-      else mag = e2m1_sr(y, rs[b * 16 + i][c]);
-      if (pq == 0.0f || ax == 0.0f) mag = 0u;
-      const uint32_t code = ((hv[i] >> 12) & 8u) | mag;
-      if (i < 8) lo |= code << (4 * i);
-      else hi |= code << (4 * (i - 8));
-      if (ERR) {
-        const float d = __fsub_rn(__fmul_rn(e2m1_value(mag), pq), ax);
-        e = __fadd_rn(e, __fmul_rn(d, d));
+      const uint32_t w = xs[b * 16 + i][cp];
+      v0[i] = __uint_as_float(w << 16);
+      v1[i] = __uint_as_float(w & 0xffff0000u);
+      m0 = max(m0, w & 0x7fffu);
+      m1 = max(m1, (w >> 16) & 0x7fffu);
+      if (RND == 1) {
+        const uint32_t rw = rs[b * 16 + i][cp];
+        if (i & 1) { u0[i >> 1] |= (rw & 0xffffu) << 16; u1[i >> 1] |= rw & 0xffff0000u; }
+        else { u0[i >> 1] = rw & 0xffffu; u1[i >> 1] = rw >> 16; }
       }
     }
-    *reinterpret_cast<uint2*>(&oc[c][b * 8]) = make_uint2(lo, hi);
-    os[c][b] = (uint8_t)s;
-    if (ERR) oe[c][b] = e;
+    if (RND == 0) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) { u0[k] = 0u; u1[k] = 0u; }
+    }
+    if (FMT == 1) {
+      const BlockScale s0 = nvfp4_block_scale(m0, g, six_g), s1 = nvfp4_block_scale(m1, g, six_g);
+      const uint2 e0 = nvfp4_encode16<RND>(v0, s0, u0), e1 = nvfp4_encode16<RND>(v1, s1, u1);
+      oc[2 * cp][2 * b] = e0.x; oc[2 * cp][2 * b + 1] = e0.y;
+      oc[2 * cp + 1][2 * b] = e1.x; oc[2 * cp + 1][2 * b + 1] = e1.y;
+      os[2 * cp][b] = (uint8_t)s0.s;
+      os[2 * cp + 1][b] = (uint8_t)s1.s;
+      if (ERR) {
+        oe[2 * cp][b] = nvfp4_block_err(v0, e0, s0.p);
+        oe[2 * cp + 1][b] = nvfp4_block_err(v1, e1, s1.p);
+      }
+    } else {
+      const uint4 e0 = fp8_encode16<RND>(v0, inv8, u0), e1 = fp8_encode16<RND>(v1, inv8, u1);
+      oc[2 * cp][4 * b] = e0.x; oc[2 * cp][4 * b + 1] = e0.y; oc[2 * cp][4 * b + 2] = e0.z; oc[2 * cp][4 * b + 3] = e0.w;
+      oc[2 * cp + 1][4 * b] = e1.x; oc[2 * cp + 1][4 * b + 1] = e1.y;
+      oc[2 * cp + 1][4 * b + 2] = e1.z; oc[2 * cp + 1][4 * b + 3] = e1.w;
+    }
   }
   __syncthreads();
-  // store codes: 64 output rows x 64 bytes
+  // codes: output rows c0.., contraction r0..r0+127 (OB bytes per row)
+  constexpr int BPB = FMT == 1 ? 8 : 16;   // bytes per 16-element block
   if (LAYOUT == 0) {
-    // row pitch out_cols/2 is only a multiple of 8 bytes: one 8-byte store per block
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int idx = t + 256 * j, row = idx >> 3, b = idx & 7;
+    // row pitch of the row-major layout is only block-aligned: one store per block
+    for (int idx = t; idx < kTC * 8; idx += 256) {
+      const int row = idx >> 3, b = idx & 7;
       const int64_t orow = c0 + row;
-      if (orow < p.out_rows && r0 + 16 * b < p.out_cols)
-        *reinterpret_cast<uint2*>(p.codes + orow * (p.out_cols >> 1) + (r0 >> 1) + 8 * b) =
-            *reinterpret_cast<const uint2*>(&oc[row][8 * b]);
+      if (orow >= p.out_rows || r0 + 16 * b >= p.out_cols) continue;
+      uint8_t* dst = p.codes + orow * (p.out_cols * BPB / 16) + (r0 + 16 * b) * BPB / 16;
+      if (FMT == 1) *reinterpret_cast<uint2*>(dst) = make_uint2(oc[row][2 * b], oc[row][2 * b + 1]);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(oc[row][4 * b], oc[row][4 * b + 1], oc[row][4 * b + 2],
+                                                       oc[row][4 * b + 3]);
     }
   } else {
-    const int row = t >> 2, ch = t & 3;
-    const int64_t orow = c0 + row;
-    if (orow < p.orp)
-      *reinterpret_cast<uint4*>(p.codes + orow * (p.ocp >> 1) + (r0 >> 1) + ch * 16) =
-          *reinterpret_cast<const uint4*>(&oc[row][ch * 16]);
+    constexpr int CH = OB / 16;              // 16-byte chunks per tile row
+    for (int idx = t; idx < kTC * CH; idx += 256) {
+      const int row = idx / CH, ch = idx % CH;
+      const int64_t orow = c0 + row;
+      if (orow >= p.orp) continue;
+      *reinterpret_cast<uint4*>(p.codes + orow * (p.ocp * BPB / 16) + r0 * BPB / 16 + ch * 16) =
+          make_uint4(oc[row][4 * ch], oc[row][4 * ch + 1], oc[row][4 * ch + 2], oc[row][4 * ch + 3]);
+    }
   }
-  if (t < kTC) {
+  if (FMT == 1 && t < kTC) {
     const int64_t orow = c0 + t;
     const int64_t kb0 = r0 >> 4;
     if (LAYOUT == 0) {
-      if (orow < p.out_rows) {
-        for (int b = 0; b < 8 && (kb0 + b) * 16 < p.out_cols; ++b) {
+      if (orow < p.out_rows)
+        for (int b = 0; b < 8 && (kb0 + b) * 16 < p.out_cols; ++b)
           p.scales[orow * (p.out_cols >> 4) + kb0 + b] = os[t][b];
-          if (ERR && p.block_err) p.block_err[orow * (p.out_cols >> 4) + kb0 + b] = oe[t][b];
-        }
-      }
     } else if (orow < p.orp) {
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if ((kb0 + 4 * h) * 16 >= p.ocp) break;
         const uint32_t v = (uint32_t)os[t][4 * h] | ((uint32_t)os[t][4 * h + 1] << 8) |
                            ((uint32_t)os[t][4 * h + 2] << 16) | ((uint32_t)os[t][4 * h + 3] << 24);
         *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(orow, kb0 + 4 * h, p.ocp)) = v;
       }
-      if (ERR && p.block_err && orow < p.out_rows)
-        for (int b = 0; b < 8 && (kb0 + b) * 16 < p.out_cols; ++b)
-          p.block_err[orow * (p.out_cols >> 4) + kb0 + b] = oe[t][b];
     }
-  }
-}
-
-// ------------------------------------------------------------------ a4: FP8 E4M3 with a tensor scale
-template <int RND>
-__device__ __forceinline__ uint32_t fp8_encode(uint32_t h, float inv, uint32_t u16) {
-  const float ax = bf16_bits_to_float(h & 0x7fffu);
-  uint32_t mag;
-  if (RND == 0) mag = e4m3_rn_sat(__fmul_rn(ax, inv));
-  else mag = e4m3_sr(__fmul_rn(ax, inv), u16);
-  if (ax == 0.0f) mag = 0u;
-  return ((h >> 8) & 0x80u) | mag;
-}
-
-template <int LAYOUT, int RND>
-__global__ void __launch_bounds__(256) quant_fp8_rows_kernel(QuantParams p) {
-  const float s = load_scale(p, 448.0f);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.g_out = s;
-  if (isnan(s)) return;
-  const float inv = __frcp_rn(s);
-  const int64_t hb_row = p.ocp >> 3;
-  const int64_t total = p.orp * hb_row;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t hb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; hb < total; hb += stride) {
-    const int64_t r = hb / hb_row, c8 = hb - r * hb_row;
-    const bool valid = r < p.out_rows && (c8 << 3) < p.out_cols;
-    if (LAYOUT == 0 && !valid) continue;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (valid) {
-      uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + r * p.cols + (c8 << 3)));
-      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-    }
-    U4 rb{0u, 0u, 0u, 0u};
-    if (RND == 1 && valid) rb = sr_words((uint64_t)((r * p.cols + (c8 << 3)) >> 3), p.seed, p.stream_id);
-    uint32_t o[2] = {0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t h = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
-      o[i >> 2] |= fp8_encode<RND>(h, inv, RND ? sr_half(rb, i) : 0u) << (8 * (i & 3));
-    }
-    const int64_t pitch = LAYOUT == 0 ? p.out_cols : p.ocp;
-    *reinterpret_cast<uint2*>(p.codes + r * pitch + (c8 << 3)) = make_uint2(o[0], o[1]);
-  }
-}
-
-template <int LAYOUT, int RND>
-__global__ void __launch_bounds__(256) quant_fp8_cols_kernel(QuantParams p) {
-  __shared__ __align__(16) uint16_t xs[kTR][kXP];
-  __shared__ __align__(16) uint16_t rs[RND ? kTR : 1][RND ? kTC : 8];
-  __shared__ __align__(16) uint8_t oc[kTC][kTR + 16];
-  const float s = load_scale(p, 448.0f);
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.g_out = s;
-  if (isnan(s)) return;
-  const float inv = __frcp_rn(s);
-  const int64_t r0 = (int64_t)blockIdx.x * kTR, c0 = (int64_t)blockIdx.y * kTC;
-  const int t = threadIdx.x;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int row = (t >> 3) + 32 * j, ch = t & 7;
-    const int64_t gr = r0 + row, gc = c0 + ch * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (gr < p.rows && gc < p.cols) v = __ldg(reinterpret_cast<const uint4*>(p.x + gr * p.cols + gc));
-    *reinterpret_cast<uint4*>(&xs[row][ch * 8]) = v;
-    if (RND == 1) {
-      U4 w = sr_words((uint64_t)((gr * p.cols + gc) >> 3), p.seed, p.stream_id);
-      *reinterpret_cast<uint4*>(&rs[row][ch * 8]) = make_uint4(w.x, w.y, w.z, w.w);
-    }
-  }
-  __syncthreads();
-  // thread -> (output row c, 16 consecutive contraction elements b*16..b*16+15)
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int c = t & 63, b = (t >> 6) + 4 * j;
-    uint32_t o[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t h = xs[b * 16 + i][c];
-      o[i >> 2] |= fp8_encode<RND>(h, inv, RND ? (uint32_t)rs[b * 16 + i][c] : 0u) << (8 * (i & 3));
-    }
-    *reinterpret_cast<uint4*>(&oc[c][b * 16]) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  __syncthreads();
-  // store: 64 output rows x 128 bytes
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int row = (t >> 3) + 32 * j, ch = t & 7;
-    const int64_t orow = c0 + row;
-    const uint4 v = *reinterpret_cast<const uint4*>(&oc[row][ch * 16]);
-    if (LAYOUT == 0) {
-      if (orow < p.out_rows && r0 + ch * 16 < p.out_cols)
-        *reinterpret_cast<uint4*>(p.codes + orow * p.out_cols + r0 + ch * 16) = v;
-    } else if (orow < p.orp && r0 + ch * 16 < p.ocp) {
-      *reinterpret_cast<uint4*>(p.codes + orow * p.ocp + r0 + ch * 16) = v;
-    }
+    if (ERR && p.block_err && orow < p.out_rows)
+      for (int b = 0; b < 8 && (kb0 + b) * 16 < p.out_cols; ++b)
+        p.block_err[orow * (p.out_cols >> 4) + kb0 + b] = oe[t][b];
   }
 }
 
 // ------------------------------------------------------------------ a8: statistics
-// One pass over the tensor: ||A||^2, the squared errors of NVFP4 and FP8
-// quantization under the tensor's rounding, and the expected SR squared
-// error sum (hi-|y|)(|y|-lo) q^2 on both grids.  Per-thread sums are fp32
-// (each covers a few hundred elements), per-CTA and final sums fp64.
+// One pass: ||A||^2, the squared errors of NVFP4 and FP8 quantization under
+// the tensor's rounding, and the expected SR squared error on both grids,
+// sum (hi-|y|)(|y|-lo) q^2.  For round-to-nearest it is formed from the
+// rounding error d and the grid step h as |d| h - d^2 (equal to it because
+// |d| = min(y-lo, hi-y)); for stochastic rounding from the fraction f of the
+// step, f (1-f) h^2.  Per-thread sums are fp32 (a few hundred elements),
+// per-CTA and final sums fp64.
 template <int RND, bool BLK>
 __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
-  const uint32_t mbits = *p.amax_bits;
-  if (mbits >= 0x7f80u) {
+  const float amax = p.scales3[0], g = p.scales3[1], s8 = p.scales3[2];
+  if (isnan(amax)) {
     if (blockIdx.x == 0 && threadIdx.x == 0)
       for (int k = 0; k < 8; ++k) p.raw_out[k] = __longlong_as_double(0x7ff8000000000000ll);
     return;
   }
-  const float g = tensor_scale_from_bits(mbits, 2688.0f);
-  const float s8 = tensor_scale_from_bits(mbits, 448.0f);
-  const float inv8 = __frcp_rn(s8);
   const float six_g = __fmul_rn(6.0f, g);
-  const int64_t hb_row = p.cols >> 3;
-  const int64_t total = p.rows * hb_row;
-  const int64_t total_w = (total + 31) & ~(int64_t)31;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const float inv8 = __frcp_rn(s8);
+  const bool special8 = !(inv8 < kInf);
+  const uint32_t bpr = (uint32_t)(p.cols >> 4);
+  const uint32_t spr = (bpr + 31) >> 5;
+  const uint32_t total = (uint32_t)p.rows * spr;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
   float sx2 = 0.f, e4 = 0.f, e8 = 0.f, v4 = 0.f, v8 = 0.f;
-  for (int64_t hb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; hb - (threadIdx.x & 31) < total_w;
-       hb += stride) {
-    const bool valid = hb < total;
-    const int64_t r = valid ? hb / hb_row : 0, c8 = valid ? hb - r * hb_row : 0;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    U4 rb{0u, 0u, 0u, 0u};
-    if (valid) {
-      uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + r * p.cols + (c8 << 3)));
-      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-      if (RND == 1) rb = sr_words((uint64_t)((r * p.cols + (c8 << 3)) >> 3), p.seed, p.stream_id);
-    }
-    uint32_t m2 = __vmaxu2(__vmaxu2(w[0] & 0x7fff7fffu, w[1] & 0x7fff7fffu),
-                           __vmaxu2(w[2] & 0x7fff7fffu, w[3] & 0x7fff7fffu));
-    uint32_t mh = max(m2 & 0xffffu, m2 >> 16);
-    mh = max(mh, __shfl_xor_sync(0xffffffffu, mh, 1));
-    const uint32_t sb = e4m3_rn_sat(__fdiv_rn(bf16_bits_to_float(mh), six_g));
-    const float pq = __fmul_rn(e4m3_decode_pos(sb), g);
-    const float inv = __frcp_rn(pq);
-    const float pq2 = __fmul_rn(pq, pq), s82 = __fmul_rn(s8, s8);
-    float be4 = 0.f, be8 = 0.f;
+  for (uint32_t seg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); seg < total; seg += wstride) {
+    const uint32_t r = seg / spr, kb = (seg - r * spr) * 32 + lane;
+    if (kb >= bpr) continue;
+    const int64_t e0 = (int64_t)r * p.cols + (int64_t)kb * 16;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + e0);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    float v[16];
+    unpack16(a, b, v);
+    uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (RND == 1) sr_bits16(e0, p.seed, p.stream_id, u);
+    const BlockScale bs = nvfp4_block_scale(amax16_bits(a, b), g, six_g);
+    float be4 = 0.f, be8 = 0.f, bv4 = 0.f, bv8 = 0.f, bx2 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t h = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
-      const float ax = bf16_bits_to_float(h & 0x7fffu);
-      const uint32_t u = RND ? sr_half(rb, i) : 0u;
-      sx2 = __fadd_rn(sx2, __fmul_rn(ax, ax));
-      // NVFP4
-      const float y = __fmul_rn(ax, inv);
-      uint32_t mag = RND ? e2m1_sr(y, u) : e2m1_rn(y);
-      const bool z4 = (pq == 0.0f || ax == 0.0f);
-      if (z4) mag = 0u;
-      const float d4 = __fsub_rn(__fmul_rn(e2m1_value(mag), pq), ax);
-      be4 = __fadd_rn(be4, __fmul_rn(d4, d4));
-      if (!z4 && y < 6.0f) {
-        const uint32_t lo = (uint32_t)(y >= 0.5f) + (uint32_t)(y >= 1.0f) + (uint32_t)(y >= 1.5f) +
-                            (uint32_t)(y >= 2.0f) + (uint32_t)(y >= 3.0f) + (uint32_t)(y >= 4.0f);
-        const float vl = e2m1_value(lo), vh = e2m1_value(lo + 1u);
-        v4 = __fadd_rn(v4, __fmul_rn(__fmul_rn(__fsub_rn(vh, y), __fsub_rn(y, vl)), pq2));
+    for (int i = 0; i < 16; i += 2) {
+      float d4[2], d8[2], val4[2], val8[2];
+      // ---------------- NVFP4
+      if (bs.special) {
+        val4[0] = (bs.p == 0.0f || v[i] == 0.0f) ? 0.0f : copysignf(6.0f, v[i]);
+        val4[1] = (bs.p == 0.0f || v[i + 1] == 0.0f) ? 0.0f : copysignf(6.0f, v[i + 1]);
+        d4[0] = __fsub_rn(__fmul_rn(val4[0], bs.p), v[i]);
+        d4[1] = __fsub_rn(__fmul_rn(val4[1], bs.p), v[i + 1]);
+      } else if (RND == 0) {
+        const float2 q = e2m1x2_decode(e2m1x2_rn(__fmul_rn(v[i], bs.inv), __fmul_rn(v[i + 1], bs.inv)));
+        val4[0] = q.x; val4[1] = q.y;
+        d4[0] = __fsub_rn(__fmul_rn(q.x, bs.p), v[i]);
+        d4[1] = __fsub_rn(__fmul_rn(q.y, bs.p), v[i + 1]);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float y = __fmul_rn(fabsf(v[i + k]), bs.inv);
+          const float h = y < 2.0f ? 0.5f : (y < 4.0f ? 1.0f : 2.0f);
+          const float ad = fabsf(d4[k]);
+          if (y < 6.0f) bv4 = __fadd_rn(bv4, __fsub_rn(__fmul_rn(ad, __fmul_rn(h, bs.p)), __fmul_rn(ad, ad)));
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float ax = fabsf(v[i + k]);
+          const float y = __fmul_rn(ax, bs.inv);
+          const uint32_t mag = e2m1_sr(y, uhalf(u, i + k));
+          val4[k] = e2m1_value(mag);
+          d4[k] = __fsub_rn(__fmul_rn(val4[k], bs.p), ax);
+          if (y < 6.0f) {
+            // fraction of the step: the 22 bits below E2M1's mantissa bit
+            const uint32_t fb = y >= 1.0f ? (__float_as_uint(y) & 0x3fffffu)
+                                          : ((uint32_t)__fmul_rn(y, 8388608.0f) & 0x3fffffu);
+            const float f = __fmul_rn((float)fb, 2.384185791015625e-07f);   // 2^-22
+            const float h = y < 2.0f ? 0.5f : (y < 4.0f ? 1.0f : 2.0f);
+            bv4 = __fadd_rn(bv4, __fmul_rn(__fmul_rn(f, __fsub_rn(1.0f, f)), __fmul_rn(h, h)));
+          }
+        }
       }
-      // FP8
-      const float y8 = __fmul_rn(ax, inv8);
-      uint32_t c8c = RND ? e4m3_sr(y8, u) : e4m3_rn_sat(y8);
-      if (ax == 0.0f) c8c = 0u;
-      const float d8 = __fsub_rn(__fmul_rn(e4m3_decode_pos(c8c), s8), ax);
-      be8 = __fadd_rn(be8, __fmul_rn(d8, d8));
-      if (ax != 0.0f && y8 < 448.0f) {
-        const uint32_t lo8 = e4m3_sr(y8, 0xffffu);   // threshold never met: truncation code
-        const float vl = e4m3_decode_pos(lo8), vh = e4m3_decode_pos(lo8 + 1u);
-        v8 = __fadd_rn(v8, __fmul_rn(__fmul_rn(__fsub_rn(vh, y8), __fsub_rn(y8, vl)), s82));
+      // ---------------- FP8
+      if (special8) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          val8[k] = v[i + k] == 0.0f ? 0.0f : copysignf(448.0f, v[i + k]);
+          d8[k] = __fsub_rn(__fmul_rn(val8[k], s8), v[i + k]);
+        }
+      } else if (RND == 0) {
+        const float2 q = e4m3x2_decode(e4m3x2_rn_sat(__fmul_rn(v[i], inv8), __fmul_rn(v[i + 1], inv8)));
+        d8[0] = __fsub_rn(__fmul_rn(q.x, s8), v[i]);
+        d8[1] = __fsub_rn(__fmul_rn(q.y, s8), v[i + 1]);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float y = __fmul_rn(fabsf(v[i + k]), inv8);
+          // E4M3 step at y: 2^(E-3) in the normal range, 2^-9 below it
+          const uint32_t hb = max((__float_as_uint(y) & 0x7f800000u) - 0x01800000u, 0x3b000000u);
+          const float ad = fabsf(d8[k]);
+          if (y < 448.0f)
+            bv8 = __fadd_rn(bv8, __fsub_rn(__fmul_rn(ad, __fmul_rn(__uint_as_float(hb), s8)), __fmul_rn(ad, ad)));
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float ax = fabsf(v[i + k]);
+          const float y = __fmul_rn(ax, inv8);
+          const uint32_t c = e4m3_sr(y, uhalf(u, i + k));
+          d8[k] = __fsub_rn(__fmul_rn(e4m3_decode_pos(c), s8), ax);
+          if (y < 448.0f) {
+            const uint32_t yb = __float_as_uint(y);
+            const uint32_t fb = y >= 0.015625f ? (yb & 0xfffffu) : ((uint32_t)__fmul_rn(y, 536870912.0f) & 0xfffffu);
+            const float f = __fmul_rn((float)fb, 9.5367431640625e-07f);   // 2^-20
+            const float h = __uint_as_float(max((yb & 0x7f800000u) - 0x01800000u, 0x3b000000u));
+            bv8 = __fadd_rn(bv8, __fmul_rn(__fmul_rn(f, __fsub_rn(1.0f, f)), __fmul_rn(h, h)));
+          }
+        }
+      }
+      (void)val4; (void)val8;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        bx2 = __fadd_rn(bx2, __fmul_rn(v[i + k], v[i + k]));
+        be4 = __fadd_rn(be4, __fmul_rn(d4[k], d4[k]));
+        be8 = __fadd_rn(be8, __fmul_rn(d8[k], d8[k]));
       }
     }
+    if (RND == 1) {   // fractions were in units of the step: scale by p^2 and s^2
+      bv4 = bs.special ? 0.0f : __fmul_rn(bv4, __fmul_rn(bs.p, bs.p));
+      bv8 = special8 ? 0.0f : __fmul_rn(bv8, __fmul_rn(s8, s8));
+    } else {
+      if (bs.special) bv4 = 0.0f;
+      if (special8) bv8 = 0.0f;
+    }
+    sx2 = __fadd_rn(sx2, bx2);
     e4 = __fadd_rn(e4, be4);
     e8 = __fadd_rn(e8, be8);
+    v4 = __fadd_rn(v4, bv4);
+    v8 = __fadd_rn(v8, bv8);
     if (BLK) {
-      const float b4 = __fadd_rn(be4, __shfl_xor_sync(0xffffffffu, be4, 1));
-      const float b8 = __fadd_rn(be8, __shfl_xor_sync(0xffffffffu, be8, 1));
-      if (valid && (c8 & 1) == 0) {
-        const int64_t bi = r * (p.cols >> 4) + (c8 >> 1);
-        if (p.block_err4) p.block_err4[bi] = b4;
-        if (p.block_err8) p.block_err8[bi] = b8;
-      }
+      const int64_t bi = (int64_t)r * bpr + kb;
+      if (p.block_err4) p.block_err4[bi] = be4;
+      if (p.block_err8) p.block_err8[bi] = be8;
     }
   }
   double acc[5] = {(double)sx2, (double)e4, (double)e8, (double)v4, (double)v8};
@@ -479,7 +522,7 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
   block_sum_f64<5>(tot);
   if (threadIdx.x == 0) {
     for (int k = 0; k < 5; ++k) p.raw_out[k] = tot[k];
-    p.raw_out[5] = (double)bf16_bits_to_float(mbits);
+    p.raw_out[5] = (double)amax;
     p.raw_out[6] = (double)(p.rows * p.cols);
     p.raw_out[7] = 0.0;
     *p.counter = 0;
@@ -494,18 +537,20 @@ static int fill_grid(int64_t work_items, int per_cta, int max_ctas) {
   return (int)g;
 }
 
-cudaError_t launch_amax(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, uint32_t* result_bits,
-                        float* result_float, uint32_t* status, int num_sms, cudaStream_t st) {
-  int grid = fill_grid(n >> 3, 256 * 4, 2 * num_sms);
-  amax_kernel<<<grid, 256, 0, st>>>(x, n, partials, counter, result_bits, result_float, status);
+cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, float* out3,
+                          uint32_t* status, int num_sms, cudaStream_t st) {
+  const int grid = fill_grid(n >> 3, 256 * 4, 4 * num_sms);
+  scales_kernel<<<grid, 256, 0, st>>>(x, n, partials, counter, out3, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_nvfp4(const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
-                               cudaStream_t st) {
+template <int FMT>
+static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
+                             cudaStream_t st) {
   if (orient == 0) {
-    int grid = fill_grid(p.orp * (p.ocp >> 3), 256, 8 * num_sms);
-#define SNIP_L(LY, RN, ER) quant_nvfp4_rows_kernel<LY, RN, ER><<<grid, 256, 0, st>>>(p)
+    const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
+    const int grid = fill_grid(segs, 8, 16 * num_sms);
+#define SNIP_L(LY, RN, ER) quant_rows_kernel<FMT, LY, RN, ER><<<grid, 256, 0, st>>>(p)
     if (layout == 0) {
       if (rnd == 0) { if (err) SNIP_L(0, 0, true); else SNIP_L(0, 0, false); }
       else { if (err) SNIP_L(0, 1, true); else SNIP_L(0, 1, false); }
@@ -516,8 +561,8 @@ cudaError_t launch_quant_nvfp4(const QuantParams& p, int orient, int layout, int
 #undef SNIP_L
   } else {
     // source rows tile the output contraction, source cols the output rows
-    dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
-#define SNIP_L(LY, RN, ER) quant_nvfp4_cols_kernel<LY, RN, ER><<<grid, 256, 0, st>>>(p)
+    const dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
+#define SNIP_L(LY, RN, ER) quant_cols_kernel<FMT, LY, RN, ER><<<grid, 256, 0, st>>>(p)
     if (layout == 0) {
       if (rnd == 0) { if (err) SNIP_L(0, 0, true); else SNIP_L(0, 0, false); }
       else { if (err) SNIP_L(0, 1, true); else SNIP_L(0, 1, false); }
@@ -527,24 +572,18 @@ cudaError_t launch_quant_nvfp4(const QuantParams& p, int orient, int layout, int
     }
 #undef SNIP_L
   }
-  return cudaGetLastError();
 }
 
-cudaError_t launch_quant_fp8(const QuantParams& p, int orient, int layout, int rnd, int num_sms, cudaStream_t st) {
-  if (orient == 0) {
-    int grid = fill_grid(p.orp * (p.ocp >> 3), 256, 8 * num_sms);
-    if (layout == 0) { if (rnd == 0) quant_fp8_rows_kernel<0, 0><<<grid, 256, 0, st>>>(p); else quant_fp8_rows_kernel<0, 1><<<grid, 256, 0, st>>>(p); }
-    else { if (rnd == 0) quant_fp8_rows_kernel<1, 0><<<grid, 256, 0, st>>>(p); else quant_fp8_rows_kernel<1, 1><<<grid, 256, 0, st>>>(p); }
-  } else {
-    dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
-    if (layout == 0) { if (rnd == 0) quant_fp8_cols_kernel<0, 0><<<grid, 256, 0, st>>>(p); else quant_fp8_cols_kernel<0, 1><<<grid, 256, 0, st>>>(p); }
-    else { if (rnd == 0) quant_fp8_cols_kernel<1, 0><<<grid, 256, 0, st>>>(p); else quant_fp8_cols_kernel<1, 1><<<grid, 256, 0, st>>>(p); }
-  }
+cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
+                         cudaStream_t st) {
+  if (fmt == 1) launch_quant_fmt<1>(p, orient, layout, rnd, err, num_sms, st);
+  else launch_quant_fmt<0>(p, orient, layout, rnd, false, num_sms, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_stats(const StatsParams& p, int rnd, int num_sms, cudaStream_t st) {
-  int grid = fill_grid(p.rows * (p.cols >> 3), 256 * 4, 2 * num_sms);
+  const int64_t segs = p.rows * (((p.cols >> 4) + 31) >> 5);
+  const int grid = fill_grid(segs, 8 * 4, 4 * num_sms);
   const bool blk = p.block_err4 || p.block_err8;
   if (rnd == 0) { if (blk) stats_kernel<0, true><<<grid, 256, 0, st>>>(p); else stats_kernel<0, false><<<grid, 256, 0, st>>>(p); }
   else { if (blk) stats_kernel<1, true><<<grid, 256, 0, st>>>(p); else stats_kernel<1, false><<<grid, 256, 0, st>>>(p); }

@@ -11,6 +11,7 @@
 // functions of the input.
 #pragma once
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace snip {
@@ -30,11 +31,18 @@ __device__ __forceinline__ uint32_t e4m3_rn_sat(float t) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(t), "f"(t));
   return r & 0xffu;
 }
-// Two values at once: low byte <- lo, high byte <- hi.
+// Two signed values at once: low byte <- lo, high byte <- hi (sign kept).
 __device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Two E4M3 codes (low byte first) -> their values (exact in f16, then f32).
+__device__ __forceinline__ float2 e4m3x2_decode(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_codes));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
 }
 
 // Value of a non-negative E4M3 code (0..0x7e): 2^(e-7)(1+m/8), or m 2^-9.
@@ -43,47 +51,48 @@ __device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
   return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
 }
 
-// Stochastic rounding of y >= 0 (finite) onto the finite E4M3 grid: lo is y
-// truncated to 3 mantissa bits, frac = (y - lo) / step is exact, go up iff
-// u16 < floor(frac * 2^16); y >= 448 gives 448.  Returns the magnitude code.
+// Stochastic rounding of y >= 0 (finite) onto the finite E4M3 grid with 16
+// random bits: up iff u16 < floor(frac * 2^16), y >= 448 gives 448.
+// Carry form: with the value's 20 dropped mantissa bits (exponent-aligned
+// fixed point below 2^-6), adding (65535 - u16) << 4 carries into the kept
+// bits exactly when u16 < floor(frac * 2^16).  Returns the magnitude code.
 __device__ __forceinline__ uint32_t e4m3_sr(float y, uint32_t u16) {
-  if (y >= 448.0f) return 0x7eu;
-  uint32_t code_lo, thr;
-  if (y >= 0.015625f) {                     // normal range: 2^-6 <= y < 448
-    uint32_t b = __float_as_uint(y);
-    code_lo = ((((b >> 23) & 0xffu) - 120u) << 3) | ((b >> 20) & 7u);
-    thr = (b >> 4) & 0xffffu;               // the 20 dropped mantissa bits, top 16
-  } else {                                  // subnormal range: steps of 2^-9
-    uint32_t t = (uint32_t)__fmul_rn(y, 33554432.0f);   // y * 2^25, exact, < 2^19
-    code_lo = t >> 16;
-    thr = t & 0xffffu;
-  }
-  return code_lo + (u16 < thr ? 1u : 0u);
+  const uint32_t b = __float_as_uint(y);
+  const uint32_t base = y >= 0.015625f ? b - 0x3C000000u                       // (exp-120)<<23 | mantissa
+                                       : (uint32_t)__fmul_rn(y, 536870912.0f);  // y * 2^29, < 2^23
+  const uint32_t code = (base + ((65535u - u16) << 4)) >> 20;
+  return code < 0x7eu ? code : 0x7eu;
 }
 
 // ------------------------------------------------------------------ E2M1
-// Round-to-nearest onto {0, .5, 1, 1.5, 2, 3, 4, 6} with ties to the even
-// code, saturating at 6: count the midpoints below y (a tie counts only when
-// the upper neighbour has the even code).  y >= 0 or NaN (-> 0).
-__device__ __forceinline__ uint32_t e2m1_rn(float y) {
-  return (uint32_t)(y > 0.25f) + (uint32_t)(y >= 0.75f) + (uint32_t)(y > 1.25f) +
-         (uint32_t)(y >= 1.75f) + (uint32_t)(y > 2.5f) + (uint32_t)(y >= 3.5f) +
-         (uint32_t)(y > 5.0f);
+// Round-to-nearest-even of two signed values to E2M1 (saturating at +-6),
+// hardware cvt: returns one byte, lo in bits 0..3 and hi in bits 4..7.
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two E2M1 codes (one byte, low nibble first) -> their values.
+__device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
 }
 
-// Stochastic rounding onto the E2M1 grid with 16 random bits: lo = largest
-// grid value <= y, frac = (y - lo)/(hi - lo) (exact: the step is a power of
-// two), up iff u16 < floor(frac * 2^16); y >= 6 gives 6; NaN gives 0.
+// Stochastic rounding of y >= 0 (finite) onto {0,.5,1,1.5,2,3,4,6} with 16
+// random bits: lo = largest grid value <= y, up iff u16 < floor(frac*2^16)
+// with frac = (y-lo)/(hi-lo); y >= 6 gives 6.  Carry form as in e4m3_sr: the
+// 22 bits below E2M1's one mantissa bit (fixed point 2^-23 below 1) plus
+// (65535 - u16) << 6 carry into the kept bits exactly when the rule rounds
+// up.  Returns the magnitude code 0..7.
 __device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t u16) {
-  if (y >= 6.0f) return 7u;
-  if (!(y > 0.0f)) return 0u;
-  uint32_t idx = (uint32_t)(y >= 0.5f) + (uint32_t)(y >= 1.0f) + (uint32_t)(y >= 1.5f) +
-                 (uint32_t)(y >= 2.0f) + (uint32_t)(y >= 3.0f) + (uint32_t)(y >= 4.0f);
-  float lo = idx <= 4u ? __fmul_rn((float)idx, 0.5f) : (idx == 5u ? 3.0f : 4.0f);
-  float inv_step = idx < 4u ? 2.0f : (idx < 6u ? 1.0f : 0.5f);
-  float frac = __fmul_rn(__fsub_rn(y, lo), inv_step);
-  uint32_t thr = (uint32_t)__fmul_rn(frac, 65536.0f);
-  return idx + (u16 < thr ? 1u : 0u);
+  const uint32_t b = __float_as_uint(y);
+  const uint32_t base = y >= 1.0f ? b - 0x3F000000u                          // 2*(exp-126) | m1, << 22
+                                  : (uint32_t)__fmul_rn(y, 8388608.0f);      // y * 2^23, < 2^23
+  const uint32_t code = (base + ((65535u - u16) << 6)) >> 22;
+  return code < 7u ? code : 7u;
 }
 
 // Value of an E2M1 magnitude code 0..7.

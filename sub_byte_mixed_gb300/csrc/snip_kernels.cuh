@@ -16,11 +16,10 @@ struct QuantParams {
   int64_t out_rows, out_cols;   // output orientation (out_cols = the blocked/contraction dim)
   int64_t orp, ocp;             // padded output dims (== out_rows/out_cols for the row-major layout)
   uint64_t seed, stream_id;
-  const float* g_in;            // tensor scale given by the caller, or null
-  const uint32_t* amax_bits;    // published amax word (bf16 magnitude bits) when g_in is null
+  const float* scale;           // device fp32 tensor scale to use (NVFP4 g or FP8 s)
   uint8_t* codes;
   uint8_t* scales;              // NVFP4 only
-  float* g_out;
+  float* g_out;                 // nullable: receives *scale
   float* block_err;             // NVFP4 only, nullable
 };
 
@@ -28,7 +27,7 @@ struct StatsParams {
   const uint16_t* x;
   int64_t rows, cols;
   uint64_t seed, stream_id;
-  const uint32_t* amax_bits;
+  const float* scales3;         // {amax, NVFP4 g, FP8 s}
   double* partials;             // 5 doubles per CTA
   uint32_t* counter;
   double* raw_out;              // SNIP_STATS_NVALS doubles
@@ -96,11 +95,10 @@ __device__ __forceinline__ void block_sum_f64(double (&v)[N]) {
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_amax(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, uint32_t* result_bits,
-                        float* result_float, uint32_t* status, int num_sms, cudaStream_t st);
-cudaError_t launch_quant_nvfp4(const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
-                               cudaStream_t st);
-cudaError_t launch_quant_fp8(const QuantParams& p, int orient, int layout, int rnd, int num_sms, cudaStream_t st);
+cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, float* out3,
+                          uint32_t* status, int num_sms, cudaStream_t st);
+cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
+                         cudaStream_t st);
 cudaError_t launch_stats(const StatsParams& p, int rnd, int num_sms, cudaStream_t st);
 
 // GEMM: D = ga*gb*A B^T on MMA-layout operands.  fmt 1 = NVFP4, 0 = FP8.
@@ -111,5 +109,7 @@ cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, 
 
 // Upper bound on the number of amax / stats partial slots any launch uses.
 constexpr int kMaxPartials = 1024;
+
+__device__ __forceinline__ U4 make_zero_u4() { return U4{0u, 0u, 0u, 0u}; }
 
 }  // namespace snip

@@ -29,7 +29,7 @@ STATS_NVALS = 8
 # every symbol include/snip.h declares
 EXPORTS = (
     "snip_status_string", "snip_version", "snip_device_check", "snip_workspace_init", "snip_workspace_status",
-    "snip_quantize_workspace_size", "snip_amax", "snip_quantize_nvfp4", "snip_quantize_fp8",
+    "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_quantize_nvfp4", "snip_quantize_fp8",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
     "snip_quant_stats", "snip_stats_finalize",
@@ -69,6 +69,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_workspace_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_int)]),
         "snip_quantize_workspace_size": (sz, [i64, i64]),
         "snip_amax": (i32, [vp, i64, vp, vp, sz, vp]),
+        "snip_tensor_scales": (i32, [vp, i64, vp, vp, sz, vp]),
         "snip_quantize_nvfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_fp8": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, sz, vp]),
         "snip_quantized_bytes": (i32, [i32, i32, i64, i64, szp, szp]),
@@ -80,7 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_qlinear_workspace_size": (sz, [vp, i32, i64, i64, i64]),
         "snip_qlinear_fwd": (i32, [vp, i32, vp, vp, i64, i64, i64, vp, vp, sz, vp]),
         "snip_qlinear_bwd": (i32, [vp, i32, vp, vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]),
-        "snip_quant_stats": (i32, [vp, i64, i64, i32, u64, u64, vp, vp, vp, vp, sz, vp]),
+        "snip_quant_stats": (i32, [vp, i64, i64, i32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "snip_stats_finalize": (i32, [vp, ctypes.POINTER(SnipStats)]),
     }
     for name, (res, args) in sig.items():
@@ -129,6 +130,10 @@ def snip_amax(x, n, amax_out, ws, ws_bytes, stream):
     _call("snip_amax", x, n, amax_out, ws, ws_bytes, stream)
 
 
+def snip_tensor_scales(x, n, scales_out, ws, ws_bytes, stream):
+    _call("snip_tensor_scales", x, n, scales_out, ws, ws_bytes, stream)
+
+
 def snip_quantize_nvfp4(x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
                         block_sqerr, ws, ws_bytes, stream):
     _call("snip_quantize_nvfp4", x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
@@ -162,10 +167,10 @@ def snip_qlinear_bwd(plan, layer, X, W, dY, T, K, N, dX, dW, ws, ws_bytes, strea
     _call("snip_qlinear_bwd", plan, layer, X, W, dY, T, K, N, dX, dW, ws, ws_bytes, stream)
 
 
-def snip_quant_stats(a, rows, cols, rnd, seed, stream_id, raw_out, block_err_nvfp4, block_err_fp8, ws, ws_bytes,
-                     stream):
-    _call("snip_quant_stats", a, rows, cols, rnd, seed, stream_id, raw_out, block_err_nvfp4, block_err_fp8, ws,
-          ws_bytes, stream)
+def snip_quant_stats(a, rows, cols, rnd, seed, stream_id, scales_in, raw_out, block_err_nvfp4, block_err_fp8, ws,
+                     ws_bytes, stream):
+    _call("snip_quant_stats", a, rows, cols, rnd, seed, stream_id, scales_in, raw_out, block_err_nvfp4,
+          block_err_fp8, ws, ws_bytes, stream)
 
 
 def snip_stats_finalize(raw_host) -> SnipStats:
@@ -264,6 +269,15 @@ class QuantFP8:
     layout: int
 
 
+def tensor_scales(x, ws: Workspace | None = None, out=None):
+    """Device float tensor (3,) = {amax, NVFP4 g, FP8 s} of a bf16 tensor."""
+    torch = _torch()
+    ws = ws or small_workspace()
+    out = out if out is not None else torch.empty(3, dtype=torch.float32, device=x.device)
+    snip_tensor_scales(x.data_ptr(), x.numel(), out.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return out
+
+
 def amax(x, ws: Workspace | None = None):
     torch = _torch()
     ws = ws or small_workspace()
@@ -342,7 +356,8 @@ def qlinear_bwd(plan: Plan, layer: int, X, W, dY, ws: Workspace, dX=None, dW=Non
     return dX, dW
 
 
-def quant_stats(a, rnd=RTN, seed=0, stream_id=0, want_block_err=False, ws: Workspace | None = None, raw=None):
+def quant_stats(a, rnd=RTN, seed=0, stream_id=0, want_block_err=False, ws: Workspace | None = None, raw=None,
+                scales=None):
     """Launch the statistics pass; returns (raw device tensor, block errors or None)."""
     torch = _torch()
     ws = ws or small_workspace()
@@ -352,6 +367,6 @@ def quant_stats(a, rnd=RTN, seed=0, stream_id=0, want_block_err=False, ws: Works
     if want_block_err:
         b4 = torch.empty((rows, cols // 16), dtype=torch.float32, device=a.device)
         b8 = torch.empty((rows, cols // 16), dtype=torch.float32, device=a.device)
-    snip_quant_stats(a.data_ptr(), rows, cols, rnd, seed, stream_id, raw.data_ptr(), _ptr(b4), _ptr(b8), ws.ptr,
-                     ws.nbytes, _stream())
+    snip_quant_stats(a.data_ptr(), rows, cols, rnd, seed, stream_id, _ptr(scales), raw.data_ptr(), _ptr(b4), _ptr(b8),
+                     ws.ptr, ws.nbytes, _stream())
     return raw, (b4, b8)

@@ -32,6 +32,29 @@ def test_amax_exact(snip, shape):
     assert got == ref
 
 
+@pytest.mark.parametrize("shape", [(64, 128), (1040, 784), (0, 16)])
+def test_tensor_scales(snip, shape):
+    x = _x(shape, tid=6)
+    sc = snip.tensor_scales(x.cuda()).cpu().numpy()
+    m = float(x.float().abs().max()) if x.numel() else 0.0
+    assert sc[0] == m
+    assert sc[1] == oracle.nvfp4_global_scale(m) and sc[2] == oracle.fp8_tensor_scale(m)
+
+
+def test_precomputed_scales_match(snip):
+    """Quantizing with g_in from snip_tensor_scales gives the same bits as
+    letting the call compute the scale itself."""
+    x = _x((272, 400), seed=9, tid=2).cuda()
+    sc = snip.tensor_scales(x)
+    for rnd in (0, 1):
+        a = snip.quantize_nvfp4(x, rnd=rnd, seed=2, layout=snip.MMA)
+        b = snip.quantize_nvfp4(x, rnd=rnd, seed=2, layout=snip.MMA, g_in=sc[1:2])
+        assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales) and torch.equal(a.g, b.g)
+        f = snip.quantize_fp8(x, orient=1, rnd=rnd, seed=2)
+        h = snip.quantize_fp8(x, orient=1, rnd=rnd, seed=2, s_in=sc[2:3])
+        assert torch.equal(f.codes, h.codes)
+
+
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("orient", [0, 1])
 @pytest.mark.parametrize("rnd", [0, 1])

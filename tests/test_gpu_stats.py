@@ -19,8 +19,10 @@ def snip():
     return need_gpu()
 
 
-def _check(snip, x, rnd, seed=0, sid=0, blocks=True):
-    raw, (b4, b8) = snip.quant_stats(x.cuda(), rnd=rnd, seed=seed, stream_id=sid, want_block_err=blocks)
+def _check(snip, x, rnd, seed=0, sid=0, blocks=True, precomputed=False):
+    xd = x.cuda()
+    sc = snip.tensor_scales(xd) if precomputed else None
+    raw, (b4, b8) = snip.quant_stats(xd, rnd=rnd, seed=seed, stream_id=sid, want_block_err=blocks, scales=sc)
     got = raw.cpu().numpy()
     ref = oracle.quant_stats(x, rnd=rnd, seed=seed, stream_id=sid, want_block_err=blocks)
     r = ref["raw"]
@@ -40,6 +42,7 @@ def _check(snip, x, rnd, seed=0, sid=0, blocks=True):
 @pytest.mark.parametrize("rnd", [0, 1])
 def test_stats_normal(snip, shape, rnd):
     _check(snip, inputs.normal_bf16(shape, 1e-3, 3, 7), rnd, seed=2, sid=18)
+    _check(snip, inputs.normal_bf16(shape, 1.0, 3, 8), rnd, seed=2, sid=18, precomputed=True)
 
 
 def test_stats_outliers(snip):
