@@ -74,6 +74,14 @@ __global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restri
   }
 }
 
+// Bit pattern of the E4M3 grid step at y >= 0: 2^(E-3) for y in the normal
+// range (E = floor(log2 y)), 2^-9 below it (signed max: zero and tiny y have
+// exponent fields below 3).
+__device__ __forceinline__ uint32_t e4m3_step_bits(float y) {
+  const int32_t e = (int32_t)(__float_as_uint(y) & 0x7f800000u) - 0x01800000;
+  return (uint32_t)max(e, 0x3b000000);
+}
+
 // Byte offset of the E4M3 scale of (row r, block kb) in the MMA layout.
 __device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64_t ocp) {
   const int64_t chunk = (r >> 7) * (ocp >> 6) + (kb >> 2);
@@ -458,7 +466,7 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
         for (int k = 0; k < 2; ++k) {
           const float y = __fmul_rn(fabsf(v[i + k]), inv8);
           // E4M3 step at y: 2^(E-3) in the normal range, 2^-9 below it
-          const uint32_t hb = max((__float_as_uint(y) & 0x7f800000u) - 0x01800000u, 0x3b000000u);
+          const uint32_t hb = e4m3_step_bits(y);
           const float ad = fabsf(d8[k]);
           if (y < 448.0f)
             bv8 = __fadd_rn(bv8, __fsub_rn(__fmul_rn(ad, __fmul_rn(__uint_as_float(hb), s8)), __fmul_rn(ad, ad)));
@@ -474,7 +482,7 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
             const uint32_t yb = __float_as_uint(y);
             const uint32_t fb = y >= 0.015625f ? (yb & 0xfffffu) : ((uint32_t)__fmul_rn(y, 536870912.0f) & 0xfffffu);
             const float f = __fmul_rn((float)fb, 9.5367431640625e-07f);   // 2^-20
-            const float h = __uint_as_float(max((yb & 0x7f800000u) - 0x01800000u, 0x3b000000u));
+            const float h = __uint_as_float(e4m3_step_bits(y));
             bv8 = __fadd_rn(bv8, __fmul_rn(__fmul_rn(f, __fsub_rn(1.0f, f)), __fmul_rn(h, h)));
           }
         }
