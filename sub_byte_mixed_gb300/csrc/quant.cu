@@ -380,9 +380,18 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
 // the tensor's rounding, and the expected SR squared error on both grids,
 // sum (hi-|y|)(|y|-lo) q^2.  For round-to-nearest it is formed from the
 // rounding error d and the grid step h as |d| h - d^2 (equal to it because
-// |d| = min(y-lo, hi-y)); for stochastic rounding from the fraction f of the
-// step, f (1-f) h^2.  Per-thread sums are fp32 (a few hundred elements),
-// per-CTA and final sums fp64.
+// |d| = min(y-lo, hi-y)), accumulated per block as p*sum(|d| h) - sum(d^2)
+// over the unsaturated elements; for stochastic rounding from the fraction f
+// of the step, f (1-f) h^2, times p^2 per block.  The sums need no bit
+// exactness, so they use fused multiply-adds; per-thread sums are fp32 (a few
+// hundred elements), per-CTA and final sums fp64.
+
+// Bit pattern of the E2M1 grid step at y >= 0: 0.5 below 2, then 2^(E-1).
+__device__ __forceinline__ uint32_t e2m1_step_bits(float y) {
+  const int32_t e = (int32_t)(__float_as_uint(y) & 0x7f800000u) - 0x00800000;
+  return (uint32_t)max(e, 0x3f000000);
+}
+
 template <int RND, bool BLK>
 __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
   const float amax = p.scales3[0], g = p.scales3[1], s8 = p.scales3[2];
@@ -411,102 +420,87 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     if (RND == 1) sr_bits16(e0, p.seed, p.stream_id, u);
     const BlockScale bs = nvfp4_block_scale(amax16_bits(a, b), g, six_g);
-    float be4 = 0.f, be8 = 0.f, bv4 = 0.f, bv8 = 0.f, bx2 = 0.f;
+    float bx2 = 0.f, be4 = 0.f, be8 = 0.f, A4 = 0.f, B4 = 0.f, A8 = 0.f, B8 = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-      float d4[2], d8[2], val4[2], val8[2];
+      bx2 = fmaf(v[i], v[i], fmaf(v[i + 1], v[i + 1], bx2));
       // ---------------- NVFP4
       if (bs.special) {
-        val4[0] = (bs.p == 0.0f || v[i] == 0.0f) ? 0.0f : copysignf(6.0f, v[i]);
-        val4[1] = (bs.p == 0.0f || v[i + 1] == 0.0f) ? 0.0f : copysignf(6.0f, v[i + 1]);
-        d4[0] = __fsub_rn(__fmul_rn(val4[0], bs.p), v[i]);
-        d4[1] = __fsub_rn(__fmul_rn(val4[1], bs.p), v[i + 1]);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float q = (bs.p == 0.0f || v[i + k] == 0.0f) ? 0.0f : copysignf(6.0f, v[i + k]);
+          const float d = fmaf(q, bs.p, -v[i + k]);
+          be4 = fmaf(d, d, be4);
+        }
       } else if (RND == 0) {
-        const float2 q = e2m1x2_decode(e2m1x2_rn(__fmul_rn(v[i], bs.inv), __fmul_rn(v[i + 1], bs.inv)));
-        val4[0] = q.x; val4[1] = q.y;
-        d4[0] = __fsub_rn(__fmul_rn(q.x, bs.p), v[i]);
-        d4[1] = __fsub_rn(__fmul_rn(q.y, bs.p), v[i + 1]);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float y = __fmul_rn(fabsf(v[i + k]), bs.inv);
-          const float h = y < 2.0f ? 0.5f : (y < 4.0f ? 1.0f : 2.0f);
-          const float ad = fabsf(d4[k]);
-          if (y < 6.0f) bv4 = __fadd_rn(bv4, __fsub_rn(__fmul_rn(ad, __fmul_rn(h, bs.p)), __fmul_rn(ad, ad)));
-        }
+        const float y0 = __fmul_rn(v[i], bs.inv), y1 = __fmul_rn(v[i + 1], bs.inv);
+        const float2 q = e2m1x2_decode(e2m1x2_rn(y0, y1));
+        const float d0 = fmaf(q.x, bs.p, -v[i]), d1 = fmaf(q.y, bs.p, -v[i + 1]);
+        be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
+        const float m0 = fabsf(y0) < 6.0f ? d0 : 0.0f, m1 = fabsf(y1) < 6.0f ? d1 : 0.0f;
+        A4 = fmaf(fabsf(m0), __uint_as_float(e2m1_step_bits(fabsf(y0))), A4);
+        A4 = fmaf(fabsf(m1), __uint_as_float(e2m1_step_bits(fabsf(y1))), A4);
+        B4 = fmaf(m0, m0, fmaf(m1, m1, B4));
       } else {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float ax = fabsf(v[i + k]);
-          const float y = __fmul_rn(ax, bs.inv);
-          const uint32_t mag = e2m1_sr(y, uhalf(u, i + k));
-          val4[k] = e2m1_value(mag);
-          d4[k] = __fsub_rn(__fmul_rn(val4[k], bs.p), ax);
-          if (y < 6.0f) {
-            // fraction of the step: the 22 bits below E2M1's mantissa bit
-            const uint32_t fb = y >= 1.0f ? (__float_as_uint(y) & 0x3fffffu)
-                                          : ((uint32_t)__fmul_rn(y, 8388608.0f) & 0x3fffffu);
-            const float f = __fmul_rn((float)fb, 2.384185791015625e-07f);   // 2^-22
-            const float h = y < 2.0f ? 0.5f : (y < 4.0f ? 1.0f : 2.0f);
-            bv4 = __fadd_rn(bv4, __fmul_rn(__fmul_rn(f, __fsub_rn(1.0f, f)), __fmul_rn(h, h)));
-          }
-        }
+        const float y0 = __fmul_rn(fabsf(v[i]), bs.inv), y1 = __fmul_rn(fabsf(v[i + 1]), bs.inv);
+        const uint32_t b0 = e2m1_sr_base(y0), b1 = e2m1_sr_base(y1);
+        const uint32_t c0 = e2m1_sr_from_base(b0, uhalf(u, i)), c1 = e2m1_sr_from_base(b1, uhalf(u, i + 1));
+        const float2 q = e2m1x2_decode(c0 | (c1 << 4));
+        const float d0 = fmaf(q.x, bs.p, -fabsf(v[i])), d1 = fmaf(q.y, bs.p, -fabsf(v[i + 1]));
+        be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
+        // f (1-f) h^2 with f the 22 bits below E2M1's mantissa bit
+        const float f0 = __fmul_rn((float)(b0 & 0x3fffffu), 2.384185791015625e-07f);
+        const float f1 = __fmul_rn((float)(b1 & 0x3fffffu), 2.384185791015625e-07f);
+        const float h0 = __uint_as_float(e2m1_step_bits(y0)), h1 = __uint_as_float(e2m1_step_bits(y1));
+        const float w0 = y0 < 6.0f ? fmaf(-f0, f0, f0) * (h0 * h0) : 0.0f;
+        const float w1 = y1 < 6.0f ? fmaf(-f1, f1, f1) * (h1 * h1) : 0.0f;
+        A4 += w0 + w1;
       }
       // ---------------- FP8
       if (special8) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          val8[k] = v[i + k] == 0.0f ? 0.0f : copysignf(448.0f, v[i + k]);
-          d8[k] = __fsub_rn(__fmul_rn(val8[k], s8), v[i + k]);
+          const float q = v[i + k] == 0.0f ? 0.0f : copysignf(448.0f, v[i + k]);
+          const float d = fmaf(q, s8, -v[i + k]);
+          be8 = fmaf(d, d, be8);
         }
       } else if (RND == 0) {
-        const float2 q = e4m3x2_decode(e4m3x2_rn_sat(__fmul_rn(v[i], inv8), __fmul_rn(v[i + 1], inv8)));
-        d8[0] = __fsub_rn(__fmul_rn(q.x, s8), v[i]);
-        d8[1] = __fsub_rn(__fmul_rn(q.y, s8), v[i + 1]);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float y = __fmul_rn(fabsf(v[i + k]), inv8);
-          // E4M3 step at y: 2^(E-3) in the normal range, 2^-9 below it
-          const uint32_t hb = e4m3_step_bits(y);
-          const float ad = fabsf(d8[k]);
-          if (y < 448.0f)
-            bv8 = __fadd_rn(bv8, __fsub_rn(__fmul_rn(ad, __fmul_rn(__uint_as_float(hb), s8)), __fmul_rn(ad, ad)));
-        }
+        const float y0 = __fmul_rn(v[i], inv8), y1 = __fmul_rn(v[i + 1], inv8);
+        const float2 q = e4m3x2_decode(e4m3x2_rn_sat(y0, y1));
+        const float d0 = fmaf(q.x, s8, -v[i]), d1 = fmaf(q.y, s8, -v[i + 1]);
+        be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
+        const float m0 = fabsf(y0) < 448.0f ? d0 : 0.0f, m1 = fabsf(y1) < 448.0f ? d1 : 0.0f;
+        A8 = fmaf(fabsf(m0), __uint_as_float(e4m3_step_bits(fabsf(y0))), A8);
+        A8 = fmaf(fabsf(m1), __uint_as_float(e4m3_step_bits(fabsf(y1))), A8);
+        B8 = fmaf(m0, m0, fmaf(m1, m1, B8));
       } else {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float ax = fabsf(v[i + k]);
-          const float y = __fmul_rn(ax, inv8);
-          const uint32_t c = e4m3_sr(y, uhalf(u, i + k));
-          d8[k] = __fsub_rn(__fmul_rn(e4m3_decode_pos(c), s8), ax);
-          if (y < 448.0f) {
-            const uint32_t yb = __float_as_uint(y);
-            const uint32_t fb = y >= 0.015625f ? (yb & 0xfffffu) : ((uint32_t)__fmul_rn(y, 536870912.0f) & 0xfffffu);
-            const float f = __fmul_rn((float)fb, 9.5367431640625e-07f);   // 2^-20
-            const float h = __uint_as_float(e4m3_step_bits(y));
-            bv8 = __fadd_rn(bv8, __fmul_rn(__fmul_rn(f, __fsub_rn(1.0f, f)), __fmul_rn(h, h)));
-          }
-        }
-      }
-      (void)val4; (void)val8;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        bx2 = __fadd_rn(bx2, __fmul_rn(v[i + k], v[i + k]));
-        be4 = __fadd_rn(be4, __fmul_rn(d4[k], d4[k]));
-        be8 = __fadd_rn(be8, __fmul_rn(d8[k], d8[k]));
+        const float y0 = __fmul_rn(fabsf(v[i]), inv8), y1 = __fmul_rn(fabsf(v[i + 1]), inv8);
+        const uint32_t b0 = e4m3_sr_base(y0), b1 = e4m3_sr_base(y1);
+        const uint32_t c0 = e4m3_sr_from_base(b0, uhalf(u, i)), c1 = e4m3_sr_from_base(b1, uhalf(u, i + 1));
+        const float2 q = e4m3x2_decode(c0 | (c1 << 8));
+        const float d0 = fmaf(q.x, s8, -fabsf(v[i])), d1 = fmaf(q.y, s8, -fabsf(v[i + 1]));
+        be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
+        const float f0 = __fmul_rn((float)(b0 & 0xfffffu), 9.5367431640625e-07f);   // 2^-20
+        const float f1 = __fmul_rn((float)(b1 & 0xfffffu), 9.5367431640625e-07f);
+        const float h0 = __uint_as_float(e4m3_step_bits(y0)), h1 = __uint_as_float(e4m3_step_bits(y1));
+        const float w0 = y0 < 448.0f ? fmaf(-f0, f0, f0) * (h0 * h0) : 0.0f;
+        const float w1 = y1 < 448.0f ? fmaf(-f1, f1, f1) * (h1 * h1) : 0.0f;
+        A8 += w0 + w1;
       }
     }
+    float bv4, bv8;
     if (RND == 1) {   // fractions were in units of the step: scale by p^2 and s^2
-      bv4 = bs.special ? 0.0f : __fmul_rn(bv4, __fmul_rn(bs.p, bs.p));
-      bv8 = special8 ? 0.0f : __fmul_rn(bv8, __fmul_rn(s8, s8));
-    } else {
-      if (bs.special) bv4 = 0.0f;
-      if (special8) bv8 = 0.0f;
+      bv4 = bs.special ? 0.0f : A4 * (bs.p * bs.p);
+      bv8 = special8 ? 0.0f : A8 * (s8 * s8);
+    } else {          // p * sum(|d| h) - sum(d^2) over unsaturated elements
+      bv4 = bs.special ? 0.0f : fmaf(bs.p, A4, -B4);
+      bv8 = special8 ? 0.0f : fmaf(s8, A8, -B8);
     }
-    sx2 = __fadd_rn(sx2, bx2);
-    e4 = __fadd_rn(e4, be4);
-    e8 = __fadd_rn(e8, be8);
-    v4 = __fadd_rn(v4, bv4);
-    v8 = __fadd_rn(v8, bv8);
+    sx2 += bx2;
+    e4 += be4;
+    e8 += be8;
+    v4 += bv4;
+    v8 += bv8;
     if (BLK) {
       const int64_t bi = (int64_t)r * bpr + kb;
       if (p.block_err4) p.block_err4[bi] = be4;

@@ -56,13 +56,15 @@ __device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
 // Carry form: with the value's 20 dropped mantissa bits (exponent-aligned
 // fixed point below 2^-6), adding (65535 - u16) << 4 carries into the kept
 // bits exactly when u16 < floor(frac * 2^16).  Returns the magnitude code.
-__device__ __forceinline__ uint32_t e4m3_sr(float y, uint32_t u16) {
-  const uint32_t b = __float_as_uint(y);
-  const uint32_t base = y >= 0.015625f ? b - 0x3C000000u                       // (exp-120)<<23 | mantissa
-                                       : (uint32_t)__fmul_rn(y, 536870912.0f);  // y * 2^29, < 2^23
+__device__ __forceinline__ uint32_t e4m3_sr_base(float y) {
+  return y >= 0.015625f ? __float_as_uint(y) - 0x3C000000u                 // (exp-120)<<23 | mantissa
+                        : (uint32_t)__fmul_rn(y, 536870912.0f);           // y * 2^29, < 2^23
+}
+__device__ __forceinline__ uint32_t e4m3_sr_from_base(uint32_t base, uint32_t u16) {
   const uint32_t code = (base + ((65535u - u16) << 4)) >> 20;
   return code < 0x7eu ? code : 0x7eu;
 }
+__device__ __forceinline__ uint32_t e4m3_sr(float y, uint32_t u16) { return e4m3_sr_from_base(e4m3_sr_base(y), u16); }
 
 // ------------------------------------------------------------------ E2M1
 // Round-to-nearest-even of two signed values to E2M1 (saturating at +-6),
@@ -87,13 +89,15 @@ __device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
 // 22 bits below E2M1's one mantissa bit (fixed point 2^-23 below 1) plus
 // (65535 - u16) << 6 carry into the kept bits exactly when the rule rounds
 // up.  Returns the magnitude code 0..7.
-__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t u16) {
-  const uint32_t b = __float_as_uint(y);
-  const uint32_t base = y >= 1.0f ? b - 0x3F000000u                          // 2*(exp-126) | m1, << 22
-                                  : (uint32_t)__fmul_rn(y, 8388608.0f);      // y * 2^23, < 2^23
+__device__ __forceinline__ uint32_t e2m1_sr_base(float y) {
+  return y >= 1.0f ? __float_as_uint(y) - 0x3F000000u                     // 2*(exp-126) | m1, << 22
+                   : (uint32_t)__fmul_rn(y, 8388608.0f);                  // y * 2^23, < 2^23
+}
+__device__ __forceinline__ uint32_t e2m1_sr_from_base(uint32_t base, uint32_t u16) {
   const uint32_t code = (base + ((65535u - u16) << 6)) >> 22;
   return code < 7u ? code : 7u;
 }
+__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t u16) { return e2m1_sr_from_base(e2m1_sr_base(y), u16); }
 
 // Value of an E2M1 magnitude code 0..7.
 __device__ __forceinline__ float e2m1_value(uint32_t m) {
