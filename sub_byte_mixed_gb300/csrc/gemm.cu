@@ -9,15 +9,21 @@
 // elements of each operand row); FP8 E4M3 operands on kind::f8f6f4.  The fp32
 // tensor scales multiply the fp32 accumulator in the epilogue.
 //
-// Structure (one CTA per SM, persistent over output tiles, 10 warps):
-//   warp 0     TMA producer: 128B-swizzled code tiles via cp.async.bulk.tensor,
-//              block-scale chunks via cp.async.bulk, into a STAGES-deep ring;
-//   warp 1     allocates tensor memory and issues tcgen05.cp (scales smem ->
-//              TMEM) and tcgen05.mma (accumulator in TMEM) from one thread;
-//   warps 2-9  epilogue: each warp drains 32 accumulator rows x BN/2 columns
-//              from TMEM into registers with back-to-back tcgen05.ld, hands
-//              the accumulator back to the MMA warp at once, then scales by
-//              ga*gb and stores fp32 rows while the next tile's MMAs run.
+// Structure (one CTA per SM, persistent over output tiles, 14 warps):
+//   warp 0      TMA producer: 128B-swizzled code tiles via cp.async.bulk.tensor,
+//               block-scale chunks via cp.async.bulk, into a STAGES-deep ring;
+//   warp 1      allocates tensor memory and issues tcgen05.mma (accumulator in
+//               TMEM) from one thread;
+//   warps 2-5   NVFP4 only: stage each ring slot's block scales into tensor
+//               memory through registers (ld.shared + tcgen05.st), one warp per
+//               32-lane quadrant, writing the 32-lane x 4-column image that a
+//               32x128b.warpx4 copy would make.  tcgen05.cp from the MMA thread
+//               costs ~60 tensor-pipe cycles per copy, serialised with the
+//               MMAs; the register path runs beside them;
+//   warps 6-13  epilogue: each warp drains 32 accumulator rows x BN/2 columns
+//               from TMEM into registers (two rounds), hands the accumulator
+//               back to the MMA warp, then scales by ga*gb and stores fp32
+//               rows while the next tile's MMAs run.
 // Every wait is bounded (globaltimer); on expiry the CTA raises the timeout
 // bit of the status word, lets all roles fall through, drains in-flight
 // tensor-core work and frees its tensor memory before returning.
@@ -46,11 +52,14 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = 512;
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_STAGES + 1;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+  static constexpr int SF_WARPS = 4;               // scale staging, one per TMEM lane quadrant
+  static constexpr int EPI_WARP0 = 2 + SF_WARPS;
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_COLS = BN / 2;          // accumulator columns drained by one epilogue warp
-  static constexpr int THREADS = 32 * (2 + EPI_WARPS);
+  static constexpr int EPI_ROUND = 64;             // columns per drain round (register budget)
+  static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   // Instruction descriptor.  Block-scaled FP4: A/B type E2M1 (1) in bits 7-9
   // and 10-12, K-major, N>>3 in bits 17-22, scale type UE4M3 (0) in bit 23,
   // M>>4 in bits 24-28.  FP8: D type f32 (1) in bits 4-5, A/B type E4M3 (0).
@@ -60,7 +69,7 @@ struct GemmCfg {
 };
 
 template <int FMT, int BN>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   using C = GemmCfg<FMT, BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -72,6 +81,7 @@ __global__ void __launch_bounds__(320, 1)
   auto tfull = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::ACC_STAGES + a); };
   const uint32_t drain = bar0 + 8u * (2 * C::STAGES + 2 * C::ACC_STAGES);
+  auto sfready = [&](int s) { return bar0 + 8u * (2 * C::STAGES + 2 * C::ACC_STAGES + 1 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -80,6 +90,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int s = 0; s < C::STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
     for (int a = 0; a < C::ACC_STAGES; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), C::EPI_WARPS); }
     mbar_init(drain, 1);
+    for (int st = 0; st < C::STAGES; ++st) mbar_init(sfready(st), C::SF_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -136,22 +147,15 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * BN;
         for (int kb = 0; kb < p.num_k_stages; ++kb) {
-          if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          // NVFP4: the scale-staging warps signal once the slot's data and scales are in place
+          if (!mbar_wait_bounded(FMT ? sfready(stage) : full(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t sB = sA + C::A_BYTES;
           const uint32_t sf = tmem + C::SF_TMEM_BASE + stage * C::SF_COLS;
-          if (FMT) {
-            const uint32_t sSFA = sB + C::B_BYTES, sSFB = sSFA + C::SFA_BYTES;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) tc_cp_32x128b_x4(sf + 4 * k, smem_desc(sSFA + 512 * k, 0, 128, 0));
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-              for (int nb = 0; nb < BN / 128; ++nb)
-                tc_cp_32x128b_x4(sf + C::SFA_COLS + k * (BN / 32) + 4 * nb,
-                                 smem_desc(sSFB + nb * 2048 + 512 * k, 0, 128, 0));
-          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t adesc = smem_desc(sA + 32 * k, 16, 1024, 2);
@@ -172,41 +176,85 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
     }
+  } else if (warp < C::EPI_WARP0) {
+    // ---------------------------------------------------------- scale staging (NVFP4)
+    if constexpr (FMT == 1) {
+      const int q = warp & 3;   // TMEM lane quadrant this warp may access
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int kb = 0; kb < p.num_k_stages; ++kb) {
+          // the slot's previous scales were consumed: the producer refilled it only after its MMAs completed
+          if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          const uint8_t* sSFA = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+          const uint8_t* sSFB = sSFA + C::SFA_BYTES;
+          uint32_t v[C::SF_COLS];
+          // lane l of every quadrant holds row l of each 512-byte chunk: columns 4k..4k+3 of the
+          // A scales of MMA k, then per MMA k the BN/128 chunks of the B scales
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 t = *reinterpret_cast<const uint4*>(sSFA + 512 * k + 16 * lane);
+            v[4 * k] = t.x; v[4 * k + 1] = t.y; v[4 * k + 2] = t.z; v[4 * k + 3] = t.w;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int nb = 0; nb < BN / 128; ++nb) {
+              const uint4 t = *reinterpret_cast<const uint4*>(sSFB + 2048 * nb + 512 * k + 16 * lane);
+              const int o = C::SFA_COLS + k * (BN / 32) + 4 * nb;
+              v[o] = t.x; v[o + 1] = t.y; v[o + 2] = t.z; v[o + 3] = t.w;
+            }
+          const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + C::SF_TMEM_BASE + stage * C::SF_COLS;
+#pragma unroll
+          for (int c = 0; c < C::SF_COLS / 16; ++c) tmem_st_32x32b_x16(taddr + 16 * c, v + 16 * c);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sfready(stage));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;       // which BN/2 columns it drains
+    const int q = warp & 3;                          // TMEM lane quadrant this warp may access
+    const int half = (warp - C::EPI_WARP0) >> 2;     // which BN/2 columns it drains
     const float alpha = __fmul_rn(*p.ga, *p.gb);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
-      uint32_t r[C::EPI_COLS / 32][32];
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + half * C::EPI_COLS;
-#pragma unroll
-      for (int c = 0; c < C::EPI_COLS / 32; ++c) tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(acc));
       const int64_t row = (int64_t)mt * C::BM + q * 32 + lane;
-      if (row < p.M) {
-        float* drow = p.D + row * p.ldd;
-        const int64_t col0 = (int64_t)nt * BN + half * C::EPI_COLS;
+      float* drow = p.D + row * p.ldd;
+      const int64_t col0 = (int64_t)nt * BN + half * C::EPI_COLS;
+#pragma unroll 1
+      for (int rd = 0; rd < C::EPI_COLS / C::EPI_ROUND; ++rd) {
+        uint32_t r[C::EPI_ROUND / 32][32];
 #pragma unroll
-        for (int c = 0; c < C::EPI_COLS / 32; ++c)
+        for (int c = 0; c < C::EPI_ROUND / 32; ++c) tmem_ld_32x32b_x32(taddr + rd * C::EPI_ROUND + c * 32, r[c]);
+        tmem_ld_wait();
+        if (rd == C::EPI_COLS / C::EPI_ROUND - 1) {   // accumulator fully read: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty(acc));
+        }
+        if (row < p.M) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int64_t col = col0 + c * 32 + 4 * j;
-            if (col < p.N) {
-              const float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[c][4 * j])),
-                                           __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 1])),
-                                           __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 2])),
-                                           __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 3])));
-              *reinterpret_cast<float4*>(drow + col) = v;
+          for (int c = 0; c < C::EPI_ROUND / 32; ++c)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int64_t col = col0 + rd * C::EPI_ROUND + c * 32 + 4 * j;
+              if (col < p.N) {
+                const float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[c][4 * j])),
+                                             __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 1])),
+                                             __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 2])),
+                                             __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 3])));
+                *reinterpret_cast<float4*>(drow + col) = v;
+              }
             }
-          }
+        }
       }
       if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
     }
