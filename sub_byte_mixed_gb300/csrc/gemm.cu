@@ -241,17 +241,28 @@ __global__ void __launch_bounds__(448, 1)
           if (lane == 0) mbar_arrive(tempty(acc));
         }
         if (row < p.M) {
+          // 32-byte (or 16-byte when D is only 16-byte aligned) streaming stores: whole L2 sectors
+          // per thread, without evicting the operands
 #pragma unroll
           for (int c = 0; c < C::EPI_ROUND / 32; ++c)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int64_t col = col0 + rd * C::EPI_ROUND + c * 32 + 4 * j;
-              if (col < p.N) {
-                const float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[c][4 * j])),
-                                             __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 1])),
-                                             __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 2])),
-                                             __fmul_rn(alpha, __uint_as_float(r[c][4 * j + 3])));
-                *reinterpret_cast<float4*>(drow + col) = v;
+            for (int j = 0; j < 4; ++j) {
+              const int64_t col = col0 + rd * C::EPI_ROUND + c * 32 + 8 * j;
+              const uint32_t* rr = &r[c][8 * j];
+              if (p.v8 && col + 8 <= p.N) {
+                st_global_cs_v8(drow + col, __fmul_rn(alpha, __uint_as_float(rr[0])),
+                                __fmul_rn(alpha, __uint_as_float(rr[1])), __fmul_rn(alpha, __uint_as_float(rr[2])),
+                                __fmul_rn(alpha, __uint_as_float(rr[3])), __fmul_rn(alpha, __uint_as_float(rr[4])),
+                                __fmul_rn(alpha, __uint_as_float(rr[5])), __fmul_rn(alpha, __uint_as_float(rr[6])),
+                                __fmul_rn(alpha, __uint_as_float(rr[7])));
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  if (col + 4 * h < p.N)
+                    st_global_cs_v4(drow + col + 4 * h, __fmul_rn(alpha, __uint_as_float(rr[4 * h])),
+                                    __fmul_rn(alpha, __uint_as_float(rr[4 * h + 1])),
+                                    __fmul_rn(alpha, __uint_as_float(rr[4 * h + 2])),
+                                    __fmul_rn(alpha, __uint_as_float(rr[4 * h + 3])));
               }
             }
         }
@@ -316,6 +327,7 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
   if (!make_code_map(&ta, a_codes, a_rows, row_bytes, C::BM) || !make_code_map(&tb, b_codes, b_rows, row_bytes, BN))
     return cudaErrorInvalidValue;
   p.num_k_stages = (int)(row_bytes / C::KB);
+  p.v8 = (reinterpret_cast<uintptr_t>(p.D) % 32 == 0) && (p.ldd % 8 == 0);
   p.num_m_tiles = (int)((p.M + C::BM - 1) / C::BM);
   p.num_n_tiles = (int)((p.N + BN - 1) / BN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;

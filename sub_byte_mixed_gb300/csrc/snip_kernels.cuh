@@ -45,6 +45,7 @@ struct GemmParams {
   int64_t kp;                   // padded contraction (elements)
   int num_k_stages;             // kp / elements-per-stage
   int num_m_tiles, num_n_tiles;
+  int v8;                       // D rows allow 32-byte stores
   uint32_t* status;
   uint64_t timeout_ns;
 };
