@@ -163,6 +163,22 @@ snip_status snip_amax(const void* x, int64_t n, float* amax_out, void* ws, size_
 snip_status snip_tensor_scales(const void* x, int64_t n, float* scales_out, void* ws, size_t ws_bytes,
                                void* stream);
 
+/* Variant of snip_tensor_scales that needs no workspace and allocates nothing,
+ * for callers that cannot allocate device memory where they run: a host
+ * callback enqueued with cudaLaunchHostFunc (no allocating CUDA call allowed
+ * there), code inside a framework whose caching allocator owns all device
+ * memory, or a latency-critical path that must not synchronize the device.
+ * The pages have no counterpart of this call; it exists for such callers.
+ * x: device bf16, n elements, at most 2^30 (SNIP_ERR_SHAPE beyond that);
+ * scales_out: device, 3 floats {amax, g, s} as for snip_tensor_scales; a
+ * non-finite element makes them NaN (there is no status word to read).
+ * The kernel's scratch is one fixed 64 KB device array shared by every call
+ * on a device and kept until the process exits: calls that overlap on the GPU
+ * (different streams without ordering) race on it and must not be issued.
+ * The first call on each device looks up the array's device address (set-up);
+ * make that first call outside any stream capture. */
+snip_status snip_tensor_scales_noalloc(const void* x, int64_t n, float* scales_out, void* stream);
+
 /* ---------------------------------------------------------------- a2/a3: NVFP4 */
 
 /* NVFP4 quantization of a bf16 rows x cols tensor ("FP4 all the way",

@@ -29,7 +29,8 @@ STATS_NVALS = 8
 # every symbol include/snip.h declares
 EXPORTS = (
     "snip_status_string", "snip_version", "snip_device_check", "snip_workspace_init", "snip_workspace_status",
-    "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_quantize_nvfp4", "snip_quantize_fp8",
+    "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_tensor_scales_noalloc",
+    "snip_quantize_nvfp4", "snip_quantize_fp8",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
     "snip_quant_stats", "snip_stats_finalize",
@@ -70,6 +71,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_quantize_workspace_size": (sz, [i64, i64]),
         "snip_amax": (i32, [vp, i64, vp, vp, sz, vp]),
         "snip_tensor_scales": (i32, [vp, i64, vp, vp, sz, vp]),
+        "snip_tensor_scales_noalloc": (i32, [vp, i64, vp, vp]),
         "snip_quantize_nvfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_fp8": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, sz, vp]),
         "snip_quantized_bytes": (i32, [i32, i32, i64, i64, szp, szp]),
@@ -132,6 +134,10 @@ def snip_amax(x, n, amax_out, ws, ws_bytes, stream):
 
 def snip_tensor_scales(x, n, scales_out, ws, ws_bytes, stream):
     _call("snip_tensor_scales", x, n, scales_out, ws, ws_bytes, stream)
+
+
+def snip_tensor_scales_noalloc(x, n, scales_out, stream):
+    _call("snip_tensor_scales_noalloc", x, n, scales_out, stream)
 
 
 def snip_quantize_nvfp4(x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
