@@ -29,6 +29,8 @@
 // tensor-core work and frees its tensor memory before returning.
 #include <cuda.h>
 
+#include <cstring>
+
 #include "snip_kernels.cuh"
 
 namespace snip {
@@ -279,6 +281,259 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
+// ------------------------------------------------------------------ 2-CTA variant
+// A cluster of two CTAs on neighbouring SMs computes one 256 x 256 tile with
+// tcgen05.mma.cta_group::2: CTA r holds rows 128r..128r+127 of the pair's A
+// tile and of its B tile, and accumulates its 128 rows x 256 columns in its
+// own tensor memory.  Per SM that halves the B bytes per FLOP, which is what
+// limits the one-CTA kernel (shared-memory fill).  The leader (rank 0) issues
+// the MMAs and multicasts its commits to both CTAs; both CTAs' A/B loads
+// complete on the leader's full barrier; block scales land on a local barrier
+// and each CTA's four staging warps write them into its own tensor memory,
+// then arrive on the leader's sf_ready barrier.  SFB_FULL: each CTA's tensor
+// memory holds the scales of all 256 B rows (else only its own 128).
+template <int FMT, int SFB_FULL>
+struct Gemm2Cfg {
+  static constexpr int BM = 128, BN = 256, BNC = 128, KB = 128;
+  static constexpr int A_BYTES = BM * KB, B_BYTES = BNC * KB;
+  static constexpr int SFA_BYTES = FMT ? 2048 : 0;
+  static constexpr int SFB_BYTES = FMT ? (SFB_FULL ? 4096 : 2048) : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGES = FMT ? 5 : 6;
+  static constexpr int ACC_STAGES = FMT ? 1 : 2;
+  static constexpr int SFA_COLS = 16;
+  static constexpr int SFB_COLS_K = SFB_FULL ? 8 : 4;     // scale columns of B per MMA
+  static constexpr int SF_COLS = FMT ? SFA_COLS + 4 * SFB_COLS_K : 0;
+  static constexpr int SF_TMEM_BASE = ACC_STAGES * BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0, "1024-byte aligned stages");
+  static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_STAGES + 1;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+  static constexpr int SF_WARPS = 4, EPI_WARP0 = 6, EPI_WARPS = 8, EPI_COLS = BN / 2, EPI_ROUND = 64;
+  static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+  static constexpr uint32_t IDESC =
+      FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24))
+          : ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24));
+};
+
+template <int FMT, int SFB_FULL>
+__global__ void __launch_bounds__(448, 1)
+    gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                        GemmParams p) {
+  using C = Gemm2Cfg<FMT, SFB_FULL>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto sffull = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
+  auto sfready = [&](int s) { return bar0 + 8u * (3 * C::STAGES + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (4 * C::STAGES + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (4 * C::STAGES + C::ACC_STAGES + a); };
+  const uint32_t drain = bar0 + 8u * (4 * C::STAGES + 2 * C::ACC_STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+      mbar_init(sffull(s), 1);
+      mbar_init(sfready(s), 2 * C::SF_WARPS);
+    }
+    for (int a = 0; a < C::ACC_STAGES; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 2 * C::EPI_WARPS); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); }
+  if (warp == 1) { tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS); tmem_relinquish_pair(); }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers and tensor memory exist before any cross-CTA traffic
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int num_pairs = gridDim.x >> 1, pair = blockIdx.x >> 1;
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;   // 256 x 256 tiles
+  const int64_t groups_k = p.kp >> 8;                     // 2 KB scale slabs per 128-row group
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer (both CTAs)
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+        for (int kb = 0; kb < p.num_k_stages; ++kb) {
+          if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          uint8_t* sA = smem + stage * C::STAGE_BYTES;
+          uint8_t* sB = sA + C::A_BYTES;
+          if (FMT) {
+            uint8_t* sSFA = sB + C::B_BYTES;
+            uint8_t* sSFB = sSFA + C::SFA_BYTES;
+            mbar_arrive_expect_tx(sffull(stage), C::SFA_BYTES + C::SFB_BYTES);
+            const int64_t ga = 2 * mt + rank;
+            tma_load_2d(smem_u32(sSFA), &tmSFA, 0, (int32_t)(8 * (ga * groups_k + kb)), sffull(stage));
+            if (SFB_FULL) {
+              for (int h = 0; h < 2; ++h)
+                tma_load_2d(smem_u32(sSFB + 2048 * h), &tmSFB, 0, (int32_t)(8 * ((2 * nt + h) * groups_k + kb)),
+                            sffull(stage));
+            } else {
+              tma_load_2d(smem_u32(sSFB), &tmSFB, 0, (int32_t)(8 * ((2 * nt + rank) * groups_k + kb)),
+                          sffull(stage));
+            }
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full(stage), 2 * (C::A_BYTES + C::B_BYTES));
+          const uint32_t leader_full = mapa_shared(full(stage), 0);
+          tma_load_2d_pair(smem_u32(sA), &tmA, kb * C::KB, (2 * mt + rank) * C::BM, leader_full);
+          tma_load_2d_pair(smem_u32(sB), &tmB, kb * C::KB, (2 * nt + rank) * C::BNC, leader_full);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer (leader only)
+    if (lane == 0 && rank == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        if (!mbar_wait_bounded(tempty(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * C::BN;
+        for (int kb = 0; kb < p.num_k_stages; ++kb) {
+          if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          if (FMT && !mbar_wait_bounded(sfready(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t sB = sA + C::A_BYTES;
+          const uint32_t sf = tmem + C::SF_TMEM_BASE + stage * C::SF_COLS;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t adesc = smem_desc(sA + 32 * k, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(sB + 32 * k, 16, 1024, 2);
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            if (FMT) tc_mma_nvf4_pair(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * C::SFB_COLS_K, accum);
+            else tc_mma_f8_pair(d_tmem, adesc, bdesc, C::IDESC, accum);
+          }
+          tc_commit_pair_mc(empty(stage), 0x3);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(tfull(acc), 0x3);
+        if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+      }
+      tc_commit_pair_mc(drain, 0x1);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
+    }
+  } else if (warp < C::EPI_WARP0) {
+    // ---------------------------------------------------------- scale staging (both CTAs, NVFP4)
+    if constexpr (FMT == 1) {
+      const int q = warp & 3;
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        for (int kb = 0; kb < p.num_k_stages; ++kb) {
+          if (!mbar_wait_bounded(sffull(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          const uint8_t* sSFA = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+          const uint8_t* sSFB = sSFA + C::SFA_BYTES;
+          uint32_t v[C::SF_COLS];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 t = *reinterpret_cast<const uint4*>(sSFA + 512 * k + 16 * lane);
+            v[4 * k] = t.x; v[4 * k + 1] = t.y; v[4 * k + 2] = t.z; v[4 * k + 3] = t.w;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int nb = 0; nb < C::SFB_COLS_K / 4; ++nb) {
+              const uint4 t = *reinterpret_cast<const uint4*>(sSFB + 2048 * nb + 512 * k + 16 * lane);
+              const int o = C::SFA_COLS + k * C::SFB_COLS_K + 4 * nb;
+              v[o] = t.x; v[o + 1] = t.y; v[o + 2] = t.z; v[o + 3] = t.w;
+            }
+          const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + C::SF_TMEM_BASE + stage * C::SF_COLS;
+#pragma unroll
+          for (int c = 0; c < C::SF_COLS / 16; ++c) tmem_st_32x32b_x16(taddr + 16 * c, v + 16 * c);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(sfready(stage), 0));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    const int half = (warp - C::EPI_WARP0) >> 2;
+    const float alpha = __fmul_rn(*p.ga, *p.gb);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+      if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * C::BN + half * C::EPI_COLS;
+      const int64_t row = (int64_t)(2 * mt + rank) * C::BM + q * 32 + lane;
+      float* drow = p.D + row * p.ldd;
+      const int64_t col0 = (int64_t)nt * C::BN + half * C::EPI_COLS;
+#pragma unroll 1
+      for (int rd = 0; rd < C::EPI_COLS / C::EPI_ROUND; ++rd) {
+        uint32_t r[C::EPI_ROUND / 32][32];
+#pragma unroll
+        for (int c = 0; c < C::EPI_ROUND / 32; ++c) tmem_ld_32x32b_x32(taddr + rd * C::EPI_ROUND + c * 32, r[c]);
+        tmem_ld_wait();
+        if (rd == C::EPI_COLS / C::EPI_ROUND - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
+        }
+        if (row < p.M) {
+#pragma unroll
+          for (int c = 0; c < C::EPI_ROUND / 32; ++c)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int64_t col = col0 + rd * C::EPI_ROUND + c * 32 + 8 * j;
+              const uint32_t* rr = &r[c][8 * j];
+              if (p.v8 && col + 8 <= p.N) {
+                st_global_cs_v8(drow + col, __fmul_rn(alpha, __uint_as_float(rr[0])),
+                                __fmul_rn(alpha, __uint_as_float(rr[1])), __fmul_rn(alpha, __uint_as_float(rr[2])),
+                                __fmul_rn(alpha, __uint_as_float(rr[3])), __fmul_rn(alpha, __uint_as_float(rr[4])),
+                                __fmul_rn(alpha, __uint_as_float(rr[5])), __fmul_rn(alpha, __uint_as_float(rr[6])),
+                                __fmul_rn(alpha, __uint_as_float(rr[7])));
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  if (col + 4 * h < p.N)
+                    st_global_cs_v4(drow + col + 4 * h, __fmul_rn(alpha, __uint_as_float(rr[4 * h])),
+                                    __fmul_rn(alpha, __uint_as_float(rr[4 * h + 1])),
+                                    __fmul_rn(alpha, __uint_as_float(rr[4 * h + 2])),
+                                    __fmul_rn(alpha, __uint_as_float(rr[4 * h + 3])));
+              }
+            }
+        }
+      }
+      if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // the peer's epilogue and the leader's MMAs are done with both tensor memories
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -336,10 +591,84 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
   return cudaGetLastError();
 }
 
+// 2-D byte view of an MMA-layout scale buffer: rows of 256 bytes, loaded 8 rows
+// (one 2 KB slab = 128 rows x 256 contraction elements) at a time.
+static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {256u, (cuuint64_t)(bytes / 256)};
+  cuuint64_t strides[1] = {256u};
+  cuuint32_t box[2] = {256u, 8u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, int SFB_FULL>
+static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
+                                    GemmParams p, int num_sms, cudaStream_t st) {
+  using C = Gemm2Cfg<FMT, SFB_FULL>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT, SFB_FULL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t row_bytes = FMT ? p.kp / 2 : p.kp;
+  CUtensorMap ta, tb, tsa, tsb;
+  memset(&tsa, 0, sizeof tsa);
+  memset(&tsb, 0, sizeof tsb);
+  if (!make_code_map(&ta, a_codes, a_rows, row_bytes, C::BM) || !make_code_map(&tb, b_codes, b_rows, row_bytes, C::BNC))
+    return cudaErrorInvalidValue;
+  if (FMT && (!make_scale_map(&tsa, p.a_scales, a_rows * p.kp / 16) || !make_scale_map(&tsb, p.b_scales, b_rows * p.kp / 16)))
+    return cudaErrorInvalidValue;
+  p.num_k_stages = (int)(row_bytes / C::KB);
+  p.v8 = (reinterpret_cast<uintptr_t>(p.D) % 32 == 0) && (p.ldd % 8 == 0);
+  p.num_m_tiles = (int)((p.M + 255) / 256);
+  p.num_n_tiles = (int)((p.N + 255) / 256);
+  const int tiles = p.num_m_tiles * p.num_n_tiles;
+  const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT, SFB_FULL>, ta, tb, tsa, tsb, p);
+}
+
+// Which GEMM kernel the library uses: 0 = one CTA per tile, 1/2 = CTA pair
+// with full / half B scales per CTA.  Internal switch for the tests.
+static int g_gemm_variant = 0;
+
 cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,
                         int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st) {
+  if (g_gemm_variant == 1) {
+    if (fmt == 1) return launch_gemm_pair<1, 1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+    return launch_gemm_pair<0, 1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  }
+  if (g_gemm_variant == 2) {
+    if (fmt == 1) return launch_gemm_pair<1, 0>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+    return launch_gemm_pair<0, 1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  }
   if (fmt == 1) return launch_gemm_cfg<1, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
   return launch_gemm_cfg<0, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
 }
 
 }  // namespace snip
+
+// Selects the GEMM kernel variant (see g_gemm_variant); returns the previous one.
+extern "C" int snip_internal_set_gemm_variant(int v) {
+  const int old = snip::g_gemm_variant;
+  if (v >= 0 && v <= 2) snip::g_gemm_variant = v;
+  return old;
+}
