@@ -111,8 +111,14 @@ __global__ void __launch_bounds__(448, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+        int mt, nt;
+        tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group, mt, nt);
         for (int kb = 0; kb < p.num_k_stages; ++kb) {
+          // warm L2 with the boxes this CTA loads one ring later
+          if (kb + C::STAGES < p.num_k_stages) {
+            tma_prefetch_l2(&tmA, (kb + C::STAGES) * C::KB, mt * C::BM);
+            tma_prefetch_l2(&tmB, (kb + C::STAGES) * C::KB, nt * BN);
+          }
           if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::A_BYTES;
@@ -224,7 +230,8 @@ __global__ void __launch_bounds__(448, 1)
     const float alpha = __fmul_rn(*p.ga, *p.gb);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+      int mt, nt;
+      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group, mt, nt);
       if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + half * C::EPI_COLS;
@@ -368,8 +375,13 @@ __global__ void __launch_bounds__(448, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
-        const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+        int mt, nt;
+        tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group, mt, nt);
         for (int kb = 0; kb < p.num_k_stages; ++kb) {
+          if (kb + C::STAGES < p.num_k_stages) {
+            tma_prefetch_l2(&tmA, (kb + C::STAGES) * C::KB, (2 * mt + rank) * C::BM);
+            tma_prefetch_l2(&tmB, (kb + C::STAGES) * C::KB, (2 * nt + rank) * C::BNC);
+          }
           if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::A_BYTES;
@@ -478,7 +490,8 @@ __global__ void __launch_bounds__(448, 1)
     const float alpha = __fmul_rn(*p.ga, *p.gb);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
-      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+      int mt, nt;
+      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group, mt, nt);
       if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * C::BN + half * C::EPI_COLS;
@@ -587,6 +600,8 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
   p.num_n_tiles = (int)((p.N + BN - 1) / BN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int grid = tiles < num_sms ? tiles : num_sms;
+  p.group = grid / p.num_n_tiles;
+  if (p.group < 1) p.group = 1;
   gemm_tn_kernel<FMT, BN><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
@@ -630,6 +645,8 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   p.num_n_tiles = (int)((p.N + 255) / 256);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
+  p.group = pairs / p.num_n_tiles;
+  if (p.group < 1) p.group = 1;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(2 * pairs, 1, 1);
