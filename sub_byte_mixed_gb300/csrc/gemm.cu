@@ -111,14 +111,8 @@ __global__ void __launch_bounds__(448, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        int mt, nt;
-        tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group, mt, nt);
+        const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
         for (int kb = 0; kb < p.num_k_stages; ++kb) {
-          // warm L2 with the boxes this CTA loads one ring later
-          if (kb + C::STAGES < p.num_k_stages) {
-            tma_prefetch_l2(&tmA, (kb + C::STAGES) * C::KB, mt * C::BM);
-            tma_prefetch_l2(&tmB, (kb + C::STAGES) * C::KB, nt * BN);
-          }
           if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::A_BYTES;
@@ -230,8 +224,7 @@ __global__ void __launch_bounds__(448, 1)
     const float alpha = __fmul_rn(*p.ga, *p.gb);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      int mt, nt;
-      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group, mt, nt);
+      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + half * C::EPI_COLS;
@@ -297,19 +290,21 @@ __global__ void __launch_bounds__(448, 1)
 // the MMAs and multicasts its commits to both CTAs; both CTAs' A/B loads
 // complete on the leader's full barrier; block scales land on a local barrier
 // and each CTA's four staging warps write them into its own tensor memory,
-// then arrive on the leader's sf_ready barrier.  SFB_FULL: each CTA's tensor
-// memory holds the scales of all 256 B rows (else only its own 128).
-template <int FMT, int SFB_FULL>
+// then arrive on the leader's sf_ready barrier.  Each CTA's tensor memory must
+// hold the scales of all 256 B rows (each CTA's tensor core multiplies its A
+// rows by the whole B tile); holding only its own 128 gives wrong products.
+// The library routes FP8 GEMMs here; NVFP4 runs faster on the one-CTA kernel.
+template <int FMT>
 struct Gemm2Cfg {
   static constexpr int BM = 128, BN = 256, BNC = 128, KB = 128;
   static constexpr int A_BYTES = BM * KB, B_BYTES = BNC * KB;
   static constexpr int SFA_BYTES = FMT ? 2048 : 0;
-  static constexpr int SFB_BYTES = FMT ? (SFB_FULL ? 4096 : 2048) : 0;
+  static constexpr int SFB_BYTES = FMT ? 4096 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGES = FMT ? 5 : 6;
   static constexpr int ACC_STAGES = FMT ? 1 : 2;
   static constexpr int SFA_COLS = 16;
-  static constexpr int SFB_COLS_K = SFB_FULL ? 8 : 4;     // scale columns of B per MMA
+  static constexpr int SFB_COLS_K = 8;                    // scale columns of B per MMA (256 rows)
   static constexpr int SF_COLS = FMT ? SFA_COLS + 4 * SFB_COLS_K : 0;
   static constexpr int SF_TMEM_BASE = ACC_STAGES * BN;
   static constexpr int TMEM_COLS = 512;
@@ -324,12 +319,12 @@ struct Gemm2Cfg {
           : ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24));
 };
 
-template <int FMT, int SFB_FULL>
+template <int FMT>
 __global__ void __launch_bounds__(448, 1)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         GemmParams p) {
-  using C = Gemm2Cfg<FMT, SFB_FULL>;
+  using C = Gemm2Cfg<FMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -375,13 +370,8 @@ __global__ void __launch_bounds__(448, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
-        int mt, nt;
-        tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group, mt, nt);
+        const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
         for (int kb = 0; kb < p.num_k_stages; ++kb) {
-          if (kb + C::STAGES < p.num_k_stages) {
-            tma_prefetch_l2(&tmA, (kb + C::STAGES) * C::KB, (2 * mt + rank) * C::BM);
-            tma_prefetch_l2(&tmB, (kb + C::STAGES) * C::KB, (2 * nt + rank) * C::BNC);
-          }
           if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::A_BYTES;
@@ -391,14 +381,9 @@ __global__ void __launch_bounds__(448, 1)
             mbar_arrive_expect_tx(sffull(stage), C::SFA_BYTES + C::SFB_BYTES);
             const int64_t ga = 2 * mt + rank;
             tma_load_2d(smem_u32(sSFA), &tmSFA, 0, (int32_t)(8 * (ga * groups_k + kb)), sffull(stage));
-            if (SFB_FULL) {
-              for (int h = 0; h < 2; ++h)
-                tma_load_2d(smem_u32(sSFB + 2048 * h), &tmSFB, 0, (int32_t)(8 * ((2 * nt + h) * groups_k + kb)),
-                            sffull(stage));
-            } else {
-              tma_load_2d(smem_u32(sSFB), &tmSFB, 0, (int32_t)(8 * ((2 * nt + rank) * groups_k + kb)),
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(smem_u32(sSFB + 2048 * h), &tmSFB, 0, (int32_t)(8 * ((2 * nt + h) * groups_k + kb)),
                           sffull(stage));
-            }
           }
           if (rank == 0) mbar_arrive_expect_tx(full(stage), 2 * (C::A_BYTES + C::B_BYTES));
           const uint32_t leader_full = mapa_shared(full(stage), 0);
@@ -490,8 +475,7 @@ __global__ void __launch_bounds__(448, 1)
     const float alpha = __fmul_rn(*p.ga, *p.gb);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
-      int mt, nt;
-      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group, mt, nt);
+      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * C::BN + half * C::EPI_COLS;
@@ -600,8 +584,6 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
   p.num_n_tiles = (int)((p.N + BN - 1) / BN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  p.group = grid / p.num_n_tiles;
-  if (p.group < 1) p.group = 1;
   gemm_tn_kernel<FMT, BN><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
@@ -620,13 +602,13 @@ static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int SFB_FULL>
+template <int FMT>
 static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
                                     GemmParams p, int num_sms, cudaStream_t st) {
-  using C = Gemm2Cfg<FMT, SFB_FULL>;
+  using C = Gemm2Cfg<FMT>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT, SFB_FULL>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -645,8 +627,6 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   p.num_n_tiles = (int)((p.N + 255) / 256);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
-  p.group = pairs / p.num_n_tiles;
-  if (p.group < 1) p.group = 1;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(2 * pairs, 1, 1);
@@ -660,32 +640,18 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT, SFB_FULL>, ta, tb, tsa, tsb, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT>, ta, tb, tsa, tsb, p);
 }
 
-// Which GEMM kernel the library uses: 0 = one CTA per tile, 1/2 = CTA pair
-// with full / half B scales per CTA.  Internal switch for the tests.
-static int g_gemm_variant = 0;
-
+// Measured on GB300 at the Llama-7B shapes: NVFP4 runs faster on the one-CTA
+// kernel (its scale staging per stage is the same work either way, and the
+// pair's cross-CTA handshakes cost more than its halved B traffic saves),
+// FP8 faster on the CTA pair (about 10-15%).
 cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,
                         int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st) {
-  if (g_gemm_variant == 1) {
-    if (fmt == 1) return launch_gemm_pair<1, 1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
-    return launch_gemm_pair<0, 1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
-  }
-  if (g_gemm_variant == 2) {
-    if (fmt == 1) return launch_gemm_pair<1, 0>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
-    return launch_gemm_pair<0, 1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
-  }
   if (fmt == 1) return launch_gemm_cfg<1, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
-  return launch_gemm_cfg<0, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  return launch_gemm_pair<0>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
 }
 
 }  // namespace snip
 
-// Selects the GEMM kernel variant (see g_gemm_variant); returns the previous one.
-extern "C" int snip_internal_set_gemm_variant(int v) {
-  const int old = snip::g_gemm_variant;
-  if (v >= 0 && v <= 2) snip::g_gemm_variant = v;
-  return old;
-}

@@ -46,7 +46,6 @@ struct GemmParams {
   int num_k_stages;             // kp / elements-per-stage
   int num_m_tiles, num_n_tiles;
   int v8;                       // D rows allow 32-byte stores
-  int group;                    // m-tiles per raster group (see tile_coords)
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -111,17 +110,6 @@ cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, 
 
 // Upper bound on the number of amax / stats partial slots any launch uses.
 constexpr int kMaxPartials = 1024;
-
-// Raster order of output tiles: groups of `group` m-tiles; inside a group the
-// m index runs fastest, then n.  The tiles in flight at once then share a few
-// A panels and all B panels, which stay in L2 across waves.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group, int& mt, int& nt) {
-  const int per_group = group * num_n;
-  const int g = tile / per_group, r = tile - g * per_group;
-  const int gm = min(group, num_m - g * group);
-  nt = r / gm;
-  mt = g * group + (r - nt * gm);
-}
 
 __device__ __forceinline__ U4 make_zero_u4() { return U4{0u, 0u, 0u, 0u}; }
 
