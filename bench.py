@@ -84,6 +84,7 @@ def config_json(cfg, plan, args):
         "flop_per_step": cfg.flops_fwd_bwd(),
         "l2": "inputs larger than L2 (no flush)",
         "rounding": "RTN forward, SR (Philox4x32-10, 16 bits/elem) backward",
+        "stats": "SNIP statistics of X, W (forward rounding) and dY (dgrad rounding) fused into their row-block quantizations",
     }
 
 
@@ -269,15 +270,14 @@ class Step:
                 t = src[name]
                 rows, cols = t.shape
                 g = scp[name] + fo
-                if f == snip.NVFP4:
-                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
-                            self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, None, ws, wsb, stream)
-                    calls.append((L.snip_quantize_nvfp4, args, qcat, bpe * t.numel()))
-                else:
-                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
-                            self.codes[r].data_ptr(), g, ws, wsb, stream)
-                    calls.append((L.snip_quantize_fp8, args, qcat, bpe * t.numel()))
-                if r in (1, 3, 5):   # both operands of a GEMM are ready
+                if r in (0, 1, 2):
+                    # row-block quantization with SNIP's statistics of the same tensor in one pass
+                    k = r
+                    args = (f, t.data_ptr(), rows, cols, rnd[r], 0, sid + r, scp[name], snip.MMA,
+                            self.codes[r].data_ptr(), self.scales[r].data_ptr() if f == snip.NVFP4 else None,
+                            self.raw[j, k].data_ptr(), ws, wsb, stream)
+                    calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel()))
+                elif f == snip.NVFP4:                if r in (1, 3, 5):   # both operands of a GEMM are ready
                     a, b = r - 1, r
                     M, N, K = {1: (T, l.N, l.K), 3: (T, l.K, l.N), 5: (l.N, l.K, T)}[r]
                     D = {1: self.Y[j], 3: self.dX[j], 5: self.dW[j]}[r]
@@ -288,12 +288,6 @@ class Step:
                     args = (f, self.codes[a].data_ptr(), sa, ga, self.codes[b].data_ptr(), sb, gb, M, N, K,
                             D.data_ptr(), D.stride(0), ws, wsb, stream)
                     calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K))
-            for k, (name, rn, s_id) in enumerate(((l.x_id, 0, sid + 0), ("W", 0, sid + 1), ("dY", 1, sid + 2))):
-                t = src[name]
-                rows, cols = t.shape
-                args = (t.data_ptr(), rows, cols, rn, 0, s_id, scp[name], self.raw[j, k].data_ptr(), None, None, ws,
-                        wsb, stream)
-                calls.append((L.snip_quant_stats, args, "stats", STATS_BYTES_PER_ELEM * t.numel()))
         self.calls = calls
         # one kernel per call (the scales are computed once per tensor and passed in)
         self.launches_per_step = len(calls)
@@ -311,7 +305,7 @@ class Step:
 
 def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
     """The same step through the layer API (snip_qlinear_fwd / _bwd,
-    snip_quant_stats) with host buffers: pinned inputs copied in and outputs
+    statistics fused into their quantizations) with host buffers: pinned inputs copied in and outputs
     copied out inside the timed region."""
     import torch
     inp = step.inp
@@ -337,11 +331,9 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
             d.copy_(h, non_blocking=True)
         for j, l in enumerate(cfg.linears):
             X = inp.X[l.x_id]
-            snip.qlinear_fwd(p, j, X, inp.W[j], ws, Y=step.Y[j])
-            snip.qlinear_bwd(p, j, X, inp.W[j], inp.dY[j], ws, dX=step.dX[j], dW=step.dW[j])
-            for k, (t, rn) in enumerate(((X, 0), (inp.W[j], 0), (inp.dY[j], 1))):
-                snip.quant_stats(t, rnd=rn, seed=0, stream_id=8 * j + k, ws=ws, raw=step.raw[j, k])
-        # (the layer API computes each tensor's scales inside the calls)
+            # statistics of X, W (forward) and dY (dgrad) come out of the quantization passes
+            snip.qlinear_fwd(p, j, X, inp.W[j], ws, Y=step.Y[j], stats=step.raw[j, 0:2])
+            snip.qlinear_bwd(p, j, X, inp.W[j], inp.dY[j], ws, dX=step.dX[j], dW=step.dW[j], stats=step.raw[j, 2])
         for h, d in zip(hY + hdX + hdW, step.Y + step.dX + step.dW):
             h.copy_(d, non_blocking=True)
         hraw.copy_(step.raw, non_blocking=True)
@@ -359,7 +351,7 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
     ms = e0.elapsed_time(e1) / nsteps
     return {"value": cfg.flops_fwd_bwd() / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "path": "snip_qlinear_fwd/bwd + snip_quant_stats, pinned host in/out"}
+            "path": "snip_qlinear_fwd/bwd with fused statistics, pinned host in/out"}
 
 
 def run_ours(args, rank, world, local_rank):

@@ -257,18 +257,23 @@ size_t snip_qlinear_workspace_size(const snip_plan* plan, int layer, int64_t T, 
 /* Forward (SNIP Figure 5): Y = Q(X) Q(W)^T.  X device T x K bf16, W device
  * N x K bf16, Y device T x N fp32.  Both quantized along K in the layer's
  * format with the plan's rounding (default RTN), stream ids layer*8+{0,1}.
- * T, K, N multiples of 16. */
+ * T, K, N multiples of 16.  stats_out (device, nullable, 2 x SNIP_STATS_NVALS
+ * doubles): SNIP's statistics of X then of W (as snip_quant_stats with the
+ * forward rounding), computed inside the forward quantization passes. */
 snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, const void* W,
-                             int64_t T, int64_t K, int64_t N, float* Y,
+                             int64_t T, int64_t K, int64_t N, float* Y, double* stats_out,
                              void* ws, size_t ws_bytes, void* stream);
 
 /* Backward (SNIP Figure 5): dX = Q(dY) Q(W^T)^T (dY and W^T quantized along
  * N) and dW = Q(dY^T) Q(X^T)^T (both quantized along T), stochastic rounding
  * by default ("FP4 all the way", Outline), stream ids layer*8+{2,3,4,5}.
- * dY device T x N bf16, dX device T x K fp32, dW device N x K fp32. */
+ * dY device T x N bf16, dX device T x K fp32, dW device N x K fp32.
+ * stats_out (device, nullable, SNIP_STATS_NVALS doubles): SNIP's statistics of
+ * dY under the dgrad rounding and stream (layer*8+2), computed inside dY's
+ * dgrad quantization pass. */
 snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W,
                              const void* dY, int64_t T, int64_t K, int64_t N, float* dX, float* dW,
-                             void* ws, size_t ws_bytes, void* stream);
+                             double* stats_out, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- a8: statistics */
 
@@ -282,6 +287,18 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
 snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_round rnd, uint64_t seed,
                              uint64_t stream_id, const float* scales_in, double* raw_out, float* block_err_nvfp4,
                              float* block_err_fp8, void* ws, size_t ws_bytes, void* stream);
+
+/* One pass that both quantizes x with blocks along cols (as snip_quantize_*
+ * with the given layout, rounding and stream) and computes SNIP's statistics
+ * of x under that same rounding and random bits (as snip_quant_stats): the
+ * tensor is read once.  fmt selects the codes written (scales: NVFP4 only);
+ * scales_in (device, nullable) = {amax, g, s} from snip_tensor_scales (NULL:
+ * computed first); raw_out device SNIP_STATS_NVALS doubles.  Errors as for
+ * snip_quantize_nvfp4 / snip_quant_stats. */
+snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, int64_t cols, snip_round rnd,
+                                uint64_t seed, uint64_t stream_id, const float* scales_in, snip_layout layout,
+                                uint8_t* codes, uint8_t* scales, double* raw_out, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /* Host helper: derive ratios and sqrt(3) flags from a host copy of raw_out. */
 snip_status snip_stats_finalize(const double* raw_host, snip_stats* out);

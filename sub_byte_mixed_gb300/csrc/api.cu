@@ -91,8 +91,9 @@ snip_status run_scales(const void* x, int64_t n, float* out3, void* ws, int num_
 // One quantization with the tensor scale `scale` (device float).
 snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int orient, int rnd, uint64_t seed,
                          uint64_t stream_id, const float* scale, int layout, uint8_t* codes, uint8_t* scales,
-                         float* g_out, float* block_err, int num_sms, cudaStream_t st) {
-  QuantParams p;
+                         float* g_out, float* block_err, int num_sms, cudaStream_t st, const float* scales3 = nullptr,
+                         double* raw_out = nullptr, void* ws = nullptr) {
+  QuantParams p = {};
   p.x = static_cast<const uint16_t*>(x);
   p.rows = rows;
   p.cols = cols;
@@ -107,6 +108,12 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   p.scales = scales;
   p.g_out = g_out;
   p.block_err = block_err;
+  if (raw_out) {   // statistics fused into this (row-block) quantization
+    p.scales3 = scales3;
+    p.partials = ws_at<double>(ws, kOffStatsPartials);
+    p.counter = ws_at<uint32_t>(ws, kOffStatsCounter);
+    p.raw_out = raw_out;
+  }
   // an empty output still publishes its tensor scale: the one-CTA row kernel does that
   if (p.orp == 0 || p.ocp == 0) orient = SNIP_BLOCKS_ALONG_COLS;
   return cuda_status(launch_quant(fmt == SNIP_FMT_NVFP4 ? 1 : 0, p, orient, layout, rnd, block_err != nullptr,
@@ -372,7 +379,7 @@ size_t snip_qlinear_workspace_size(const snip_plan* plan, int layer, int64_t T, 
 }
 
 snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, const void* W, int64_t T, int64_t K,
-                             int64_t N, float* Y, void* ws, size_t ws_bytes, void* stream) {
+                             int64_t N, float* Y, double* stats_out, void* ws, size_t ws_bytes, void* stream) {
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
@@ -393,19 +400,19 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
   if ((s = run_scales(W, N * K, sw, ws, sms, st)) != SNIP_OK) return s;
   if ((s = run_quantize(fmt, X, T, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_X_FWD], plan->seed, sid + SNIP_TAG_X_FWD,
                         sx + si, SNIP_LAYOUT_MMA, b + L.op[0].codes_off, b + L.op[0].scales_off, nullptr, nullptr,
-                        sms, st)) != SNIP_OK)
+                        sms, st, sx, stats_out, ws)) != SNIP_OK)
     return s;
   if ((s = run_quantize(fmt, W, N, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_W_FWD], plan->seed, sid + SNIP_TAG_W_FWD,
                         sw + si, SNIP_LAYOUT_MMA, b + L.op[1].codes_off, b + L.op[1].scales_off, nullptr, nullptr,
-                        sms, st)) != SNIP_OK)
+                        sms, st, sw, stats_out ? stats_out + SNIP_STATS_NVALS : nullptr, ws)) != SNIP_OK)
     return s;
   return run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, sx + si, b + L.op[1].codes_off,
                   b + L.op[1].scales_off, sw + si, T, N, K, Y, N, ws, sms, st);
 }
 
 snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W, const void* dY,
-                             int64_t T, int64_t K, int64_t N, float* dX, float* dW, void* ws, size_t ws_bytes,
-                             void* stream) {
+                             int64_t T, int64_t K, int64_t N, float* dX, float* dW, double* stats_out, void* ws,
+                             size_t ws_bytes, void* stream) {
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
@@ -430,7 +437,7 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
   // dgrad: dX = Q(dY) Q(W^T)^T, contraction N
   if ((s = run_quantize(fmt, dY, T, N, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_DY_DGRAD], plan->seed,
                         sid + SNIP_TAG_DY_DGRAD, sd + si, SNIP_LAYOUT_MMA, b + L.op[0].codes_off,
-                        b + L.op[0].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
+                        b + L.op[0].scales_off, nullptr, nullptr, sms, st, sd, stats_out, ws)) != SNIP_OK)
     return s;
   if ((s = run_quantize(fmt, W, N, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_WT_DGRAD], plan->seed,
                         sid + SNIP_TAG_WT_DGRAD, sw + si, SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
@@ -470,7 +477,7 @@ snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_rou
     if ((s = run_scales(a, rows * cols, slot, ws, sms, st)) != SNIP_OK) return s;
     sc = slot;
   }
-  StatsParams p;
+  StatsParams p = {};
   p.x = static_cast<const uint16_t*>(a);
   p.rows = rows;
   p.cols = cols;
@@ -483,6 +490,30 @@ snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_rou
   p.block_err4 = block_err_nvfp4;
   p.block_err8 = block_err_fp8;
   return cuda_status(launch_stats(p, rnd, sms, st));
+}
+
+snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, int64_t cols, snip_round rnd,
+                                uint64_t seed, uint64_t stream_id, const float* scales_in, snip_layout layout,
+                                uint8_t* codes, uint8_t* scales, double* raw_out, void* ws, size_t ws_bytes,
+                                void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if (!valid_enum(fmt, 2) || !raw_out) return SNIP_ERR_INVALID_ARG;
+  float g_dummy;   // validation only: g_out is not written by this entry point
+  s = check_quantize_args(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, layout, codes,
+                          fmt == SNIP_FMT_NVFP4 ? scales : nullptr, &g_dummy, ws, ws_bytes);
+  if (s != SNIP_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float* sc = scales_in;
+  if (!sc) {
+    float* slot = scale_slot(ws, 3);
+    if ((s = run_scales(x, rows * cols, slot, ws, sms, st)) != SNIP_OK) return s;
+    sc = slot;
+  }
+  return run_quantize(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, seed, stream_id,
+                      sc + (fmt == SNIP_FMT_NVFP4 ? 1 : 2), layout, codes, scales, nullptr, nullptr, sms, st, sc,
+                      raw_out, ws);
 }
 
 snip_status snip_stats_finalize(const double* raw, snip_stats* out) {

@@ -199,22 +199,174 @@ __device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, c
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// ------------------------------------------------------------------ a8: statistics
+// One pass: ||A||^2, the squared errors of NVFP4 and FP8 quantization under
+// the tensor's rounding, and the expected SR squared error on both grids,
+// sum (hi-|y|)(|y|-lo) q^2.  For round-to-nearest it is formed from the
+// rounding error d and the grid step h as |d| h - d^2 (equal to it because
+// |d| = min(y-lo, hi-y)), accumulated per block as p*sum(|d| h) - sum(d^2)
+// over the unsaturated elements; for stochastic rounding from the fraction f
+// of the step, f (1-f) h^2, times p^2 per block.  The sums need no bit
+// exactness, so they use fused multiply-adds; per-thread sums are fp32 (a few
+// hundred elements), per-CTA and final sums fp64.
+
+// Bit pattern of the E2M1 grid step at y >= 0: 0.5 below 2, then 2^(E-1).
+__device__ __forceinline__ uint32_t e2m1_step_bits(float y) {
+  const int32_t e = (int32_t)(__float_as_uint(y) & 0x7f800000u) - 0x00800000;
+  return (uint32_t)max(e, 0x3f000000);
+}
+
+// Statistics of one 16-element block: squares of the values, the squared
+// errors of NVFP4 (block scale bs) and FP8 (tensor scale s8) quantization
+// under rounding RND, and the expected SR variance on both grids.
+struct BlockStats {
+  float x2, e4, e8, v4, v8;
+};
+template <int RND>
+__device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
+                                                    float s8, float inv8, bool special8) {
+  float bx2 = 0.f, be4 = 0.f, be8 = 0.f, A4 = 0.f, B4 = 0.f, A8 = 0.f, B8 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    bx2 = fmaf(v[i], v[i], fmaf(v[i + 1], v[i + 1], bx2));
+    // ---------------- NVFP4
+    if (bs.special) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float q = (bs.p == 0.0f || v[i + k] == 0.0f) ? 0.0f : copysignf(6.0f, v[i + k]);
+        const float d = fmaf(q, bs.p, -v[i + k]);
+        be4 = fmaf(d, d, be4);
+      }
+    } else if (RND == 0) {
+      const float y0 = __fmul_rn(v[i], bs.inv), y1 = __fmul_rn(v[i + 1], bs.inv);
+      const float2 q = e2m1x2_decode(e2m1x2_rn(y0, y1));
+      const float d0 = fmaf(q.x, bs.p, -v[i]), d1 = fmaf(q.y, bs.p, -v[i + 1]);
+      be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
+      const float m0 = fabsf(y0) < 6.0f ? d0 : 0.0f, m1 = fabsf(y1) < 6.0f ? d1 : 0.0f;
+      A4 = fmaf(fabsf(m0), __uint_as_float(e2m1_step_bits(fabsf(y0))), A4);
+      A4 = fmaf(fabsf(m1), __uint_as_float(e2m1_step_bits(fabsf(y1))), A4);
+      B4 = fmaf(m0, m0, fmaf(m1, m1, B4));
+    } else {
+      const float y0 = __fmul_rn(fabsf(v[i]), bs.inv), y1 = __fmul_rn(fabsf(v[i + 1]), bs.inv);
+      const uint32_t b0 = e2m1_sr_base(y0), b1 = e2m1_sr_base(y1);
+      const uint32_t c0 = e2m1_sr_from_base(b0, uhalf(u, i)), c1 = e2m1_sr_from_base(b1, uhalf(u, i + 1));
+      const float2 q = e2m1x2_decode(c0 | (c1 << 4));
+      const float d0 = fmaf(q.x, bs.p, -fabsf(v[i])), d1 = fmaf(q.y, bs.p, -fabsf(v[i + 1]));
+      be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
+      // f (1-f) h^2 with f the 22 bits below E2M1's mantissa bit
+      const float f0 = __fmul_rn((float)(b0 & 0x3fffffu), 2.384185791015625e-07f);
+      const float f1 = __fmul_rn((float)(b1 & 0x3fffffu), 2.384185791015625e-07f);
+      const float h0 = __uint_as_float(e2m1_step_bits(y0)), h1 = __uint_as_float(e2m1_step_bits(y1));
+      const float w0 = y0 < 6.0f ? fmaf(-f0, f0, f0) * (h0 * h0) : 0.0f;
+      const float w1 = y1 < 6.0f ? fmaf(-f1, f1, f1) * (h1 * h1) : 0.0f;
+      A4 += w0 + w1;
+    }
+    // ---------------- FP8
+    if (special8) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float q = v[i + k] == 0.0f ? 0.0f : copysignf(448.0f, v[i + k]);
+        const float d = fmaf(q, s8, -v[i + k]);
+        be8 = fmaf(d, d, be8);
+      }
+    } else if (RND == 0) {
+      const float y0 = __fmul_rn(v[i], inv8), y1 = __fmul_rn(v[i + 1], inv8);
+      const float2 q = e4m3x2_decode(e4m3x2_rn_sat(y0, y1));
+      const float d0 = fmaf(q.x, s8, -v[i]), d1 = fmaf(q.y, s8, -v[i + 1]);
+      be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
+      const float m0 = fabsf(y0) < 448.0f ? d0 : 0.0f, m1 = fabsf(y1) < 448.0f ? d1 : 0.0f;
+      A8 = fmaf(fabsf(m0), __uint_as_float(e4m3_step_bits(fabsf(y0))), A8);
+      A8 = fmaf(fabsf(m1), __uint_as_float(e4m3_step_bits(fabsf(y1))), A8);
+      B8 = fmaf(m0, m0, fmaf(m1, m1, B8));
+    } else {
+      const float y0 = __fmul_rn(fabsf(v[i]), inv8), y1 = __fmul_rn(fabsf(v[i + 1]), inv8);
+      const uint32_t b0 = e4m3_sr_base(y0), b1 = e4m3_sr_base(y1);
+      const uint32_t c0 = e4m3_sr_from_base(b0, uhalf(u, i)), c1 = e4m3_sr_from_base(b1, uhalf(u, i + 1));
+      const float2 q = e4m3x2_decode(c0 | (c1 << 8));
+      const float d0 = fmaf(q.x, s8, -fabsf(v[i])), d1 = fmaf(q.y, s8, -fabsf(v[i + 1]));
+      be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
+      const float f0 = __fmul_rn((float)(b0 & 0xfffffu), 9.5367431640625e-07f);   // 2^-20
+      const float f1 = __fmul_rn((float)(b1 & 0xfffffu), 9.5367431640625e-07f);
+      const float h0 = __uint_as_float(e4m3_step_bits(y0)), h1 = __uint_as_float(e4m3_step_bits(y1));
+      const float w0 = y0 < 448.0f ? fmaf(-f0, f0, f0) * (h0 * h0) : 0.0f;
+      const float w1 = y1 < 448.0f ? fmaf(-f1, f1, f1) * (h1 * h1) : 0.0f;
+      A8 += w0 + w1;
+    }
+  }
+  float bv4, bv8;
+  if (RND == 1) {   // fractions were in units of the step: scale by p^2 and s^2
+    bv4 = bs.special ? 0.0f : A4 * (bs.p * bs.p);
+    bv8 = special8 ? 0.0f : A8 * (s8 * s8);
+  } else {          // p * sum(|d| h) - sum(d^2) over unsaturated elements
+    bv4 = bs.special ? 0.0f : fmaf(bs.p, A4, -B4);
+    bv8 = special8 ? 0.0f : fmaf(s8, A8, -B8);
+  }  BlockStats r;
+  r.x2 = bx2;
+  r.e4 = be4;
+  r.e8 = be8;
+  r.v4 = bv4;
+  r.v8 = bv8;
+  return r;
+}
+
+// CTA reduction of the five fp32 per-thread sums into fp64, then the last CTA
+// to finish adds all CTAs' partials and writes the raw statistics vector.
+__device__ __forceinline__ void stats_finish(float sx2, float e4, float e8, float v4, float v8, double* partials,
+                                             uint32_t* counter, double* raw_out, float amax, int64_t count) {
+  double acc[5] = {(double)sx2, (double)e4, (double)e8, (double)v4, (double)v8};
+  block_sum_f64<5>(acc);
+  __shared__ bool s_last;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < 5; ++k) partials[(int64_t)blockIdx.x * 5 + k] = acc[k];
+    __threadfence();
+    s_last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  double tot[5] = {0, 0, 0, 0, 0};
+  for (uint32_t j = threadIdx.x; j < gridDim.x; j += blockDim.x)
+    for (int k = 0; k < 5; ++k) tot[k] += ((volatile double*)partials)[(int64_t)j * 5 + k];
+  block_sum_f64<5>(tot);
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < 5; ++k) raw_out[k] = tot[k];
+    raw_out[5] = (double)amax;
+    raw_out[6] = (double)count;
+    raw_out[7] = 0.0;
+    *counter = 0;
+  }
+}
+
+__device__ __forceinline__ void stats_nan(double* raw_out) {
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    for (int k = 0; k < 8; ++k) raw_out[k] = __longlong_as_double(0x7ff8000000000000ll);
+}
+
 // ------------------------------------------------------------------ a2 / a4: blocks along columns
 // One thread per 16-element block; a warp covers 32 consecutive blocks of one
 // output row.  Rows and blocks past the source tensor (MMA padding) encode as
 // zeros.
-template <int FMT, int LAYOUT, int RND, bool ERR>
+// STATS: also accumulate SNIP's statistics of the tensor (both formats, this
+// call's rounding and random bits) from the same read; needs p.scales3.
+template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   const float g = *p.scale;
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = g;
-  if (isnan(g)) return;
-  const float six_g = __fmul_rn(6.0f, g);
-  const float inv8 = __frcp_rn(g);
+  if (isnan(g)) {
+    if (STATS) stats_nan(p.raw_out);
+    return;
+  }
+  // the two tensor scales (the one not used by this format feeds the statistics)
+  const float g4 = STATS ? p.scales3[1] : g, s8 = STATS ? p.scales3[2] : g;
+  const float six_g = __fmul_rn(6.0f, g4);
+  const float inv8 = __frcp_rn(s8);
+  const bool special8 = !(inv8 < kInf);
   const uint32_t bpr = (uint32_t)(p.ocp >> 4);   // blocks per output row (padded)
   const uint32_t spr = (bpr + 31) >> 5;          // 32-block segments per row
   const uint32_t total = (uint32_t)p.orp * spr;
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
+  float sx2 = 0.f, e4 = 0.f, e8 = 0.f, v4 = 0.f, v8 = 0.f;
   for (uint32_t seg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); seg < total; seg += wstride) {
     const uint32_t r = seg / spr, kb = (seg - r * spr) * 32 + lane;
     if (kb >= bpr) continue;
@@ -230,8 +382,17 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     unpack16(a, b, v);
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     if (RND == 1 && real) sr_bits16(e0, p.seed, p.stream_id, u);
+    BlockScale bs;
+    if (FMT == 1 || STATS) bs = nvfp4_block_scale(amax16_bits(a, b), g4, six_g);
+    if (STATS && real) {
+      const BlockStats st = stats_block16<RND>(v, bs, u, s8, inv8, special8);
+      sx2 += st.x2;
+      e4 += st.e4;
+      e8 += st.e8;
+      v4 += st.v4;
+      v8 += st.v8;
+    }
     if (FMT == 1) {
-      const BlockScale bs = nvfp4_block_scale(amax16_bits(a, b), g, six_g);
       const uint2 c = nvfp4_encode16<RND>(v, bs, u);
       if (LAYOUT == 0) {
         if (!real) continue;
@@ -249,6 +410,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
       *reinterpret_cast<uint4*>(p.codes + (int64_t)r * pitch + (int64_t)kb * 16) = c;
     }
   }
+  if (STATS) stats_finish(sx2, e4, e8, v4, v8, p.partials, p.counter, p.raw_out, p.scales3[0], p.rows * p.cols);
 }
 
 // ------------------------------------------------------------------ a3 / a4: blocks along rows (transposed output)
@@ -375,29 +537,12 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
   }
 }
 
-// ------------------------------------------------------------------ a8: statistics
-// One pass: ||A||^2, the squared errors of NVFP4 and FP8 quantization under
-// the tensor's rounding, and the expected SR squared error on both grids,
-// sum (hi-|y|)(|y|-lo) q^2.  For round-to-nearest it is formed from the
-// rounding error d and the grid step h as |d| h - d^2 (equal to it because
-// |d| = min(y-lo, hi-y)), accumulated per block as p*sum(|d| h) - sum(d^2)
-// over the unsaturated elements; for stochastic rounding from the fraction f
-// of the step, f (1-f) h^2, times p^2 per block.  The sums need no bit
-// exactness, so they use fused multiply-adds; per-thread sums are fp32 (a few
-// hundred elements), per-CTA and final sums fp64.
-
-// Bit pattern of the E2M1 grid step at y >= 0: 0.5 below 2, then 2^(E-1).
-__device__ __forceinline__ uint32_t e2m1_step_bits(float y) {
-  const int32_t e = (int32_t)(__float_as_uint(y) & 0x7f800000u) - 0x00800000;
-  return (uint32_t)max(e, 0x3f000000);
-}
-
+// ------------------------------------------------------------------ a8: statistics kernel
 template <int RND, bool BLK>
 __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
   const float amax = p.scales3[0], g = p.scales3[1], s8 = p.scales3[2];
   if (isnan(amax)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-      for (int k = 0; k < 8; ++k) p.raw_out[k] = __longlong_as_double(0x7ff8000000000000ll);
+    stats_nan(p.raw_out);
     return;
   }
   const float six_g = __fmul_rn(6.0f, g);
@@ -420,115 +565,19 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     if (RND == 1) sr_bits16(e0, p.seed, p.stream_id, u);
     const BlockScale bs = nvfp4_block_scale(amax16_bits(a, b), g, six_g);
-    float bx2 = 0.f, be4 = 0.f, be8 = 0.f, A4 = 0.f, B4 = 0.f, A8 = 0.f, B8 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      bx2 = fmaf(v[i], v[i], fmaf(v[i + 1], v[i + 1], bx2));
-      // ---------------- NVFP4
-      if (bs.special) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float q = (bs.p == 0.0f || v[i + k] == 0.0f) ? 0.0f : copysignf(6.0f, v[i + k]);
-          const float d = fmaf(q, bs.p, -v[i + k]);
-          be4 = fmaf(d, d, be4);
-        }
-      } else if (RND == 0) {
-        const float y0 = __fmul_rn(v[i], bs.inv), y1 = __fmul_rn(v[i + 1], bs.inv);
-        const float2 q = e2m1x2_decode(e2m1x2_rn(y0, y1));
-        const float d0 = fmaf(q.x, bs.p, -v[i]), d1 = fmaf(q.y, bs.p, -v[i + 1]);
-        be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
-        const float m0 = fabsf(y0) < 6.0f ? d0 : 0.0f, m1 = fabsf(y1) < 6.0f ? d1 : 0.0f;
-        A4 = fmaf(fabsf(m0), __uint_as_float(e2m1_step_bits(fabsf(y0))), A4);
-        A4 = fmaf(fabsf(m1), __uint_as_float(e2m1_step_bits(fabsf(y1))), A4);
-        B4 = fmaf(m0, m0, fmaf(m1, m1, B4));
-      } else {
-        const float y0 = __fmul_rn(fabsf(v[i]), bs.inv), y1 = __fmul_rn(fabsf(v[i + 1]), bs.inv);
-        const uint32_t b0 = e2m1_sr_base(y0), b1 = e2m1_sr_base(y1);
-        const uint32_t c0 = e2m1_sr_from_base(b0, uhalf(u, i)), c1 = e2m1_sr_from_base(b1, uhalf(u, i + 1));
-        const float2 q = e2m1x2_decode(c0 | (c1 << 4));
-        const float d0 = fmaf(q.x, bs.p, -fabsf(v[i])), d1 = fmaf(q.y, bs.p, -fabsf(v[i + 1]));
-        be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
-        // f (1-f) h^2 with f the 22 bits below E2M1's mantissa bit
-        const float f0 = __fmul_rn((float)(b0 & 0x3fffffu), 2.384185791015625e-07f);
-        const float f1 = __fmul_rn((float)(b1 & 0x3fffffu), 2.384185791015625e-07f);
-        const float h0 = __uint_as_float(e2m1_step_bits(y0)), h1 = __uint_as_float(e2m1_step_bits(y1));
-        const float w0 = y0 < 6.0f ? fmaf(-f0, f0, f0) * (h0 * h0) : 0.0f;
-        const float w1 = y1 < 6.0f ? fmaf(-f1, f1, f1) * (h1 * h1) : 0.0f;
-        A4 += w0 + w1;
-      }
-      // ---------------- FP8
-      if (special8) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float q = v[i + k] == 0.0f ? 0.0f : copysignf(448.0f, v[i + k]);
-          const float d = fmaf(q, s8, -v[i + k]);
-          be8 = fmaf(d, d, be8);
-        }
-      } else if (RND == 0) {
-        const float y0 = __fmul_rn(v[i], inv8), y1 = __fmul_rn(v[i + 1], inv8);
-        const float2 q = e4m3x2_decode(e4m3x2_rn_sat(y0, y1));
-        const float d0 = fmaf(q.x, s8, -v[i]), d1 = fmaf(q.y, s8, -v[i + 1]);
-        be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
-        const float m0 = fabsf(y0) < 448.0f ? d0 : 0.0f, m1 = fabsf(y1) < 448.0f ? d1 : 0.0f;
-        A8 = fmaf(fabsf(m0), __uint_as_float(e4m3_step_bits(fabsf(y0))), A8);
-        A8 = fmaf(fabsf(m1), __uint_as_float(e4m3_step_bits(fabsf(y1))), A8);
-        B8 = fmaf(m0, m0, fmaf(m1, m1, B8));
-      } else {
-        const float y0 = __fmul_rn(fabsf(v[i]), inv8), y1 = __fmul_rn(fabsf(v[i + 1]), inv8);
-        const uint32_t b0 = e4m3_sr_base(y0), b1 = e4m3_sr_base(y1);
-        const uint32_t c0 = e4m3_sr_from_base(b0, uhalf(u, i)), c1 = e4m3_sr_from_base(b1, uhalf(u, i + 1));
-        const float2 q = e4m3x2_decode(c0 | (c1 << 8));
-        const float d0 = fmaf(q.x, s8, -fabsf(v[i])), d1 = fmaf(q.y, s8, -fabsf(v[i + 1]));
-        be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
-        const float f0 = __fmul_rn((float)(b0 & 0xfffffu), 9.5367431640625e-07f);   // 2^-20
-        const float f1 = __fmul_rn((float)(b1 & 0xfffffu), 9.5367431640625e-07f);
-        const float h0 = __uint_as_float(e4m3_step_bits(y0)), h1 = __uint_as_float(e4m3_step_bits(y1));
-        const float w0 = y0 < 448.0f ? fmaf(-f0, f0, f0) * (h0 * h0) : 0.0f;
-        const float w1 = y1 < 448.0f ? fmaf(-f1, f1, f1) * (h1 * h1) : 0.0f;
-        A8 += w0 + w1;
-      }
-    }
-    float bv4, bv8;
-    if (RND == 1) {   // fractions were in units of the step: scale by p^2 and s^2
-      bv4 = bs.special ? 0.0f : A4 * (bs.p * bs.p);
-      bv8 = special8 ? 0.0f : A8 * (s8 * s8);
-    } else {          // p * sum(|d| h) - sum(d^2) over unsaturated elements
-      bv4 = bs.special ? 0.0f : fmaf(bs.p, A4, -B4);
-      bv8 = special8 ? 0.0f : fmaf(s8, A8, -B8);
-    }
-    sx2 += bx2;
-    e4 += be4;
-    e8 += be8;
-    v4 += bv4;
-    v8 += bv8;
+    const BlockStats st = stats_block16<RND>(v, bs, u, s8, inv8, special8);
+    sx2 += st.x2;
+    e4 += st.e4;
+    e8 += st.e8;
+    v4 += st.v4;
+    v8 += st.v8;
     if (BLK) {
       const int64_t bi = (int64_t)r * bpr + kb;
-      if (p.block_err4) p.block_err4[bi] = be4;
-      if (p.block_err8) p.block_err8[bi] = be8;
+      if (p.block_err4) p.block_err4[bi] = st.e4;
+      if (p.block_err8) p.block_err8[bi] = st.e8;
     }
   }
-  double acc[5] = {(double)sx2, (double)e4, (double)e8, (double)v4, (double)v8};
-  block_sum_f64<5>(acc);
-  __shared__ bool s_last;
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < 5; ++k) p.partials[(int64_t)blockIdx.x * 5 + k] = acc[k];
-    __threadfence();
-    s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  double tot[5] = {0, 0, 0, 0, 0};
-  for (uint32_t j = threadIdx.x; j < gridDim.x; j += blockDim.x)
-    for (int k = 0; k < 5; ++k) tot[k] += ((volatile double*)p.partials)[(int64_t)j * 5 + k];
-  block_sum_f64<5>(tot);
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < 5; ++k) p.raw_out[k] = tot[k];
-    p.raw_out[5] = (double)amax;
-    p.raw_out[6] = (double)(p.rows * p.cols);
-    p.raw_out[7] = 0.0;
-    *p.counter = 0;
-  }
+  stats_finish(sx2, e4, e8, v4, v8, p.partials, p.counter, p.raw_out, amax, p.rows * p.cols);
 }
 
 // ------------------------------------------------------------------ host-side launchers
@@ -551,15 +600,19 @@ static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int r
                              cudaStream_t st) {
   if (orient == 0) {
     const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
-    const int grid = fill_grid(segs, 8, 16 * num_sms);
-#define SNIP_L(LY, RN, ER) quant_rows_kernel<FMT, LY, RN, ER><<<grid, 256, 0, st>>>(p)
+    const bool stats = p.raw_out != nullptr;
+    // with statistics, one partial slot per CTA: keep the grid within them
+    const int grid = fill_grid(segs, 8, stats ? 4 * num_sms : 16 * num_sms);
+#define SNIP_L(LY, RN, ER, SS) quant_rows_kernel<FMT, LY, RN, ER, SS><<<grid, 256, 0, st>>>(p)
+#define SNIP_LS(LY, RN, ER) do { if (stats) SNIP_L(LY, RN, ER, true); else SNIP_L(LY, RN, ER, false); } while (0)
     if (layout == 0) {
-      if (rnd == 0) { if (err) SNIP_L(0, 0, true); else SNIP_L(0, 0, false); }
-      else { if (err) SNIP_L(0, 1, true); else SNIP_L(0, 1, false); }
+      if (rnd == 0) { if (err) SNIP_LS(0, 0, true); else SNIP_LS(0, 0, false); }
+      else { if (err) SNIP_LS(0, 1, true); else SNIP_LS(0, 1, false); }
     } else {
-      if (rnd == 0) { if (err) SNIP_L(1, 0, true); else SNIP_L(1, 0, false); }
-      else { if (err) SNIP_L(1, 1, true); else SNIP_L(1, 1, false); }
+      if (rnd == 0) { if (err) SNIP_LS(1, 0, true); else SNIP_LS(1, 0, false); }
+      else { if (err) SNIP_LS(1, 1, true); else SNIP_LS(1, 1, false); }
     }
+#undef SNIP_LS
 #undef SNIP_L
   } else {
     // source rows tile the output contraction, source cols the output rows

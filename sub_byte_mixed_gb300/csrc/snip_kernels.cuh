@@ -21,6 +21,11 @@ struct QuantParams {
   uint8_t* scales;              // NVFP4 only
   float* g_out;                 // nullable: receives *scale
   float* block_err;             // NVFP4 only, nullable
+  // statistics fused into a row-block quantization (raw_out non-null)
+  const float* scales3;         // {amax, NVFP4 g, FP8 s}
+  double* partials;
+  uint32_t* counter;
+  double* raw_out;
 };
 
 struct StatsParams {

@@ -33,7 +33,7 @@ EXPORTS = (
     "snip_quantize_nvfp4", "snip_quantize_fp8",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
-    "snip_quant_stats", "snip_stats_finalize",
+    "snip_quant_stats", "snip_quantize_stats", "snip_stats_finalize",
 )
 
 
@@ -81,8 +81,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_plan_get": (i32, [vp, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_uint64)]),
         "snip_plan_destroy": (None, [vp]),
         "snip_qlinear_workspace_size": (sz, [vp, i32, i64, i64, i64]),
-        "snip_qlinear_fwd": (i32, [vp, i32, vp, vp, i64, i64, i64, vp, vp, sz, vp]),
-        "snip_qlinear_bwd": (i32, [vp, i32, vp, vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]),
+        "snip_qlinear_fwd": (i32, [vp, i32, vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]),
+        "snip_qlinear_bwd": (i32, [vp, i32, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, sz, vp]),
+        "snip_quantize_stats": (i32, [i32, vp, i64, i64, i32, u64, u64, vp, i32, vp, vp, vp, vp, sz, vp]),
         "snip_quant_stats": (i32, [vp, i64, i64, i32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "snip_stats_finalize": (i32, [vp, ctypes.POINTER(SnipStats)]),
     }
@@ -165,12 +166,18 @@ def snip_qlinear_workspace_size(plan, layer, T, K, N) -> int:
     return load().snip_qlinear_workspace_size(plan, layer, T, K, N)
 
 
-def snip_qlinear_fwd(plan, layer, X, W, T, K, N, Y, ws, ws_bytes, stream):
-    _call("snip_qlinear_fwd", plan, layer, X, W, T, K, N, Y, ws, ws_bytes, stream)
+def snip_qlinear_fwd(plan, layer, X, W, T, K, N, Y, stats_out, ws, ws_bytes, stream):
+    _call("snip_qlinear_fwd", plan, layer, X, W, T, K, N, Y, stats_out, ws, ws_bytes, stream)
 
 
-def snip_qlinear_bwd(plan, layer, X, W, dY, T, K, N, dX, dW, ws, ws_bytes, stream):
-    _call("snip_qlinear_bwd", plan, layer, X, W, dY, T, K, N, dX, dW, ws, ws_bytes, stream)
+def snip_qlinear_bwd(plan, layer, X, W, dY, T, K, N, dX, dW, stats_out, ws, ws_bytes, stream):
+    _call("snip_qlinear_bwd", plan, layer, X, W, dY, T, K, N, dX, dW, stats_out, ws, ws_bytes, stream)
+
+
+def snip_quantize_stats(fmt, x, rows, cols, rnd, seed, stream_id, scales_in, layout, codes, scales, raw_out, ws,
+                        ws_bytes, stream):
+    _call("snip_quantize_stats", fmt, x, rows, cols, rnd, seed, stream_id, scales_in, layout, codes, scales, raw_out,
+          ws, ws_bytes, stream)
 
 
 def snip_quant_stats(a, rows, cols, rnd, seed, stream_id, scales_in, raw_out, block_err_nvfp4, block_err_fp8, ws,
@@ -341,25 +348,44 @@ def qlinear_workspace(plan: Plan, layer: int, T: int, K: int, N: int, device="cu
     return Workspace(snip_qlinear_workspace_size(plan.handle, layer, T, K, N), device)
 
 
-def qlinear_fwd(plan: Plan, layer: int, X, W, ws: Workspace, Y=None):
+def qlinear_fwd(plan: Plan, layer: int, X, W, ws: Workspace, Y=None, stats=None):
+    """Y = Q(X) Q(W)^T; `stats` (device float64 (2, STATS_NVALS) or None) receives
+    the statistics of X and W from the same quantization passes."""
     torch = _torch()
     T, K = X.shape
     N = W.shape[0]
     Y = Y if Y is not None else torch.empty((T, N), dtype=torch.float32, device=X.device)
-    snip_qlinear_fwd(plan.handle, layer, X.data_ptr(), W.data_ptr(), T, K, N, Y.data_ptr(), ws.ptr, ws.nbytes,
-                     _stream())
+    snip_qlinear_fwd(plan.handle, layer, X.data_ptr(), W.data_ptr(), T, K, N, Y.data_ptr(), _ptr(stats), ws.ptr,
+                     ws.nbytes, _stream())
     return Y
 
 
-def qlinear_bwd(plan: Plan, layer: int, X, W, dY, ws: Workspace, dX=None, dW=None):
+def qlinear_bwd(plan: Plan, layer: int, X, W, dY, ws: Workspace, dX=None, dW=None, stats=None):
+    """dX = Q(dY) Q(W^T)^T and dW = Q(dY^T) Q(X^T)^T; `stats` (device float64
+    (STATS_NVALS,) or None) receives the statistics of dY under the dgrad rounding."""
     torch = _torch()
     T, K = X.shape
     N = W.shape[0]
     dX = dX if dX is not None else torch.empty((T, K), dtype=torch.float32, device=X.device)
     dW = dW if dW is not None else torch.empty((N, K), dtype=torch.float32, device=X.device)
     snip_qlinear_bwd(plan.handle, layer, X.data_ptr(), W.data_ptr(), dY.data_ptr(), T, K, N, dX.data_ptr(),
-                     dW.data_ptr(), ws.ptr, ws.nbytes, _stream())
+                     dW.data_ptr(), _ptr(stats), ws.ptr, ws.nbytes, _stream())
     return dX, dW
+
+
+def quantize_stats(fmt, x, rnd=RTN, seed=0, stream_id=0, layout=MMA, scales=None, ws: Workspace | None = None):
+    """One pass: quantize x (blocks along cols) and compute its statistics.
+    Returns (QuantNVFP4 or QuantFP8 without a g/s tensor, raw statistics)."""
+    torch = _torch()
+    ws = ws or small_workspace()
+    rows, cols = x.shape
+    cb, sb = snip_quantized_bytes(fmt, layout, rows, cols)
+    codes = torch.empty(max(cb, 16), dtype=torch.uint8, device=x.device)
+    sc = torch.empty(max(sb, 16), dtype=torch.uint8, device=x.device)
+    raw = torch.empty(STATS_NVALS, dtype=torch.float64, device=x.device)
+    snip_quantize_stats(fmt, x.data_ptr(), rows, cols, rnd, seed, stream_id, _ptr(scales), layout, codes.data_ptr(),
+                        sc.data_ptr() if fmt == NVFP4 else None, raw.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return codes[:cb], sc[:sb], raw
 
 
 def quant_stats(a, rnd=RTN, seed=0, stream_id=0, want_block_err=False, ws: Workspace | None = None, raw=None,

@@ -74,3 +74,44 @@ def test_stats_outlier_sweep_full_size(snip):
     x = inputs.outlier_bf16(8192, 8192, seed=0, tensor_id=100)
     _check(snip, x, 0, blocks=False)
     _check(snip, x, 1, seed=1, sid=2, blocks=True)
+
+
+@pytest.mark.parametrize("fmt", [1, 0])
+@pytest.mark.parametrize("rnd", [0, 1])
+@pytest.mark.parametrize("shape", [(272, 400), (1024, 2048)])
+def test_fused_quantize_stats(snip, fmt, rnd, shape):
+    """The fused pass writes the same codes as the plain quantizer and the same
+    statistics as the oracle (blocks along cols, this call's rounding)."""
+    x = inputs.outlier_bf16(shape[0], shape[1], seed=6, tensor_id=3, frac=0.002)
+    xd = x.cuda()
+    codes, scales, raw = snip.quantize_stats(fmt, xd, rnd=rnd, seed=7, stream_id=10)
+    q = (snip.quantize_nvfp4 if fmt == 1 else snip.quantize_fp8)(xd, rnd=rnd, seed=7, stream_id=10,
+                                                                   layout=snip.MMA)
+    assert torch.equal(codes, q.codes)
+    if fmt == 1:
+        assert torch.equal(scales, q.scales)
+    ref = oracle.quant_stats(x, rnd=rnd, seed=7, stream_id=10)["raw"]
+    got = raw.cpu().numpy()
+    for k in range(7):
+        assert got[k] == pytest.approx(ref[k], rel=STATS_REL, abs=1e-300), (k, got[k], ref[k])
+
+
+def test_qlinear_stats_outputs(snip):
+    """snip_qlinear_fwd/bwd statistics outputs equal SNIP's statistics of X, W
+    (forward rounding) and dY (dgrad rounding, stream layer*8+2)."""
+    X, W, dY = inputs.single_linear_inputs(272, 400, 336, seed=8)
+    layer, seed = 1, 4
+    for code in (1, 0):
+        plan = snip.Plan([code, code], seed=seed)
+        ws = snip.qlinear_workspace(plan, layer, 272, 400, 336)
+        sf = torch.empty((2, snip.STATS_NVALS), dtype=torch.float64, device="cuda")
+        sb = torch.empty(snip.STATS_NVALS, dtype=torch.float64, device="cuda")
+        snip.qlinear_fwd(plan, layer, X.cuda(), W.cuda(), ws, stats=sf)
+        snip.qlinear_bwd(plan, layer, X.cuda(), W.cuda(), dY.cuda(), ws, stats=sb)
+        torch.cuda.synchronize()
+        assert ws.status() == snip.SNIP_OK
+        refs = [oracle.quant_stats(X)["raw"], oracle.quant_stats(W)["raw"],
+                oracle.quant_stats(dY, rnd=1, seed=seed, stream_id=layer * 8 + 2)["raw"]]
+        for got, ref in zip([sf[0].cpu().numpy(), sf[1].cpu().numpy(), sb.cpu().numpy()], refs):
+            for k in range(7):
+                assert got[k] == pytest.approx(ref[k], rel=STATS_REL, abs=1e-300), (k, got[k], ref[k])
