@@ -277,7 +277,15 @@ class Step:
                             self.codes[r].data_ptr(), self.scales[r].data_ptr() if f == snip.NVFP4 else None,
                             self.raw[j, k].data_ptr(), ws, wsb, stream)
                     calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel()))
-                elif f == snip.NVFP4:                if r in (1, 3, 5):   # both operands of a GEMM are ready
+                elif f == snip.NVFP4:
+                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
+                            self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, None, ws, wsb, stream)
+                    calls.append((L.snip_quantize_nvfp4, args, qcat, bpe * t.numel()))
+                else:
+                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
+                            self.codes[r].data_ptr(), g, ws, wsb, stream)
+                    calls.append((L.snip_quantize_fp8, args, qcat, bpe * t.numel()))
+                if r in (1, 3, 5):   # both operands of a GEMM are ready
                     a, b = r - 1, r
                     M, N, K = {1: (T, l.N, l.K), 3: (T, l.K, l.N), 5: (l.N, l.K, T)}[r]
                     D = {1: self.Y[j], 3: self.dX[j], 5: self.dW[j]}[r]
