@@ -202,17 +202,19 @@ def kernel_source_hash(kind: str) -> str:
 
 
 def ncu_traffic(category: str):
-    """dram bytes per launch recorded in profiles/ for this kernel category,
-    valid only if the kernel sources are unchanged since the capture."""
+    """DRAM bytes per unit of algorithmic work (per FLOP for a GEMM, per
+    algorithmic byte for a quantizer) recorded in profiles/traffic.md for
+    this kernel category, valid only while the kernel sources are unchanged
+    since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
     kind = "gemm" if category.startswith("gemm") else "quant"
     want = kernel_source_hash(kind)
     for line in open(path):
-        m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+]+)\s*\|\s*([0-9.eE+]+)\s*\|", line)
+        m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+-]+)\s*\|", line)
         if m and m.group(1) == category and m.group(2) == want:
-            return {"bytes_per_launch": float(m.group(3)), "units_per_launch": float(m.group(4))}
+            return float(m.group(3))
     return None
 
 
@@ -445,7 +447,8 @@ def run_ours(args, rank, world, local_rank):
     tr = ncu_traffic(dom)
     traffic = None
     if tr is not None:
-        traffic = tr["bytes_per_launch"]
+        # DRAM bytes of one average launch = recorded bytes per unit x units per launch
+        traffic = tr * cat_units[dom] / cat_n[dom]
     roofline = {"bound": "tensor" if dom.startswith("gemm") else "hbm", "kernel": dom,
                 "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"], "frac": d["frac"],
                 "traffic": traffic, "peak_source": f"{peaks['source']} ("
