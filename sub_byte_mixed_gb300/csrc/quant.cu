@@ -202,13 +202,14 @@ __device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, c
 // ------------------------------------------------------------------ a8: statistics
 // One pass: ||A||^2, the squared errors of NVFP4 and FP8 quantization under
 // the tensor's rounding, and the expected SR squared error on both grids,
-// sum (hi-|y|)(|y|-lo) q^2.  For round-to-nearest it is formed from the
-// rounding error d and the grid step h as |d| h - d^2 (equal to it because
-// |d| = min(y-lo, hi-y)), accumulated per block as p*sum(|d| h) - sum(d^2)
-// over the unsaturated elements; for stochastic rounding from the fraction f
-// of the step, f (1-f) h^2, times p^2 per block.  The sums need no bit
-// exactness, so they use fused multiply-adds; per-thread sums are fp32 (a few
-// hundred elements), per-CTA and final sums fp64.
+// sum (hi-|y|)(|y|-lo) q^2.  With d the signed distance from |y| (clamped to
+// the grid's top) to a neighbouring grid value and h = hi - lo, that product
+// is |d| (h - |d|) for either neighbour.  Round to nearest supplies the
+// nearest neighbour, accumulated per block as p*sum(|d| h) - sum(d^2) over
+// the unsaturated elements; stochastic rounding supplies the neighbour it
+// picked, summed in units of the step and scaled by p^2 per block.  The sums
+// need no bit exactness, so they use fused multiply-adds; per-thread sums are
+// fp32 (a few hundred elements), per-CTA and final sums fp64.
 
 // Bit pattern of the E2M1 grid step at y >= 0: 0.5 below 2, then 2^(E-1).
 __device__ __forceinline__ uint32_t e2m1_step_bits(float y) {
@@ -219,16 +220,22 @@ __device__ __forceinline__ uint32_t e2m1_step_bits(float y) {
 // Statistics of one 16-element block: squares of the values, the squared
 // errors of NVFP4 (block scale bs) and FP8 (tensor scale s8) quantization
 // under rounding RND, and the expected SR variance on both grids.
+// CF = 1 / 0 also returns the block's NVFP4 / FP8 codes (packed as by
+// nvfp4_encode16 / fp8_encode16) from the same conversions, except where
+// that format's scale is special (bs.special, special8): there the caller
+// encodes.  CF = -1: statistics only.
 struct BlockStats {
   float x2, e4, e8, v4, v8;
 };
-template <int RND>
+template <int CF, int RND>
 __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
-                                                    float s8, float inv8, bool special8) {
+                                                    float s8, float inv8, bool special8, uint4& codes) {
   float bx2 = 0.f, be4 = 0.f, be8 = 0.f, A4 = 0.f, B4 = 0.f, A8 = 0.f, B8 = 0.f;
+  uint32_t cw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
     bx2 = fmaf(v[i], v[i], fmaf(v[i + 1], v[i + 1], bx2));
+    const uint32_t sg0 = __float_as_uint(v[i]) >> 31, sg1 = __float_as_uint(v[i + 1]) >> 31;
     // ---------------- NVFP4
     if (bs.special) {
 #pragma unroll
@@ -239,7 +246,9 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       }
     } else if (RND == 0) {
       const float y0 = __fmul_rn(v[i], bs.inv), y1 = __fmul_rn(v[i + 1], bs.inv);
-      const float2 q = e2m1x2_decode(e2m1x2_rn(y0, y1));
+      const uint32_t byte = e2m1x2_rn(y0, y1);
+      if (CF == 1) cw[i >> 3] |= byte << (4 * (i & 7));
+      const float2 q = e2m1x2_decode(byte);
       const float d0 = fmaf(q.x, bs.p, -v[i]), d1 = fmaf(q.y, bs.p, -v[i + 1]);
       be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
       const float m0 = fabsf(y0) < 6.0f ? d0 : 0.0f, m1 = fabsf(y1) < 6.0f ? d1 : 0.0f;
@@ -248,18 +257,15 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       B4 = fmaf(m0, m0, fmaf(m1, m1, B4));
     } else {
       const float y0 = __fmul_rn(fabsf(v[i]), bs.inv), y1 = __fmul_rn(fabsf(v[i + 1]), bs.inv);
-      const uint32_t b0 = e2m1_sr_base(y0), b1 = e2m1_sr_base(y1);
-      const uint32_t c0 = e2m1_sr_from_base(b0, uhalf(u, i)), c1 = e2m1_sr_from_base(b1, uhalf(u, i + 1));
-      const float2 q = e2m1x2_decode(c0 | (c1 << 4));
+      const uint32_t mag = e2m1_sr(y0, uhalf(u, i)) | (e2m1_sr(y1, uhalf(u, i + 1)) << 4);
+      if (CF == 1) cw[i >> 3] |= (mag | (sg0 << 3) | (sg1 << 7)) << (4 * (i & 7));
+      const float2 q = e2m1x2_decode(mag);
       const float d0 = fmaf(q.x, bs.p, -fabsf(v[i])), d1 = fmaf(q.y, bs.p, -fabsf(v[i + 1]));
       be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
-      // f (1-f) h^2 with f the 22 bits below E2M1's mantissa bit
-      const float f0 = __fmul_rn((float)(b0 & 0x3fffffu), 2.384185791015625e-07f);
-      const float f1 = __fmul_rn((float)(b1 & 0x3fffffu), 2.384185791015625e-07f);
+      const float c0 = q.x - fminf(y0, 6.0f), c1 = q.y - fminf(y1, 6.0f);
       const float h0 = __uint_as_float(e2m1_step_bits(y0)), h1 = __uint_as_float(e2m1_step_bits(y1));
-      const float w0 = y0 < 6.0f ? fmaf(-f0, f0, f0) * (h0 * h0) : 0.0f;
-      const float w1 = y1 < 6.0f ? fmaf(-f1, f1, f1) * (h1 * h1) : 0.0f;
-      A4 += w0 + w1;
+      A4 = fmaf(fabsf(c0), h0 - fabsf(c0), A4);
+      A4 = fmaf(fabsf(c1), h1 - fabsf(c1), A4);
     }
     // ---------------- FP8
     if (special8) {
@@ -271,7 +277,9 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       }
     } else if (RND == 0) {
       const float y0 = __fmul_rn(v[i], inv8), y1 = __fmul_rn(v[i + 1], inv8);
-      const float2 q = e4m3x2_decode(e4m3x2_rn_sat(y0, y1));
+      const uint32_t pair = e4m3x2_rn_sat(y0, y1);
+      if (CF == 0) cw[i >> 2] |= pair << (8 * (i & 3));
+      const float2 q = e4m3x2_decode(pair);
       const float d0 = fmaf(q.x, s8, -v[i]), d1 = fmaf(q.y, s8, -v[i + 1]);
       be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
       const float m0 = fabsf(y0) < 448.0f ? d0 : 0.0f, m1 = fabsf(y1) < 448.0f ? d1 : 0.0f;
@@ -280,27 +288,27 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       B8 = fmaf(m0, m0, fmaf(m1, m1, B8));
     } else {
       const float y0 = __fmul_rn(fabsf(v[i]), inv8), y1 = __fmul_rn(fabsf(v[i + 1]), inv8);
-      const uint32_t b0 = e4m3_sr_base(y0), b1 = e4m3_sr_base(y1);
-      const uint32_t c0 = e4m3_sr_from_base(b0, uhalf(u, i)), c1 = e4m3_sr_from_base(b1, uhalf(u, i + 1));
-      const float2 q = e4m3x2_decode(c0 | (c1 << 8));
+      const uint32_t mag = e4m3_sr(y0, uhalf(u, i)) | (e4m3_sr(y1, uhalf(u, i + 1)) << 8);
+      if (CF == 0) cw[i >> 2] |= (mag | (sg0 << 7) | (sg1 << 15)) << (8 * (i & 3));
+      const float2 q = e4m3x2_decode(mag);
       const float d0 = fmaf(q.x, s8, -fabsf(v[i])), d1 = fmaf(q.y, s8, -fabsf(v[i + 1]));
       be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
-      const float f0 = __fmul_rn((float)(b0 & 0xfffffu), 9.5367431640625e-07f);   // 2^-20
-      const float f1 = __fmul_rn((float)(b1 & 0xfffffu), 9.5367431640625e-07f);
+      const float c0 = q.x - fminf(y0, 448.0f), c1 = q.y - fminf(y1, 448.0f);
       const float h0 = __uint_as_float(e4m3_step_bits(y0)), h1 = __uint_as_float(e4m3_step_bits(y1));
-      const float w0 = y0 < 448.0f ? fmaf(-f0, f0, f0) * (h0 * h0) : 0.0f;
-      const float w1 = y1 < 448.0f ? fmaf(-f1, f1, f1) * (h1 * h1) : 0.0f;
-      A8 += w0 + w1;
+      A8 = fmaf(fabsf(c0), h0 - fabsf(c0), A8);
+      A8 = fmaf(fabsf(c1), h1 - fabsf(c1), A8);
     }
   }
   float bv4, bv8;
-  if (RND == 1) {   // fractions were in units of the step: scale by p^2 and s^2
+  if (RND == 1) {   // sums were in units of the scale: multiply by p^2 and s^2
     bv4 = bs.special ? 0.0f : A4 * (bs.p * bs.p);
     bv8 = special8 ? 0.0f : A8 * (s8 * s8);
   } else {          // p * sum(|d| h) - sum(d^2) over unsaturated elements
     bv4 = bs.special ? 0.0f : fmaf(bs.p, A4, -B4);
     bv8 = special8 ? 0.0f : fmaf(s8, A8, -B8);
-  }  BlockStats r;
+  }
+  codes = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  BlockStats r;
   r.x2 = bx2;
   r.e4 = be4;
   r.e8 = be8;
@@ -384,27 +392,42 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     if (RND == 1 && real) sr_bits16(e0, p.seed, p.stream_id, u);
     BlockScale bs;
     if (FMT == 1 || STATS) bs = nvfp4_block_scale(amax16_bits(a, b), g4, six_g);
-    if (STATS && real) {
-      const BlockStats st = stats_block16<RND>(v, bs, u, s8, inv8, special8);
-      sx2 += st.x2;
-      e4 += st.e4;
-      e8 += st.e8;
-      v4 += st.v4;
-      v8 += st.v8;
+    uint4 c = make_uint4(0u, 0u, 0u, 0u);   // FP8: 16 codes; NVFP4: .x, .y
+    if (STATS) {
+      // the codes come out of the statistics' own conversions
+      if (real) {
+        const BlockStats st = stats_block16<FMT, RND>(v, bs, u, s8, inv8, special8, c);
+        sx2 += st.x2;
+        e4 += st.e4;
+        e8 += st.e8;
+        v4 += st.v4;
+        v8 += st.v8;
+        if (FMT == 1 && bs.special) {
+          const uint2 e = nvfp4_encode16<RND>(v, bs, u);
+          c.x = e.x;
+          c.y = e.y;
+        }
+        if (FMT == 0 && special8) c = fp8_encode16<RND>(v, inv8, u);
+      }
+    } else if (FMT == 1) {
+      const uint2 e = nvfp4_encode16<RND>(v, bs, u);
+      c.x = e.x;
+      c.y = e.y;
+    } else {
+      c = fp8_encode16<RND>(v, inv8, u);
     }
     if (FMT == 1) {
-      const uint2 c = nvfp4_encode16<RND>(v, bs, u);
+      const uint2 c2 = make_uint2(c.x, c.y);
       if (LAYOUT == 0) {
         if (!real) continue;
-        *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.out_cols >> 1) + (int64_t)kb * 8) = c;
+        *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.out_cols >> 1) + (int64_t)kb * 8) = c2;
         p.scales[(int64_t)r * (p.out_cols >> 4) + kb] = (uint8_t)bs.s;
       } else {
-        *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.ocp >> 1) + (int64_t)kb * 8) = c;
+        *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.ocp >> 1) + (int64_t)kb * 8) = c2;
         p.scales[mma_scale_offset(r, kb, p.ocp)] = (uint8_t)bs.s;
       }
-      if (ERR && real && p.block_err) p.block_err[(int64_t)r * (p.out_cols >> 4) + kb] = nvfp4_block_err(v, c, bs.p);
+      if (ERR && real && p.block_err) p.block_err[(int64_t)r * (p.out_cols >> 4) + kb] = nvfp4_block_err(v, c2, bs.p);
     } else {
-      const uint4 c = fp8_encode16<RND>(v, inv8, u);
       const int64_t pitch = LAYOUT == 0 ? p.out_cols : p.ocp;
       if (LAYOUT == 0 && !real) continue;
       *reinterpret_cast<uint4*>(p.codes + (int64_t)r * pitch + (int64_t)kb * 16) = c;
@@ -565,7 +588,8 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     if (RND == 1) sr_bits16(e0, p.seed, p.stream_id, u);
     const BlockScale bs = nvfp4_block_scale(amax16_bits(a, b), g, six_g);
-    const BlockStats st = stats_block16<RND>(v, bs, u, s8, inv8, special8);
+    uint4 unused;
+    const BlockStats st = stats_block16<-1, RND>(v, bs, u, s8, inv8, special8, unused);
     sx2 += st.x2;
     e4 += st.e4;
     e8 += st.e8;

@@ -56,9 +56,11 @@ __device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
 // Carry form: with the value's 20 dropped mantissa bits (exponent-aligned
 // fixed point below 2^-6), adding (65535 - u16) << 4 carries into the kept
 // bits exactly when u16 < floor(frac * 2^16).  Returns the magnitude code.
+// Below 2^-6 the fixed point is floor(y * 2^29), read off the mantissa of
+// 2^-6 + y rounded toward zero (its ulp is 2^-29).
 __device__ __forceinline__ uint32_t e4m3_sr_base(float y) {
   return y >= 0.015625f ? __float_as_uint(y) - 0x3C000000u                 // (exp-120)<<23 | mantissa
-                        : (uint32_t)__fmul_rn(y, 536870912.0f);           // y * 2^29, < 2^23
+                        : __float_as_uint(__fadd_rz(y, 0.015625f)) - 0x3C800000u;
 }
 __device__ __forceinline__ uint32_t e4m3_sr_from_base(uint32_t base, uint32_t u16) {
   const uint32_t code = (base + ((65535u - u16) << 4)) >> 20;
@@ -89,9 +91,11 @@ __device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
 // 22 bits below E2M1's one mantissa bit (fixed point 2^-23 below 1) plus
 // (65535 - u16) << 6 carry into the kept bits exactly when the rule rounds
 // up.  Returns the magnitude code 0..7.
+// Below 1 the fixed point is floor(y * 2^23), the mantissa of 1 + y rounded
+// toward zero.
 __device__ __forceinline__ uint32_t e2m1_sr_base(float y) {
   return y >= 1.0f ? __float_as_uint(y) - 0x3F000000u                     // 2*(exp-126) | m1, << 22
-                   : (uint32_t)__fmul_rn(y, 8388608.0f);                  // y * 2^23, < 2^23
+                   : __float_as_uint(__fadd_rz(y, 1.0f)) - 0x3F800000u;
 }
 __device__ __forceinline__ uint32_t e2m1_sr_from_base(uint32_t base, uint32_t u16) {
   const uint32_t code = (base + ((65535u - u16) << 6)) >> 22;
