@@ -293,7 +293,8 @@ __global__ void __launch_bounds__(448, 1)
 // then arrive on the leader's sf_ready barrier.  Each CTA's tensor memory must
 // hold the scales of all 256 B rows (each CTA's tensor core multiplies its A
 // rows by the whole B tile); holding only its own 128 gives wrong products.
-// The library routes FP8 GEMMs here; NVFP4 runs faster on the one-CTA kernel.
+// The library routes every GEMM with at least one full wave of 256 x 256
+// tiles here (both formats); smaller ones run on the one-CTA kernel.
 template <int FMT>
 struct Gemm2Cfg {
   static constexpr int BM = 128, BN = 256, BNC = 128, KB = 128;
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(448, 1)
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(sfready(stage), 0));
+          if (lane == 0) mbar_arrive_remote(mapa_shared(sfready(stage), 0));
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(448, 1)
         if (rd == C::EPI_COLS / C::EPI_ROUND - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
+          if (lane == 0) mbar_arrive_remote(mapa_shared(tempty(acc), 0));
         }
         if (row < p.M) {
 #pragma unroll
@@ -643,14 +644,19 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT>, ta, tb, tsa, tsb, p);
 }
 
-// Measured on GB300 at the Llama-7B shapes: NVFP4 runs faster on the one-CTA
-// kernel (its scale staging per stage is the same work either way, and the
-// pair's cross-CTA handshakes cost more than its halved B traffic saves),
-// FP8 faster on the CTA pair (about 10-15%).
+// Measured on GB300 at the Llama-7B shapes, the CTA pair beats the one-CTA
+// kernel by about 11% (NVFP4) and 2-15% (FP8).  GEMMs too small to give
+// every SM pair a 256 x 256 tile run on the one-CTA kernel's 128 x 256
+// tiles instead, which spreads them over twice as many SMs.
 cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,
                         int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st) {
-  if (fmt == 1) return launch_gemm_cfg<1, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
-  return launch_gemm_pair<0>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
+  const bool pair = pair_tiles >= num_sms / 2;
+  if (fmt == 1)
+    return pair ? launch_gemm_pair<1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
+                : launch_gemm_cfg<1, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  return pair ? launch_gemm_pair<0>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
+              : launch_gemm_cfg<0, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
 }
 
 }  // namespace snip

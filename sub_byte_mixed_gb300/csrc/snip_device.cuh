@@ -208,8 +208,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t ra
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Arrive on a barrier of another CTA of the cluster.  The release is at CTA
+// scope: what the arrive publishes is tensor-memory traffic (ordered by
+// tcgen05.wait + tcgen05.fence::before_thread_sync on this side and
+// tcgen05.fence::after_thread_sync on the waiting side), not generic memory.
+// A cluster-scope release here costs about a microsecond per arrive, which
+// made a per-stage handshake the bottleneck of the CTA-pair GEMM.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

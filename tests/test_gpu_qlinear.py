@@ -66,6 +66,22 @@ def test_standalone_gemm_identity_and_random(snip, fmt, code):
                f"{fmt} random")
 
 
+@pytest.mark.parametrize("fmt,code", FMTS)
+@pytest.mark.parametrize("shape", [(2048, 2560, 512), (2000, 2512, 272)])
+def test_gemm_cta_pair_path(snip, fmt, code, shape):
+    """GEMMs with at least one 256 x 256 tile per SM pair run on the CTA-pair
+    kernel: an exact wave of tiles and a ragged one (M, N not multiples of
+    256, K not a multiple of the 256-element stage)."""
+    M, N, K = shape
+    assert ((M + 255) // 256) * ((N + 255) // 256) >= torch.cuda.get_device_properties(0).multi_processor_count // 2
+    X = inputs.normal_bf16((M, K), 1.0, 6, 1)
+    W = inputs.normal_bf16((N, K), 0.02, 6, 2)
+    q = snip.quantize_nvfp4 if code == 1 else snip.quantize_fp8
+    D = snip.gemm(code, q(X.cuda(), layout=snip.MMA), q(W.cuda(), layout=snip.MMA), M, N, K).cpu().numpy()
+    gemm_close(D, oracle.gemm_tn(oracle.quantize(fmt, X).dequant(), oracle.quantize(fmt, W).dequant()),
+               f"{fmt} pair {shape}")
+
+
 def test_gemm_into_strided_output(snip):
     X = inputs.normal_bf16((128, 256), 1.0, 4, 1)
     W = inputs.normal_bf16((64, 256), 1.0, 4, 2)
