@@ -74,14 +74,6 @@ __global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restri
   }
 }
 
-// Bit pattern of the E4M3 grid step at y >= 0: 2^(E-3) for y in the normal
-// range (E = floor(log2 y)), 2^-9 below it (signed max: zero and tiny y have
-// exponent fields below 3).
-__device__ __forceinline__ uint32_t e4m3_step_bits(float y) {
-  const int32_t e = (int32_t)(__float_as_uint(y) & 0x7f800000u) - 0x01800000;
-  return (uint32_t)max(e, 0x3b000000);
-}
-
 // Byte offset of the E4M3 scale of (row r, block kb) in the MMA layout.
 __device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64_t ocp) {
   const int64_t chunk = (r >> 7) * (ocp >> 6) + (kb >> 2);
@@ -202,19 +194,23 @@ __device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, c
 // ------------------------------------------------------------------ a8: statistics
 // One pass: ||A||^2, the squared errors of NVFP4 and FP8 quantization under
 // the tensor's rounding, and the expected SR squared error on both grids,
-// sum (hi-|y|)(|y|-lo) q^2.  With d the signed distance from |y| (clamped to
-// the grid's top) to a neighbouring grid value and h = hi - lo, that product
-// is |d| (h - |d|) for either neighbour.  Round to nearest supplies the
-// nearest neighbour, accumulated per block as p*sum(|d| h) - sum(d^2) over
-// the unsaturated elements; stochastic rounding supplies the neighbour it
-// picked, summed in units of the step and scaled by p^2 per block.  The sums
+// sum (hi-|y|)(|y|-lo) q^2.  With c the signed distance from |y| (clamped to
+// the grid's top, where the product is 0) to a neighbouring grid value and
+// h = hi - lo, that product is |c| (h - |c|) for either neighbour: the
+// rounding of the pass (nearest, or the stochastic pick) supplies the
+// neighbour.  It is summed in units of the scale and multiplied by p^2 (s^2)
+// per block.  The sums
 // need no bit exactness, so they use fused multiply-adds; per-thread sums are
 // fp32 (a few hundred elements), per-CTA and final sums fp64.
 
-// Bit pattern of the E2M1 grid step at y >= 0: 0.5 below 2, then 2^(E-1).
-__device__ __forceinline__ uint32_t e2m1_step_bits(float y) {
-  const int32_t e = (int32_t)(__float_as_uint(y) & 0x7f800000u) - 0x00800000;
-  return (uint32_t)max(e, 0x3f000000);
+// Grid steps as floats: twice the E2M1 step at |y| (0.5 below 2, then
+// 2^(E-1)) and eight times the E4M3 step at |y| (2^(E-3) from 2^-6 up,
+// 2^-9 below), from the exponent field of y.
+__device__ __forceinline__ float e2m1_step_x2(float y) {
+  return fmaxf(__uint_as_float(__float_as_uint(y) & 0x7f800000u), 1.0f);
+}
+__device__ __forceinline__ float e4m3_step_x8(float y) {
+  return fmaxf(__uint_as_float(__float_as_uint(y) & 0x7f800000u), 0.015625f);
 }
 
 // Statistics of one 16-element block: squares of the values, the squared
@@ -230,7 +226,7 @@ struct BlockStats {
 template <int CF, int RND>
 __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
                                                     float s8, float inv8, bool special8, uint4& codes) {
-  float bx2 = 0.f, be4 = 0.f, be8 = 0.f, A4 = 0.f, B4 = 0.f, A8 = 0.f, B8 = 0.f;
+  float bx2 = 0.f, be4 = 0.f, be8 = 0.f, A4 = 0.f, A8 = 0.f;
   uint32_t cw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
@@ -244,28 +240,30 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
         const float d = fmaf(q, bs.p, -v[i + k]);
         be4 = fmaf(d, d, be4);
       }
-    } else if (RND == 0) {
-      const float y0 = __fmul_rn(v[i], bs.inv), y1 = __fmul_rn(v[i + 1], bs.inv);
-      const uint32_t byte = e2m1x2_rn(y0, y1);
-      if (CF == 1) cw[i >> 3] |= byte << (4 * (i & 7));
-      const float2 q = e2m1x2_decode(byte);
-      const float d0 = fmaf(q.x, bs.p, -v[i]), d1 = fmaf(q.y, bs.p, -v[i + 1]);
-      be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
-      const float m0 = fabsf(y0) < 6.0f ? d0 : 0.0f, m1 = fabsf(y1) < 6.0f ? d1 : 0.0f;
-      A4 = fmaf(fabsf(m0), __uint_as_float(e2m1_step_bits(fabsf(y0))), A4);
-      A4 = fmaf(fabsf(m1), __uint_as_float(e2m1_step_bits(fabsf(y1))), A4);
-      B4 = fmaf(m0, m0, fmaf(m1, m1, B4));
     } else {
-      const float y0 = __fmul_rn(fabsf(v[i]), bs.inv), y1 = __fmul_rn(fabsf(v[i + 1]), bs.inv);
-      const uint32_t mag = e2m1_sr(y0, uhalf(u, i)) | (e2m1_sr(y1, uhalf(u, i + 1)) << 4);
-      if (CF == 1) cw[i >> 3] |= (mag | (sg0 << 3) | (sg1 << 7)) << (4 * (i & 7));
-      const float2 q = e2m1x2_decode(mag);
-      const float d0 = fmaf(q.x, bs.p, -fabsf(v[i])), d1 = fmaf(q.y, bs.p, -fabsf(v[i + 1]));
+      float y0, y1;
+      float2 q;
+      if (RND == 0) {
+        y0 = __fmul_rn(v[i], bs.inv);
+        y1 = __fmul_rn(v[i + 1], bs.inv);
+        const uint32_t byte = e2m1x2_rn(y0, y1);
+        if (CF == 1) cw[i >> 3] |= byte << (4 * (i & 7));
+        q = e2m1x2_decode(byte);
+      } else {
+        y0 = __fmul_rn(fabsf(v[i]), bs.inv);
+        y1 = __fmul_rn(fabsf(v[i + 1]), bs.inv);
+        const uint32_t mag = e2m1_sr(y0, uhalf(u, i)) | (e2m1_sr(y1, uhalf(u, i + 1)) << 4);
+        if (CF == 1) cw[i >> 3] |= (mag | (sg0 << 3) | (sg1 << 7)) << (4 * (i & 7));
+        q = e2m1x2_decode(mag);
+      }
+      // RTN: signed q, y; SR: magnitudes
+      const float d0 = fmaf(q.x, bs.p, RND ? -fabsf(v[i]) : -v[i]);
+      const float d1 = fmaf(q.y, bs.p, RND ? -fabsf(v[i + 1]) : -v[i + 1]);
       be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
-      const float c0 = q.x - fminf(y0, 6.0f), c1 = q.y - fminf(y1, 6.0f);
-      const float h0 = __uint_as_float(e2m1_step_bits(y0)), h1 = __uint_as_float(e2m1_step_bits(y1));
-      A4 = fmaf(fabsf(c0), h0 - fabsf(c0), A4);
-      A4 = fmaf(fabsf(c1), h1 - fabsf(c1), A4);
+      const float c0 = fabsf(fabsf(q.x) - fminf(fabsf(y0), 6.0f));
+      const float c1 = fabsf(fabsf(q.y) - fminf(fabsf(y1), 6.0f));
+      A4 = fmaf(c0, fmaf(e2m1_step_x2(y0), 0.5f, -c0), A4);
+      A4 = fmaf(c1, fmaf(e2m1_step_x2(y1), 0.5f, -c1), A4);
     }
     // ---------------- FP8
     if (special8) {
@@ -275,38 +273,34 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
         const float d = fmaf(q, s8, -v[i + k]);
         be8 = fmaf(d, d, be8);
       }
-    } else if (RND == 0) {
-      const float y0 = __fmul_rn(v[i], inv8), y1 = __fmul_rn(v[i + 1], inv8);
-      const uint32_t pair = e4m3x2_rn_sat(y0, y1);
-      if (CF == 0) cw[i >> 2] |= pair << (8 * (i & 3));
-      const float2 q = e4m3x2_decode(pair);
-      const float d0 = fmaf(q.x, s8, -v[i]), d1 = fmaf(q.y, s8, -v[i + 1]);
-      be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
-      const float m0 = fabsf(y0) < 448.0f ? d0 : 0.0f, m1 = fabsf(y1) < 448.0f ? d1 : 0.0f;
-      A8 = fmaf(fabsf(m0), __uint_as_float(e4m3_step_bits(fabsf(y0))), A8);
-      A8 = fmaf(fabsf(m1), __uint_as_float(e4m3_step_bits(fabsf(y1))), A8);
-      B8 = fmaf(m0, m0, fmaf(m1, m1, B8));
     } else {
-      const float y0 = __fmul_rn(fabsf(v[i]), inv8), y1 = __fmul_rn(fabsf(v[i + 1]), inv8);
-      const uint32_t mag = e4m3_sr(y0, uhalf(u, i)) | (e4m3_sr(y1, uhalf(u, i + 1)) << 8);
-      if (CF == 0) cw[i >> 2] |= (mag | (sg0 << 7) | (sg1 << 15)) << (8 * (i & 3));
-      const float2 q = e4m3x2_decode(mag);
-      const float d0 = fmaf(q.x, s8, -fabsf(v[i])), d1 = fmaf(q.y, s8, -fabsf(v[i + 1]));
+      float y0, y1;
+      float2 q;
+      if (RND == 0) {
+        y0 = __fmul_rn(v[i], inv8);
+        y1 = __fmul_rn(v[i + 1], inv8);
+        const uint32_t pair = e4m3x2_rn_sat(y0, y1);
+        if (CF == 0) cw[i >> 2] |= pair << (8 * (i & 3));
+        q = e4m3x2_decode(pair);
+      } else {
+        y0 = __fmul_rn(fabsf(v[i]), inv8);
+        y1 = __fmul_rn(fabsf(v[i + 1]), inv8);
+        const uint32_t mag = e4m3_sr(y0, uhalf(u, i)) | (e4m3_sr(y1, uhalf(u, i + 1)) << 8);
+        if (CF == 0) cw[i >> 2] |= (mag | (sg0 << 7) | (sg1 << 15)) << (8 * (i & 3));
+        q = e4m3x2_decode(mag);
+      }
+      const float d0 = fmaf(q.x, s8, RND ? -fabsf(v[i]) : -v[i]);
+      const float d1 = fmaf(q.y, s8, RND ? -fabsf(v[i + 1]) : -v[i + 1]);
       be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
-      const float c0 = q.x - fminf(y0, 448.0f), c1 = q.y - fminf(y1, 448.0f);
-      const float h0 = __uint_as_float(e4m3_step_bits(y0)), h1 = __uint_as_float(e4m3_step_bits(y1));
-      A8 = fmaf(fabsf(c0), h0 - fabsf(c0), A8);
-      A8 = fmaf(fabsf(c1), h1 - fabsf(c1), A8);
+      const float c0 = fabsf(fabsf(q.x) - fminf(fabsf(y0), 448.0f));
+      const float c1 = fabsf(fabsf(q.y) - fminf(fabsf(y1), 448.0f));
+      A8 = fmaf(c0, fmaf(e4m3_step_x8(y0), 0.125f, -c0), A8);
+      A8 = fmaf(c1, fmaf(e4m3_step_x8(y1), 0.125f, -c1), A8);
     }
   }
-  float bv4, bv8;
-  if (RND == 1) {   // sums were in units of the scale: multiply by p^2 and s^2
-    bv4 = bs.special ? 0.0f : A4 * (bs.p * bs.p);
-    bv8 = special8 ? 0.0f : A8 * (s8 * s8);
-  } else {          // p * sum(|d| h) - sum(d^2) over unsaturated elements
-    bv4 = bs.special ? 0.0f : fmaf(bs.p, A4, -B4);
-    bv8 = special8 ? 0.0f : fmaf(s8, A8, -B8);
-  }
+  // the variances were summed in units of the scale
+  const float bv4 = bs.special ? 0.0f : A4 * (bs.p * bs.p);
+  const float bv8 = special8 ? 0.0f : A8 * (s8 * s8);
   codes = make_uint4(cw[0], cw[1], cw[2], cw[3]);
   BlockStats r;
   r.x2 = bx2;
@@ -375,8 +369,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
   float sx2 = 0.f, e4 = 0.f, e8 = 0.f, v4 = 0.f, v8 = 0.f;
-  for (uint32_t seg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); seg < total; seg += wstride) {
-    const uint32_t r = seg / spr, kb = (seg - r * spr) * 32 + lane;
+  // segment -> (row, segment in row), stepped without a division per iteration
+  const uint32_t seg0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const uint32_t wq = wstride / spr, wr = wstride - wq * spr;
+  uint32_t r = seg0 / spr, sr = seg0 - r * spr;
+  for (uint32_t seg = seg0; seg < total; seg += wstride, r += wq, sr += wr) {
+    if (sr >= spr) { sr -= spr; ++r; }
+    const uint32_t kb = sr * 32 + lane;
     if (kb >= bpr) continue;
     const bool real = r < p.out_rows && (int64_t)kb * 16 < p.out_cols;
     uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
@@ -577,8 +576,13 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
   float sx2 = 0.f, e4 = 0.f, e8 = 0.f, v4 = 0.f, v8 = 0.f;
-  for (uint32_t seg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); seg < total; seg += wstride) {
-    const uint32_t r = seg / spr, kb = (seg - r * spr) * 32 + lane;
+  // segment -> (row, segment in row), stepped without a division per iteration
+  const uint32_t seg0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const uint32_t wq = wstride / spr, wr = wstride - wq * spr;
+  uint32_t r = seg0 / spr, sr = seg0 - r * spr;
+  for (uint32_t seg = seg0; seg < total; seg += wstride, r += wq, sr += wr) {
+    if (sr >= spr) { sr -= spr; ++r; }
+    const uint32_t kb = sr * 32 + lane;
     if (kb >= bpr) continue;
     const int64_t e0 = (int64_t)r * p.cols + (int64_t)kb * 16;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + e0);
