@@ -218,6 +218,25 @@ def ncu_traffic(category: str):
     return None
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(ms: float, world: int, device: str) -> float:
+    """The slowest rank's time per step (every rank gets it)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Replicas: every rank runs the whole step on its own block, so the job
+    does world x the flops of one step in the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- our arm
 
 class Step:
@@ -413,10 +432,7 @@ def run_ours(args, rank, world, local_rank):
             cat_ms[cat] = cat_ms.get(cat, 0.0) + t
             cat_units[cat] = cat_units.get(cat, 0.0) + units
             cat_n[cat] = cat_n.get(cat, 0) + 1
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, "cuda")
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
@@ -427,7 +443,7 @@ def run_ours(args, rank, world, local_rank):
         return
     flops = cfg.flops_fwd_bwd() if not layers else sum(
         6 * cfg.T * l.K * l.N for l in cfg.linears if l.name in layers)
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms)
     peaks = measured_peaks()
     breakdown = {}
     for cat in cat_ms:
