@@ -50,7 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="llama-7b-block")
-    ap.add_argument("--plan", default="mix", choices=["mix", "nvfp4", "fp8"])
+    ap.add_argument("--plan", default="mix", choices=["mix", "nvfp4", "fp8", "snip"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -67,7 +67,8 @@ def parse_args(argv=None):
 def workload(args):
     from sub_byte_mixed_gb300 import inputs
     cfg = inputs.BLOCKS[args.config]
-    if args.plan == "mix":
+    if args.plan in ("mix", "snip"):
+        # "snip" starts from the seeded plan; run_ours replaces it with SNIP's selection
         plan = inputs.seeded_plan(cfg, cfg.fp4_target, seed=0)
     else:
         plan = inputs.all_plan(inputs.FMT_NVFP4 if args.plan == "nvfp4" else inputs.FMT_FP8)
@@ -85,6 +86,9 @@ def config_json(cfg, plan, args):
         "l2": "inputs larger than L2 (no flush)",
         "rounding": "RTN forward, SR (Philox4x32-10, 16 bits/elem) backward",
         "stats": "SNIP statistics of X, W (forward rounding) and dY (dgrad rounding) fused into their row-block quantizations",
+        "plan_source": ("SNIP selection from one step's statistics (snip_plan_select, FP4-FLOP target "
+                        f"{cfg.fp4_target})") if args.plan == "snip" else
+                       ("seeded plan at the FP4-FLOP target" if args.plan == "mix" else "uniform"),
     }
 
 
@@ -394,6 +398,17 @@ def run_ours(args, rank, world, local_rank):
     cfg, plan = workload(args)
     layers = [x for x in args.layers.split(",") if x]
     step = Step(cfg, plan, snip, "cuda", layers)
+    if args.plan == "snip" and layers:
+        raise SystemExit("--plan snip selects formats for the whole block; it cannot be combined with --layers")
+    if args.plan == "snip":
+        # SNIP's loop: statistics of one step feed the layer-wise selection (C ABI, host code)
+        step.run()
+        torch.cuda.synchronize()
+        c8, c4 = snip.snip_plan_costs(step.raw.cpu().numpy())
+        flops = [6.0 * cfg.T * l.K * l.N for l in cfg.linears]
+        plan, _, _ = snip.snip_plan_select(flops, c8, c4, cfg.fp4_target)
+        del step
+        step = Step(cfg, plan, snip, "cuda", layers)
     torch.cuda.synchronize()
     ncalls = len(step.calls)
     sampler = ClockSampler(local_rank) if rank == 0 and not args.profile_run else None

@@ -303,6 +303,43 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
 /* Host helper: derive ratios and sqrt(3) flags from a host copy of raw_out. */
 snip_status snip_stats_finalize(const double* raw_host, snip_stats* out);
 
+/* ---------------------------------------------------------------- plan selection (host) */
+
+/* Per-layer cost of each format for SNIP's plan selection ("SNIP" (Pan et
+ * al.), Abstract and Figure 2: statistics collected during training feed an
+ * ILP over layer-wise precision).  The pages do not print the forward loss
+ * divergence or backward weight divergence, so the cost of format f for a
+ * layer is a proxy from the statistics pass: the relative squared
+ * quantization error of its three operand tensors under their own rounding,
+ * cost_f = sum over X, W, dY of ||Q_f(A) - A||^2 / ||A||^2 (a tensor with
+ * ||A|| = 0 adds 0).
+ * raw_host (host): n_layers x 3 x SNIP_STATS_NVALS doubles, the raw statistics
+ * of X, W and dY of each layer in that order (as written by snip_qlinear_fwd's
+ * and snip_qlinear_bwd's stats_out or by snip_quant_stats).
+ * cost_fp8 / cost_nvfp4 (host, n_layers doubles) receive the costs.
+ * Errors: SNIP_ERR_INVALID_ARG (null pointers, n_layers < 0),
+ * SNIP_ERR_NONFINITE (a non-finite statistic).  No device work. */
+snip_status snip_plan_costs(int n_layers, const double* raw_host, double* cost_fp8, double* cost_nvfp4);
+
+/* SNIP's layer-wise format choice: among all FP8/NVFP4 assignments whose FP4
+ * share of the GEMM FLOPs is at least fp4_fraction, the one with the least
+ * total cost (sum of cost_nvfp4 over FP4 layers and cost_fp8 over the rest) --
+ * the knapsack-like ILP of "SNIP" (Abstract; Figure 3 for the efficiency
+ * measure), solved exactly by dynamic programming over the FP4 FLOPs in units
+ * of their greatest common divisor.
+ * flops (host, n_layers doubles): each layer's fwd+bwd GEMM FLOPs (6 T K N),
+ * integral and <= 2^53.  The FP4 FLOPs required are ceil(fp4_fraction * U -
+ * 1e-9) units of U in total (fp4_fraction in [0, 1]).  Ties go to FP8 for a
+ * layer and to the smaller FP4 share for the set.
+ * fmt_out (host, n_layers ints) receives snip_format values; fp4_fraction_out
+ * and cost_out (host, nullable) the achieved FP4 FLOP share and total cost.
+ * Errors: SNIP_ERR_INVALID_ARG (null pointers, a fraction outside [0, 1],
+ * non-integral, negative or too large FLOPs, non-finite costs),
+ * SNIP_ERR_SHAPE (the table n_layers x (U + 1) exceeds 2^28 cells).  The
+ * pages' extension of the ILP to pipeline-parallel stages is not built. */
+snip_status snip_plan_select(int n_layers, const double* flops, const double* cost_fp8, const double* cost_nvfp4,
+                             double fp4_fraction, int* fmt_out, double* fp4_fraction_out, double* cost_out);
+
 #ifdef __cplusplus
 }
 #endif

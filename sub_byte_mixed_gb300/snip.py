@@ -33,7 +33,7 @@ EXPORTS = (
     "snip_quantize_nvfp4", "snip_quantize_fp8",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
-    "snip_quant_stats", "snip_quantize_stats", "snip_stats_finalize",
+    "snip_quant_stats", "snip_quantize_stats", "snip_stats_finalize", "snip_plan_costs", "snip_plan_select",
 )
 
 
@@ -86,6 +86,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_quantize_stats": (i32, [i32, vp, i64, i64, i32, u64, u64, vp, i32, vp, vp, vp, vp, sz, vp]),
         "snip_quant_stats": (i32, [vp, i64, i64, i32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "snip_stats_finalize": (i32, [vp, ctypes.POINTER(SnipStats)]),
+        "snip_plan_costs": (i32, [i32, vp, vp, vp]),
+        "snip_plan_select": (i32, [i32, vp, vp, vp, ctypes.c_double, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -191,6 +193,35 @@ def snip_stats_finalize(raw_host) -> SnipStats:
     out = SnipStats()
     _call("snip_stats_finalize", arr, ctypes.byref(out))
     return out
+
+
+def snip_plan_costs(raw_host):
+    """raw_host: n_layers x 3 x STATS_NVALS (X, W, dY statistics of each layer)
+    -> (cost_fp8, cost_nvfp4) lists."""
+    import numpy as np
+    raw = np.ascontiguousarray(raw_host, dtype=np.float64).reshape(-1, 3, STATS_NVALS)
+    n = raw.shape[0]
+    c8 = np.zeros(n, dtype=np.float64)
+    c4 = np.zeros(n, dtype=np.float64)
+    _call("snip_plan_costs", n, raw.ctypes.data, c8.ctypes.data, c4.ctypes.data)
+    return c8, c4
+
+
+def snip_plan_select(flops, cost_fp8, cost_nvfp4, fp4_fraction):
+    """-> (formats per layer, achieved FP4 FLOP share, total cost)."""
+    import numpy as np
+    f = np.ascontiguousarray(flops, dtype=np.float64)
+    c8 = np.ascontiguousarray(cost_fp8, dtype=np.float64)
+    c4 = np.ascontiguousarray(cost_nvfp4, dtype=np.float64)
+    n = f.shape[0]
+    if c8.shape != (n,) or c4.shape != (n,):
+        raise ValueError("flops, cost_fp8 and cost_nvfp4 need one entry per layer")
+    fmt = np.zeros(max(n, 1), dtype=np.int32)
+    frac = ctypes.c_double()
+    cost = ctypes.c_double()
+    _call("snip_plan_select", n, f.ctypes.data, c8.ctypes.data, c4.ctypes.data, float(fp4_fraction),
+          fmt.ctypes.data, ctypes.byref(frac), ctypes.byref(cost))
+    return [int(v) for v in fmt[:n]], frac.value, cost.value
 
 
 # ----------------------------------------------------------------------------- torch conveniences
