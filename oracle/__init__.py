@@ -86,6 +86,12 @@ def lib():
         L.oracle_quantize_nvfp4.restype = i32
         L.oracle_dequant_nvfp4.argtypes = [c_u8p, c_u8p, ctypes.c_float, i64, i64, c_dp]
         L.oracle_dequant_nvfp4.restype = None
+        L.oracle_e8m0_value.argtypes = [i32]; L.oracle_e8m0_value.restype = ctypes.c_double
+        L.oracle_mxfp4_shared_exp.argtypes = [ctypes.c_float]; L.oracle_mxfp4_shared_exp.restype = i32
+        L.oracle_quantize_mxfp4.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_u8p, c_u8p]
+        L.oracle_quantize_mxfp4.restype = i32
+        L.oracle_dequant_mxfp4.argtypes = [c_u8p, c_u8p, i64, i64, c_dp]
+        L.oracle_dequant_mxfp4.restype = None
         L.oracle_quantize_fp8.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp, c_u8p, c_fp]
         L.oracle_quantize_fp8.restype = i32
         L.oracle_dequant_fp8.argtypes = [c_u8p, ctypes.c_float, i64, c_dp]
@@ -191,6 +197,22 @@ class NVFP4:
         return out
 
 
+class MXFP4:
+    """An MXFP4 tensor of shape (rows, cols): codes rows x cols/2 (low nibble =
+    even column), E8M0 scales rows x cols/32; no tensor scale."""
+
+    def __init__(self, codes, scales, rows, cols):
+        self.codes, self.scales = codes, scales
+        self.rows, self.cols = rows, cols
+        self.g = 1.0
+
+    def dequant(self) -> np.ndarray:
+        out = np.empty((self.rows, self.cols), dtype=np.float64)
+        lib().oracle_dequant_mxfp4(_ptr(self.codes, ctypes.c_uint8), _ptr(self.scales, ctypes.c_uint8),
+                                   self.rows, self.cols, _ptr(out, ctypes.c_double))
+        return out
+
+
 class FP8:
     """An FP8 E4M3 tensor of shape (rows, cols) with one fp32 scale s."""
 
@@ -243,7 +265,27 @@ def quantize_fp8(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: i
     return FP8(codes, s.value, OR, OC)
 
 
+def quantize_mxfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0) -> MXFP4:
+    """MXFP4 quantization (OCP Microscaling v1.0: 32 E2M1 values per E8M0
+    power-of-two scale) of a bf16 (rows, cols) tensor; orientation and random
+    bits as for NVFP4."""
+    b = _bits(x)
+    rows, cols = b.shape
+    OR, OC = (rows, cols) if orient == 0 else (cols, rows)
+    codes = np.zeros((OR, OC // 2), dtype=np.uint8)
+    scales = np.zeros((OR, OC // 32), dtype=np.uint8)
+    st = lib().oracle_quantize_mxfp4(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
+                                     _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+    if st == 1:
+        raise NonFiniteInput("non-finite input")
+    if st != 0:
+        raise ValueError(f"shape error: blocks of 32 need the blocked dim % 32 == 0 (got {OR}x{OC})")
+    return MXFP4(codes, scales, OR, OC)
+
+
 def quantize(fmt: str, x, orient=0, rnd=RTN, seed=0, stream_id=0):
+    if fmt == "mxfp4":
+        return quantize_mxfp4(x, orient, rnd, seed, stream_id)
     if fmt == "nvfp4":
         return quantize_nvfp4(x, orient, rnd, seed, stream_id)
     if fmt == "fp8":

@@ -315,6 +315,89 @@ void oracle_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales, float g,
 }
 
 /* ------------------------------------------------------------------------ */
+/* MXFP4 (OCP Microscaling Formats specification v1.0, the format the FP4    */
+/* study of "FP4 all the way" weighs against NVFP4 on block size and scale  */
+/* format): 32 E2M1 elements share one E8M0 scale, a power of two           */
+/* 2^(code - 127); there is no tensor scale.                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Value of an E8M0 code: 2^(code - 127); code 255 is NaN. */
+double oracle_e8m0_value(int code) {
+    if (code == 255) return NAN;
+    double v = 1.0;
+    for (int k = 127; k < code; ++k) v *= 2.0;
+    for (int k = code; k < 127; ++k) v /= 2.0;
+    return v;
+}
+
+/* The block's shared exponent: floor(log2(amax)) less the largest E2M1
+ * exponent (2, as 6 = 1.5 x 2^2), clamped to E8M0's [-127, 127]; an
+ * all-zero block takes -127. */
+int oracle_mxfp4_shared_exp(float amax) {
+    if (amax == 0.0f) return -127;
+    double a = amax;
+    int e = 0;
+    while (a >= 2.0) { a /= 2.0; ++e; }
+    while (a < 1.0) { a *= 2.0; --e; }
+    int se = e - 2;
+    if (se < -127) se = -127;
+    if (se > 127) se = 127;
+    return se;
+}
+
+/* Quantize a bf16 rows x cols tensor to MXFP4: per block of 32 along the
+ * blocked dim, se = oracle_mxfp4_shared_exp(block amax), scale code se + 127,
+ * y = |x| * 2^-se (one fp32 multiplication by that power of two), code =
+ * sign | E2M1(y) rounded as for NVFP4 (nearest, or stochastic with the same
+ * random bits per source element).  Orientation and return values as for
+ * NVFP4; codes OR x OC/2 bytes, scales OR x OC/32 bytes; needs OC % 32 == 0. */
+int oracle_quantize_mxfp4(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
+                          uint64_t seed, uint64_t stream_id, uint8_t* codes, uint8_t* scales) {
+    int64_t OR = orient == 0 ? rows : cols, OC = orient == 0 ? cols : rows;
+    if (OC % 32 != 0) return 2;
+    float amax;
+    if (oracle_amax_bf16(x, rows * cols, &amax)) return 1;
+    int64_t nb = OC / 32;
+    for (int64_t i = 0; i < OR; ++i) {
+        for (int64_t b = 0; b < nb; ++b) {
+            float xs[32];
+            uint64_t es[32];
+            float ab = 0.0f;
+            for (int k = 0; k < 32; ++k) {
+                es[k] = (uint64_t)src_index(orient, rows, cols, i, b * 32 + k);
+                xs[k] = bf16_to_float(x[es[k]]);
+                if (fabsf(xs[k]) > ab) ab = fabsf(xs[k]);
+            }
+            int se = oracle_mxfp4_shared_exp(ab);
+            scales[i * nb + b] = (uint8_t)(se + 127);
+            float inv = (float)oracle_e8m0_value(127 - se);   /* 2^-se, exact in fp32 */
+            for (int k = 0; k < 32; ++k) {
+                int sign = signbit(xs[k]) ? 8 : 0;
+                float y = fabsf(xs[k]) * inv;
+                int mag = rnd == 0 ? oracle_e2m1_rtn(y)
+                                   : oracle_e2m1_sr(y, oracle_sr_bits(seed, stream_id, es[k]));
+                int code = sign | mag;
+                int64_t col = b * 32 + k;
+                uint8_t* byte = &codes[i * (OC / 2) + col / 2];
+                if ((col & 1) == 0) *byte = (uint8_t)((*byte & 0xf0) | code);
+                else *byte = (uint8_t)((*byte & 0x0f) | (code << 4));
+            }
+        }
+    }
+    return 0;
+}
+
+/* Dequantize MXFP4 (OR x OC) into fp64: value(code) * 2^(scale - 127). */
+void oracle_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t OR, int64_t OC, double* out) {
+    for (int64_t i = 0; i < OR; ++i)
+        for (int64_t k = 0; k < OC; ++k) {
+            uint8_t byte = codes[i * (OC / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            out[i * OC + k] = oracle_e2m1_value(code) * oracle_e8m0_value(scales[i * (OC / 32) + k / 32]);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* FP8 E4M3 with one fp32 scale per tensor                                   */
 /* ------------------------------------------------------------------------ */
 
