@@ -59,7 +59,8 @@ def test_saturation_and_ties():
 
 
 def test_error_bound_and_orientation():
-    x = (torch.randn(64, 96) * torch.exp(torch.randn(64, 96) * 2)).to(torch.bfloat16)
+    g = torch.Generator().manual_seed(4)
+    x = (torch.randn(64, 96, generator=g) * torch.exp(torch.randn(64, 96, generator=g) * 2)).to(torch.bfloat16)
     q = oracle.quantize_mxfp4(x)
     xf = x.float().numpy().astype(np.float64)
     scale = np.repeat(np.array([[math.ldexp(1.0, int(c) - 127) for c in r] for r in q.scales]), 32, axis=1)
@@ -72,20 +73,19 @@ def test_error_bound_and_orientation():
 
 
 def test_stochastic_rounding_unbiased():
-    x = (torch.randn(8, 64) * 3).to(torch.bfloat16)
+    g = torch.Generator().manual_seed(5)
+    x = (torch.randn(8, 64, generator=g) * 3).to(torch.bfloat16)
     xf = x.float().numpy().astype(np.float64)
     n = 300
     acc = np.zeros_like(xf)
-    acc2 = np.zeros_like(xf)
     for seed in range(n):
-        d = oracle.quantize_mxfp4(x, rnd=oracle.SR, seed=seed, stream_id=3).dequant()
-        acc += d
-        acc2 += d * d
+        acc += oracle.quantize_mxfp4(x, rnd=oracle.SR, seed=seed, stream_id=3).dequant()
     mean = acc / n
-    var = np.maximum(acc2 / n - mean * mean, 1e-30)
-    # saturated elements are biased by definition (6 at the top): compare the rest within 5 s.e.
+    # saturated elements are biased by definition (6 at the top); the others' SR error has
+    # variance (hi-y)(y-lo) <= (step/2)^2 with step <= 2 in units of the block scale
     q0 = oracle.quantize_mxfp4(x)
     scale = np.repeat(np.array([[math.ldexp(1.0, int(c) - 127) for c in r] for r in q0.scales]), 32, axis=1)
     unsat = np.abs(xf) / scale < 6.0
-    z = np.abs(mean - xf)[unsat] / np.sqrt(var[unsat] / n)
-    assert np.mean(z < 5.0) > 0.999
+    assert np.all(np.abs(mean - xf)[unsat] <= 5.0 * scale[unsat] / math.sqrt(n))
+    # and the mean error over all unsaturated elements is far below one step
+    assert abs(np.mean(((mean - xf) / scale)[unsat])) < 0.02
