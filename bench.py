@@ -38,6 +38,7 @@ METRIC = "qlinear fwd+bwd TFLOP/s (NVFP4/FP8 mix) & quantizer GB/s, % of GB300 r
 UNIT = "TFLOP/s"
 SCALES_BYTES_PER_ELEM = 2                        # amax pass: read
 NVFP4_BYTES_PER_ELEM = 2 + 0.5 + 1 / 16          # read + codes + block scales
+MXFP4_BYTES_PER_ELEM = 2 + 0.5 + 1 / 32          # read + codes + E8M0 block scales
 FP8_BYTES_PER_ELEM = 2 + 1                       # read + codes
 STATS_BYTES_PER_ELEM = 2                         # read
 FP4_OVER_BF16, FP8_OVER_BF16 = 13.5 / 2.25, 4.5 / 2.25   # nominal dense ratios
@@ -50,7 +51,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="llama-7b-block")
-    ap.add_argument("--plan", default="mix", choices=["mix", "nvfp4", "fp8", "snip"])
+    ap.add_argument("--plan", default="mix", choices=["mix", "nvfp4", "fp8", "mxfp4", "snip"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -71,7 +72,7 @@ def workload(args):
         # "snip" starts from the seeded plan; run_ours replaces it with SNIP's selection
         plan = inputs.seeded_plan(cfg, cfg.fp4_target, seed=0)
     else:
-        plan = inputs.all_plan(inputs.FMT_NVFP4 if args.plan == "nvfp4" else inputs.FMT_FP8)
+        plan = inputs.all_plan({"nvfp4": inputs.FMT_NVFP4, "fp8": inputs.FMT_FP8, "mxfp4": inputs.FMT_MXFP4}[args.plan])
     return cfg, plan
 
 
@@ -80,7 +81,8 @@ def config_json(cfg, plan, args):
     return {
         "workload": f"{cfg.name}: T={cfg.T} hidden={cfg.hidden} inter={cfg.inter} kv_out={cfg.kv_out}; "
                     f"7 linears fwd+dgrad+wgrad+stats",
-        "plan": {n: ("nvfp4" if f == inputs.FMT_NVFP4 else "fp8") for n, f in zip(inputs.LAYER_NAMES, plan)},
+        "plan": {n: {inputs.FMT_NVFP4: "nvfp4", inputs.FMT_FP8: "fp8", inputs.FMT_MXFP4: "mxfp4"}[f]
+                 for n, f in zip(inputs.LAYER_NAMES, plan)},
         "fp4_flop_fraction": round(cfg.fp4_flop_fraction(plan), 4),
         "flop_per_step": cfg.flops_fwd_bwd(),
         "l2": "inputs larger than L2 (no flush)",
@@ -283,10 +285,10 @@ class Step:
             scp = {l.x_id: self.sc[j, 0].data_ptr(), "W": self.sc[j, 1].data_ptr(), "dY": self.sc[j, 2].data_ptr()}
             sid = 8 * j
             rnd = [0, 0, 1, 1, 1, 1]
-            qcat = "quant_nvfp4" if f == snip.NVFP4 else "quant_fp8"
-            gcat = "gemm_nvfp4" if f == snip.NVFP4 else "gemm_fp8"
-            bpe = NVFP4_BYTES_PER_ELEM if f == snip.NVFP4 else FP8_BYTES_PER_ELEM
-            fo = 4 if f == snip.NVFP4 else 8          # byte offset of g (NVFP4) or s (FP8) in a slot
+            fname = {snip.NVFP4: "nvfp4", snip.FP8: "fp8", snip.MXFP4: "mxfp4"}[f]
+            qcat, gcat = "quant_" + fname, "gemm_" + fname
+            bpe = {snip.NVFP4: NVFP4_BYTES_PER_ELEM, snip.FP8: FP8_BYTES_PER_ELEM, snip.MXFP4: MXFP4_BYTES_PER_ELEM}[f]
+            fo = 8 if f == snip.FP8 else 4            # byte offset of s (FP8) or g (NVFP4; MXFP4: unused) in a slot
             for name in (l.x_id, "W", "dY"):
                 t = src[name]
                 calls.append((L.snip_tensor_scales, (t.data_ptr(), t.numel(), scp[name], ws, wsb, stream), "scales",
@@ -299,13 +301,17 @@ class Step:
                     # row-block quantization with SNIP's statistics of the same tensor in one pass
                     k = r
                     args = (f, t.data_ptr(), rows, cols, rnd[r], 0, sid + r, scp[name], snip.MMA,
-                            self.codes[r].data_ptr(), self.scales[r].data_ptr() if f == snip.NVFP4 else None,
+                            self.codes[r].data_ptr(), self.scales[r].data_ptr() if f != snip.FP8 else None,
                             self.raw[j, k].data_ptr(), ws, wsb, stream)
                     calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel()))
                 elif f == snip.NVFP4:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, None, ws, wsb, stream)
                     calls.append((L.snip_quantize_nvfp4, args, qcat, bpe * t.numel()))
+                elif f == snip.MXFP4:
+                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, snip.MMA,
+                            self.codes[r].data_ptr(), self.scales[r].data_ptr(), ws, wsb, stream)
+                    calls.append((L.snip_quantize_mxfp4, args, qcat, bpe * t.numel()))
                 else:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), g, ws, wsb, stream)
@@ -314,10 +320,10 @@ class Step:
                     a, b = r - 1, r
                     M, N, K = {1: (T, l.N, l.K), 3: (T, l.K, l.N), 5: (l.N, l.K, T)}[r]
                     D = {1: self.Y[j], 3: self.dX[j], 5: self.dW[j]}[r]
-                    sa = self.scales[a].data_ptr() if f == snip.NVFP4 else None
-                    sb = self.scales[b].data_ptr() if f == snip.NVFP4 else None
-                    ga = scp[roles(l)[a][0]] + fo
-                    gb = scp[roles(l)[b][0]] + fo
+                    sa = self.scales[a].data_ptr() if f != snip.FP8 else None
+                    sb = self.scales[b].data_ptr() if f != snip.FP8 else None
+                    ga = scp[roles(l)[a][0]] + fo if f != snip.MXFP4 else None
+                    gb = scp[roles(l)[b][0]] + fo if f != snip.MXFP4 else None
                     args = (f, self.codes[a].data_ptr(), sa, ga, self.codes[b].data_ptr(), sb, gb, M, N, K,
                             D.data_ptr(), D.stride(0), ws, wsb, stream)
                     calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K))
@@ -465,7 +471,7 @@ def run_ours(args, rank, world, local_rank):
         t = cat_ms[cat] / 1e3
         if cat.startswith("gemm"):
             ach = cat_units[cat] / t / 1e12
-            pk = peaks["bf16_sustained"] * (FP4_OVER_BF16 if cat == "gemm_nvfp4" else FP8_OVER_BF16)
+            pk = peaks["bf16_sustained"] * (FP8_OVER_BF16 if cat == "gemm_fp8" else FP4_OVER_BF16)
             breakdown[cat] = {"ms_per_step": cat_ms[cat] / args.steps, "launches_per_step": cat_n[cat] // args.steps,
                               "achieved": ach, "unit": "TFLOP/s", "peak": pk, "frac": ach / pk}
         else:

@@ -65,7 +65,12 @@ typedef enum {
     SNIP_ERR_WORKSPACE = 8          /* workspace missing or too small            */
 } snip_status;
 
-typedef enum { SNIP_FMT_FP8_E4M3 = 0, SNIP_FMT_NVFP4 = 1 } snip_format;
+/* FP8_E4M3: one fp32 tensor scale.  NVFP4: 16 E2M1 values per E4M3 block
+ * scale, plus an fp32 tensor scale ("FP4 all the way", Outline).  MXFP4: 32
+ * E2M1 values per E8M0 power-of-two block scale, no tensor scale (OCP
+ * Microscaling Formats v1.0; the block-size / scale-format alternative that
+ * the FP4 study weighs NVFP4 against). */
+typedef enum { SNIP_FMT_FP8_E4M3 = 0, SNIP_FMT_NVFP4 = 1, SNIP_FMT_MXFP4 = 2 } snip_format;
 typedef enum { SNIP_RTN = 0, SNIP_SR = 1 } snip_round;
 
 /* Orientation of a quantization of a rows x cols tensor.
@@ -77,6 +82,7 @@ typedef enum { SNIP_BLOCKS_ALONG_COLS = 0, SNIP_BLOCKS_ALONG_ROWS = 1 } snip_ori
 /* Output layout of a quantization (OR x OC = output rows x contraction).
  * ROWMAJOR: NVFP4 codes OR x OC/2 bytes (element 2j in bits 0..3 of byte j,
  *           bit 3 of each code the sign), E4M3 scales OR x OC/16 bytes;
+ *           MXFP4 codes the same, E8M0 scales OR x OC/32 bytes;
  *           FP8 codes OR x OC bytes.
  * MMA:      the GEMM operand layout.  Rows are padded to ORp = roundup(OR,256)
  *           and the contraction to OCp = roundup(OC,256) for NVFP4 (128 for
@@ -84,7 +90,10 @@ typedef enum { SNIP_BLOCKS_ALONG_COLS = 0, SNIP_BLOCKS_ALONG_ROWS = 1 } snip_ori
  *           row-major ORp x OCp/2 (NVFP4) or ORp x OCp (FP8).  NVFP4 scales
  *           are stored in 512-byte chunks, one per (128-row group rg, group of
  *           four 16-element blocks kc): chunk index rg*(OCp/64) + kc, and row
- *           r, block kb at byte (r%32)*16 + ((r/32)%4)*4 + kb%4 of its chunk. */
+ *           r, block kb at byte (r%32)*16 + ((r/32)%4)*4 + kb%4 of its chunk.
+ *           MXFP4 codes as NVFP4 (OCp = roundup(OC,256)); its E8M0 scales use
+ *           the same chunk image with 32-element blocks: chunk index
+ *           rg*(OCp/128) + kc, kc a group of four 32-element blocks. */
 typedef enum { SNIP_LAYOUT_ROWMAJOR = 0, SNIP_LAYOUT_MMA = 1 } snip_layout;
 
 /* Index of each quantization inside a qlinear call; the Philox stream id of
@@ -217,6 +226,24 @@ snip_status snip_quantize_fp8(const void* x, int64_t rows, int64_t cols, snip_or
                               snip_layout layout, uint8_t* codes, float* s_out,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- NEXT-2: MXFP4 */
+
+/* MXFP4 quantization (OCP Microscaling Formats v1.0), a format variant of the
+ * FP4 study ("FP4 all the way", Outline: block size and scale format): per
+ * block of 32 along the blocked dim, the E8M0 scale code is
+ * max(exponent field of the block's largest |x| as bf16 - 2, 0), i.e.
+ * 2^(floor(log2 amax) - 2) clamped at 2^-127; elements y = |x| * 2^-(code-127)
+ * are rounded to E2M1 exactly as for NVFP4 (RTN nearest-even saturating at 6,
+ * or SR with the same Philox bits per source element); there is no tensor
+ * scale.  codes/scales sized by snip_quantized_bytes(SNIP_FMT_MXFP4, ...).
+ * The blocked dim (cols for ALONG_COLS, rows for ALONG_ROWS) must be a
+ * multiple of 32 and cols a multiple of 16 (SNIP_ERR_SHAPE).  A non-finite
+ * input raises SNIP_ERR_NONFINITE in the workspace status (outputs
+ * unspecified).  ws as for snip_quantize_nvfp4. */
+snip_status snip_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, snip_orient orient,
+                                snip_round rnd, uint64_t seed, uint64_t stream_id, snip_layout layout,
+                                uint8_t* codes, uint8_t* scales, void* ws, size_t ws_bytes, void* stream);
+
 /* Bytes of the code and scale buffers of a quantization whose output has
  * out_rows rows and contraction out_cols, in `layout`.  Host-only. */
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
@@ -227,9 +254,11 @@ snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t ou
 /* D[m, n] = ga * gb * sum_k A[m, k] B[n, k] for m < M, n < N, fp32 output with
  * row pitch ldd (elements).  A (M rows) and B (N rows) are quantized operands
  * in the MMA layout with contraction K; ga/gb are device floats (NVFP4: the
- * tensor scales g; FP8: the tensor scales s).  NVFP4 uses the tensor cores'
- * block-scaled FP4 MMA with E4M3 block scales; FP8 the E4M3 x E4M3 MMA.
- * Accumulation is fp32.  Needs K % 16 == 0 (SNIP_ERR_SHAPE).
+ * tensor scales g; FP8: the tensor scales s; MXFP4: unused, may be NULL).
+ * NVFP4 uses the tensor cores' block-scaled FP4 MMA with E4M3 block scales
+ * (scale_vec::4X), MXFP4 the same MMA with E8M0 scales (scale_vec::2X), FP8
+ * the E4M3 x E4M3 MMA.  Accumulation is fp32.  Needs K % 16 == 0 (MXFP4:
+ * K % 32 == 0), else SNIP_ERR_SHAPE.
  * ws: at least SNIP_WS_HEADER_BYTES (status word; a timed-out wait raises
  * SNIP_ERR_TIMEOUT there). */
 snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
@@ -257,7 +286,7 @@ size_t snip_qlinear_workspace_size(const snip_plan* plan, int layer, int64_t T, 
 /* Forward (SNIP Figure 5): Y = Q(X) Q(W)^T.  X device T x K bf16, W device
  * N x K bf16, Y device T x N fp32.  Both quantized along K in the layer's
  * format with the plan's rounding (default RTN), stream ids layer*8+{0,1}.
- * T, K, N multiples of 16.  stats_out (device, nullable, 2 x SNIP_STATS_NVALS
+ * T, K, N multiples of 16 (32 for an MXFP4 layer).  stats_out (device, nullable, 2 x SNIP_STATS_NVALS
  * doubles): SNIP's statistics of X then of W (as snip_quant_stats with the
  * forward rounding), computed inside the forward quantization passes. */
 snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, const void* W,

@@ -65,16 +65,21 @@ inline snip_status cuda_status(cudaError_t e) {
 
 // Padded dims of the MMA operand layout.
 inline int64_t mma_rows(int64_t r) { return round_up(r, 256); }
-inline int64_t mma_cols(int snip_fmt, int64_t c) { return round_up(c, snip_fmt == SNIP_FMT_NVFP4 ? 256 : 128); }
+inline bool is_fp4(int snip_fmt) { return snip_fmt == SNIP_FMT_NVFP4 || snip_fmt == SNIP_FMT_MXFP4; }
+inline int64_t mma_cols(int snip_fmt, int64_t c) { return round_up(c, is_fp4(snip_fmt) ? 256 : 128); }
+// kernel format ids: 0 FP8, 1 NVFP4, 2 MXFP4
+inline int kernel_fmt(int snip_fmt) { return snip_fmt == SNIP_FMT_NVFP4 ? 1 : snip_fmt == SNIP_FMT_MXFP4 ? 2 : 0; }
+// elements per block along the blocked dim
+inline int64_t block_elems(int snip_fmt) { return snip_fmt == SNIP_FMT_MXFP4 ? 32 : 16; }
 
 struct OperandBytes { size_t codes, scales; };
 OperandBytes operand_bytes(int fmt, int layout, int64_t orows, int64_t ocols) {
-  if (layout == SNIP_LAYOUT_ROWMAJOR) {
-    if (fmt == SNIP_FMT_NVFP4) return {(size_t)(orows * ocols / 2), (size_t)(orows * ocols / 16)};
-    return {(size_t)(orows * ocols), 0};
+  int64_t r = orows, c = ocols;
+  if (layout != SNIP_LAYOUT_ROWMAJOR) {
+    r = mma_rows(orows);
+    c = mma_cols(fmt, ocols);
   }
-  const int64_t r = mma_rows(orows), c = mma_cols(fmt, ocols);
-  if (fmt == SNIP_FMT_NVFP4) return {(size_t)(r * c / 2), (size_t)(r * c / 16)};
+  if (is_fp4(fmt)) return {(size_t)(r * c / 2), (size_t)(r * c / block_elems(fmt))};
   return {(size_t)(r * c), 0};
 }
 
@@ -116,8 +121,25 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   }
   // an empty output still publishes its tensor scale: the one-CTA row kernel does that
   if (p.orp == 0 || p.ocp == 0) orient = SNIP_BLOCKS_ALONG_COLS;
-  return cuda_status(launch_quant(fmt == SNIP_FMT_NVFP4 ? 1 : 0, p, orient, layout, rnd, block_err != nullptr,
-                                  num_sms, st));
+  if (fmt == SNIP_FMT_MXFP4 && raw_out) {
+    // MXFP4 codes, then the statistics in their own pass (same rounding and random bits)
+    p.scales3 = nullptr;
+    p.raw_out = nullptr;
+    cudaError_t e = launch_quant(2, p, orient, layout, rnd, false, num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    StatsParams sp = {};
+    sp.x = p.x;
+    sp.rows = rows;
+    sp.cols = cols;
+    sp.seed = seed;
+    sp.stream_id = stream_id;
+    sp.scales3 = scales3;
+    sp.partials = ws_at<double>(ws, kOffStatsPartials);
+    sp.counter = ws_at<uint32_t>(ws, kOffStatsCounter);
+    sp.raw_out = raw_out;
+    return cuda_status(launch_stats(sp, rnd, num_sms, st));
+  }
+  return cuda_status(launch_quant(kernel_fmt(fmt), p, orient, layout, rnd, block_err != nullptr, num_sms, st));
 }
 
 // Standalone quantization: tensor scales (unless given) then the quantizer.
@@ -129,7 +151,7 @@ snip_status run_quantize_api(int fmt, const void* x, int64_t rows, int64_t cols,
     float* slot = scale_slot(ws, 0);
     snip_status s = run_scales(x, rows * cols, slot, ws, num_sms, st);
     if (s != SNIP_OK) return s;
-    scale = slot + (fmt == SNIP_FMT_NVFP4 ? 1 : 2);
+    scale = slot + (fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1);   // MXFP4 reads it only to detect non-finite input
   }
   return run_quantize(fmt, x, rows, cols, orient, rnd, seed, stream_id, scale, layout, codes, scales, g_out,
                       block_err, num_sms, st);
@@ -151,8 +173,8 @@ snip_status run_gemm(int fmt, const uint8_t* a_codes, const uint8_t* a_scales, c
   p.kp = mma_cols(fmt, K);
   p.status = ws_at<uint32_t>(ws, kOffStatus);
   p.timeout_ns = kTimeoutNs;
-  return cuda_status(launch_gemm(fmt == SNIP_FMT_NVFP4 ? 1 : 0, a_codes, mma_rows(M), b_codes, mma_rows(N), p,
-                                 num_sms, st));
+  if (fmt == SNIP_FMT_MXFP4) p.ga = p.gb = nullptr;   // no tensor scales
+  return cuda_status(launch_gemm(kernel_fmt(fmt), a_codes, mma_rows(M), b_codes, mma_rows(N), p, num_sms, st));
 }
 
 bool valid_enum(int v, int n) { return v >= 0 && v < n; }
@@ -172,7 +194,7 @@ const char* snip_status_string(snip_status s) {
   switch (s) {
     case SNIP_OK: return "ok";
     case SNIP_ERR_INVALID_ARG: return "invalid argument";
-    case SNIP_ERR_SHAPE: return "shape not supported (dims must be multiples of 16)";
+    case SNIP_ERR_SHAPE: return "shape not supported (dims must be multiples of 16; 32 along MXFP4 blocks)";
     case SNIP_ERR_ALIGN: return "device pointer not 16-byte aligned";
     case SNIP_ERR_NONFINITE: return "input holds a non-finite value";
     case SNIP_ERR_TIMEOUT: return "a kernel wait timed out";
@@ -234,7 +256,7 @@ snip_status snip_tensor_scales(const void* x, int64_t n, float* scales_out, void
 
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
                                  size_t* codes_bytes, size_t* scales_bytes) {
-  if (!valid_enum(fmt, 2) || !valid_enum(layout, 2) || out_rows < 0 || out_cols < 0) return SNIP_ERR_INVALID_ARG;
+  if (!valid_enum(fmt, 3) || !valid_enum(layout, 2) || out_rows < 0 || out_cols < 0) return SNIP_ERR_INVALID_ARG;
   OperandBytes b = operand_bytes(fmt, layout, out_rows, out_cols);
   if (codes_bytes) *codes_bytes = b.codes;
   if (scales_bytes) *scales_bytes = b.scales;
@@ -246,8 +268,11 @@ static snip_status check_quantize_args(int fmt, const void* x, int64_t rows, int
                                        const void* ws, size_t ws_bytes) {
   if (!valid_enum(orient, 2) || !valid_enum(rnd, 2) || !valid_enum(layout, 2)) return SNIP_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0 || !g_out || !codes || (rows * cols > 0 && !x)) return SNIP_ERR_INVALID_ARG;
-  if (fmt == SNIP_FMT_NVFP4 && !scales) return SNIP_ERR_INVALID_ARG;
-  if (cols % 16 != 0 || (orient == SNIP_BLOCKS_ALONG_ROWS && rows % 16 != 0)) return SNIP_ERR_SHAPE;
+  if (is_fp4(fmt) && !scales) return SNIP_ERR_INVALID_ARG;
+  const int64_t be = block_elems(fmt);   // the blocked dim is a whole number of blocks
+  if (cols % 16 != 0 || (orient == SNIP_BLOCKS_ALONG_ROWS && rows % be != 0) ||
+      (orient == SNIP_BLOCKS_ALONG_COLS && cols % be != 0))
+    return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(ws) || (scales && !aligned16(scales))) return SNIP_ERR_ALIGN;
   return SNIP_OK;
@@ -279,20 +304,35 @@ snip_status snip_quantize_fp8(const void* x, int64_t rows, int64_t cols, snip_or
                           nullptr, s_out, nullptr, ws, sms, static_cast<cudaStream_t>(stream));
 }
 
+snip_status snip_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, snip_orient orient, snip_round rnd,
+                                uint64_t seed, uint64_t stream_id, snip_layout layout, uint8_t* codes, uint8_t* scales,
+                                void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  float g_dummy;   // validation only: MXFP4 has no tensor scale to return
+  s = check_quantize_args(SNIP_FMT_MXFP4, x, rows, cols, orient, rnd, layout, codes, scales, &g_dummy, ws, ws_bytes);
+  if (s != SNIP_OK) return s;
+  return run_quantize_api(SNIP_FMT_MXFP4, x, rows, cols, orient, rnd, seed, stream_id, nullptr, layout, codes, scales,
+                          nullptr, nullptr, ws, sms, static_cast<cudaStream_t>(stream));
+}
+
 snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
                       const uint8_t* b_codes, const uint8_t* b_scales, const float* gb, int64_t M, int64_t N,
                       int64_t K, float* D, int64_t ldd, void* ws, size_t ws_bytes, void* stream) {
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
-  if (!valid_enum(fmt, 2) || M < 0 || N < 0 || K < 0 || ldd < N) return SNIP_ERR_INVALID_ARG;
+  if (!valid_enum(fmt, 3) || M < 0 || N < 0 || K < 0 || ldd < N) return SNIP_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return SNIP_OK;
-  if (!a_codes || !b_codes || !ga || !gb || !D) return SNIP_ERR_INVALID_ARG;
-  if (fmt == SNIP_FMT_NVFP4 && (!a_scales || !b_scales)) return SNIP_ERR_INVALID_ARG;
+  if (!a_codes || !b_codes || !D) return SNIP_ERR_INVALID_ARG;
+  if (fmt != SNIP_FMT_MXFP4 && (!ga || !gb)) return SNIP_ERR_INVALID_ARG;
+  if (is_fp4(fmt) && (!a_scales || !b_scales)) return SNIP_ERR_INVALID_ARG;
+  if (fmt == SNIP_FMT_MXFP4 && K % 32 != 0) return SNIP_ERR_SHAPE;
   if (K % 16 != 0 || K == 0 || ldd % 4 != 0) return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < SNIP_WS_HEADER_BYTES) return SNIP_ERR_WORKSPACE;
   if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(D) || !aligned16(ws) ||
-      (fmt == SNIP_FMT_NVFP4 && (!aligned16(a_scales) || !aligned16(b_scales))))
+      (is_fp4(fmt) && (!aligned16(a_scales) || !aligned16(b_scales))))
     return SNIP_ERR_ALIGN;
   return run_gemm(fmt, a_codes, a_scales, ga, b_codes, b_scales, gb, M, N, K, D, ldd, ws, sms,
                   static_cast<cudaStream_t>(stream));
@@ -302,7 +342,7 @@ snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_
 snip_status snip_plan_create(int n_layers, const int* formats, uint64_t seed, snip_plan** out) {
   if (n_layers <= 0 || !formats || !out) return SNIP_ERR_INVALID_ARG;
   for (int i = 0; i < n_layers; ++i)
-    if (!valid_enum(formats[i], 2)) return SNIP_ERR_INVALID_ARG;
+    if (!valid_enum(formats[i], 3)) return SNIP_ERR_INVALID_ARG;
   snip_plan* p = new (std::nothrow) snip_plan;
   if (!p) return SNIP_ERR_INVALID_ARG;
   p->fmt.assign(formats, formats + n_layers);
@@ -366,7 +406,8 @@ QlLayout ql_layout(int fmt, int64_t T, int64_t K, int64_t N, bool bwd) {
 snip_status check_ql(const snip_plan* plan, int layer, int64_t T, int64_t K, int64_t N) {
   if (!plan || layer < 0 || layer >= (int)plan->fmt.size()) return SNIP_ERR_INVALID_ARG;
   if (T <= 0 || K <= 0 || N <= 0) return SNIP_ERR_INVALID_ARG;
-  if (T % 16 || K % 16 || N % 16) return SNIP_ERR_SHAPE;
+  const int64_t be = block_elems(plan->fmt[layer]);   // every dim is blocked by one of the quantizations
+  if (T % be || K % be || N % be) return SNIP_ERR_SHAPE;
   return SNIP_OK;
 }
 }  // namespace
@@ -393,7 +434,7 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
   const uint64_t sid = (uint64_t)layer * 8;
   QlLayout L = ql_layout(fmt, T, K, N, false);
   uint8_t* b = static_cast<uint8_t*>(ws);
-  const int si = fmt == SNIP_FMT_NVFP4 ? 1 : 2;   // which tensor scale the format uses
+  const int si = fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1;   // which tensor scale the format uses (MXFP4: none; g only flags non-finite input)
   float* sx = scale_slot(ws, 0);
   float* sw = scale_slot(ws, 1);
   if ((s = run_scales(X, T * K, sx, ws, sms, st)) != SNIP_OK) return s;
@@ -427,7 +468,7 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
   const uint64_t sid = (uint64_t)layer * 8;
   QlLayout L = ql_layout(fmt, T, K, N, true);
   uint8_t* b = static_cast<uint8_t*>(ws);
-  const int si = fmt == SNIP_FMT_NVFP4 ? 1 : 2;
+  const int si = fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1;
   float* sx = scale_slot(ws, 0);
   float* sw = scale_slot(ws, 1);
   float* sd = scale_slot(ws, 2);
@@ -499,10 +540,10 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
-  if (!valid_enum(fmt, 2) || !raw_out) return SNIP_ERR_INVALID_ARG;
+  if (!valid_enum(fmt, 3) || !raw_out) return SNIP_ERR_INVALID_ARG;
   float g_dummy;   // validation only: g_out is not written by this entry point
   s = check_quantize_args(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, layout, codes,
-                          fmt == SNIP_FMT_NVFP4 ? scales : nullptr, &g_dummy, ws, ws_bytes);
+                          is_fp4(fmt) ? scales : nullptr, &g_dummy, ws, ws_bytes);
   if (s != SNIP_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float* sc = scales_in;
@@ -512,7 +553,7 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
     sc = slot;
   }
   return run_quantize(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, seed, stream_id,
-                      sc + (fmt == SNIP_FMT_NVFP4 ? 1 : 2), layout, codes, scales, nullptr, nullptr, sms, st, sc,
+                      sc + (fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1), layout, codes, scales, nullptr, nullptr, sms, st, sc,
                       raw_out, ws);
 }
 

@@ -41,15 +41,18 @@ struct GemmCfg {
   static constexpr int KB = 128;  // contraction bytes per stage and row (256 FP4 / 128 FP8 elements)
   static constexpr int A_BYTES = BM * KB;
   static constexpr int B_BYTES = BN * KB;
-  static constexpr int SFA_BYTES = FMT ? 2048 : 0;               // 4 chunks of 512 B
-  static constexpr int SFB_BYTES = FMT ? (BN / 128) * 2048 : 0;
+  // block-scale chunks of 512 B per 128 rows and stage: NVFP4 4 (16-element
+  // blocks, 4 per MMA), MXFP4 2 (32-element blocks, 4 per chunk word = 2 MMAs)
+  static constexpr int CH = FMT == 2 ? 2 : 4;
+  static constexpr int SFA_BYTES = FMT ? CH * 512 : 0;
+  static constexpr int SFB_BYTES = FMT ? (BN / 128) * CH * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGES = 4;
   static constexpr int ACC_STAGES = (FMT && BN == 256) ? 1 : 2;
   // tensor-memory columns of one stage's scale factors: per MMA (K=64), A
   // takes 4 columns (128 rows / 32 lanes) and B takes BN/32
-  static constexpr int SFA_COLS = 16;
-  static constexpr int SF_COLS = FMT ? SFA_COLS + 4 * (BN / 32) : 0;
+  static constexpr int SFA_COLS = 4 * CH;
+  static constexpr int SF_COLS = FMT ? SFA_COLS + CH * (BN / 32) : 0;
   static constexpr int SF_TMEM_BASE = ACC_STAGES * BN;
   static constexpr int TMEM_COLS = 512;
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
@@ -63,10 +66,13 @@ struct GemmCfg {
   static constexpr int EPI_ROUND = 64;             // columns per drain round (register budget)
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   // Instruction descriptor.  Block-scaled FP4: A/B type E2M1 (1) in bits 7-9
-  // and 10-12, K-major, N>>3 in bits 17-22, scale type UE4M3 (0) in bit 23,
-  // M>>4 in bits 24-28.  FP8: D type f32 (1) in bits 4-5, A/B type E4M3 (0).
+  // and 10-12, K-major, N>>3 in bits 17-22, scale type in bit 23 (UE4M3 0 for
+  // NVFP4, UE8M0 1 for MXFP4), M>>4 in bits 24-28; MXFP4's scale-factor IDs
+  // (bits 4-5 for B, 29-30 for A) are set per MMA.  FP8: D type f32 (1) in
+  // bits 4-5, A/B type E4M3 (0).
   static constexpr uint32_t IDESC =
-      FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24))
+      FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((FMT == 2 ? 1u : 0u) << 23) |
+             ((uint32_t)(BM >> 4) << 24))
           : ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24));
 };
 
@@ -103,7 +109,7 @@ __global__ void __launch_bounds__(448, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
-  const int64_t sf_chunks_per_group = p.kp >> 6;   // 512-byte scale chunks per 128-row group
+  const int64_t sf_chunks_per_group = p.kp >> (FMT == 2 ? 7 : 6);   // 512-byte scale chunks per 128-row group
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -122,13 +128,13 @@ __global__ void __launch_bounds__(448, 1)
           if (FMT) {
             uint8_t* sSFA = sB + C::B_BYTES;
             uint8_t* sSFB = sSFA + C::SFA_BYTES;
-            bulk_load(smem_u32(sSFA), p.a_scales + ((int64_t)mt * sf_chunks_per_group + kb * 4) * 512, 2048,
-                      full(stage));
+            bulk_load(smem_u32(sSFA), p.a_scales + ((int64_t)mt * sf_chunks_per_group + kb * C::CH) * 512,
+                      C::SFA_BYTES, full(stage));
 #pragma unroll
             for (int nb = 0; nb < BN / 128; ++nb)
-              bulk_load(smem_u32(sSFB + nb * 2048),
-                        p.b_scales + ((int64_t)(nt * (BN / 128) + nb) * sf_chunks_per_group + kb * 4) * 512, 2048,
-                        full(stage));
+              bulk_load(smem_u32(sSFB + nb * C::SFA_BYTES),
+                        p.b_scales + ((int64_t)(nt * (BN / 128) + nb) * sf_chunks_per_group + kb * C::CH) * 512,
+                        C::SFA_BYTES, full(stage));
           }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -163,7 +169,10 @@ __global__ void __launch_bounds__(448, 1)
             const uint64_t adesc = smem_desc(sA + 32 * k, 16, 1024, 2);
             const uint64_t bdesc = smem_desc(sB + 32 * k, 16, 1024, 2);
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            if (FMT) tc_mma_nvf4(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * (BN / 32), accum);
+            if (FMT == 1) tc_mma_nvf4(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * (BN / 32), accum);
+            else if (FMT == 2)   // chunk word k/2, byte pair 2*(k%2) as the scale-factor ID of A and B
+              tc_mma_mxf4(d_tmem, adesc, bdesc, C::IDESC | ((2u * (k & 1)) << 4) | ((2u * (k & 1)) << 29),
+                          sf + 4 * (k >> 1), sf + C::SFA_COLS + (k >> 1) * (BN / 32), accum);
             else tc_mma_f8(d_tmem, adesc, bdesc, C::IDESC, accum);
           }
           tc_commit(empty(stage));
@@ -179,8 +188,8 @@ __global__ void __launch_bounds__(448, 1)
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
     }
   } else if (warp < C::EPI_WARP0) {
-    // ---------------------------------------------------------- scale staging (NVFP4)
-    if constexpr (FMT == 1) {
+    // ---------------------------------------------------------- scale staging (block-scaled formats)
+    if constexpr (FMT >= 1) {
       const int q = warp & 3;   // TMEM lane quadrant this warp may access
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -194,21 +203,23 @@ __global__ void __launch_bounds__(448, 1)
           // lane l of every quadrant holds row l of each 512-byte chunk: columns 4k..4k+3 of the
           // A scales of MMA k, then per MMA k the BN/128 chunks of the B scales
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < C::CH; ++k) {
             const uint4 t = *reinterpret_cast<const uint4*>(sSFA + 512 * k + 16 * lane);
             v[4 * k] = t.x; v[4 * k + 1] = t.y; v[4 * k + 2] = t.z; v[4 * k + 3] = t.w;
           }
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < C::CH; ++k)
 #pragma unroll
             for (int nb = 0; nb < BN / 128; ++nb) {
-              const uint4 t = *reinterpret_cast<const uint4*>(sSFB + 2048 * nb + 512 * k + 16 * lane);
+              const uint4 t = *reinterpret_cast<const uint4*>(sSFB + C::SFA_BYTES * nb + 512 * k + 16 * lane);
               const int o = C::SFA_COLS + k * (BN / 32) + 4 * nb;
               v[o] = t.x; v[o + 1] = t.y; v[o + 2] = t.z; v[o + 3] = t.w;
             }
           const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + C::SF_TMEM_BASE + stage * C::SF_COLS;
 #pragma unroll
           for (int c = 0; c < C::SF_COLS / 16; ++c) tmem_st_32x32b_x16(taddr + 16 * c, v + 16 * c);
+          if constexpr (C::SF_COLS % 16 != 0)
+            tmem_st_32x32b_x8(taddr + C::SF_COLS / 16 * 16, v + C::SF_COLS / 16 * 16);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
@@ -221,7 +232,7 @@ __global__ void __launch_bounds__(448, 1)
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;                          // TMEM lane quadrant this warp may access
     const int half = (warp - C::EPI_WARP0) >> 2;     // which BN/2 columns it drains
-    const float alpha = __fmul_rn(*p.ga, *p.gb);
+    const float alpha = p.ga ? __fmul_rn(*p.ga, *p.gb) : 1.0f;   // MXFP4 has no tensor scales
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
@@ -299,14 +310,15 @@ template <int FMT>
 struct Gemm2Cfg {
   static constexpr int BM = 128, BN = 256, BNC = 128, KB = 128;
   static constexpr int A_BYTES = BM * KB, B_BYTES = BNC * KB;
-  static constexpr int SFA_BYTES = FMT ? 2048 : 0;
-  static constexpr int SFB_BYTES = FMT ? 4096 : 0;
+  static constexpr int CH = FMT == 2 ? 2 : 4;      // 512-byte scale chunks per 128 rows and stage
+  static constexpr int SFA_BYTES = FMT ? CH * 512 : 0;
+  static constexpr int SFB_BYTES = FMT ? 2 * CH * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int STAGES = FMT ? 5 : 6;
+  static constexpr int STAGES = FMT == 1 ? 5 : 6;
   static constexpr int ACC_STAGES = FMT ? 1 : 2;
-  static constexpr int SFA_COLS = 16;
-  static constexpr int SFB_COLS_K = 8;                    // scale columns of B per MMA (256 rows)
-  static constexpr int SF_COLS = FMT ? SFA_COLS + 4 * SFB_COLS_K : 0;
+  static constexpr int SFA_COLS = 4 * CH;
+  static constexpr int SFB_COLS_K = 8;                    // scale columns of B per chunk (256 rows)
+  static constexpr int SF_COLS = FMT ? SFA_COLS + CH * SFB_COLS_K : 0;
   static constexpr int SF_TMEM_BASE = ACC_STAGES * BN;
   static constexpr int TMEM_COLS = 512;
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
@@ -316,7 +328,8 @@ struct Gemm2Cfg {
   static constexpr int SF_WARPS = 4, EPI_WARP0 = 6, EPI_WARPS = 8, EPI_COLS = BN / 2, EPI_ROUND = 64;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   static constexpr uint32_t IDESC =
-      FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24))
+      FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((FMT == 2 ? 1u : 0u) << 23) |
+             ((uint32_t)(256 >> 4) << 24))
           : ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24));
 };
 
@@ -381,10 +394,11 @@ __global__ void __launch_bounds__(448, 1)
             uint8_t* sSFB = sSFA + C::SFA_BYTES;
             mbar_arrive_expect_tx(sffull(stage), C::SFA_BYTES + C::SFB_BYTES);
             const int64_t ga = 2 * mt + rank;
-            tma_load_2d(smem_u32(sSFA), &tmSFA, 0, (int32_t)(8 * (ga * groups_k + kb)), sffull(stage));
+            constexpr int R = C::SFA_BYTES / 256;   // 256-byte rows of one 128-row group's stage scales
+            tma_load_2d(smem_u32(sSFA), &tmSFA, 0, (int32_t)(R * (ga * groups_k + kb)), sffull(stage));
             for (int h = 0; h < 2; ++h)
-              tma_load_2d(smem_u32(sSFB + 2048 * h), &tmSFB, 0, (int32_t)(8 * ((2 * nt + h) * groups_k + kb)),
-                          sffull(stage));
+              tma_load_2d(smem_u32(sSFB + C::SFA_BYTES * h), &tmSFB, 0,
+                          (int32_t)(R * ((2 * nt + h) * groups_k + kb)), sffull(stage));
           }
           if (rank == 0) mbar_arrive_expect_tx(full(stage), 2 * (C::A_BYTES + C::B_BYTES));
           const uint32_t leader_full = mapa_shared(full(stage), 0);
@@ -419,7 +433,11 @@ __global__ void __launch_bounds__(448, 1)
             const uint64_t adesc = smem_desc(sA + 32 * k, 16, 1024, 2);
             const uint64_t bdesc = smem_desc(sB + 32 * k, 16, 1024, 2);
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            if (FMT) tc_mma_nvf4_pair(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * C::SFB_COLS_K, accum);
+            if (FMT == 1)
+              tc_mma_nvf4_pair(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * C::SFB_COLS_K, accum);
+            else if (FMT == 2)
+              tc_mma_mxf4_pair(d_tmem, adesc, bdesc, C::IDESC | ((2u * (k & 1)) << 4) | ((2u * (k & 1)) << 29),
+                               sf + 4 * (k >> 1), sf + C::SFA_COLS + (k >> 1) * C::SFB_COLS_K, accum);
             else tc_mma_f8_pair(d_tmem, adesc, bdesc, C::IDESC, accum);
           }
           tc_commit_pair_mc(empty(stage), 0x3);
@@ -434,8 +452,8 @@ __global__ void __launch_bounds__(448, 1)
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
     }
   } else if (warp < C::EPI_WARP0) {
-    // ---------------------------------------------------------- scale staging (both CTAs, NVFP4)
-    if constexpr (FMT == 1) {
+    // ---------------------------------------------------------- scale staging (both CTAs, block-scaled formats)
+    if constexpr (FMT >= 1) {
       const int q = warp & 3;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -446,21 +464,23 @@ __global__ void __launch_bounds__(448, 1)
           const uint8_t* sSFB = sSFA + C::SFA_BYTES;
           uint32_t v[C::SF_COLS];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < C::CH; ++k) {
             const uint4 t = *reinterpret_cast<const uint4*>(sSFA + 512 * k + 16 * lane);
             v[4 * k] = t.x; v[4 * k + 1] = t.y; v[4 * k + 2] = t.z; v[4 * k + 3] = t.w;
           }
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < C::CH; ++k)
 #pragma unroll
             for (int nb = 0; nb < C::SFB_COLS_K / 4; ++nb) {
-              const uint4 t = *reinterpret_cast<const uint4*>(sSFB + 2048 * nb + 512 * k + 16 * lane);
+              const uint4 t = *reinterpret_cast<const uint4*>(sSFB + C::SFA_BYTES * nb + 512 * k + 16 * lane);
               const int o = C::SFA_COLS + k * C::SFB_COLS_K + 4 * nb;
               v[o] = t.x; v[o + 1] = t.y; v[o + 2] = t.z; v[o + 3] = t.w;
             }
           const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + C::SF_TMEM_BASE + stage * C::SF_COLS;
 #pragma unroll
           for (int c = 0; c < C::SF_COLS / 16; ++c) tmem_st_32x32b_x16(taddr + 16 * c, v + 16 * c);
+          if constexpr (C::SF_COLS % 16 != 0)
+            tmem_st_32x32b_x8(taddr + C::SF_COLS / 16 * 16, v + C::SF_COLS / 16 * 16);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
@@ -473,7 +493,7 @@ __global__ void __launch_bounds__(448, 1)
     // ---------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     const int half = (warp - C::EPI_WARP0) >> 2;
-    const float alpha = __fmul_rn(*p.ga, *p.gb);
+    const float alpha = p.ga ? __fmul_rn(*p.ga, *p.gb) : 1.0f;   // MXFP4 has no tensor scales
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
@@ -589,14 +609,15 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
   return cudaGetLastError();
 }
 
-// 2-D byte view of an MMA-layout scale buffer: rows of 256 bytes, loaded 8 rows
-// (one 2 KB slab = 128 rows x 256 contraction elements) at a time.
-static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes) {
+// 2-D byte view of an MMA-layout scale buffer: rows of 256 bytes, loaded
+// box_rows rows (one 128-row group's scales for 256 contraction elements:
+// 2 KB for NVFP4, 1 KB for MXFP4) at a time.
+static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {256u, (cuuint64_t)(bytes / 256)};
   cuuint64_t strides[1] = {256u};
-  cuuint32_t box[2] = {256u, 8u};
+  cuuint32_t box[2] = {256u, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -620,7 +641,9 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   memset(&tsb, 0, sizeof tsb);
   if (!make_code_map(&ta, a_codes, a_rows, row_bytes, C::BM) || !make_code_map(&tb, b_codes, b_rows, row_bytes, C::BNC))
     return cudaErrorInvalidValue;
-  if (FMT && (!make_scale_map(&tsa, p.a_scales, a_rows * p.kp / 16) || !make_scale_map(&tsb, p.b_scales, b_rows * p.kp / 16)))
+  const int64_t sf_div = FMT == 2 ? 32 : 16;   // elements per scale byte
+  if (FMT && (!make_scale_map(&tsa, p.a_scales, a_rows * p.kp / sf_div, C::SFA_BYTES / 256) ||
+              !make_scale_map(&tsb, p.b_scales, b_rows * p.kp / sf_div, C::SFA_BYTES / 256)))
     return cudaErrorInvalidValue;
   p.num_k_stages = (int)(row_bytes / C::KB);
   p.v8 = (reinterpret_cast<uintptr_t>(p.D) % 32 == 0) && (p.ldd % 8 == 0);
@@ -628,8 +651,7 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   p.num_n_tiles = (int)((p.N + 255) / 256);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof cfg);
+  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
@@ -655,6 +677,9 @@ cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, 
   if (fmt == 1)
     return pair ? launch_gemm_pair<1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
                 : launch_gemm_cfg<1, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  if (fmt == 2)
+    return pair ? launch_gemm_pair<2>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
+                : launch_gemm_cfg<2, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
   return pair ? launch_gemm_pair<0>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
               : launch_gemm_cfg<0, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
 }

@@ -79,6 +79,13 @@ __device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64
   const int64_t chunk = (r >> 7) * (ocp >> 6) + (kb >> 2);
   return chunk * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
 }
+// MXFP4: the same chunk image with one E8M0 byte per 32-element block, so a
+// chunk covers 128 contraction elements (two MMAs of 64).
+__device__ __forceinline__ int64_t mma_scale_offset_mx(int64_t r, int64_t kb32, int64_t ocp) {
+  const int64_t chunk = (r >> 7) * (ocp >> 7) + (kb32 >> 2);
+  return chunk * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb32 & 3);
+}
+
 
 // ------------------------------------------------------------------ per-block helpers
 // 16 bf16 values (two uint4) -> signed floats.
@@ -109,6 +116,21 @@ __device__ __forceinline__ BlockScale nvfp4_block_scale(uint32_t amax_bits, floa
   r.p = __fmul_rn(e4m3_decode_pos(r.s), g);
   r.inv = __frcp_rn(r.p);
   r.special = !(r.inv < kInf);
+  return r;
+}
+
+// MXFP4 block scale (OCP Microscaling v1.0) from the 32-block's largest
+// magnitude as a bf16 bit pattern: E8M0 code = max(exponent field - 2, 0),
+// i.e. 2^(floor(log2 amax) - 2) clamped at 2^-127 (subnormal or zero amax);
+// inv = 2^-(code - 127), a normal power of two.  Encoding then runs the
+// NVFP4 element path with this inverse.
+__device__ __forceinline__ BlockScale mxfp4_block_scale(uint32_t amax_bits) {
+  BlockScale r;
+  const int32_t e = (int32_t)(amax_bits >> 7) - 2;
+  r.s = (uint32_t)max(e, 0);
+  r.inv = __uint_as_float((254u - r.s) << 23);
+  r.p = 0.0f;   // unused: MXFP4 never takes the special path
+  r.special = false;
   return r;
 }
 
@@ -350,10 +372,13 @@ __device__ __forceinline__ void stats_nan(double* raw_out) {
 // zeros.
 // STATS: also accumulate SNIP's statistics of the tensor (both formats, this
 // call's rounding and random bits) from the same read; needs p.scales3.
+// FMT: 0 FP8, 1 NVFP4, 2 MXFP4 (lanes 2i and 2i+1 hold the two halves of one
+// 32-element block and share its scale through a shuffle; no statistics).
 template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
-  const float g = *p.scale;
-  if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = g;
+  static_assert(FMT != 2 || (!STATS && !ERR), "MXFP4 quantization has no fused statistics or block errors");
+  const float g = *p.scale;   // MXFP4: read only for the non-finite check
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = (FMT == 2 && !isnan(g)) ? 1.0f : g;
   if (isnan(g)) {
     if (STATS) stats_nan(p.raw_out);
     return;
@@ -376,7 +401,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   for (uint32_t seg = seg0; seg < total; seg += wstride, r += wq, sr += wr) {
     if (sr >= spr) { sr -= spr; ++r; }
     const uint32_t kb = sr * 32 + lane;
-    if (kb >= bpr) continue;
+    if (FMT != 2 && kb >= bpr) continue;   // MXFP4 lanes leave after the pair shuffle
     const bool real = r < p.out_rows && (int64_t)kb * 16 < p.out_cols;
     uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
     const int64_t e0 = (int64_t)r * p.cols + (int64_t)kb * 16;
@@ -390,8 +415,14 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     if (RND == 1 && real) sr_bits16(e0, p.seed, p.stream_id, u);
     BlockScale bs;
+    if (FMT == 2) {
+      uint32_t m = amax16_bits(a, b);
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      if (kb >= bpr) continue;
+      bs = mxfp4_block_scale(m);
+    }
     if (FMT == 1 || STATS) bs = nvfp4_block_scale(amax16_bits(a, b), g4, six_g);
-    uint4 c = make_uint4(0u, 0u, 0u, 0u);   // FP8: 16 codes; NVFP4: .x, .y
+    uint4 c = make_uint4(0u, 0u, 0u, 0u);   // FP8: 16 codes; FP4: .x, .y
     if (STATS) {
       // the codes come out of the statistics' own conversions
       if (real) {
@@ -408,14 +439,24 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
         }
         if (FMT == 0 && special8) c = fp8_encode16<RND>(v, inv8, u);
       }
-    } else if (FMT == 1) {
+    } else if (FMT >= 1) {
       const uint2 e = nvfp4_encode16<RND>(v, bs, u);
       c.x = e.x;
       c.y = e.y;
     } else {
       c = fp8_encode16<RND>(v, inv8, u);
     }
-    if (FMT == 1) {
+    if (FMT == 2) {   // the even lane of a pair writes the block's scale
+      const uint2 c2 = make_uint2(c.x, c.y);
+      if (LAYOUT == 0) {
+        if (!real) continue;
+        *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.out_cols >> 1) + (int64_t)kb * 8) = c2;
+        if (!(kb & 1)) p.scales[(int64_t)r * (p.out_cols >> 5) + (kb >> 1)] = (uint8_t)bs.s;
+      } else {
+        *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.ocp >> 1) + (int64_t)kb * 8) = c2;
+        if (!(kb & 1)) p.scales[mma_scale_offset_mx(r, kb >> 1, p.ocp)] = (uint8_t)bs.s;
+      }
+    } else if (FMT == 1) {
       const uint2 c2 = make_uint2(c.x, c.y);
       if (LAYOUT == 0) {
         if (!real) continue;
@@ -442,17 +483,22 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
 constexpr int kTR = 128, kTC = 64;
 constexpr int kXW = kTC / 2 + 4;   // words per staged source row (pairs of bf16), padded
 
+// FMT: 0 FP8, 1 NVFP4, 2 MXFP4 (a 32-row block is split over threads b and
+// b^1, which exchange their half maxima through shared memory).
 template <int FMT, int LAYOUT, int RND, bool ERR>
 __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
-  constexpr int OB = FMT == 1 ? kTR / 2 : kTR;   // output bytes per row of the tile
+  static_assert(FMT != 2 || !ERR, "MXFP4 quantization has no block errors");
+  constexpr int OB = FMT >= 1 ? kTR / 2 : kTR;   // output bytes per row of the tile
   constexpr int OW = OB / 4 + 1;                  // staged output row, words (odd: fewer conflicts)
   __shared__ __align__(16) uint32_t xs[kTR][kXW];
   __shared__ __align__(16) uint32_t rs[RND ? kTR : 1][RND ? kXW : 4];
   __shared__ uint32_t oc[kTC][OW];
-  __shared__ uint8_t os[FMT == 1 ? kTC : 1][8];
+  __shared__ uint8_t os[FMT >= 1 ? kTC : 1][8];
+  __shared__ uint32_t amx[FMT == 2 ? 8 : 1][FMT == 2 ? 32 : 1][2];
   __shared__ float oe[ERR ? kTC : 1][8];
-  const float g = *p.scale;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = g;
+  const float g = *p.scale;   // MXFP4: read only for the non-finite check
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && p.g_out)
+    *p.g_out = (FMT == 2 && !isnan(g)) ? 1.0f : g;
   if (isnan(g)) return;
   const float six_g = __fmul_rn(6.0f, g);
   const float inv8 = __frcp_rn(g);
@@ -496,7 +542,21 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) { u0[k] = 0u; u1[k] = 0u; }
     }
-    if (FMT == 1) {
+    if (FMT == 2) {
+      amx[b][cp][0] = m0;
+      amx[b][cp][1] = m1;
+      __syncthreads();
+      m0 = max(m0, amx[b ^ 1][cp][0]);
+      m1 = max(m1, amx[b ^ 1][cp][1]);
+      const BlockScale s0 = mxfp4_block_scale(m0), s1 = mxfp4_block_scale(m1);
+      const uint2 e0 = nvfp4_encode16<RND>(v0, s0, u0), e1 = nvfp4_encode16<RND>(v1, s1, u1);
+      oc[2 * cp][2 * b] = e0.x; oc[2 * cp][2 * b + 1] = e0.y;
+      oc[2 * cp + 1][2 * b] = e1.x; oc[2 * cp + 1][2 * b + 1] = e1.y;
+      if (!(b & 1)) {
+        os[2 * cp][b >> 1] = (uint8_t)s0.s;
+        os[2 * cp + 1][b >> 1] = (uint8_t)s1.s;
+      }
+    } else if (FMT == 1) {
       const BlockScale s0 = nvfp4_block_scale(m0, g, six_g), s1 = nvfp4_block_scale(m1, g, six_g);
       const uint2 e0 = nvfp4_encode16<RND>(v0, s0, u0), e1 = nvfp4_encode16<RND>(v1, s1, u1);
       oc[2 * cp][2 * b] = e0.x; oc[2 * cp][2 * b + 1] = e0.y;
@@ -516,7 +576,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
   }
   __syncthreads();
   // codes: output rows c0.., contraction r0..r0+127 (OB bytes per row)
-  constexpr int BPB = FMT == 1 ? 8 : 16;   // bytes per 16-element block
+  constexpr int BPB = FMT >= 1 ? 8 : 16;   // bytes per 16-element block
   if (LAYOUT == 0) {
     // row pitch of the row-major layout is only block-aligned: one store per block
     for (int idx = t; idx < kTC * 8; idx += 256) {
@@ -524,7 +584,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
       const int64_t orow = c0 + row;
       if (orow >= p.out_rows || r0 + 16 * b >= p.out_cols) continue;
       uint8_t* dst = p.codes + orow * (p.out_cols * BPB / 16) + (r0 + 16 * b) * BPB / 16;
-      if (FMT == 1) *reinterpret_cast<uint2*>(dst) = make_uint2(oc[row][2 * b], oc[row][2 * b + 1]);
+      if (FMT >= 1) *reinterpret_cast<uint2*>(dst) = make_uint2(oc[row][2 * b], oc[row][2 * b + 1]);
       else *reinterpret_cast<uint4*>(dst) = make_uint4(oc[row][4 * b], oc[row][4 * b + 1], oc[row][4 * b + 2],
                                                        oc[row][4 * b + 3]);
     }
@@ -536,6 +596,20 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
       if (orow >= p.orp) continue;
       *reinterpret_cast<uint4*>(p.codes + orow * (p.ocp * BPB / 16) + r0 * BPB / 16 + ch * 16) =
           make_uint4(oc[row][4 * ch], oc[row][4 * ch + 1], oc[row][4 * ch + 2], oc[row][4 * ch + 3]);
+    }
+  }
+  if (FMT == 2 && t < kTC) {
+    // four E8M0 bytes per output row: the tile's 128 contraction elements
+    const int64_t orow = c0 + t;
+    const int64_t kb0 = r0 >> 5;
+    if (LAYOUT == 0) {
+      if (orow < p.out_rows)
+        for (int b = 0; b < 4 && (kb0 + b) * 32 < p.out_cols; ++b)
+          p.scales[orow * (p.out_cols >> 5) + kb0 + b] = os[t][b];
+    } else if (orow < p.orp) {
+      const uint32_t v = (uint32_t)os[t][0] | ((uint32_t)os[t][1] << 8) | ((uint32_t)os[t][2] << 16) |
+                         ((uint32_t)os[t][3] << 24);
+      *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset_mx(orow, kb0, p.ocp)) = v;
     }
   }
   if (FMT == 1 && t < kTC) {
@@ -657,9 +731,34 @@ static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int r
   }
 }
 
+// MXFP4: no statistics or block errors, so only those instantiations exist.
+static void launch_quant_mx(const QuantParams& p, int orient, int layout, int rnd, int num_sms, cudaStream_t st) {
+  if (orient == 0) {
+    const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
+    const int grid = fill_grid(segs, 8, 16 * num_sms);
+    if (layout == 0) {
+      if (rnd == 0) quant_rows_kernel<2, 0, 0, false, false><<<grid, 256, 0, st>>>(p);
+      else quant_rows_kernel<2, 0, 1, false, false><<<grid, 256, 0, st>>>(p);
+    } else {
+      if (rnd == 0) quant_rows_kernel<2, 1, 0, false, false><<<grid, 256, 0, st>>>(p);
+      else quant_rows_kernel<2, 1, 1, false, false><<<grid, 256, 0, st>>>(p);
+    }
+  } else {
+    const dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
+    if (layout == 0) {
+      if (rnd == 0) quant_cols_kernel<2, 0, 0, false><<<grid, 256, 0, st>>>(p);
+      else quant_cols_kernel<2, 0, 1, false><<<grid, 256, 0, st>>>(p);
+    } else {
+      if (rnd == 0) quant_cols_kernel<2, 1, 0, false><<<grid, 256, 0, st>>>(p);
+      else quant_cols_kernel<2, 1, 1, false><<<grid, 256, 0, st>>>(p);
+    }
+  }
+}
+
 cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
                          cudaStream_t st) {
-  if (fmt == 1) launch_quant_fmt<1>(p, orient, layout, rnd, err, num_sms, st);
+  if (fmt == 2) launch_quant_mx(p, orient, layout, rnd, num_sms, st);
+  else if (fmt == 1) launch_quant_fmt<1>(p, orient, layout, rnd, err, num_sms, st);
   else launch_quant_fmt<0>(p, orient, layout, rnd, false, num_sms, st);
   return cudaGetLastError();
 }

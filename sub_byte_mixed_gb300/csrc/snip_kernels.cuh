@@ -107,7 +107,8 @@ cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, 
                          cudaStream_t st);
 cudaError_t launch_stats(const StatsParams& p, int rnd, int num_sms, cudaStream_t st);
 
-// GEMM: D = ga*gb*A B^T on MMA-layout operands.  fmt 1 = NVFP4, 0 = FP8.
+// GEMM: D = ga*gb*A B^T on MMA-layout operands.  fmt 1 = NVFP4, 2 = MXFP4 (ga, gb
+// null: no tensor scales), 0 = FP8.
 // a_codes / b_codes are passed to the launcher, which builds the TMA tensor
 // maps.
 cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,

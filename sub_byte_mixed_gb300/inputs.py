@@ -22,7 +22,7 @@ import torch
 SIGMA_X, SIGMA_W, SIGMA_DY = 1.0, 0.02, 1e-3
 
 LAYER_NAMES = ("Q", "K", "V", "O", "Gate", "Up", "Down")
-FMT_FP8, FMT_NVFP4 = 0, 1          # per-layer format codes of a plan
+FMT_FP8, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2   # per-layer format codes of a plan
 
 
 def _gen(seed: int, tensor_id: int, device) -> torch.Generator:
@@ -85,7 +85,7 @@ class BlockConfig:
 
     def fp4_flop_fraction(self, plan) -> float:
         tot = sum(l.K * l.N for l in self.linears)
-        return sum(l.K * l.N for l, f in zip(self.linears, plan) if f == FMT_NVFP4) / tot
+        return sum(l.K * l.N for l, f in zip(self.linears, plan) if f in (FMT_NVFP4, FMT_MXFP4)) / tot
 
 
 # TinyLlama-1B: hidden 2048, intermediate 5632, 32 heads / 4 KV heads (K,V out 256), 2 x 2048 tokens

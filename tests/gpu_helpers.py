@@ -55,3 +55,17 @@ def gemm_close(got, ref, what=""):
     assert rel <= GEMM_REL_FRO, f"{what}: rel Frobenius {rel:.3e}"
     assert mx <= GEMM_MAX_ABS_OF_RMS * rms + 1e-30, f"{what}: max abs {mx:.3e} vs rms {rms:.3e}"
     return rel, mx / rms if rms > 0 else 0.0
+
+
+def mma_mx_scales_to_rowmajor(scales, out_rows, out_cols):
+    """Gather the chunked MMA-layout E8M0 scales of MXFP4 (chunks of four
+    32-element blocks) into a padded rows x blocks matrix."""
+    s = scales.cpu().numpy()
+    ocp = (out_cols + 255) // 256 * 256
+    orp = (out_rows + 255) // 256 * 256
+    r = np.arange(orp)[:, None]
+    kb = np.arange(ocp // 32)[None, :]
+    chunk = (r // 128) * (ocp // 128) + kb // 4
+    off = chunk * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + kb % 4
+    full = s[off]
+    return full, full[:out_rows, : out_cols // 32]

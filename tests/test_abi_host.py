@@ -47,6 +47,9 @@ def test_quantized_bytes(snip):
     # MMA layout: rows padded to 256, contraction to 256 (NVFP4) / 128 (FP8)
     assert snip.snip_quantized_bytes(snip.NVFP4, snip.MMA, 64, 128) == (256 * 128, 256 * 16)
     assert snip.snip_quantized_bytes(snip.FP8, snip.MMA, 300, 130) == (512 * 256, 0)
+    # MXFP4: NVFP4's codes, one E8M0 byte per 32 elements
+    assert snip.snip_quantized_bytes(snip.MXFP4, snip.ROWMAJOR, 64, 128) == (64 * 64, 64 * 4)
+    assert snip.snip_quantized_bytes(snip.MXFP4, snip.MMA, 64, 288) == (256 * 256, 256 * 16)
     with pytest.raises(snip.SnipError):
         snip.snip_quantized_bytes(5, 0, 1, 1)
 
