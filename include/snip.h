@@ -332,6 +332,26 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
 /* Host helper: derive ratios and sqrt(3) flags from a host copy of raw_out. */
 snip_status snip_stats_finalize(const double* raw_host, snip_stats* out);
 
+/* ---------------------------------------------------------------- NEXT-4: dW-level sqrt(3) check */
+
+/* The weight-gradient form of the quantization-noise threshold of "FP4 all
+ * the way" (Outline: quantized training loses efficiency once the gradient
+ * norm falls below about sqrt(3) times the quantization noise): the
+ * full-precision weight gradient dW = dY^T X is formed from the bf16 tensors
+ * (cuBLAS GEMM, fp32 accumulation) and compared with a quantized one:
+ * out2 (device, 2 doubles) = { ||dW||^2, ||dW_q - dW||^2 }.
+ * X device T x K bf16, dY device T x N bf16, dW_q device N x K fp32 (dense,
+ * e.g. snip_qlinear_bwd's dW).  T, K, N multiples of 16 (SNIP_ERR_SHAPE).
+ * ws: snip_dw_noise_workspace_size(K, N) bytes (it holds dW).  Errors as for
+ * the other entry points; SNIP_ERR_CUDA if cuBLAS fails. */
+size_t snip_dw_noise_workspace_size(int64_t K, int64_t N);
+snip_status snip_dw_noise(const void* X, const void* dY, int64_t T, int64_t K, int64_t N, const float* dW_q,
+                          double* out2, void* ws, size_t ws_bytes, void* stream);
+/* Host helper: ratio = sqrt(||dW||^2 / ||dW_q - dW||^2) (infinite for a zero
+ * error) and below_sqrt3 = ratio < sqrt(3), from a host copy of out2.
+ * SNIP_ERR_NONFINITE for a non-finite input sum. */
+snip_status snip_dw_noise_finalize(const double* out2_host, double* ratio, int* below_sqrt3);
+
 /* ---------------------------------------------------------------- plan selection (host) */
 
 /* Per-layer cost of each format for SNIP's plan selection ("SNIP" (Pan et

@@ -111,6 +111,12 @@ class NonFiniteInput(ValueError):
     """The tensor holds an infinity or a NaN: the encodings reject it."""
 
 
+def _bits_to_f64(x) -> np.ndarray:
+    """bf16 tensor -> float64 values (exact: bf16 is the top half of binary32)."""
+    b = _bits(x).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
 def _bits(x) -> np.ndarray:
     """bf16 tensor (torch, or uint16 numpy bit patterns) -> contiguous uint16 numpy."""
     if isinstance(x, np.ndarray):
@@ -331,6 +337,17 @@ def qlinear_wgrad(fmt, dY, X, layer=0, seed=0, rnd_dyt=SR, rnd_xt=SR, rows=None)
     dytq = quantize(fmt, dY, 1, rnd_dyt, seed, stream_id(layer, TAG_DYT_WGRAD))
     xtq = quantize(fmt, X, 1, rnd_xt, seed, stream_id(layer, TAG_XT_WGRAD))
     return gemm_tn(dytq.dequant(), xtq.dequant(), rows)
+
+
+def dw_noise(X, dY, dW_q):
+    """The weight-gradient form of the sqrt(3) check ("FP4 all the way",
+    Outline): with dW = dY^T X of the unquantized bf16 tensors (fp64 product),
+    returns (||dW||^2, ||dW_q - dW||^2)."""
+    x = _bits_to_f64(X)
+    dy = _bits_to_f64(dY)
+    dw = dy.T @ x
+    d = np.asarray(dW_q, dtype=np.float64) - dw
+    return float(np.sum(dw * dw)), float(np.sum(d * d))
 
 
 # ----------------------------------------------------------------------------- statistics

@@ -67,7 +67,10 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}")
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[obj for _, obj, _ in results]]
+    # cuBLAS serves the one plain library GEMM (the full-precision dW of snip_dw_noise)
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(cc))), "lib64")
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[obj for _, obj, _ in results], "-lcublas",
+           "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)

@@ -1,6 +1,9 @@
 // api.cu -- the C ABI declared in include/snip.h: argument checks, workspace
 // layout, the per-layer precision plan and the launch sequence of each call.
 // Every compute step runs in the kernels of quant.cu and gemm.cu.
+#include <cublas_v2.h>
+
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -555,6 +558,58 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
   return run_quantize(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, seed, stream_id,
                       sc + (fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1), layout, codes, scales, nullptr, nullptr, sms, st, sc,
                       raw_out, ws);
+}
+
+// ---------------------------------------------------------------- NEXT-4: dW-level sqrt(3) check
+namespace {
+cublasHandle_t g_cublas[64] = {nullptr};   // one handle per device, created on first use
+}
+
+size_t snip_dw_noise_workspace_size(int64_t K, int64_t N) {
+  if (K < 0 || N < 0) return 0;
+  return kSmallWorkspaceRounded + (size_t)(K * N) * sizeof(float);
+}
+
+snip_status snip_dw_noise(const void* X, const void* dY, int64_t T, int64_t K, int64_t N, const float* dW_q,
+                          double* out2, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if (!X || !dY || !dW_q || !out2 || T <= 0 || K <= 0 || N <= 0) return SNIP_ERR_INVALID_ARG;
+  if (T % 16 || K % 16 || N % 16) return SNIP_ERR_SHAPE;
+  if (!ws || ws_bytes < snip_dw_noise_workspace_size(K, N)) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(dW_q) || !aligned16(ws)) return SNIP_ERR_ALIGN;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SNIP_ERR_CUDA;
+  if (!g_cublas[dev] && cublasCreate(&g_cublas[dev]) != CUBLAS_STATUS_SUCCESS) {
+    g_cublas[dev] = nullptr;
+    fprintf(stderr, "snip: cublasCreate failed\n");
+    return SNIP_ERR_CUDA;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cublasHandle_t h = g_cublas[dev];
+  if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return SNIP_ERR_CUDA;
+  float* ref = ws_at<float>(ws, kSmallWorkspaceRounded);
+  // dW = dY^T X (N x K, row-major) from the bf16 tensors, fp32 accumulation: in column-major terms
+  // dW^T (K x N) = X' (K x T) * dY'^T (T x N), X' and dY' the row-major X and dY read column-major
+  const float one = 1.0f, zero = 0.0f;
+  const cublasStatus_t cs =
+      cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, (int)K, (int)N, (int)T, &one, X, CUDA_R_16BF, (int)K, dY,
+                   CUDA_R_16BF, (int)N, &zero, ref, CUDA_R_32F, (int)K, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  if (cs != CUBLAS_STATUS_SUCCESS) {
+    fprintf(stderr, "snip: cublasGemmEx failed (%d)\n", (int)cs);
+    return SNIP_ERR_CUDA;
+  }
+  return cuda_status(launch_dw_noise(dW_q, ref, K * N, ws_at<double>(ws, kOffStatsPartials),
+                                     ws_at<uint32_t>(ws, kOffStatsCounter), out2, sms, st));
+}
+
+snip_status snip_dw_noise_finalize(const double* out2_host, double* ratio, int* below_sqrt3) {
+  if (!out2_host || !ratio || !below_sqrt3) return SNIP_ERR_INVALID_ARG;
+  if (!std::isfinite(out2_host[0]) || !std::isfinite(out2_host[1])) return SNIP_ERR_NONFINITE;
+  *ratio = out2_host[1] == 0.0 ? HUGE_VAL : std::sqrt(out2_host[0] / out2_host[1]);
+  *below_sqrt3 = *ratio < 1.7320508075688772;
+  return SNIP_OK;
 }
 
 snip_status snip_stats_finalize(const double* raw, snip_stats* out) {

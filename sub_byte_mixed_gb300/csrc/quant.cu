@@ -682,6 +682,45 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
   stats_finish(sx2, e4, e8, v4, v8, p.partials, p.counter, p.raw_out, amax, p.rows * p.cols);
 }
 
+// ------------------------------------------------------------------ NEXT-4: dW-level noise
+// ||ref||^2 and ||q - ref||^2 over n fp32 values (n % 4 == 0): 16-byte loads,
+// fp32 per thread, fp64 across CTAs, the last CTA writes out2.
+__global__ void __launch_bounds__(256) dw_noise_kernel(const float4* __restrict__ q, const float4* __restrict__ ref,
+                                                       int64_t n4, double* __restrict__ partials,
+                                                       uint32_t* __restrict__ counter, double* __restrict__ out2) {
+  float s_ref = 0.f, s_err = 0.f;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 a = __ldcs(q + i), b = __ldcs(ref + i);
+    s_ref = fmaf(b.x, b.x, fmaf(b.y, b.y, fmaf(b.z, b.z, fmaf(b.w, b.w, s_ref))));
+    const float d0 = a.x - b.x, d1 = a.y - b.y, d2 = a.z - b.z, d3 = a.w - b.w;
+    s_err = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, s_err))));
+  }
+  double acc[2] = {(double)s_ref, (double)s_err};
+  block_sum_f64<2>(acc);
+  __shared__ bool s_last;
+  if (threadIdx.x == 0) {
+    partials[2 * blockIdx.x] = acc[0];
+    partials[2 * blockIdx.x + 1] = acc[1];
+    __threadfence();
+    s_last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  double tot[2] = {0.0, 0.0};
+  for (uint32_t j = threadIdx.x; j < gridDim.x; j += blockDim.x) {
+    tot[0] += ((volatile double*)partials)[2 * j];
+    tot[1] += ((volatile double*)partials)[2 * j + 1];
+  }
+  block_sum_f64<2>(tot);
+  if (threadIdx.x == 0) {
+    out2[0] = tot[0];
+    out2[1] = tot[1];
+    *counter = 0;
+  }
+}
+
 // ------------------------------------------------------------------ host-side launchers
 static int fill_grid(int64_t work_items, int per_cta, int max_ctas) {
   int64_t g = (work_items + per_cta - 1) / per_cta;
@@ -760,6 +799,14 @@ cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, 
   if (fmt == 2) launch_quant_mx(p, orient, layout, rnd, num_sms, st);
   else if (fmt == 1) launch_quant_fmt<1>(p, orient, layout, rnd, err, num_sms, st);
   else launch_quant_fmt<0>(p, orient, layout, rnd, false, num_sms, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_noise(const float* q, const float* ref, int64_t n, double* partials, uint32_t* counter,
+                            double* out2, int num_sms, cudaStream_t st) {
+  const int grid = fill_grid(n >> 2, 256 * 4, 4 * num_sms);
+  dw_noise_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(q), reinterpret_cast<const float4*>(ref),
+                                        n >> 2, partials, counter, out2);
   return cudaGetLastError();
 }
 

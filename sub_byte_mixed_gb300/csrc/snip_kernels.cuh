@@ -106,6 +106,9 @@ cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint
 cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
                          cudaStream_t st);
 cudaError_t launch_stats(const StatsParams& p, int rnd, int num_sms, cudaStream_t st);
+// {||ref||^2, ||q - ref||^2} of n fp32 values (n % 4 == 0) into out2 (device).
+cudaError_t launch_dw_noise(const float* q, const float* ref, int64_t n, double* partials, uint32_t* counter,
+                            double* out2, int num_sms, cudaStream_t st);
 
 // GEMM: D = ga*gb*A B^T on MMA-layout operands.  fmt 1 = NVFP4, 2 = MXFP4 (ga, gb
 // null: no tensor scales), 0 = FP8.

@@ -34,6 +34,7 @@ EXPORTS = (
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
     "snip_quant_stats", "snip_quantize_stats", "snip_stats_finalize", "snip_plan_costs", "snip_plan_select",
+    "snip_dw_noise_workspace_size", "snip_dw_noise", "snip_dw_noise_finalize",
 )
 
 
@@ -88,6 +89,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_quant_stats": (i32, [vp, i64, i64, i32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "snip_stats_finalize": (i32, [vp, ctypes.POINTER(SnipStats)]),
         "snip_plan_costs": (i32, [i32, vp, vp, vp]),
+        "snip_dw_noise_workspace_size": (sz, [i64, i64]),
+        "snip_dw_noise": (i32, [vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]),
+        "snip_dw_noise_finalize": (i32, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
         "snip_plan_select": (i32, [i32, vp, vp, vp, ctypes.c_double, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -199,6 +203,22 @@ def snip_stats_finalize(raw_host) -> SnipStats:
     out = SnipStats()
     _call("snip_stats_finalize", arr, ctypes.byref(out))
     return out
+
+
+def snip_dw_noise_workspace_size(K, N) -> int:
+    return load().snip_dw_noise_workspace_size(K, N)
+
+
+def snip_dw_noise(X, dY, T, K, N, dW_q, out2, ws, ws_bytes, stream):
+    _call("snip_dw_noise", X, dY, T, K, N, dW_q, out2, ws, ws_bytes, stream)
+
+
+def snip_dw_noise_finalize(out2_host):
+    """-> (ratio ||dW|| / ||dW_q - dW||, below sqrt(3))."""
+    arr = (ctypes.c_double * 2)(*[float(v) for v in out2_host])
+    ratio, flag = ctypes.c_double(), ctypes.c_int()
+    _call("snip_dw_noise_finalize", arr, ctypes.byref(ratio), ctypes.byref(flag))
+    return ratio.value, bool(flag.value)
 
 
 def snip_plan_costs(raw_host):
@@ -449,6 +469,18 @@ def quantize_stats(fmt, x, rnd=RTN, seed=0, stream_id=0, layout=MMA, scales=None
     snip_quantize_stats(fmt, x.data_ptr(), rows, cols, rnd, seed, stream_id, _ptr(scales), layout, codes.data_ptr(),
                         sc.data_ptr() if fmt in (NVFP4, MXFP4) else None, raw.data_ptr(), ws.ptr, ws.nbytes, _stream())
     return codes[:cb], sc[:sb], raw
+
+
+def dw_noise(X, dY, dW_q, ws: Workspace | None = None):
+    """{||dW||^2, ||dW_q - dW||^2} (device float64 (2,)) with dW = dY^T X from the bf16 tensors."""
+    torch = _torch()
+    T, K = X.shape
+    N = dY.shape[1]
+    ws = ws or Workspace(snip_dw_noise_workspace_size(K, N), X.device)
+    out = torch.empty(2, dtype=torch.float64, device=X.device)
+    snip_dw_noise(X.data_ptr(), dY.data_ptr(), T, K, N, dW_q.data_ptr(), out.data_ptr(), ws.ptr, ws.nbytes,
+                  _stream())
+    return out
 
 
 def quant_stats(a, rnd=RTN, seed=0, stream_id=0, want_block_err=False, ws: Workspace | None = None, raw=None,
