@@ -21,6 +21,7 @@ the data path); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -276,6 +277,7 @@ class Step:
         ws, wsb, stream = self.ws.ptr, self.ws.nbytes, torch.cuda.current_stream().cuda_stream
         self.stream = stream
         calls = []   # (fn, args, category, units) units = bytes (HBM kernels) or flops (GEMMs)
+        self._keep = []   # ctypes arrays referenced by the calls
         for j, (l, f) in enumerate(zip(cfg.linears, plan)):
             if layers and l.name not in layers:
                 continue
@@ -289,10 +291,14 @@ class Step:
             qcat, gcat = "quant_" + fname, "gemm_" + fname
             bpe = {snip.NVFP4: NVFP4_BYTES_PER_ELEM, snip.FP8: FP8_BYTES_PER_ELEM, snip.MXFP4: MXFP4_BYTES_PER_ELEM}[f]
             fo = 8 if f == snip.FP8 else 4            # byte offset of s (FP8) or g (NVFP4; MXFP4: unused) in a slot
-            for name in (l.x_id, "W", "dY"):
-                t = src[name]
-                calls.append((L.snip_tensor_scales, (t.data_ptr(), t.numel(), scp[name], ws, wsb, stream), "scales",
-                              SCALES_BYTES_PER_ELEM * t.numel()))
+            # the three tensors' scales in one launch
+            names = (l.x_id, "W", "dY")
+            xs = (ctypes.c_void_p * 3)(*[src[nm].data_ptr() for nm in names])
+            ns = (ctypes.c_int64 * 3)(*[src[nm].numel() for nm in names])
+            outs = (ctypes.c_void_p * 3)(*[scp[nm] for nm in names])
+            self._keep.append((xs, ns, outs))
+            calls.append((L.snip_tensor_scales_multi, (3, xs, ns, outs, ws, wsb, stream), "scales",
+                          SCALES_BYTES_PER_ELEM * sum(src[nm].numel() for nm in names)))
             for r, (name, orient, orr, occ) in enumerate(roles(l)):
                 t = src[name]
                 rows, cols = t.shape

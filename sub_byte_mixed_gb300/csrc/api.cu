@@ -22,6 +22,7 @@ namespace {
 constexpr size_t kOffStatus = 0;        // uint32 sticky status bits
 constexpr size_t kOffAmaxCounter = 4;   // uint32, self-resetting
 constexpr size_t kOffStatsCounter = 8;  // uint32, self-resetting
+constexpr size_t kOffMultiCounters = 16; // kMaxMultiScales x uint32, self-resetting
 constexpr size_t kOffScaleSlots = 64;   // 8 slots x 4 floats {amax, NVFP4 g, FP8 s, -} (12 bytes used)
 constexpr size_t kOffAmaxPartials = SNIP_WS_HEADER_BYTES;                            // kMaxPartials x uint32
 constexpr size_t kOffStatsPartials = kOffAmaxPartials + 4 * kMaxPartials;            // kMaxPartials x 5 doubles
@@ -94,6 +95,20 @@ snip_status run_scales(const void* x, int64_t n, float* out3, void* ws, int num_
   return cuda_status(launch_scales(static_cast<const uint16_t*>(x), n, ws_at<uint32_t>(ws, kOffAmaxPartials),
                                    ws_at<uint32_t>(ws, kOffAmaxCounter), out3, ws_at<uint32_t>(ws, kOffStatus),
                                    num_sms, st));
+}
+
+// Scales of `count` tensors in one launch (count <= kMaxMultiScales).
+snip_status run_scales_multi(int count, const void* const* xs, const int64_t* ns, float* const* outs, void* ws,
+                             int num_sms, cudaStream_t st) {
+  ScalesMulti m = {};
+  m.count = count;
+  for (int t = 0; t < count; ++t) {
+    m.x[t] = static_cast<const uint16_t*>(xs[t]);
+    m.n[t] = ns[t];
+    m.out3[t] = outs[t];
+  }
+  return cuda_status(launch_scales_multi(m, ws_at<uint32_t>(ws, kOffAmaxPartials), ws_at<uint32_t>(ws, kOffMultiCounters),
+                                         ws_at<uint32_t>(ws, kOffStatus), num_sms, st));
 }
 
 // One quantization with the tensor scale `scale` (device float).
@@ -255,6 +270,21 @@ snip_status snip_tensor_scales(const void* x, int64_t n, float* scales_out, void
   if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
   if (!aligned16(x) || !aligned16(ws)) return SNIP_ERR_ALIGN;
   return run_scales(x, n, scales_out, ws, sms, static_cast<cudaStream_t>(stream));
+}
+
+snip_status snip_tensor_scales_multi(int count, const void* const* xs, const int64_t* ns, float* const* scales_out,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if (count < 1 || count > kMaxMultiScales || !xs || !ns || !scales_out) return SNIP_ERR_INVALID_ARG;
+  for (int t = 0; t < count; ++t) {
+    if (ns[t] < 0 || (!xs[t] && ns[t] > 0) || !scales_out[t]) return SNIP_ERR_INVALID_ARG;
+    if (!aligned16(xs[t])) return SNIP_ERR_ALIGN;
+  }
+  if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(ws)) return SNIP_ERR_ALIGN;
+  return run_scales_multi(count, xs, ns, scales_out, ws, sms, static_cast<cudaStream_t>(stream));
 }
 
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
@@ -440,8 +470,12 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
   const int si = fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1;   // which tensor scale the format uses (MXFP4: none; g only flags non-finite input)
   float* sx = scale_slot(ws, 0);
   float* sw = scale_slot(ws, 1);
-  if ((s = run_scales(X, T * K, sx, ws, sms, st)) != SNIP_OK) return s;
-  if ((s = run_scales(W, N * K, sw, ws, sms, st)) != SNIP_OK) return s;
+  {
+    const void* xs[2] = {X, W};
+    const int64_t ns[2] = {T * K, N * K};
+    float* outs[2] = {sx, sw};
+    if ((s = run_scales_multi(2, xs, ns, outs, ws, sms, st)) != SNIP_OK) return s;
+  }
   if ((s = run_quantize(fmt, X, T, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_X_FWD], plan->seed, sid + SNIP_TAG_X_FWD,
                         sx + si, SNIP_LAYOUT_MMA, b + L.op[0].codes_off, b + L.op[0].scales_off, nullptr, nullptr,
                         sms, st, sx, stats_out, ws)) != SNIP_OK)
@@ -475,9 +509,12 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
   float* sx = scale_slot(ws, 0);
   float* sw = scale_slot(ws, 1);
   float* sd = scale_slot(ws, 2);
-  if ((s = run_scales(dY, T * N, sd, ws, sms, st)) != SNIP_OK) return s;
-  if ((s = run_scales(W, N * K, sw, ws, sms, st)) != SNIP_OK) return s;
-  if ((s = run_scales(X, T * K, sx, ws, sms, st)) != SNIP_OK) return s;
+  {
+    const void* xs[3] = {dY, W, X};
+    const int64_t ns[3] = {T * N, N * K, T * K};
+    float* outs[3] = {sd, sw, sx};
+    if ((s = run_scales_multi(3, xs, ns, outs, ws, sms, st)) != SNIP_OK) return s;
+  }
   // dgrad: dX = Q(dY) Q(W^T)^T, contraction N
   if ((s = run_quantize(fmt, dY, T, N, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_DY_DGRAD], plan->seed,
                         sid + SNIP_TAG_DY_DGRAD, sd + si, SNIP_LAYOUT_MMA, b + L.op[0].codes_off,

@@ -29,36 +29,36 @@ constexpr float kInf = __builtin_huge_valf();
 // an infinity or NaN.  Each CTA publishes its max; the last CTA to finish
 // reduces them and writes out3 = {amax, g = amax/2688, s = amax/448} (g = s = 1
 // for an all-zero tensor; all NaN and the status bit for non-finite input).
-__global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restrict__ x, int64_t n,
-                                                        uint32_t* __restrict__ partials,
-                                                        uint32_t* __restrict__ counter, float* __restrict__ out3,
-                                                        uint32_t* __restrict__ status) {
+// The work of one CTA among nblk on one tensor (local CTA index lb).
+__device__ __forceinline__ void scales_body(const uint16_t* __restrict__ x, int64_t n, uint32_t lb, uint32_t nblk,
+                                            uint32_t* __restrict__ partials, uint32_t* __restrict__ counter,
+                                            float* __restrict__ out3, uint32_t* __restrict__ status) {
   uint32_t m2 = 0;
   const int64_t nvec = n >> 3;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)nblk * blockDim.x;
+  int64_t i = (int64_t)lb * blockDim.x + threadIdx.x;
   for (; i + 3 * stride < nvec; i += 4 * stride) {
     const uint4 a = __ldg(xv + i), b = __ldg(xv + i + stride), c = __ldg(xv + i + 2 * stride),
                 d = __ldg(xv + i + 3 * stride);
     m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(mag_max4(a), mag_max4(b)), __vmaxu2(mag_max4(c), mag_max4(d))));
   }
   for (; i < nvec; i += stride) m2 = __vmaxu2(m2, mag_max4(__ldg(xv + i)));
-  if (blockIdx.x == 0 && threadIdx.x < (n & 7)) m2 = __vmaxu2(m2, (uint32_t)(x[(nvec << 3) + threadIdx.x] & 0x7fffu));
+  if (lb == 0 && threadIdx.x < (n & 7)) m2 = __vmaxu2(m2, (uint32_t)(x[(nvec << 3) + threadIdx.x] & 0x7fffu));
   uint32_t m = max(m2 & 0xffffu, m2 >> 16);
   m = block_max_u32(m);
   __shared__ bool s_last;
   if (threadIdx.x == 0) {
-    partials[blockIdx.x] = m;
+    partials[lb] = m;
     if (m >= 0x7f80u) atomicOr(status, kDevNonFinite);
     __threadfence();
-    s_last = atomicAdd(counter, 1u) == gridDim.x - 1;
+    s_last = atomicAdd(counter, 1u) == nblk - 1;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   uint32_t mm = 0;
-  for (uint32_t j = threadIdx.x; j < gridDim.x; j += blockDim.x) mm = max(mm, ((volatile uint32_t*)partials)[j]);
+  for (uint32_t j = threadIdx.x; j < nblk; j += blockDim.x) mm = max(mm, ((volatile uint32_t*)partials)[j]);
   mm = block_max_u32(mm);
   if (threadIdx.x == 0) {
     if (mm >= 0x7f80u) {
@@ -72,6 +72,25 @@ __global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restri
     }
     *counter = 0;  // ready for the next reduction on this workspace
   }
+}
+
+__global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                        uint32_t* __restrict__ partials,
+                                                        uint32_t* __restrict__ counter, float* __restrict__ out3,
+                                                        uint32_t* __restrict__ status) {
+  scales_body(x, n, blockIdx.x, gridDim.x, partials, counter, out3, status);
+}
+
+// Several tensors in one launch: tensor t owns CTAs [cta0[t], cta0[t+1]), its
+// partial slots at the same indices and its own completion counter.
+__global__ void __launch_bounds__(256, 4) scales_multi_kernel(ScalesMulti m, uint32_t* __restrict__ partials,
+                                                              uint32_t* __restrict__ counters,
+                                                              uint32_t* __restrict__ status) {
+  int t = 0;
+  while (t + 1 < m.count && (int)blockIdx.x >= m.cta0[t + 1]) ++t;
+  const uint32_t c0 = (uint32_t)m.cta0[t];
+  scales_body(m.x[t], m.n[t], blockIdx.x - c0, (uint32_t)(m.cta0[t + 1] - m.cta0[t]), partials + c0, counters + t,
+              m.out3[t], status);
 }
 
 // Byte offset of the E4M3 scale of (row r, block kb) in the MMA layout.
@@ -727,6 +746,26 @@ static int fill_grid(int64_t work_items, int per_cta, int max_ctas) {
   if (g < 1) g = 1;
   if (g > max_ctas) g = max_ctas;
   return (int)g;
+}
+
+cudaError_t launch_scales_multi(ScalesMulti m, uint32_t* partials, uint32_t* counters, uint32_t* status,
+                                int num_sms, cudaStream_t st) {
+  // CTAs in proportion to each tensor's size, at least one each, within the partial slots
+  int64_t total = 0;
+  for (int t = 0; t < m.count; ++t) total += m.n[t];
+  const int64_t want = fill_grid(total >> 3, 256 * 4, 4 * num_sms);
+  int c = 0;
+  for (int t = 0; t < m.count; ++t) {
+    m.cta0[t] = c;
+    int64_t k = total > 0 ? (want * m.n[t] + total - 1) / total : 1;
+    const int64_t need = ((m.n[t] >> 3) + 1023) / 1024;   // no more CTAs than 4 loads per thread need
+    if (k > need) k = need;
+    if (k < 1) k = 1;
+    c += (int)k;
+  }
+  m.cta0[m.count] = c;
+  scales_multi_kernel<<<c, 256, 0, st>>>(m, partials, counters, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, float* out3,

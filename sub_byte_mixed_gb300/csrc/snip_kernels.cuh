@@ -103,6 +103,17 @@ __device__ __forceinline__ void block_sum_f64(double (&v)[N]) {
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, float* out3,
                           uint32_t* status, int num_sms, cudaStream_t st);
+// Up to kMaxMultiScales tensors' scales in one launch (cta0 filled by the launcher).
+constexpr int kMaxMultiScales = 4;
+struct ScalesMulti {
+  const uint16_t* x[kMaxMultiScales];
+  int64_t n[kMaxMultiScales];
+  float* out3[kMaxMultiScales];
+  int cta0[kMaxMultiScales + 1];
+  int count;
+};
+cudaError_t launch_scales_multi(ScalesMulti m, uint32_t* partials, uint32_t* counters, uint32_t* status,
+                                int num_sms, cudaStream_t st);
 cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
                          cudaStream_t st);
 cudaError_t launch_stats(const StatsParams& p, int rnd, int num_sms, cudaStream_t st);

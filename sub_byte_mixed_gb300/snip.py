@@ -29,7 +29,8 @@ STATS_NVALS = 8
 # every symbol include/snip.h declares
 EXPORTS = (
     "snip_status_string", "snip_version", "snip_device_check", "snip_workspace_init", "snip_workspace_status",
-    "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_tensor_scales_noalloc",
+    "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_tensor_scales_multi",
+    "snip_tensor_scales_noalloc",
     "snip_quantize_nvfp4", "snip_quantize_fp8", "snip_quantize_mxfp4",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
@@ -73,6 +74,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_amax": (i32, [vp, i64, vp, vp, sz, vp]),
         "snip_tensor_scales": (i32, [vp, i64, vp, vp, sz, vp]),
         "snip_tensor_scales_noalloc": (i32, [vp, i64, vp, vp]),
+        "snip_tensor_scales_multi": (i32, [i32, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_nvfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_fp8": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, sz, vp]),
         "snip_quantize_mxfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, i32, vp, vp, vp, sz, vp]),
@@ -346,6 +348,17 @@ class QuantFP8:
     out_rows: int
     out_cols: int
     layout: int
+
+
+def tensor_scales_multi(xs, outs, ws: Workspace | None = None):
+    """{amax, g, s} of each bf16 tensor in xs into the device float (3,) tensors outs, one launch."""
+    ws = ws or small_workspace()
+    n = len(xs)
+    ptrs = (ctypes.c_void_p * n)(*[x.data_ptr() for x in xs])
+    ns = (ctypes.c_int64 * n)(*[x.numel() for x in xs])
+    op = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    _call("snip_tensor_scales_multi", n, ptrs, ns, op, ws.ptr, ws.nbytes, _stream())
+    return outs
 
 
 def tensor_scales(x, ws: Workspace | None = None, out=None):

@@ -41,6 +41,34 @@ def test_tensor_scales(snip, shape):
     assert sc[1] == oracle.nvfp4_global_scale(m) and sc[2] == oracle.fp8_tensor_scale(m)
 
 
+def test_tensor_scales_multi(snip):
+    """One launch over tensors of very different sizes (empty, a ragged few,
+    medium, large) gives each tensor the scales of its own pass; a
+    non-finite tensor among them flags the status and NaNs only its own."""
+    shapes = [(0, 16), (3, 16), (257, 96), (2048, 1024)]
+    xs = [_x(sh, tid=20 + i) for i, sh in enumerate(shapes)]
+    xs[1] = xs[1].float().mul(1e30).to(torch.bfloat16)          # a huge amax
+    outs = [torch.full((3,), -1.0, device="cuda") for _ in xs]
+    ws = snip.Workspace(snip.snip_quantize_workspace_size(0, 0))
+    snip.tensor_scales_multi([x.cuda() for x in xs], outs, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == snip.SNIP_OK
+    for x, o in zip(xs, outs):
+        m = float(x.float().abs().max()) if x.numel() else 0.0
+        sc = o.cpu().numpy()
+        assert sc[0] == m and sc[1] == oracle.nvfp4_global_scale(m) and sc[2] == oracle.fp8_tensor_scale(m)
+    bad = xs[2].clone()
+    bad[100, 7] = float("inf")
+    outs2 = [torch.zeros(3, device="cuda") for _ in range(3)]
+    ws2 = snip.Workspace(snip.snip_quantize_workspace_size(0, 0))
+    snip.tensor_scales_multi([xs[3].cuda(), bad.cuda(), xs[2].cuda()], outs2, ws=ws2)
+    torch.cuda.synchronize()
+    assert ws2.status() == snip.SNIP_ERR_NONFINITE
+    assert np.isnan(outs2[1].cpu().numpy()).all()
+    assert outs2[0].cpu().numpy()[0] == float(xs[3].float().abs().max())
+    assert outs2[2].cpu().numpy()[0] == float(xs[2].float().abs().max())
+
+
 def test_precomputed_scales_match(snip):
     """Quantizing with g_in from snip_tensor_scales gives the same bits as
     letting the call compute the scale itself."""
