@@ -82,17 +82,18 @@ def lib():
         L.oracle_nvfp4_global_scale.argtypes = [ctypes.c_float]; L.oracle_nvfp4_global_scale.restype = ctypes.c_float
         L.oracle_fp8_tensor_scale.argtypes = [ctypes.c_float]; L.oracle_fp8_tensor_scale.restype = ctypes.c_float
         L.oracle_quantize_nvfp4.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp,
-                                            c_u8p, c_u8p, c_fp, c_dp]
+                                            c_u8p, c_u8p, c_fp, c_dp, ctypes.POINTER(ctypes.c_int64), i64]
         L.oracle_quantize_nvfp4.restype = i32
         L.oracle_dequant_nvfp4.argtypes = [c_u8p, c_u8p, ctypes.c_float, i64, i64, c_dp]
         L.oracle_dequant_nvfp4.restype = None
         L.oracle_e8m0_value.argtypes = [i32]; L.oracle_e8m0_value.restype = ctypes.c_double
         L.oracle_mxfp4_shared_exp.argtypes = [ctypes.c_float]; L.oracle_mxfp4_shared_exp.restype = i32
-        L.oracle_quantize_mxfp4.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_u8p, c_u8p]
+        c_i64p = ctypes.POINTER(ctypes.c_int64)
+        L.oracle_quantize_mxfp4.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_u8p, c_u8p, c_i64p, i64]
         L.oracle_quantize_mxfp4.restype = i32
         L.oracle_dequant_mxfp4.argtypes = [c_u8p, c_u8p, i64, i64, c_dp]
         L.oracle_dequant_mxfp4.restype = None
-        L.oracle_quantize_fp8.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp, c_u8p, c_fp]
+        L.oracle_quantize_fp8.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp, c_u8p, c_fp, c_i64p, i64]
         L.oracle_quantize_fp8.restype = i32
         L.oracle_dequant_fp8.argtypes = [c_u8p, ctypes.c_float, i64, c_dp]
         L.oracle_dequant_fp8.restype = None
@@ -232,14 +233,27 @@ class FP8:
         return out
 
 
+def _selection(rows):
+    """Output-row selection (None = all) -> (int64 array or None, pointer, count)."""
+    if rows is None:
+        return None, None, 0
+    sel = np.ascontiguousarray(rows, dtype=np.int64)
+    return sel, _ptr(sel, ctypes.c_int64), sel.shape[0]
+
+
 def quantize_nvfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0,
-                   g_in: float | None = None, want_block_err: bool = False) -> NVFP4:
+                   g_in: float | None = None, want_block_err: bool = False, rows=None) -> NVFP4:
     """NVFP4 quantization of a bf16 (rows, cols) tensor; orient=1 quantizes the
     transpose with blocks along the original rows (random bits still indexed
-    by the source element)."""
+    by the source element).  rows (optional): compute only these output rows
+    (tensor scale and random bits as for the whole tensor)."""
     b = _bits(x)
+    sel, psel, nsel = _selection(rows)
     rows, cols = b.shape
     OR, OC = (rows, cols) if orient == 0 else (cols, rows)
+    if sel is not None:
+        assert np.all((sel >= 0) & (sel < OR))
+        OR = nsel
     codes = np.zeros((OR, OC // 2), dtype=np.uint8)
     scales = np.zeros((OR, OC // 16), dtype=np.uint8)
     berr = np.zeros((OR, OC // 16), dtype=np.float64) if want_block_err else None
@@ -248,7 +262,7 @@ def quantize_nvfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id:
     st = lib().oracle_quantize_nvfp4(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
                                      gin, _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
                                      ctypes.byref(g),
-                                     _ptr(berr, ctypes.c_double) if berr is not None else None)
+                                     _ptr(berr, ctypes.c_double) if berr is not None else None, psel, nsel)
     if st == 1:
         raise NonFiniteInput("non-finite input")
     if st != 0:
@@ -257,31 +271,39 @@ def quantize_nvfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id:
 
 
 def quantize_fp8(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0,
-                 s_in: float | None = None) -> FP8:
+                 s_in: float | None = None, rows=None) -> FP8:
     b = _bits(x)
+    sel, psel, nsel = _selection(rows)
     rows, cols = b.shape
     OR, OC = (rows, cols) if orient == 0 else (cols, rows)
+    if sel is not None:
+        assert np.all((sel >= 0) & (sel < OR))
+        OR = nsel
     codes = np.zeros((OR, OC), dtype=np.uint8)
     s = ctypes.c_float()
     sin = ctypes.byref(ctypes.c_float(s_in)) if s_in is not None else None
     st = lib().oracle_quantize_fp8(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
-                                   sin, _ptr(codes, ctypes.c_uint8), ctypes.byref(s))
+                                   sin, _ptr(codes, ctypes.c_uint8), ctypes.byref(s), psel, nsel)
     if st == 1:
         raise NonFiniteInput("non-finite input")
     return FP8(codes, s.value, OR, OC)
 
 
-def quantize_mxfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0) -> MXFP4:
+def quantize_mxfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0, rows=None) -> MXFP4:
     """MXFP4 quantization (OCP Microscaling v1.0: 32 E2M1 values per E8M0
-    power-of-two scale) of a bf16 (rows, cols) tensor; orientation and random
-    bits as for NVFP4."""
+    power-of-two scale) of a bf16 (rows, cols) tensor; orientation, random
+    bits and the output-row selection as for NVFP4."""
     b = _bits(x)
+    sel, psel, nsel = _selection(rows)
     rows, cols = b.shape
     OR, OC = (rows, cols) if orient == 0 else (cols, rows)
+    if sel is not None:
+        assert np.all((sel >= 0) & (sel < OR))
+        OR = nsel
     codes = np.zeros((OR, OC // 2), dtype=np.uint8)
     scales = np.zeros((OR, OC // 32), dtype=np.uint8)
     st = lib().oracle_quantize_mxfp4(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
-                                     _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+                                     _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8), psel, nsel)
     if st == 1:
         raise NonFiniteInput("non-finite input")
     if st != 0:
@@ -289,13 +311,13 @@ def quantize_mxfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id:
     return MXFP4(codes, scales, OR, OC)
 
 
-def quantize(fmt: str, x, orient=0, rnd=RTN, seed=0, stream_id=0):
+def quantize(fmt: str, x, orient=0, rnd=RTN, seed=0, stream_id=0, rows=None):
     if fmt == "mxfp4":
-        return quantize_mxfp4(x, orient, rnd, seed, stream_id)
+        return quantize_mxfp4(x, orient, rnd, seed, stream_id, rows=rows)
     if fmt == "nvfp4":
-        return quantize_nvfp4(x, orient, rnd, seed, stream_id)
+        return quantize_nvfp4(x, orient, rnd, seed, stream_id, rows=rows)
     if fmt == "fp8":
-        return quantize_fp8(x, orient, rnd, seed, stream_id)
+        return quantize_fp8(x, orient, rnd, seed, stream_id, rows=rows)
     raise ValueError(fmt)
 
 

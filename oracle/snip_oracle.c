@@ -249,11 +249,15 @@ float oracle_nvfp4_global_scale(float amax) {
  *   scales       OR x OC/16 E4M3 bytes, row-major.
  *   g_out        the tensor scale used.
  *   block_sqerr  (nullable) OR x OC/16 sums of squared dequantization error.
+ *   sel, n_sel   (nullable) compute only output rows sel[0..n_sel) (the tensor
+ *                scale still comes from the whole tensor, the random bits from
+ *                each element's index in it); outputs then have n_sel rows.
  * Returns 0, or 1 if the input holds a non-finite value (outputs untouched),
  * or 2 on a shape error. */
 int oracle_quantize_nvfp4(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
                           uint64_t seed, uint64_t stream_id, const float* g_in,
-                          uint8_t* codes, uint8_t* scales, float* g_out, double* block_sqerr) {
+                          uint8_t* codes, uint8_t* scales, float* g_out, double* block_sqerr,
+                          const int64_t* sel, int64_t n_sel) {
     int64_t OR = orient == 0 ? rows : cols, OC = orient == 0 ? cols : rows;
     if (OC % 16 != 0) return 2;
     float amax;
@@ -261,7 +265,9 @@ int oracle_quantize_nvfp4(const uint16_t* x, int64_t rows, int64_t cols, int ori
     float g = g_in ? *g_in : oracle_nvfp4_global_scale(amax);
     *g_out = g;
     int64_t nb = OC / 16;
-    for (int64_t i = 0; i < OR; ++i) {
+    int64_t nout = sel ? n_sel : OR;
+    for (int64_t ii = 0; ii < nout; ++ii) {
+        int64_t i = sel ? sel[ii] : ii;   /* output row computed; results go to row ii */
         for (int64_t b = 0; b < nb; ++b) {
             float xs[16];
             uint64_t es[16];
@@ -275,7 +281,7 @@ int oracle_quantize_nvfp4(const uint16_t* x, int64_t rows, int64_t cols, int ori
             float six_g = 6.0f * g;
             float t = ab / six_g;
             int sb = oracle_e4m3_rtn(t);
-            scales[i * nb + b] = (uint8_t)sb;
+            scales[ii * nb + b] = (uint8_t)sb;
             float p = (float)oracle_e4m3_value(sb) * g;
             double q = oracle_e4m3_value(sb) * (double)g; /* exact step of one grid unit */
             double err = 0.0;
@@ -290,13 +296,13 @@ int oracle_quantize_nvfp4(const uint16_t* x, int64_t rows, int64_t cols, int ori
                 }
                 int code = sign | mag;
                 int64_t col = b * 16 + k;
-                uint8_t* byte = &codes[i * (OC / 2) + col / 2];
+                uint8_t* byte = &codes[ii * (OC / 2) + col / 2];
                 if ((col & 1) == 0) *byte = (uint8_t)((*byte & 0xf0) | code);
                 else *byte = (uint8_t)((*byte & 0x0f) | (code << 4));
                 double xhat = oracle_e2m1_value(code) * q;
                 err += (xhat - (double)xs[k]) * (xhat - (double)xs[k]);
             }
-            if (block_sqerr) block_sqerr[i * nb + b] = err;
+            if (block_sqerr) block_sqerr[ii * nb + b] = err;
         }
     }
     return 0;
@@ -350,15 +356,19 @@ int oracle_mxfp4_shared_exp(float amax) {
  * y = |x| * 2^-se (one fp32 multiplication by that power of two), code =
  * sign | E2M1(y) rounded as for NVFP4 (nearest, or stochastic with the same
  * random bits per source element).  Orientation and return values as for
- * NVFP4; codes OR x OC/2 bytes, scales OR x OC/32 bytes; needs OC % 32 == 0. */
+ * NVFP4; codes OR x OC/2 bytes, scales OR x OC/32 bytes; needs OC % 32 == 0;
+ * sel, n_sel as for NVFP4. */
 int oracle_quantize_mxfp4(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
-                          uint64_t seed, uint64_t stream_id, uint8_t* codes, uint8_t* scales) {
+                          uint64_t seed, uint64_t stream_id, uint8_t* codes, uint8_t* scales,
+                          const int64_t* sel, int64_t n_sel) {
     int64_t OR = orient == 0 ? rows : cols, OC = orient == 0 ? cols : rows;
     if (OC % 32 != 0) return 2;
     float amax;
     if (oracle_amax_bf16(x, rows * cols, &amax)) return 1;
     int64_t nb = OC / 32;
-    for (int64_t i = 0; i < OR; ++i) {
+    int64_t nout = sel ? n_sel : OR;
+    for (int64_t ii = 0; ii < nout; ++ii) {
+        int64_t i = sel ? sel[ii] : ii;
         for (int64_t b = 0; b < nb; ++b) {
             float xs[32];
             uint64_t es[32];
@@ -369,7 +379,7 @@ int oracle_quantize_mxfp4(const uint16_t* x, int64_t rows, int64_t cols, int ori
                 if (fabsf(xs[k]) > ab) ab = fabsf(xs[k]);
             }
             int se = oracle_mxfp4_shared_exp(ab);
-            scales[i * nb + b] = (uint8_t)(se + 127);
+            scales[ii * nb + b] = (uint8_t)(se + 127);
             float inv = (float)oracle_e8m0_value(127 - se);   /* 2^-se, exact in fp32 */
             for (int k = 0; k < 32; ++k) {
                 int sign = signbit(xs[k]) ? 8 : 0;
@@ -378,7 +388,7 @@ int oracle_quantize_mxfp4(const uint16_t* x, int64_t rows, int64_t cols, int ori
                                    : oracle_e2m1_sr(y, oracle_sr_bits(seed, stream_id, es[k]));
                 int code = sign | mag;
                 int64_t col = b * 32 + k;
-                uint8_t* byte = &codes[i * (OC / 2) + col / 2];
+                uint8_t* byte = &codes[ii * (OC / 2) + col / 2];
                 if ((col & 1) == 0) *byte = (uint8_t)((*byte & 0xf0) | code);
                 else *byte = (uint8_t)((*byte & 0x0f) | (code << 4));
             }
@@ -408,18 +418,20 @@ float oracle_fp8_tensor_scale(float amax) {
 
 /* Quantize a bf16 rows x cols tensor to E4M3 codes with one tensor scale s
  * (x ~ code * s).  Orientation, rounding and return values as for NVFP4;
- * codes is OR x OC bytes. */
+ * codes is OR x OC bytes; sel, n_sel as for NVFP4. */
 int oracle_quantize_fp8(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
                         uint64_t seed, uint64_t stream_id, const float* s_in,
-                        uint8_t* codes, float* s_out) {
+                        uint8_t* codes, float* s_out, const int64_t* sel, int64_t n_sel) {
     int64_t OR = orient == 0 ? rows : cols, OC = orient == 0 ? cols : rows;
     float amax;
     if (oracle_amax_bf16(x, rows * cols, &amax)) return 1;
     float s = s_in ? *s_in : oracle_fp8_tensor_scale(amax);
     *s_out = s;
     float inv = 1.0f / s;
-    for (int64_t i = 0; i < OR; ++i)
+    int64_t nout = sel ? n_sel : OR;
+    for (int64_t ii = 0; ii < nout; ++ii)
         for (int64_t k = 0; k < OC; ++k) {
+            int64_t i = sel ? sel[ii] : ii;
             uint64_t e = (uint64_t)src_index(orient, rows, cols, i, k);
             float xv = bf16_to_float(x[e]);
             int sign = signbit(xv) ? 0x80 : 0;
@@ -429,7 +441,7 @@ int oracle_quantize_fp8(const uint16_t* x, int64_t rows, int64_t cols, int orien
                 mag = rnd == 0 ? oracle_e4m3_rtn(y)
                                : oracle_e4m3_sr(y, oracle_sr_bits(seed, stream_id, e));
             }
-            codes[i * OC + k] = (uint8_t)(sign | mag);
+            codes[ii * OC + k] = (uint8_t)(sign | mag);
         }
     return 0;
 }
@@ -484,8 +496,8 @@ int oracle_quant_stats(const uint16_t* x, int64_t rows, int64_t cols, int rnd,
     double* bl4 = (double*)calloc((size_t)(n / 16 + 1), sizeof(double));
     if (!c4 || !s4 || !c8 || !bl4) { free(c4); free(s4); free(c8); free(bl4); return 3; }
     float g, s;
-    int st = oracle_quantize_nvfp4(x, rows, cols, 0, rnd, seed, stream_id, NULL, c4, s4, &g, bl4);
-    if (st == 0) st = oracle_quantize_fp8(x, rows, cols, 0, rnd, seed, stream_id, NULL, c8, &s);
+    int st = oracle_quantize_nvfp4(x, rows, cols, 0, rnd, seed, stream_id, NULL, c4, s4, &g, bl4, NULL, 0);
+    if (st == 0) st = oracle_quantize_fp8(x, rows, cols, 0, rnd, seed, stream_id, NULL, c8, &s, NULL, 0);
     if (st != 0) { free(c4); free(s4); free(c8); free(bl4); return st; }
     for (int k = 0; k < ST_N; ++k) out[k] = 0.0;
     float amax;

@@ -267,3 +267,20 @@ def test_shape_rule(oracle_lib):
         oracle_lib.quantize_nvfp4(bf16(np.ones((2, 24))))
     with pytest.raises(ValueError):
         oracle_lib.quantize_nvfp4(bf16(np.ones((24, 32))), orient=1)
+
+
+def test_output_row_selection_matches_full_quantization(oracle_lib):
+    """Quantizing only some output rows gives exactly those rows of the full
+    quantization (tensor scale from the whole tensor, random bits by each
+    element's index in it), for every format, orientation and rounding."""
+    g = torch.Generator().manual_seed(9)
+    x = (torch.randn(64, 96, generator=g) * 2).to(torch.bfloat16)
+    for fmt in ("nvfp4", "fp8", "mxfp4"):
+        for orient, sel in ((0, np.array([63, 2, 17, 40])), (1, np.array([95, 0, 40, 41]))):
+            for rnd in (oracle_lib.RTN, oracle_lib.SR):
+                full = oracle_lib.quantize(fmt, x, orient, rnd, 3, 5)
+                sub = oracle_lib.quantize(fmt, x, orient, rnd, 3, 5, rows=sel)
+                np.testing.assert_array_equal(full.codes[sel], sub.codes)
+                if fmt != "fp8":
+                    np.testing.assert_array_equal(full.scales[sel], sub.scales)
+                np.testing.assert_array_equal(full.dequant()[sel], sub.dequant())
