@@ -89,6 +89,14 @@ def lib():
         L.oracle_e8m0_value.argtypes = [i32]; L.oracle_e8m0_value.restype = ctypes.c_double
         L.oracle_mxfp4_shared_exp.argtypes = [ctypes.c_float]; L.oracle_mxfp4_shared_exp.restype = i32
         c_i64p = ctypes.POINTER(ctypes.c_int64)
+        L.oracle_e5m2_value.argtypes = [i32]; L.oracle_e5m2_value.restype = ctypes.c_double
+        L.oracle_e5m2_rtn.argtypes = [ctypes.c_float]; L.oracle_e5m2_rtn.restype = i32
+        L.oracle_e5m2_sr.argtypes = [ctypes.c_float, u32]; L.oracle_e5m2_sr.restype = i32
+        L.oracle_e5m2_tensor_scale.argtypes = [ctypes.c_float]; L.oracle_e5m2_tensor_scale.restype = ctypes.c_float
+        L.oracle_quantize_e5m2.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp, c_u8p, c_fp, c_i64p, i64]
+        L.oracle_quantize_e5m2.restype = i32
+        L.oracle_dequant_e5m2.argtypes = [c_u8p, ctypes.c_float, i64, c_dp]
+        L.oracle_dequant_e5m2.restype = None
         L.oracle_quantize_mxfp4.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_u8p, c_u8p, c_i64p, i64]
         L.oracle_quantize_mxfp4.restype = i32
         L.oracle_dequant_mxfp4.argtypes = [c_u8p, c_u8p, i64, i64, c_dp]
@@ -156,6 +164,18 @@ def e2m1_sr(y: float, u16: int) -> int:
 
 def e4m3_sr(y: float, u16: int) -> int:
     return lib().oracle_e4m3_sr(float(y), int(u16))
+
+
+def e5m2_value(code: int) -> float:
+    return lib().oracle_e5m2_value(int(code))
+
+
+def e5m2_rtn(t: float) -> int:
+    return lib().oracle_e5m2_rtn(float(t))
+
+
+def e5m2_sr(y: float, u16: int) -> int:
+    return lib().oracle_e5m2_sr(float(y), int(u16))
 
 
 def philox4x32_10(ctr, key):
@@ -289,6 +309,40 @@ def quantize_fp8(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: i
     return FP8(codes, s.value, OR, OC)
 
 
+class E5M2:
+    """An FP8 E5M2 tensor of shape (rows, cols) with one fp32 scale s."""
+
+    def __init__(self, codes, s, rows, cols):
+        self.codes, self.s, self.rows, self.cols = codes, s, rows, cols
+
+    def dequant(self) -> np.ndarray:
+        out = np.empty((self.rows, self.cols), dtype=np.float64)
+        lib().oracle_dequant_e5m2(_ptr(self.codes, ctypes.c_uint8), self.s, self.rows * self.cols,
+                                  _ptr(out, ctypes.c_double))
+        return out
+
+
+def quantize_e5m2(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0,
+                  s_in: float | None = None, rows=None) -> E5M2:
+    """FP8 E5M2 quantization with one tensor scale amax / 57344; orientation,
+    random bits and row selection as for the other formats."""
+    b = _bits(x)
+    sel, psel, nsel = _selection(rows)
+    rows, cols = b.shape
+    OR, OC = (rows, cols) if orient == 0 else (cols, rows)
+    if sel is not None:
+        assert np.all((sel >= 0) & (sel < OR))
+        OR = nsel
+    codes = np.zeros((OR, OC), dtype=np.uint8)
+    s = ctypes.c_float()
+    sin = ctypes.byref(ctypes.c_float(s_in)) if s_in is not None else None
+    st = lib().oracle_quantize_e5m2(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
+                                    sin, _ptr(codes, ctypes.c_uint8), ctypes.byref(s), psel, nsel)
+    if st == 1:
+        raise NonFiniteInput("non-finite input")
+    return E5M2(codes, s.value, OR, OC)
+
+
 def quantize_mxfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0, rows=None) -> MXFP4:
     """MXFP4 quantization (OCP Microscaling v1.0: 32 E2M1 values per E8M0
     power-of-two scale) of a bf16 (rows, cols) tensor; orientation, random
@@ -312,6 +366,8 @@ def quantize_mxfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id:
 
 
 def quantize(fmt: str, x, orient=0, rnd=RTN, seed=0, stream_id=0, rows=None):
+    if fmt == "e5m2":
+        return quantize_e5m2(x, orient, rnd, seed, stream_id, rows=rows)
     if fmt == "mxfp4":
         return quantize_mxfp4(x, orient, rnd, seed, stream_id, rows=rows)
     if fmt == "nvfp4":

@@ -155,6 +155,62 @@ int oracle_e4m3_sr(float y, uint32_t u16) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits; exponent 31 holds    */
+/* infinities and NaNs, the largest finite magnitude is 57344 (code 0x7b).   */
+/* The gradient format of FP8 training recipes; here the NEXT-2 variant for  */
+/* dY and dY^T.                                                              */
+/* ------------------------------------------------------------------------ */
+
+double oracle_e5m2_value(int code) {
+    int s = (code >> 7) & 1, e = (code >> 2) & 31, m = code & 3;
+    if (e == 31) return m == 0 ? (s ? -INFINITY : INFINITY) : NAN;
+    double mag = (e == 0) ? ldexp((double)m, -16) : ldexp(1.0 + m / 4.0, e - 15);
+    return s ? -mag : mag;
+}
+
+/* The 124 finite non-negative E5M2 values in code order (0x00..0x7b), which
+ * is also ascending order. */
+static double e5m2_table[0x7c];
+static int e5m2_table_ready = 0;
+static void e5m2_table_init(void) {
+    if (e5m2_table_ready) return;
+    for (int c = 0; c <= 0x7b; ++c) e5m2_table[c] = oracle_e5m2_value(c);
+    e5m2_table_ready = 1;
+}
+
+static int e5m2_floor_code(double y) {
+    e5m2_table_init();
+    int lo = 0, hi = 0x7b;
+    if (y >= e5m2_table[hi]) return hi;
+    while (hi - lo > 1) {          /* invariant: value(lo) <= y < value(hi) */
+        int mid = (lo + hi) / 2;
+        if (e5m2_table[mid] <= y) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+/* Nearest finite E5M2 magnitude code to t >= 0, ties to even, saturating at 57344. */
+int oracle_e5m2_rtn(float t) {
+    int c = e5m2_floor_code((double)t);
+    if (c == 0x7b) return c;
+    double dlo = (double)t - e5m2_table[c], dhi = e5m2_table[c + 1] - (double)t;
+    if (dlo < dhi) return c;
+    if (dhi < dlo) return c + 1;
+    return (c & 1) == 0 ? c : c + 1;
+}
+
+/* Stochastic rounding of y >= 0 onto the finite E5M2 grid (the rule of
+ * oracle_e2m1_sr); y >= 57344 gives 57344. */
+int oracle_e5m2_sr(float y, uint32_t u16) {
+    if (y >= 57344.0f) return 0x7b;
+    int lo = e5m2_floor_code((double)y);
+    double vlo = e5m2_table[lo], vhi = e5m2_table[lo + 1];
+    double frac = ((double)y - vlo) / (vhi - vlo);
+    uint32_t thr = (uint32_t)floor(frac * 65536.0);
+    return (u16 < thr) ? lo + 1 : lo;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As   */
 /* Easy as 1, 2, 3", SC'11): a 4x32-bit counter, 2x32-bit key, ten rounds of */
 /* two 32x32->64 multiplies, with a Weyl-sequence key schedule.              */
@@ -448,6 +504,46 @@ int oracle_quantize_fp8(const uint16_t* x, int64_t rows, int64_t cols, int orien
 
 void oracle_dequant_fp8(const uint8_t* codes, float s, int64_t n, double* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(codes[i]) * (double)s;
+}
+
+/* E5M2 with one tensor scale s = amax / 57344 (1 for an all-zero tensor) or
+ * *s_in: code = sign | E5M2(|x| * (1/s)), nearest-even saturating (RTN) or
+ * stochastic with the element's 16 Philox bits (SR).  Orientation, row
+ * selection and return values as for oracle_quantize_fp8. */
+float oracle_e5m2_tensor_scale(float amax) {
+    if (amax == 0.0f) return 1.0f;
+    return amax / 57344.0f;
+}
+
+int oracle_quantize_e5m2(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
+                         uint64_t seed, uint64_t stream_id, const float* s_in,
+                         uint8_t* codes, float* s_out, const int64_t* sel, int64_t n_sel) {
+    int64_t OR = orient == 0 ? rows : cols, OC = orient == 0 ? cols : rows;
+    float amax;
+    if (oracle_amax_bf16(x, rows * cols, &amax)) return 1;
+    float s = s_in ? *s_in : oracle_e5m2_tensor_scale(amax);
+    *s_out = s;
+    float inv = 1.0f / s;
+    int64_t nout = sel ? n_sel : OR;
+    for (int64_t ii = 0; ii < nout; ++ii)
+        for (int64_t k = 0; k < OC; ++k) {
+            int64_t i = sel ? sel[ii] : ii;
+            uint64_t e = (uint64_t)src_index(orient, rows, cols, i, k);
+            float xv = bf16_to_float(x[e]);
+            int sign = signbit(xv) ? 0x80 : 0;
+            int mag = 0;
+            if (xv != 0.0f) {
+                float y = fabsf(xv) * inv;
+                mag = rnd == 0 ? oracle_e5m2_rtn(y)
+                               : oracle_e5m2_sr(y, oracle_sr_bits(seed, stream_id, e));
+            }
+            codes[ii * OC + k] = (uint8_t)(sign | mag);
+        }
+    return 0;
+}
+
+void oracle_dequant_e5m2(const uint8_t* codes, float s, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e5m2_value(codes[i]) * (double)s;
 }
 
 /* ------------------------------------------------------------------------ */
