@@ -69,8 +69,17 @@ typedef enum {
  * scale, plus an fp32 tensor scale ("FP4 all the way", Outline).  MXFP4: 32
  * E2M1 values per E8M0 power-of-two block scale, no tensor scale (OCP
  * Microscaling Formats v1.0; the block-size / scale-format alternative that
- * the FP4 study weighs NVFP4 against). */
-typedef enum { SNIP_FMT_FP8_E4M3 = 0, SNIP_FMT_NVFP4 = 1, SNIP_FMT_MXFP4 = 2 } snip_format;
+ * the FP4 study weighs NVFP4 against).  FP8_E5M2: one fp32 tensor scale
+ * s = amax / 57344, for gradients; as a GEMM format it means A in E5M2 and B
+ * in E4M3.  FP8_E5M2_GRAD is a layer format only (plans): E5M2 for dY and
+ * dY^T, E4M3 for X, W, W^T and X^T. */
+typedef enum {
+    SNIP_FMT_FP8_E4M3 = 0,
+    SNIP_FMT_NVFP4 = 1,
+    SNIP_FMT_MXFP4 = 2,
+    SNIP_FMT_FP8_E5M2 = 3,
+    SNIP_FMT_FP8_E5M2_GRAD = 4
+} snip_format;
 typedef enum { SNIP_RTN = 0, SNIP_SR = 1 } snip_round;
 
 /* Orientation of a quantization of a rows x cols tensor.
@@ -83,7 +92,7 @@ typedef enum { SNIP_BLOCKS_ALONG_COLS = 0, SNIP_BLOCKS_ALONG_ROWS = 1 } snip_ori
  * ROWMAJOR: NVFP4 codes OR x OC/2 bytes (element 2j in bits 0..3 of byte j,
  *           bit 3 of each code the sign), E4M3 scales OR x OC/16 bytes;
  *           MXFP4 codes the same, E8M0 scales OR x OC/32 bytes;
- *           FP8 codes OR x OC bytes.
+ *           FP8 (E4M3 or E5M2) codes OR x OC bytes.
  * MMA:      the GEMM operand layout.  Rows are padded to ORp = roundup(OR,256)
  *           and the contraction to OCp = roundup(OC,256) for NVFP4 (128 for
  *           FP8), padding filled with zero codes and zero scales.  Codes are
@@ -252,6 +261,20 @@ snip_status snip_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, snip_
                                 snip_round rnd, uint64_t seed, uint64_t stream_id, snip_layout layout,
                                 uint8_t* codes, uint8_t* scales, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- NEXT-2: FP8 E5M2 gradients */
+
+/* FP8 E5M2 quantization with one fp32 tensor scale s = amax / 57344 (1 for an
+ * all-zero tensor): code = sign | E5M2(|x| * (1/s)), nearest-even saturating at
+ * 57344 (RTN) or stochastic with 16 Philox bits (SR) -- the gradient format of
+ * the FP8 variant (a NEXT-2 format alternative; the pages' FP8 is E4M3).
+ * amax_in (device, nullable): the tensor's amax (scales_out[0] of
+ * snip_tensor_scales); NULL computes it.  s_out (device) receives s.
+ * Orientation, layout and errors as for snip_quantize_fp8. */
+snip_status snip_quantize_e5m2(const void* x, int64_t rows, int64_t cols, snip_orient orient,
+                               snip_round rnd, uint64_t seed, uint64_t stream_id, const float* amax_in,
+                               snip_layout layout, uint8_t* codes, float* s_out,
+                               void* ws, size_t ws_bytes, void* stream);
+
 /* Bytes of the code and scale buffers of a quantization whose output has
  * out_rows rows and contraction out_cols, in `layout`.  Host-only. */
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
@@ -262,7 +285,8 @@ snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t ou
 /* D[m, n] = ga * gb * sum_k A[m, k] B[n, k] for m < M, n < N, fp32 output with
  * row pitch ldd (elements).  A (M rows) and B (N rows) are quantized operands
  * in the MMA layout with contraction K; ga/gb are device floats (NVFP4: the
- * tensor scales g; FP8: the tensor scales s; MXFP4: unused, may be NULL).
+ * tensor scales g; FP8: the tensor scales s; MXFP4: unused, may be NULL;
+ * FP8_E5M2: A is E5M2 with its scale s5, B is E4M3 with its scale s).
  * NVFP4 uses the tensor cores' block-scaled FP4 MMA with E4M3 block scales
  * (scale_vec::4X), MXFP4 the same MMA with E8M0 scales (scale_vec::2X), FP8
  * the E4M3 x E4M3 MMA.  Accumulation is fp32.  Needs K % 16 == 0 (MXFP4:
@@ -277,7 +301,8 @@ snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_
 /* ---------------------------------------------------------------- plan */
 
 /* A per-layer precision plan (SNIP, Abstract: one format per layer).  formats
- * (host, n_layers entries) are snip_format values.  Every layer starts with
+ * (host, n_layers entries) are snip_format values: FP8_E4M3, NVFP4, MXFP4 or
+ * FP8_E5M2_GRAD (not FP8_E5M2, an operand format).  Every layer starts with
  * the rounding of "FP4 all the way": RTN for the forward quantizations (tags
  * X_FWD, W_FWD) and SR for the four backward ones.  *out is a host object
  * owned by the caller (snip_plan_destroy). */

@@ -71,8 +71,29 @@ inline snip_status cuda_status(cudaError_t e) {
 inline int64_t mma_rows(int64_t r) { return round_up(r, 256); }
 inline bool is_fp4(int snip_fmt) { return snip_fmt == SNIP_FMT_NVFP4 || snip_fmt == SNIP_FMT_MXFP4; }
 inline int64_t mma_cols(int snip_fmt, int64_t c) { return round_up(c, is_fp4(snip_fmt) ? 256 : 128); }
-// kernel format ids: 0 FP8, 1 NVFP4, 2 MXFP4
-inline int kernel_fmt(int snip_fmt) { return snip_fmt == SNIP_FMT_NVFP4 ? 1 : snip_fmt == SNIP_FMT_MXFP4 ? 2 : 0; }
+// quantizer kernel format ids: 0 FP8 E4M3, 1 NVFP4, 2 MXFP4, 3 FP8 E5M2
+inline int kernel_fmt(int snip_fmt) {
+  return snip_fmt == SNIP_FMT_NVFP4 ? 1 : snip_fmt == SNIP_FMT_MXFP4 ? 2 : snip_fmt == SNIP_FMT_FP8_E5M2 ? 3 : 0;
+}
+// GEMM kernel format ids: 0 FP8 (A E4M3 or E5M2), 1 NVFP4, 2 MXFP4
+inline int gemm_kernel_fmt(int snip_fmt) {
+  return snip_fmt == SNIP_FMT_NVFP4 ? 1 : snip_fmt == SNIP_FMT_MXFP4 ? 2 : 0;
+}
+// Which float of a tensor-scale slot {amax, g, s, s5} a quantization reads:
+// NVFP4 g (MXFP4 only checks it for NaN), FP8 s, E5M2 the amax (the kernel
+// derives s5 = amax / 57344 and writes it as g_out).
+inline int scale_index(int snip_fmt) {
+  return snip_fmt == SNIP_FMT_FP8_E4M3 ? 2 : snip_fmt == SNIP_FMT_FP8_E5M2 ? 0 : 1;
+}
+// ... and which one the GEMM epilogue multiplies by (null: none).
+inline const float* gemm_scale(const float* slot, int snip_fmt) {
+  return snip_fmt == SNIP_FMT_FP8_E4M3 ? slot + 2 : snip_fmt == SNIP_FMT_FP8_E5M2 ? slot + 3
+         : snip_fmt == SNIP_FMT_MXFP4 ? nullptr : slot + 1;
+}
+// Operand formats of a layer format: a layer with E5M2 gradients quantizes
+// dY and dY^T in E5M2 and everything else in E4M3.
+inline int forward_fmt(int layer_fmt) { return layer_fmt == SNIP_FMT_FP8_E5M2_GRAD ? SNIP_FMT_FP8_E4M3 : layer_fmt; }
+inline int gradient_fmt(int layer_fmt) { return layer_fmt == SNIP_FMT_FP8_E5M2_GRAD ? SNIP_FMT_FP8_E5M2 : layer_fmt; }
 // elements per block along the blocked dim
 inline int64_t block_elems(int snip_fmt) { return snip_fmt == SNIP_FMT_MXFP4 ? 32 : 16; }
 
@@ -139,11 +160,11 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   }
   // an empty output still publishes its tensor scale: the one-CTA row kernel does that
   if (p.orp == 0 || p.ocp == 0) orient = SNIP_BLOCKS_ALONG_COLS;
-  if (fmt == SNIP_FMT_MXFP4 && raw_out) {
-    // MXFP4 codes, then the statistics in their own pass (same rounding and random bits)
+  if ((fmt == SNIP_FMT_MXFP4 || fmt == SNIP_FMT_FP8_E5M2) && raw_out) {
+    // MXFP4 / E5M2 codes, then the statistics in their own pass (same rounding and random bits)
     p.scales3 = nullptr;
     p.raw_out = nullptr;
-    cudaError_t e = launch_quant(2, p, orient, layout, rnd, false, num_sms, st);
+    cudaError_t e = launch_quant(kernel_fmt(fmt), p, orient, layout, rnd, false, num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     StatsParams sp = {};
     sp.x = p.x;
@@ -169,7 +190,7 @@ snip_status run_quantize_api(int fmt, const void* x, int64_t rows, int64_t cols,
     float* slot = scale_slot(ws, 0);
     snip_status s = run_scales(x, rows * cols, slot, ws, num_sms, st);
     if (s != SNIP_OK) return s;
-    scale = slot + (fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1);   // MXFP4 reads it only to detect non-finite input
+    scale = slot + scale_index(fmt);
   }
   return run_quantize(fmt, x, rows, cols, orient, rnd, seed, stream_id, scale, layout, codes, scales, g_out,
                       block_err, num_sms, st);
@@ -192,7 +213,8 @@ snip_status run_gemm(int fmt, const uint8_t* a_codes, const uint8_t* a_scales, c
   p.status = ws_at<uint32_t>(ws, kOffStatus);
   p.timeout_ns = kTimeoutNs;
   if (fmt == SNIP_FMT_MXFP4) p.ga = p.gb = nullptr;   // no tensor scales
-  return cuda_status(launch_gemm(kernel_fmt(fmt), a_codes, mma_rows(M), b_codes, mma_rows(N), p, num_sms, st));
+  p.a_e5m2 = fmt == SNIP_FMT_FP8_E5M2;
+  return cuda_status(launch_gemm(gemm_kernel_fmt(fmt), a_codes, mma_rows(M), b_codes, mma_rows(N), p, num_sms, st));
 }
 
 bool valid_enum(int v, int n) { return v >= 0 && v < n; }
@@ -289,7 +311,7 @@ snip_status snip_tensor_scales_multi(int count, const void* const* xs, const int
 
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
                                  size_t* codes_bytes, size_t* scales_bytes) {
-  if (!valid_enum(fmt, 3) || !valid_enum(layout, 2) || out_rows < 0 || out_cols < 0) return SNIP_ERR_INVALID_ARG;
+  if (!valid_enum(fmt, 4) || !valid_enum(layout, 2) || out_rows < 0 || out_cols < 0) return SNIP_ERR_INVALID_ARG;
   OperandBytes b = operand_bytes(fmt, layout, out_rows, out_cols);
   if (codes_bytes) *codes_bytes = b.codes;
   if (scales_bytes) *scales_bytes = b.scales;
@@ -350,13 +372,25 @@ snip_status snip_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, snip_
                           nullptr, nullptr, ws, sms, static_cast<cudaStream_t>(stream));
 }
 
+snip_status snip_quantize_e5m2(const void* x, int64_t rows, int64_t cols, snip_orient orient, snip_round rnd,
+                               uint64_t seed, uint64_t stream_id, const float* amax_in, snip_layout layout,
+                               uint8_t* codes, float* s_out, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  s = check_quantize_args(SNIP_FMT_FP8_E5M2, x, rows, cols, orient, rnd, layout, codes, nullptr, s_out, ws, ws_bytes);
+  if (s != SNIP_OK) return s;
+  return run_quantize_api(SNIP_FMT_FP8_E5M2, x, rows, cols, orient, rnd, seed, stream_id, amax_in, layout, codes,
+                          nullptr, s_out, nullptr, ws, sms, static_cast<cudaStream_t>(stream));
+}
+
 snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
                       const uint8_t* b_codes, const uint8_t* b_scales, const float* gb, int64_t M, int64_t N,
                       int64_t K, float* D, int64_t ldd, void* ws, size_t ws_bytes, void* stream) {
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
-  if (!valid_enum(fmt, 3) || M < 0 || N < 0 || K < 0 || ldd < N) return SNIP_ERR_INVALID_ARG;
+  if (!valid_enum(fmt, 4) || M < 0 || N < 0 || K < 0 || ldd < N) return SNIP_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return SNIP_OK;
   if (!a_codes || !b_codes || !D) return SNIP_ERR_INVALID_ARG;
   if (fmt != SNIP_FMT_MXFP4 && (!ga || !gb)) return SNIP_ERR_INVALID_ARG;
@@ -375,7 +409,7 @@ snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_
 snip_status snip_plan_create(int n_layers, const int* formats, uint64_t seed, snip_plan** out) {
   if (n_layers <= 0 || !formats || !out) return SNIP_ERR_INVALID_ARG;
   for (int i = 0; i < n_layers; ++i)
-    if (!valid_enum(formats[i], 3)) return SNIP_ERR_INVALID_ARG;
+    if (!valid_enum(formats[i], 5) || formats[i] == SNIP_FMT_FP8_E5M2) return SNIP_ERR_INVALID_ARG;
   snip_plan* p = new (std::nothrow) snip_plan;
   if (!p) return SNIP_ERR_INVALID_ARG;
   p->fmt.assign(formats, formats + n_layers);
@@ -447,7 +481,7 @@ snip_status check_ql(const snip_plan* plan, int layer, int64_t T, int64_t K, int
 
 size_t snip_qlinear_workspace_size(const snip_plan* plan, int layer, int64_t T, int64_t K, int64_t N) {
   if (check_ql(plan, layer, T, K, N) != SNIP_OK) return 0;
-  const int fmt = plan->fmt[layer];
+  const int fmt = forward_fmt(plan->fmt[layer]);   // E5M2 operands have E4M3's size
   size_t a = ql_layout(fmt, T, K, N, false).total, b = ql_layout(fmt, T, K, N, true).total;
   return a > b ? a : b;
 }
@@ -462,12 +496,11 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
   if (!ws || ws_bytes < snip_qlinear_workspace_size(plan, layer, T, K, N)) return SNIP_ERR_WORKSPACE;
   if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(ws)) return SNIP_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int fmt = plan->fmt[layer];
+  const int qf = forward_fmt(plan->fmt[layer]);   // format of X and W
   const int* rnd = &plan->rnd[(size_t)layer * 6];
   const uint64_t sid = (uint64_t)layer * 8;
-  QlLayout L = ql_layout(fmt, T, K, N, false);
+  QlLayout L = ql_layout(qf, T, K, N, false);
   uint8_t* b = static_cast<uint8_t*>(ws);
-  const int si = fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1;   // which tensor scale the format uses (MXFP4: none; g only flags non-finite input)
   float* sx = scale_slot(ws, 0);
   float* sw = scale_slot(ws, 1);
   {
@@ -476,16 +509,16 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
     float* outs[2] = {sx, sw};
     if ((s = run_scales_multi(2, xs, ns, outs, ws, sms, st)) != SNIP_OK) return s;
   }
-  if ((s = run_quantize(fmt, X, T, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_X_FWD], plan->seed, sid + SNIP_TAG_X_FWD,
-                        sx + si, SNIP_LAYOUT_MMA, b + L.op[0].codes_off, b + L.op[0].scales_off, nullptr, nullptr,
-                        sms, st, sx, stats_out, ws)) != SNIP_OK)
+  if ((s = run_quantize(qf, X, T, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_X_FWD], plan->seed, sid + SNIP_TAG_X_FWD,
+                        sx + scale_index(qf), SNIP_LAYOUT_MMA, b + L.op[0].codes_off, b + L.op[0].scales_off, nullptr,
+                        nullptr, sms, st, sx, stats_out, ws)) != SNIP_OK)
     return s;
-  if ((s = run_quantize(fmt, W, N, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_W_FWD], plan->seed, sid + SNIP_TAG_W_FWD,
-                        sw + si, SNIP_LAYOUT_MMA, b + L.op[1].codes_off, b + L.op[1].scales_off, nullptr, nullptr,
-                        sms, st, sw, stats_out ? stats_out + SNIP_STATS_NVALS : nullptr, ws)) != SNIP_OK)
+  if ((s = run_quantize(qf, W, N, K, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_W_FWD], plan->seed, sid + SNIP_TAG_W_FWD,
+                        sw + scale_index(qf), SNIP_LAYOUT_MMA, b + L.op[1].codes_off, b + L.op[1].scales_off, nullptr,
+                        nullptr, sms, st, sw, stats_out ? stats_out + SNIP_STATS_NVALS : nullptr, ws)) != SNIP_OK)
     return s;
-  return run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, sx + si, b + L.op[1].codes_off,
-                  b + L.op[1].scales_off, sw + si, T, N, K, Y, N, ws, sms, st);
+  return run_gemm(qf, b + L.op[0].codes_off, b + L.op[0].scales_off, gemm_scale(sx, qf), b + L.op[1].codes_off,
+                  b + L.op[1].scales_off, gemm_scale(sw, qf), T, N, K, Y, N, ws, sms, st);
 }
 
 snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W, const void* dY,
@@ -500,15 +533,16 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
   if (!aligned16(X) || !aligned16(W) || !aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(ws))
     return SNIP_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int fmt = plan->fmt[layer];
+  const int qg = gradient_fmt(plan->fmt[layer]);   // format of dY and dY^T (the GEMMs' A operands)
+  const int qf = forward_fmt(plan->fmt[layer]);    // format of W^T and X^T
   const int* rnd = &plan->rnd[(size_t)layer * 6];
   const uint64_t sid = (uint64_t)layer * 8;
-  QlLayout L = ql_layout(fmt, T, K, N, true);
+  QlLayout L = ql_layout(qf, T, K, N, true);
   uint8_t* b = static_cast<uint8_t*>(ws);
-  const int si = fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1;
   float* sx = scale_slot(ws, 0);
   float* sw = scale_slot(ws, 1);
   float* sd = scale_slot(ws, 2);
+  float* sd_out = qg == SNIP_FMT_FP8_E5M2 ? sd + 3 : nullptr;   // E5M2: the quantizer publishes s5 here
   {
     const void* xs[3] = {dY, W, X};
     const int64_t ns[3] = {T * N, N * K, T * K};
@@ -516,28 +550,28 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
     if ((s = run_scales_multi(3, xs, ns, outs, ws, sms, st)) != SNIP_OK) return s;
   }
   // dgrad: dX = Q(dY) Q(W^T)^T, contraction N
-  if ((s = run_quantize(fmt, dY, T, N, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_DY_DGRAD], plan->seed,
-                        sid + SNIP_TAG_DY_DGRAD, sd + si, SNIP_LAYOUT_MMA, b + L.op[0].codes_off,
-                        b + L.op[0].scales_off, nullptr, nullptr, sms, st, sd, stats_out, ws)) != SNIP_OK)
+  if ((s = run_quantize(qg, dY, T, N, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_DY_DGRAD], plan->seed,
+                        sid + SNIP_TAG_DY_DGRAD, sd + scale_index(qg), SNIP_LAYOUT_MMA, b + L.op[0].codes_off,
+                        b + L.op[0].scales_off, sd_out, nullptr, sms, st, sd, stats_out, ws)) != SNIP_OK)
     return s;
-  if ((s = run_quantize(fmt, W, N, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_WT_DGRAD], plan->seed,
-                        sid + SNIP_TAG_WT_DGRAD, sw + si, SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
+  if ((s = run_quantize(qf, W, N, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_WT_DGRAD], plan->seed,
+                        sid + SNIP_TAG_WT_DGRAD, sw + scale_index(qf), SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
                         b + L.op[1].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
     return s;
-  if ((s = run_gemm(fmt, b + L.op[0].codes_off, b + L.op[0].scales_off, sd + si, b + L.op[1].codes_off,
-                    b + L.op[1].scales_off, sw + si, T, K, N, dX, K, ws, sms, st)) != SNIP_OK)
+  if ((s = run_gemm(qg, b + L.op[0].codes_off, b + L.op[0].scales_off, gemm_scale(sd, qg), b + L.op[1].codes_off,
+                    b + L.op[1].scales_off, gemm_scale(sw, qf), T, K, N, dX, K, ws, sms, st)) != SNIP_OK)
     return s;
   // wgrad: dW = Q(dY^T) Q(X^T)^T, contraction T
-  if ((s = run_quantize(fmt, dY, T, N, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_DYT_WGRAD], plan->seed,
-                        sid + SNIP_TAG_DYT_WGRAD, sd + si, SNIP_LAYOUT_MMA, b + L.op[2].codes_off,
-                        b + L.op[2].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
+  if ((s = run_quantize(qg, dY, T, N, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_DYT_WGRAD], plan->seed,
+                        sid + SNIP_TAG_DYT_WGRAD, sd + scale_index(qg), SNIP_LAYOUT_MMA, b + L.op[2].codes_off,
+                        b + L.op[2].scales_off, sd_out, nullptr, sms, st)) != SNIP_OK)
     return s;
-  if ((s = run_quantize(fmt, X, T, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_XT_WGRAD], plan->seed,
-                        sid + SNIP_TAG_XT_WGRAD, sx + si, SNIP_LAYOUT_MMA, b + L.op[3].codes_off,
+  if ((s = run_quantize(qf, X, T, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_XT_WGRAD], plan->seed,
+                        sid + SNIP_TAG_XT_WGRAD, sx + scale_index(qf), SNIP_LAYOUT_MMA, b + L.op[3].codes_off,
                         b + L.op[3].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
     return s;
-  return run_gemm(fmt, b + L.op[2].codes_off, b + L.op[2].scales_off, sd + si, b + L.op[3].codes_off,
-                  b + L.op[3].scales_off, sx + si, N, K, T, dW, K, ws, sms, st);
+  return run_gemm(qg, b + L.op[2].codes_off, b + L.op[2].scales_off, gemm_scale(sd, qg), b + L.op[3].codes_off,
+                  b + L.op[3].scales_off, gemm_scale(sx, qf), N, K, T, dW, K, ws, sms, st);
 }
 
 // ---------------------------------------------------------------- statistics
@@ -580,7 +614,7 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
-  if (!valid_enum(fmt, 3) || !raw_out) return SNIP_ERR_INVALID_ARG;
+  if (!valid_enum(fmt, 4) || !raw_out) return SNIP_ERR_INVALID_ARG;
   float g_dummy;   // validation only: g_out is not written by this entry point
   s = check_quantize_args(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, layout, codes,
                           is_fp4(fmt) ? scales : nullptr, &g_dummy, ws, ws_bytes);
@@ -592,9 +626,8 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
     if ((s = run_scales(x, rows * cols, slot, ws, sms, st)) != SNIP_OK) return s;
     sc = slot;
   }
-  return run_quantize(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, seed, stream_id,
-                      sc + (fmt == SNIP_FMT_FP8_E4M3 ? 2 : 1), layout, codes, scales, nullptr, nullptr, sms, st, sc,
-                      raw_out, ws);
+  return run_quantize(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, seed, stream_id, sc + scale_index(fmt), layout,
+                      codes, scales, nullptr, nullptr, sms, st, sc, raw_out, ws);
 }
 
 // ---------------------------------------------------------------- NEXT-4: dW-level sqrt(3) check

@@ -69,7 +69,7 @@ struct GemmCfg {
   // and 10-12, K-major, N>>3 in bits 17-22, scale type in bit 23 (UE4M3 0 for
   // NVFP4, UE8M0 1 for MXFP4), M>>4 in bits 24-28; MXFP4's scale-factor IDs
   // (bits 4-5 for B, 29-30 for A) are set per MMA.  FP8: D type f32 (1) in
-  // bits 4-5, A/B type E4M3 (0).
+  // bits 4-5, A/B type E4M3 (0) in bits 7-9 and 10-12 (A may be E5M2, 1, per GEMM).
   static constexpr uint32_t IDESC =
       FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((FMT == 2 ? 1u : 0u) << 23) |
              ((uint32_t)(BM >> 4) << 24))
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(448, 1)
             else if (FMT == 2)   // chunk word k/2, byte pair 2*(k%2) as the scale-factor ID of A and B
               tc_mma_mxf4(d_tmem, adesc, bdesc, C::IDESC | ((2u * (k & 1)) << 4) | ((2u * (k & 1)) << 29),
                           sf + 4 * (k >> 1), sf + C::SFA_COLS + (k >> 1) * (BN / 32), accum);
-            else tc_mma_f8(d_tmem, adesc, bdesc, C::IDESC, accum);
+            else tc_mma_f8(d_tmem, adesc, bdesc, C::IDESC | ((uint32_t)p.a_e5m2 << 7), accum);   // A type E5M2 = 1
           }
           tc_commit(empty(stage));
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(448, 1)
             else if (FMT == 2)
               tc_mma_mxf4_pair(d_tmem, adesc, bdesc, C::IDESC | ((2u * (k & 1)) << 4) | ((2u * (k & 1)) << 29),
                                sf + 4 * (k >> 1), sf + C::SFA_COLS + (k >> 1) * C::SFB_COLS_K, accum);
-            else tc_mma_f8_pair(d_tmem, adesc, bdesc, C::IDESC, accum);
+            else tc_mma_f8_pair(d_tmem, adesc, bdesc, C::IDESC | ((uint32_t)p.a_e5m2 << 7), accum);
           }
           tc_commit_pair_mc(empty(stage), 0x3);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }

@@ -207,29 +207,38 @@ __device__ __forceinline__ float nvfp4_block_err(const float (&v)[16], const uin
   return e;
 }
 
-// Encode 16 signed values to E4M3 with the tensor scale's inverse.
-template <int RND>
+// Encode 16 signed values to E4M3 (E5 false) or E5M2 (E5 true) with the
+// tensor scale's inverse.
+template <int RND, bool E5 = false>
 __device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, const uint32_t (&u)[8]) {
+  constexpr uint32_t kMaxCode = E5 ? 0x7bu : 0x7eu;
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   if (!(inv < kInf)) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t sign = (__float_as_uint(v[i]) >> 24) & 0x80u;
-      w[i >> 2] |= (sign | (v[i] == 0.0f ? 0u : 0x7eu)) << (8 * (i & 3));
+      w[i >> 2] |= (sign | (v[i] == 0.0f ? 0u : kMaxCode)) << (8 * (i & 3));
     }
   } else if (RND == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      w[i >> 1] |= e4m3x2_rn_sat(__fmul_rn(v[2 * i], inv), __fmul_rn(v[2 * i + 1], inv)) << (16 * (i & 1));
+    for (int i = 0; i < 8; ++i) {
+      const float a = __fmul_rn(v[2 * i], inv), b = __fmul_rn(v[2 * i + 1], inv);
+      w[i >> 1] |= (E5 ? e5m2x2_rn_sat(a, b) : e4m3x2_rn_sat(a, b)) << (16 * (i & 1));
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t b = __float_as_uint(v[i]);
       const float y = __fmul_rn(__uint_as_float(b & 0x7fffffffu), inv);
-      w[i >> 2] |= (((b >> 24) & 0x80u) | e4m3_sr(y, uhalf(u, i))) << (8 * (i & 3));
+      w[i >> 2] |= (((b >> 24) & 0x80u) | (E5 ? e5m2_sr(y, uhalf(u, i)) : e4m3_sr(y, uhalf(u, i)))) << (8 * (i & 3));
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// E5M2 tensor scale from the tensor's amax: amax / 57344 (1 for zero; NaN stays NaN).
+__device__ __forceinline__ float e5m2_tensor_scale(float amax) {
+  return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 57344.0f);
 }
 
 // ------------------------------------------------------------------ a8: statistics
@@ -395,8 +404,9 @@ __device__ __forceinline__ void stats_nan(double* raw_out) {
 // 32-element block and share its scale through a shuffle; no statistics).
 template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
-  static_assert(FMT != 2 || (!STATS && !ERR), "MXFP4 quantization has no fused statistics or block errors");
-  const float g = *p.scale;   // MXFP4: read only for the non-finite check
+  static_assert(FMT < 2 || (!STATS && !ERR), "MXFP4 / E5M2 quantization has no fused statistics or block errors");
+  // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
+  const float g = FMT == 3 ? e5m2_tensor_scale(*p.scale) : *p.scale;
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = (FMT == 2 && !isnan(g)) ? 1.0f : g;
   if (isnan(g)) {
     if (STATS) stats_nan(p.raw_out);
@@ -458,12 +468,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
         }
         if (FMT == 0 && special8) c = fp8_encode16<RND>(v, inv8, u);
       }
-    } else if (FMT >= 1) {
+    } else if (FMT == 1 || FMT == 2) {
       const uint2 e = nvfp4_encode16<RND>(v, bs, u);
       c.x = e.x;
       c.y = e.y;
     } else {
-      c = fp8_encode16<RND>(v, inv8, u);
+      c = fp8_encode16<RND, FMT == 3>(v, inv8, u);
     }
     if (FMT == 2) {   // the even lane of a pair writes the block's scale
       const uint2 c2 = make_uint2(c.x, c.y);
@@ -506,16 +516,18 @@ constexpr int kXW = kTC / 2 + 4;   // words per staged source row (pairs of bf16
 // b^1, which exchange their half maxima through shared memory).
 template <int FMT, int LAYOUT, int RND, bool ERR>
 __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
-  static_assert(FMT != 2 || !ERR, "MXFP4 quantization has no block errors");
-  constexpr int OB = FMT >= 1 ? kTR / 2 : kTR;   // output bytes per row of the tile
+  static_assert(FMT < 2 || !ERR, "MXFP4 / E5M2 quantization has no block errors");
+  constexpr bool FP4 = FMT == 1 || FMT == 2;
+  constexpr int OB = FP4 ? kTR / 2 : kTR;         // output bytes per row of the tile
   constexpr int OW = OB / 4 + 1;                  // staged output row, words (odd: fewer conflicts)
   __shared__ __align__(16) uint32_t xs[kTR][kXW];
   __shared__ __align__(16) uint32_t rs[RND ? kTR : 1][RND ? kXW : 4];
   __shared__ uint32_t oc[kTC][OW];
-  __shared__ uint8_t os[FMT >= 1 ? kTC : 1][8];
+  __shared__ uint8_t os[FP4 ? kTC : 1][8];
   __shared__ uint32_t amx[FMT == 2 ? 8 : 1][FMT == 2 ? 32 : 1][2];
   __shared__ float oe[ERR ? kTC : 1][8];
-  const float g = *p.scale;   // MXFP4: read only for the non-finite check
+  // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
+  const float g = FMT == 3 ? e5m2_tensor_scale(*p.scale) : *p.scale;
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && p.g_out)
     *p.g_out = (FMT == 2 && !isnan(g)) ? 1.0f : g;
   if (isnan(g)) return;
@@ -587,7 +599,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
         oe[2 * cp + 1][b] = nvfp4_block_err(v1, e1, s1.p);
       }
     } else {
-      const uint4 e0 = fp8_encode16<RND>(v0, inv8, u0), e1 = fp8_encode16<RND>(v1, inv8, u1);
+      const uint4 e0 = fp8_encode16<RND, FMT == 3>(v0, inv8, u0), e1 = fp8_encode16<RND, FMT == 3>(v1, inv8, u1);
       oc[2 * cp][4 * b] = e0.x; oc[2 * cp][4 * b + 1] = e0.y; oc[2 * cp][4 * b + 2] = e0.z; oc[2 * cp][4 * b + 3] = e0.w;
       oc[2 * cp + 1][4 * b] = e1.x; oc[2 * cp + 1][4 * b + 1] = e1.y;
       oc[2 * cp + 1][4 * b + 2] = e1.z; oc[2 * cp + 1][4 * b + 3] = e1.w;
@@ -595,7 +607,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
   }
   __syncthreads();
   // codes: output rows c0.., contraction r0..r0+127 (OB bytes per row)
-  constexpr int BPB = FMT >= 1 ? 8 : 16;   // bytes per 16-element block
+  constexpr int BPB = FP4 ? 8 : 16;   // bytes per 16-element block
   if (LAYOUT == 0) {
     // row pitch of the row-major layout is only block-aligned: one store per block
     for (int idx = t; idx < kTC * 8; idx += 256) {
@@ -603,7 +615,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
       const int64_t orow = c0 + row;
       if (orow >= p.out_rows || r0 + 16 * b >= p.out_cols) continue;
       uint8_t* dst = p.codes + orow * (p.out_cols * BPB / 16) + (r0 + 16 * b) * BPB / 16;
-      if (FMT >= 1) *reinterpret_cast<uint2*>(dst) = make_uint2(oc[row][2 * b], oc[row][2 * b + 1]);
+      if (FP4) *reinterpret_cast<uint2*>(dst) = make_uint2(oc[row][2 * b], oc[row][2 * b + 1]);
       else *reinterpret_cast<uint4*>(dst) = make_uint4(oc[row][4 * b], oc[row][4 * b + 1], oc[row][4 * b + 2],
                                                        oc[row][4 * b + 3]);
     }
@@ -833,9 +845,34 @@ static void launch_quant_mx(const QuantParams& p, int orient, int layout, int rn
   }
 }
 
+// E5M2: no statistics or block errors either.
+static void launch_quant_e5(const QuantParams& p, int orient, int layout, int rnd, int num_sms, cudaStream_t st) {
+  if (orient == 0) {
+    const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
+    const int grid = fill_grid(segs, 8, 16 * num_sms);
+    if (layout == 0) {
+      if (rnd == 0) quant_rows_kernel<3, 0, 0, false, false><<<grid, 256, 0, st>>>(p);
+      else quant_rows_kernel<3, 0, 1, false, false><<<grid, 256, 0, st>>>(p);
+    } else {
+      if (rnd == 0) quant_rows_kernel<3, 1, 0, false, false><<<grid, 256, 0, st>>>(p);
+      else quant_rows_kernel<3, 1, 1, false, false><<<grid, 256, 0, st>>>(p);
+    }
+  } else {
+    const dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
+    if (layout == 0) {
+      if (rnd == 0) quant_cols_kernel<3, 0, 0, false><<<grid, 256, 0, st>>>(p);
+      else quant_cols_kernel<3, 0, 1, false><<<grid, 256, 0, st>>>(p);
+    } else {
+      if (rnd == 0) quant_cols_kernel<3, 1, 0, false><<<grid, 256, 0, st>>>(p);
+      else quant_cols_kernel<3, 1, 1, false><<<grid, 256, 0, st>>>(p);
+    }
+  }
+}
+
 cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
                          cudaStream_t st) {
-  if (fmt == 2) launch_quant_mx(p, orient, layout, rnd, num_sms, st);
+  if (fmt == 3) launch_quant_e5(p, orient, layout, rnd, num_sms, st);
+  else if (fmt == 2) launch_quant_mx(p, orient, layout, rnd, num_sms, st);
   else if (fmt == 1) launch_quant_fmt<1>(p, orient, layout, rnd, err, num_sms, st);
   else launch_quant_fmt<0>(p, orient, layout, rnd, false, num_sms, st);
   return cudaGetLastError();

@@ -68,6 +68,26 @@ __device__ __forceinline__ uint32_t e4m3_sr_from_base(uint32_t base, uint32_t u1
 }
 __device__ __forceinline__ uint32_t e4m3_sr(float y, uint32_t u16) { return e4m3_sr_from_base(e4m3_sr_base(y), u16); }
 
+// ------------------------------------------------------------------ E5M2
+// 1 sign, 5 exponent (bias 15), 2 mantissa bits; largest finite 57344 (0x7b).
+__device__ __forceinline__ uint32_t e5m2x2_rn_sat(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Stochastic rounding of y >= 0 onto the finite E5M2 grid, carry form as for
+// E4M3 with 21 dropped mantissa bits; below 2^-14 the fixed point is
+// floor(y * 2^37), the mantissa of 2^-14 + y rounded toward zero.
+__device__ __forceinline__ uint32_t e5m2_sr_base(float y) {
+  return y >= 6.103515625e-05f ? __float_as_uint(y) - 0x38000000u                 // (exp-112)<<23 | mantissa
+                               : __float_as_uint(__fadd_rz(y, 6.103515625e-05f)) - 0x38800000u;
+}
+__device__ __forceinline__ uint32_t e5m2_sr_from_base(uint32_t base, uint32_t u16) {
+  const uint32_t code = (base + ((65535u - u16) << 5)) >> 21;
+  return code < 0x7bu ? code : 0x7bu;
+}
+__device__ __forceinline__ uint32_t e5m2_sr(float y, uint32_t u16) { return e5m2_sr_from_base(e5m2_sr_base(y), u16); }
+
 // ------------------------------------------------------------------ E2M1
 // Round-to-nearest-even of two signed values to E2M1 (saturating at +-6),
 // hardware cvt: returns one byte, lo in bits 0..3 and hi in bits 4..7.

@@ -51,6 +51,7 @@ struct GemmParams {
   int num_k_stages;             // kp / elements-per-stage
   int num_m_tiles, num_n_tiles;
   int v8;                       // D rows allow 32-byte stores
+  int a_e5m2;                   // FP8 only: A is E5M2 (B stays E4M3)
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -122,7 +123,7 @@ cudaError_t launch_dw_noise(const float* q, const float* ref, int64_t n, double*
                             double* out2, int num_sms, cudaStream_t st);
 
 // GEMM: D = ga*gb*A B^T on MMA-layout operands.  fmt 1 = NVFP4, 2 = MXFP4 (ga, gb
-// null: no tensor scales), 0 = FP8.
+// null: no tensor scales), 0 = FP8 (p.a_e5m2: A in E5M2, B in E4M3).
 // a_codes / b_codes are passed to the launcher, which builds the TMA tensor
 // maps.
 cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,

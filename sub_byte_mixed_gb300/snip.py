@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsnip.so")
 
 SNIP_OK, SNIP_ERR_INVALID_ARG, SNIP_ERR_SHAPE, SNIP_ERR_ALIGN, SNIP_ERR_NONFINITE, SNIP_ERR_TIMEOUT, \
     SNIP_ERR_CUDA, SNIP_ERR_UNSUPPORTED_DEVICE, SNIP_ERR_WORKSPACE = range(9)
-FP8, NVFP4, MXFP4 = 0, 1, 2
+FP8, NVFP4, MXFP4, FP8_E5M2, FP8_E5M2_GRAD = 0, 1, 2, 3, 4
 RTN, SR = 0, 1
 ALONG_COLS, ALONG_ROWS = 0, 1
 ROWMAJOR, MMA = 0, 1
@@ -31,7 +31,7 @@ EXPORTS = (
     "snip_status_string", "snip_version", "snip_device_check", "snip_workspace_init", "snip_workspace_status",
     "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_tensor_scales_multi",
     "snip_tensor_scales_noalloc",
-    "snip_quantize_nvfp4", "snip_quantize_fp8", "snip_quantize_mxfp4",
+    "snip_quantize_nvfp4", "snip_quantize_fp8", "snip_quantize_mxfp4", "snip_quantize_e5m2",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
     "snip_quant_stats", "snip_quantize_stats", "snip_stats_finalize", "snip_plan_costs", "snip_plan_select",
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_quantize_nvfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_fp8": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, sz, vp]),
         "snip_quantize_mxfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, i32, vp, vp, vp, sz, vp]),
+        "snip_quantize_e5m2": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, sz, vp]),
         "snip_quantized_bytes": (i32, [i32, i32, i64, i64, szp, szp]),
         "snip_gemm": (i32, [i32, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp, sz, vp]),
         "snip_plan_create": (i32, [i32, ctypes.POINTER(ctypes.c_int), u64, ctypes.POINTER(vp)]),
@@ -159,6 +160,12 @@ def snip_quantize_nvfp4(x, rows, cols, orient, rnd, seed, stream_id, g_in, layou
 def snip_quantize_mxfp4(x, rows, cols, orient, rnd, seed, stream_id, layout, codes, scales, ws, ws_bytes, stream):
     _call("snip_quantize_mxfp4", x, rows, cols, orient, rnd, seed, stream_id, layout, codes, scales, ws, ws_bytes,
           stream)
+
+
+def snip_quantize_e5m2(x, rows, cols, orient, rnd, seed, stream_id, amax_in, layout, codes, s_out, ws, ws_bytes,
+                       stream):
+    _call("snip_quantize_e5m2", x, rows, cols, orient, rnd, seed, stream_id, amax_in, layout, codes, s_out, ws,
+          ws_bytes, stream)
 
 
 def snip_quantize_fp8(x, rows, cols, orient, rnd, seed, stream_id, s_in, layout, codes, s_out, ws, ws_bytes, stream):
@@ -422,6 +429,21 @@ def quantize_mxfp4(x, orient=ALONG_COLS, rnd=RTN, seed=0, stream_id=0, layout=RO
     return QuantMXFP4(codes[:cb], scales[:sb], orows, ocols, layout)
 
 
+def quantize_e5m2(x, orient=ALONG_COLS, rnd=RTN, seed=0, stream_id=0, amax_in=None, layout=ROWMAJOR,
+                  ws: Workspace | None = None) -> QuantFP8:
+    """FP8 E5M2 quantization (tensor scale amax / 57344), returned like QuantFP8."""
+    torch = _torch()
+    ws = ws or small_workspace()
+    rows, cols = x.shape
+    orows, ocols = (rows, cols) if orient == ALONG_COLS else (cols, rows)
+    cb, _ = snip_quantized_bytes(FP8_E5M2, layout, orows, ocols)
+    codes = torch.empty(max(cb, 16), dtype=torch.uint8, device=x.device)
+    s = torch.empty(1, dtype=torch.float32, device=x.device)
+    snip_quantize_e5m2(x.data_ptr(), rows, cols, orient, rnd, seed, stream_id, _ptr(amax_in), layout,
+                       codes.data_ptr(), s.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return QuantFP8(codes[:cb], s, orows, ocols, layout)
+
+
 def gemm(fmt, a, b, M, N, K, out=None, ws: Workspace | None = None):
     """D = A B^T on two MMA-layout quantized operands (QuantNVFP4 / QuantFP8)."""
     torch = _torch()
@@ -434,8 +456,8 @@ def gemm(fmt, a, b, M, N, K, out=None, ws: Workspace | None = None):
     elif fmt == MXFP4:
         snip_gemm(MXFP4, a.codes.data_ptr(), a.scales.data_ptr(), None, b.codes.data_ptr(), b.scales.data_ptr(),
                   None, M, N, K, D.data_ptr(), D.stride(0), ws.ptr, ws.nbytes, _stream())
-    else:
-        snip_gemm(FP8, a.codes.data_ptr(), None, a.s.data_ptr(), b.codes.data_ptr(), None, b.s.data_ptr(),
+    else:   # FP8: fmt FP8 (both E4M3) or FP8_E5M2 (A in E5M2, B in E4M3)
+        snip_gemm(fmt, a.codes.data_ptr(), None, a.s.data_ptr(), b.codes.data_ptr(), None, b.s.data_ptr(),
                   M, N, K, D.data_ptr(), D.stride(0), ws.ptr, ws.nbytes, _stream())
     return D
 

@@ -14,6 +14,9 @@ from gpu_helpers import gemm_close, need_gpu
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 FMT_NAMES = {0: "fp8", 1: "nvfp4", 2: "mxfp4"}
+# forward (X, W, W^T, X^T) and gradient (dY, dY^T) operand formats of each layer format
+FWD = {0: "fp8", 1: "nvfp4", 2: "mxfp4", 4: "fp8"}
+GRAD = {0: "fp8", 1: "nvfp4", 2: "mxfp4", 4: "e5m2"}
 
 
 @pytest.fixture(scope="module")
@@ -40,19 +43,21 @@ def _block_sampled(snip, cfg, plan_fmts, seed=0, n=48):
         dx = dX[ti][:, ki].cpu().numpy()
         dw = dW[ni][:, ki].cpu().numpy()
         del Y, dX, dW, ws
-        fmt = FMT_NAMES[plan_fmts[j]]
+        ff, fg = FWD[plan_fmts[j]], GRAD[plan_fmts[j]]
         Xc, Wc, dYc = X.cpu(), W.cpu(), dY.cpu()
-        q = lambda a, o, r, tag, rows: oracle.quantize(fmt, a, o, r, seed, oracle.stream_id(j, tag), rows=rows).dequant()
-        gemm_close(y, oracle.gemm_tn(q(Xc, 0, 0, 0, t), q(Wc, 0, 0, 1, nn)), f"{cfg.name} {lin.name} Y")
-        gemm_close(dx, oracle.gemm_tn(q(dYc, 0, 1, 2, t), q(Wc, 1, 1, 3, kk)), f"{cfg.name} {lin.name} dX")
-        gemm_close(dw, oracle.gemm_tn(q(dYc, 1, 1, 4, nn), q(Xc, 1, 1, 5, kk)), f"{cfg.name} {lin.name} dW")
+        q = lambda f, a, o, r, tag, rows: oracle.quantize(f, a, o, r, seed, oracle.stream_id(j, tag),
+                                                          rows=rows).dequant()
+        gemm_close(y, oracle.gemm_tn(q(ff, Xc, 0, 0, 0, t), q(ff, Wc, 0, 0, 1, nn)), f"{cfg.name} {lin.name} Y")
+        gemm_close(dx, oracle.gemm_tn(q(fg, dYc, 0, 1, 2, t), q(ff, Wc, 1, 1, 3, kk)), f"{cfg.name} {lin.name} dX")
+        gemm_close(dw, oracle.gemm_tn(q(fg, dYc, 1, 1, 4, nn), q(ff, Xc, 1, 1, 5, kk)), f"{cfg.name} {lin.name} dW")
 
 
-@pytest.mark.parametrize("plan", ["mix", "nvfp4", "fp8", "mxfp4"])
+@pytest.mark.parametrize("plan", ["mix", "nvfp4", "fp8", "mxfp4", "fp8-e5m2-grad"])
 def test_llama7b_block_sampled(snip, plan):
     cfg = inputs.LLAMA7B
     fmts = (inputs.seeded_plan(cfg, cfg.fp4_target, seed=0) if plan == "mix" else
-            inputs.all_plan({"nvfp4": inputs.FMT_NVFP4, "fp8": inputs.FMT_FP8, "mxfp4": inputs.FMT_MXFP4}[plan]))
+            inputs.all_plan({"nvfp4": inputs.FMT_NVFP4, "fp8": inputs.FMT_FP8, "mxfp4": inputs.FMT_MXFP4,
+                             "fp8-e5m2-grad": 4}[plan]))
     _block_sampled(snip, cfg, fmts)
 
 
