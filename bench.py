@@ -348,6 +348,70 @@ class Step:
                 events[i][1].record()
 
 
+def quantizer_sweep(snip, hbm_gbs: float, reps: int = 10):
+    """Standalone quantizers on the 8192 x 8192 tensor with 0.1% outliers (x100): each variant's
+    algorithmic GB/s (bf16 read + codes + scales written; statistics and tensor scales read only)
+    and its fraction of the measured HBM copy bandwidth.  Reading a 1.5 GB scratch buffer before
+    each timed launch flushes L2 with clean lines (no write-back overlaps the launch) and keeps the
+    GPU busy while the host queues the pre-marshalled C-ABI call, so no idle gap is timed."""
+    import torch
+    from sub_byte_mixed_gb300 import inputs
+    L = snip.load()
+    x = inputs.outlier_bf16(8192, 8192, seed=0, tensor_id=1, device="cuda")
+    n, R, C = x.numel(), 8192, 8192
+    ws = snip.Workspace(snip.snip_quantize_workspace_size(0, 0))
+    st = torch.cuda.current_stream().cuda_stream
+    sc = torch.empty(4, dtype=torch.float32, device="cuda")
+    L.snip_tensor_scales(x.data_ptr(), n, sc.data_ptr(), ws.ptr, ws.nbytes, st)
+    cb, sb = snip.snip_quantized_bytes(snip.NVFP4, snip.MMA, R, C)
+    codes = torch.empty(max(cb, C * R), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(max(sb, 16), dtype=torch.uint8, device="cuda")
+    s_out = torch.empty(1, dtype=torch.float32, device="cuda")
+    raw = torch.empty(snip.STATS_NVALS, dtype=torch.float64, device="cuda")
+    xp, cp, sp, w = x.data_ptr(), codes.data_ptr(), scales.data_ptr(), (ws.ptr, ws.nbytes, st)
+    g, s8 = sc.data_ptr() + 4, sc.data_ptr() + 8
+    variants = {   # name: (C-ABI function, arguments, algorithmic bytes per element)
+        "scales": (L.snip_tensor_scales, (xp, n, sc.data_ptr(), *w), 2.0),
+        "nvfp4_rtn_rows": (L.snip_quantize_nvfp4, (xp, R, C, 0, 0, 0, 1, g, snip.MMA, cp, sp, s_out.data_ptr(), None, *w),
+                           2 + 0.5625),
+        "nvfp4_sr_rows": (L.snip_quantize_nvfp4, (xp, R, C, 0, 1, 0, 2, g, snip.MMA, cp, sp, s_out.data_ptr(), None, *w),
+                          2 + 0.5625),
+        "nvfp4_sr_cols": (L.snip_quantize_nvfp4, (xp, R, C, 1, 1, 0, 3, g, snip.MMA, cp, sp, s_out.data_ptr(), None, *w),
+                          2 + 0.5625),
+        "mxfp4_sr_cols": (L.snip_quantize_mxfp4, (xp, R, C, 1, 1, 0, 4, snip.MMA, cp, sp, *w), 2 + 0.53125),
+        "fp8_rtn_rows": (L.snip_quantize_fp8, (xp, R, C, 0, 0, 0, 5, s8, snip.MMA, cp, s_out.data_ptr(), *w), 3.0),
+        "fp8_sr_cols": (L.snip_quantize_fp8, (xp, R, C, 1, 1, 0, 6, s8, snip.MMA, cp, s_out.data_ptr(), *w), 3.0),
+        "stats_rtn": (L.snip_quant_stats, (xp, R, C, 0, 0, 7, sc.data_ptr(), raw.data_ptr(), None, None, *w), 2.0),
+        "quant_stats_nvfp4_rtn": (L.snip_quantize_stats, (snip.NVFP4, xp, R, C, 0, 0, 8, sc.data_ptr(), snip.MMA, cp, sp,
+                                                          raw.data_ptr(), *w), 2 + 0.5625),
+        "quant_stats_nvfp4_sr": (L.snip_quantize_stats, (snip.NVFP4, xp, R, C, 1, 0, 9, sc.data_ptr(), snip.MMA, cp, sp,
+                                                         raw.data_ptr(), *w), 2 + 0.5625),
+    }
+    flush = torch.ones(1536 << 20 >> 2, dtype=torch.int32, device="cuda")
+    flush_out = torch.empty((), dtype=torch.int32, device="cuda")
+    out = {}
+    for name, (fn, args, bpe) in variants.items():
+        if fn(*args) != 0:
+            raise RuntimeError(f"{name} failed")
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(reps):
+            torch.max(flush, out=flush_out)   # reads 1.5 GB
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn(*args)
+            e1.record()
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+        ms = tot / reps
+        gbs = bpe * n / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 3)}
+    if ws.status() != snip.SNIP_OK:
+        raise RuntimeError("device status " + snip.status_string(ws.status()))
+    return {"tensor": "8192x8192 bf16, N(0,1) with 0.1% of entries x100 (seeded)", "l2": "flushed before each launch",
+            "variants": out}
+
+
 def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
     """The same step through the layer API (snip_qlinear_fwd / _bwd, statistics fused into their
     quantizations) with host buffers: every step copies all inputs (X, W, dY, bf16) in from pinned host
@@ -502,6 +566,9 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
+    qsweep = None
+    if not args.profile_run and not layers and rank == 0:
+        qsweep = quantizer_sweep(snip, measured_peaks()["hbm_gbs"])
     e2e = None
     if not args.no_e2e and not args.profile_run and not layers and rank == 0:
         e2e = e2e_run(cfg, plan, snip, step, args.e2e_steps)
@@ -550,6 +617,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "quantizer": quant,
         "gemm_only": {"value": gemm_fl / (gemm_ms * 1e-3) / 1e12, "unit": UNIT},
+        "quantizer_sweep": qsweep,
         "breakdown": breakdown,
         "clocks": clocks,
         "e2e": e2e,
