@@ -165,10 +165,24 @@ __device__ __forceinline__ uint32_t uhalf(const uint32_t (&u)[8], int i) {
   return (i & 1) ? (u[i >> 1] >> 16) : (u[i >> 1] & 0xffffu);
 }
 
+// Sources of the 16 random bits of element i of a block, for the encoders:
+// packed two per word (element i in half i%2 of word i/2) ...
+struct PackedBits {
+  const uint32_t* u;
+  __device__ __forceinline__ uint32_t operator()(int i) const { return (i & 1) ? (u[i >> 1] >> 16) : (u[i >> 1] & 0xffffu); }
+};
+// ... or one word per element, shared by two source columns: the even column's
+// bits in the low half (HI false), the odd column's in the high half.
+template <bool HI>
+struct WordHalfBits {
+  const uint32_t* r;
+  __device__ __forceinline__ uint32_t operator()(int i) const { return HI ? (r[i] >> 16) : (r[i] & 0xffffu); }
+};
+
 // Encode one NVFP4 block of 16 signed values into two words of packed codes
 // (element 2j in the low nibble of byte j).  RND: 0 nearest, 1 stochastic.
-template <int RND>
-__device__ __forceinline__ uint2 nvfp4_encode16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8]) {
+template <int RND, class Bits = PackedBits>
+__device__ __forceinline__ uint2 nvfp4_encode16(const float (&v)[16], const BlockScale& bs, Bits bits) {
   uint32_t w[2] = {0u, 0u};
   if (bs.special) {
     // p == 0: every magnitude 0; 1/p overflowed: non-zero elements saturate to 6
@@ -187,7 +201,7 @@ __device__ __forceinline__ uint2 nvfp4_encode16(const float (&v)[16], const Bloc
     for (int i = 0; i < 16; ++i) {
       const uint32_t b = __float_as_uint(v[i]);
       const float y = __fmul_rn(__uint_as_float(b & 0x7fffffffu), bs.inv);
-      w[i >> 3] |= (((b >> 28) & 8u) | e2m1_sr(y, uhalf(u, i))) << (4 * (i & 7));
+      w[i >> 3] |= (((b >> 28) & 8u) | e2m1_sr(y, bits(i))) << (4 * (i & 7));
     }
   }
   return make_uint2(w[0], w[1]);
@@ -209,8 +223,8 @@ __device__ __forceinline__ float nvfp4_block_err(const float (&v)[16], const uin
 
 // Encode 16 signed values to E4M3 (E5 false) or E5M2 (E5 true) with the
 // tensor scale's inverse.
-template <int RND, bool E5 = false>
-__device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, const uint32_t (&u)[8]) {
+template <int RND, bool E5 = false, class Bits = PackedBits>
+__device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, Bits bits) {
   constexpr uint32_t kMaxCode = E5 ? 0x7bu : 0x7eu;
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   if (!(inv < kInf)) {
@@ -230,7 +244,7 @@ __device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, c
     for (int i = 0; i < 16; ++i) {
       const uint32_t b = __float_as_uint(v[i]);
       const float y = __fmul_rn(__uint_as_float(b & 0x7fffffffu), inv);
-      w[i >> 2] |= (((b >> 24) & 0x80u) | (E5 ? e5m2_sr(y, uhalf(u, i)) : e4m3_sr(y, uhalf(u, i)))) << (8 * (i & 3));
+      w[i >> 2] |= (((b >> 24) & 0x80u) | (E5 ? e5m2_sr(y, bits(i)) : e4m3_sr(y, bits(i)))) << (8 * (i & 3));
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
@@ -462,18 +476,18 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
         v4 += st.v4;
         v8 += st.v8;
         if (FMT == 1 && bs.special) {
-          const uint2 e = nvfp4_encode16<RND>(v, bs, u);
+          const uint2 e = nvfp4_encode16<RND>(v, bs, PackedBits{u});
           c.x = e.x;
           c.y = e.y;
         }
-        if (FMT == 0 && special8) c = fp8_encode16<RND>(v, inv8, u);
+        if (FMT == 0 && special8) c = fp8_encode16<RND>(v, inv8, PackedBits{u});
       }
     } else if (FMT == 1 || FMT == 2) {
-      const uint2 e = nvfp4_encode16<RND>(v, bs, u);
+      const uint2 e = nvfp4_encode16<RND>(v, bs, PackedBits{u});
       c.x = e.x;
       c.y = e.y;
     } else {
-      c = fp8_encode16<RND, FMT == 3>(v, inv8, u);
+      c = fp8_encode16<RND, FMT == 3>(v, inv8, PackedBits{u});
     }
     if (FMT == 2) {   // the even lane of a pair writes the block's scale
       const uint2 c2 = make_uint2(c.x, c.y);
@@ -555,7 +569,8 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
     const int cp = t & 31, b = t >> 5;
     float v0[16], v1[16];
     uint32_t m0 = 0, m1 = 0;
-    uint32_t u0[8], u1[8];
+    // random words of rows b*16..b*16+15: column 2cp's bits in the low half, 2cp+1's in the high half
+    uint32_t rw[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t w = xs[b * 16 + i][cp];
@@ -563,16 +578,10 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
       v1[i] = __uint_as_float(w & 0xffff0000u);
       m0 = max(m0, w & 0x7fffu);
       m1 = max(m1, (w >> 16) & 0x7fffu);
-      if (RND == 1) {
-        const uint32_t rw = rs[b * 16 + i][cp];
-        if (i & 1) { u0[i >> 1] |= (rw & 0xffffu) << 16; u1[i >> 1] |= rw & 0xffff0000u; }
-        else { u0[i >> 1] = rw & 0xffffu; u1[i >> 1] = rw >> 16; }
-      }
+      rw[i] = RND == 1 ? rs[b * 16 + i][cp] : 0u;
     }
-    if (RND == 0) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) { u0[k] = 0u; u1[k] = 0u; }
-    }
+    const WordHalfBits<false> u0{rw};
+    const WordHalfBits<true> u1{rw};
     if (FMT == 2) {
       amx[b][cp][0] = m0;
       amx[b][cp][1] = m1;
