@@ -201,7 +201,7 @@ def measured_peaks():
 
 def kernel_source_hash(kind: str) -> str:
     files = {"gemm": ["gemm.cu", "snip_device.cuh", "snip_kernels.cuh"],
-             "quant": ["quant.cu", "snip_device.cuh", "snip_kernels.cuh"]}[kind]
+             "quant": ["quant.cu", "snip_device.cuh", "snip_kernels.cuh", "snip_quant.cuh"]}[kind]
     h = hashlib.sha256()
     for f in files:
         h.update(open(os.path.join(ROOT, "sub_byte_mixed_gb300", "csrc", f), "rb").read())

@@ -298,6 +298,39 @@ snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_
                       int64_t M, int64_t N, int64_t K, float* D, int64_t ldd,
                       void* ws, size_t ws_bytes, void* stream);
 
+/* NEXT-3: the GEMM whose product is the next layer's operand -- typically the
+ * dgrad product dX, the preceding layer's dY -- also writes that operand
+ * quantized, so the bf16 round trip and a separate quantization pass go
+ * away ("SNIP", Figure 5: each GEMM operand quantized along its own
+ * contraction dim; the preceding layer's dgrad contracts over this dX's
+ * columns).  The product D = ga*gb*A B^T is rounded to bf16 and quantized to
+ * NVFP4 in 16-element blocks along its rows (N), with the given tensor scale
+ * (the pages say nothing about when its amax is known: the caller passes
+ * one, e.g. the previous step's amax_out / 2688; values beyond 6 * 448 * g
+ * saturate), nearest or stochastic with the bits of element index m*N + n.
+ * codes / scales (device, 16-byte aligned): the MMA layout of an M x N NVFP4
+ * operand, sized by snip_quantized_bytes(SNIP_FMT_NVFP4, SNIP_LAYOUT_MMA, M,
+ * N); padding is written as zeros.  amax_out (device, nullable) receives
+ * max |bf16(D)| of this product, for the next scale. */
+typedef struct {
+    const float* g_in;
+    int rnd;               /* snip_round */
+    uint64_t seed;
+    uint64_t stream_id;
+    uint8_t* codes;
+    uint8_t* scales;
+    float* amax_out;
+} snip_requant;
+
+/* snip_gemm plus the re-quantized product described above; D (fp32) may be
+ * NULL when only the quantized operand is wanted.  N % 16 == 0.  Errors as
+ * for snip_gemm; SNIP_ERR_INVALID_ARG for a null rq, rq->g_in, rq->codes or
+ * rq->scales. */
+snip_status snip_gemm_requant(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
+                              const uint8_t* b_codes, const uint8_t* b_scales, const float* gb,
+                              int64_t M, int64_t N, int64_t K, float* D, int64_t ldd, const snip_requant* rq,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- plan */
 
 /* A per-layer precision plan (SNIP, Abstract: one format per layer).  formats

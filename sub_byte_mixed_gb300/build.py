@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsnip.so")
 SOURCES = ["quant.cu", "gemm.cu", "api.cu", "noalloc.cu", "plan_select.cu"]
-HEADERS = ["snip_device.cuh", "snip_kernels.cuh"]
+HEADERS = ["snip_device.cuh", "snip_kernels.cuh", "snip_quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

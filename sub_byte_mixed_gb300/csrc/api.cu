@@ -198,7 +198,7 @@ snip_status run_quantize_api(int fmt, const void* x, int64_t rows, int64_t cols,
 
 snip_status run_gemm(int fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga, const uint8_t* b_codes,
                      const uint8_t* b_scales, const float* gb, int64_t M, int64_t N, int64_t K, float* D, int64_t ldd,
-                     void* ws, int num_sms, cudaStream_t st) {
+                     void* ws, int num_sms, cudaStream_t st, const snip_requant* rq = nullptr) {
   GemmParams p;
   memset(&p, 0, sizeof p);
   p.a_scales = a_scales;
@@ -214,6 +214,25 @@ snip_status run_gemm(int fmt, const uint8_t* a_codes, const uint8_t* a_scales, c
   p.timeout_ns = kTimeoutNs;
   if (fmt == SNIP_FMT_MXFP4) p.ga = p.gb = nullptr;   // no tensor scales
   p.a_e5m2 = fmt == SNIP_FMT_FP8_E5M2;
+  if (rq) {
+    const int64_t orp = mma_rows(M), ocp = round_up(N, 256);
+    p.rq_codes = rq->codes;
+    p.rq_scales = rq->scales;
+    p.rq_g = rq->g_in;
+    p.rq_amax = reinterpret_cast<uint32_t*>(rq->amax_out);
+    p.rq_ocp = ocp;
+    p.rq_seed = rq->seed;
+    p.rq_stream = rq->stream_id;
+    p.rq_rnd = rq->rnd;
+    // the tiles write every padded row and column they cover; one-CTA tiles (128 rows) may
+    // leave the last rows of the 256-row padding, so those codes and all scales start at zero
+    const int64_t covered = round_up(M, 128);
+    cudaError_t e = cudaSuccess;
+    if (covered < orp) e = cudaMemsetAsync(rq->codes + covered * (ocp / 2), 0, (size_t)((orp - covered) * (ocp / 2)), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(rq->scales, 0, (size_t)(orp * ocp / 16), st);
+    if (e == cudaSuccess && rq->amax_out) e = cudaMemsetAsync(rq->amax_out, 0, sizeof(float), st);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   return cuda_status(launch_gemm(gemm_kernel_fmt(fmt), a_codes, mma_rows(M), b_codes, mma_rows(N), p, num_sms, st));
 }
 
@@ -403,6 +422,30 @@ snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_
     return SNIP_ERR_ALIGN;
   return run_gemm(fmt, a_codes, a_scales, ga, b_codes, b_scales, gb, M, N, K, D, ldd, ws, sms,
                   static_cast<cudaStream_t>(stream));
+}
+
+snip_status snip_gemm_requant(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
+                              const uint8_t* b_codes, const uint8_t* b_scales, const float* gb, int64_t M, int64_t N,
+                              int64_t K, float* D, int64_t ldd, const snip_requant* rq, void* ws, size_t ws_bytes,
+                              void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if (!rq || !rq->g_in || !rq->codes || !rq->scales || !valid_enum(rq->rnd, 2)) return SNIP_ERR_INVALID_ARG;
+  if (!valid_enum(fmt, 4) || M < 0 || N < 0 || K < 0 || (D && ldd < N)) return SNIP_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return SNIP_OK;
+  if (!a_codes || !b_codes) return SNIP_ERR_INVALID_ARG;
+  if (fmt != SNIP_FMT_MXFP4 && (!ga || !gb)) return SNIP_ERR_INVALID_ARG;
+  if (is_fp4(fmt) && (!a_scales || !b_scales)) return SNIP_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K == 0 || N % 16 != 0 || (D && ldd % 4 != 0) || (fmt == SNIP_FMT_MXFP4 && K % 32 != 0))
+    return SNIP_ERR_SHAPE;
+  if (!ws || ws_bytes < SNIP_WS_HEADER_BYTES) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(a_codes) || !aligned16(b_codes) || (D && !aligned16(D)) || !aligned16(ws) ||
+      !aligned16(rq->codes) || !aligned16(rq->scales) ||
+      (is_fp4(fmt) && (!aligned16(a_scales) || !aligned16(b_scales))))
+    return SNIP_ERR_ALIGN;
+  return run_gemm(fmt, a_codes, a_scales, ga, b_codes, b_scales, gb, M, N, K, D, D ? ldd : N, ws, sms,
+                  static_cast<cudaStream_t>(stream), rq);
 }
 
 // ---------------------------------------------------------------- plan

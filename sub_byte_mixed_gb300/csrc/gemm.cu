@@ -28,10 +28,12 @@
 // bit of the status word, lets all roles fall through, drains in-flight
 // tensor-core work and frees its tensor memory before returning.
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 #include <cstring>
 
 #include "snip_kernels.cuh"
+#include "snip_quant.cuh"
 
 namespace snip {
 
@@ -76,7 +78,47 @@ struct GemmCfg {
           : ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24));
 };
 
-template <int FMT, int BN>
+// NEXT-3: NVFP4 re-quantization of 32 output columns of one row.  The values
+// alpha * acc are rounded to bf16 (the output's storage type), then quantized
+// with the given tensor scale in 16-element row blocks -- nearest, or
+// stochastic with the bits of each element's index in the row-major M x N
+// output -- and written in the MMA operand layout.  Returns the largest
+// magnitude as a bf16 bit pattern.
+template <int RND>
+__device__ __forceinline__ uint32_t requant32(const uint32_t (&r)[32], float alpha, int64_t row, int64_t col,
+                                              const GemmParams& p, float g, float six_g) {
+  uint32_t am = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float v[16];
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(alpha, __uint_as_float(r[16 * h + i]))));
+      v[i] = __uint_as_float(bits << 16);
+      mb = max(mb, bits & 0x7fffu);
+    }
+    const BlockScale bs = nvfp4_block_scale(mb, g, six_g);
+    const int64_t c = col + 16 * h;
+    uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (RND) sr_bits16(row * p.N + c, p.rq_seed, p.rq_stream, u);
+    *reinterpret_cast<uint2*>(p.rq_codes + row * (p.rq_ocp >> 1) + (c >> 1)) = nvfp4_encode16<RND>(v, bs, PackedBits{u});
+    p.rq_scales[mma_scale_offset(row, c >> 4, p.rq_ocp)] = (uint8_t)bs.s;
+    am = max(am, mb);
+  }
+  return am;
+}
+
+// The largest magnitude of a warp's re-quantized values, published once per warp.
+__device__ __forceinline__ void requant_publish_amax(uint32_t am, uint32_t* out) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(out, am << 16);   // bf16 pattern -> fp32 bits: order kept
+}
+
+// RQ: the epilogue also re-quantizes the product (snip_gemm_requant); a
+// separate instantiation, so the plain GEMM keeps its registers.
+template <int FMT, int BN, bool RQ = false>
 __global__ void __launch_bounds__(448, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   using C = GemmCfg<FMT, BN>;
@@ -233,6 +275,8 @@ __global__ void __launch_bounds__(448, 1)
     const int q = warp & 3;                          // TMEM lane quadrant this warp may access
     const int half = (warp - C::EPI_WARP0) >> 2;     // which BN/2 columns it drains
     const float alpha = p.ga ? __fmul_rn(*p.ga, *p.gb) : 1.0f;   // MXFP4 has no tensor scales
+    const float rq_g = RQ ? *p.rq_g : 1.0f, rq_six_g = __fmul_rn(6.0f, rq_g);
+    uint32_t rq_am = 0;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
@@ -240,7 +284,7 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + half * C::EPI_COLS;
       const int64_t row = (int64_t)mt * C::BM + q * 32 + lane;
-      float* drow = p.D + row * p.ldd;
+      float* drow = p.D ? p.D + row * p.ldd : nullptr;
       const int64_t col0 = (int64_t)nt * BN + half * C::EPI_COLS;
 #pragma unroll 1
       for (int rd = 0; rd < C::EPI_COLS / C::EPI_ROUND; ++rd) {
@@ -253,7 +297,15 @@ __global__ void __launch_bounds__(448, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty(acc));
         }
-        if (row < p.M) {
+        if (RQ) {   // the next GEMM's operand, written for the padded rows too (zeros)
+#pragma unroll
+          for (int c = 0; c < C::EPI_ROUND / 32; ++c) {
+            const int64_t col = col0 + rd * C::EPI_ROUND + c * 32;
+            rq_am = max(rq_am, p.rq_rnd ? requant32<1>(r[c], alpha, row, col, p, rq_g, rq_six_g)
+                                        : requant32<0>(r[c], alpha, row, col, p, rq_g, rq_six_g));
+          }
+        }
+        if (p.D && row < p.M) {
           // 32-byte (or 16-byte when D is only 16-byte aligned) streaming stores: whole L2 sectors
           // per thread, without evicting the operands
 #pragma unroll
@@ -282,6 +334,7 @@ __global__ void __launch_bounds__(448, 1)
       }
       if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
     }
+    if (RQ && p.rq_amax) requant_publish_amax(rq_am, p.rq_amax);
   }
   __syncwarp();
   tc_fence_before();
@@ -333,7 +386,7 @@ struct Gemm2Cfg {
           : ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24));
 };
 
-template <int FMT>
+template <int FMT, bool RQ = false>
 __global__ void __launch_bounds__(448, 1)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -494,6 +547,8 @@ __global__ void __launch_bounds__(448, 1)
     const int q = warp & 3;
     const int half = (warp - C::EPI_WARP0) >> 2;
     const float alpha = p.ga ? __fmul_rn(*p.ga, *p.gb) : 1.0f;   // MXFP4 has no tensor scales
+    const float rq_g = RQ ? *p.rq_g : 1.0f, rq_six_g = __fmul_rn(6.0f, rq_g);
+    uint32_t rq_am = 0;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
@@ -501,7 +556,7 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * C::BN + half * C::EPI_COLS;
       const int64_t row = (int64_t)(2 * mt + rank) * C::BM + q * 32 + lane;
-      float* drow = p.D + row * p.ldd;
+      float* drow = p.D ? p.D + row * p.ldd : nullptr;
       const int64_t col0 = (int64_t)nt * C::BN + half * C::EPI_COLS;
 #pragma unroll 1
       for (int rd = 0; rd < C::EPI_COLS / C::EPI_ROUND; ++rd) {
@@ -514,7 +569,15 @@ __global__ void __launch_bounds__(448, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(mapa_shared(tempty(acc), 0));
         }
-        if (row < p.M) {
+        if (RQ) {
+#pragma unroll
+          for (int c = 0; c < C::EPI_ROUND / 32; ++c) {
+            const int64_t col = col0 + rd * C::EPI_ROUND + c * 32;
+            rq_am = max(rq_am, p.rq_rnd ? requant32<1>(r[c], alpha, row, col, p, rq_g, rq_six_g)
+                                        : requant32<0>(r[c], alpha, row, col, p, rq_g, rq_six_g));
+          }
+        }
+        if (p.D && row < p.M) {
 #pragma unroll
           for (int c = 0; c < C::EPI_ROUND / 32; ++c)
 #pragma unroll
@@ -541,6 +604,7 @@ __global__ void __launch_bounds__(448, 1)
       }
       if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
     }
+    if (RQ && p.rq_amax) requant_publish_amax(rq_am, p.rq_amax);
   }
   __syncwarp();
   tc_fence_before();
@@ -584,13 +648,13 @@ static bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int BN>
+template <int FMT, int BN, bool RQ>
 static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
                                    GemmParams p, int num_sms, cudaStream_t st) {
   using C = GemmCfg<FMT, BN>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<FMT, BN, RQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -605,7 +669,7 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
   p.num_n_tiles = (int)((p.N + BN - 1) / BN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_tn_kernel<FMT, BN><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
+  gemm_tn_kernel<FMT, BN, RQ><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -624,13 +688,13 @@ static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT>
+template <int FMT, bool RQ>
 static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
                                     GemmParams p, int num_sms, cudaStream_t st) {
   using C = Gemm2Cfg<FMT>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT, RQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -663,25 +727,33 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT>, ta, tb, tsa, tsb, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT, RQ>, ta, tb, tsa, tsb, p);
 }
 
 // Measured on GB300 at the Llama-7B shapes, the CTA pair beats the one-CTA
 // kernel by about 11% (NVFP4) and 2-15% (FP8).  GEMMs too small to give
 // every SM pair a 256 x 256 tile run on the one-CTA kernel's 128 x 256
 // tiles instead, which spreads them over twice as many SMs.
+template <bool RQ>
+static cudaError_t launch_gemm_rq(int fmt, bool pair, const uint8_t* a_codes, int64_t a_rows_padded,
+                                  const uint8_t* b_codes, int64_t b_rows_padded, const GemmParams& p, int num_sms,
+                                  cudaStream_t st) {
+  if (fmt == 1)
+    return pair ? launch_gemm_pair<1, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
+                : launch_gemm_cfg<1, 256, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  if (fmt == 2)
+    return pair ? launch_gemm_pair<2, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
+                : launch_gemm_cfg<2, 256, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  return pair ? launch_gemm_pair<0, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
+              : launch_gemm_cfg<0, 256, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+}
+
 cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,
                         int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st) {
   const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
   const bool pair = pair_tiles >= num_sms / 2;
-  if (fmt == 1)
-    return pair ? launch_gemm_pair<1>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
-                : launch_gemm_cfg<1, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
-  if (fmt == 2)
-    return pair ? launch_gemm_pair<2>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
-                : launch_gemm_cfg<2, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
-  return pair ? launch_gemm_pair<0>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
-              : launch_gemm_cfg<0, 256>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  if (p.rq_codes) return launch_gemm_rq<true>(fmt, pair, a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  return launch_gemm_rq<false>(fmt, pair, a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
 }
 
 }  // namespace snip

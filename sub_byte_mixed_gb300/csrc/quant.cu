@@ -18,10 +18,10 @@
 // rounding uses the carry form of the 16-bit rule (snip_device.cuh), with one
 // Philox4x32-10 call per 8 source elements.
 #include "snip_kernels.cuh"
+#include "snip_quant.cuh"
 
 namespace snip {
 
-constexpr float kInf = __builtin_huge_valf();
 
 // ------------------------------------------------------------------ a1: tensor scales
 // Magnitudes are compared as bf16 bit patterns (sign cleared): for finite
@@ -91,120 +91,6 @@ __global__ void __launch_bounds__(256, 4) scales_multi_kernel(ScalesMulti m, uin
   const uint32_t c0 = (uint32_t)m.cta0[t];
   scales_body(m.x[t], m.n[t], blockIdx.x - c0, (uint32_t)(m.cta0[t + 1] - m.cta0[t]), partials + c0, counters + t,
               m.out3[t], status);
-}
-
-// Byte offset of the E4M3 scale of (row r, block kb) in the MMA layout.
-__device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64_t ocp) {
-  const int64_t chunk = (r >> 7) * (ocp >> 6) + (kb >> 2);
-  return chunk * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
-}
-// MXFP4: the same chunk image with one E8M0 byte per 32-element block, so a
-// chunk covers 128 contraction elements (two MMAs of 64).
-__device__ __forceinline__ int64_t mma_scale_offset_mx(int64_t r, int64_t kb32, int64_t ocp) {
-  const int64_t chunk = (r >> 7) * (ocp >> 7) + (kb32 >> 2);
-  return chunk * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb32 & 3);
-}
-
-
-// ------------------------------------------------------------------ per-block helpers
-// 16 bf16 values (two uint4) -> signed floats.
-__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&v)[16]) {
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-__device__ __forceinline__ uint32_t amax16_bits(const uint4& a, const uint4& b) {
-  const uint32_t m2 = __vmaxu2(mag_max4(a), mag_max4(b));
-  return max(m2 & 0xffffu, m2 >> 16);
-}
-
-// Block scale of NVFP4: s_b = E4M3(amax_b / (6 g)) (nearest even, saturating),
-// p = decode(s_b) * g, inv = 1 / p.  `special` marks p == 0 or 1/p overflow,
-// where codes are decided without the product (zero -> 0, else 6).
-struct BlockScale {
-  uint32_t s;
-  float p, inv;
-  bool special;
-};
-__device__ __forceinline__ BlockScale nvfp4_block_scale(uint32_t amax_bits, float g, float six_g) {
-  BlockScale r;
-  r.s = e4m3_rn_sat(__fdiv_rn(bf16_bits_to_float(amax_bits), six_g));
-  r.p = __fmul_rn(e4m3_decode_pos(r.s), g);
-  r.inv = __frcp_rn(r.p);
-  r.special = !(r.inv < kInf);
-  return r;
-}
-
-// MXFP4 block scale (OCP Microscaling v1.0) from the 32-block's largest
-// magnitude as a bf16 bit pattern: E8M0 code = max(exponent field - 2, 0),
-// i.e. 2^(floor(log2 amax) - 2) clamped at 2^-127 (subnormal or zero amax);
-// inv = 2^-(code - 127), a normal power of two.  Encoding then runs the
-// NVFP4 element path with this inverse.
-__device__ __forceinline__ BlockScale mxfp4_block_scale(uint32_t amax_bits) {
-  BlockScale r;
-  const int32_t e = (int32_t)(amax_bits >> 7) - 2;
-  r.s = (uint32_t)max(e, 0);
-  r.inv = __uint_as_float((254u - r.s) << 23);
-  r.p = 0.0f;   // unused: MXFP4 never takes the special path
-  r.special = false;
-  return r;
-}
-
-// The 16 random halves of source elements e0 .. e0+15 (e0 % 8 == 0).
-__device__ __forceinline__ void sr_bits16(int64_t e0, uint64_t seed, uint64_t sid, uint32_t (&u)[8]) {
-  const U4 w0 = sr_words((uint64_t)e0 >> 3, seed, sid);
-  const U4 w1 = sr_words(((uint64_t)e0 >> 3) + 1, seed, sid);
-  u[0] = w0.x; u[1] = w0.y; u[2] = w0.z; u[3] = w0.w;
-  u[4] = w1.x; u[5] = w1.y; u[6] = w1.z; u[7] = w1.w;
-}
-// random half of element i from the packed words (element i in half i%2 of word i/2)
-__device__ __forceinline__ uint32_t uhalf(const uint32_t (&u)[8], int i) {
-  return (i & 1) ? (u[i >> 1] >> 16) : (u[i >> 1] & 0xffffu);
-}
-
-// Sources of the 16 random bits of element i of a block, for the encoders:
-// packed two per word (element i in half i%2 of word i/2) ...
-struct PackedBits {
-  const uint32_t* u;
-  __device__ __forceinline__ uint32_t operator()(int i) const { return (i & 1) ? (u[i >> 1] >> 16) : (u[i >> 1] & 0xffffu); }
-};
-// ... or one word per element, shared by two source columns: the even column's
-// bits in the low half (HI false), the odd column's in the high half.
-template <bool HI>
-struct WordHalfBits {
-  const uint32_t* r;
-  __device__ __forceinline__ uint32_t operator()(int i) const { return HI ? (r[i] >> 16) : (r[i] & 0xffffu); }
-};
-
-// Encode one NVFP4 block of 16 signed values into two words of packed codes
-// (element 2j in the low nibble of byte j).  RND: 0 nearest, 1 stochastic.
-template <int RND, class Bits = PackedBits>
-__device__ __forceinline__ uint2 nvfp4_encode16(const float (&v)[16], const BlockScale& bs, Bits bits) {
-  uint32_t w[2] = {0u, 0u};
-  if (bs.special) {
-    // p == 0: every magnitude 0; 1/p overflowed: non-zero elements saturate to 6
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t sign = (__float_as_uint(v[i]) >> 28) & 8u;
-      const uint32_t mag = (bs.p == 0.0f || v[i] == 0.0f) ? 0u : 7u;
-      w[i >> 3] |= (sign | mag) << (4 * (i & 7));
-    }
-  } else if (RND == 0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      w[i >> 2] |= e2m1x2_rn(__fmul_rn(v[2 * i], bs.inv), __fmul_rn(v[2 * i + 1], bs.inv)) << (8 * (i & 3));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t b = __float_as_uint(v[i]);
-      const float y = __fmul_rn(__uint_as_float(b & 0x7fffffffu), bs.inv);
-      w[i >> 3] |= (((b >> 28) & 8u) | e2m1_sr(y, bits(i))) << (4 * (i & 7));
-    }
-  }
-  return make_uint2(w[0], w[1]);
 }
 
 // Squared dequantization error of an encoded block (x_hat = value(code) * p).

@@ -52,6 +52,14 @@ struct GemmParams {
   int num_m_tiles, num_n_tiles;
   int v8;                       // D rows allow 32-byte stores
   int a_e5m2;                   // FP8 only: A is E5M2 (B stays E4M3)
+  // NVFP4 re-quantization of the output for the next GEMM (null rq_codes: off)
+  uint8_t* rq_codes;            // MMA layout, rows padded to 256, N padded to rq_ocp
+  uint8_t* rq_scales;
+  const float* rq_g;            // tensor scale to quantize with (given, e.g. delayed)
+  uint32_t* rq_amax;            // max |bf16(output)| as float bits (atomicMax; zeroed by the host)
+  int64_t rq_ocp;
+  uint64_t rq_seed, rq_stream;
+  int rq_rnd;
   uint32_t* status;
   uint64_t timeout_ns;
 };

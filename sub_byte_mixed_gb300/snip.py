@@ -35,7 +35,7 @@ EXPORTS = (
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
     "snip_quant_stats", "snip_quantize_stats", "snip_stats_finalize", "snip_plan_costs", "snip_plan_select",
-    "snip_dw_noise_workspace_size", "snip_dw_noise", "snip_dw_noise_finalize",
+    "snip_dw_noise_workspace_size", "snip_dw_noise", "snip_dw_noise_finalize", "snip_gemm_requant",
 )
 
 
@@ -43,6 +43,12 @@ class SnipError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
         super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
+
+
+class SnipRequant(ctypes.Structure):
+    _fields_ = [("g_in", ctypes.c_void_p), ("rnd", ctypes.c_int), ("seed", ctypes.c_uint64),
+                ("stream_id", ctypes.c_uint64), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("amax_out", ctypes.c_void_p)]
 
 
 class SnipStats(ctypes.Structure):
@@ -93,6 +99,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_stats_finalize": (i32, [vp, ctypes.POINTER(SnipStats)]),
         "snip_plan_costs": (i32, [i32, vp, vp, vp]),
         "snip_dw_noise_workspace_size": (sz, [i64, i64]),
+        "snip_gemm_requant": (i32, [i32, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, i64,
+                                    ctypes.POINTER(SnipRequant), vp, sz, vp]),
         "snip_dw_noise": (i32, [vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]),
         "snip_dw_noise_finalize": (i32, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
         "snip_plan_select": (i32, [i32, vp, vp, vp, ctypes.c_double, vp, vp, vp]),
@@ -516,6 +524,27 @@ def dw_noise(X, dY, dW_q, ws: Workspace | None = None):
     snip_dw_noise(X.data_ptr(), dY.data_ptr(), T, K, N, dW_q.data_ptr(), out.data_ptr(), ws.ptr, ws.nbytes,
                   _stream())
     return out
+
+
+def gemm_requant(fmt, a, b, M, N, K, g_in, rnd=SR, seed=0, stream_id=0, want_d=True, ws: Workspace | None = None):
+    """D = A B^T (fp32, or None) plus D rounded to bf16 and quantized to NVFP4 row blocks with the
+    device tensor scale g_in (1-element float tensor) -> (D, QuantNVFP4 in the MMA layout, amax tensor)."""
+    torch = _torch()
+    ws = ws or small_workspace()
+    dev = a.codes.device
+    D = torch.empty((M, N), dtype=torch.float32, device=dev) if want_d else None
+    cb, sb = snip_quantized_bytes(NVFP4, MMA, M, N)
+    codes = torch.empty(max(cb, 16), dtype=torch.uint8, device=dev)
+    scales = torch.empty(max(sb, 16), dtype=torch.uint8, device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    rq = SnipRequant(g_in.data_ptr(), rnd, seed, stream_id, codes.data_ptr(), scales.data_ptr(), amax.data_ptr())
+    sa = a.scales.data_ptr() if fmt in (NVFP4, MXFP4) else None
+    sb_ = b.scales.data_ptr() if fmt in (NVFP4, MXFP4) else None
+    ga = (a.g if fmt == NVFP4 else a.s).data_ptr() if fmt != MXFP4 else None
+    gb = (b.g if fmt == NVFP4 else b.s).data_ptr() if fmt != MXFP4 else None
+    _call("snip_gemm_requant", fmt, a.codes.data_ptr(), sa, ga, b.codes.data_ptr(), sb_, gb, M, N, K,
+          D.data_ptr() if D is not None else None, N, ctypes.byref(rq), ws.ptr, ws.nbytes, _stream())
+    return D, QuantNVFP4(codes[:cb], scales[:sb], g_in, M, N, MMA), amax
 
 
 def quant_stats(a, rnd=RTN, seed=0, stream_id=0, want_block_err=False, ws: Workspace | None = None, raw=None,
