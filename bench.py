@@ -412,6 +412,45 @@ def quantizer_sweep(snip, hbm_gbs: float, reps: int = 10):
             "variants": out}
 
 
+def requant_compare(snip, reps: int = 10):
+    """The Down linear's dgrad of the 7B block (dX = dY W: 8192 x 11008, contraction 4096), NVFP4:
+    the product re-quantized in the GEMM epilogue for the preceding layer (snip_gemm_requant, no fp32
+    output) against the unfused chain it replaces -- fp32 dX, a bf16 copy, then the row-block SR
+    quantization of that copy."""
+    import torch
+    from sub_byte_mixed_gb300 import inputs
+    M, N, K = 8192, 11008, 4096
+    dY = inputs.normal_bf16((M, K), 1e-3, 0, 40, "cuda")
+    Wt = inputs.normal_bf16((N, K), 0.02, 0, 41, "cuda")
+    a = snip.quantize_nvfp4(dY, rnd=1, layout=snip.MMA)
+    b = snip.quantize_nvfp4(Wt, rnd=1, layout=snip.MMA)
+    g = torch.tensor([1e-5], dtype=torch.float32, device="cuda")
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    Db = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+
+    def fused():
+        snip.gemm_requant(snip.NVFP4, a, b, M, N, K, g, rnd=1, seed=0, stream_id=2, want_d=False)
+
+    def unfused():
+        snip.gemm(snip.NVFP4, a, b, M, N, K, out=D)
+        Db.copy_(D)
+        snip.quantize_nvfp4(Db, rnd=1, seed=0, stream_id=2, g_in=g, layout=snip.MMA)
+
+    out = {}
+    for name, fn in (("fused_ms", fused), ("unfused_ms", unfused)):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = round(e0.elapsed_time(e1) / reps, 4)
+    out["shape"] = f"{M}x{N}x{K} NVFP4, SR re-quantization"
+    return out
+
+
 def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
     """The same step through the layer API (snip_qlinear_fwd / _bwd, statistics fused into their
     quantizations) with host buffers: every step copies all inputs (X, W, dY, bf16) in from pinned host
@@ -566,9 +605,10 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
-    qsweep = None
+    qsweep = rqcmp = None
     if not args.profile_run and not layers and rank == 0:
         qsweep = quantizer_sweep(snip, measured_peaks()["hbm_gbs"])
+        rqcmp = requant_compare(snip)
     e2e = None
     if not args.no_e2e and not args.profile_run and not layers and rank == 0:
         e2e = e2e_run(cfg, plan, snip, step, args.e2e_steps)
@@ -618,6 +658,7 @@ def run_ours(args, rank, world, local_rank):
         "quantizer": quant,
         "gemm_only": {"value": gemm_fl / (gemm_ms * 1e-3) / 1e12, "unit": UNIT},
         "quantizer_sweep": qsweep,
+        "next3_requant": rqcmp,
         "breakdown": breakdown,
         "clocks": clocks,
         "e2e": e2e,
