@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--plan", default="mix", choices=["mix", "nvfp4", "fp8", "mxfp4", "snip"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="run every call on one stream (no quantization beside the GEMMs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-run", action="store_true",
                     help="exactly --warmup untimed steps, no clock settle, e2e or CPU baseline (for ncu)")
@@ -89,6 +91,9 @@ def config_json(cfg, plan, args):
         "l2": "inputs larger than L2 (no flush)",
         "rounding": "RTN forward, SR (Philox4x32-10, 16 bits/elem) backward",
         "stats": "SNIP statistics of X, W (forward rounding) and dY (dgrad rounding) fused into their row-block quantizations",
+        "schedule": ("one stream" if args.no_overlap else
+                     "quantizations and GEMMs on two streams: a linear's quantizations run beside the previous "
+                     "linear's GEMMs (events order every GEMM after its operands)"),
         "plan_source": ("SNIP selection from one step's statistics (snip_plan_select, FP4-FLOP target "
                         f"{cfg.fp4_target})") if args.plan == "snip" else
                        ("seeded plan at the FP4-FLOP target" if args.plan == "mix" else "uniform"),
@@ -249,10 +254,16 @@ def whole_job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
 class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
-    def __init__(self, cfg, plan, snip, device, layers=None):
+    def __init__(self, cfg, plan, snip, device, layers=None, overlap=True):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
+        # overlap: quantizations on one stream, GEMMs on another, so that a linear's quantizations run
+        # beside the previous linear's GEMMs; operand buffers alternate between two sets by linear
+        self.overlap = overlap
+        self.sQ = torch.cuda.current_stream()
+        self.sG = torch.cuda.Stream() if overlap else self.sQ
+        nsets = 2 if overlap else 1
         L = snip.load()
         self.inp = inputs.block_inputs(cfg, seed=0, device=device)
         T = cfg.T
@@ -272,17 +283,20 @@ class Step:
             for r, (_, _, orr, occ) in enumerate(roles(l)):
                 c, s = snip.snip_quantized_bytes(f, snip.MMA, orr, occ)
                 csz[r], ssz[r] = max(csz[r], c), max(ssz[r], s)
-        self.codes = [torch.empty(c, dtype=torch.uint8, device=device) for c in csz]
-        self.scales = [torch.empty(max(s, 16), dtype=torch.uint8, device=device) for s in ssz]
-        ws, wsb, stream = self.ws.ptr, self.ws.nbytes, torch.cuda.current_stream().cuda_stream
+        codes_sets = [[torch.empty(c, dtype=torch.uint8, device=device) for c in csz] for _ in range(nsets)]
+        scales_sets = [[torch.empty(max(s, 16), dtype=torch.uint8, device=device) for s in ssz] for _ in range(nsets)]
+        ws, wsb, stream = self.ws.ptr, self.ws.nbytes, self.sQ.cuda_stream
+        gstream = self.sG.cuda_stream
         self.stream = stream
-        calls = []   # (fn, args, category, units) units = bytes (HBM kernels) or flops (GEMMs)
+        calls = []   # (fn, args, category, units, stream kind 'q'/'g', linear, GEMM index or -1)
+        self.gemm_ws = snip.Workspace(snip.WS_HEADER_BYTES, device) if overlap else self.ws
         self._keep = []   # ctypes arrays referenced by the calls
         for j, (l, f) in enumerate(zip(cfg.linears, plan)):
             if layers and l.name not in layers:
                 continue
             X = self.inp.X[l.x_id]
             W, dY = self.inp.W[j], self.inp.dY[j]
+            self.codes, self.scales = codes_sets[j % nsets], scales_sets[j % nsets]
             src = {l.x_id: X, "W": W, "dY": dY}
             scp = {l.x_id: self.sc[j, 0].data_ptr(), "W": self.sc[j, 1].data_ptr(), "dY": self.sc[j, 2].data_ptr()}
             sid = 8 * j
@@ -298,7 +312,7 @@ class Step:
             outs = (ctypes.c_void_p * 3)(*[scp[nm] for nm in names])
             self._keep.append((xs, ns, outs))
             calls.append((L.snip_tensor_scales_multi, (3, xs, ns, outs, ws, wsb, stream), "scales",
-                          SCALES_BYTES_PER_ELEM * sum(src[nm].numel() for nm in names)))
+                          SCALES_BYTES_PER_ELEM * sum(src[nm].numel() for nm in names), "q", j, -1))
             for r, (name, orient, orr, occ) in enumerate(roles(l)):
                 t = src[name]
                 rows, cols = t.shape
@@ -309,19 +323,19 @@ class Step:
                     args = (f, t.data_ptr(), rows, cols, rnd[r], 0, sid + r, scp[name], snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr() if f != snip.FP8 else None,
                             self.raw[j, k].data_ptr(), ws, wsb, stream)
-                    calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel()))
+                    calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", j, -1))
                 elif f == snip.NVFP4:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, None, ws, wsb, stream)
-                    calls.append((L.snip_quantize_nvfp4, args, qcat, bpe * t.numel()))
+                    calls.append((L.snip_quantize_nvfp4, args, qcat, bpe * t.numel(), "q", j, -1))
                 elif f == snip.MXFP4:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), ws, wsb, stream)
-                    calls.append((L.snip_quantize_mxfp4, args, qcat, bpe * t.numel()))
+                    calls.append((L.snip_quantize_mxfp4, args, qcat, bpe * t.numel(), "q", j, -1))
                 else:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), g, ws, wsb, stream)
-                    calls.append((L.snip_quantize_fp8, args, qcat, bpe * t.numel()))
+                    calls.append((L.snip_quantize_fp8, args, qcat, bpe * t.numel(), "q", j, -1))
                 if r in (1, 3, 5):   # both operands of a GEMM are ready
                     a, b = r - 1, r
                     M, N, K = {1: (T, l.N, l.K), 3: (T, l.K, l.N), 5: (l.N, l.K, T)}[r]
@@ -330,22 +344,58 @@ class Step:
                     sb = self.scales[b].data_ptr() if f != snip.FP8 else None
                     ga = scp[roles(l)[a][0]] + fo if f != snip.MXFP4 else None
                     gb = scp[roles(l)[b][0]] + fo if f != snip.MXFP4 else None
+                    gw = self.gemm_ws
                     args = (f, self.codes[a].data_ptr(), sa, ga, self.codes[b].data_ptr(), sb, gb, M, N, K,
-                            D.data_ptr(), D.stride(0), ws, wsb, stream)
-                    calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K))
+                            D.data_ptr(), D.stride(0), gw.ptr, gw.nbytes, gstream)
+                    calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K, "g", j, r // 2))
         self.calls = calls
+        # the same calls with every launch on the quantization stream (kernels one after another)
+        self.serial_args = [a if k == "q" else a[:-1] + (stream,) for (_, a, _, _, k, _, _) in calls]
         # one kernel per call (the scales are computed once per tensor and passed in)
         self.launches_per_step = len(calls)
 
-    def run(self, events=None):
-        for i, (fn, args, _, _) in enumerate(self.calls):
+    def run(self, events=None, serial=False):
+        """One step.  With overlap, a GEMM waits for its two operands' quantizations, and the
+        quantizations of linear j wait until linear j-2's GEMMs (the last readers of the same
+        operand buffers) are done; the step ends on the quantization stream after all GEMMs.
+        serial: every kernel on the quantization stream, one after another (per-kernel timing)."""
+        import torch
+        ready, gdone = {}, {}
+        last_g = None
+        overlap = self.overlap and not serial
+        for i, (fn, args, _, _, kind, j, gi) in enumerate(self.calls):
+            if serial:
+                args = self.serial_args[i]
+            stream = self.sQ if kind == "q" or serial else self.sG
+            if overlap:
+                if kind == "q" and gi < 0 and (j - 2) in gdone and fn.__name__ == "snip_tensor_scales_multi":
+                    self.sQ.wait_event(gdone[j - 2])
+                if kind == "g":
+                    self.sG.wait_event(ready[(j, gi)])
             if events is not None:
-                events[i][0].record()
+                events[i][0].record(stream)
             st = fn(*args)
             if st != 0:
                 raise RuntimeError(f"{fn.__name__} failed with status {st}")
             if events is not None:
-                events[i][1].record()
+                events[i][1].record(stream)
+            if overlap:
+                nxt = self.calls[i + 1] if i + 1 < len(self.calls) else None
+                if kind == "q" and nxt is not None and nxt[4] == "g":   # both operands of the next GEMM written
+                    ev = torch.cuda.Event()
+                    ev.record(self.sQ)
+                    ready[(nxt[5], nxt[6])] = ev
+                if kind == "g":
+                    ev = torch.cuda.Event()
+                    ev.record(self.sG)
+                    gdone[j] = ev
+                    last_g = ev
+        if overlap and last_g is not None:
+            self.sQ.wait_event(last_g)
+
+    def status(self):
+        s = self.ws.status()
+        return s if s != self.snip.SNIP_OK or not self.overlap else self.gemm_ws.status()
 
 
 def quantizer_sweep(snip, hbm_gbs: float, reps: int = 10):
@@ -465,7 +515,9 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
     hraw = torch.empty(step.raw.shape, dtype=step.raw.dtype).pin_memory()
     p = snip.Plan(plan, seed=0)
     wsb = max(snip.snip_qlinear_workspace_size(p.handle, j, cfg.T, l.K, l.N) for j, l in enumerate(cfg.linears))
-    ws = snip.Workspace(wsb)
+    # two layer-call streams, linears alternating between them with a workspace each: a linear's
+    # quantizations run beside the previous linear's GEMMs
+    wss = [snip.Workspace(wsb), snip.Workspace(wsb)]
     h2d = sum(t.numel() * t.element_size() for t in list(hX.values()) + hW + hdY)
     d2h = hraw.numel() * 8
 
@@ -473,6 +525,7 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
     # inputs are copied while earlier linears compute, and its statistics read back while later ones do;
     # events keep each device buffer from being overwritten before its last reader is done.
     sC, sH, sD = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    sCs = [sC, torch.cuda.Stream()]
     n = len(cfg.linears)
     ev = lambda: torch.cuda.Event()
     last_user = {}   # x_id -> last linear reading that activation
@@ -500,17 +553,20 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
                 loaded[j] = ev()
                 loaded[j].record(sH)
         for j, l in enumerate(cfg.linears):
-            sC.wait_event(loaded[j])
+            sc, ws = sCs[j % 2], wss[j % 2]
+            sc.wait_event(loaded[j])
             if first_user[l.x_id] != j:
-                sC.wait_event(loaded[first_user[l.x_id]])
+                sc.wait_event(loaded[first_user[l.x_id]])
             if state["drained"][j] is not None:
-                sC.wait_event(state["drained"][j])      # the previous step's statistics copied out
+                sc.wait_event(state["drained"][j])      # the previous step's statistics copied out
             X = inp.X[l.x_id]
             # statistics of X, W (forward) and dY (dgrad) come out of the quantization passes
-            snip.qlinear_fwd(p, j, X, inp.W[j], ws, Y=step.Y[j], stats=step.raw[j, 0:2])
-            snip.qlinear_bwd(p, j, X, inp.W[j], inp.dY[j], ws, dX=step.dX[j], dW=step.dW[j], stats=step.raw[j, 2])
+            with torch.cuda.stream(sc):
+                snip.qlinear_fwd(p, j, X, inp.W[j], ws, Y=step.Y[j], stats=step.raw[j, 0:2])
+                snip.qlinear_bwd(p, j, X, inp.W[j], inp.dY[j], ws, dX=step.dX[j], dW=step.dW[j],
+                                 stats=step.raw[j, 2])
             done = ev()
-            done.record(sC)
+            done.record(sc)
             state["computed"][j] = done
             with torch.cuda.stream(sD):
                 sD.wait_event(done)
@@ -525,20 +581,36 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
     e0.record(sC)
     sH.wait_event(e0)
     sD.wait_event(e0)
+    sCs[1].wait_event(e0)
     for _ in range(nsteps):
         one()
     for j in range(n):
         sC.wait_event(state["drained"][j])
     e1.record(sC)
     torch.cuda.synchronize()
-    if ws.status() != snip.SNIP_OK:
-        raise RuntimeError("device status " + snip.status_string(ws.status()))
+    for ws in wss:
+        if ws.status() != snip.SNIP_OK:
+            raise RuntimeError("device status " + snip.status_string(ws.status()))
     ms = e0.elapsed_time(e1) / nsteps
+    # the host->device copies of one step alone, for the bound they put on the step
+    torch.cuda.synchronize()
+    e0.record(sH)
+    for _ in range(nsteps):
+        with torch.cuda.stream(sH):
+            for k in hX:
+                inp.X[k].copy_(hX[k], non_blocking=True)
+            for j in range(n):
+                inp.W[j].copy_(hW[j], non_blocking=True)
+                inp.dY[j].copy_(hdY[j], non_blocking=True)
+    e1.record(sH)
+    torch.cuda.synchronize()
+    ms_h2d = e0.elapsed_time(e1) / nsteps
     return {"value": cfg.flops_fwd_bwd() / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "h2d_only_ms_per_step": ms_h2d,
+            "h2d_gbs": h2d / (ms_h2d * 1e-3) / 1e9,
             "path": "snip_qlinear_fwd/bwd with fused statistics; all inputs copied in from pinned host memory "
                     "and the step's SNIP statistics read back every step, overlapping other linears' calls "
-                    "(three streams); Y, dX, dW stay on the device"}
+                    "(copy-in, two layer-call and copy-out streams); Y, dX, dW stay on the device"}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -551,7 +623,7 @@ def run_ours(args, rank, world, local_rank):
     snip.snip_device_check()
     cfg, plan = workload(args)
     layers = [x for x in args.layers.split(",") if x]
-    step = Step(cfg, plan, snip, "cuda", layers)
+    step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap)
     if args.plan == "snip" and layers:
         raise SystemExit("--plan snip selects formats for the whole block; it cannot be combined with --layers")
     if args.plan == "snip":
@@ -562,7 +634,7 @@ def run_ours(args, rank, world, local_rank):
         flops = [6.0 * cfg.T * l.K * l.N for l in cfg.linears]
         plan, _, _ = snip.snip_plan_select(flops, c8, c4, cfg.fp4_target)
         del step
-        step = Step(cfg, plan, snip, "cuda", layers)
+        step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap)
     torch.cuda.synchronize()
     ncalls = len(step.calls)
     sampler = ClockSampler(local_rank) if rank == 0 and not args.profile_run else None
@@ -590,19 +662,36 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     ms = start.elapsed_time(stop) / args.steps
-    status = step.ws.status()
+    status = step.status()
     if status != snip.SNIP_OK:
         raise RuntimeError("device status " + snip.status_string(status))
-    # per-category kernel time inside the timed region
+    ms_serial = None
+    if step.overlap:
+        # per-kernel durations: kernels that share the SMs stretch each other's event times, so the
+        # breakdown and the roofline come from the same step run serially, K more steps in a row
+        for _ in range(3):
+            step.run(serial=True)
+        torch.cuda.synchronize()
+        start.record()
+        for s in range(args.steps):
+            step.run(events[s], serial=True)
+        stop.record()
+        torch.cuda.synchronize()
+        ms_serial = start.elapsed_time(stop) / args.steps
+        status = step.status()
+        if status != snip.SNIP_OK:
+            raise RuntimeError("device status " + snip.status_string(status))
+    # per-category kernel time
     cat_ms, cat_units, cat_n = {}, {}, {}
     for s in range(args.steps):
-        for i, (_, _, cat, units) in enumerate(step.calls):
+        for i, (_, _, cat, units, _, _, _) in enumerate(step.calls):
             t = events[s][i][0].elapsed_time(events[s][i][1])
             cat_ms[cat] = cat_ms.get(cat, 0.0) + t
             cat_units[cat] = cat_units.get(cat, 0.0) + units
             cat_n[cat] = cat_n.get(cat, 0) + 1
+    t2 = time.time()
     ms = max_over_ranks(ms, world, "cuda")
-    clocks = sampler.summary(t0, t1) if sampler else None
+    clocks = sampler.summary(t0, t2) if sampler else None
     if sampler:
         sampler.stop()
     qsweep = rqcmp = None
@@ -640,7 +729,11 @@ def run_ours(args, rank, world, local_rank):
         traffic = tr * cat_units[dom] / cat_n[dom]
     roofline = {"bound": "tensor" if dom.startswith("gemm") else "hbm", "kernel": dom,
                 "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"], "frac": d["frac"],
-                "traffic": traffic, "peak_source": f"{peaks['source']} ("
+                "traffic": traffic,
+                "timed": ("CUDA events around each launch in K serial steps after the overlapped timed region "
+                          "(kernels alone on the GPU)" if step.overlap else
+                          "CUDA events around each launch in the timed region"),
+                "peak_source": f"{peaks['source']} ("
                 + ("bf16 sustained x nominal FP4/FP8 ratio" if dom.startswith("gemm") else "HBM copy") + ")"}
     qcats = [c for c in breakdown if not c.startswith("gemm")]
     q_bytes = sum(cat_units[c] for c in qcats) / args.steps
@@ -663,6 +756,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": step.launches_per_step * args.steps,
+        "ms_per_step_one_stream": ms_serial,
     }
     if layers:
         line["config"]["layers"] = layers
