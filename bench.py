@@ -486,8 +486,19 @@ def requant_compare(snip, reps: int = 10):
         Db.copy_(D)
         snip.quantize_nvfp4(Db, rnd=1, seed=0, stream_id=2, g_in=g, layout=snip.MMA)
 
+    # both orientations: the preceding layer's dgrad operand (row blocks) and its wgrad operand dY^T
+    # (column blocks, along the tokens)
+    def fused_both():
+        snip.gemm_requant(snip.NVFP4, a, b, M, N, K, g, rnd=1, seed=0, stream_id=2, want_d=False, cols=True,
+                          rnd_t=1, stream_id_t=4)
+
+    def unfused_both():
+        unfused()
+        snip.quantize_nvfp4(Db, orient=snip.ALONG_ROWS, rnd=1, seed=0, stream_id=4, g_in=g, layout=snip.MMA)
+
     out = {}
-    for name, fn in (("fused_ms", fused), ("unfused_ms", unfused)):
+    for name, fn in (("fused_ms", fused), ("unfused_ms", unfused), ("fused_both_ms", fused_both),
+                     ("unfused_both_ms", unfused_both)):
         fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -497,7 +508,7 @@ def requant_compare(snip, reps: int = 10):
         e1.record()
         torch.cuda.synchronize()
         out[name] = round(e0.elapsed_time(e1) / reps, 4)
-    out["shape"] = f"{M}x{N}x{K} NVFP4, SR re-quantization"
+    out["shape"] = f"{M}x{N}x{K} NVFP4, SR re-quantization (row blocks; _both: row and column blocks)"
     return out
 
 

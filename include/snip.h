@@ -300,32 +300,47 @@ snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_
 
 /* NEXT-3: the GEMM whose product is the next layer's operand -- typically the
  * dgrad product dX, the preceding layer's dY -- also writes that operand
- * quantized, so the bf16 round trip and a separate quantization pass go
- * away ("SNIP", Figure 5: each GEMM operand quantized along its own
- * contraction dim; the preceding layer's dgrad contracts over this dX's
- * columns).  The product D = ga*gb*A B^T is rounded to bf16 and quantized to
- * NVFP4 in 16-element blocks along its rows (N), with the given tensor scale
- * (the pages say nothing about when its amax is known: the caller passes
- * one, e.g. the previous step's amax_out / 2688; values beyond 6 * 448 * g
- * saturate), nearest or stochastic with the bits of element index m*N + n.
- * codes / scales (device, 16-byte aligned): the MMA layout of an M x N NVFP4
- * operand, sized by snip_quantized_bytes(SNIP_FMT_NVFP4, SNIP_LAYOUT_MMA, M,
- * N); padding is written as zeros.  amax_out (device, nullable) receives
- * max |bf16(D)| of this product, for the next scale. */
+ * quantized, in both orientations, so the bf16 round trip and two separate
+ * quantization passes go away ("SNIP", Figure 5: each GEMM operand quantized
+ * along its own contraction dim; the preceding layer's dgrad contracts over
+ * this dX's columns, its wgrad over its rows).  The product D = ga*gb*A B^T
+ * is rounded to bf16 and quantized to NVFP4 with the given tensor scale (the
+ * pages say nothing about when its amax is known: the caller passes one,
+ * e.g. the previous step's amax_out / 2688; values beyond 6 * 448 * g
+ * saturate):
+ *   rows    (codes, scales; rnd, stream_id): 16-element blocks along the rows
+ *           of D (along N) -- the M x N operand, as snip_quantize_nvfp4 with
+ *           SNIP_BLOCKS_ALONG_COLS on bf16(D);
+ *   columns (codes_t, scales_t; rnd_t, stream_id_t): 16-element blocks down
+ *           the columns of D (along M) -- the N x M operand D^T, as
+ *           snip_quantize_nvfp4 with SNIP_BLOCKS_ALONG_ROWS on bf16(D).
+ * Each orientation is nearest or stochastic; stochastic rounding takes the
+ * bits of element index m*N + n of its own stream (the same bits the
+ * quantizer draws for bf16(D)).  Either orientation may be omitted (NULL
+ * codes), not both.  codes / scales (device, 16-byte aligned): the MMA layout
+ * of the M x N (rows) or N x M (columns) NVFP4 operand, sized by
+ * snip_quantized_bytes(SNIP_FMT_NVFP4, SNIP_LAYOUT_MMA, ...); padding is
+ * written as zeros.  amax_out (device, nullable) receives max |bf16(D)| of
+ * this product, for the next scale. */
 typedef struct {
     const float* g_in;
-    int rnd;               /* snip_round */
-    uint64_t seed;
-    uint64_t stream_id;
-    uint8_t* codes;
+    int rnd;               /* snip_round of the row blocks */
+    uint64_t seed;         /* both orientations */
+    uint64_t stream_id;    /* row blocks */
+    uint8_t* codes;        /* row blocks: M x N operand (nullable) */
     uint8_t* scales;
     float* amax_out;
+    int rnd_t;             /* snip_round of the column blocks */
+    uint64_t stream_id_t;  /* column blocks */
+    uint8_t* codes_t;      /* column blocks: N x M operand D^T (nullable) */
+    uint8_t* scales_t;
 } snip_requant;
 
 /* snip_gemm plus the re-quantized product described above; D (fp32) may be
- * NULL when only the quantized operand is wanted.  N % 16 == 0.  Errors as
- * for snip_gemm; SNIP_ERR_INVALID_ARG for a null rq, rq->g_in, rq->codes or
- * rq->scales. */
+ * NULL when only the quantized operand is wanted.  N % 16 == 0, and M % 16 ==
+ * 0 when the column blocks are written, else SNIP_ERR_SHAPE.  Errors as for
+ * snip_gemm; SNIP_ERR_INVALID_ARG for a null rq or rq->g_in, no orientation,
+ * an orientation without its scales, or a rounding outside snip_round. */
 snip_status snip_gemm_requant(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
                               const uint8_t* b_codes, const uint8_t* b_scales, const float* gb,
                               int64_t M, int64_t N, int64_t K, float* D, int64_t ldd, const snip_requant* rq,

@@ -224,12 +224,28 @@ snip_status run_gemm(int fmt, const uint8_t* a_codes, const uint8_t* a_scales, c
     p.rq_seed = rq->seed;
     p.rq_stream = rq->stream_id;
     p.rq_rnd = rq->rnd;
+    // column blocks: the N x M transpose, rows padded to 256, contraction M to 256
+    const int64_t orp_t = mma_rows(N), ocp_t = round_up(M, 256);
+    p.rq_codes_t = rq->codes_t;
+    p.rq_scales_t = rq->scales_t;
+    p.rq_ocp_t = ocp_t;
+    p.rq_stream_t = rq->stream_id_t;
+    p.rq_rnd_t = rq->rnd_t;
     // the tiles write every padded row and column they cover; one-CTA tiles (128 rows) may
-    // leave the last rows of the 256-row padding, so those codes and all scales start at zero
+    // leave the last 128 rows of the 256-row padding of M, so those codes and all scales start at zero
     const int64_t covered = round_up(M, 128);
     cudaError_t e = cudaSuccess;
-    if (covered < orp) e = cudaMemsetAsync(rq->codes + covered * (ocp / 2), 0, (size_t)((orp - covered) * (ocp / 2)), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(rq->scales, 0, (size_t)(orp * ocp / 16), st);
+    if (rq->codes) {
+      if (covered < orp)
+        e = cudaMemsetAsync(rq->codes + covered * (ocp / 2), 0, (size_t)((orp - covered) * (ocp / 2)), st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(rq->scales, 0, (size_t)(orp * ocp / 16), st);
+    }
+    if (rq->codes_t) {   // there the uncovered rows of D are the last contraction columns of every row
+      if (e == cudaSuccess && covered < ocp_t)
+        e = cudaMemset2DAsync(rq->codes_t + covered / 2, (size_t)(ocp_t / 2), 0, (size_t)((ocp_t - covered) / 2),
+                              (size_t)orp_t, st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(rq->scales_t, 0, (size_t)(orp_t * ocp_t / 16), st);
+    }
     if (e == cudaSuccess && rq->amax_out) e = cudaMemsetAsync(rq->amax_out, 0, sizeof(float), st);
     if (e != cudaSuccess) return cuda_status(e);
   }
@@ -431,17 +447,20 @@ snip_status snip_gemm_requant(snip_format fmt, const uint8_t* a_codes, const uin
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
-  if (!rq || !rq->g_in || !rq->codes || !rq->scales || !valid_enum(rq->rnd, 2)) return SNIP_ERR_INVALID_ARG;
+  if (!rq || !rq->g_in || (!rq->codes && !rq->codes_t) || (rq->codes && !rq->scales) ||
+      (rq->codes_t && !rq->scales_t) || !valid_enum(rq->rnd, 2) || !valid_enum(rq->rnd_t, 2))
+    return SNIP_ERR_INVALID_ARG;
   if (!valid_enum(fmt, 4) || M < 0 || N < 0 || K < 0 || (D && ldd < N)) return SNIP_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return SNIP_OK;
   if (!a_codes || !b_codes) return SNIP_ERR_INVALID_ARG;
   if (fmt != SNIP_FMT_MXFP4 && (!ga || !gb)) return SNIP_ERR_INVALID_ARG;
   if (is_fp4(fmt) && (!a_scales || !b_scales)) return SNIP_ERR_INVALID_ARG;
-  if (K % 16 != 0 || K == 0 || N % 16 != 0 || (D && ldd % 4 != 0) || (fmt == SNIP_FMT_MXFP4 && K % 32 != 0))
+  if (K % 16 != 0 || K == 0 || N % 16 != 0 || (rq->codes_t && M % 16 != 0) || (D && ldd % 4 != 0) ||
+      (fmt == SNIP_FMT_MXFP4 && K % 32 != 0))
     return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < SNIP_WS_HEADER_BYTES) return SNIP_ERR_WORKSPACE;
   if (!aligned16(a_codes) || !aligned16(b_codes) || (D && !aligned16(D)) || !aligned16(ws) ||
-      !aligned16(rq->codes) || !aligned16(rq->scales) ||
+      !aligned16(rq->codes) || !aligned16(rq->scales) || !aligned16(rq->codes_t) || !aligned16(rq->scales_t) ||
       (is_fp4(fmt) && (!aligned16(a_scales) || !aligned16(b_scales))))
     return SNIP_ERR_ALIGN;
   return run_gemm(fmt, a_codes, a_scales, ga, b_codes, b_scales, gb, M, N, K, D, D ? ldd : N, ws, sms,

@@ -37,7 +37,13 @@
 
 namespace snip {
 
-template <int FMT, int BN>
+// Shared memory per CTA (227 KB), and the transposed re-quantization's
+// staging: per epilogue warp 32 rows x 9 pairs {two bf16 values, their two
+// random halves} (8 used, one pad: conflict-free row writes and column reads).
+constexpr int kMaxSmem = 232448;
+constexpr int kRqStageWords = 32 * 9;
+
+template <int FMT, int BN, bool RQ = false>
 struct GemmCfg {
   static constexpr int BM = 128;
   static constexpr int KB = 128;  // contraction bytes per stage and row (256 FP4 / 128 FP8 elements)
@@ -49,7 +55,9 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = FMT ? CH * 512 : 0;
   static constexpr int SFB_BYTES = FMT ? (BN / 128) * CH * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int STAGES = 4;
+  static constexpr int RQ_BYTES = RQ ? 8 * kRqStageWords * 8 : 0;   // 8 epilogue warps
+  // four stages; a re-quantizing instantiation gives one up where its staging would not fit
+  static constexpr int STAGES = 4 * STAGE_BYTES + 2048 + RQ_BYTES <= kMaxSmem ? 4 : 3;
   static constexpr int ACC_STAGES = (FMT && BN == 256) ? 1 : 2;
   // tensor-memory columns of one stage's scale factors: per MMA (K=64), A
   // takes 4 columns (128 rows / 32 lanes) and B takes BN/32
@@ -60,12 +68,13 @@ struct GemmCfg {
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
   static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_STAGES + 1;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024 + RQ_BYTES;
+  static_assert(SMEM_BYTES <= kMaxSmem, "shared memory budget");
   static constexpr int SF_WARPS = 4;               // scale staging, one per TMEM lane quadrant
   static constexpr int EPI_WARP0 = 2 + SF_WARPS;
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_COLS = BN / 2;          // accumulator columns drained by one epilogue warp
-  static constexpr int EPI_ROUND = 64;             // columns per drain round (register budget)
+  static constexpr int EPI_ROUND = RQ ? 32 : 64;   // columns per drain round (register budget)
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   // Instruction descriptor.  Block-scaled FP4: A/B type E2M1 (1) in bits 7-9
   // and 10-12, K-major, N>>3 in bits 17-22, scale type in bit 23 (UE4M3 0 for
@@ -116,12 +125,65 @@ __device__ __forceinline__ void requant_publish_amax(uint32_t am, uint32_t* out)
   if ((threadIdx.x & 31) == 0) atomicMax(out, am << 16);   // bf16 pattern -> fp32 bits: order kept
 }
 
+// Random half of a block's element i, read from the staging (row i of the
+// lane's block, the half chosen by the lane's column parity).
+struct StagedBits {
+  const uint2* s;   // the lane's first staged pair
+  uint32_t sh;
+  __device__ __forceinline__ uint32_t operator()(int i) const { return (s[i * 9].y >> sh) & 0xffffu; }
+};
+
+// NEXT-3, transposed: NVFP4 blocks of 16 consecutive rows m of one column n
+// (the operand D^T, contraction M) for 32 output columns of the warp's 32
+// rows m0..m0+31; `row` is this lane's row, `col` the first column.  The warp
+// swaps rows and columns through its shared-memory staging in halves of 16
+// columns: lane l then holds column l%16, rows 16*(l/16)..+15 -- one block,
+// with the random bits the column quantizer draws for element m*N + n.
+// Returns the largest magnitude as a bf16 bit pattern.
+template <int RND>
+__device__ __forceinline__ uint32_t requant32_t(const uint32_t (&r)[32], float alpha, int64_t row, int64_t m0,
+                                                int64_t col, const GemmParams& p, float g, float six_g, uint2* stg) {
+  const int lane = threadIdx.x & 31, cc = lane & 15, h = lane >> 4;
+  const uint32_t sh = 16u * (uint32_t)(cc & 1);
+  uint32_t am = 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (RND) sr_bits16(row * p.N + col + 16 * s, p.rq_seed, p.rq_stream_t, u);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(alpha, __uint_as_float(r[16 * s + 2 * k]))));
+      const uint32_t hi =
+          __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(alpha, __uint_as_float(r[16 * s + 2 * k + 1]))));
+      am = max(am, max(lo & 0x7fffu, hi & 0x7fffu));
+      stg[lane * 9 + k] = make_uint2(lo | (hi << 16), u[k]);
+    }
+    __syncwarp();
+    const uint2* mine = stg + 16 * h * 9 + (cc >> 1);
+    float v[16];
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t x = (mine[i * 9].x >> sh) & 0xffffu;
+      v[i] = __uint_as_float(x << 16);
+      mb = max(mb, x & 0x7fffu);
+    }
+    const BlockScale bs = nvfp4_block_scale(mb, g, six_g);
+    const int64_t n = col + 16 * s + cc, m = m0 + 16 * h;
+    *reinterpret_cast<uint2*>(p.rq_codes_t + n * (p.rq_ocp_t >> 1) + (m >> 1)) =
+        nvfp4_encode16<RND>(v, bs, StagedBits{mine, sh});
+    p.rq_scales_t[mma_scale_offset(n, m >> 4, p.rq_ocp_t)] = (uint8_t)bs.s;
+    __syncwarp();   // every lane has read this half before the next one is staged
+  }
+  return am;
+}
+
 // RQ: the epilogue also re-quantizes the product (snip_gemm_requant); a
 // separate instantiation, so the plain GEMM keeps its registers.
 template <int FMT, int BN, bool RQ = false>
 __global__ void __launch_bounds__(448, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
-  using C = GemmCfg<FMT, BN>;
+  using C = GemmCfg<FMT, BN, RQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -277,6 +339,8 @@ __global__ void __launch_bounds__(448, 1)
     const float alpha = p.ga ? __fmul_rn(*p.ga, *p.gb) : 1.0f;   // MXFP4 has no tensor scales
     const float rq_g = RQ ? *p.rq_g : 1.0f, rq_six_g = __fmul_rn(6.0f, rq_g);
     uint32_t rq_am = 0;
+    uint2* rq_stg = reinterpret_cast<uint2*>(smem + C::STAGES * C::STAGE_BYTES + 1024) +
+                    (warp - C::EPI_WARP0) * kRqStageWords;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
@@ -301,8 +365,12 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
           for (int c = 0; c < C::EPI_ROUND / 32; ++c) {
             const int64_t col = col0 + rd * C::EPI_ROUND + c * 32;
-            rq_am = max(rq_am, p.rq_rnd ? requant32<1>(r[c], alpha, row, col, p, rq_g, rq_six_g)
-                                        : requant32<0>(r[c], alpha, row, col, p, rq_g, rq_six_g));
+            if (p.rq_codes)
+              rq_am = max(rq_am, p.rq_rnd ? requant32<1>(r[c], alpha, row, col, p, rq_g, rq_six_g)
+                                          : requant32<0>(r[c], alpha, row, col, p, rq_g, rq_six_g));
+            if (p.rq_codes_t)
+              rq_am = max(rq_am, p.rq_rnd_t ? requant32_t<1>(r[c], alpha, row, row - lane, col, p, rq_g, rq_six_g, rq_stg)
+                                            : requant32_t<0>(r[c], alpha, row, row - lane, col, p, rq_g, rq_six_g, rq_stg));
           }
         }
         if (p.D && row < p.M) {
@@ -359,7 +427,7 @@ __global__ void __launch_bounds__(448, 1)
 // rows by the whole B tile); holding only its own 128 gives wrong products.
 // The library routes every GEMM with at least one full wave of 256 x 256
 // tiles here (both formats); smaller ones run on the one-CTA kernel.
-template <int FMT>
+template <int FMT, bool RQ = false>
 struct Gemm2Cfg {
   static constexpr int BM = 128, BN = 256, BNC = 128, KB = 128;
   static constexpr int A_BYTES = BM * KB, B_BYTES = BNC * KB;
@@ -367,7 +435,10 @@ struct Gemm2Cfg {
   static constexpr int SFA_BYTES = FMT ? CH * 512 : 0;
   static constexpr int SFB_BYTES = FMT ? 2 * CH * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int STAGES = FMT == 1 ? 5 : 6;
+  static constexpr int RQ_BYTES = RQ ? 8 * kRqStageWords * 8 : 0;
+  static constexpr int BASE_STAGES = FMT == 1 ? 5 : 6;
+  static constexpr int STAGES =
+      BASE_STAGES * STAGE_BYTES + 2048 + RQ_BYTES <= kMaxSmem ? BASE_STAGES : BASE_STAGES - 1;
   static constexpr int ACC_STAGES = FMT ? 1 : 2;
   static constexpr int SFA_COLS = 4 * CH;
   static constexpr int SFB_COLS_K = 8;                    // scale columns of B per chunk (256 rows)
@@ -377,8 +448,9 @@ struct Gemm2Cfg {
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
   static_assert(STAGE_BYTES % 1024 == 0, "1024-byte aligned stages");
   static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_STAGES + 1;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
-  static constexpr int SF_WARPS = 4, EPI_WARP0 = 6, EPI_WARPS = 8, EPI_COLS = BN / 2, EPI_ROUND = 64;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024 + RQ_BYTES;
+  static_assert(SMEM_BYTES <= kMaxSmem, "shared memory budget");
+  static constexpr int SF_WARPS = 4, EPI_WARP0 = 6, EPI_WARPS = 8, EPI_COLS = BN / 2, EPI_ROUND = RQ ? 32 : 64;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   static constexpr uint32_t IDESC =
       FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((FMT == 2 ? 1u : 0u) << 23) |
@@ -391,7 +463,7 @@ __global__ void __launch_bounds__(448, 1)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         GemmParams p) {
-  using C = Gemm2Cfg<FMT>;
+  using C = Gemm2Cfg<FMT, RQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -549,6 +621,8 @@ __global__ void __launch_bounds__(448, 1)
     const float alpha = p.ga ? __fmul_rn(*p.ga, *p.gb) : 1.0f;   // MXFP4 has no tensor scales
     const float rq_g = RQ ? *p.rq_g : 1.0f, rq_six_g = __fmul_rn(6.0f, rq_g);
     uint32_t rq_am = 0;
+    uint2* rq_stg = reinterpret_cast<uint2*>(smem + C::STAGES * C::STAGE_BYTES + 1024) +
+                    (warp - C::EPI_WARP0) * kRqStageWords;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
@@ -573,8 +647,12 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
           for (int c = 0; c < C::EPI_ROUND / 32; ++c) {
             const int64_t col = col0 + rd * C::EPI_ROUND + c * 32;
-            rq_am = max(rq_am, p.rq_rnd ? requant32<1>(r[c], alpha, row, col, p, rq_g, rq_six_g)
-                                        : requant32<0>(r[c], alpha, row, col, p, rq_g, rq_six_g));
+            if (p.rq_codes)
+              rq_am = max(rq_am, p.rq_rnd ? requant32<1>(r[c], alpha, row, col, p, rq_g, rq_six_g)
+                                          : requant32<0>(r[c], alpha, row, col, p, rq_g, rq_six_g));
+            if (p.rq_codes_t)
+              rq_am = max(rq_am, p.rq_rnd_t ? requant32_t<1>(r[c], alpha, row, row - lane, col, p, rq_g, rq_six_g, rq_stg)
+                                            : requant32_t<0>(r[c], alpha, row, row - lane, col, p, rq_g, rq_six_g, rq_stg));
           }
         }
         if (p.D && row < p.M) {
@@ -651,7 +729,7 @@ static bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int
 template <int FMT, int BN, bool RQ>
 static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
                                    GemmParams p, int num_sms, cudaStream_t st) {
-  using C = GemmCfg<FMT, BN>;
+  using C = GemmCfg<FMT, BN, RQ>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<FMT, BN, RQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -691,7 +769,7 @@ static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes, i
 template <int FMT, bool RQ>
 static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
                                     GemmParams p, int num_sms, cudaStream_t st) {
-  using C = Gemm2Cfg<FMT>;
+  using C = Gemm2Cfg<FMT, RQ>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT, RQ>,
@@ -752,7 +830,7 @@ cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, 
                         int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st) {
   const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
   const bool pair = pair_tiles >= num_sms / 2;
-  if (p.rq_codes) return launch_gemm_rq<true>(fmt, pair, a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  if (p.rq_codes || p.rq_codes_t) return launch_gemm_rq<true>(fmt, pair, a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
   return launch_gemm_rq<false>(fmt, pair, a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
 }
 

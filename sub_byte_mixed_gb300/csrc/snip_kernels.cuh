@@ -52,7 +52,7 @@ struct GemmParams {
   int num_m_tiles, num_n_tiles;
   int v8;                       // D rows allow 32-byte stores
   int a_e5m2;                   // FP8 only: A is E5M2 (B stays E4M3)
-  // NVFP4 re-quantization of the output for the next GEMM (null rq_codes: off)
+  // NVFP4 re-quantization of the output for the next GEMM (null rq_codes: no row blocks)
   uint8_t* rq_codes;            // MMA layout, rows padded to 256, N padded to rq_ocp
   uint8_t* rq_scales;
   const float* rq_g;            // tensor scale to quantize with (given, e.g. delayed)
@@ -60,6 +60,12 @@ struct GemmParams {
   int64_t rq_ocp;
   uint64_t rq_seed, rq_stream;
   int rq_rnd;
+  // column blocks of the same bf16 output: rows of its transpose (null rq_codes_t: off)
+  uint8_t* rq_codes_t;          // MMA layout, N padded to 256 rows, M padded to rq_ocp_t
+  uint8_t* rq_scales_t;
+  int64_t rq_ocp_t;
+  uint64_t rq_stream_t;
+  int rq_rnd_t;
   uint32_t* status;
   uint64_t timeout_ns;
 };

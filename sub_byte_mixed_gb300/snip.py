@@ -48,7 +48,8 @@ class SnipError(RuntimeError):
 class SnipRequant(ctypes.Structure):
     _fields_ = [("g_in", ctypes.c_void_p), ("rnd", ctypes.c_int), ("seed", ctypes.c_uint64),
                 ("stream_id", ctypes.c_uint64), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
-                ("amax_out", ctypes.c_void_p)]
+                ("amax_out", ctypes.c_void_p), ("rnd_t", ctypes.c_int), ("stream_id_t", ctypes.c_uint64),
+                ("codes_t", ctypes.c_void_p), ("scales_t", ctypes.c_void_p)]
 
 
 class SnipStats(ctypes.Structure):
@@ -526,25 +527,37 @@ def dw_noise(X, dY, dW_q, ws: Workspace | None = None):
     return out
 
 
-def gemm_requant(fmt, a, b, M, N, K, g_in, rnd=SR, seed=0, stream_id=0, want_d=True, ws: Workspace | None = None):
-    """D = A B^T (fp32, or None) plus D rounded to bf16 and quantized to NVFP4 row blocks with the
-    device tensor scale g_in (1-element float tensor) -> (D, QuantNVFP4 in the MMA layout, amax tensor)."""
+def gemm_requant(fmt, a, b, M, N, K, g_in, rnd=SR, seed=0, stream_id=0, want_d=True, rows=True, cols=False,
+                 rnd_t=SR, stream_id_t=0, ws: Workspace | None = None):
+    """D = A B^T (fp32, or None) plus D rounded to bf16 and quantized to NVFP4 with the device tensor
+    scale g_in (1-element float tensor): row blocks (the M x N operand; rnd, stream_id) and/or column
+    blocks (the N x M operand D^T; rnd_t, stream_id_t), both in the MMA layout
+    -> (D, rows QuantNVFP4 or None, amax tensor, columns QuantNVFP4 or None)."""
     torch = _torch()
     ws = ws or small_workspace()
     dev = a.codes.device
     D = torch.empty((M, N), dtype=torch.float32, device=dev) if want_d else None
-    cb, sb = snip_quantized_bytes(NVFP4, MMA, M, N)
-    codes = torch.empty(max(cb, 16), dtype=torch.uint8, device=dev)
-    scales = torch.empty(max(sb, 16), dtype=torch.uint8, device=dev)
+
+    def buffers(orows, ocols):
+        cb, sb = snip_quantized_bytes(NVFP4, MMA, orows, ocols)
+        return (torch.empty(max(cb, 16), dtype=torch.uint8, device=dev),
+                torch.empty(max(sb, 16), dtype=torch.uint8, device=dev), cb, sb)
+
+    r = buffers(M, N) if rows else None
+    c = buffers(N, M) if cols else None
     amax = torch.empty(1, dtype=torch.float32, device=dev)
-    rq = SnipRequant(g_in.data_ptr(), rnd, seed, stream_id, codes.data_ptr(), scales.data_ptr(), amax.data_ptr())
+    rq = SnipRequant(g_in.data_ptr(), rnd, seed, stream_id, r[0].data_ptr() if r else None,
+                     r[1].data_ptr() if r else None, amax.data_ptr(), rnd_t, stream_id_t,
+                     c[0].data_ptr() if c else None, c[1].data_ptr() if c else None)
     sa = a.scales.data_ptr() if fmt in (NVFP4, MXFP4) else None
     sb_ = b.scales.data_ptr() if fmt in (NVFP4, MXFP4) else None
     ga = (a.g if fmt == NVFP4 else a.s).data_ptr() if fmt != MXFP4 else None
     gb = (b.g if fmt == NVFP4 else b.s).data_ptr() if fmt != MXFP4 else None
     _call("snip_gemm_requant", fmt, a.codes.data_ptr(), sa, ga, b.codes.data_ptr(), sb_, gb, M, N, K,
           D.data_ptr() if D is not None else None, N, ctypes.byref(rq), ws.ptr, ws.nbytes, _stream())
-    return D, QuantNVFP4(codes[:cb], scales[:sb], g_in, M, N, MMA), amax
+    qr = QuantNVFP4(r[0][:r[2]], r[1][:r[3]], g_in, M, N, MMA) if r else None
+    qc = QuantNVFP4(c[0][:c[2]], c[1][:c[3]], g_in, N, M, MMA) if c else None
+    return D, qr, amax, qc
 
 
 def quant_stats(a, rnd=RTN, seed=0, stream_id=0, want_block_err=False, ws: Workspace | None = None, raw=None,

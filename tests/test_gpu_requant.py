@@ -40,7 +40,7 @@ def test_requant_product(snip, fmt, M, N, K, rnd):
     fname = "nvfp4" if fmt == 1 else "fp8"
     ref = oracle.gemm_tn(oracle.quantize(fname, A, 0, 1, 1, 2).dequant(), oracle.quantize(fname, B, 0, 1, 1, 3).dequant())
     g = torch.tensor([0.8 * float(np.abs(ref).max()) / 2688.0], dtype=torch.float32, device="cuda")
-    D, rq, amax = snip.gemm_requant(fmt, a, b, M, N, K, g, rnd=rnd, seed=7, stream_id=11)
+    D, rq, amax, _ = snip.gemm_requant(fmt, a, b, M, N, K, g, rnd=rnd, seed=7, stream_id=11)
     torch.cuda.synchronize()
     # 1. bit-exact against quantizing bf16(D) with the same scale, rounding and random bits
     Db = D.to(torch.bfloat16)
@@ -69,8 +69,8 @@ def test_requant_without_fp32_output(snip):
     a = snip.quantize_nvfp4(A.cuda(), layout=snip.MMA)
     b = snip.quantize_nvfp4(B.cuda(), layout=snip.MMA)
     g = torch.tensor([1e-3], dtype=torch.float32, device="cuda")
-    D, rq1, _ = snip.gemm_requant(snip.NVFP4, a, b, M, N, K, g, rnd=1, seed=3, stream_id=4)
-    none, rq2, _ = snip.gemm_requant(snip.NVFP4, a, b, M, N, K, g, rnd=1, seed=3, stream_id=4, want_d=False)
+    D, rq1, _, _ = snip.gemm_requant(snip.NVFP4, a, b, M, N, K, g, rnd=1, seed=3, stream_id=4)
+    none, rq2, _, _ = snip.gemm_requant(snip.NVFP4, a, b, M, N, K, g, rnd=1, seed=3, stream_id=4, want_d=False)
     torch.cuda.synchronize()
     assert none is None
     np.testing.assert_array_equal(rq1.codes.cpu().numpy(), rq2.codes.cpu().numpy())
@@ -81,3 +81,101 @@ def test_requant_without_fp32_output(snip):
     out = snip.gemm(snip.NVFP4, rq2, c, M, 128, N)
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
+
+
+# ---------------------------------------------------------------- column blocks (the transposed operand)
+
+def _operands(snip, fmt, M, N, K, seed):
+    A = inputs.normal_bf16((M, K), 1e-3, seed, 1)
+    B = inputs.normal_bf16((N, K), 0.02, seed, 2)
+    q = snip.quantize_nvfp4 if fmt == 1 else snip.quantize_fp8
+    a = q(A.cuda(), rnd=1, seed=1, stream_id=2, layout=snip.MMA)
+    b = q(B.cuda(), rnd=1, seed=1, stream_id=3, layout=snip.MMA)
+    fname = "nvfp4" if fmt == 1 else "fp8"
+    ref = oracle.gemm_tn(oracle.quantize(fname, A, 0, 1, 1, 2).dequant(), oracle.quantize(fname, B, 0, 1, 1, 3).dequant())
+    return a, b, ref
+
+
+# (192, 160) and (272, 400): one-CTA tiles, M not a multiple of 256 (272 also leaves 128 rows of the
+# 256-row padding uncovered); (2048, 2560): CTA-pair tiles
+@pytest.mark.parametrize("fmt", [1, 0])
+@pytest.mark.parametrize("M,N,K", [(192, 160, 256), (272, 400, 336), (2048, 2560, 512)])
+@pytest.mark.parametrize("rnd,rnd_t", [(0, 0), (1, 1), (0, 1)])
+def test_requant_both_orientations(snip, fmt, M, N, K, rnd, rnd_t):
+    a, b, ref = _operands(snip, fmt, M, N, K, 14)
+    g = torch.tensor([0.8 * float(np.abs(ref).max()) / 2688.0], dtype=torch.float32, device="cuda")
+    D, rq, amax, rq_t = snip.gemm_requant(fmt, a, b, M, N, K, g, rnd=rnd, seed=9, stream_id=21, cols=True,
+                                          rnd_t=rnd_t, stream_id_t=23)
+    torch.cuda.synchronize()
+    Db = D.to(torch.bfloat16)
+    # 1. bit-exact: each orientation equals the library quantizer on bf16(D), same scale, rounding, bits
+    ref_r = snip.quantize_nvfp4(Db, rnd=rnd, seed=9, stream_id=21, g_in=g, layout=snip.MMA)
+    ref_c = snip.quantize_nvfp4(Db, orient=snip.ALONG_ROWS, rnd=rnd_t, seed=9, stream_id=23, g_in=g, layout=snip.MMA)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(rq.codes.cpu().numpy(), ref_r.codes.cpu().numpy())
+    np.testing.assert_array_equal(rq.scales.cpu().numpy(), ref_r.scales.cpu().numpy())
+    assert rq_t.codes.numel() == ref_c.codes.numel() and rq_t.scales.numel() == ref_c.scales.numel()
+    np.testing.assert_array_equal(rq_t.codes.cpu().numpy(), ref_c.codes.cpu().numpy())
+    np.testing.assert_array_equal(rq_t.scales.cpu().numpy(), ref_c.scales.cpu().numpy())
+    assert float(amax.cpu()) == float(Db.float().abs().max())
+    # 2. the column blocks against the oracle's transposed quantization of its fp64 product in bf16
+    orc = oracle.quantize_nvfp4(torch.from_numpy(ref).to(torch.bfloat16), orient=1, rnd=rnd_t, seed=9, stream_id=23,
+                                g_in=float(g.cpu()))
+    _, codes = mma_codes_to_rowmajor(rq_t.codes, N, M, fmt_nvfp4=True)
+    _, scales = mma_scales_to_rowmajor(rq_t.scales, N, M)
+    assert np.mean(scales == orc.scales) > 0.999
+    assert np.mean(codes == orc.codes) > 0.999
+    mg, mo = _mag(codes), _mag(orc.codes)
+    assert np.all(np.abs(mg.astype(int) - mo.astype(int)) <= 1)
+
+
+def test_requant_columns_only_and_as_wgrad_operand(snip):
+    """Column blocks alone equal those written beside the row blocks, and feed the next GEMM (the
+    preceding layer's wgrad, contraction over the tokens M) exactly like the quantizer's output."""
+    M, N, K = 512, 256, 256
+    a, b, ref = _operands(snip, 1, M, N, K, 15)
+    g = torch.tensor([float(np.abs(ref).max()) / 2688.0], dtype=torch.float32, device="cuda")
+    _, _, _, both = snip.gemm_requant(snip.NVFP4, a, b, M, N, K, g, rnd=1, seed=5, stream_id=6, cols=True,
+                                      rnd_t=1, stream_id_t=7)
+    none, rows, amax, only = snip.gemm_requant(snip.NVFP4, a, b, M, N, K, g, seed=5, want_d=False, rows=False,
+                                               cols=True, rnd_t=1, stream_id_t=7)
+    torch.cuda.synchronize()
+    assert none is None and rows is None
+    np.testing.assert_array_equal(only.codes.cpu().numpy(), both.codes.cpu().numpy())
+    np.testing.assert_array_equal(only.scales.cpu().numpy(), both.scales.cpu().numpy())
+    # dW_prev = dY^T X: dY^T (N x M, blocks along M) times X^T quantized along M
+    X = inputs.normal_bf16((M, 384), 1.0, 15, 3).cuda()
+    xt = snip.quantize_nvfp4(X, orient=snip.ALONG_ROWS, rnd=1, seed=5, stream_id=8, layout=snip.MMA)
+    D = snip.gemm(snip.NVFP4, a, b, M, N, K)
+    torch.cuda.synchronize()
+    lib = snip.quantize_nvfp4(D.to(torch.bfloat16), orient=snip.ALONG_ROWS, rnd=1, seed=5, stream_id=7, g_in=g,
+                              layout=snip.MMA)
+    out_fused = snip.gemm(snip.NVFP4, only, xt, N, 384, M)
+    out_lib = snip.gemm(snip.NVFP4, lib, xt, N, 384, M)
+    torch.cuda.synchronize()
+    assert torch.equal(out_fused, out_lib)
+
+
+def test_requant_argument_errors(snip):
+    import ctypes
+    M, N, K = 200, 256, 256   # M not a multiple of 16: no column blocks
+    a, b, _ = _operands(snip, 1, 208, N, K, 16)
+    g = torch.tensor([1e-3], dtype=torch.float32, device="cuda")
+    buf = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    ws = snip.small_workspace()
+    L = snip.load()
+
+    def call(rq, m=M):
+        return L.snip_gemm_requant(snip.NVFP4, a.codes.data_ptr(), a.scales.data_ptr(), a.g.data_ptr(),
+                                   b.codes.data_ptr(), b.scales.data_ptr(), b.g.data_ptr(), m, N, K, None, N,
+                                   ctypes.byref(rq), ws.ptr, ws.nbytes, None)
+
+    p = buf.data_ptr()
+    assert call(snip.SnipRequant(g.data_ptr(), 0, 0, 0, None, None, None, 0, 0, p, p)) == snip.SNIP_ERR_SHAPE
+    assert call(snip.SnipRequant(g.data_ptr(), 0, 0, 0, None, None, None, 0, 0, None, None)) == \
+        snip.SNIP_ERR_INVALID_ARG
+    assert call(snip.SnipRequant(g.data_ptr(), 0, 0, 0, None, None, None, 0, 0, p, None), 208) == \
+        snip.SNIP_ERR_INVALID_ARG
+    assert call(snip.SnipRequant(g.data_ptr(), 0, 0, 0, None, None, None, 2, 0, p, p), 208) == \
+        snip.SNIP_ERR_INVALID_ARG
+    torch.cuda.synchronize()
