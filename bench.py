@@ -58,6 +58,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-overlap", action="store_true",
                     help="run every call on one stream (no quantization beside the GEMMs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--vs-cublaslt", action="store_true",
+                    help="instead of the step: the library's NVFP4 and FP8 GEMMs against cuBLASLt's on the "
+                         "block's shapes (builds cublaslt_gemm.cu), one JSON line")
     ap.add_argument("--profile-run", action="store_true",
                     help="exactly --warmup untimed steps, no clock settle, e2e or CPU baseline (for ncu)")
     ap.add_argument("--layers", default="", help="comma-separated subset of Q,K,V,O,Gate,Up,Down (profiling)")
@@ -802,8 +805,73 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+GEMM_SHAPES = [  # (M, N, K): the 7B block's Down fwd / dgrad / wgrad and Q fwd, the 70B block's Down fwd
+    ("llama7b Down fwd", 8192, 4096, 11008), ("llama7b Down dgrad", 8192, 11008, 4096),
+    ("llama7b Down wgrad", 4096, 11008, 8192), ("llama7b Q fwd", 8192, 4096, 4096),
+    ("llama70b Down fwd", 16384, 8192, 28672)]
+
+
+def vs_cublaslt(reps: int = 20):
+    """Both GEMMs timed the same way (best of back-to-back launches on one set of buffers, L2-warm,
+    CUDA events), on constant operands: fp32 output, NVFP4 with E4M3 block scales and FP8 E4M3."""
+    import torch
+    from sub_byte_mixed_gb300 import build, snip
+    build.build()
+    snip.load()
+    here = os.path.dirname(os.path.abspath(__file__))
+    exe = os.path.join(here, "sub_byte_mixed_gb300", "_build", "cublaslt_gemm")
+    os.makedirs(os.path.dirname(exe), exist_ok=True)
+    subprocess.check_call([build.nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-o", exe,
+                           os.path.join(here, "cublaslt_gemm.cu"), "-lcublasLt"])
+    rows = []
+    for name, M, N, K in GEMM_SHAPES:
+        for fmt, fname in ((snip.NVFP4, "nvfp4"), (snip.FP8, "fp8")):
+            ops = []
+            for r in (M, N):
+                cb, sb = snip.snip_quantized_bytes(fmt, snip.MMA, r, K)
+                codes = torch.full((cb,), 0x22 if fmt == snip.NVFP4 else 0x38, dtype=torch.uint8, device="cuda")
+                one = torch.ones(1, dtype=torch.float32, device="cuda")
+                if fmt == snip.NVFP4:
+                    scales = torch.full((sb,), 0x38, dtype=torch.uint8, device="cuda")
+                    ops.append(snip.QuantNVFP4(codes, scales, one, r, K, snip.MMA))
+                else:
+                    ops.append(snip.QuantFP8(codes, one, r, K, snip.MMA))
+            D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            ws = snip.small_workspace()
+            best = None
+            for _ in range(3):
+                snip.gemm(fmt, ops[0], ops[1], M, N, K, out=D, ws=ws)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(reps):
+                    snip.gemm(fmt, ops[0], ops[1], M, N, K, out=D, ws=ws)
+                e1.record()
+                torch.cuda.synchronize()
+                t = e0.elapsed_time(e1) / reps
+                best = t if best is None else min(best, t)
+            if ws.status() != snip.SNIP_OK:
+                raise RuntimeError("device status " + snip.status_string(ws.status()))
+            del ops, D
+            torch.cuda.empty_cache()
+            out = subprocess.run([exe, fname, str(M), str(N), str(K), str(reps)], capture_output=True, text=True)
+            lt = json.loads(out.stdout.strip().splitlines()[-1])
+            fl = 2.0 * M * N * K
+            ours = fl / (best * 1e-3) / 1e12
+            rows.append({"gemm": name, "fmt": fname, "M": M, "N": N, "K": K, "ours_ms": round(best, 5),
+                         "ours_tflops": round(ours, 1), "cublaslt_ms": lt.get("ms"),
+                         "cublaslt_tflops": lt.get("tflops"),
+                         "ratio": round(ours / lt["tflops"], 3) if "tflops" in lt else None})
+    print(json.dumps({"metric": "GEMM TFLOP/s, this library vs cuBLASLt (fp32 output)", "unit": "TFLOP/s",
+                      "timing": f"best of 3 x {reps} back-to-back launches, same buffers (L2-warm), CUDA events",
+                      "operands": "constant codes (1.0), unit scales", "rows": rows}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.vs_cublaslt:
+        vs_cublaslt()
+        return
     if args.cpu_sample_only:
         print(json.dumps(cpu_sample(args.cpu_sample_seconds)), flush=True)
         return
