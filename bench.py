@@ -208,7 +208,7 @@ def measured_peaks():
 
 
 def kernel_source_hash(kind: str) -> str:
-    files = {"gemm": ["gemm.cu", "snip_device.cuh", "snip_kernels.cuh"],
+    files = {"gemm": ["gemm.cu", "snip_device.cuh", "snip_kernels.cuh", "snip_quant.cuh"],
              "quant": ["quant.cu", "snip_device.cuh", "snip_kernels.cuh", "snip_quant.cuh"]}[kind]
     h = hashlib.sha256()
     for f in files:
