@@ -86,6 +86,11 @@ def lib():
         L.oracle_quantize_nvfp4.restype = i32
         L.oracle_dequant_nvfp4.argtypes = [c_u8p, c_u8p, ctypes.c_float, i64, i64, c_dp]
         L.oracle_dequant_nvfp4.restype = None
+        L.oracle_quantize_nvfp4_block.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp, i32,
+                                                  c_u8p, c_u8p, c_fp, ctypes.POINTER(ctypes.c_int64), i64]
+        L.oracle_quantize_nvfp4_block.restype = i32
+        L.oracle_dequant_nvfp4_block.argtypes = [c_u8p, c_u8p, ctypes.c_float, i32, i64, i64, c_dp]
+        L.oracle_dequant_nvfp4_block.restype = None
         L.oracle_e8m0_value.argtypes = [i32]; L.oracle_e8m0_value.restype = ctypes.c_double
         L.oracle_mxfp4_shared_exp.argtypes = [ctypes.c_float]; L.oracle_mxfp4_shared_exp.restype = i32
         c_i64p = ctypes.POINTER(ctypes.c_int64)
@@ -224,6 +229,21 @@ class NVFP4:
         return out
 
 
+class NVFP4Block:
+    """E2M1 codes with one E4M3 scale per `block` elements (B = 16 is NVFP4): codes
+    rows x cols/2 (low nibble = even column), scales rows x cols/block, tensor scale g."""
+
+    def __init__(self, codes, scales, g, rows, cols, block):
+        self.codes, self.scales, self.g = codes, scales, g
+        self.rows, self.cols, self.block = rows, cols, block
+
+    def dequant(self) -> np.ndarray:
+        out = np.empty((self.rows, self.cols), dtype=np.float64)
+        lib().oracle_dequant_nvfp4_block(_ptr(self.codes, ctypes.c_uint8), _ptr(self.scales, ctypes.c_uint8),
+                                         self.g, self.block, self.rows, self.cols, _ptr(out, ctypes.c_double))
+        return out
+
+
 class MXFP4:
     """An MXFP4 tensor of shape (rows, cols): codes rows x cols/2 (low nibble =
     even column), E8M0 scales rows x cols/32; no tensor scale."""
@@ -288,6 +308,33 @@ def quantize_nvfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id:
     if st != 0:
         raise ValueError(f"shape error: blocks of 16 need the blocked dim % 16 == 0 (got {OR}x{OC})")
     return NVFP4(codes, scales, g.value, OR, OC, berr)
+
+
+def quantize_nvfp4_block(x, block: int, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0,
+                         g_in: float | None = None, rows=None) -> NVFP4Block:
+    """E2M1 + E4M3 quantization with one scale per `block` (16, 32, 64, 128) elements
+    along the blocked dim; otherwise as quantize_nvfp4."""
+    b = _bits(x)
+    sel, psel, nsel = _selection(rows)
+    rows, cols = b.shape
+    OR, OC = (rows, cols) if orient == 0 else (cols, rows)
+    if sel is not None:
+        assert np.all((sel >= 0) & (sel < OR))
+        OR = nsel
+    if OC % block != 0:
+        raise ValueError(f"shape error: blocks of {block} need the blocked dim % {block} == 0 (got {OR}x{OC})")
+    codes = np.zeros((OR, OC // 2), dtype=np.uint8)
+    scales = np.zeros((OR, OC // block), dtype=np.uint8)
+    g = ctypes.c_float()
+    gin = ctypes.byref(ctypes.c_float(g_in)) if g_in is not None else None
+    st = lib().oracle_quantize_nvfp4_block(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
+                                           gin, block, _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                                           ctypes.byref(g), psel, nsel)
+    if st == 1:
+        raise NonFiniteInput("non-finite input")
+    if st != 0:
+        raise ValueError(f"bad block size {block} or shape {OR}x{OC}")
+    return NVFP4Block(codes, scales, g.value, OR, OC, block)
 
 
 def quantize_fp8(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0,
@@ -372,6 +419,8 @@ def quantize(fmt: str, x, orient=0, rnd=RTN, seed=0, stream_id=0, rows=None):
         return quantize_mxfp4(x, orient, rnd, seed, stream_id, rows=rows)
     if fmt == "nvfp4":
         return quantize_nvfp4(x, orient, rnd, seed, stream_id, rows=rows)
+    if fmt.startswith("nvfp4-b"):   # nvfp4-b32 / -b64 / -b128: longer scale blocks
+        return quantize_nvfp4_block(x, int(fmt[7:]), orient, rnd, seed, stream_id, rows=rows)
     if fmt == "fp8":
         return quantize_fp8(x, orient, rnd, seed, stream_id, rows=rows)
     raise ValueError(fmt)

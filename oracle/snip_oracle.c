@@ -377,6 +377,78 @@ void oracle_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales, float g,
 }
 
 /* ------------------------------------------------------------------------ */
+/* NVFP4 element and scale formats with longer blocks (the block-size axis   */
+/* of the FP4 study in "FP4 all the way", summary page, Outline): B = 16,    */
+/* 32, 64 or 128 E2M1 values share one E4M3 scale under the same tensor     */
+/* scale g.  B = 16 is NVFP4 itself.                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Quantize a bf16 rows x cols tensor with one E4M3 scale per `block`
+ * consecutive elements along the blocked dim (orient as for NVFP4; the
+ * blocked dim must be a multiple of block).  Every step is NVFP4's (R1, R2,
+ * R5, R6, R15) with the block maximum taken over `block` elements.
+ * Outputs: codes OR x OC/2 bytes as for NVFP4; scales OR x OC/block E4M3
+ * bytes (one per block, row-major); g_out; sel / n_sel as for NVFP4.
+ * Returns 0, 1 (non-finite input) or 2 (shape). */
+int oracle_quantize_nvfp4_block(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
+                                uint64_t seed, uint64_t stream_id, const float* g_in, int block,
+                                uint8_t* codes, uint8_t* scales, float* g_out,
+                                const int64_t* sel, int64_t n_sel) {
+    int64_t OR = orient == 0 ? rows : cols, OC = orient == 0 ? cols : rows;
+    if (block < 16 || block > 128 || (block & (block - 1)) != 0 || OC % block != 0) return 2;
+    float amax;
+    if (oracle_amax_bf16(x, rows * cols, &amax)) return 1;
+    float g = g_in ? *g_in : oracle_nvfp4_global_scale(amax);
+    *g_out = g;
+    int64_t nb = OC / block;
+    int64_t nout = sel ? n_sel : OR;
+    for (int64_t ii = 0; ii < nout; ++ii) {
+        int64_t i = sel ? sel[ii] : ii;
+        for (int64_t b = 0; b < nb; ++b) {
+            /* the block's largest magnitude over all of its elements */
+            float ab = 0.0f;
+            for (int k = 0; k < block; ++k) {
+                float v = fabsf(bf16_to_float(x[src_index(orient, rows, cols, i, b * block + k)]));
+                if (v > ab) ab = v;
+            }
+            float six_g = 6.0f * g;
+            int sb = oracle_e4m3_rtn(ab / six_g);
+            scales[ii * nb + b] = (uint8_t)sb;
+            float p = (float)oracle_e4m3_value(sb) * g;
+            for (int k = 0; k < block; ++k) {
+                uint64_t e = (uint64_t)src_index(orient, rows, cols, i, b * block + k);
+                float xv = bf16_to_float(x[e]);
+                int sign = signbit(xv) ? 8 : 0;
+                int mag = 0;
+                if (p != 0.0f && xv != 0.0f) {
+                    float inv = 1.0f / p;
+                    float y = fabsf(xv) * inv;
+                    mag = rnd == 0 ? oracle_e2m1_rtn(y) : oracle_e2m1_sr(y, oracle_sr_bits(seed, stream_id, e));
+                }
+                int code = sign | mag;
+                int64_t col = b * block + k;
+                uint8_t* byte = &codes[ii * (OC / 2) + col / 2];
+                if ((col & 1) == 0) *byte = (uint8_t)((*byte & 0xf0) | code);
+                else *byte = (uint8_t)((*byte & 0x0f) | (code << 4));
+            }
+        }
+    }
+    return 0;
+}
+
+/* Dequantize (OR x OC, one scale per `block` elements) into fp64. */
+void oracle_dequant_nvfp4_block(const uint8_t* codes, const uint8_t* scales, float g, int block,
+                                int64_t OR, int64_t OC, double* out) {
+    for (int64_t i = 0; i < OR; ++i)
+        for (int64_t k = 0; k < OC; ++k) {
+            uint8_t byte = codes[i * (OC / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            double s = oracle_e4m3_value(scales[i * (OC / block) + k / block]);
+            out[i * OC + k] = oracle_e2m1_value(code) * s * (double)g;
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* MXFP4 (OCP Microscaling Formats specification v1.0, the format the FP4    */
 /* study of "FP4 all the way" weighs against NVFP4 on block size and scale  */
 /* format): 32 E2M1 elements share one E8M0 scale, a power of two           */
