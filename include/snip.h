@@ -72,13 +72,21 @@ typedef enum {
  * the FP4 study weighs NVFP4 against).  FP8_E5M2: one fp32 tensor scale
  * s = amax / 57344, for gradients; as a GEMM format it means A in E5M2 and B
  * in E4M3.  FP8_E5M2_GRAD is a layer format only (plans): E5M2 for dY and
- * dY^T, E4M3 for X, W, W^T and X^T. */
+ * dY^T, E4M3 for X, W, W^T and X^T.  NVFP4_B32 / _B64 / _B128: NVFP4's
+ * elements, scales and tensor scale with 32, 64 or 128 values per E4M3
+ * scale (the block-size axis of the FP4 study, "FP4 all the way", Outline);
+ * they are stored in NVFP4's layouts with each scale repeated for every 16
+ * elements it covers, so they are NVFP4 operands to the GEMM, which gives
+ * exactly the longer blocks' product. */
 typedef enum {
     SNIP_FMT_FP8_E4M3 = 0,
     SNIP_FMT_NVFP4 = 1,
     SNIP_FMT_MXFP4 = 2,
     SNIP_FMT_FP8_E5M2 = 3,
-    SNIP_FMT_FP8_E5M2_GRAD = 4
+    SNIP_FMT_FP8_E5M2_GRAD = 4,
+    SNIP_FMT_NVFP4_B32 = 5,
+    SNIP_FMT_NVFP4_B64 = 6,
+    SNIP_FMT_NVFP4_B128 = 7
 } snip_format;
 typedef enum { SNIP_RTN = 0, SNIP_SR = 1 } snip_round;
 
@@ -231,6 +239,19 @@ snip_status snip_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, snip_
                                 snip_layout layout, uint8_t* codes, uint8_t* scales, float* g_out,
                                 float* block_sqerr, void* ws, size_t ws_bytes, void* stream);
 
+/* NVFP4 with `block` (16, 32, 64 or 128) elements per E4M3 scale: every step
+ * as snip_quantize_nvfp4 with the block maximum taken over `block` elements
+ * ("FP4 all the way", Outline: the block-size axis of the FP4 study).  The
+ * outputs use NVFP4's layouts (sizes from snip_quantized_bytes with
+ * SNIP_FMT_NVFP4), each scale written once per 16 elements it covers, so
+ * they feed snip_gemm as NVFP4 operands.  The blocked dim must be a multiple
+ * of `block` (SNIP_ERR_SHAPE); any other block is SNIP_ERR_INVALID_ARG.
+ * block = 16 is snip_quantize_nvfp4 (without block errors). */
+snip_status snip_quantize_nvfp4_block(const void* x, int64_t rows, int64_t cols, snip_orient orient,
+                                      snip_round rnd, uint64_t seed, uint64_t stream_id, const float* g_in,
+                                      int block, snip_layout layout, uint8_t* codes, uint8_t* scales,
+                                      float* g_out, void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- a4: FP8 */
 
 /* FP8 E4M3 quantization with one fp32 tensor scale s = amax / 448 (1 for an
@@ -349,8 +370,9 @@ snip_status snip_gemm_requant(snip_format fmt, const uint8_t* a_codes, const uin
 /* ---------------------------------------------------------------- plan */
 
 /* A per-layer precision plan (SNIP, Abstract: one format per layer).  formats
- * (host, n_layers entries) are snip_format values: FP8_E4M3, NVFP4, MXFP4 or
- * FP8_E5M2_GRAD (not FP8_E5M2, an operand format).  Every layer starts with
+ * (host, n_layers entries) are snip_format values: FP8_E4M3, NVFP4, MXFP4,
+ * FP8_E5M2_GRAD or NVFP4_B32/_B64/_B128 (not FP8_E5M2, an operand format; a
+ * longer-block layer needs T, K and N multiples of its block).  Every layer starts with
  * the rounding of "FP4 all the way": RTN for the forward quantizations (tags
  * X_FWD, W_FWD) and SR for the four backward ones.  *out is a host object
  * owned by the caller (snip_plan_destroy). */
@@ -401,7 +423,9 @@ snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_rou
 /* One pass that both quantizes x with blocks along cols (as snip_quantize_*
  * with the given layout, rounding and stream) and computes SNIP's statistics
  * of x under that same rounding and random bits (as snip_quant_stats): the
- * tensor is read once.  fmt selects the codes written (scales: NVFP4 only);
+ * tensor is read once (MXFP4, E5M2 and the longer NVFP4 blocks: the
+ * statistics run in a second pass over it).  fmt selects the codes written
+ * (scales: the FP4 formats);
  * scales_in (device, nullable) = {amax, g, s} from snip_tensor_scales (NULL:
  * computed first); raw_out device SNIP_STATS_NVALS doubles.  Errors as for
  * snip_quantize_nvfp4 / snip_quant_stats. */

@@ -69,15 +69,27 @@ inline snip_status cuda_status(cudaError_t e) {
 
 // Padded dims of the MMA operand layout.
 inline int64_t mma_rows(int64_t r) { return round_up(r, 256); }
-inline bool is_fp4(int snip_fmt) { return snip_fmt == SNIP_FMT_NVFP4 || snip_fmt == SNIP_FMT_MXFP4; }
+// NVFP4 and its longer-block variants (same layouts and GEMM; one scale per
+// 16, 32, 64 or 128 elements)
+inline bool is_nvfp4(int snip_fmt) {
+  return snip_fmt == SNIP_FMT_NVFP4 || snip_fmt == SNIP_FMT_NVFP4_B32 || snip_fmt == SNIP_FMT_NVFP4_B64 ||
+         snip_fmt == SNIP_FMT_NVFP4_B128;
+}
+inline bool is_fp4(int snip_fmt) { return is_nvfp4(snip_fmt) || snip_fmt == SNIP_FMT_MXFP4; }
+// 16-element blocks sharing one scale
+inline int nvfp4_group(int snip_fmt) {
+  return snip_fmt == SNIP_FMT_NVFP4_B32 ? 2 : snip_fmt == SNIP_FMT_NVFP4_B64 ? 4 : snip_fmt == SNIP_FMT_NVFP4_B128 ? 8 : 1;
+}
+// operand formats (quantizer outputs, GEMM inputs); FP8_E5M2_GRAD is a layer format only
+inline bool valid_operand_fmt(int f) { return f >= 0 && f <= 7 && f != SNIP_FMT_FP8_E5M2_GRAD; }
 inline int64_t mma_cols(int snip_fmt, int64_t c) { return round_up(c, is_fp4(snip_fmt) ? 256 : 128); }
 // quantizer kernel format ids: 0 FP8 E4M3, 1 NVFP4, 2 MXFP4, 3 FP8 E5M2
 inline int kernel_fmt(int snip_fmt) {
-  return snip_fmt == SNIP_FMT_NVFP4 ? 1 : snip_fmt == SNIP_FMT_MXFP4 ? 2 : snip_fmt == SNIP_FMT_FP8_E5M2 ? 3 : 0;
+  return is_nvfp4(snip_fmt) ? 1 : snip_fmt == SNIP_FMT_MXFP4 ? 2 : snip_fmt == SNIP_FMT_FP8_E5M2 ? 3 : 0;
 }
 // GEMM kernel format ids: 0 FP8 (A E4M3 or E5M2), 1 NVFP4, 2 MXFP4
 inline int gemm_kernel_fmt(int snip_fmt) {
-  return snip_fmt == SNIP_FMT_NVFP4 ? 1 : snip_fmt == SNIP_FMT_MXFP4 ? 2 : 0;
+  return is_nvfp4(snip_fmt) ? 1 : snip_fmt == SNIP_FMT_MXFP4 ? 2 : 0;
 }
 // Which float of a tensor-scale slot {amax, g, s, s5} a quantization reads:
 // NVFP4 g (MXFP4 only checks it for NaN), FP8 s, E5M2 the amax (the kernel
@@ -94,8 +106,9 @@ inline const float* gemm_scale(const float* slot, int snip_fmt) {
 // dY and dY^T in E5M2 and everything else in E4M3.
 inline int forward_fmt(int layer_fmt) { return layer_fmt == SNIP_FMT_FP8_E5M2_GRAD ? SNIP_FMT_FP8_E4M3 : layer_fmt; }
 inline int gradient_fmt(int layer_fmt) { return layer_fmt == SNIP_FMT_FP8_E5M2_GRAD ? SNIP_FMT_FP8_E5M2 : layer_fmt; }
-// elements per block along the blocked dim
-inline int64_t block_elems(int snip_fmt) { return snip_fmt == SNIP_FMT_MXFP4 ? 32 : 16; }
+// elements per block along the blocked dim, and per stored scale byte
+inline int64_t block_elems(int snip_fmt) { return snip_fmt == SNIP_FMT_MXFP4 ? 32 : 16 * nvfp4_group(snip_fmt); }
+inline int64_t scale_elems(int snip_fmt) { return snip_fmt == SNIP_FMT_MXFP4 ? 32 : 16; }
 
 struct OperandBytes { size_t codes, scales; };
 OperandBytes operand_bytes(int fmt, int layout, int64_t orows, int64_t ocols) {
@@ -104,7 +117,7 @@ OperandBytes operand_bytes(int fmt, int layout, int64_t orows, int64_t ocols) {
     r = mma_rows(orows);
     c = mma_cols(fmt, ocols);
   }
-  if (is_fp4(fmt)) return {(size_t)(r * c / 2), (size_t)(r * c / block_elems(fmt))};
+  if (is_fp4(fmt)) return {(size_t)(r * c / 2), (size_t)(r * c / scale_elems(fmt))};
   return {(size_t)(r * c), 0};
 }
 
@@ -152,6 +165,7 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   p.scales = scales;
   p.g_out = g_out;
   p.block_err = block_err;
+  p.group = nvfp4_group(fmt);
   if (raw_out) {   // statistics fused into this (row-block) quantization
     p.scales3 = scales3;
     p.partials = ws_at<double>(ws, kOffStatsPartials);
@@ -160,8 +174,9 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   }
   // an empty output still publishes its tensor scale: the one-CTA row kernel does that
   if (p.orp == 0 || p.ocp == 0) orient = SNIP_BLOCKS_ALONG_COLS;
-  if ((fmt == SNIP_FMT_MXFP4 || fmt == SNIP_FMT_FP8_E5M2) && raw_out) {
-    // MXFP4 / E5M2 codes, then the statistics in their own pass (same rounding and random bits)
+  if ((fmt == SNIP_FMT_MXFP4 || fmt == SNIP_FMT_FP8_E5M2 || p.group > 1) && raw_out) {
+    // MXFP4 / E5M2 / longer-block NVFP4 codes, then the statistics in their own pass (same rounding
+    // and random bits)
     p.scales3 = nullptr;
     p.raw_out = nullptr;
     cudaError_t e = launch_quant(kernel_fmt(fmt), p, orient, layout, rnd, false, num_sms, st);
@@ -346,7 +361,7 @@ snip_status snip_tensor_scales_multi(int count, const void* const* xs, const int
 
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
                                  size_t* codes_bytes, size_t* scales_bytes) {
-  if (!valid_enum(fmt, 4) || !valid_enum(layout, 2) || out_rows < 0 || out_cols < 0) return SNIP_ERR_INVALID_ARG;
+  if (!valid_operand_fmt(fmt) || !valid_enum(layout, 2) || out_rows < 0 || out_cols < 0) return SNIP_ERR_INVALID_ARG;
   OperandBytes b = operand_bytes(fmt, layout, out_rows, out_cols);
   if (codes_bytes) *codes_bytes = b.codes;
   if (scales_bytes) *scales_bytes = b.scales;
@@ -379,6 +394,22 @@ snip_status snip_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, snip_
   if (s != SNIP_OK) return s;
   return run_quantize_api(SNIP_FMT_NVFP4, x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales,
                           g_out, block_sqerr, ws, sms, static_cast<cudaStream_t>(stream));
+}
+
+snip_status snip_quantize_nvfp4_block(const void* x, int64_t rows, int64_t cols, snip_orient orient, snip_round rnd,
+                                      uint64_t seed, uint64_t stream_id, const float* g_in, int block,
+                                      snip_layout layout, uint8_t* codes, uint8_t* scales, float* g_out, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  const int fmt = block == 16 ? SNIP_FMT_NVFP4 : block == 32 ? SNIP_FMT_NVFP4_B32 : block == 64 ? SNIP_FMT_NVFP4_B64
+                  : block == 128 ? SNIP_FMT_NVFP4_B128 : -1;
+  if (fmt < 0) return SNIP_ERR_INVALID_ARG;
+  s = check_quantize_args(fmt, x, rows, cols, orient, rnd, layout, codes, scales, g_out, ws, ws_bytes);
+  if (s != SNIP_OK) return s;
+  return run_quantize_api(fmt, x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
+                          nullptr, ws, sms, static_cast<cudaStream_t>(stream));
 }
 
 snip_status snip_quantize_fp8(const void* x, int64_t rows, int64_t cols, snip_orient orient, snip_round rnd,
@@ -425,7 +456,7 @@ snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
-  if (!valid_enum(fmt, 4) || M < 0 || N < 0 || K < 0 || ldd < N) return SNIP_ERR_INVALID_ARG;
+  if (!valid_operand_fmt(fmt) || M < 0 || N < 0 || K < 0 || ldd < N) return SNIP_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return SNIP_OK;
   if (!a_codes || !b_codes || !D) return SNIP_ERR_INVALID_ARG;
   if (fmt != SNIP_FMT_MXFP4 && (!ga || !gb)) return SNIP_ERR_INVALID_ARG;
@@ -450,7 +481,7 @@ snip_status snip_gemm_requant(snip_format fmt, const uint8_t* a_codes, const uin
   if (!rq || !rq->g_in || (!rq->codes && !rq->codes_t) || (rq->codes && !rq->scales) ||
       (rq->codes_t && !rq->scales_t) || !valid_enum(rq->rnd, 2) || !valid_enum(rq->rnd_t, 2))
     return SNIP_ERR_INVALID_ARG;
-  if (!valid_enum(fmt, 4) || M < 0 || N < 0 || K < 0 || (D && ldd < N)) return SNIP_ERR_INVALID_ARG;
+  if (!valid_operand_fmt(fmt) || M < 0 || N < 0 || K < 0 || (D && ldd < N)) return SNIP_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return SNIP_OK;
   if (!a_codes || !b_codes) return SNIP_ERR_INVALID_ARG;
   if (fmt != SNIP_FMT_MXFP4 && (!ga || !gb)) return SNIP_ERR_INVALID_ARG;
@@ -471,7 +502,7 @@ snip_status snip_gemm_requant(snip_format fmt, const uint8_t* a_codes, const uin
 snip_status snip_plan_create(int n_layers, const int* formats, uint64_t seed, snip_plan** out) {
   if (n_layers <= 0 || !formats || !out) return SNIP_ERR_INVALID_ARG;
   for (int i = 0; i < n_layers; ++i)
-    if (!valid_enum(formats[i], 5) || formats[i] == SNIP_FMT_FP8_E5M2) return SNIP_ERR_INVALID_ARG;
+    if (!valid_enum(formats[i], 8) || formats[i] == SNIP_FMT_FP8_E5M2) return SNIP_ERR_INVALID_ARG;
   snip_plan* p = new (std::nothrow) snip_plan;
   if (!p) return SNIP_ERR_INVALID_ARG;
   p->fmt.assign(formats, formats + n_layers);
@@ -676,7 +707,7 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
-  if (!valid_enum(fmt, 4) || !raw_out) return SNIP_ERR_INVALID_ARG;
+  if (!valid_operand_fmt(fmt) || !raw_out) return SNIP_ERR_INVALID_ARG;
   float g_dummy;   // validation only: g_out is not written by this entry point
   s = check_quantize_args(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, layout, codes,
                           is_fp4(fmt) ? scales : nullptr, &g_dummy, ws, ws_bytes);

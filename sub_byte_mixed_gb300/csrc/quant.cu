@@ -330,7 +330,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   for (uint32_t seg = seg0; seg < total; seg += wstride, r += wq, sr += wr) {
     if (sr >= spr) { sr -= spr; ++r; }
     const uint32_t kb = sr * 32 + lane;
-    if (FMT != 2 && kb >= bpr) continue;   // MXFP4 lanes leave after the pair shuffle
+    // MXFP4 lanes, and NVFP4 lanes of longer blocks, leave after the shuffles that share block maxima
+    if (FMT != 2 && kb >= bpr && !(FMT == 1 && !STATS && p.group > 1)) continue;
     const bool real = r < p.out_rows && (int64_t)kb * 16 < p.out_cols;
     uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
     const int64_t e0 = (int64_t)r * p.cols + (int64_t)kb * 16;
@@ -350,7 +351,15 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
       if (kb >= bpr) continue;
       bs = mxfp4_block_scale(m);
     }
-    if (FMT == 1 || STATS) bs = nvfp4_block_scale(amax16_bits(a, b), g4, six_g);
+    if (FMT == 1 && !STATS && p.group > 1) {
+      // one scale for p.group consecutive 16-element blocks: lanes 2^k apart share their maxima
+      uint32_t m = amax16_bits(a, b);
+      for (int o = 1; o < p.group; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (kb >= bpr) continue;
+      bs = nvfp4_block_scale(m, g4, six_g);
+    } else if (FMT == 1 || STATS) {
+      bs = nvfp4_block_scale(amax16_bits(a, b), g4, six_g);
+    }
     uint4 c = make_uint4(0u, 0u, 0u, 0u);   // FP8: 16 codes; FP4: .x, .y
     if (STATS) {
       // the codes come out of the statistics' own conversions
@@ -424,7 +433,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
   __shared__ __align__(16) uint32_t rs[RND ? kTR : 1][RND ? kXW : 4];
   __shared__ uint32_t oc[kTC][OW];
   __shared__ uint8_t os[FP4 ? kTC : 1][8];
-  __shared__ uint32_t amx[FMT == 2 ? 8 : 1][FMT == 2 ? 32 : 1][2];
+  __shared__ uint32_t amx[FP4 ? 8 : 1][FP4 ? 32 : 1][2];
   __shared__ float oe[ERR ? kTC : 1][8];
   // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
   const float g = FMT == 3 ? e5m2_tensor_scale(*p.scale) : *p.scale;
@@ -483,6 +492,16 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
         os[2 * cp + 1][b >> 1] = (uint8_t)s1.s;
       }
     } else if (FMT == 1) {
+      if (p.group > 1) {   // longer blocks: the maxima of the tile's p.group-block groups (uniform branch)
+        amx[b][cp][0] = m0;
+        amx[b][cp][1] = m1;
+        __syncthreads();
+        const int b0 = b & ~(p.group - 1);
+        for (int j = 0; j < p.group; ++j) {
+          m0 = max(m0, amx[b0 + j][cp][0]);
+          m1 = max(m1, amx[b0 + j][cp][1]);
+        }
+      }
       const BlockScale s0 = nvfp4_block_scale(m0, g, six_g), s1 = nvfp4_block_scale(m1, g, six_g);
       const uint2 e0 = nvfp4_encode16<RND>(v0, s0, u0), e1 = nvfp4_encode16<RND>(v1, s1, u1);
       oc[2 * cp][2 * b] = e0.x; oc[2 * cp][2 * b + 1] = e0.y;

@@ -23,6 +23,8 @@ SIGMA_X, SIGMA_W, SIGMA_DY = 1.0, 0.02, 1e-3
 
 LAYER_NAMES = ("Q", "K", "V", "O", "Gate", "Up", "Down")
 FMT_FP8, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2   # per-layer format codes of a plan
+FMT_NVFP4_B32, FMT_NVFP4_B64, FMT_NVFP4_B128 = 5, 6, 7   # NVFP4 with 32 / 64 / 128 elements per scale
+FP4_FORMATS = (FMT_NVFP4, FMT_MXFP4, FMT_NVFP4_B32, FMT_NVFP4_B64, FMT_NVFP4_B128)
 
 
 def _gen(seed: int, tensor_id: int, device) -> torch.Generator:
@@ -85,7 +87,7 @@ class BlockConfig:
 
     def fp4_flop_fraction(self, plan) -> float:
         tot = sum(l.K * l.N for l in self.linears)
-        return sum(l.K * l.N for l, f in zip(self.linears, plan) if f in (FMT_NVFP4, FMT_MXFP4)) / tot
+        return sum(l.K * l.N for l, f in zip(self.linears, plan) if f in FP4_FORMATS) / tot
 
 
 # TinyLlama-1B: hidden 2048, intermediate 5632, 32 heads / 4 KV heads (K,V out 256), 2 x 2048 tokens

@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsnip.so")
 SNIP_OK, SNIP_ERR_INVALID_ARG, SNIP_ERR_SHAPE, SNIP_ERR_ALIGN, SNIP_ERR_NONFINITE, SNIP_ERR_TIMEOUT, \
     SNIP_ERR_CUDA, SNIP_ERR_UNSUPPORTED_DEVICE, SNIP_ERR_WORKSPACE = range(9)
 FP8, NVFP4, MXFP4, FP8_E5M2, FP8_E5M2_GRAD = 0, 1, 2, 3, 4
+NVFP4_B32, NVFP4_B64, NVFP4_B128 = 5, 6, 7     # NVFP4 with 32 / 64 / 128 elements per scale
+NVFP4_BLOCK = {NVFP4: 16, NVFP4_B32: 32, NVFP4_B64: 64, NVFP4_B128: 128}
 RTN, SR = 0, 1
 ALONG_COLS, ALONG_ROWS = 0, 1
 ROWMAJOR, MMA = 0, 1
@@ -31,7 +33,8 @@ EXPORTS = (
     "snip_status_string", "snip_version", "snip_device_check", "snip_workspace_init", "snip_workspace_status",
     "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_tensor_scales_multi",
     "snip_tensor_scales_noalloc",
-    "snip_quantize_nvfp4", "snip_quantize_fp8", "snip_quantize_mxfp4", "snip_quantize_e5m2",
+    "snip_quantize_nvfp4", "snip_quantize_nvfp4_block", "snip_quantize_fp8", "snip_quantize_mxfp4",
+    "snip_quantize_e5m2",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
     "snip_quant_stats", "snip_quantize_stats", "snip_stats_finalize", "snip_plan_costs", "snip_plan_select",
@@ -83,6 +86,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_tensor_scales_noalloc": (i32, [vp, i64, vp, vp]),
         "snip_tensor_scales_multi": (i32, [i32, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_nvfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
+        "snip_quantize_nvfp4_block": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, i32, vp, vp, vp, vp, sz,
+                                            vp]),
         "snip_quantize_fp8": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, sz, vp]),
         "snip_quantize_mxfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, i32, vp, vp, vp, sz, vp]),
         "snip_quantize_e5m2": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, sz, vp]),
@@ -164,6 +169,12 @@ def snip_quantize_nvfp4(x, rows, cols, orient, rnd, seed, stream_id, g_in, layou
                         block_sqerr, ws, ws_bytes, stream):
     _call("snip_quantize_nvfp4", x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
           block_sqerr, ws, ws_bytes, stream)
+
+
+def snip_quantize_nvfp4_block(x, rows, cols, orient, rnd, seed, stream_id, g_in, block, layout, codes, scales,
+                              g_out, ws, ws_bytes, stream):
+    _call("snip_quantize_nvfp4_block", x, rows, cols, orient, rnd, seed, stream_id, g_in, block, layout, codes,
+          scales, g_out, ws, ws_bytes, stream)
 
 
 def snip_quantize_mxfp4(x, rows, cols, orient, rnd, seed, stream_id, layout, codes, scales, ws, ws_bytes, stream):
@@ -410,6 +421,23 @@ def quantize_nvfp4(x, orient=ALONG_COLS, rnd=RTN, seed=0, stream_id=0, g_in=None
     return QuantNVFP4(codes[:cb], scales[:sb], g, orows, ocols, layout, berr)
 
 
+def quantize_nvfp4_block(x, block, orient=ALONG_COLS, rnd=RTN, seed=0, stream_id=0, g_in=None, layout=ROWMAJOR,
+                         ws: Workspace | None = None) -> QuantNVFP4:
+    """NVFP4 with `block` (16, 32, 64, 128) elements per E4M3 scale, in NVFP4's layouts (each scale
+    repeated for every 16 elements it covers): an NVFP4 operand for gemm()."""
+    torch = _torch()
+    ws = ws or small_workspace()
+    rows, cols = x.shape
+    orows, ocols = (rows, cols) if orient == ALONG_COLS else (cols, rows)
+    cb, sb = snip_quantized_bytes(NVFP4, layout, orows, ocols)
+    codes = torch.empty(max(cb, 16), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(max(sb, 16), dtype=torch.uint8, device=x.device)
+    g = torch.empty(1, dtype=torch.float32, device=x.device)
+    snip_quantize_nvfp4_block(x.data_ptr(), rows, cols, orient, rnd, seed, stream_id, _ptr(g_in), block, layout,
+                              codes.data_ptr(), scales.data_ptr(), g.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return QuantNVFP4(codes[:cb], scales[:sb], g, orows, ocols, layout)
+
+
 def quantize_fp8(x, orient=ALONG_COLS, rnd=RTN, seed=0, stream_id=0, s_in=None, layout=ROWMAJOR,
                  ws: Workspace | None = None) -> QuantFP8:
     torch = _torch()
@@ -458,7 +486,7 @@ def gemm(fmt, a, b, M, N, K, out=None, ws: Workspace | None = None):
     torch = _torch()
     ws = ws or small_workspace()
     D = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=a.codes.device)
-    if fmt == NVFP4:
+    if fmt in NVFP4_BLOCK:   # NVFP4 and its longer-block variants: the same operands and GEMM
         snip_gemm(NVFP4, a.codes.data_ptr(), a.scales.data_ptr(), a.g.data_ptr(), b.codes.data_ptr(),
                   b.scales.data_ptr(), b.g.data_ptr(), M, N, K, D.data_ptr(), D.stride(0), ws.ptr, ws.nbytes,
                   _stream())

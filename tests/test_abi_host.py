@@ -50,8 +50,13 @@ def test_quantized_bytes(snip):
     # MXFP4: NVFP4's codes, one E8M0 byte per 32 elements
     assert snip.snip_quantized_bytes(snip.MXFP4, snip.ROWMAJOR, 64, 128) == (64 * 64, 64 * 4)
     assert snip.snip_quantized_bytes(snip.MXFP4, snip.MMA, 64, 288) == (256 * 256, 256 * 16)
-    with pytest.raises(snip.SnipError):
-        snip.snip_quantized_bytes(5, 0, 1, 1)
+    # longer NVFP4 blocks use NVFP4's layouts (one scale byte per 16 elements)
+    for f in (snip.NVFP4_B32, snip.NVFP4_B64, snip.NVFP4_B128):
+        for layout, r, c in ((snip.ROWMAJOR, 64, 256), (snip.MMA, 300, 384)):
+            assert snip.snip_quantized_bytes(f, layout, r, c) == snip.snip_quantized_bytes(snip.NVFP4, layout, r, c)
+    for bad in (snip.FP8_E5M2_GRAD, 8, -1):   # a layer-only format, then no format
+        with pytest.raises(snip.SnipError):
+            snip.snip_quantized_bytes(bad, 0, 1, 1)
 
 
 def test_plan_and_workspace_sizes(snip):
