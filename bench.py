@@ -52,7 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="llama-7b-block")
-    ap.add_argument("--plan", default="mix", choices=["mix", "nvfp4", "fp8", "mxfp4", "snip"])
+    ap.add_argument("--plan", default="mix",
+                    choices=["mix", "nvfp4", "fp8", "mxfp4", "nvfp4-b32", "nvfp4-b64", "nvfp4-b128", "snip"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
@@ -71,6 +72,11 @@ def parse_args(argv=None):
 
 # ----------------------------------------------------------------------------- workload description
 
+# plan format names <-> the library's format codes (the same as inputs.FMT_*)
+FORMAT_OF_NAME = {"fp8": 0, "nvfp4": 1, "mxfp4": 2, "nvfp4-b32": 5, "nvfp4-b64": 6, "nvfp4-b128": 7}
+NAME_OF_FORMAT = {v: k for k, v in FORMAT_OF_NAME.items()}
+
+
 def workload(args):
     from sub_byte_mixed_gb300 import inputs
     cfg = inputs.BLOCKS[args.config]
@@ -78,7 +84,7 @@ def workload(args):
         # "snip" starts from the seeded plan; run_ours replaces it with SNIP's selection
         plan = inputs.seeded_plan(cfg, cfg.fp4_target, seed=0)
     else:
-        plan = inputs.all_plan({"nvfp4": inputs.FMT_NVFP4, "fp8": inputs.FMT_FP8, "mxfp4": inputs.FMT_MXFP4}[args.plan])
+        plan = inputs.all_plan(FORMAT_OF_NAME[args.plan])
     return cfg, plan
 
 
@@ -87,8 +93,7 @@ def config_json(cfg, plan, args):
     return {
         "workload": f"{cfg.name}: T={cfg.T} hidden={cfg.hidden} inter={cfg.inter} kv_out={cfg.kv_out}; "
                     f"7 linears fwd+dgrad+wgrad+stats",
-        "plan": {n: {inputs.FMT_NVFP4: "nvfp4", inputs.FMT_FP8: "fp8", inputs.FMT_MXFP4: "mxfp4"}[f]
-                 for n, f in zip(inputs.LAYER_NAMES, plan)},
+        "plan": {n: NAME_OF_FORMAT[f] for n, f in zip(inputs.LAYER_NAMES, plan)},
         "fp4_flop_fraction": round(cfg.fp4_flop_fraction(plan), 4),
         "flop_per_step": cfg.flops_fwd_bwd(),
         "l2": "inputs larger than L2 (no flush)",
@@ -294,6 +299,7 @@ class Step:
         calls = []   # (fn, args, category, units, stream kind 'q'/'g', linear, GEMM index or -1)
         self.gemm_ws = snip.Workspace(snip.WS_HEADER_BYTES, device) if overlap else self.ws
         self._keep = []   # ctypes arrays referenced by the calls
+        extra_launches = 0
         for j, (l, f) in enumerate(zip(cfg.linears, plan)):
             if layers and l.name not in layers:
                 continue
@@ -304,9 +310,10 @@ class Step:
             scp = {l.x_id: self.sc[j, 0].data_ptr(), "W": self.sc[j, 1].data_ptr(), "dY": self.sc[j, 2].data_ptr()}
             sid = 8 * j
             rnd = [0, 0, 1, 1, 1, 1]
-            fname = {snip.NVFP4: "nvfp4", snip.FP8: "fp8", snip.MXFP4: "mxfp4"}[f]
+            block = snip.NVFP4_BLOCK.get(f, 0)      # NVFP4 and its longer blocks: NVFP4's kernels
+            fname = "nvfp4" if block else {snip.FP8: "fp8", snip.MXFP4: "mxfp4"}[f]
             qcat, gcat = "quant_" + fname, "gemm_" + fname
-            bpe = {snip.NVFP4: NVFP4_BYTES_PER_ELEM, snip.FP8: FP8_BYTES_PER_ELEM, snip.MXFP4: MXFP4_BYTES_PER_ELEM}[f]
+            bpe = NVFP4_BYTES_PER_ELEM if block else {snip.FP8: FP8_BYTES_PER_ELEM, snip.MXFP4: MXFP4_BYTES_PER_ELEM}[f]
             fo = 8 if f == snip.FP8 else 4            # byte offset of s (FP8) or g (NVFP4; MXFP4: unused) in a slot
             # the three tensors' scales in one launch
             names = (l.x_id, "W", "dY")
@@ -327,6 +334,12 @@ class Step:
                             self.codes[r].data_ptr(), self.scales[r].data_ptr() if f != snip.FP8 else None,
                             self.raw[j, k].data_ptr(), ws, wsb, stream)
                     calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", j, -1))
+                    if f == snip.MXFP4 or block > 16:
+                        extra_launches += 1   # these formats' statistics run in a second kernel
+                elif block > 16:
+                    args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, block, snip.MMA,
+                            self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, ws, wsb, stream)
+                    calls.append((L.snip_quantize_nvfp4_block, args, qcat, bpe * t.numel(), "q", j, -1))
                 elif f == snip.NVFP4:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, None, ws, wsb, stream)
@@ -354,8 +367,9 @@ class Step:
         self.calls = calls
         # the same calls with every launch on the quantization stream (kernels one after another)
         self.serial_args = [a if k == "q" else a[:-1] + (stream,) for (_, a, _, _, k, _, _) in calls]
-        # one kernel per call (the scales are computed once per tensor and passed in)
-        self.launches_per_step = len(calls)
+        # one kernel per call (the scales are computed once per tensor and passed in), plus the
+        # statistics kernels of the formats whose statistics are not fused
+        self.launches_per_step = len(calls) + extra_launches
 
     def run(self, events=None, serial=False):
         """One step.  With overlap, a GEMM waits for its two operands' quantizations, and the
