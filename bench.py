@@ -54,7 +54,7 @@ def parse_args(argv=None):
     ap.add_argument("--config", default="llama-7b-block")
     ap.add_argument("--plan", default="mix",
                     choices=["mix", "nvfp4", "fp8", "mxfp4", "nvfp4-b32", "nvfp4-b64", "nvfp4-b128", "snip"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
                     help="run every call on one stream (no quantization beside the GEMMs)")
@@ -603,7 +603,8 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
                 dr.record(sD)
                 state["drained"][j] = dr
 
-    one()
+    for _ in range(2):   # warm-up: first-use costs of the layer calls and the pinned buffers
+        one()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(sC)
