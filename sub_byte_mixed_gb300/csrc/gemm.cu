@@ -427,19 +427,27 @@ __global__ void __launch_bounds__(448, 1)
 // rows by the whole B tile); holding only its own 128 gives wrong products.
 // The library routes every GEMM with at least one full wave of 256 x 256
 // tiles here (both formats); smaller ones run on the one-CTA kernel.
-template <int FMT, bool RQ = false>
+// NS: 256-column MMA sub-tiles per pair tile.  NS = 2 (FP8 only, which keeps no
+// scale factors in tensor memory) makes 256 x 512 tiles: two MMAs per k-step
+// share the A tile, so a CTA receives 48 KB per stage for twice the FLOPs of
+// a 32 KB stage (25% less shared-memory fill per FLOP), with its two 256-column
+// accumulators filling tensor memory (one accumulator stage).
+template <int FMT, bool RQ = false, int NS = 1>
 struct Gemm2Cfg {
-  static constexpr int BM = 128, BN = 256, BNC = 128, KB = 128;
-  static constexpr int A_BYTES = BM * KB, B_BYTES = BNC * KB;
+  static_assert(NS == 1 || (NS == 2 && FMT == 0 && !RQ), "256 x 512 pair tiles: FP8 without re-quantization");
+  static constexpr int MMA_N = 256;
+  static constexpr int BM = 128, BN = MMA_N * NS, BNC = 128, KB = 128;
+  static constexpr int A_BYTES = BM * KB, B_BYTES = NS * BNC * KB;
   static constexpr int CH = FMT == 2 ? 2 : 4;      // 512-byte scale chunks per 128 rows and stage
   static constexpr int SFA_BYTES = FMT ? CH * 512 : 0;
   static constexpr int SFB_BYTES = FMT ? 2 * CH * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int RQ_BYTES = RQ ? 8 * kRqStageWords * 8 : 0;
+  // NVFP4 five stages (tensor memory holds five stages of scales), else six, or fewer to fit
   static constexpr int BASE_STAGES = FMT == 1 ? 5 : 6;
-  static constexpr int STAGES =
-      BASE_STAGES * STAGE_BYTES + 2048 + RQ_BYTES <= kMaxSmem ? BASE_STAGES : BASE_STAGES - 1;
-  static constexpr int ACC_STAGES = FMT ? 1 : 2;
+  static constexpr int FIT_STAGES = (kMaxSmem - 2048 - RQ_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = BASE_STAGES < FIT_STAGES ? BASE_STAGES : FIT_STAGES;
+  static constexpr int ACC_STAGES = (FMT || NS == 2) ? 1 : 2;
   static constexpr int SFA_COLS = 4 * CH;
   static constexpr int SFB_COLS_K = 8;                    // scale columns of B per chunk (256 rows)
   static constexpr int SF_COLS = FMT ? SFA_COLS + CH * SFB_COLS_K : 0;
@@ -453,17 +461,17 @@ struct Gemm2Cfg {
   static constexpr int SF_WARPS = 4, EPI_WARP0 = 6, EPI_WARPS = 8, EPI_COLS = BN / 2, EPI_ROUND = RQ ? 32 : 64;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   static constexpr uint32_t IDESC =
-      FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((FMT == 2 ? 1u : 0u) << 23) |
+      FMT ? ((1u << 7) | (1u << 10) | ((uint32_t)(MMA_N >> 3) << 17) | ((FMT == 2 ? 1u : 0u) << 23) |
              ((uint32_t)(256 >> 4) << 24))
-          : ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24));
+          : ((1u << 4) | ((uint32_t)(MMA_N >> 3) << 17) | ((uint32_t)(256 >> 4) << 24));
 };
 
-template <int FMT, bool RQ = false>
+template <int FMT, bool RQ = false, int NS = 1>
 __global__ void __launch_bounds__(448, 1)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         GemmParams p) {
-  using C = Gemm2Cfg<FMT, RQ>;
+  using C = Gemm2Cfg<FMT, RQ, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -528,7 +536,10 @@ __global__ void __launch_bounds__(448, 1)
           if (rank == 0) mbar_arrive_expect_tx(full(stage), 2 * (C::A_BYTES + C::B_BYTES));
           const uint32_t leader_full = mapa_shared(full(stage), 0);
           tma_load_2d_pair(smem_u32(sA), &tmA, kb * C::KB, (2 * mt + rank) * C::BM, leader_full);
-          tma_load_2d_pair(smem_u32(sB), &tmB, kb * C::KB, (2 * nt + rank) * C::BNC, leader_full);
+#pragma unroll
+          for (int h = 0; h < NS; ++h)   // this CTA's 128 rows of each 256-row B sub-tile
+            tma_load_2d_pair(smem_u32(sB + h * C::BNC * C::KB), &tmB, kb * C::KB, (2 * (NS * nt + h) + rank) * C::BNC,
+                             leader_full);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -556,14 +567,18 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t adesc = smem_desc(sA + 32 * k, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(sB + 32 * k, 16, 1024, 2);
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            if (FMT == 1)
-              tc_mma_nvf4_pair(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * C::SFB_COLS_K, accum);
-            else if (FMT == 2)
-              tc_mma_mxf4_pair(d_tmem, adesc, bdesc, C::IDESC | ((2u * (k & 1)) << 4) | ((2u * (k & 1)) << 29),
-                               sf + 4 * (k >> 1), sf + C::SFA_COLS + (k >> 1) * C::SFB_COLS_K, accum);
-            else tc_mma_f8_pair(d_tmem, adesc, bdesc, C::IDESC | ((uint32_t)p.a_e5m2 << 7), accum);
+#pragma unroll
+            for (int h = 0; h < NS; ++h) {   // sub-tile h accumulates in columns [256 h, 256 h + 256)
+              const uint64_t bdesc = smem_desc(sB + h * C::BNC * C::KB + 32 * k, 16, 1024, 2);
+              if (FMT == 1)
+                tc_mma_nvf4_pair(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * C::SFB_COLS_K,
+                                 accum);
+              else if (FMT == 2)
+                tc_mma_mxf4_pair(d_tmem, adesc, bdesc, C::IDESC | ((2u * (k & 1)) << 4) | ((2u * (k & 1)) << 29),
+                                 sf + 4 * (k >> 1), sf + C::SFA_COLS + (k >> 1) * C::SFB_COLS_K, accum);
+              else tc_mma_f8_pair(d_tmem + h * C::MMA_N, adesc, bdesc, C::IDESC | ((uint32_t)p.a_e5m2 << 7), accum);
+            }
           }
           tc_commit_pair_mc(empty(stage), 0x3);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -766,13 +781,13 @@ static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, bool RQ>
+template <int FMT, bool RQ, int NS = 1>
 static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
                                     GemmParams p, int num_sms, cudaStream_t st) {
-  using C = Gemm2Cfg<FMT, RQ>;
+  using C = Gemm2Cfg<FMT, RQ, NS>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT, RQ>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT, RQ, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -790,7 +805,7 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   p.num_k_stages = (int)(row_bytes / C::KB);
   p.v8 = (reinterpret_cast<uintptr_t>(p.D) % 32 == 0) && (p.ldd % 8 == 0);
   p.num_m_tiles = (int)((p.M + 255) / 256);
-  p.num_n_tiles = (int)((p.N + 255) / 256);
+  p.num_n_tiles = (int)((p.N + C::BN - 1) / C::BN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
   cudaLaunchConfig_t cfg = {};
@@ -805,7 +820,23 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT, RQ>, ta, tb, tsa, tsb, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT, RQ, NS>, ta, tb, tsa, tsb, p);
+}
+
+// FP8 on 256 x 512 pair tiles for long contractions (measured on GB300: the
+// 16384 x 8192 x 28672 GEMM 21% faster, 8192 x 4096 x 4096 25% and
+// 8192 x 4096 x 11008 13% slower: the single accumulator stage exposes the
+// 512-column drain once per tile, which short contractions cannot hide),
+// where N's 256-row blocks pair up (so no TMA box starts past the padded B
+// rows) and their coarser waves over the SM pairs cost less than the ~20%
+// the wider tile saves.
+static bool fp8_wide_tiles(const GemmParams& p, int num_sms) {
+  const int64_t mt = (p.M + 255) / 256, nb = (p.N + 255) / 256, P = num_sms / 2;
+  if (p.kp < 16384 || nb % 2 != 0 || P <= 0) return false;
+  const int64_t t1 = mt * nb, t2 = t1 / 2;
+  if (t2 < P) return false;
+  const double e1 = (double)t1 / (double)((t1 + P - 1) / P * P), e2 = (double)t2 / (double)((t2 + P - 1) / P * P);
+  return e2 * 1.2 > e1;
 }
 
 // Measured on GB300 at the Llama-7B shapes, the CTA pair beats the one-CTA
@@ -822,6 +853,9 @@ static cudaError_t launch_gemm_rq(int fmt, bool pair, const uint8_t* a_codes, in
   if (fmt == 2)
     return pair ? launch_gemm_pair<2, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
                 : launch_gemm_cfg<2, 256, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
+  if constexpr (!RQ)
+    if (pair && fp8_wide_tiles(p, num_sms))
+      return launch_gemm_pair<0, false, 2>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
   return pair ? launch_gemm_pair<0, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st)
               : launch_gemm_cfg<0, 256, RQ>(a_codes, a_rows_padded, b_codes, b_rows_padded, p, num_sms, st);
 }

@@ -82,6 +82,26 @@ def test_gemm_cta_pair_path(snip, fmt, code, shape):
                f"{fmt} pair {shape}")
 
 
+@pytest.mark.parametrize("shape,e5m2", [((4864, 2048, 16384), False), ((4800, 2000, 16400), True)])
+def test_gemm_fp8_wide_pair_tiles(snip, shape, e5m2):
+    """FP8 GEMMs with long contractions whose 256 x 512 pair tiles fill whole waves of SM pairs
+    run two N = 256 MMAs per k-step (19 x 4 tiles on 76 pairs): an exact case and a ragged one
+    (M, N not multiples of the tile, N's last 512-column tile partly past N, K not a multiple of
+    the 128-element stage); A in E4M3 or E5M2."""
+    M, N, K = shape
+    X = inputs.normal_bf16((M, K), 1.0, 9, 1)
+    W = inputs.normal_bf16((N, K), 0.02, 9, 2)
+    if e5m2:
+        a = snip.quantize_e5m2(X.cuda(), layout=snip.MMA)
+        ref_a = oracle.quantize_e5m2(X)
+    else:
+        a = snip.quantize_fp8(X.cuda(), layout=snip.MMA)
+        ref_a = oracle.quantize_fp8(X)
+    b = snip.quantize_fp8(W.cuda(), layout=snip.MMA)
+    D = snip.gemm(snip.FP8_E5M2 if e5m2 else snip.FP8, a, b, M, N, K).cpu().numpy()
+    gemm_close(D, oracle.gemm_tn(ref_a.dequant(), oracle.quantize_fp8(W).dequant()), f"fp8 wide {shape}")
+
+
 def test_gemm_into_strided_output(snip):
     X = inputs.normal_bf16((128, 256), 1.0, 4, 1)
     W = inputs.normal_bf16((64, 256), 1.0, 4, 2)
