@@ -262,7 +262,7 @@ def whole_job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
 class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
-    def __init__(self, cfg, plan, snip, device, layers=None, overlap=True):
+    def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
@@ -327,7 +327,7 @@ class Step:
                 t = src[name]
                 rows, cols = t.shape
                 g = scp[name] + fo
-                if r in (0, 1, 2):
+                if r in (0, 1, 2) and stats:
                     # row-block quantization with SNIP's statistics of the same tensor in one pass
                     k = r
                     args = (f, t.data_ptr(), rows, cols, rnd[r], 0, sid + r, scp[name], snip.MMA,
@@ -718,6 +718,28 @@ def run_ours(args, rank, world, local_rank):
             cat_ms[cat] = cat_ms.get(cat, 0.0) + t
             cat_units[cat] = cat_units.get(cat, 0.0) + units
             cat_n[cat] = cat_n.get(cat, 0) + 1
+    # the same step without SNIP's statistics (SNIP collects them periodically; the steps in between
+    # only quantize and multiply), timed the same way, for the statistics' share of the step
+    no_stats = None
+    if not args.profile_run and rank == 0:
+        step2 = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, stats=False)
+        for _ in range(3):
+            step2.run()
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(args.steps):
+            step2.run()
+        stop.record()
+        torch.cuda.synchronize()
+        if step2.status() != snip.SNIP_OK:
+            raise RuntimeError("device status " + snip.status_string(step2.status()))
+        ms2 = start.elapsed_time(stop) / args.steps
+        flops2 = cfg.flops_fwd_bwd() if not layers else sum(6 * cfg.T * l.K * l.N for l in cfg.linears
+                                                             if l.name in layers)
+        no_stats = {"value": flops2 / (ms2 * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms2,
+                    "launches_per_step": step2.launches_per_step,
+                    "what": "the same step with plain row-block quantizations in place of the statistics-fused ones"}
+        del step2
     t2 = time.time()
     ms = max_over_ranks(ms, world, "cuda")
     clocks = sampler.summary(t0, t2) if sampler else None
@@ -786,6 +808,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "gpu_launches": step.launches_per_step * args.steps,
         "ms_per_step_one_stream": ms_serial,
+        "without_stats": no_stats,
     }
     if layers:
         line["config"]["layers"] = layers
