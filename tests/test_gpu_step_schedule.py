@@ -1,0 +1,43 @@
+"""The benchmark step's two-stream schedule (quantizations on one stream, GEMMs
+on another, operand buffers alternating between two sets by linear) against
+the same calls on one stream: Y, dX, dW and the statistics of every linear
+must be identical, so no GEMM reads an operand before its quantization has
+written it or after the next user of its buffer set has overwritten it."""
+import os
+import sys
+
+import pytest
+import torch
+
+from gpu_helpers import need_gpu
+
+pytestmark = pytest.mark.gpu
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+
+@pytest.mark.parametrize("plan_kind", ["mix", "nvfp4-b64"])
+def test_two_stream_step_matches_one_stream(plan_kind):
+    snip = need_gpu()
+    import bench
+    from sub_byte_mixed_gb300 import inputs
+    cfg = inputs.TINYLLAMA
+    plan = (inputs.seeded_plan(cfg, cfg.fp4_target, seed=0) if plan_kind == "mix"
+            else inputs.all_plan(bench.FORMAT_OF_NAME[plan_kind]))
+    serial = bench.Step(cfg, plan, snip, "cuda", overlap=False)
+    serial.run()
+    torch.cuda.synchronize()
+    assert serial.status() == snip.SNIP_OK
+    ref = ([y.clone() for y in serial.Y], [d.clone() for d in serial.dX], [w.clone() for w in serial.dW],
+           serial.raw.clone())
+    del serial
+    over = bench.Step(cfg, plan, snip, "cuda", overlap=True)
+    for _ in range(2):   # the second step also reuses both buffer sets across the step boundary
+        over.run()
+    torch.cuda.synchronize()
+    assert over.status() == snip.SNIP_OK
+    for j in range(len(cfg.linears)):
+        assert torch.equal(over.Y[j], ref[0][j]), ("Y", j)
+        assert torch.equal(over.dX[j], ref[1][j]), ("dX", j)
+        assert torch.equal(over.dW[j], ref[2][j]), ("dW", j)
+    assert torch.equal(over.raw, ref[3])
