@@ -160,6 +160,17 @@ int snip_version(void);
  * 10.3), else SNIP_ERR_UNSUPPORTED_DEVICE (or SNIP_ERR_CUDA). */
 snip_status snip_device_check(void);
 
+/* Self-check of the failure path shared by every pipeline wait in the GEMMs:
+ * a one-CTA kernel waits on an mbarrier phase that nothing completes.  After
+ * limit_ns (clamped to [1 us, 1 s]) the wait gives up, raises the timeout bit
+ * of the workspace status word (snip_workspace_status then reports
+ * SNIP_ERR_TIMEOUT) and sets the CTA's abort flag, on which a second waiting
+ * thread with a 4x longer limit gives up too.  out (device, 3 uint32):
+ * {1 if the first wait completed else 0, the same for the second wait, the
+ * second thread's ns in its wait}.  No trap or fault: the context stays
+ * usable.  ws: at least SNIP_WS_HEADER_BYTES. */
+snip_status snip_wait_check(uint64_t limit_ns, uint32_t* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Zero the status word of a workspace (async on `stream`). */
 snip_status snip_workspace_init(void* ws, size_t ws_bytes, void* stream);
 

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsnip.so")
-SOURCES = ["quant.cu", "gemm.cu", "api.cu", "noalloc.cu", "plan_select.cu"]
+SOURCES = ["quant.cu", "gemm.cu", "api.cu", "noalloc.cu", "plan_select.cu", "waitcheck.cu"]
 HEADERS = ["snip_device.cuh", "snip_kernels.cuh", "snip_quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -359,6 +359,17 @@ snip_status snip_tensor_scales_multi(int count, const void* const* xs, const int
   return run_scales_multi(count, xs, ns, scales_out, ws, sms, static_cast<cudaStream_t>(stream));
 }
 
+snip_status snip_wait_check(uint64_t limit_ns, uint32_t* out, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if (!out) return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < SNIP_WS_HEADER_BYTES) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(ws)) return SNIP_ERR_ALIGN;
+  const uint64_t lim = limit_ns < 1000u ? 1000u : limit_ns > 1000000000u ? 1000000000u : limit_ns;
+  return cuda_status(launch_wait_check(ws_at<uint32_t>(ws, kOffStatus), lim, out, static_cast<cudaStream_t>(stream)));
+}
+
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,
                                  size_t* codes_bytes, size_t* scales_bytes) {
   if (!valid_operand_fmt(fmt) || !valid_enum(layout, 2) || out_rows < 0 || out_cols < 0) return SNIP_ERR_INVALID_ARG;

@@ -145,6 +145,9 @@ cudaError_t launch_dw_noise(const float* q, const float* ref, int64_t n, double*
 cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,
                         int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st);
 
+// Self-check of the bounded wait (waitcheck.cu): out = {completed 0, completed 1, ns}.
+cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, uint32_t* out, cudaStream_t st);
+
 // Upper bound on the number of amax / stats partial slots any launch uses.
 constexpr int kMaxPartials = 1024;
 

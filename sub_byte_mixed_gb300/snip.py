@@ -33,7 +33,7 @@ EXPORTS = (
     "snip_status_string", "snip_version", "snip_device_check", "snip_workspace_init", "snip_workspace_status",
     "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_tensor_scales_multi",
     "snip_tensor_scales_noalloc",
-    "snip_quantize_nvfp4", "snip_quantize_nvfp4_block", "snip_quantize_fp8", "snip_quantize_mxfp4",
+    "snip_wait_check", "snip_quantize_nvfp4", "snip_quantize_nvfp4_block", "snip_quantize_fp8", "snip_quantize_mxfp4",
     "snip_quantize_e5m2",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
@@ -85,6 +85,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_tensor_scales": (i32, [vp, i64, vp, vp, sz, vp]),
         "snip_tensor_scales_noalloc": (i32, [vp, i64, vp, vp]),
         "snip_tensor_scales_multi": (i32, [i32, vp, vp, vp, vp, sz, vp]),
+        "snip_wait_check": (i32, [u64, vp, vp, sz, vp]),
         "snip_quantize_nvfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_nvfp4_block": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, i32, vp, vp, vp, vp, sz,
                                             vp]),
@@ -169,6 +170,18 @@ def snip_quantize_nvfp4(x, rows, cols, orient, rnd, seed, stream_id, g_in, layou
                         block_sqerr, ws, ws_bytes, stream):
     _call("snip_quantize_nvfp4", x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
           block_sqerr, ws, ws_bytes, stream)
+
+
+def snip_wait_check(limit_ns, out, ws, ws_bytes, stream):
+    _call("snip_wait_check", limit_ns, out, ws, ws_bytes, stream)
+
+
+def wait_check(limit_ns: int, ws: Workspace):
+    """Run the bounded-wait self-check on `ws` -> device uint32 tensor {completed 0, completed 1, ns}."""
+    torch = _torch()
+    out = torch.full((3,), 0xFFFF, dtype=torch.int32, device=ws.buf.device)
+    snip_wait_check(limit_ns, out.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return out
 
 
 def snip_quantize_nvfp4_block(x, rows, cols, orient, rnd, seed, stream_id, g_in, block, layout, codes, scales,
