@@ -718,28 +718,36 @@ def run_ours(args, rank, world, local_rank):
             cat_ms[cat] = cat_ms.get(cat, 0.0) + t
             cat_units[cat] = cat_units.get(cat, 0.0) + units
             cat_n[cat] = cat_n.get(cat, 0) + 1
-    # the same step without SNIP's statistics (SNIP collects them periodically; the steps in between
-    # only quantize and multiply), timed the same way, for the statistics' share of the step
-    no_stats = None
-    if not args.profile_run and rank == 0:
-        step2 = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, stats=False)
+    flops_step = cfg.flops_fwd_bwd() if not layers else sum(6 * cfg.T * l.K * l.N for l in cfg.linears
+                                                             if l.name in layers)
+
+    def time_variant(plan_v, stats_v):
+        """Another step of the same block, timed as the headline (K steps after 3 warm-up steps)."""
+        sv = Step(cfg, plan_v, snip, "cuda", layers, overlap=not args.no_overlap, stats=stats_v)
         for _ in range(3):
-            step2.run()
+            sv.run()
         torch.cuda.synchronize()
         start.record()
         for _ in range(args.steps):
-            step2.run()
+            sv.run()
         stop.record()
         torch.cuda.synchronize()
-        if step2.status() != snip.SNIP_OK:
-            raise RuntimeError("device status " + snip.status_string(step2.status()))
-        ms2 = start.elapsed_time(stop) / args.steps
-        flops2 = cfg.flops_fwd_bwd() if not layers else sum(6 * cfg.T * l.K * l.N for l in cfg.linears
-                                                             if l.name in layers)
-        no_stats = {"value": flops2 / (ms2 * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms2,
-                    "launches_per_step": step2.launches_per_step,
-                    "what": "the same step with plain row-block quantizations in place of the statistics-fused ones"}
-        del step2
+        if sv.status() != snip.SNIP_OK:
+            raise RuntimeError("device status " + snip.status_string(sv.status()))
+        msv = start.elapsed_time(stop) / args.steps
+        return {"value": flops_step / (msv * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": msv,
+                "launches_per_step": sv.launches_per_step, "fp4_flop_fraction": round(cfg.fp4_flop_fraction(plan_v), 4)}
+
+    # the same step without SNIP's statistics (SNIP collects them periodically; the steps in between
+    # only quantize and multiply), for the statistics' share of the step; and the block's uniform plans
+    no_stats = other_plans = None
+    if not args.profile_run and rank == 0:
+        no_stats = time_variant(plan, False)
+        no_stats["what"] = "the same step with plain row-block quantizations in place of the statistics-fused ones"
+        if args.plan in ("mix", "snip") and not layers:
+            from sub_byte_mixed_gb300 import inputs as inp_mod
+            other_plans = {name: time_variant(inp_mod.all_plan(FORMAT_OF_NAME[name]), True)
+                           for name in ("fp8", "nvfp4")}
     t2 = time.time()
     ms = max_over_ranks(ms, world, "cuda")
     clocks = sampler.summary(t0, t2) if sampler else None
@@ -809,6 +817,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": step.launches_per_step * args.steps,
         "ms_per_step_one_stream": ms_serial,
         "without_stats": no_stats,
+        "uniform_plans": other_plans,
     }
     if layers:
         line["config"]["layers"] = layers

@@ -321,7 +321,8 @@ snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t ou
  * FP8_E5M2: A is E5M2 with its scale s5, B is E4M3 with its scale s).
  * NVFP4 uses the tensor cores' block-scaled FP4 MMA with E4M3 block scales
  * (scale_vec::4X), MXFP4 the same MMA with E8M0 scales (scale_vec::2X), FP8
- * the E4M3 x E4M3 MMA.  Accumulation is fp32.  Needs K % 16 == 0 (MXFP4:
+ * the E4M3 x E4M3 MMA.  NVFP4_B32/_B64/_B128 operands are NVFP4 operands
+ * (their repeated scales give the longer blocks' product exactly).  Accumulation is fp32.  Needs K % 16 == 0 (MXFP4:
  * K % 32 == 0), else SNIP_ERR_SHAPE.
  * ws: at least SNIP_WS_HEADER_BYTES (status word; a timed-out wait raises
  * SNIP_ERR_TIMEOUT there). */
