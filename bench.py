@@ -334,8 +334,8 @@ class Step:
                             self.codes[r].data_ptr(), self.scales[r].data_ptr() if f != snip.FP8 else None,
                             self.raw[j, k].data_ptr(), ws, wsb, stream)
                     calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", j, -1))
-                    if f == snip.MXFP4 or block > 16:
-                        extra_launches += 1   # these formats' statistics run in a second kernel
+                    if f == snip.MXFP4:
+                        extra_launches += 1   # MXFP4's statistics run in a second kernel
                 elif block > 16:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, block, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, ws, wsb, stream)

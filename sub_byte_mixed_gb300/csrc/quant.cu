@@ -302,8 +302,13 @@ __device__ __forceinline__ void stats_nan(double* raw_out) {
 // call's rounding and random bits) from the same read; needs p.scales3.
 // FMT: 0 FP8, 1 NVFP4, 2 MXFP4 (lanes 2i and 2i+1 hold the two halves of one
 // 32-element block and share its scale through a shuffle; no statistics).
-template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS>
+// LONG (with STATS, NVFP4 only): codes with p.group-block scales beside the
+// 16-element statistics -- its own instantiation, so the statistics kernels of
+// the other formats keep their registers.  Without STATS p.group is read at run
+// time.
+template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS, bool LONG = false>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
+  static_assert(!LONG || (FMT == 1 && STATS), "LONG: NVFP4 with fused statistics");
   static_assert(FMT < 2 || (!STATS && !ERR), "MXFP4 / E5M2 quantization has no fused statistics or block errors");
   // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
   const float g = FMT == 3 ? e5m2_tensor_scale(*p.scale) : *p.scale;
@@ -331,7 +336,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     if (sr >= spr) { sr -= spr; ++r; }
     const uint32_t kb = sr * 32 + lane;
     // MXFP4 lanes, and NVFP4 lanes of longer blocks, leave after the shuffles that share block maxima
-    if (FMT != 2 && kb >= bpr && !(FMT == 1 && !STATS && p.group > 1)) continue;
+    const bool longer = FMT == 1 && (STATS ? LONG : p.group > 1);
+    if (FMT != 2 && kb >= bpr && !longer) continue;
     const bool real = r < p.out_rows && (int64_t)kb * 16 < p.out_cols;
     uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
     const int64_t e0 = (int64_t)r * p.cols + (int64_t)kb * 16;
@@ -344,24 +350,42 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     unpack16(a, b, v);
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     if (RND == 1 && real) sr_bits16(e0, p.seed, p.stream_id, u);
-    BlockScale bs;
+    // bs: the 16-element NVFP4 scale (codes, and the statistics' NVFP4 candidate); bw: the scale
+    // the codes are written with -- bs, or with longer blocks the scale of p.group 16-element blocks
+    BlockScale bs, bw;
     if (FMT == 2) {
       uint32_t m = amax16_bits(a, b);
       m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
       if (kb >= bpr) continue;
       bs = mxfp4_block_scale(m);
     }
-    if (FMT == 1 && !STATS && p.group > 1) {
+    if (longer) {
       // one scale for p.group consecutive 16-element blocks: lanes 2^k apart share their maxima
-      uint32_t m = amax16_bits(a, b);
+      const uint32_t m16 = amax16_bits(a, b);
+      uint32_t m = m16;
       for (int o = 1; o < p.group; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (kb >= bpr) continue;
-      bs = nvfp4_block_scale(m, g4, six_g);
+      bw = nvfp4_block_scale(m, g4, six_g);
+      bs = STATS ? nvfp4_block_scale(m16, g4, six_g) : bw;
     } else if (FMT == 1 || STATS) {
       bs = nvfp4_block_scale(amax16_bits(a, b), g4, six_g);
     }
+    if (!longer) bw = bs;
     uint4 c = make_uint4(0u, 0u, 0u, 0u);   // FP8: 16 codes; FP4: .x, .y
-    if (STATS) {
+    if (STATS && longer) {
+      // statistics of the two candidate formats (16-element NVFP4, FP8), codes with the longer block's scale
+      if (real) {
+        const BlockStats st = stats_block16<-1, RND>(v, bs, u, s8, inv8, special8, c);
+        sx2 += st.x2;
+        e4 += st.e4;
+        e8 += st.e8;
+        v4 += st.v4;
+        v8 += st.v8;
+        const uint2 e = nvfp4_encode16<RND>(v, bw, PackedBits{u});
+        c.x = e.x;
+        c.y = e.y;
+      }
+    } else if (STATS) {
       // the codes come out of the statistics' own conversions
       if (real) {
         const BlockStats st = stats_block16<FMT, RND>(v, bs, u, s8, inv8, special8, c);
@@ -378,7 +402,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
         if (FMT == 0 && special8) c = fp8_encode16<RND>(v, inv8, PackedBits{u});
       }
     } else if (FMT == 1 || FMT == 2) {
-      const uint2 e = nvfp4_encode16<RND>(v, bs, PackedBits{u});
+      const uint2 e = nvfp4_encode16<RND>(v, bw, PackedBits{u});
       c.x = e.x;
       c.y = e.y;
     } else {
@@ -399,12 +423,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
       if (LAYOUT == 0) {
         if (!real) continue;
         *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.out_cols >> 1) + (int64_t)kb * 8) = c2;
-        p.scales[(int64_t)r * (p.out_cols >> 4) + kb] = (uint8_t)bs.s;
+        p.scales[(int64_t)r * (p.out_cols >> 4) + kb] = (uint8_t)bw.s;
       } else {
         *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.ocp >> 1) + (int64_t)kb * 8) = c2;
-        p.scales[mma_scale_offset(r, kb, p.ocp)] = (uint8_t)bs.s;
+        p.scales[mma_scale_offset(r, kb, p.ocp)] = (uint8_t)bw.s;
       }
-      if (ERR && real && p.block_err) p.block_err[(int64_t)r * (p.out_cols >> 4) + kb] = nvfp4_block_err(v, c2, bs.p);
+      if (ERR && real && p.block_err) p.block_err[(int64_t)r * (p.out_cols >> 4) + kb] = nvfp4_block_err(v, c2, bw.p);
     } else {
       const int64_t pitch = LAYOUT == 0 ? p.out_cols : p.ocp;
       if (LAYOUT == 0 && !real) continue;
@@ -709,6 +733,18 @@ static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int r
     const bool stats = p.raw_out != nullptr;
     // with statistics, one partial slot per CTA: keep the grid within them
     const int grid = fill_grid(segs, 8, stats ? 4 * num_sms : 16 * num_sms);
+    if constexpr (FMT == 1) {
+      if (stats && p.group > 1) {   // longer NVFP4 blocks with fused statistics (no block errors)
+        if (layout == 0) {
+          if (rnd == 0) quant_rows_kernel<1, 0, 0, false, true, true><<<grid, 256, 0, st>>>(p);
+          else quant_rows_kernel<1, 0, 1, false, true, true><<<grid, 256, 0, st>>>(p);
+        } else {
+          if (rnd == 0) quant_rows_kernel<1, 1, 0, false, true, true><<<grid, 256, 0, st>>>(p);
+          else quant_rows_kernel<1, 1, 1, false, true, true><<<grid, 256, 0, st>>>(p);
+        }
+        return;
+      }
+    }
 #define SNIP_L(LY, RN, ER, SS) quant_rows_kernel<FMT, LY, RN, ER, SS><<<grid, 256, 0, st>>>(p)
 #define SNIP_LS(LY, RN, ER) do { if (stats) SNIP_L(LY, RN, ER, true); else SNIP_L(LY, RN, ER, false); } while (0)
     if (layout == 0) {

@@ -22,7 +22,7 @@ struct QuantParams {
   float* g_out;                 // nullable: receives *scale
   float* block_err;             // NVFP4 only, nullable
   int group;                    // NVFP4: 16-element blocks sharing one scale (0 or 1: NVFP4;
-                                // 2, 4, 8: 32-, 64-, 128-element blocks; no fused statistics)
+                                // 2, 4, 8: 32-, 64-, 128-element blocks)
   // statistics fused into a row-block quantization (raw_out non-null)
   const float* scales3;         // {amax, NVFP4 g, FP8 s}
   double* partials;

@@ -552,7 +552,8 @@ def quantize_stats(fmt, x, rnd=RTN, seed=0, stream_id=0, layout=MMA, scales=None
     sc = torch.empty(max(sb, 16), dtype=torch.uint8, device=x.device)
     raw = torch.empty(STATS_NVALS, dtype=torch.float64, device=x.device)
     snip_quantize_stats(fmt, x.data_ptr(), rows, cols, rnd, seed, stream_id, _ptr(scales), layout, codes.data_ptr(),
-                        sc.data_ptr() if fmt in (NVFP4, MXFP4) else None, raw.data_ptr(), ws.ptr, ws.nbytes, _stream())
+                        sc.data_ptr() if fmt in NVFP4_BLOCK or fmt == MXFP4 else None, raw.data_ptr(), ws.ptr,
+                        ws.nbytes, _stream())
     return codes[:cb], sc[:sb], raw
 
 

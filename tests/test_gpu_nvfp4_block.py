@@ -126,3 +126,19 @@ def test_block_errors(snip):
         snip.qlinear_fwd(plan, 0, torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda"),
                          torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda"), snip.Workspace(1 << 22))
     assert e.value.status == snip.SNIP_ERR_SHAPE
+
+
+@pytest.mark.parametrize("fmt,block", [(5, 32), (7, 128)])
+@pytest.mark.parametrize("rnd", [0, 1])
+def test_block_quantize_stats_fused(snip, fmt, block, rnd):
+    """Longer-block codes and SNIP's statistics of the candidate formats from one pass."""
+    x = _x((256, 1024), 40 + block)
+    codes, scales, raw = snip.quantize_stats(fmt, x.cuda(), rnd=rnd, seed=6, stream_id=13, layout=snip.ROWMAJOR)
+    torch.cuda.synchronize()
+    ref = oracle.quantize_nvfp4_block(x, block, rnd=rnd, seed=6, stream_id=13)
+    np.testing.assert_array_equal(codes.cpu().numpy().reshape(ref.codes.shape), ref.codes)
+    np.testing.assert_array_equal(scales.cpu().numpy().reshape(ref.rows, -1), _expand(ref.scales, block))
+    r = oracle.quant_stats(x, rnd=rnd, seed=6, stream_id=13)["raw"]
+    got = raw.cpu().numpy()
+    for k in range(7):
+        assert got[k] == pytest.approx(r[k], rel=STATS_REL, abs=1e-300), k
