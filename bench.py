@@ -56,6 +56,8 @@ def parse_args(argv=None):
                     choices=["mix", "nvfp4", "fp8", "mxfp4", "nvfp4-b32", "nvfp4-b64", "nvfp4-b128", "snip"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="issue the step's calls one by one instead of replaying them as a captured CUDA graph")
     ap.add_argument("--no-overlap", action="store_true",
                     help="run every call on one stream (no quantization beside the GEMMs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -101,7 +103,8 @@ def config_json(cfg, plan, args):
         "stats": "SNIP statistics of X, W (forward rounding) and dY (dgrad rounding) fused into their row-block quantizations",
         "schedule": ("one stream" if args.no_overlap else
                      "quantizations and GEMMs on two streams: a linear's quantizations run beside the previous "
-                     "linear's GEMMs (events order every GEMM after its operands)"),
+                     "linear's GEMMs (events order every GEMM after its operands)")
+                    + ("; the step captured once as a CUDA graph and replayed" if not args.no_graph else ""),
         "plan_source": ("SNIP selection from one step's statistics (snip_plan_select, FP4-FLOP target "
                         f"{cfg.fp4_target})") if args.plan == "snip" else
                        ("seeded plan at the FP4-FLOP target" if args.plan == "mix" else "uniform"),
@@ -262,15 +265,18 @@ def whole_job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
 class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
-    def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True):
+    def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True, own_stream=False):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
         # overlap: quantizations on one stream, GEMMs on another, so that a linear's quantizations run
         # beside the previous linear's GEMMs; operand buffers alternate between two sets by linear
         self.overlap = overlap
-        self.sQ = torch.cuda.current_stream()
+        # own_stream: the quantization stream is a stream of its own (a graph cannot be captured on
+        # the default stream); run() then joins the caller's stream at both ends
+        self.sQ = torch.cuda.Stream() if own_stream else torch.cuda.current_stream()
         self.sG = torch.cuda.Stream() if overlap else self.sQ
+        self.graph = None
         nsets = 2 if overlap else 1
         L = snip.load()
         self.inp = inputs.block_inputs(cfg, seed=0, device=device)
@@ -380,6 +386,11 @@ class Step:
         ready, gdone = {}, {}
         last_g = None
         overlap = self.overlap and not serial
+        cur = torch.cuda.current_stream()
+        if cur != self.sQ:
+            ev = torch.cuda.Event()
+            ev.record(cur)
+            self.sQ.wait_event(ev)
         for i, (fn, args, _, _, kind, j, gi) in enumerate(self.calls):
             if serial:
                 args = self.serial_args[i]
@@ -409,6 +420,25 @@ class Step:
                     last_g = ev
         if overlap and last_g is not None:
             self.sQ.wait_event(last_g)
+        if cur != self.sQ:
+            ev = torch.cuda.Event()
+            ev.record(self.sQ)
+            cur.wait_event(ev)
+
+    def capture(self):
+        """Record one step (both streams, with their events) as a CUDA graph."""
+        import torch
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.sQ):
+            self.graph.capture_begin()
+            self.run()
+            self.graph.capture_end()
+        torch.cuda.synchronize()
+
+    def replay(self):
+        """One step from the captured graph, on the caller's stream."""
+        self.graph.replay()
 
     def status(self):
         s = self.ws.status()
@@ -652,7 +682,8 @@ def run_ours(args, rank, world, local_rank):
     snip.snip_device_check()
     cfg, plan = workload(args)
     layers = [x for x in args.layers.split(",") if x]
-    step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap)
+    graph = not args.no_graph
+    step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph)
     if args.plan == "snip" and layers:
         raise SystemExit("--plan snip selects formats for the whole block; it cannot be combined with --layers")
     if args.plan == "snip":
@@ -663,7 +694,7 @@ def run_ours(args, rank, world, local_rank):
         flops = [6.0 * cfg.T * l.K * l.N for l in cfg.linears]
         plan, _, _ = snip.snip_plan_select(flops, c8, c4, cfg.fp4_target)
         del step
-        step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap)
+        step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph)
     torch.cuda.synchronize()
     ncalls = len(step.calls)
     sampler = ClockSampler(local_rank) if rank == 0 and not args.profile_run else None
@@ -675,6 +706,10 @@ def run_ours(args, rank, world, local_rank):
         while time.time() - t_settle < 1.0:
             step.run()
             torch.cuda.synchronize()
+    if graph:
+        step.capture()   # the whole step, both streams, as one CUDA graph
+        for _ in range(2):
+            step.replay()
     events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(ncalls)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -684,7 +719,10 @@ def run_ours(args, rank, world, local_rank):
     t0 = time.time()
     start.record()
     for s in range(args.steps):
-        step.run(events[s])
+        if graph:
+            step.replay()
+        else:
+            step.run()
     stop.record()
     torch.cuda.synchronize()
     t1 = time.time()
@@ -694,22 +732,21 @@ def run_ours(args, rank, world, local_rank):
     status = step.status()
     if status != snip.SNIP_OK:
         raise RuntimeError("device status " + snip.status_string(status))
-    ms_serial = None
-    if step.overlap:
-        # per-kernel durations: kernels that share the SMs stretch each other's event times, so the
-        # breakdown and the roofline come from the same step run serially, K more steps in a row
-        for _ in range(3):
-            step.run(serial=True)
-        torch.cuda.synchronize()
-        start.record()
-        for s in range(args.steps):
-            step.run(events[s], serial=True)
-        stop.record()
-        torch.cuda.synchronize()
-        ms_serial = start.elapsed_time(stop) / args.steps
-        status = step.status()
-        if status != snip.SNIP_OK:
-            raise RuntimeError("device status " + snip.status_string(status))
+    # per-kernel durations: kernels that share the SMs stretch each other's event times, and a
+    # replayed graph has no per-launch events, so the breakdown and the roofline come from the
+    # same calls issued one at a time on one stream, K more steps in a row
+    for _ in range(3):
+        step.run(serial=True)
+    torch.cuda.synchronize()
+    start.record()
+    for s in range(args.steps):
+        step.run(events[s], serial=True)
+    stop.record()
+    torch.cuda.synchronize()
+    ms_serial = start.elapsed_time(stop) / args.steps
+    status = step.status()
+    if status != snip.SNIP_OK:
+        raise RuntimeError("device status " + snip.status_string(status))
     # per-category kernel time
     cat_ms, cat_units, cat_n = {}, {}, {}
     for s in range(args.steps):
@@ -723,13 +760,19 @@ def run_ours(args, rank, world, local_rank):
 
     def time_variant(plan_v, stats_v):
         """Another step of the same block, timed as the headline (K steps after 3 warm-up steps)."""
-        sv = Step(cfg, plan_v, snip, "cuda", layers, overlap=not args.no_overlap, stats=stats_v)
+        sv = Step(cfg, plan_v, snip, "cuda", layers, overlap=not args.no_overlap, stats=stats_v, own_stream=graph)
         for _ in range(3):
             sv.run()
+        if graph:
+            sv.capture()
+            sv.replay()
         torch.cuda.synchronize()
         start.record()
         for _ in range(args.steps):
-            sv.run()
+            if graph:
+                sv.replay()
+            else:
+                sv.run()
         stop.record()
         torch.cuda.synchronize()
         if sv.status() != snip.SNIP_OK:
@@ -789,9 +832,8 @@ def run_ours(args, rank, world, local_rank):
     roofline = {"bound": "tensor" if dom.startswith("gemm") else "hbm", "kernel": dom,
                 "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"], "frac": d["frac"],
                 "traffic": traffic,
-                "timed": ("CUDA events around each launch in K serial steps after the overlapped timed region "
-                          "(kernels alone on the GPU)" if step.overlap else
-                          "CUDA events around each launch in the timed region"),
+                "timed": "CUDA events around each launch in K steps issued one call at a time on one stream, "
+                         "right after the timed region (kernels alone on the GPU)",
                 "peak_source": f"{peaks['source']} ("
                 + ("bf16 sustained x nominal FP4/FP8 ratio" if dom.startswith("gemm") else "HBM copy") + ")"}
     qcats = [c for c in breakdown if not c.startswith("gemm")]

@@ -1,6 +1,7 @@
 """The benchmark step's two-stream schedule (quantizations on one stream, GEMMs
-on another, operand buffers alternating between two sets by linear) against
-the same calls on one stream: Y, dX, dW and the statistics of every linear
+on another, operand buffers alternating between two sets by linear), issued
+call by call and replayed from a captured CUDA graph, against the same calls
+on one stream: Y, dX, dW and the statistics of every linear
 must be identical, so no GEMM reads an operand before its quantization has
 written it or after the next user of its buffer set has overwritten it."""
 import os
@@ -41,3 +42,16 @@ def test_two_stream_step_matches_one_stream(plan_kind):
         assert torch.equal(over.dX[j], ref[1][j]), ("dX", j)
         assert torch.equal(over.dW[j], ref[2][j]), ("dW", j)
     assert torch.equal(over.raw, ref[3])
+    del over
+    # the same two-stream step captured once as a CUDA graph and replayed
+    graph = bench.Step(cfg, plan, snip, "cuda", overlap=True, own_stream=True)
+    graph.run()
+    graph.capture()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert graph.status() == snip.SNIP_OK
+    for j in range(len(cfg.linears)):
+        assert torch.equal(graph.Y[j], ref[0][j]) and torch.equal(graph.dX[j], ref[1][j]), j
+        assert torch.equal(graph.dW[j], ref[2][j]), j
+    assert torch.equal(graph.raw, ref[3])
