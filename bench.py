@@ -305,7 +305,6 @@ class Step:
         calls = []   # (fn, args, category, units, stream kind 'q'/'g', linear, GEMM index or -1)
         self.gemm_ws = snip.Workspace(snip.WS_HEADER_BYTES, device) if overlap else self.ws
         self._keep = []   # ctypes arrays referenced by the calls
-        extra_launches = 0
         for j, (l, f) in enumerate(zip(cfg.linears, plan)):
             if layers and l.name not in layers:
                 continue
@@ -340,8 +339,6 @@ class Step:
                             self.codes[r].data_ptr(), self.scales[r].data_ptr() if f != snip.FP8 else None,
                             self.raw[j, k].data_ptr(), ws, wsb, stream)
                     calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", j, -1))
-                    if f == snip.MXFP4:
-                        extra_launches += 1   # MXFP4's statistics run in a second kernel
                 elif block > 16:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, block, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, ws, wsb, stream)
@@ -373,9 +370,9 @@ class Step:
         self.calls = calls
         # the same calls with every launch on the quantization stream (kernels one after another)
         self.serial_args = [a if k == "q" else a[:-1] + (stream,) for (_, a, _, _, k, _, _) in calls]
-        # one kernel per call (the scales are computed once per tensor and passed in), plus the
-        # statistics kernels of the formats whose statistics are not fused
-        self.launches_per_step = len(calls) + extra_launches
+        # one kernel per call (the scales are computed once per tensor and passed in; every plan
+        # format here has its statistics fused into its row-block quantization)
+        self.launches_per_step = len(calls)
 
     def run(self, events=None, serial=False):
         """One step.  With overlap, a GEMM waits for its two operands' quantizations, and the

@@ -174,8 +174,8 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   }
   // an empty output still publishes its tensor scale: the one-CTA row kernel does that
   if (p.orp == 0 || p.ocp == 0) orient = SNIP_BLOCKS_ALONG_COLS;
-  if ((fmt == SNIP_FMT_MXFP4 || fmt == SNIP_FMT_FP8_E5M2) && raw_out) {
-    // MXFP4 / E5M2 codes, then the statistics in their own pass (same rounding and random bits)
+  if (fmt == SNIP_FMT_FP8_E5M2 && raw_out) {
+    // E5M2 codes, then the statistics in their own pass (same rounding and random bits)
     p.scales3 = nullptr;
     p.raw_out = nullptr;
     cudaError_t e = launch_quant(kernel_fmt(fmt), p, orient, layout, rnd, false, num_sms, st);

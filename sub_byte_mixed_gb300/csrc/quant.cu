@@ -301,7 +301,8 @@ __device__ __forceinline__ void stats_nan(double* raw_out) {
 // STATS: also accumulate SNIP's statistics of the tensor (both formats, this
 // call's rounding and random bits) from the same read; needs p.scales3.
 // FMT: 0 FP8, 1 NVFP4, 2 MXFP4 (lanes 2i and 2i+1 hold the two halves of one
-// 32-element block and share its scale through a shuffle; no statistics).
+// 32-element block and share its scale through a shuffle; with STATS each lane
+// also takes the statistics of its 16 elements under the candidate formats).
 // LONG (with STATS, NVFP4 only): codes with p.group-block scales beside the
 // 16-element statistics -- its own instantiation, so the statistics kernels of
 // the other formats keep their registers.  Without STATS p.group is read at run
@@ -309,7 +310,8 @@ __device__ __forceinline__ void stats_nan(double* raw_out) {
 template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS, bool LONG = false>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   static_assert(!LONG || (FMT == 1 && STATS), "LONG: NVFP4 with fused statistics");
-  static_assert(FMT < 2 || (!STATS && !ERR), "MXFP4 / E5M2 quantization has no fused statistics or block errors");
+  static_assert(FMT < 2 || !ERR, "MXFP4 / E5M2 quantization has no block errors");
+  static_assert(FMT != 3 || !STATS, "E5M2 quantization has no fused statistics");
   // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
   const float g = FMT == 3 ? e5m2_tensor_scale(*p.scale) : *p.scale;
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = (FMT == 2 && !isnan(g)) ? 1.0f : g;
@@ -354,10 +356,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     // the codes are written with -- bs, or with longer blocks the scale of p.group 16-element blocks
     BlockScale bs, bw;
     if (FMT == 2) {
-      uint32_t m = amax16_bits(a, b);
-      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      const uint32_t m16 = amax16_bits(a, b);
+      const uint32_t m = max(m16, __shfl_xor_sync(0xffffffffu, m16, 1));
       if (kb >= bpr) continue;
-      bs = mxfp4_block_scale(m);
+      bw = mxfp4_block_scale(m);
+      // the statistics' NVFP4 candidate has its own 16-element scale; the codes use the E8M0 one
+      bs = STATS ? nvfp4_block_scale(m16, g4, six_g) : bw;
     }
     if (longer) {
       // one scale for p.group consecutive 16-element blocks: lanes 2^k apart share their maxima
@@ -370,10 +374,11 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     } else if (FMT == 1 || STATS) {
       bs = nvfp4_block_scale(amax16_bits(a, b), g4, six_g);
     }
-    if (!longer) bw = bs;
+    if (!longer && FMT != 2) bw = bs;
     uint4 c = make_uint4(0u, 0u, 0u, 0u);   // FP8: 16 codes; FP4: .x, .y
-    if (STATS && longer) {
-      // statistics of the two candidate formats (16-element NVFP4, FP8), codes with the longer block's scale
+    if (STATS && (longer || FMT == 2)) {
+      // statistics of the two candidate formats (16-element NVFP4, FP8); codes with the scale of the
+      // longer NVFP4 block or the MXFP4 block
       if (real) {
         const BlockStats st = stats_block16<-1, RND>(v, bs, u, s8, inv8, special8, c);
         sx2 += st.x2;
@@ -413,10 +418,10 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
       if (LAYOUT == 0) {
         if (!real) continue;
         *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.out_cols >> 1) + (int64_t)kb * 8) = c2;
-        if (!(kb & 1)) p.scales[(int64_t)r * (p.out_cols >> 5) + (kb >> 1)] = (uint8_t)bs.s;
+        if (!(kb & 1)) p.scales[(int64_t)r * (p.out_cols >> 5) + (kb >> 1)] = (uint8_t)bw.s;
       } else {
         *reinterpret_cast<uint2*>(p.codes + (int64_t)r * (p.ocp >> 1) + (int64_t)kb * 8) = c2;
-        if (!(kb & 1)) p.scales[mma_scale_offset_mx(r, kb >> 1, p.ocp)] = (uint8_t)bs.s;
+        if (!(kb & 1)) p.scales[mma_scale_offset_mx(r, kb >> 1, p.ocp)] = (uint8_t)bw.s;
       }
     } else if (FMT == 1) {
       const uint2 c2 = make_uint2(c.x, c.y);
@@ -775,8 +780,18 @@ static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int r
 static void launch_quant_mx(const QuantParams& p, int orient, int layout, int rnd, int num_sms, cudaStream_t st) {
   if (orient == 0) {
     const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
-    const int grid = fill_grid(segs, 8, 16 * num_sms);
-    if (layout == 0) {
+    const bool stats = p.raw_out != nullptr;
+    // with statistics, one partial slot per CTA: keep the grid within them
+    const int grid = fill_grid(segs, 8, stats ? 4 * num_sms : 16 * num_sms);
+    if (stats) {
+      if (layout == 0) {
+        if (rnd == 0) quant_rows_kernel<2, 0, 0, false, true><<<grid, 256, 0, st>>>(p);
+        else quant_rows_kernel<2, 0, 1, false, true><<<grid, 256, 0, st>>>(p);
+      } else {
+        if (rnd == 0) quant_rows_kernel<2, 1, 0, false, true><<<grid, 256, 0, st>>>(p);
+        else quant_rows_kernel<2, 1, 1, false, true><<<grid, 256, 0, st>>>(p);
+      }
+    } else if (layout == 0) {
       if (rnd == 0) quant_rows_kernel<2, 0, 0, false, false><<<grid, 256, 0, st>>>(p);
       else quant_rows_kernel<2, 0, 1, false, false><<<grid, 256, 0, st>>>(p);
     } else {
