@@ -435,7 +435,7 @@ snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_rou
 /* One pass that both quantizes x with blocks along cols (as snip_quantize_*
  * with the given layout, rounding and stream) and computes SNIP's statistics
  * of x under that same rounding and random bits (as snip_quant_stats): the
- * tensor is read once (E5M2: the statistics run in a second pass over it).  fmt selects the codes written
+ * tensor is read once.  fmt selects the codes written
  * (scales: the FP4 formats);
  * scales_in (device, nullable) = {amax, g, s} from snip_tensor_scales (NULL:
  * computed first); raw_out device SNIP_STATS_NVALS doubles.  Errors as for

@@ -174,24 +174,6 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   }
   // an empty output still publishes its tensor scale: the one-CTA row kernel does that
   if (p.orp == 0 || p.ocp == 0) orient = SNIP_BLOCKS_ALONG_COLS;
-  if (fmt == SNIP_FMT_FP8_E5M2 && raw_out) {
-    // E5M2 codes, then the statistics in their own pass (same rounding and random bits)
-    p.scales3 = nullptr;
-    p.raw_out = nullptr;
-    cudaError_t e = launch_quant(kernel_fmt(fmt), p, orient, layout, rnd, false, num_sms, st);
-    if (e != cudaSuccess) return cuda_status(e);
-    StatsParams sp = {};
-    sp.x = p.x;
-    sp.rows = rows;
-    sp.cols = cols;
-    sp.seed = seed;
-    sp.stream_id = stream_id;
-    sp.scales3 = scales3;
-    sp.partials = ws_at<double>(ws, kOffStatsPartials);
-    sp.counter = ws_at<uint32_t>(ws, kOffStatsCounter);
-    sp.raw_out = raw_out;
-    return cuda_status(launch_stats(sp, rnd, num_sms, st));
-  }
   return cuda_status(launch_quant(kernel_fmt(fmt), p, orient, layout, rnd, block_err != nullptr, num_sms, st));
 }
 

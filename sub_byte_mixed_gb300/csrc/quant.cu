@@ -311,7 +311,6 @@ template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS, bool LONG = false>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   static_assert(!LONG || (FMT == 1 && STATS), "LONG: NVFP4 with fused statistics");
   static_assert(FMT < 2 || !ERR, "MXFP4 / E5M2 quantization has no block errors");
-  static_assert(FMT != 3 || !STATS, "E5M2 quantization has no fused statistics");
   // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
   const float g = FMT == 3 ? e5m2_tensor_scale(*p.scale) : *p.scale;
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) *p.g_out = (FMT == 2 && !isnan(g)) ? 1.0f : g;
@@ -324,6 +323,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   const float six_g = __fmul_rn(6.0f, g4);
   const float inv8 = __frcp_rn(s8);
   const bool special8 = !(inv8 < kInf);
+  // E5M2 codes beside the statistics: the E5M2 tensor scale's inverse (without statistics, inv8)
+  const float inv5 = FMT == 3 && STATS ? __frcp_rn(g) : inv8;
   const uint32_t bpr = (uint32_t)(p.ocp >> 4);   // blocks per output row (padded)
   const uint32_t spr = (bpr + 31) >> 5;          // 32-block segments per row
   const uint32_t total = (uint32_t)p.orp * spr;
@@ -376,9 +377,9 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     }
     if (!longer && FMT != 2) bw = bs;
     uint4 c = make_uint4(0u, 0u, 0u, 0u);   // FP8: 16 codes; FP4: .x, .y
-    if (STATS && (longer || FMT == 2)) {
-      // statistics of the two candidate formats (16-element NVFP4, FP8); codes with the scale of the
-      // longer NVFP4 block or the MXFP4 block
+    if (STATS && (longer || FMT >= 2)) {
+      // statistics of the two candidate formats (16-element NVFP4, E4M3); codes with the scale of
+      // the longer NVFP4 block, of the MXFP4 block, or E5M2's tensor scale
       if (real) {
         const BlockStats st = stats_block16<-1, RND>(v, bs, u, s8, inv8, special8, c);
         sx2 += st.x2;
@@ -386,9 +387,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
         e8 += st.e8;
         v4 += st.v4;
         v8 += st.v8;
-        const uint2 e = nvfp4_encode16<RND>(v, bw, PackedBits{u});
-        c.x = e.x;
-        c.y = e.y;
+        if (FMT == 3) {
+          c = fp8_encode16<RND, true>(v, inv5, PackedBits{u});
+        } else {
+          const uint2 e = nvfp4_encode16<RND>(v, bw, PackedBits{u});
+          c.x = e.x;
+          c.y = e.y;
+        }
       }
     } else if (STATS) {
       // the codes come out of the statistics' own conversions
@@ -810,12 +815,22 @@ static void launch_quant_mx(const QuantParams& p, int orient, int layout, int rn
   }
 }
 
-// E5M2: no statistics or block errors either.
+// E5M2: no block errors either.
 static void launch_quant_e5(const QuantParams& p, int orient, int layout, int rnd, int num_sms, cudaStream_t st) {
   if (orient == 0) {
     const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
-    const int grid = fill_grid(segs, 8, 16 * num_sms);
-    if (layout == 0) {
+    const bool stats = p.raw_out != nullptr;
+    // with statistics, one partial slot per CTA: keep the grid within them
+    const int grid = fill_grid(segs, 8, stats ? 4 * num_sms : 16 * num_sms);
+    if (stats) {
+      if (layout == 0) {
+        if (rnd == 0) quant_rows_kernel<3, 0, 0, false, true><<<grid, 256, 0, st>>>(p);
+        else quant_rows_kernel<3, 0, 1, false, true><<<grid, 256, 0, st>>>(p);
+      } else {
+        if (rnd == 0) quant_rows_kernel<3, 1, 0, false, true><<<grid, 256, 0, st>>>(p);
+        else quant_rows_kernel<3, 1, 1, false, true><<<grid, 256, 0, st>>>(p);
+      }
+    } else if (layout == 0) {
       if (rnd == 0) quant_rows_kernel<3, 0, 0, false, false><<<grid, 256, 0, st>>>(p);
       else quant_rows_kernel<3, 0, 1, false, false><<<grid, 256, 0, st>>>(p);
     } else {

@@ -95,3 +95,18 @@ def test_qlinear_e5m2_gradients(snip, shape):
 def test_plan_rejects_operand_format(snip):
     with pytest.raises(snip.SnipError):
         snip.Plan([snip.FP8_E5M2], seed=0)
+
+
+@pytest.mark.parametrize("rnd", [0, 1])
+def test_e5m2_quantize_stats_fused(snip, rnd):
+    """E5M2 codes and SNIP's statistics of the candidate formats (NVFP4, E4M3) from one pass."""
+    x = inputs.normal_bf16((256, 768), 1e-3, 17, 1)
+    codes, _, raw = snip.quantize_stats(snip.FP8_E5M2, x.cuda(), rnd=rnd, seed=4, stream_id=10,
+                                        layout=snip.ROWMAJOR)
+    torch.cuda.synchronize()
+    ref = oracle.quantize_e5m2(x, rnd=rnd, seed=4, stream_id=10)
+    np.testing.assert_array_equal(codes.cpu().numpy().reshape(ref.codes.shape), ref.codes)
+    r = oracle.quant_stats(x, rnd=rnd, seed=4, stream_id=10)["raw"]
+    got = raw.cpu().numpy()
+    for k in range(7):
+        assert got[k] == pytest.approx(r[k], rel=STATS_REL, abs=1e-300), k
