@@ -781,7 +781,7 @@ static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int r
   }
 }
 
-// MXFP4: no statistics or block errors, so only those instantiations exist.
+// MXFP4: no block errors; row blocks with or without fused statistics.
 static void launch_quant_mx(const QuantParams& p, int orient, int layout, int rnd, int num_sms, cudaStream_t st) {
   if (orient == 0) {
     const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
