@@ -84,6 +84,14 @@ def lib():
         L.oracle_quantize_nvfp4.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp,
                                             c_u8p, c_u8p, c_fp, c_dp, ctypes.POINTER(ctypes.c_int64), i64]
         L.oracle_quantize_nvfp4.restype = i32
+        L.oracle_quantize_nvfp4_at.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp, u64,
+                                               c_u8p, c_u8p, c_fp, c_dp, ctypes.POINTER(ctypes.c_int64), i64]
+        L.oracle_quantize_nvfp4_at.restype = i32
+        L.oracle_quantize_fp8_at.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp, u64, c_u8p, c_fp,
+                                             ctypes.POINTER(ctypes.c_int64), i64]
+        L.oracle_quantize_fp8_at.restype = i32
+        L.oracle_quant_stats_at.argtypes = [c_u16p, i64, i64, i32, u64, u64, c_fp, c_fp, u64, c_dp, c_dp, c_dp]
+        L.oracle_quant_stats_at.restype = i32
         L.oracle_dequant_nvfp4.argtypes = [c_u8p, c_u8p, ctypes.c_float, i64, i64, c_dp]
         L.oracle_dequant_nvfp4.restype = None
         L.oracle_quantize_nvfp4_block.argtypes = [c_u16p, i64, i64, i32, i32, u64, u64, c_fp, i32,
@@ -282,11 +290,14 @@ def _selection(rows):
 
 
 def quantize_nvfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0,
-                   g_in: float | None = None, want_block_err: bool = False, rows=None) -> NVFP4:
+                   g_in: float | None = None, want_block_err: bool = False, rows=None,
+                   index_base: int = 0) -> NVFP4:
     """NVFP4 quantization of a bf16 (rows, cols) tensor; orient=1 quantizes the
     transpose with blocks along the original rows (random bits still indexed
     by the source element).  rows (optional): compute only these output rows
-    (tensor scale and random bits as for the whole tensor)."""
+    (tensor scale and random bits as for the whole tensor).  index_base: x is
+    the part of a larger row-major tensor that starts at that element (random
+    bits as for the larger tensor; pass its tensor scale as g_in)."""
     b = _bits(x)
     sel, psel, nsel = _selection(rows)
     rows, cols = b.shape
@@ -299,8 +310,8 @@ def quantize_nvfp4(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id:
     berr = np.zeros((OR, OC // 16), dtype=np.float64) if want_block_err else None
     g = ctypes.c_float()
     gin = ctypes.byref(ctypes.c_float(g_in)) if g_in is not None else None
-    st = lib().oracle_quantize_nvfp4(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
-                                     gin, _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+    st = lib().oracle_quantize_nvfp4_at(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
+                                     gin, index_base, _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
                                      ctypes.byref(g),
                                      _ptr(berr, ctypes.c_double) if berr is not None else None, psel, nsel)
     if st == 1:
@@ -338,7 +349,8 @@ def quantize_nvfp4_block(x, block: int, orient: int = 0, rnd: int = RTN, seed: i
 
 
 def quantize_fp8(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: int = 0,
-                 s_in: float | None = None, rows=None) -> FP8:
+                 s_in: float | None = None, rows=None, index_base: int = 0) -> FP8:
+    """E4M3 with one tensor scale; orientation, rows and index_base as for quantize_nvfp4."""
     b = _bits(x)
     sel, psel, nsel = _selection(rows)
     rows, cols = b.shape
@@ -349,8 +361,8 @@ def quantize_fp8(x, orient: int = 0, rnd: int = RTN, seed: int = 0, stream_id: i
     codes = np.zeros((OR, OC), dtype=np.uint8)
     s = ctypes.c_float()
     sin = ctypes.byref(ctypes.c_float(s_in)) if s_in is not None else None
-    st = lib().oracle_quantize_fp8(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
-                                   sin, _ptr(codes, ctypes.c_uint8), ctypes.byref(s), psel, nsel)
+    st = lib().oracle_quantize_fp8_at(_ptr(b, ctypes.c_uint16), rows, cols, orient, rnd, seed, stream_id,
+                                      sin, index_base, _ptr(codes, ctypes.c_uint8), ctypes.byref(s), psel, nsel)
     if st == 1:
         raise NonFiniteInput("non-finite input")
     return FP8(codes, s.value, OR, OC)
@@ -479,18 +491,22 @@ def dw_noise(X, dY, dW_q):
 
 # ----------------------------------------------------------------------------- statistics
 
-def quant_stats(x, rnd=RTN, seed=0, stream_id=0, want_block_err=False):
+def quant_stats(x, rnd=RTN, seed=0, stream_id=0, want_block_err=False, g_in=None, s_in=None, index_base=0):
     """SNIP statistics of one tensor: raw sums (ST_* slots) plus derived ratios.
     ratio_f = ||A|| / ||Q_f(A) - A||, below_sqrt3_f = ratio_f < sqrt(3) ("FP4 all
     the way", Outline: quantized learning loses efficiency when the gradient
-    norm falls below ~sqrt(3) x the quantization noise)."""
+    norm falls below ~sqrt(3) x the quantization noise).  For a part of a larger
+    tensor: g_in / s_in its tensor scales and index_base the part's first
+    element (the raw sums of the parts add up to the tensor's)."""
     b = _bits(x)
     rows, cols = b.shape
     raw = np.zeros(ST_N, dtype=np.float64)
     be4 = np.zeros((rows, cols // 16), dtype=np.float64) if want_block_err else None
     be8 = np.zeros((rows, cols // 16), dtype=np.float64) if want_block_err else None
-    st = lib().oracle_quant_stats(_ptr(b, ctypes.c_uint16), rows, cols, rnd, seed, stream_id,
-                                  _ptr(raw, ctypes.c_double),
+    gin = ctypes.byref(ctypes.c_float(g_in)) if g_in is not None else None
+    sin = ctypes.byref(ctypes.c_float(s_in)) if s_in is not None else None
+    st = lib().oracle_quant_stats_at(_ptr(b, ctypes.c_uint16), rows, cols, rnd, seed, stream_id, gin, sin,
+                                     index_base, _ptr(raw, ctypes.c_double),
                                   _ptr(be4, ctypes.c_double) if be4 is not None else None,
                                   _ptr(be8, ctypes.c_double) if be8 is not None else None)
     if st == 1:

@@ -310,10 +310,27 @@ float oracle_nvfp4_global_scale(float amax) {
  *                each element's index in it); outputs then have n_sel rows.
  * Returns 0, or 1 if the input holds a non-finite value (outputs untouched),
  * or 2 on a shape error. */
+int oracle_quantize_nvfp4_at(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
+                             uint64_t seed, uint64_t stream_id, const float* g_in, uint64_t index_base,
+                             uint8_t* codes, uint8_t* scales, float* g_out, double* block_sqerr,
+                             const int64_t* sel, int64_t n_sel);
 int oracle_quantize_nvfp4(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
                           uint64_t seed, uint64_t stream_id, const float* g_in,
                           uint8_t* codes, uint8_t* scales, float* g_out, double* block_sqerr,
                           const int64_t* sel, int64_t n_sel) {
+    return oracle_quantize_nvfp4_at(x, rows, cols, orient, rnd, seed, stream_id, g_in, 0, codes, scales, g_out,
+                                    block_sqerr, sel, n_sel);
+}
+
+/* The same, for x holding a part of a larger row-major tensor that starts at
+ * element index_base of it (a shard of whole rows, index_base = first row *
+ * cols): every element draws the random bits of its index in the whole tensor
+ * (R6), so the shards of a tensor quantize exactly as the tensor does when
+ * they share its tensor scale (g_in). */
+int oracle_quantize_nvfp4_at(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
+                             uint64_t seed, uint64_t stream_id, const float* g_in, uint64_t index_base,
+                             uint8_t* codes, uint8_t* scales, float* g_out, double* block_sqerr,
+                             const int64_t* sel, int64_t n_sel) {
     int64_t OR = orient == 0 ? rows : cols, OC = orient == 0 ? cols : rows;
     if (OC % 16 != 0) return 2;
     float amax;
@@ -348,7 +365,7 @@ int oracle_quantize_nvfp4(const uint16_t* x, int64_t rows, int64_t cols, int ori
                     float inv = 1.0f / p;
                     float y = fabsf(xs[k]) * inv;
                     mag = rnd == 0 ? oracle_e2m1_rtn(y)
-                                   : oracle_e2m1_sr(y, oracle_sr_bits(seed, stream_id, es[k]));
+                                   : oracle_e2m1_sr(y, oracle_sr_bits(seed, stream_id, index_base + es[k]));
                 }
                 int code = sign | mag;
                 int64_t col = b * 16 + k;
@@ -547,9 +564,20 @@ float oracle_fp8_tensor_scale(float amax) {
 /* Quantize a bf16 rows x cols tensor to E4M3 codes with one tensor scale s
  * (x ~ code * s).  Orientation, rounding and return values as for NVFP4;
  * codes is OR x OC bytes; sel, n_sel as for NVFP4. */
+int oracle_quantize_fp8_at(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
+                           uint64_t seed, uint64_t stream_id, const float* s_in, uint64_t index_base,
+                           uint8_t* codes, float* s_out, const int64_t* sel, int64_t n_sel);
 int oracle_quantize_fp8(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
                         uint64_t seed, uint64_t stream_id, const float* s_in,
                         uint8_t* codes, float* s_out, const int64_t* sel, int64_t n_sel) {
+    return oracle_quantize_fp8_at(x, rows, cols, orient, rnd, seed, stream_id, s_in, 0, codes, s_out, sel, n_sel);
+}
+
+/* The same for a part of a larger tensor starting at element index_base of it
+ * (as oracle_quantize_nvfp4_at). */
+int oracle_quantize_fp8_at(const uint16_t* x, int64_t rows, int64_t cols, int orient, int rnd,
+                           uint64_t seed, uint64_t stream_id, const float* s_in, uint64_t index_base,
+                           uint8_t* codes, float* s_out, const int64_t* sel, int64_t n_sel) {
     int64_t OR = orient == 0 ? rows : cols, OC = orient == 0 ? cols : rows;
     float amax;
     if (oracle_amax_bf16(x, rows * cols, &amax)) return 1;
@@ -567,7 +595,7 @@ int oracle_quantize_fp8(const uint16_t* x, int64_t rows, int64_t cols, int orien
             if (xv != 0.0f) {
                 float y = fabsf(xv) * inv;
                 mag = rnd == 0 ? oracle_e4m3_rtn(y)
-                               : oracle_e4m3_sr(y, oracle_sr_bits(seed, stream_id, e));
+                               : oracle_e4m3_sr(y, oracle_sr_bits(seed, stream_id, index_base + e));
             }
             codes[ii * OC + k] = (uint8_t)(sign | mag);
         }
@@ -653,9 +681,23 @@ static void e4m3_bracket(float y, double* lo, double* hi) {
  * out[ST_N] receives the raw sums; block_err_nvfp4 / block_err_fp8
  * (nullable, rows x cols/16) receive per-block squared errors.
  * Returns 0, 1 for non-finite input, 2 for a shape error. */
+int oracle_quant_stats_at(const uint16_t* x, int64_t rows, int64_t cols, int rnd, uint64_t seed,
+                          uint64_t stream_id, const float* g_in, const float* s_in, uint64_t index_base,
+                          double* out, double* block_err_nvfp4, double* block_err_fp8);
 int oracle_quant_stats(const uint16_t* x, int64_t rows, int64_t cols, int rnd,
                        uint64_t seed, uint64_t stream_id, double* out,
                        double* block_err_nvfp4, double* block_err_fp8) {
+    return oracle_quant_stats_at(x, rows, cols, rnd, seed, stream_id, NULL, NULL, 0, out, block_err_nvfp4,
+                                 block_err_fp8);
+}
+
+/* The statistics of a part of a larger tensor (rows starting at element
+ * index_base of it) under the whole tensor's scales g_in, s_in (NULL: this
+ * part's own): the sums of the parts are the whole tensor's; out[ST_AMAX] is
+ * this part's amax (the whole tensor's is their maximum). */
+int oracle_quant_stats_at(const uint16_t* x, int64_t rows, int64_t cols, int rnd, uint64_t seed,
+                          uint64_t stream_id, const float* g_in, const float* s_in, uint64_t index_base,
+                          double* out, double* block_err_nvfp4, double* block_err_fp8) {
     if (cols % 16 != 0) return 2;
     int64_t n = rows * cols;
     uint8_t* c4 = (uint8_t*)calloc((size_t)(n / 2 + 1), 1);
@@ -664,8 +706,10 @@ int oracle_quant_stats(const uint16_t* x, int64_t rows, int64_t cols, int rnd,
     double* bl4 = (double*)calloc((size_t)(n / 16 + 1), sizeof(double));
     if (!c4 || !s4 || !c8 || !bl4) { free(c4); free(s4); free(c8); free(bl4); return 3; }
     float g, s;
-    int st = oracle_quantize_nvfp4(x, rows, cols, 0, rnd, seed, stream_id, NULL, c4, s4, &g, bl4, NULL, 0);
-    if (st == 0) st = oracle_quantize_fp8(x, rows, cols, 0, rnd, seed, stream_id, NULL, c8, &s, NULL, 0);
+    int st = oracle_quantize_nvfp4_at(x, rows, cols, 0, rnd, seed, stream_id, g_in, index_base, c4, s4, &g, bl4,
+                                      NULL, 0);
+    if (st == 0)
+        st = oracle_quantize_fp8_at(x, rows, cols, 0, rnd, seed, stream_id, s_in, index_base, c8, &s, NULL, 0);
     if (st != 0) { free(c4); free(s4); free(c8); free(bl4); return st; }
     for (int k = 0; k < ST_N; ++k) out[k] = 0.0;
     float amax;
