@@ -307,6 +307,27 @@ snip_status snip_quantize_e5m2(const void* x, int64_t rows, int64_t cols, snip_o
                                snip_layout layout, uint8_t* codes, float* s_out,
                                void* ws, size_t ws_bytes, void* stream);
 
+/* Quantization of a part of a larger tensor, for a layer split by tokens
+ * across devices (SNIP, Figure 5: every operand of the layer quantized along
+ * its contraction dim; a token shard of X or dY is a block of whole rows):
+ * x holds rows x cols of a row-major tensor starting at its element
+ * index_base (first row * cols, a multiple of 16, else SNIP_ERR_SHAPE).  It is
+ * quantized as fmt (an operand format) with the whole tensor's scales
+ * scales_in (device, {amax, g, s} as snip_tensor_scales writes them for the
+ * whole tensor, e.g. from a MAX all-reduce of the parts' amax), and every
+ * element draws the random bits of its index in the whole tensor ("FP4 all
+ * the way", Outline: SR; the bits of element e are those of R6), so the codes
+ * equal the whole tensor's quantization's output rows (ALONG_COLS) or columns
+ * (ALONG_ROWS, the part's rows a whole number of blocks).  raw_out (device,
+ * nullable, ALONG_COLS only): SNIP's statistics of this part under those
+ * scales, in the same pass; the parts' sums add up to the whole tensor's
+ * (SNIP_ST_AMAX: take the maximum).  Other arguments and errors as for
+ * snip_quantize_nvfp4 / snip_quantize_stats. */
+snip_status snip_quantize_part(snip_format fmt, const void* x, int64_t rows, int64_t cols, snip_orient orient,
+                               snip_round rnd, uint64_t seed, uint64_t stream_id, uint64_t index_base,
+                               const float* scales_in, snip_layout layout, uint8_t* codes, uint8_t* scales,
+                               double* raw_out, void* ws, size_t ws_bytes, void* stream);
+
 /* Bytes of the code and scale buffers of a quantization whose output has
  * out_rows rows and contraction out_cols, in `layout`.  Host-only. */
 snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t out_rows, int64_t out_cols,

@@ -149,8 +149,9 @@ snip_status run_scales_multi(int count, const void* const* xs, const int64_t* ns
 snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int orient, int rnd, uint64_t seed,
                          uint64_t stream_id, const float* scale, int layout, uint8_t* codes, uint8_t* scales,
                          float* g_out, float* block_err, int num_sms, cudaStream_t st, const float* scales3 = nullptr,
-                         double* raw_out = nullptr, void* ws = nullptr) {
+                         double* raw_out = nullptr, void* ws = nullptr, uint64_t index_base = 0) {
   QuantParams p = {};
+  p.index_base = index_base;
   p.x = static_cast<const uint16_t*>(x);
   p.rows = rows;
   p.cols = cols;
@@ -713,6 +714,25 @@ snip_status snip_quantize_stats(snip_format fmt, const void* x, int64_t rows, in
   }
   return run_quantize(fmt, x, rows, cols, SNIP_BLOCKS_ALONG_COLS, rnd, seed, stream_id, sc + scale_index(fmt), layout,
                       codes, scales, nullptr, nullptr, sms, st, sc, raw_out, ws);
+}
+
+snip_status snip_quantize_part(snip_format fmt, const void* x, int64_t rows, int64_t cols, snip_orient orient,
+                               snip_round rnd, uint64_t seed, uint64_t stream_id, uint64_t index_base,
+                               const float* scales_in, snip_layout layout, uint8_t* codes, uint8_t* scales,
+                               double* raw_out, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if (!valid_operand_fmt(fmt) || !scales_in || (raw_out && orient != SNIP_BLOCKS_ALONG_COLS))
+    return SNIP_ERR_INVALID_ARG;
+  if (index_base % 16 != 0) return SNIP_ERR_SHAPE;
+  float g_dummy;   // validation only: the scales come in, none is written
+  s = check_quantize_args(fmt, x, rows, cols, orient, rnd, layout, codes, is_fp4(fmt) ? scales : nullptr, &g_dummy,
+                          ws, ws_bytes);
+  if (s != SNIP_OK) return s;
+  return run_quantize(fmt, x, rows, cols, orient, rnd, seed, stream_id, scales_in + scale_index(fmt), layout, codes,
+                      is_fp4(fmt) ? scales : nullptr, nullptr, nullptr, sms, static_cast<cudaStream_t>(stream),
+                      raw_out ? scales_in : nullptr, raw_out, ws, index_base);
 }
 
 // ---------------------------------------------------------------- NEXT-4: dW-level sqrt(3) check

@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     float v[16];
     unpack16(a, b, v);
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (RND == 1 && real) sr_bits16(e0, p.seed, p.stream_id, u);
+    if (RND == 1 && real) sr_bits16(e0 + (int64_t)p.index_base, p.seed, p.stream_id, u);
     // bs: the 16-element NVFP4 scale (codes, and the statistics' NVFP4 candidate); bw: the scale
     // the codes are written with -- bs, or with longer blocks the scale of p.group 16-element blocks
     BlockScale bs, bw;
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
     *reinterpret_cast<uint4*>(&xs[row][ch * 4]) = v;
     if (RND == 1) {
       U4 w = make_zero_u4();
-      if (in) w = sr_words((uint64_t)(gr * p.cols + gc) >> 3, p.seed, p.stream_id);
+      if (in) w = sr_words(((uint64_t)(gr * p.cols + gc) + p.index_base) >> 3, p.seed, p.stream_id);
       *reinterpret_cast<uint4*>(&rs[row][ch * 4]) = make_uint4(w.x, w.y, w.z, w.w);
     }
   }

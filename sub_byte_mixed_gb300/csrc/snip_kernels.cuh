@@ -23,6 +23,8 @@ struct QuantParams {
   float* block_err;             // NVFP4 only, nullable
   int group;                    // NVFP4: 16-element blocks sharing one scale (0 or 1: NVFP4;
                                 // 2, 4, 8: 32-, 64-, 128-element blocks)
+  uint64_t index_base;          // x is a part of a larger tensor starting at this element (a
+                                // multiple of 16): random bits follow the whole tensor's indices
   // statistics fused into a row-block quantization (raw_out non-null)
   const float* scales3;         // {amax, NVFP4 g, FP8 s}
   double* partials;

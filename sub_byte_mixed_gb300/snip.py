@@ -33,7 +33,7 @@ EXPORTS = (
     "snip_status_string", "snip_version", "snip_device_check", "snip_workspace_init", "snip_workspace_status",
     "snip_quantize_workspace_size", "snip_amax", "snip_tensor_scales", "snip_tensor_scales_multi",
     "snip_tensor_scales_noalloc",
-    "snip_wait_check", "snip_quantize_nvfp4", "snip_quantize_nvfp4_block", "snip_quantize_fp8", "snip_quantize_mxfp4",
+    "snip_wait_check", "snip_quantize_part", "snip_quantize_nvfp4", "snip_quantize_nvfp4_block", "snip_quantize_fp8", "snip_quantize_mxfp4",
     "snip_quantize_e5m2",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_tensor_scales_noalloc": (i32, [vp, i64, vp, vp]),
         "snip_tensor_scales_multi": (i32, [i32, vp, vp, vp, vp, sz, vp]),
         "snip_wait_check": (i32, [u64, vp, vp, sz, vp]),
+        "snip_quantize_part": (i32, [i32, vp, i64, i64, i32, i32, u64, u64, u64, vp, i32, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_nvfp4": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
         "snip_quantize_nvfp4_block": (i32, [vp, i64, i64, i32, i32, u64, u64, vp, i32, i32, vp, vp, vp, vp, sz,
                                             vp]),
@@ -170,6 +171,30 @@ def snip_quantize_nvfp4(x, rows, cols, orient, rnd, seed, stream_id, g_in, layou
                         block_sqerr, ws, ws_bytes, stream):
     _call("snip_quantize_nvfp4", x, rows, cols, orient, rnd, seed, stream_id, g_in, layout, codes, scales, g_out,
           block_sqerr, ws, ws_bytes, stream)
+
+
+def snip_quantize_part(fmt, x, rows, cols, orient, rnd, seed, stream_id, index_base, scales_in, layout, codes,
+                       scales, raw_out, ws, ws_bytes, stream):
+    _call("snip_quantize_part", fmt, x, rows, cols, orient, rnd, seed, stream_id, index_base, scales_in, layout,
+          codes, scales, raw_out, ws, ws_bytes, stream)
+
+
+def quantize_part(fmt, x, index_base, scales_in, orient=ALONG_COLS, rnd=RTN, seed=0, stream_id=0, layout=ROWMAJOR,
+                  stats=False, ws: Workspace | None = None):
+    """Quantize x, a part of a larger tensor starting at its element index_base, with the whole
+    tensor's scales (device {amax, g, s}) -> (codes, scales or None, raw statistics or None)."""
+    torch = _torch()
+    ws = ws or small_workspace()
+    rows, cols = x.shape
+    orows, ocols = (rows, cols) if orient == ALONG_COLS else (cols, rows)
+    cb, sb = snip_quantized_bytes(fmt, layout, orows, ocols)
+    codes = torch.empty(max(cb, 16), dtype=torch.uint8, device=x.device)
+    fp4 = fmt in NVFP4_BLOCK or fmt == MXFP4
+    sc = torch.empty(max(sb, 16), dtype=torch.uint8, device=x.device) if fp4 else None
+    raw = torch.empty(STATS_NVALS, dtype=torch.float64, device=x.device) if stats else None
+    snip_quantize_part(fmt, x.data_ptr(), rows, cols, orient, rnd, seed, stream_id, index_base, scales_in.data_ptr(),
+                       layout, codes.data_ptr(), _ptr(sc), _ptr(raw), ws.ptr, ws.nbytes, _stream())
+    return codes[:cb], (sc[:sb] if fp4 else None), raw
 
 
 def snip_wait_check(limit_ns, out, ws, ws_bytes, stream):
