@@ -556,7 +556,7 @@ def requant_compare(snip, reps: int = 10):
     return out
 
 
-def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
+def e2e_run(cfg, plan, snip, step: Step, nsteps: int, rounds_n: int = 5):
     """The same step through the layer API (snip_qlinear_fwd / _bwd, statistics fused into their
     quantizations) with host buffers: every step copies all inputs (X, W, dY, bf16) in from pinned host
     memory and reads the step's metric -- SNIP's statistics of every operand tensor -- back to the host,
@@ -634,20 +634,29 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
         one()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(sC)
-    sH.wait_event(e0)
-    sD.wait_event(e0)
-    sCs[1].wait_event(e0)
-    for _ in range(nsteps):
-        one()
-    for j in range(n):
-        sC.wait_event(state["drained"][j])
-    e1.record(sC)
-    torch.cuda.synchronize()
+    # several rounds of nsteps, the median reported: a round now and then runs about twice as long
+    # (the host-driven step leaves the GPU waiting on copies); the clocks are sampled meanwhile
+    sampler = ClockSampler(torch.cuda.current_device())
+    t_start = time.time()
+    rounds = []
+    for _ in range(rounds_n):
+        e0.record(sC)
+        sH.wait_event(e0)
+        sD.wait_event(e0)
+        sCs[1].wait_event(e0)
+        for _ in range(nsteps):
+            one()
+        for j in range(n):
+            sC.wait_event(state["drained"][j])
+        e1.record(sC)
+        torch.cuda.synchronize()
+        rounds.append(e0.elapsed_time(e1) / nsteps)
+    clocks = sampler.summary(t_start, time.time())
+    sampler.stop()
     for ws in wss:
         if ws.status() != snip.SNIP_OK:
             raise RuntimeError("device status " + snip.status_string(ws.status()))
-    ms = e0.elapsed_time(e1) / nsteps
+    ms = sorted(rounds)[len(rounds) // 2]
     # the host->device copies of one step alone, for the bound they put on the step
     torch.cuda.synchronize()
     e0.record(sH)
@@ -664,6 +673,8 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int):
     return {"value": cfg.flops_fwd_bwd() / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "h2d_only_ms_per_step": ms_h2d,
             "h2d_gbs": h2d / (ms_h2d * 1e-3) / 1e9,
+            "rounds_ms_per_step": [round(r, 3) for r in rounds], "timing": f"median of {rounds_n} rounds of {nsteps} steps",
+            "clocks": clocks,
             "path": "snip_qlinear_fwd/bwd with fused statistics; all inputs copied in from pinned host memory "
                     "and the step's SNIP statistics read back every step, overlapping other linears' calls "
                     "(copy-in, two layer-call and copy-out streams); Y, dX, dW stay on the device"}
