@@ -153,7 +153,11 @@ typedef struct snip_plan snip_plan;
 /* Text of a status code (static storage). */
 const char* snip_status_string(snip_status s);
 
-/* ABI version (major*10000 + minor*100 + patch). */
+/* ABI version (major*10000 + minor*100 + patch) of this header; snip_version()
+ * returns the library's, which must match.  0.2.0: snip_requant gained the
+ * column-block fields (NEXT-3), the longer-block NVFP4 formats,
+ * snip_quantize_part and snip_wait_check. */
+#define SNIP_ABI_VERSION 200
 int snip_version(void);
 
 /* SNIP_OK if the current CUDA device can run the kernels (compute capability

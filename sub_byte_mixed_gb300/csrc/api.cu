@@ -277,7 +277,7 @@ const char* snip_status_string(snip_status s) {
   return "unknown status";
 }
 
-int snip_version(void) { return 100; }
+int snip_version(void) { return SNIP_ABI_VERSION; }
 
 snip_status snip_device_check(void) { return current_device(nullptr); }
 

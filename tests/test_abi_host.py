@@ -97,3 +97,12 @@ def test_calls_without_usable_gpu_fail_loudly(snip):
     assert snip.load().snip_device_check() in (snip.SNIP_ERR_CUDA, snip.SNIP_ERR_UNSUPPORTED_DEVICE)
     st = snip.load().snip_amax(16, 8, 16, 16, 1 << 20, None)
     assert st in (snip.SNIP_ERR_CUDA, snip.SNIP_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_library_reports_the_header_version():
+    """snip_version() (no device needed) matches SNIP_ABI_VERSION in include/snip.h."""
+    import re
+    from sub_byte_mixed_gb300 import snip
+    hdr = open(os.path.join(ROOT, "include", "snip.h")).read()
+    want = int(re.search(r"#define SNIP_ABI_VERSION (\d+)", hdr).group(1))
+    assert snip.load().snip_version() == want
