@@ -113,32 +113,94 @@ def config_json(cfg, plan, args):
 
 # ----------------------------------------------------------------------------- CPU baseline (oracle)
 
-def cpu_sample(seconds: float):
-    """Time the oracle on a bounded sample of the workload: the Q linear of the
-    7B block (K = N = 4096) restricted to 256 tokens and 512 output features,
-    forward + dgrad + wgrad in NVFP4 plus the statistics of X, W and dY.
-    Repeats until `seconds` have passed; returns TFLOP/s of the sample."""
-    import numpy as np  # noqa: F401  (thread count fixed by the environment)
+# The bounded sample: the Q linear of the 7B block (K = N = 4096) restricted to 256 tokens and 512
+# output features, forward + dgrad + wgrad in NVFP4 plus the statistics of X, W and dY.
+SAMPLE_T, SAMPLE_K, SAMPLE_N = 256, 4096, 512
+SAMPLE_FLOPS = 6 * SAMPLE_T * SAMPLE_K * SAMPLE_N
+SAMPLE_TEXT = "Q linear of the 7B block cut to T=256, N=512 (K=4096), NVFP4 fwd+dgrad+wgrad+stats"
+_worker = {}
+
+
+def _oracle_worker_init():
+    """Pool worker (spawned, one thread of BLAS): the oracle and the sample's inputs, once."""
     import oracle
     from sub_byte_mixed_gb300 import inputs
-    T, K, N = 256, 4096, 512
-    X, W, dY = inputs.single_linear_inputs(T, K, N, seed=0)
-    flops = 6 * T * K * N
     oracle.build()
-    n, t0 = 0, time.perf_counter()
-    while True:
-        oracle.qlinear_fwd("nvfp4", X, W)
-        oracle.qlinear_dgrad("nvfp4", dY, W)
-        oracle.qlinear_wgrad("nvfp4", dY, X)
-        for t, r in ((X, 0), (W, 0), (dY, 1)):
-            oracle.quant_stats(t, rnd=r, seed=0, stream_id=2)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": flops * n / el / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"Q linear of the 7B block cut to T=256, N=512 (K=4096), NVFP4 fwd+dgrad+wgrad+stats, "
-                      f"{n} repetitions in {el:.1f} s, single thread"}
+    _worker["linear"] = inputs.single_linear_inputs(SAMPLE_T, SAMPLE_K, SAMPLE_N, seed=0)
+
+
+def _oracle_sample_rep(_=None) -> float:
+    """One repetition of the bounded sample in this worker; returns its seconds."""
+    import oracle
+    X, W, dY = _worker["linear"]
+    t0 = time.perf_counter()
+    oracle.qlinear_fwd("nvfp4", X, W)
+    oracle.qlinear_dgrad("nvfp4", dY, W)
+    oracle.qlinear_wgrad("nvfp4", dY, X)
+    for t, r in ((X, 0), (W, 0), (dY, 1)):
+        oracle.quant_stats(t, rnd=r, seed=0, stream_id=2)
+    return time.perf_counter() - t0
+
+
+def _oracle_quant_rows(args) -> float:
+    """NVFP4 row-block quantization (round to nearest) and SNIP's statistics of rows [r0, r1) of the
+    7B block's Q-linear activation X (8192 x 4096) under the whole tensor's scales; returns seconds."""
+    import oracle
+    from sub_byte_mixed_gb300 import inputs
+    r0, r1, g, s8 = args
+    if "x" not in _worker:
+        _worker["x"] = oracle._bits(inputs.linear_inputs(inputs.LLAMA7B, 0, seed=0)[0])
+    part = _worker["x"][r0:r1]
+    t0 = time.perf_counter()
+    oracle.quantize_nvfp4(part, 0, 0, 0, 0, g_in=g)
+    oracle.quant_stats(part, rnd=0, seed=0, stream_id=0, g_in=g, s_in=s8, index_base=r0 * part.shape[1])
+    return time.perf_counter() - t0
+
+
+def oracle_pool(n: int):
+    """n spawned worker processes for the oracle (spawn: safe in a process that may hold a CUDA context)."""
+    import multiprocessing as mp
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    os.environ["CUDA_VISIBLE_DEVICES"] = ""
+    return mp.get_context("spawn").Pool(n, initializer=_oracle_worker_init)
+
+
+def cpu_sample(seconds: float):
+    """The oracle on every host core: one spawned worker per core, each repeating the bounded sample
+    until `seconds` have passed, their flops summed over the wall time; then the quantizer and
+    statistics on the full X of the same linear (8192 x 4096), its rows split over the workers."""
+    import oracle
+    from sub_byte_mixed_gb300 import inputs
+    n = os.cpu_count() or 1
+    with oracle_pool(n) as pool:
+        pool.map(_oracle_sample_rep, range(n))            # first use: page in, build caches
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            pool.map(_oracle_sample_rep, range(n))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        # full-tensor quantizer + statistics, whole-tensor scales from the oracle's own amax
+        oracle.build()
+        X = inputs.linear_inputs(inputs.LLAMA7B, 0, seed=0)[0]
+        am = oracle.amax(X)
+        g, s8 = oracle.nvfp4_global_scale(am), oracle.fp8_tensor_scale(am)
+        R, C = X.shape
+        step = (R + n - 1) // n
+        parts = [(r0, min(R, r0 + step), g, s8) for r0 in range(0, R, step)]
+        pool.map(_oracle_quant_rows, [(0, 1, g, s8)] * n)  # each worker generates X once
+        tq = time.perf_counter()
+        pool.map(_oracle_quant_rows, parts)
+        tq = time.perf_counter() - tq
+    return {"value": SAMPLE_FLOPS * n * reps / el / 1e12, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{SAMPLE_TEXT}; {n} worker processes (one per host core, one BLAS thread each) "
+                      f"repeating it, {n * reps} repetitions in {el:.1f} s",
+            "quantizer": {"value": (2 + 0.5 + 1 / 16) * R * C / tq / 1e9, "unit": "GB/s",
+                          "sample": f"NVFP4 row-block RTN quantization + SNIP statistics of the full 7B Q-linear X "
+                                    f"({R}x{C} bf16), rows split over {n} workers, {tq:.2f} s; bytes counted "
+                                    f"as the GPU quantizer's (read + codes + scales)"}}
 
 
 def run_cpu_baseline_subprocess(seconds: float):
@@ -149,7 +211,8 @@ def run_cpu_baseline_subprocess(seconds: float):
     for line in r.stdout.splitlines()[::-1]:
         if line.startswith("{"):
             return json.loads(line)
-    return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+    return {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "failed: " + r.stderr[-300:]}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -556,12 +619,13 @@ def requant_compare(snip, reps: int = 10):
     return out
 
 
-def e2e_run(cfg, plan, snip, step: Step, nsteps: int, rounds_n: int = 5):
+def e2e_run(cfg, plan, snip, step: Step, nsteps: int, rounds_n: int = 5, with_outputs: bool = False):
     """The same step through the layer API (snip_qlinear_fwd / _bwd, statistics fused into their
     quantizations) with host buffers: every step copies all inputs (X, W, dY, bf16) in from pinned host
     memory and reads the step's metric -- SNIP's statistics of every operand tensor -- back to the host,
     inside the timed region.  Y, dX and dW stay on the device, where the next layer, the previous layer
-    and the optimizer consume them."""
+    and the optimizer consume them; with_outputs: they are copied back to pinned host memory too, every
+    step (host to host)."""
     import torch
     inp = step.inp
     hX = {k: v.cpu().pin_memory() for k, v in inp.X.items()}
@@ -575,6 +639,10 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int, rounds_n: int = 5):
     wss = [snip.Workspace(wsb), snip.Workspace(wsb)]
     h2d = sum(t.numel() * t.element_size() for t in list(hX.values()) + hW + hdY)
     d2h = hraw.numel() * 8
+    if with_outputs:
+        hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (step.Y[j], step.dX[j], step.dW[j])]
+                for j in range(len(cfg.linears))]
+        d2h += sum(t.numel() * t.element_size() for ts in hout for t in ts)
 
     # Three streams: host->device copies (H), the layer calls (C), device->host copies (D).  Linear j's
     # inputs are copied while earlier linears compute, and its statistics read back while later ones do;
@@ -626,6 +694,9 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int, rounds_n: int = 5):
             with torch.cuda.stream(sD):
                 sD.wait_event(done)
                 hraw[j].copy_(step.raw[j], non_blocking=True)
+                if with_outputs:
+                    for h, d in zip(hout[j], (step.Y[j], step.dX[j], step.dW[j])):
+                        h.copy_(d, non_blocking=True)
                 dr = ev()
                 dr.record(sD)
                 state["drained"][j] = dr
@@ -677,7 +748,9 @@ def e2e_run(cfg, plan, snip, step: Step, nsteps: int, rounds_n: int = 5):
             "clocks": clocks,
             "path": "snip_qlinear_fwd/bwd with fused statistics; all inputs copied in from pinned host memory "
                     "and the step's SNIP statistics read back every step, overlapping other linears' calls "
-                    "(copy-in, two layer-call and copy-out streams); Y, dX, dW stay on the device"}
+                    "(copy-in, two layer-call and copy-out streams); "
+                    + ("Y, dX, dW (fp32) copied back to pinned host memory every step as well"
+                       if with_outputs else "Y, dX, dW stay on the device")}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -808,9 +881,10 @@ def run_ours(args, rank, world, local_rank):
     if not args.profile_run and not layers and rank == 0:
         qsweep = quantizer_sweep(snip, measured_peaks()["hbm_gbs"])
         rqcmp = requant_compare(snip)
-    e2e = None
+    e2e = e2e_out = None
     if not args.no_e2e and not args.profile_run and not layers and rank == 0:
         e2e = e2e_run(cfg, plan, snip, step, args.e2e_steps)
+        e2e_out = e2e_run(cfg, plan, snip, step, max(2, args.e2e_steps // 2), rounds_n=3, with_outputs=True)
     if rank != 0:
         return
     flops = cfg.flops_fwd_bwd() if not layers else sum(
@@ -821,10 +895,15 @@ def run_ours(args, rank, world, local_rank):
     for cat in cat_ms:
         t = cat_ms[cat] / 1e3
         if cat.startswith("gemm"):
+            # each launch is timed alone on the GPU (serial pass): the burst bf16 figure x the nominal
+            # dense ratio is its peak; the sustained-derived fraction is kept beside it
+            ratio = FP8_OVER_BF16 if cat == "gemm_fp8" else FP4_OVER_BF16
             ach = cat_units[cat] / t / 1e12
-            pk = peaks["bf16_sustained"] * (FP8_OVER_BF16 if cat == "gemm_fp8" else FP4_OVER_BF16)
+            pk = peaks["bf16"] * ratio
+            pks = peaks["bf16_sustained"] * ratio
             breakdown[cat] = {"ms_per_step": cat_ms[cat] / args.steps, "launches_per_step": cat_n[cat] // args.steps,
-                              "achieved": ach, "unit": "TFLOP/s", "peak": pk, "frac": ach / pk}
+                              "achieved": ach, "unit": "TFLOP/s", "peak": pk, "frac": ach / pk,
+                              "peak_sustained": pks, "frac_sustained": ach / pks}
         else:
             ach = cat_units[cat] / t / 1e9
             breakdown[cat] = {"ms_per_step": cat_ms[cat] / args.steps, "launches_per_step": cat_n[cat] // args.steps,
@@ -843,7 +922,8 @@ def run_ours(args, rank, world, local_rank):
                 "timed": "CUDA events around each launch in K steps issued one call at a time on one stream, "
                          "right after the timed region (kernels alone on the GPU)",
                 "peak_source": f"{peaks['source']} ("
-                + ("bf16 sustained x nominal FP4/FP8 ratio" if dom.startswith("gemm") else "HBM copy") + ")"}
+                + ("bf16 burst x nominal FP4/FP8 dense ratio: the kernel is timed alone"
+                   if dom.startswith("gemm") else "HBM copy") + ")"}
     qcats = [c for c in breakdown if not c.startswith("gemm")]
     q_bytes = sum(cat_units[c] for c in qcats) / args.steps
     q_ms = sum(cat_ms[c] for c in qcats) / args.steps
@@ -864,6 +944,7 @@ def run_ours(args, rank, world, local_rank):
         "breakdown": breakdown,
         "clocks": clocks,
         "e2e": e2e,
+        "e2e_with_outputs": e2e_out,
         "gpu_launches": step.launches_per_step * args.steps,
         "ms_per_step_one_stream": ms_serial,
         "without_stats": no_stats,
@@ -879,25 +960,28 @@ def run_ours(args, rank, world, local_rank):
 # ----------------------------------------------------------------------------- reference arm (the oracle)
 
 def run_reference(args, rank):
+    """The oracle, as it stands, on every host core: each step is one repetition of the bounded sample
+    in each of n worker processes at once; value = n x the sample's flops / the step's wall time."""
     if rank != 0:
         return
     cfg, plan = workload(args)
+    n = os.cpu_count() or 1
     times = []
-    res = None
-    for i in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        res = cpu_sample(0.0)           # one repetition of the bounded sample per step
-        if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
+    with oracle_pool(n) as pool:
+        pool.map(_oracle_sample_rep, range(n))            # first use, untimed
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            pool.map(_oracle_sample_rep, range(n))
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
-    flops = 6 * 256 * 4096 * 512
-    value = flops / (ms * 1e-3) / 1e12
-    sample = "Q linear of the 7B block cut to T=256, N=512 (K=4096), NVFP4 fwd+dgrad+wgrad+stats, one per step"
+    value = n * SAMPLE_FLOPS / (ms * 1e-3) / 1e12
+    sample = f"{SAMPLE_TEXT}; one per worker per step, {n} worker processes (one per host core)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded N(0,s^2) bf16)",
             "config": config_json(cfg, plan, args),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

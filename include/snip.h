@@ -213,10 +213,12 @@ snip_status snip_tensor_scales_multi(int count, const void* const* xs, const int
                                      void* ws, size_t ws_bytes, void* stream);
 
 /* Variant of snip_tensor_scales that needs no workspace and allocates nothing,
- * for callers that cannot allocate device memory where they run: a host
- * callback enqueued with cudaLaunchHostFunc (no allocating CUDA call allowed
- * there), code inside a framework whose caching allocator owns all device
- * memory, or a latency-critical path that must not synchronize the device.
+ * for callers that cannot allocate device memory at the point of the call:
+ * code inside a framework whose caching allocator owns all device memory and
+ * forbids raw cudaMalloc, or a path where an allocation (which may
+ * synchronize the device) is not allowed.  It is an ordinary host-side CUDA
+ * call: like every entry point here it must not be made from a host function
+ * enqueued with cudaLaunchHostFunc, where CUDA forbids all CUDA calls.
  * The pages have no counterpart of this call; it exists for such callers.
  * x: device bf16, n elements, at most 2^30 (SNIP_ERR_SHAPE beyond that);
  * scales_out: device, 3 floats {amax, g, s} as for snip_tensor_scales; a
@@ -224,8 +226,9 @@ snip_status snip_tensor_scales_multi(int count, const void* const* xs, const int
  * The kernel's scratch is one fixed 64 KB device array shared by every call
  * on a device and kept until the process exits: calls that overlap on the GPU
  * (different streams without ordering) race on it and must not be issued.
- * The first call on each device looks up the array's device address (set-up);
- * make that first call outside any stream capture. */
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress), which may load the library's device code on that
+ * device; make that first call outside any stream capture. */
 snip_status snip_tensor_scales_noalloc(const void* x, int64_t n, float* scales_out, void* stream);
 
 /* ---------------------------------------------------------------- a2/a3: NVFP4 */
@@ -315,7 +318,11 @@ snip_status snip_quantize_e5m2(const void* x, int64_t rows, int64_t cols, snip_o
  * across devices (SNIP, Figure 5: every operand of the layer quantized along
  * its contraction dim; a token shard of X or dY is a block of whole rows):
  * x holds rows x cols of a row-major tensor starting at its element
- * index_base (first row * cols, a multiple of 16, else SNIP_ERR_SHAPE).  It is
+ * index_base = first row * cols.  index_base must be a multiple of cols and
+ * of 16, and with ALONG_ROWS the first row a multiple of the format's block
+ * length (16; 32 for MXFP4 and NVFP4_B32, 64, 128 for the longer NVFP4
+ * blocks), else SNIP_ERR_SHAPE: a block never straddles two parts.  These
+ * argument rules are checked before anything touches the device.  It is
  * quantized as fmt (an operand format) with the whole tensor's scales
  * scales_in (device, {amax, g, s} as snip_tensor_scales writes them for the
  * whole tensor, e.g. from a MAX all-reduce of the parts' amax), and every

@@ -720,12 +720,17 @@ snip_status snip_quantize_part(snip_format fmt, const void* x, int64_t rows, int
                                snip_round rnd, uint64_t seed, uint64_t stream_id, uint64_t index_base,
                                const float* scales_in, snip_layout layout, uint8_t* codes, uint8_t* scales,
                                double* raw_out, void* ws, size_t ws_bytes, void* stream) {
+  // argument rules first (they need no device): the part starts on a whole row of the tensor, and
+  // with blocks along the rows (the tokens) on a whole block of rows, so no block straddles parts
+  if (!valid_operand_fmt(fmt) || !scales_in || (raw_out && orient != SNIP_BLOCKS_ALONG_COLS) || cols <= 0 ||
+      (orient != SNIP_BLOCKS_ALONG_COLS && orient != SNIP_BLOCKS_ALONG_ROWS))
+    return SNIP_ERR_INVALID_ARG;
+  if (index_base % 16 != 0 || index_base % (uint64_t)cols != 0) return SNIP_ERR_SHAPE;
+  if (orient == SNIP_BLOCKS_ALONG_ROWS && (index_base / (uint64_t)cols) % (uint64_t)block_elems(fmt) != 0)
+    return SNIP_ERR_SHAPE;
   int sms;
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
-  if (!valid_operand_fmt(fmt) || !scales_in || (raw_out && orient != SNIP_BLOCKS_ALONG_COLS))
-    return SNIP_ERR_INVALID_ARG;
-  if (index_base % 16 != 0) return SNIP_ERR_SHAPE;
   float g_dummy;   // validation only: the scales come in, none is written
   s = check_quantize_args(fmt, x, rows, cols, orient, rnd, layout, codes, is_fp4(fmt) ? scales : nullptr, &g_dummy,
                           ws, ws_bytes);
@@ -752,6 +757,7 @@ snip_status snip_dw_noise(const void* X, const void* dY, int64_t T, int64_t K, i
   if (s != SNIP_OK) return s;
   if (!X || !dY || !dW_q || !out2 || T <= 0 || K <= 0 || N <= 0) return SNIP_ERR_INVALID_ARG;
   if (T % 16 || K % 16 || N % 16) return SNIP_ERR_SHAPE;
+  if (T > INT32_MAX || K > INT32_MAX || N > INT32_MAX) return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < snip_dw_noise_workspace_size(K, N)) return SNIP_ERR_WORKSPACE;
   if (!aligned16(X) || !aligned16(dY) || !aligned16(dW_q) || !aligned16(ws)) return SNIP_ERR_ALIGN;
   int dev = 0;

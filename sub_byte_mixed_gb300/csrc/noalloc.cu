@@ -1,10 +1,11 @@
 // noalloc.cu -- snip_tensor_scales_noalloc: the tensor-scales computation
 // (amax, NVFP4 g, FP8 s) for callers that cannot hand the library a device
 // workspace because they cannot allocate device memory at that point: code
-// running in a host callback enqueued with cudaLaunchHostFunc (which may make
-// no CUDA call that allocates), code inside a framework whose caching
-// allocator owns all device memory and forbids raw cudaMalloc, or code on a
-// latency-critical path where an allocation would synchronize the device.
+// inside a framework whose caching allocator owns all device memory and
+// forbids raw cudaMalloc, or a path where an allocation, which may
+// synchronize the device, is not allowed.  The call itself makes ordinary
+// CUDA runtime calls (a memset and a launch), so it cannot run inside a host
+// function enqueued with cudaLaunchHostFunc.
 //
 // The kernel's scratch (one partial maximum per CTA, the completion counter
 // and a status word) lives in one file-scope device array of fixed size that
@@ -54,7 +55,8 @@ extern "C" snip_status snip_tensor_scales_noalloc(const void* x, int64_t n, floa
     return SNIP_ERR_CUDA;
   if (major != 10 || minor != 3) return SNIP_ERR_UNSUPPORTED_DEVICE;
   if (!g_scratch_ptr[dev]) {
-    // set-up on this device's first call (device current); keep this call outside stream capture
+    // set-up on this device's first call (device current): the lookup may load the module on this
+    // device, so this first call belongs outside stream capture
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_scales_scratch);
     if (e != cudaSuccess || !p) {

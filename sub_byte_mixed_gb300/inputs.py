@@ -130,17 +130,26 @@ class BlockInputs:
     dY: list           # output gradient per linear (T x N)
 
 
+X_TENSOR_ID = {"attn": 1, "o": 2, "mlp": 3, "down": 4}
+
+
 def block_inputs(cfg: BlockConfig, seed: int = 0, device="cpu") -> BlockInputs:
     """Inputs of one Llama-like block: shared activations for Q/K/V and for
     Gate/Up, own activations for O and Down, one weight and one dY per linear."""
     T, h, i = cfg.T, cfg.hidden, cfg.inter
-    X = {"attn": normal_bf16((T, h), SIGMA_X, seed, 1, device),
-         "o": normal_bf16((T, h), SIGMA_X, seed, 2, device),
-         "mlp": normal_bf16((T, h), SIGMA_X, seed, 3, device),
-         "down": normal_bf16((T, i), SIGMA_X, seed, 4, device)}
+    X = {k: normal_bf16((T, h if k != "down" else i), SIGMA_X, seed, tid, device) for k, tid in X_TENSOR_ID.items()}
     W = [normal_bf16((l.N, l.K), SIGMA_W, seed, 10 + j, device) for j, l in enumerate(cfg.linears)]
     dY = [normal_bf16((T, l.N), SIGMA_DY, seed, 20 + j, device) for j, l in enumerate(cfg.linears)]
     return BlockInputs(X, W, dY)
+
+
+def linear_inputs(cfg: BlockConfig, j: int, seed: int = 0, device="cpu"):
+    """(X, W, dY) of linear j of the block, the same tensors as block_inputs
+    generates for it, without the other linears' tensors."""
+    l = cfg.linears[j]
+    return (normal_bf16((cfg.T, l.K), SIGMA_X, seed, X_TENSOR_ID[l.x_id], device),
+            normal_bf16((l.N, l.K), SIGMA_W, seed, 10 + j, device),
+            normal_bf16((cfg.T, l.N), SIGMA_DY, seed, 20 + j, device))
 
 
 def single_linear_inputs(T=64, K=128, N=128, seed=0, device="cpu"):

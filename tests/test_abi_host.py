@@ -106,3 +106,37 @@ def test_library_reports_the_header_version():
     hdr = open(os.path.join(ROOT, "include", "snip.h")).read()
     want = int(re.search(r"#define SNIP_ABI_VERSION (\d+)", hdr).group(1))
     assert snip.load().snip_version() == want
+
+
+def test_quantize_part_index_rules_need_no_device(snip):
+    """snip_quantize_part checks where the part starts before it touches the
+    device: the part begins on a whole row (index_base a multiple of cols and
+    of 16), and with blocks along the rows (the tokens) on a whole block of
+    rows, so no block straddles two parts.  Pointers are dummies: a call that
+    passes these rules goes on to the device check (which fails on a host
+    without a usable GPU, and would reject the dummies' alignment on one)."""
+    lib = snip.load()
+    P = 4096   # dummy, 16-byte aligned, never dereferenced by a rejected call
+
+    def part(fmt, orient, rows, cols, index_base):
+        return lib.snip_quantize_part(fmt, P, rows, cols, orient, snip.SR, 0, 0, index_base, P, snip.ROWMAJOR,
+                                      P, P, None, P, 1 << 20, None)
+
+    C = 256
+    # along the rows: the first row must be a whole number of blocks (16 for NVFP4, 32 for MXFP4)
+    assert part(snip.NVFP4, snip.ALONG_ROWS, 64, C, 8 * C) == snip.SNIP_ERR_SHAPE
+    assert part(snip.MXFP4, snip.ALONG_ROWS, 64, C, 16 * C) == snip.SNIP_ERR_SHAPE
+    assert part(snip.FP8, snip.ALONG_ROWS, 64, C, 24 * C) == snip.SNIP_ERR_SHAPE
+    # not a whole row, or not a multiple of 16
+    assert part(snip.NVFP4, snip.ALONG_COLS, 64, C, 16) == snip.SNIP_ERR_SHAPE
+    assert part(snip.NVFP4, snip.ALONG_COLS, 64, 48, 8) == snip.SNIP_ERR_SHAPE
+    # bad orientation
+    assert part(snip.NVFP4, 7, 64, C, 0) == snip.SNIP_ERR_INVALID_ARG
+    import torch
+    if torch.cuda.is_available():
+        return
+    # valid starts reach the device check
+    for fmt, orient, first_row in ((snip.NVFP4, snip.ALONG_ROWS, 16), (snip.MXFP4, snip.ALONG_ROWS, 32),
+                                   (snip.NVFP4, snip.ALONG_COLS, 3), (snip.FP8, snip.ALONG_ROWS, 48)):
+        st = part(fmt, orient, 64, C, first_row * C)
+        assert st in (snip.SNIP_ERR_CUDA, snip.SNIP_ERR_UNSUPPORTED_DEVICE), (fmt, orient, st)

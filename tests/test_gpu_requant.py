@@ -1,11 +1,14 @@
 """NEXT-3: the GEMM whose product feeds the next layer writes it quantized
-(NVFP4 row blocks of bf16(D), given tensor scale).  Checked three ways:
-bit-exact against the library's own quantizer applied to bf16 of the D it
-returns (the definition of the fused path; that quantizer is bit-exact
-against the oracle elsewhere); against the oracle's quantization of its fp64
-product rounded to bf16 -- codes may differ only where fp32 and fp64
-accumulation round to different bf16 values, so nearly all must agree and
-every difference is a neighbouring grid value; and the amax output exactly."""
+(NVFP4 row and column blocks of bf16(D), given tensor scale).  Checked:
+bit-exact against the oracle on operands whose products are exact in fp32
+(every partial sum representable, power-of-two tensor scales), where the
+GPU's fp32 product must equal the oracle's fp64 one and the oracle's
+quantization of its own bf16(product) fixes every code and scale; on general
+operands, bit-exact against the library's own quantizer applied to bf16 of
+the D it returns (the definition of the fused path; that quantizer is
+bit-exact against the oracle elsewhere) and, against the oracle, codes equal
+except where fp32 and fp64 accumulation round to different bf16 values (only
+to a neighbouring grid value); and the amax output exactly."""
 import numpy as np
 import pytest
 import torch
@@ -154,6 +157,70 @@ def test_requant_columns_only_and_as_wgrad_operand(snip):
     out_lib = snip.gemm(snip.NVFP4, lib, xt, N, 384, M)
     torch.cuda.synchronize()
     assert torch.equal(out_fused, out_lib)
+
+
+# ---------------------------------------------------------------- exact products: bit-exact against the oracle
+
+def _exact_operand(fmt, rows, K, seed):
+    """A bf16 rows x K operand whose quantization is exact and whose GEMM
+    products sum exactly in fp32 in any order.  NVFP4: every 16-block holds
+    one +-6 and random E2M1 values, all times 448 * 2^-10, so the tensor scale
+    g = amax / 2688 = 2^-10 and every block scale is 448: the MMA's partial
+    sums are 448^2 times sums of E2M1 products (at most 22 bits).  FP8: E4M3
+    values with exponents 6..8 (64 .. 448) and zeros, one 448, all times
+    2^-8, so s = amax / 448 = 2^-8 and products are multiples of 64 below
+    2^18 (sums of up to 512 of them stay below 2^24)."""
+    rng = np.random.default_rng(seed)
+    if fmt == 1:
+        grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+        v = grid[rng.integers(0, 8, size=(rows, K))] * rng.choice([-1.0, 1.0], size=(rows, K))
+        blk = v.reshape(rows, K // 16, 16)
+        pos = rng.integers(0, 16, size=(rows, K // 16))
+        np.put_along_axis(blk, pos[..., None], rng.choice([-6.0, 6.0], size=(rows, K // 16, 1)), axis=2)
+        x = blk.reshape(rows, K) * 448.0 * 2.0 ** -10
+    else:
+        m = rng.integers(0, 8, size=(rows, K))
+        e = rng.integers(6, 9, size=(rows, K))
+        m = np.where(e == 8, np.minimum(m, 6), m)          # 1.75 * 2^8 = 448 is the largest
+        v = (1 + m / 8.0) * 2.0 ** e * rng.choice([-1.0, 1.0], size=(rows, K))
+        v = np.where(rng.random((rows, K)) < 0.2, 0.0, v)
+        v[rng.integers(0, rows), rng.integers(0, K)] = 448.0
+        x = v * 2.0 ** -8
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    assert np.array_equal(t.float().numpy().astype(np.float64), x)   # exact in bf16
+    return t
+
+
+@pytest.mark.parametrize("fmt", [1, 0])
+@pytest.mark.parametrize("M,N,K", [(192, 160, 256), (272, 400, 336), (2048, 2560, 512)])
+@pytest.mark.parametrize("rnd,rnd_t", [(0, 0), (1, 1), (0, 1)])
+def test_requant_bit_exact_vs_oracle_on_exact_products(snip, fmt, M, N, K, rnd, rnd_t):
+    A = _exact_operand(fmt, M, K, 100 + M)
+    B = _exact_operand(fmt, N, K, 200 + N)
+    fname = "nvfp4" if fmt == 1 else "fp8"
+    q = snip.quantize_nvfp4 if fmt == 1 else snip.quantize_fp8
+    a = q(A.cuda(), rnd=1, seed=1, stream_id=2, layout=snip.MMA)
+    b = q(B.cuda(), rnd=1, seed=1, stream_id=3, layout=snip.MMA)
+    ref = oracle.gemm_tn(oracle.quantize(fname, A, 0, 1, 1, 2).dequant(), oracle.quantize(fname, B, 0, 1, 1, 3).dequant())
+    assert np.array_equal(ref.astype(np.float32).astype(np.float64), ref)   # the product is exact in fp32
+    gval = np.float32(0.8 * float(np.abs(ref).max()) / 2688.0)
+    g = torch.tensor([gval], dtype=torch.float32, device="cuda")
+    D, rq, amax, rq_t = snip.gemm_requant(fmt, a, b, M, N, K, g, rnd=rnd, seed=9, stream_id=21, cols=True,
+                                          rnd_t=rnd_t, stream_id_t=23)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(D.cpu().numpy().astype(np.float64), ref)
+    refb = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16)
+    orc = oracle.quantize_nvfp4(refb, orient=0, rnd=rnd, seed=9, stream_id=21, g_in=float(gval))
+    orc_t = oracle.quantize_nvfp4(refb, orient=1, rnd=rnd_t, seed=9, stream_id=23, g_in=float(gval))
+    _, codes = mma_codes_to_rowmajor(rq.codes, M, N, fmt_nvfp4=True)
+    _, scales = mma_scales_to_rowmajor(rq.scales, M, N)
+    np.testing.assert_array_equal(codes, orc.codes)
+    np.testing.assert_array_equal(scales, orc.scales)
+    _, codes_t = mma_codes_to_rowmajor(rq_t.codes, N, M, fmt_nvfp4=True)
+    _, scales_t = mma_scales_to_rowmajor(rq_t.scales, N, M)
+    np.testing.assert_array_equal(codes_t, orc_t.codes)
+    np.testing.assert_array_equal(scales_t, orc_t.scales)
+    assert float(amax.cpu()) == float(refb.float().abs().max())
 
 
 def test_requant_argument_errors(snip):

@@ -1,7 +1,7 @@
 """snip_tensor_scales_noalloc: the tensor-scales call for callers that cannot
-allocate device memory where they run (a cudaLaunchHostFunc callback, code
-under a framework allocator that forbids raw cudaMalloc, a path that must not
-synchronize).  It keeps its scratch in a fixed device array inside the
+allocate device memory at the point of the call (code under a framework
+allocator that forbids raw cudaMalloc, a path where an allocation and the
+device synchronisation it may bring are not allowed).  It keeps its scratch in a fixed device array inside the
 library instead of a caller workspace.  Checked against snip_tensor_scales,
 exactly (the scales are exact functions of the input), on two calls in a row
 with different tensors, so a value left in the shared scratch by the first
