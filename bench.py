@@ -328,7 +328,8 @@ def whole_job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
 class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
-    def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True, own_stream=False):
+    def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True, own_stream=False,
+                 share_x=True):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
@@ -347,7 +348,7 @@ class Step:
         self.Y = [torch.empty((T, l.N), dtype=torch.float32, device=device) for l in cfg.linears]
         self.dX = [torch.empty((T, l.K), dtype=torch.float32, device=device) for l in cfg.linears]
         self.dW = [torch.empty((l.N, l.K), dtype=torch.float32, device=device) for l in cfg.linears]
-        self.raw = torch.empty((len(cfg.linears), 3, snip.STATS_NVALS), dtype=torch.float64, device=device)
+        self.raw = torch.zeros((len(cfg.linears), 3, snip.STATS_NVALS), dtype=torch.float64, device=device)
         self.ws = snip.Workspace(snip.snip_quantize_workspace_size(0, 0), device)
         # {amax, NVFP4 g, FP8 s} of X, W and dY of every linear (16-byte slots)
         self.sc = torch.empty((len(cfg.linears), 3, 4), dtype=torch.float32, device=device)
@@ -368,9 +369,22 @@ class Step:
         calls = []   # (fn, args, category, units, stream kind 'q'/'g', linear, GEMM index or -1)
         self.gemm_ws = snip.Workspace(snip.WS_HEADER_BYTES, device) if overlap else self.ws
         self._keep = []   # ctypes arrays referenced by the calls
-        for j, (l, f) in enumerate(zip(cfg.linears, plan)):
-            if layers and l.name not in layers:
-                continue
+        # Activations read by several linears (Q/K/V, Gate/Up: SNIP, Figure 4): with share_x, their
+        # tensor scales, statistics and round-to-nearest row-block quantization (forward operand) are
+        # computed once -- the quantization once per format -- into a buffer of their own, read by
+        # every sharer's forward GEMM.  The per-linear column-block (stochastic, own stream id)
+        # quantizations of X are unchanged.
+        active = [j for j, l in enumerate(cfg.linears) if not layers or l.name in layers]
+        users = {}
+        for j in active:
+            users.setdefault(cfg.linears[j].x_id, []).append(j)
+        self.share_x = share_x
+        shared_ids = {k for k, v in users.items() if len(v) > 1} if share_x else set()
+        self.first_user = {k: v[0] for k, v in users.items()}
+        xq_owner = {}       # (x_id, format) -> (codes, scales) holding that row-block quantization
+        xbuf = {}           # format -> (codes, scales, last user of its current content)
+        for j in active:
+            l, f = cfg.linears[j], plan[j]
             X = self.inp.X[l.x_id]
             W, dY = self.inp.W[j], self.inp.dY[j]
             self.codes, self.scales = codes_sets[j % nsets], scales_sets[j % nsets]
@@ -383,18 +397,50 @@ class Step:
             qcat, gcat = "quant_" + fname, "gemm_" + fname
             bpe = NVFP4_BYTES_PER_ELEM if block else {snip.FP8: FP8_BYTES_PER_ELEM, snip.MXFP4: MXFP4_BYTES_PER_ELEM}[f]
             fo = 8 if f == snip.FP8 else 4            # byte offset of s (FP8) or g (NVFP4; MXFP4: unused) in a slot
-            # the three tensors' scales in one launch
-            names = (l.x_id, "W", "dY")
-            xs = (ctypes.c_void_p * 3)(*[src[nm].data_ptr() for nm in names])
-            ns = (ctypes.c_int64 * 3)(*[src[nm].numel() for nm in names])
-            outs = (ctypes.c_void_p * 3)(*[scp[nm] for nm in names])
+            shared = l.x_id in shared_ids
+            sharer = shared and self.first_user[l.x_id] != j
+            if sharer:   # X's tensor scales are the first user's
+                scp[l.x_id] = self.sc[self.first_user[l.x_id], 0].data_ptr()
+            # the tensors' scales in one launch (X's only for its first user)
+            names = ("W", "dY") if sharer else (l.x_id, "W", "dY")
+            xs = (ctypes.c_void_p * len(names))(*[src[nm].data_ptr() for nm in names])
+            ns = (ctypes.c_int64 * len(names))(*[src[nm].numel() for nm in names])
+            outs = (ctypes.c_void_p * len(names))(*[scp[nm] for nm in names])
             self._keep.append((xs, ns, outs))
-            calls.append((L.snip_tensor_scales_multi, (3, xs, ns, outs, ws, wsb, stream), "scales",
+            calls.append((L.snip_tensor_scales_multi, (len(names), xs, ns, outs, ws, wsb, stream), "scales",
                           SCALES_BYTES_PER_ELEM * sum(src[nm].numel() for nm in names), "q", j, -1))
+            xcodes = xscales = None      # forward operand of X when it comes from the shared buffers
             for r, (name, orient, orr, occ) in enumerate(roles(l)):
                 t = src[name]
                 rows, cols = t.shape
                 g = scp[name] + fo
+                if r == 0 and shared:
+                    key = (l.x_id, f)
+                    if key in xq_owner:          # another sharer already quantized X in this format
+                        xcodes, xscales = xq_owner[key]
+                        continue
+                    c, sbytes = snip.snip_quantized_bytes(f, snip.MMA, orr, occ)
+                    if f not in xbuf or xbuf[f][0].numel() < c:
+                        xbuf[f] = (torch.empty(c, dtype=torch.uint8, device=device),
+                                   torch.empty(max(sbytes, 16), dtype=torch.uint8, device=device), None)
+                    xc, xsb, last = xbuf[f]
+                    # the buffer's previous content is read by earlier forward GEMMs; this linear's
+                    # quantizations wait for linear j-2's GEMMs, which must cover them
+                    if last is not None and last > j - 2:
+                        raise RuntimeError("shared activations too close together for the two-set schedule")
+                    xbuf[f] = (xc, xsb, max(users[l.x_id]))
+                    xq_owner[key] = (xc, xsb)
+                    xcodes, xscales = xc, xsb
+                    dst_c, dst_s = xc.data_ptr(), xsb.data_ptr()
+                    if stats and not sharer:
+                        args = (f, t.data_ptr(), rows, cols, rnd[r], 0, sid + r, scp[name], snip.MMA, dst_c,
+                                dst_s if f != snip.FP8 else None, self.raw[j, 0].data_ptr(), ws, wsb, stream)
+                        calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", j, -1))
+                    else:
+                        args = self._plain_quant(L, f, block, t, rows, cols, orient, rnd[r], sid + r, g, dst_c, dst_s,
+                                                 ws, wsb, stream)
+                        calls.append((args[0], args[1], qcat, bpe * t.numel(), "q", j, -1))
+                    continue
                 if r in (0, 1, 2) and stats:
                     # row-block quantization with SNIP's statistics of the same tensor in one pass
                     k = r
@@ -422,12 +468,15 @@ class Step:
                     a, b = r - 1, r
                     M, N, K = {1: (T, l.N, l.K), 3: (T, l.K, l.N), 5: (l.N, l.K, T)}[r]
                     D = {1: self.Y[j], 3: self.dX[j], 5: self.dW[j]}[r]
-                    sa = self.scales[a].data_ptr() if f != snip.FP8 else None
+                    ac, asc = self.codes[a], self.scales[a]
+                    if r == 1 and xcodes is not None:
+                        ac, asc = xcodes, xscales
+                    sa = asc.data_ptr() if f != snip.FP8 else None
                     sb = self.scales[b].data_ptr() if f != snip.FP8 else None
                     ga = scp[roles(l)[a][0]] + fo if f != snip.MXFP4 else None
                     gb = scp[roles(l)[b][0]] + fo if f != snip.MXFP4 else None
                     gw = self.gemm_ws
-                    args = (f, self.codes[a].data_ptr(), sa, ga, self.codes[b].data_ptr(), sb, gb, M, N, K,
+                    args = (f, ac.data_ptr(), sa, ga, self.codes[b].data_ptr(), sb, gb, M, N, K,
                             D.data_ptr(), D.stride(0), gw.ptr, gw.nbytes, gstream)
                     calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K, "g", j, r // 2))
         self.calls = calls
@@ -436,6 +485,30 @@ class Step:
         # one kernel per call (the scales are computed once per tensor and passed in; every plan
         # format here has its statistics fused into its row-block quantization)
         self.launches_per_step = len(calls)
+
+    @staticmethod
+    def _plain_quant(L, f, block, t, rows, cols, orient, rnd, sid, g, dst_c, dst_s, ws, wsb, stream):
+        """(function, arguments) of a plain quantization of t in format f (MMA layout)."""
+        import sub_byte_mixed_gb300.snip as snip
+        if block > 16:
+            return L.snip_quantize_nvfp4_block, (t.data_ptr(), rows, cols, orient, rnd, 0, sid, g, block, snip.MMA,
+                                                 dst_c, dst_s, g, ws, wsb, stream)
+        if f == snip.NVFP4:
+            return L.snip_quantize_nvfp4, (t.data_ptr(), rows, cols, orient, rnd, 0, sid, g, snip.MMA, dst_c, dst_s, g,
+                                           None, ws, wsb, stream)
+        if f == snip.MXFP4:
+            return L.snip_quantize_mxfp4, (t.data_ptr(), rows, cols, orient, rnd, 0, sid, snip.MMA, dst_c, dst_s, ws,
+                                           wsb, stream)
+        return L.snip_quantize_fp8, (t.data_ptr(), rows, cols, orient, rnd, 0, sid, g, snip.MMA, dst_c, g, ws, wsb,
+                                     stream)
+
+    def stats_host(self):
+        """The step's statistics (linears x {X, W, dY} x raw values) on the host, the statistics of a
+        shared activation repeated for every linear that reads it."""
+        raw = self.raw.cpu().numpy().copy()
+        for j, l in enumerate(self.cfg.linears):
+            raw[j, 0] = raw[self.first_user[l.x_id], 0]
+        return raw
 
     def run(self, events=None, serial=False):
         """One step.  With overlap, a GEMM waits for its two operands' quantizations, and the
@@ -771,7 +844,7 @@ def run_ours(args, rank, world, local_rank):
         # SNIP's loop: statistics of one step feed the layer-wise selection (C ABI, host code)
         step.run()
         torch.cuda.synchronize()
-        c8, c4 = snip.snip_plan_costs(step.raw.cpu().numpy())
+        c8, c4 = snip.snip_plan_costs(step.stats_host())
         flops = [6.0 * cfg.T * l.K * l.N for l in cfg.linears]
         plan, _, _ = snip.snip_plan_select(flops, c8, c4, cfg.fp4_target)
         del step

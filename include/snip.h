@@ -485,13 +485,16 @@ snip_status snip_stats_finalize(const double* raw_host, snip_stats* out);
 /* The weight-gradient form of the quantization-noise threshold of "FP4 all
  * the way" (Outline: quantized training loses efficiency once the gradient
  * norm falls below about sqrt(3) times the quantization noise): the
- * full-precision weight gradient dW = dY^T X is formed from the bf16 tensors
- * (cuBLAS GEMM, fp32 accumulation) and compared with a quantized one:
+ * full-precision weight gradient dW = dY^T X of the bf16 tensors is compared
+ * with a quantized one:
  * out2 (device, 2 doubles) = { ||dW||^2, ||dW_q - dW||^2 }.
+ * One kernel: a bf16 tensor-core GEMM (fp32 accumulation in tensor memory)
+ * whose epilogue reads dW_q beside each tile of dW and accumulates both
+ * sums; dW is never written to memory.
  * X device T x K bf16, dY device T x N bf16, dW_q device N x K fp32 (dense,
- * e.g. snip_qlinear_bwd's dW).  T, K, N multiples of 16 (SNIP_ERR_SHAPE).
- * ws: snip_dw_noise_workspace_size(K, N) bytes (it holds dW).  Errors as for
- * the other entry points; SNIP_ERR_CUDA if cuBLAS fails. */
+ * e.g. snip_qlinear_bwd's dW).  T, K, N multiples of 16 and below 2^31
+ * (SNIP_ERR_SHAPE).  ws: snip_dw_noise_workspace_size(K, N) bytes (partial
+ * sums and the status word only).  Errors as for the other entry points. */
 size_t snip_dw_noise_workspace_size(int64_t K, int64_t N);
 snip_status snip_dw_noise(const void* X, const void* dY, int64_t T, int64_t K, int64_t N, const float* dW_q,
                           double* out2, void* ws, size_t ws_bytes, void* stream);

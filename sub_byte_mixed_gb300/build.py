@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsnip.so")
-SOURCES = ["quant.cu", "gemm.cu", "api.cu", "noalloc.cu", "plan_select.cu", "waitcheck.cu"]
+SOURCES = ["quant.cu", "gemm.cu", "dw_noise.cu", "api.cu", "noalloc.cu", "plan_select.cu", "waitcheck.cu"]
 HEADERS = ["snip_device.cuh", "snip_kernels.cuh", "snip_quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -67,10 +67,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}")
     tmp = LIB + f".tmp{os.getpid()}"
-    # cuBLAS serves the one plain library GEMM (the full-precision dW of snip_dw_noise)
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(cc))), "lib64")
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[obj for _, obj, _ in results], "-lcublas",
-           "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
+    # only the CUDA runtime (static) is linked: every GEMM is a kernel of this library
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[obj for _, obj, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)

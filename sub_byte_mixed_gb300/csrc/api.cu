@@ -1,8 +1,6 @@
 // api.cu -- the C ABI declared in include/snip.h: argument checks, workspace
 // layout, the per-layer precision plan and the launch sequence of each call.
 // Every compute step runs in the kernels of quant.cu and gemm.cu.
-#include <cublas_v2.h>
-
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -161,6 +159,7 @@ snip_status run_quantize(int fmt, const void* x, int64_t rows, int64_t cols, int
   p.ocp = layout == SNIP_LAYOUT_MMA ? mma_cols(fmt, p.out_cols) : p.out_cols;
   p.seed = seed;
   p.stream_id = stream_id;
+  p.rk = philox_round_keys(seed);
   p.scale = scale;
   p.codes = codes;
   p.scales = scales;
@@ -684,6 +683,7 @@ snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_rou
   p.cols = cols;
   p.seed = seed;
   p.stream_id = stream_id;
+  p.rk = philox_round_keys(seed);
   p.scales3 = sc;
   p.partials = ws_at<double>(ws, kOffStatsPartials);
   p.counter = ws_at<uint32_t>(ws, kOffStatsCounter);
@@ -741,13 +741,9 @@ snip_status snip_quantize_part(snip_format fmt, const void* x, int64_t rows, int
 }
 
 // ---------------------------------------------------------------- NEXT-4: dW-level sqrt(3) check
-namespace {
-cublasHandle_t g_cublas[64] = {nullptr};   // one handle per device, created on first use
-}
-
 size_t snip_dw_noise_workspace_size(int64_t K, int64_t N) {
   if (K < 0 || N < 0) return 0;
-  return kSmallWorkspaceRounded + (size_t)(K * N) * sizeof(float);
+  return kSmallWorkspaceRounded;   // partial sums and the status word: dW itself is never stored
 }
 
 snip_status snip_dw_noise(const void* X, const void* dY, int64_t T, int64_t K, int64_t N, const float* dW_q,
@@ -757,32 +753,13 @@ snip_status snip_dw_noise(const void* X, const void* dY, int64_t T, int64_t K, i
   if (s != SNIP_OK) return s;
   if (!X || !dY || !dW_q || !out2 || T <= 0 || K <= 0 || N <= 0) return SNIP_ERR_INVALID_ARG;
   if (T % 16 || K % 16 || N % 16) return SNIP_ERR_SHAPE;
-  if (T > INT32_MAX || K > INT32_MAX || N > INT32_MAX) return SNIP_ERR_SHAPE;
+  if (T > INT32_MAX || K > INT32_MAX || N > INT32_MAX) return SNIP_ERR_SHAPE;   // TMA coordinates are 32-bit
   if (!ws || ws_bytes < snip_dw_noise_workspace_size(K, N)) return SNIP_ERR_WORKSPACE;
   if (!aligned16(X) || !aligned16(dY) || !aligned16(dW_q) || !aligned16(ws)) return SNIP_ERR_ALIGN;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SNIP_ERR_CUDA;
-  if (!g_cublas[dev] && cublasCreate(&g_cublas[dev]) != CUBLAS_STATUS_SUCCESS) {
-    g_cublas[dev] = nullptr;
-    fprintf(stderr, "snip: cublasCreate failed\n");
-    return SNIP_ERR_CUDA;
-  }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cublasHandle_t h = g_cublas[dev];
-  if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return SNIP_ERR_CUDA;
-  float* ref = ws_at<float>(ws, kSmallWorkspaceRounded);
-  // dW = dY^T X (N x K, row-major) from the bf16 tensors, fp32 accumulation: in column-major terms
-  // dW^T (K x N) = X' (K x T) * dY'^T (T x N), X' and dY' the row-major X and dY read column-major
-  const float one = 1.0f, zero = 0.0f;
-  const cublasStatus_t cs =
-      cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, (int)K, (int)N, (int)T, &one, X, CUDA_R_16BF, (int)K, dY,
-                   CUDA_R_16BF, (int)N, &zero, ref, CUDA_R_32F, (int)K, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (cs != CUBLAS_STATUS_SUCCESS) {
-    fprintf(stderr, "snip: cublasGemmEx failed (%d)\n", (int)cs);
-    return SNIP_ERR_CUDA;
-  }
-  return cuda_status(launch_dw_noise(dW_q, ref, K * N, ws_at<double>(ws, kOffStatsPartials),
-                                     ws_at<uint32_t>(ws, kOffStatsCounter), out2, sms, st));
+  return cuda_status(launch_dw_noise_gemm(X, dY, T, K, N, dW_q, ws_at<double>(ws, kOffStatsPartials),
+                                          ws_at<uint32_t>(ws, kOffStatsCounter), out2,
+                                          ws_at<uint32_t>(ws, kOffStatus), kTimeoutNs, sms,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 snip_status snip_dw_noise_finalize(const double* out2_host, double* ratio, int* below_sqrt3) {

@@ -131,6 +131,9 @@ struct StagedBits {
   const uint2* s;   // the lane's first staged pair
   uint32_t sh;
   __device__ __forceinline__ uint32_t operator()(int i) const { return (s[i * 9].y >> sh) & 0xffffu; }
+  __device__ __forceinline__ float f23(int i) const {   // 2^23 + the 16 bits, as a float (sh is 0 or 16)
+    return __uint_as_float(__byte_perm(s[i * 9].y, 0x4B000000u, 0x7610u + (sh >> 3) * 0x11u));
+  }
 };
 
 // NEXT-3, transposed: NVFP4 blocks of 16 consecutive rows m of one column n

@@ -38,6 +38,14 @@ __device__ __forceinline__ void scales_body(const uint16_t* __restrict__ x, int6
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int64_t stride = (int64_t)nblk * blockDim.x;
   int64_t i = (int64_t)lb * blockDim.x + threadIdx.x;
+  // eight independent 16-byte loads in flight per thread (128 B), then four
+  for (; i + 7 * stride < nvec; i += 8 * stride) {
+    uint4 r[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r[k] = __ldg(xv + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m2 = __vmaxu2(m2, mag_max4(r[k]));
+  }
   for (; i + 3 * stride < nvec; i += 4 * stride) {
     const uint4 a = __ldg(xv + i), b = __ldg(xv + i + stride), c = __ldg(xv + i + 2 * stride),
                 d = __ldg(xv + i + 3 * stride);
@@ -86,11 +94,18 @@ __global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restri
 __global__ void __launch_bounds__(256, 4) scales_multi_kernel(ScalesMulti m, uint32_t* __restrict__ partials,
                                                               uint32_t* __restrict__ counters,
                                                               uint32_t* __restrict__ status) {
-  int t = 0;
-  while (t + 1 < m.count && (int)blockIdx.x >= m.cta0[t + 1]) ++t;
-  const uint32_t c0 = (uint32_t)m.cta0[t];
-  scales_body(m.x[t], m.n[t], blockIdx.x - c0, (uint32_t)(m.cta0[t + 1] - m.cta0[t]), partials + c0, counters + t,
-              m.out3[t], status);
+  // this CTA's tensor, picked with constant indices (a run-time index into the parameter block would
+  // copy it to local memory)
+  const uint16_t* x = m.x[0];
+  int64_t n = m.n[0];
+  float* out3 = m.out3[0];
+  int t = 0, c0 = 0, c1 = m.cta0[1];
+#pragma unroll
+  for (int k = 1; k < kMaxMultiScales; ++k)
+    if (k < m.count && (int)blockIdx.x >= m.cta0[k]) {
+      t = k; x = m.x[k]; n = m.n[k]; out3 = m.out3[k]; c0 = m.cta0[k]; c1 = m.cta0[k + 1];
+    }
+  scales_body(x, n, blockIdx.x - (uint32_t)c0, (uint32_t)(c1 - c0), partials + c0, counters + t, out3, status);
 }
 
 // Squared dequantization error of an encoded block (x_hat = value(code) * p).
@@ -126,11 +141,18 @@ __device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, B
       w[i >> 1] |= (E5 ? e5m2x2_rn_sat(a, b) : e4m3x2_rn_sat(a, b)) << (16 * (i & 1));
     }
   } else {
+    // stochastic rounding on the FMA pipe (grid_sr2), the code converted from the exact grid value
+    constexpr float kTop = E5 ? 57344.0f : 448.0f, kC = E5 ? 2097152.0f : 1048576.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t b = __float_as_uint(v[i]);
-      const float y = __fmul_rn(__uint_as_float(b & 0x7fffffffu), inv);
-      w[i >> 2] |= (((b >> 24) & 0x80u) | (E5 ? e5m2_sr(y, bits(i)) : e4m3_sr(y, bits(i)))) << (8 * (i & 3));
+    for (int i = 0; i < 16; i += 2) {
+      const float2 y = __fmul2_rn(make_float2(fabsf(v[i]), fabsf(v[i + 1])), make_float2(inv, inv));
+      const float2 yc = make_float2(fminf(y.x, kTop), fminf(y.y, kTop));
+      const float2 H = E5 ? make_float2(e5m2_step_x4(yc.x), e5m2_step_x4(yc.y))
+                          : make_float2(e4m3_step_x8(yc.x), e4m3_step_x8(yc.y));
+      const float2 g = E5 ? sr_g2<18>(bits.f23(i), bits.f23(i + 1)) : sr_g2<19>(bits.f23(i), bits.f23(i + 1));
+      const float2 q = grid_sr2(yc, H, g, kC);
+      const float a = copysignf(q.x, v[i]), b = copysignf(q.y, v[i + 1]);
+      w[i >> 2] |= (E5 ? e5m2x2_rn_sat(a, b) : e4m3x2_rn_sat(a, b)) << (16 * ((i >> 1) & 1));
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
@@ -153,67 +175,62 @@ __device__ __forceinline__ float e5m2_tensor_scale(float amax) {
 // need no bit exactness, so they use fused multiply-adds; per-thread sums are
 // fp32 (a few hundred elements), per-CTA and final sums fp64.
 
-// Grid steps as floats: twice the E2M1 step at |y| (0.5 below 2, then
-// 2^(E-1)) and eight times the E4M3 step at |y| (2^(E-3) from 2^-6 up,
-// 2^-9 below), from the exponent field of y.
-__device__ __forceinline__ float e2m1_step_x2(float y) {
-  return fmaxf(__uint_as_float(__float_as_uint(y) & 0x7f800000u), 1.0f);
-}
-__device__ __forceinline__ float e4m3_step_x8(float y) {
-  return fmaxf(__uint_as_float(__float_as_uint(y) & 0x7f800000u), 0.015625f);
-}
-
 // Statistics of one 16-element block: squares of the values, the squared
 // errors of NVFP4 (block scale bs) and FP8 (tensor scale s8) quantization
 // under rounding RND, and the expected SR variance on both grids.
 // CF = 1 / 0 also returns the block's NVFP4 / FP8 codes (packed as by
-// nvfp4_encode16 / fp8_encode16) from the same conversions, except where
-// that format's scale is special (bs.special, special8): there the caller
+// nvfp4_encode16 / fp8_encode16) from the same roundings, except where that
+// format's scale is special (bs.special, special8): there the caller
 // encodes.  CF = -1: statistics only.
+// Element pairs go through Blackwell's packed fp32 operations (__fmul2_rn,
+// __ffma2_rn, __fadd2_rz: per lane the IEEE result of the scalar operation),
+// and each candidate's rounding is the FMA-pipe form (grid_rn2 / grid_sr2),
+// which gives the grid value q of the code the rule picks; the code is then
+// the hardware conversion of that exact value.  With y clamped to the grid's
+// top (yc) and c = q - yc, the expected SR variance (hi - y)(y - lo) is
+// |c| (h - |c|) whichever neighbour q is, summed as 1/2 sum |c| H - sum c^2
+// (H = twice the E2M1 step; eight times the E4M3 step with 1/8).
 struct BlockStats {
   float x2, e4, e8, v4, v8;
 };
 template <int CF, int RND>
 __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
                                                     float s8, float inv8, bool special8, uint4& codes) {
-  float bx2 = 0.f, be4 = 0.f, be8 = 0.f, A4 = 0.f, A8 = 0.f;
+  float2 x2 = make_float2(0.f, 0.f), e4 = x2, e8 = x2, S4 = x2, S8 = x2;
+  float T4 = 0.f, T8 = 0.f, se4 = 0.f, se8 = 0.f;
   uint32_t cw[4] = {0u, 0u, 0u, 0u};
+  const float2 inv2 = make_float2(bs.inv, bs.inv), np2 = make_float2(-bs.p, -bs.p);
+  const float2 i8 = make_float2(inv8, inv8), ns8 = make_float2(-s8, -s8), m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
-    bx2 = fmaf(v[i], v[i], fmaf(v[i + 1], v[i + 1], bx2));
-    const uint32_t sg0 = __float_as_uint(v[i]) >> 31, sg1 = __float_as_uint(v[i + 1]) >> 31;
+    const float2 va = make_float2(fabsf(v[i]), fabsf(v[i + 1]));
+    x2 = __ffma2_rn(va, va, x2);
+    float2 g17 = va, g19 = va;   // random fractions of the pair (stochastic rounding)
+    if (RND) {
+      const float f0 = sr_f23<false>(u[i >> 1]), f1 = sr_f23<true>(u[i >> 1]);
+      g17 = sr_g2<17>(f0, f1);
+      g19 = sr_g2<19>(f0, f1);
+    }
     // ---------------- NVFP4
     if (bs.special) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const float q = (bs.p == 0.0f || v[i + k] == 0.0f) ? 0.0f : copysignf(6.0f, v[i + k]);
         const float d = fmaf(q, bs.p, -v[i + k]);
-        be4 = fmaf(d, d, be4);
+        se4 = fmaf(d, d, se4);
       }
     } else {
-      float y0, y1;
-      float2 q;
-      if (RND == 0) {
-        y0 = __fmul_rn(v[i], bs.inv);
-        y1 = __fmul_rn(v[i + 1], bs.inv);
-        const uint32_t byte = e2m1x2_rn(y0, y1);
-        if (CF == 1) cw[i >> 3] |= byte << (4 * (i & 7));
-        q = e2m1x2_decode(byte);
-      } else {
-        y0 = __fmul_rn(fabsf(v[i]), bs.inv);
-        y1 = __fmul_rn(fabsf(v[i + 1]), bs.inv);
-        const uint32_t mag = e2m1_sr(y0, uhalf(u, i)) | (e2m1_sr(y1, uhalf(u, i + 1)) << 4);
-        if (CF == 1) cw[i >> 3] |= (mag | (sg0 << 3) | (sg1 << 7)) << (4 * (i & 7));
-        q = e2m1x2_decode(mag);
-      }
-      // RTN: signed q, y; SR: magnitudes
-      const float d0 = fmaf(q.x, bs.p, RND ? -fabsf(v[i]) : -v[i]);
-      const float d1 = fmaf(q.y, bs.p, RND ? -fabsf(v[i + 1]) : -v[i + 1]);
-      be4 = fmaf(d0, d0, fmaf(d1, d1, be4));
-      const float c0 = fabsf(fabsf(q.x) - fminf(fabsf(y0), 6.0f));
-      const float c1 = fabsf(fabsf(q.y) - fminf(fabsf(y1), 6.0f));
-      A4 = fmaf(c0, fmaf(e2m1_step_x2(y0), 0.5f, -c0), A4);
-      A4 = fmaf(c1, fmaf(e2m1_step_x2(y1), 0.5f, -c1), A4);
+      const float2 y = __fmul2_rn(va, inv2);
+      const float2 yc = make_float2(fminf(y.x, 6.0f), fminf(y.y, 6.0f));
+      const float2 H = make_float2(e2m1_step_x2(yc.x), e2m1_step_x2(yc.y));
+      const float2 q = RND ? grid_sr2(yc, H, g17, 4194304.0f) : grid_rn2(yc, H, 4194304.0f);
+      if (CF == 1) cw[i >> 3] |= e2m1x2_rn(copysignf(q.x, v[i]), copysignf(q.y, v[i + 1])) << (4 * (i & 7));
+      const float2 d = __ffma2_rn(q, np2, va);            // |x| - |x_hat|
+      e4 = __ffma2_rn(d, d, e4);
+      const float2 c = __ffma2_rn(yc, m1, q);
+      S4 = __ffma2_rn(c, c, S4);
+      T4 = fmaf(fabsf(c.x), H.x, T4);
+      T4 = fmaf(fabsf(c.y), H.y, T4);
     }
     // ---------------- FP8
     if (special8) {
@@ -221,43 +238,31 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       for (int k = 0; k < 2; ++k) {
         const float q = v[i + k] == 0.0f ? 0.0f : copysignf(448.0f, v[i + k]);
         const float d = fmaf(q, s8, -v[i + k]);
-        be8 = fmaf(d, d, be8);
+        se8 = fmaf(d, d, se8);
       }
     } else {
-      float y0, y1;
-      float2 q;
-      if (RND == 0) {
-        y0 = __fmul_rn(v[i], inv8);
-        y1 = __fmul_rn(v[i + 1], inv8);
-        const uint32_t pair = e4m3x2_rn_sat(y0, y1);
-        if (CF == 0) cw[i >> 2] |= pair << (8 * (i & 3));
-        q = e4m3x2_decode(pair);
-      } else {
-        y0 = __fmul_rn(fabsf(v[i]), inv8);
-        y1 = __fmul_rn(fabsf(v[i + 1]), inv8);
-        const uint32_t mag = e4m3_sr(y0, uhalf(u, i)) | (e4m3_sr(y1, uhalf(u, i + 1)) << 8);
-        if (CF == 0) cw[i >> 2] |= (mag | (sg0 << 7) | (sg1 << 15)) << (8 * (i & 3));
-        q = e4m3x2_decode(mag);
-      }
-      const float d0 = fmaf(q.x, s8, RND ? -fabsf(v[i]) : -v[i]);
-      const float d1 = fmaf(q.y, s8, RND ? -fabsf(v[i + 1]) : -v[i + 1]);
-      be8 = fmaf(d0, d0, fmaf(d1, d1, be8));
-      const float c0 = fabsf(fabsf(q.x) - fminf(fabsf(y0), 448.0f));
-      const float c1 = fabsf(fabsf(q.y) - fminf(fabsf(y1), 448.0f));
-      A8 = fmaf(c0, fmaf(e4m3_step_x8(y0), 0.125f, -c0), A8);
-      A8 = fmaf(c1, fmaf(e4m3_step_x8(y1), 0.125f, -c1), A8);
+      const float2 y = __fmul2_rn(va, i8);
+      const float2 yc = make_float2(fminf(y.x, 448.0f), fminf(y.y, 448.0f));
+      const float2 H = make_float2(e4m3_step_x8(yc.x), e4m3_step_x8(yc.y));
+      const float2 q = RND ? grid_sr2(yc, H, g19, 1048576.0f) : grid_rn2(yc, H, 1048576.0f);
+      if (CF == 0) cw[i >> 2] |= e4m3x2_rn_sat(copysignf(q.x, v[i]), copysignf(q.y, v[i + 1])) << (8 * (i & 3));
+      const float2 d = __ffma2_rn(q, ns8, va);
+      e8 = __ffma2_rn(d, d, e8);
+      const float2 c = __ffma2_rn(yc, m1, q);
+      S8 = __ffma2_rn(c, c, S8);
+      T8 = fmaf(fabsf(c.x), H.x, T8);
+      T8 = fmaf(fabsf(c.y), H.y, T8);
     }
   }
   // the variances were summed in units of the scale
-  const float bv4 = bs.special ? 0.0f : A4 * (bs.p * bs.p);
-  const float bv8 = special8 ? 0.0f : A8 * (s8 * s8);
+  const float a4 = fmaf(0.5f, T4, -(S4.x + S4.y)), a8 = fmaf(0.125f, T8, -(S8.x + S8.y));
   codes = make_uint4(cw[0], cw[1], cw[2], cw[3]);
   BlockStats r;
-  r.x2 = bx2;
-  r.e4 = be4;
-  r.e8 = be8;
-  r.v4 = bv4;
-  r.v8 = bv8;
+  r.x2 = x2.x + x2.y;
+  r.e4 = bs.special ? se4 : e4.x + e4.y;
+  r.e8 = special8 ? se8 : e8.x + e8.y;
+  r.v4 = bs.special ? 0.0f : a4 * (bs.p * bs.p);
+  r.v8 = special8 ? 0.0f : a8 * (s8 * s8);
   return r;
 }
 
@@ -265,21 +270,32 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
 // to finish adds all CTAs' partials and writes the raw statistics vector.
 __device__ __forceinline__ void stats_finish(float sx2, float e4, float e8, float v4, float v8, double* partials,
                                              uint32_t* counter, double* raw_out, float amax, int64_t count) {
-  double acc[5] = {(double)sx2, (double)e4, (double)e8, (double)v4, (double)v8};
-  block_sum_f64<5>(acc);
+  // within the CTA in fp32 (256 partial sums: a few ulps), across CTAs in fp64
+  float acc[5] = {sx2, e4, e8, v4, v8};
+  block_sum_f32<5>(acc);
   __shared__ bool s_last;
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 5; ++k) partials[(int64_t)blockIdx.x * 5 + k] = acc[k];
+    for (int k = 0; k < 5; ++k) partials[(int64_t)blockIdx.x * 5 + k] = (double)acc[k];
     __threadfence();
     s_last = atomicAdd(counter, 1u) == gridDim.x - 1;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // the last CTA: warp k adds quantity k of every CTA's partials
   double tot[5] = {0, 0, 0, 0, 0};
-  for (uint32_t j = threadIdx.x; j < gridDim.x; j += blockDim.x)
-    for (int k = 0; k < 5; ++k) tot[k] += ((volatile double*)partials)[(int64_t)j * 5 + k];
-  block_sum_f64<5>(tot);
+  const uint32_t w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __shared__ double s_tot[5];
+  if (w < 5) {
+    double t = 0.0;
+    for (uint32_t j = l; j < gridDim.x; j += 32) t += ((volatile double*)partials)[(int64_t)j * 5 + w];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (l == 0) s_tot[w] = t;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int k = 0; k < 5; ++k) tot[k] = s_tot[k];
   if (threadIdx.x == 0) {
     for (int k = 0; k < 5; ++k) raw_out[k] = tot[k];
     raw_out[5] = (double)amax;
@@ -308,7 +324,7 @@ __device__ __forceinline__ void stats_nan(double* raw_out) {
 // the other formats keep their registers.  Without STATS p.group is read at run
 // time.
 template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS, bool LONG = false>
-__global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
+__global__ void __launch_bounds__(256, STATS ? 3 : 4) quant_rows_kernel(QuantParams p) {
   static_assert(!LONG || (FMT == 1 && STATS), "LONG: NVFP4 with fused statistics");
   static_assert(FMT < 2 || !ERR, "MXFP4 / E5M2 quantization has no block errors");
   // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
@@ -321,6 +337,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   // the two tensor scales (the one not used by this format feeds the statistics)
   const float g4 = STATS ? p.scales3[1] : g, s8 = STATS ? p.scales3[2] : g;
   const float six_g = __fmul_rn(6.0f, g4);
+  // p and 1/p of every NVFP4 block-scale code under g4
+  constexpr bool TAB = FMT == 1 || STATS;
+  __shared__ float2 s_tab[TAB ? kScaleCodes : 1];
+  if (TAB) {
+    fill_scale_table(s_tab, g4);
+    __syncthreads();
+  }
   const float inv8 = __frcp_rn(s8);
   const bool special8 = !(inv8 < kInf);
   // E5M2 codes beside the statistics: the E5M2 tensor scale's inverse (without statistics, inv8)
@@ -334,25 +357,37 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
   // segment -> (row, segment in row), stepped without a division per iteration
   const uint32_t seg0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const uint32_t wq = wstride / spr, wr = wstride - wq * spr;
-  uint32_t r = seg0 / spr, sr = seg0 - r * spr;
-  for (uint32_t seg = seg0; seg < total; seg += wstride, r += wq, sr += wr) {
-    if (sr >= spr) { sr -= spr; ++r; }
+  uint32_t nr = seg0 / spr, nsr = seg0 - nr * spr;
+  // software pipeline: the next segment's 32 bytes are requested before this one is encoded
+  uint4 na = make_uint4(0u, 0u, 0u, 0u), nb = na;
+  auto fetch = [&](uint32_t rr, uint32_t ss) {
+    const uint32_t kk = ss * 32 + lane;
+    na = make_uint4(0u, 0u, 0u, 0u);
+    nb = na;
+    if (rr < p.out_rows && (int64_t)kk * 16 < p.out_cols) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (int64_t)rr * p.cols + (int64_t)kk * 16);
+      na = __ldg(src);
+      nb = __ldg(src + 1);
+    }
+  };
+  if (seg0 < total) fetch(nr, nsr);
+  for (uint32_t seg = seg0; seg < total; seg += wstride) {
+    const uint32_t r = nr, sr = nsr;
+    const uint4 a = na, b = nb;
+    nr += wq;
+    nsr += wr;
+    if (nsr >= spr) { nsr -= spr; ++nr; }
+    if (seg + wstride < total) fetch(nr, nsr);
     const uint32_t kb = sr * 32 + lane;
     // MXFP4 lanes, and NVFP4 lanes of longer blocks, leave after the shuffles that share block maxima
     const bool longer = FMT == 1 && (STATS ? LONG : p.group > 1);
     if (FMT != 2 && kb >= bpr && !longer) continue;
     const bool real = r < p.out_rows && (int64_t)kb * 16 < p.out_cols;
-    uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
     const int64_t e0 = (int64_t)r * p.cols + (int64_t)kb * 16;
-    if (real) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + e0);
-      a = __ldg(src);
-      b = __ldg(src + 1);
-    }
     float v[16];
     unpack16(a, b, v);
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (RND == 1 && real) sr_bits16(e0 + (int64_t)p.index_base, p.seed, p.stream_id, u);
+    if (RND == 1 && real) sr_bits16_rk(e0 + (int64_t)p.index_base, p.stream_id, p.rk, u);
     // bs: the 16-element NVFP4 scale (codes, and the statistics' NVFP4 candidate); bw: the scale
     // the codes are written with -- bs, or with longer blocks the scale of p.group 16-element blocks
     BlockScale bs, bw;
@@ -362,7 +397,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
       if (kb >= bpr) continue;
       bw = mxfp4_block_scale(m);
       // the statistics' NVFP4 candidate has its own 16-element scale; the codes use the E8M0 one
-      bs = STATS ? nvfp4_block_scale(m16, g4, six_g) : bw;
+      bs = STATS ? nvfp4_block_scale_tab(m16, six_g, s_tab) : bw;
     }
     if (longer) {
       // one scale for p.group consecutive 16-element blocks: lanes 2^k apart share their maxima
@@ -370,10 +405,10 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
       uint32_t m = m16;
       for (int o = 1; o < p.group; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (kb >= bpr) continue;
-      bw = nvfp4_block_scale(m, g4, six_g);
-      bs = STATS ? nvfp4_block_scale(m16, g4, six_g) : bw;
+      bw = nvfp4_block_scale_tab(m, six_g, s_tab);
+      bs = STATS ? nvfp4_block_scale_tab(m16, six_g, s_tab) : bw;
     } else if (FMT == 1 || STATS) {
-      bs = nvfp4_block_scale(amax16_bits(a, b), g4, six_g);
+      bs = nvfp4_block_scale_tab(amax16_bits(a, b), six_g, s_tab);
     }
     if (!longer && FMT != 2) bw = bs;
     uint4 c = make_uint4(0u, 0u, 0u, 0u);   // FP8: 16 codes; FP4: .x, .y
@@ -476,6 +511,8 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
   if (isnan(g)) return;
   const float six_g = __fmul_rn(6.0f, g);
   const float inv8 = __frcp_rn(g);
+  __shared__ float2 s_tab[FMT == 1 ? kScaleCodes : 1];
+  if (FMT == 1) fill_scale_table(s_tab, g);   // ordered before its reads by the staging barrier below
   const int64_t r0 = (int64_t)blockIdx.x * kTR;   // source row = output contraction index
   const int64_t c0 = (int64_t)blockIdx.y * kTC;   // source col = output row
   const int t = threadIdx.x;
@@ -489,7 +526,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
     *reinterpret_cast<uint4*>(&xs[row][ch * 4]) = v;
     if (RND == 1) {
       U4 w = make_zero_u4();
-      if (in) w = sr_words(((uint64_t)(gr * p.cols + gc) + p.index_base) >> 3, p.seed, p.stream_id);
+      if (in) w = sr_words_rk(((uint64_t)(gr * p.cols + gc) + p.index_base) >> 3, p.stream_id, p.rk);
       *reinterpret_cast<uint4*>(&rs[row][ch * 4]) = make_uint4(w.x, w.y, w.z, w.w);
     }
   }
@@ -536,7 +573,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
           m1 = max(m1, amx[b0 + j][cp][1]);
         }
       }
-      const BlockScale s0 = nvfp4_block_scale(m0, g, six_g), s1 = nvfp4_block_scale(m1, g, six_g);
+      const BlockScale s0 = nvfp4_block_scale_tab(m0, six_g, s_tab), s1 = nvfp4_block_scale_tab(m1, six_g, s_tab);
       const uint2 e0 = nvfp4_encode16<RND>(v0, s0, u0), e1 = nvfp4_encode16<RND>(v1, s1, u1);
       oc[2 * cp][2 * b] = e0.x; oc[2 * cp][2 * b + 1] = e0.y;
       oc[2 * cp + 1][2 * b] = e1.x; oc[2 * cp + 1][2 * b + 1] = e1.y;
@@ -623,6 +660,9 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
   const float six_g = __fmul_rn(6.0f, g);
   const float inv8 = __frcp_rn(s8);
   const bool special8 = !(inv8 < kInf);
+  __shared__ float2 s_tab[kScaleCodes];
+  fill_scale_table(s_tab, g);
+  __syncthreads();
   const uint32_t bpr = (uint32_t)(p.cols >> 4);
   const uint32_t spr = (bpr + 31) >> 5;
   const uint32_t total = (uint32_t)p.rows * spr;
@@ -632,19 +672,33 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
   // segment -> (row, segment in row), stepped without a division per iteration
   const uint32_t seg0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const uint32_t wq = wstride / spr, wr = wstride - wq * spr;
-  uint32_t r = seg0 / spr, sr = seg0 - r * spr;
-  for (uint32_t seg = seg0; seg < total; seg += wstride, r += wq, sr += wr) {
-    if (sr >= spr) { sr -= spr; ++r; }
+  uint32_t nr = seg0 / spr, nsr = seg0 - nr * spr;
+  // software pipeline: the next segment's 32 bytes are requested before this one is evaluated
+  uint4 na = make_uint4(0u, 0u, 0u, 0u), nb = na;
+  auto fetch = [&](uint32_t rr, uint32_t ss) {
+    const uint32_t kk = ss * 32 + lane;
+    if (kk < bpr) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (int64_t)rr * p.cols + (int64_t)kk * 16);
+      na = __ldg(src);
+      nb = __ldg(src + 1);
+    }
+  };
+  if (seg0 < total) fetch(nr, nsr);
+  for (uint32_t seg = seg0; seg < total; seg += wstride) {
+    const uint32_t r = nr, sr = nsr;
+    const uint4 a = na, b = nb;
+    nr += wq;
+    nsr += wr;
+    if (nsr >= spr) { nsr -= spr; ++nr; }
+    if (seg + wstride < total) fetch(nr, nsr);
     const uint32_t kb = sr * 32 + lane;
     if (kb >= bpr) continue;
     const int64_t e0 = (int64_t)r * p.cols + (int64_t)kb * 16;
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + e0);
-    const uint4 a = __ldg(src), b = __ldg(src + 1);
     float v[16];
     unpack16(a, b, v);
     uint32_t u[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (RND == 1) sr_bits16(e0, p.seed, p.stream_id, u);
-    const BlockScale bs = nvfp4_block_scale(amax16_bits(a, b), g, six_g);
+    if (RND == 1) sr_bits16_rk(e0, p.stream_id, p.rk, u);
+    const BlockScale bs = nvfp4_block_scale_tab(amax16_bits(a, b), six_g, s_tab);
     uint4 unused;
     const BlockStats st = stats_block16<-1, RND>(v, bs, u, s8, inv8, special8, unused);
     sx2 += st.x2;
@@ -659,45 +713,6 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
     }
   }
   stats_finish(sx2, e4, e8, v4, v8, p.partials, p.counter, p.raw_out, amax, p.rows * p.cols);
-}
-
-// ------------------------------------------------------------------ NEXT-4: dW-level noise
-// ||ref||^2 and ||q - ref||^2 over n fp32 values (n % 4 == 0): 16-byte loads,
-// fp32 per thread, fp64 across CTAs, the last CTA writes out2.
-__global__ void __launch_bounds__(256) dw_noise_kernel(const float4* __restrict__ q, const float4* __restrict__ ref,
-                                                       int64_t n4, double* __restrict__ partials,
-                                                       uint32_t* __restrict__ counter, double* __restrict__ out2) {
-  float s_ref = 0.f, s_err = 0.f;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 a = __ldcs(q + i), b = __ldcs(ref + i);
-    s_ref = fmaf(b.x, b.x, fmaf(b.y, b.y, fmaf(b.z, b.z, fmaf(b.w, b.w, s_ref))));
-    const float d0 = a.x - b.x, d1 = a.y - b.y, d2 = a.z - b.z, d3 = a.w - b.w;
-    s_err = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, s_err))));
-  }
-  double acc[2] = {(double)s_ref, (double)s_err};
-  block_sum_f64<2>(acc);
-  __shared__ bool s_last;
-  if (threadIdx.x == 0) {
-    partials[2 * blockIdx.x] = acc[0];
-    partials[2 * blockIdx.x + 1] = acc[1];
-    __threadfence();
-    s_last = atomicAdd(counter, 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  double tot[2] = {0.0, 0.0};
-  for (uint32_t j = threadIdx.x; j < gridDim.x; j += blockDim.x) {
-    tot[0] += ((volatile double*)partials)[2 * j];
-    tot[1] += ((volatile double*)partials)[2 * j + 1];
-  }
-  block_sum_f64<2>(tot);
-  if (threadIdx.x == 0) {
-    out2[0] = tot[0];
-    out2[1] = tot[1];
-    *counter = 0;
-  }
 }
 
 // ------------------------------------------------------------------ host-side launchers
@@ -855,14 +870,6 @@ cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, 
   else if (fmt == 2) launch_quant_mx(p, orient, layout, rnd, num_sms, st);
   else if (fmt == 1) launch_quant_fmt<1>(p, orient, layout, rnd, err, num_sms, st);
   else launch_quant_fmt<0>(p, orient, layout, rnd, false, num_sms, st);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dw_noise(const float* q, const float* ref, int64_t n, double* partials, uint32_t* counter,
-                            double* out2, int num_sms, cudaStream_t st) {
-  const int grid = fill_grid(n >> 2, 256 * 4, 4 * num_sms);
-  dw_noise_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(q), reinterpret_cast<const float4*>(ref),
-                                        n >> 2, partials, counter, out2);
   return cudaGetLastError();
 }
 

@@ -58,9 +58,13 @@ __device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
 // bits exactly when u16 < floor(frac * 2^16).  Returns the magnitude code.
 // Below 2^-6 the fixed point is floor(y * 2^29), read off the mantissa of
 // 2^-6 + y rounded toward zero (its ulp is 2^-29).
+// The two forms are combined without a branch: with T the bottom of the
+// normal range (here 2^-6), bits(y) - bits(T/2) is the larger of the two for
+// y >= T and negative or smaller below it, where bits(T + y rounded toward
+// zero) - bits(T) is the fixed point; so the base is their signed maximum.
 __device__ __forceinline__ uint32_t e4m3_sr_base(float y) {
-  return y >= 0.015625f ? __float_as_uint(y) - 0x3C000000u                 // (exp-120)<<23 | mantissa
-                        : __float_as_uint(__fadd_rz(y, 0.015625f)) - 0x3C800000u;
+  return (uint32_t)max((int32_t)(__float_as_uint(y) - 0x3C000000u),                      // (exp-120)<<23 | mantissa
+                       (int32_t)(__float_as_uint(__fadd_rz(y, 0.015625f)) - 0x3C800000u));
 }
 __device__ __forceinline__ uint32_t e4m3_sr_from_base(uint32_t base, uint32_t u16) {
   const uint32_t code = (base + ((65535u - u16) << 4)) >> 20;
@@ -79,8 +83,8 @@ __device__ __forceinline__ uint32_t e5m2x2_rn_sat(float lo, float hi) {
 // E4M3 with 21 dropped mantissa bits; below 2^-14 the fixed point is
 // floor(y * 2^37), the mantissa of 2^-14 + y rounded toward zero.
 __device__ __forceinline__ uint32_t e5m2_sr_base(float y) {
-  return y >= 6.103515625e-05f ? __float_as_uint(y) - 0x38000000u                 // (exp-112)<<23 | mantissa
-                               : __float_as_uint(__fadd_rz(y, 6.103515625e-05f)) - 0x38800000u;
+  return (uint32_t)max((int32_t)(__float_as_uint(y) - 0x38000000u),                      // (exp-112)<<23 | mantissa
+                       (int32_t)(__float_as_uint(__fadd_rz(y, 6.103515625e-05f)) - 0x38800000u));
 }
 __device__ __forceinline__ uint32_t e5m2_sr_from_base(uint32_t base, uint32_t u16) {
   const uint32_t code = (base + ((65535u - u16) << 5)) >> 21;
@@ -113,9 +117,10 @@ __device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
 // up.  Returns the magnitude code 0..7.
 // Below 1 the fixed point is floor(y * 2^23), the mantissa of 1 + y rounded
 // toward zero.
+// (Combined as for E4M3, with T = 1.)
 __device__ __forceinline__ uint32_t e2m1_sr_base(float y) {
-  return y >= 1.0f ? __float_as_uint(y) - 0x3F000000u                     // 2*(exp-126) | m1, << 22
-                   : __float_as_uint(__fadd_rz(y, 1.0f)) - 0x3F800000u;
+  return (uint32_t)max((int32_t)(__float_as_uint(y) - 0x3F000000u),                      // 2*(exp-126) | m1, << 22
+                       (int32_t)(__float_as_uint(__fadd_rz(y, 1.0f)) - 0x3F800000u));
 }
 __device__ __forceinline__ uint32_t e2m1_sr_from_base(uint32_t base, uint32_t u16) {
   const uint32_t code = (base + ((65535u - u16) << 6)) >> 22;
@@ -126,6 +131,58 @@ __device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t u16) { return e2m1
 // Value of an E2M1 magnitude code 0..7.
 __device__ __forceinline__ float e2m1_value(uint32_t m) {
   return m <= 4u ? __fmul_rn((float)m, 0.5f) : (m == 5u ? 3.0f : (m == 6u ? 4.0f : 6.0f));
+}
+
+// ------------------------------------------------------------------ grid rounding on the FMA pipe
+// The E2M1, E4M3 and E5M2 grids have a power-of-two step h at every y >= 0
+// (E2M1: 0.5 below 2, 1 below 4, 2 up to 6; E4M3: 2^(e-3), and 2^-9 below
+// 2^-6; E5M2: 2^(e-2), and 2^-16 below 2^-14).  With C = 2^23 h, y + C
+// rounded to fp32 is C plus a multiple of h, so for y clamped to the grid's
+// top (6, 448, 57344):
+//  - nearest, ties to even: q = (y + C) - C.  The even multiple of h is the
+//    value whose code has a 0 last bit, the even code of the rule.
+//  - stochastic with 16 random bits u and n = 65535 - u:
+//    q = RZ(RZ(y + h n / 2^16) + C) - C.  y + h n / 2^16 reaches the upper
+//    neighbour hi = lo + h exactly when y - lo >= h (u + 1) / 2^16, i.e. when
+//    u < floor(frac 2^16): the 16-bit rule.  Rounding toward zero never moves
+//    a sum across a grid value (grid values are fp32 numbers), so the
+//    comparison is exact.
+// Both return the grid value itself (as fp32), and they run on the FMA pipe;
+// the integer forms above use the slower integer pipe.  H is a fixed
+// multiple of h per grid (the *_step_x* helpers) and k = 2^23 h / H.
+__device__ __forceinline__ float2 grid_rn2(float2 yc, float2 H, float k) {
+  const float2 C = __fmul2_rn(H, make_float2(k, k));
+  return __ffma2_rn(C, make_float2(-1.0f, -1.0f), __fadd2_rn(yc, C));   // exact: the sum is C plus a multiple of h
+}
+// g = h n / 2^16 / H (sr_g2)
+__device__ __forceinline__ float2 grid_sr2(float2 yc, float2 H, float2 g, float k) {
+  const float2 t = __fadd2_rz(yc, __fmul2_rn(H, g));                     // H g = h n / 2^16, exact
+  const float2 C = __fmul2_rn(H, make_float2(k, k));
+  return __ffma2_rn(C, make_float2(-1.0f, -1.0f), __fadd2_rz(t, C));
+}
+// The float 2^23 + u of a 16-bit value u (its bits: 0x4B000000 | u): the low
+// (HI false) or high half of a random word, with one byte permutation.
+template <bool HI>
+__device__ __forceinline__ float sr_f23(uint32_t word) {
+  return __uint_as_float(__byte_perm(word, 0x4B000000u, HI ? 0x7632u : 0x7610u));
+}
+// n / 2^S with n = 65535 - u for a pair of sr_f23 values: (2^23 + 65535 - f) / 2^S, exact.
+template <int S>
+__device__ __forceinline__ float2 sr_g2(float f0, float f1) {
+  constexpr float kNeg = -1.0f / (float)(1u << S);
+  constexpr float kAdd = 8454143.0f / (float)(1u << S);   // (2^23 + 65535) / 2^S
+  return __ffma2_rn(make_float2(f0, f1), make_float2(kNeg, kNeg), make_float2(kAdd, kAdd));
+}
+// Twice, eight and four times the E2M1, E4M3 and E5M2 step at y >= 0 (the
+// exponent of y as a power of two, at least the grid's bottom binade).
+__device__ __forceinline__ float e2m1_step_x2(float y) {
+  return fmaxf(__uint_as_float(__float_as_uint(y) & 0x7f800000u), 1.0f);
+}
+__device__ __forceinline__ float e4m3_step_x8(float y) {
+  return fmaxf(__uint_as_float(__float_as_uint(y) & 0x7f800000u), 0.015625f);
+}
+__device__ __forceinline__ float e5m2_step_x4(float y) {
+  return fmaxf(__uint_as_float(__float_as_uint(y) & 0x7f800000u), 6.103515625e-05f);
 }
 
 // ------------------------------------------------------------------ Philox4x32-10
@@ -145,6 +202,38 @@ __device__ __forceinline__ U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c
     c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
   }
   return U4{c0, c1, c2, c3};
+}
+
+// The round keys of one seed: round r uses (k[r], k[10 + r]), the seed's two
+// words plus r Weyl steps.  Computed once on the host and passed in a kernel's
+// parameters, the rounds read them as constants and spend no instruction on
+// the key schedule.
+struct PhiloxKey { uint32_t k[20]; };
+__host__ __device__ inline PhiloxKey philox_round_keys(uint64_t seed) {
+  PhiloxKey r;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    r.k[i] = k0;
+    r.k[10 + i] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return r;
+}
+__device__ __forceinline__ U4 philox4x32_10_rk(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, const PhiloxKey& rk) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ rk.k[r], n2 = hi0 ^ c3 ^ rk.k[10 + r];
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+  }
+  return U4{c0, c1, c2, c3};
+}
+// sr_words with the seed's round keys
+__device__ __forceinline__ U4 sr_words_rk(uint64_t group, uint64_t stream_id, const PhiloxKey& rk) {
+  return philox4x32_10_rk((uint32_t)group, (uint32_t)(group >> 32), (uint32_t)stream_id, (uint32_t)(stream_id >> 32),
+                          rk);
 }
 
 // The 4 random words covering source elements 8*group .. 8*group+7: element

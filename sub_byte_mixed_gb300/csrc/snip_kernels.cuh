@@ -16,6 +16,7 @@ struct QuantParams {
   int64_t out_rows, out_cols;   // output orientation (out_cols = the blocked/contraction dim)
   int64_t orp, ocp;             // padded output dims (== out_rows/out_cols for the row-major layout)
   uint64_t seed, stream_id;
+  PhiloxKey rk;                 // round keys of seed (philox_round_keys)
   const float* scale;           // device fp32 tensor scale to use (NVFP4 g or FP8 s)
   uint8_t* codes;
   uint8_t* scales;              // NVFP4 only
@@ -36,6 +37,7 @@ struct StatsParams {
   const uint16_t* x;
   int64_t rows, cols;
   uint64_t seed, stream_id;
+  PhiloxKey rk;                 // round keys of seed
   const float* scales3;         // {amax, NVFP4 g, FP8 s}
   double* partials;             // 5 doubles per CTA
   uint32_t* counter;
@@ -95,6 +97,31 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v) {
   return v;
 }
 
+// Sum of N floats over the CTA; result valid in thread 0.  (The fp64 pipe of
+// this GPU is a small fraction of its fp32 rate: sums within a CTA stay fp32.)
+template <int N>
+__device__ __forceinline__ void block_sum_f32(float (&v)[N]) {
+  __shared__ float red32[32][N];
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (l == 0)
+#pragma unroll
+    for (int k = 0; k < N; ++k) red32[w][k] = v[k];
+  __syncthreads();
+  if (w == 0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      v[k] = l < nw ? red32[l][k] : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    }
+  }
+}
+
 // Sum of N doubles over the CTA; result valid in thread 0.
 template <int N>
 __device__ __forceinline__ void block_sum_f64(double (&v)[N]) {
@@ -136,9 +163,11 @@ cudaError_t launch_scales_multi(ScalesMulti m, uint32_t* partials, uint32_t* cou
 cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
                          cudaStream_t st);
 cudaError_t launch_stats(const StatsParams& p, int rnd, int num_sms, cudaStream_t st);
-// {||ref||^2, ||q - ref||^2} of n fp32 values (n % 4 == 0) into out2 (device).
-cudaError_t launch_dw_noise(const float* q, const float* ref, int64_t n, double* partials, uint32_t* counter,
-                            double* out2, int num_sms, cudaStream_t st);
+// {||dW||^2, ||dW_q - dW||^2} into out2 (device) with dW = dY^T X from the bf16 tensors X (T x K) and
+// dY (T x N), dW_q N x K fp32: a bf16 tensor-core GEMM with the two sums in its epilogue (dw_noise.cu).
+cudaError_t launch_dw_noise_gemm(const void* X, const void* dY, int64_t T, int64_t K, int64_t N, const float* dwq,
+                                 double* partials, uint32_t* counter, double* out2, uint32_t* status,
+                                 uint64_t timeout_ns, int num_sms, cudaStream_t st);
 
 // GEMM: D = ga*gb*A B^T on MMA-layout operands.  fmt 1 = NVFP4, 2 = MXFP4 (ga, gb
 // null: no tensor scales), 0 = FP8 (p.a_e5m2: A in E5M2, B in E4M3).

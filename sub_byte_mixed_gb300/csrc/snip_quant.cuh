@@ -57,6 +57,25 @@ __device__ __forceinline__ BlockScale nvfp4_block_scale(uint32_t amax_bits, floa
   return r;
 }
 
+// The same scale with p and 1/p read from a table of all E4M3 scale codes
+// (fill_scale_table): the division and the E4M3 rounding stay per block.
+constexpr int kScaleCodes = 128;
+__device__ __forceinline__ void fill_scale_table(float2* tab, float g) {
+  for (int c = threadIdx.x; c < kScaleCodes; c += blockDim.x) {
+    const float pc = __fmul_rn(e4m3_decode_pos((uint32_t)c), g);
+    tab[c] = make_float2(pc, __frcp_rn(pc));
+  }
+}
+__device__ __forceinline__ BlockScale nvfp4_block_scale_tab(uint32_t amax_bits, float six_g, const float2* tab) {
+  BlockScale r;
+  r.s = e4m3_rn_sat(__fdiv_rn(bf16_bits_to_float(amax_bits), six_g));
+  const float2 t = tab[r.s];
+  r.p = t.x;
+  r.inv = t.y;
+  r.special = !(r.inv < kInf);
+  return r;
+}
+
 // MXFP4 block scale (OCP Microscaling v1.0) from the 32-block's largest
 // magnitude as a bf16 bit pattern: E8M0 code = max(exponent field - 2, 0),
 // i.e. 2^(floor(log2 amax) - 2) clamped at 2^-127 (subnormal or zero amax);
@@ -79,6 +98,12 @@ __device__ __forceinline__ void sr_bits16(int64_t e0, uint64_t seed, uint64_t si
   u[0] = w0.x; u[1] = w0.y; u[2] = w0.z; u[3] = w0.w;
   u[4] = w1.x; u[5] = w1.y; u[6] = w1.z; u[7] = w1.w;
 }
+__device__ __forceinline__ void sr_bits16_rk(int64_t e0, uint64_t sid, const PhiloxKey& rk, uint32_t (&u)[8]) {
+  const U4 w0 = sr_words_rk((uint64_t)e0 >> 3, sid, rk);
+  const U4 w1 = sr_words_rk(((uint64_t)e0 >> 3) + 1, sid, rk);
+  u[0] = w0.x; u[1] = w0.y; u[2] = w0.z; u[3] = w0.w;
+  u[4] = w1.x; u[5] = w1.y; u[6] = w1.z; u[7] = w1.w;
+}
 // random half of element i from the packed words (element i in half i%2 of word i/2)
 __device__ __forceinline__ uint32_t uhalf(const uint32_t (&u)[8], int i) {
   return (i & 1) ? (u[i >> 1] >> 16) : (u[i >> 1] & 0xffffu);
@@ -86,9 +111,11 @@ __device__ __forceinline__ uint32_t uhalf(const uint32_t (&u)[8], int i) {
 
 // Sources of the 16 random bits of element i of a block, for the encoders:
 // packed two per word (element i in half i%2 of word i/2) ...
+// Each also gives f23(i) = 2^23 + u16 as a float (sr_f23), for the FMA-pipe rounding.
 struct PackedBits {
   const uint32_t* u;
   __device__ __forceinline__ uint32_t operator()(int i) const { return (i & 1) ? (u[i >> 1] >> 16) : (u[i >> 1] & 0xffffu); }
+  __device__ __forceinline__ float f23(int i) const { return (i & 1) ? sr_f23<true>(u[i >> 1]) : sr_f23<false>(u[i >> 1]); }
 };
 // ... or one word per element, shared by two source columns: the even column's
 // bits in the low half (HI false), the odd column's in the high half.
@@ -96,6 +123,7 @@ template <bool HI>
 struct WordHalfBits {
   const uint32_t* r;
   __device__ __forceinline__ uint32_t operator()(int i) const { return HI ? (r[i] >> 16) : (r[i] & 0xffffu); }
+  __device__ __forceinline__ float f23(int i) const { return sr_f23<HI>(r[i]); }
 };
 
 // Encode one NVFP4 block of 16 signed values into two words of packed codes
@@ -116,11 +144,14 @@ __device__ __forceinline__ uint2 nvfp4_encode16(const float (&v)[16], const Bloc
     for (int i = 0; i < 8; ++i)
       w[i >> 2] |= e2m1x2_rn(__fmul_rn(v[2 * i], bs.inv), __fmul_rn(v[2 * i + 1], bs.inv)) << (8 * (i & 3));
   } else {
+    // stochastic rounding on the FMA pipe (grid_sr2), the code converted from the exact grid value
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t b = __float_as_uint(v[i]);
-      const float y = __fmul_rn(__uint_as_float(b & 0x7fffffffu), bs.inv);
-      w[i >> 3] |= (((b >> 28) & 8u) | e2m1_sr(y, bits(i))) << (4 * (i & 7));
+    for (int i = 0; i < 16; i += 2) {
+      const float2 y = __fmul2_rn(make_float2(fabsf(v[i]), fabsf(v[i + 1])), make_float2(bs.inv, bs.inv));
+      const float2 yc = make_float2(fminf(y.x, 6.0f), fminf(y.y, 6.0f));
+      const float2 H = make_float2(e2m1_step_x2(yc.x), e2m1_step_x2(yc.y));
+      const float2 q = grid_sr2(yc, H, sr_g2<17>(bits.f23(i), bits.f23(i + 1)), 4194304.0f);
+      w[i >> 3] |= e2m1x2_rn(copysignf(q.x, v[i]), copysignf(q.y, v[i + 1])) << (4 * (i & 7));
     }
   }
   return make_uint2(w[0], w[1]);

@@ -3,7 +3,10 @@ on another, operand buffers alternating between two sets by linear), issued
 call by call and replayed from a captured CUDA graph, against the same calls
 on one stream: Y, dX, dW and the statistics of every linear
 must be identical, so no GEMM reads an operand before its quantization has
-written it or after the next user of its buffer set has overwritten it."""
+written it or after the next user of its buffer set has overwritten it.  The
+step that computes a shared activation's scales, statistics and forward
+quantization once (Q/K/V, Gate/Up) gives exactly the results of the step that
+recomputes them for every linear."""
 import os
 import sys
 
@@ -25,12 +28,24 @@ def test_two_stream_step_matches_one_stream(plan_kind):
     cfg = inputs.TINYLLAMA
     plan = (inputs.seeded_plan(cfg, cfg.fp4_target, seed=0) if plan_kind == "mix"
             else inputs.all_plan(bench.FORMAT_OF_NAME[plan_kind]))
+    unshared = bench.Step(cfg, plan, snip, "cuda", overlap=False, share_x=False)
+    unshared.run()
+    torch.cuda.synchronize()
+    assert unshared.status() == snip.SNIP_OK
+    ref0 = ([y.clone() for y in unshared.Y], [d.clone() for d in unshared.dX], [w.clone() for w in unshared.dW],
+            unshared.stats_host())
+    assert unshared.launches_per_step > 0
+    del unshared
     serial = bench.Step(cfg, plan, snip, "cuda", overlap=False)
     serial.run()
     torch.cuda.synchronize()
     assert serial.status() == snip.SNIP_OK
     ref = ([y.clone() for y in serial.Y], [d.clone() for d in serial.dX], [w.clone() for w in serial.dW],
            serial.raw.clone())
+    for j in range(len(cfg.linears)):
+        assert torch.equal(ref[0][j], ref0[0][j]) and torch.equal(ref[1][j], ref0[1][j]), ("shared X", j)
+        assert torch.equal(ref[2][j], ref0[2][j]), ("shared X", j)
+    assert (serial.stats_host() == ref0[3]).all()
     del serial
     over = bench.Step(cfg, plan, snip, "cuda", overlap=True)
     for _ in range(2):   # the second step also reuses both buffer sets across the step boundary
