@@ -692,6 +692,95 @@ def requant_compare(snip, reps: int = 10):
     return out
 
 
+def chain_compare(snip, reps: int = 5):
+    """NEXT-3 in the layer path on the 7B block: the backward of Down (K = 11008, N = 4096) and of the
+    linear before it, Up (K = 4096, N = 11008), whose dY is Down's dX (T = 8192).  Unfused: Down's
+    snip_qlinear_bwd writes fp32 dX, a bf16 copy of it is Up's dY, and Up's snip_qlinear_bwd quantizes
+    it (just-in-time scale).  Fused: snip_qlinear_bwd_chain writes Up's two NVFP4 gradient operands in
+    Down's dgrad epilogue (delayed scale), and snip_qlinear_bwd_q runs Up's backward from them."""
+    import torch
+    from sub_byte_mixed_gb300 import inputs
+    cfg = inputs.LLAMA7B
+    names = [l.name for l in cfg.linears]
+    jd, ju = names.index("Down"), names.index("Up")
+    Xd, Wd, dYd = inputs.linear_inputs(cfg, jd, seed=0, device="cuda")
+    Xu, Wu, _ = inputs.linear_inputs(cfg, ju, seed=0, device="cuda")
+    T = cfg.T
+    plan = snip.Plan([1] * len(cfg.linears), seed=0)
+    wsd = snip.qlinear_workspace(plan, jd, T, cfg.linears[jd].K, cfg.linears[jd].N)
+    wsu = snip.qlinear_workspace(plan, ju, T, cfg.linears[ju].K, cfg.linears[ju].N)
+    dX = torch.empty((T, cfg.linears[jd].K), dtype=torch.float32, device="cuda")
+    dWd = torch.empty((cfg.linears[jd].N, cfg.linears[jd].K), dtype=torch.float32, device="cuda")
+    dYu = torch.empty((T, cfg.linears[jd].K), dtype=torch.bfloat16, device="cuda")
+    dXu = torch.empty((T, cfg.linears[ju].K), dtype=torch.float32, device="cuda")
+    dWu = torch.empty((cfg.linears[ju].N, cfg.linears[ju].K), dtype=torch.float32, device="cuda")
+    snip.qlinear_bwd(plan, jd, Xd, Wd, dYd, wsd, dX=dX, dW=dWd)
+    g = (snip.tensor_scales(dX.to(torch.bfloat16))[1:2]).clone()   # the delayed scale: a previous step's
+
+    def unfused():
+        snip.qlinear_bwd(plan, jd, Xd, Wd, dYd, wsd, dX=dX, dW=dWd)
+        dYu.copy_(dX)
+        snip.qlinear_bwd(plan, ju, Xu, Wu, dYu, wsu, dX=dXu, dW=dWu)
+
+    def fused():
+        _, _, rows, cols, _ = snip.qlinear_bwd_chain(plan, jd, ju, Xd, Wd, dYd, g, wsd)
+        snip.qlinear_bwd_q(plan, ju, Xu, Wu, rows, cols, wsu, dX=dXu, dW=dWu)
+
+    out = {}
+    for name, fn in (("unfused_ms", unfused), ("fused_ms", fused)):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = round(e0.elapsed_time(e1) / reps, 4)
+    if wsd.status() != snip.SNIP_OK or wsu.status() != snip.SNIP_OK:
+        raise RuntimeError("device status")
+    out["saved_ms"] = round(out["unfused_ms"] - out["fused_ms"], 4)
+    out["what"] = ("backward of the 7B block's Down and Up linears (T = 8192), Up's dY = Down's dX: fused "
+                   "(chain + backward from quantized operands) vs unfused (fp32 dX, bf16 copy, quantize)")
+    return out
+
+
+def dw_noise_time(snip, bf16_peak: float, reps: int = 10):
+    """NEXT-4 at the 7B block's Down linear (T = 8192, K = 11008, N = 4096): snip_dw_noise, the bf16
+    tensor-core GEMM dW = dY^T X with ||dW||^2 and ||dW_q - dW||^2 in its epilogue, against the
+    measured bf16 burst peak (the kernel is timed alone, back to back, operands from HBM: 247 MB of
+    bf16 inputs and 180 MB of dW_q)."""
+    import torch
+    from sub_byte_mixed_gb300 import inputs
+    cfg = inputs.LLAMA7B
+    j = [l.name for l in cfg.linears].index("Down")
+    X, W, dY = inputs.linear_inputs(cfg, j, seed=0, device="cuda")
+    T, K, N = cfg.T, cfg.linears[j].K, cfg.linears[j].N
+    dwq = torch.randn((N, K), dtype=torch.float32, device="cuda")
+    ws = snip.Workspace(snip.snip_dw_noise_workspace_size(K, N))
+    out = torch.empty(2, dtype=torch.float64, device="cuda")
+    L = snip.load()
+    args = (X.data_ptr(), dY.data_ptr(), T, K, N, dwq.data_ptr(), out.data_ptr(), ws.ptr, ws.nbytes,
+            torch.cuda.current_stream().cuda_stream)
+    for _ in range(2):
+        if L.snip_dw_noise(*args) != 0:
+            raise RuntimeError("snip_dw_noise failed")
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        L.snip_dw_noise(*args)
+    e1.record()
+    torch.cuda.synchronize()
+    if ws.status() != snip.SNIP_OK:
+        raise RuntimeError("device status " + snip.status_string(ws.status()))
+    ms = e0.elapsed_time(e1) / reps
+    tf = 2.0 * T * K * N / (ms * 1e-3) / 1e12
+    return {"shape": f"T={T} K={K} N={N} (7B Down)", "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+            "frac_bf16_burst": round(tf / bf16_peak, 3),
+            "what": "bf16 tcgen05 GEMM dW = dY^T X, norms of dW and dW_q - dW in its epilogue; dW never stored"}
+
+
 def e2e_run(cfg, plan, snip, step: Step, nsteps: int, rounds_n: int = 5, with_outputs: bool = False):
     """The same step through the layer API (snip_qlinear_fwd / _bwd, statistics fused into their
     quantizations) with host buffers: every step copies all inputs (X, W, dY, bf16) in from pinned host
@@ -950,10 +1039,12 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.summary(t0, t2) if sampler else None
     if sampler:
         sampler.stop()
-    qsweep = rqcmp = None
+    qsweep = rqcmp = dwn = chn = None
     if not args.profile_run and not layers and rank == 0:
         qsweep = quantizer_sweep(snip, measured_peaks()["hbm_gbs"])
         rqcmp = requant_compare(snip)
+        dwn = dw_noise_time(snip, measured_peaks()["bf16"])
+        chn = chain_compare(snip)
     e2e = e2e_out = None
     if not args.no_e2e and not args.profile_run and not layers and rank == 0:
         e2e = e2e_run(cfg, plan, snip, step, args.e2e_steps)
@@ -1014,6 +1105,8 @@ def run_ours(args, rank, world, local_rank):
         "gemm_only": {"value": gemm_fl / (gemm_ms * 1e-3) / 1e12, "unit": UNIT},
         "quantizer_sweep": qsweep,
         "next3_requant": rqcmp,
+        "next4_dw_noise": dwn,
+        "next3_chain": chn,
         "breakdown": breakdown,
         "clocks": clocks,
         "e2e": e2e,

@@ -22,7 +22,9 @@
  * Conventions for every entry point
  *  - All tensor pointers are DEVICE pointers owned by the caller; the library
  *    allocates no device memory (except tensor memory inside its GEMM kernels,
- *    which is freed before each kernel exits).  Host pointers are marked.
+ *    which is freed before each kernel exits), links no other GPU library and
+ *    keeps no device state beyond the fixed scratch array of
+ *    snip_tensor_scales_noalloc.  Host pointers are marked.
  *  - Tensors are dense row-major.  bf16 inputs are passed as `const void*` to
  *    2-byte IEEE bfloat16 values.  Device pointers must be 16-byte aligned
  *    (SNIP_ERR_ALIGN otherwise).
@@ -156,8 +158,9 @@ const char* snip_status_string(snip_status s);
 /* ABI version (major*10000 + minor*100 + patch) of this header; snip_version()
  * returns the library's, which must match.  0.2.0: snip_requant gained the
  * column-block fields (NEXT-3), the longer-block NVFP4 formats,
- * snip_quantize_part and snip_wait_check. */
-#define SNIP_ABI_VERSION 200
+ * snip_quantize_part and snip_wait_check.  0.3.0: snip_qlinear_fwd_multi;
+ * snip_dw_noise needs only the small workspace (no K x N buffer). */
+#define SNIP_ABI_VERSION 300
 int snip_version(void);
 
 /* SNIP_OK if the current CUDA device can run the kernels (compute capability
@@ -440,6 +443,27 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
                              int64_t T, int64_t K, int64_t N, float* Y, double* stats_out,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* Forward of several layers that read one activation (SNIP, Figure 4: Q, K
+ * and V read the same X, Gate and Up another): for i < count,
+ * Y[i] = Q(X) Q(W[i])^T exactly as snip_qlinear_fwd(plan, layers[i], ...)
+ * computes it, with X's tensor scales and statistics computed once and X's
+ * quantization once per group of layers that quantize it alike (same
+ * forward format, round-to-nearest X_FWD rounding: the stream id is then
+ * irrelevant); a layer whose X_FWD rounding is stochastic quantizes X with
+ * its own stream id.  count in [1, 8]; layers (host) distinct layer indices;
+ * X device T x K bf16; W (host array) device N[i] x K bf16; N (host array);
+ * Y (host array) device T x N[i] fp32.  stats_x (device, nullable,
+ * SNIP_STATS_NVALS doubles): SNIP's statistics of X under the forward
+ * rounding; stats_w (host array or NULL; entries device or NULL): those of
+ * W[i].  ws: snip_qlinear_fwd_multi_workspace_size bytes.  Shape and
+ * argument rules as snip_qlinear_fwd for every layer. */
+size_t snip_qlinear_fwd_multi_workspace_size(const snip_plan* plan, int count, const int* layers, int64_t T,
+                                             int64_t K, const int64_t* N);
+snip_status snip_qlinear_fwd_multi(const snip_plan* plan, int count, const int* layers, const void* X,
+                                   const void* const* W, int64_t T, int64_t K, const int64_t* N, float* const* Y,
+                                   double* stats_x, double* const* stats_w, void* ws, size_t ws_bytes,
+                                   void* stream);
+
 /* Backward (SNIP Figure 5): dX = Q(dY) Q(W^T)^T (dY and W^T quantized along
  * N) and dW = Q(dY^T) Q(X^T)^T (both quantized along T), stochastic rounding
  * by default ("FP4 all the way", Outline), stream ids layer*8+{2,3,4,5}.
@@ -450,6 +474,43 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
 snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W,
                              const void* dY, int64_t T, int64_t K, int64_t N, float* dX, float* dW,
                              double* stats_out, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- NEXT-3: the backward chain */
+
+/* SNIP, Figure 5 chains the linears: a layer's dX is the gradient dY of the
+ * layer before it.  snip_qlinear_bwd_chain runs `layer`'s backward exactly
+ * as snip_qlinear_bwd, except that its dgrad GEMM also writes its product,
+ * rounded to bf16, as the preceding layer prev_layer's two gradient operands
+ * (the re-quantizing epilogue of snip_gemm_requant): row blocks along K
+ * (prev_layer's dgrad operand, its DY_DGRAD rounding and stream id
+ * prev_layer*8+2) and column blocks along T (its wgrad operand dY^T,
+ * DYT_WGRAD rounding, stream id prev_layer*8+4), NVFP4 in the MMA layout,
+ * quantized with the given tensor scale g_prev (device float; a delayed
+ * scale such as the previous step's amax_prev / 2688: the product's own
+ * amax is known only after it is formed).  amax_prev (device float,
+ * nullable) receives max |bf16(dX)|.  dX (fp32) may be NULL.
+ * prev_layer's format must be NVFP4 (SNIP_ERR_INVALID_ARG otherwise).
+ * Buffer sizes: snip_quantized_bytes(NVFP4, MMA, T, K) for prev_codes /
+ * prev_scales, (NVFP4, MMA, K, T) for prev_codes_t / prev_scales_t.
+ * The identity stands between the two layers: the pages place no function
+ * between consecutive linears on this path. */
+snip_status snip_qlinear_bwd_chain(const snip_plan* plan, int layer, int prev_layer, const void* X, const void* W,
+                                   const void* dY, int64_t T, int64_t K, int64_t N, float* dX, float* dW,
+                                   double* stats_out, const float* g_prev, uint8_t* prev_codes,
+                                   uint8_t* prev_scales, uint8_t* prev_codes_t, uint8_t* prev_scales_t,
+                                   float* amax_prev, void* ws, size_t ws_bytes, void* stream);
+
+/* The backward of an NVFP4 layer whose gradient arrives already quantized
+ * (snip_qlinear_bwd_chain's outputs): dX = Q(dY) Q(W^T)^T and
+ * dW = Q(dY^T) Q(X^T)^T with Q(dY), Q(dY^T) given (dy_* and dyt_*, NVFP4,
+ * MMA layout, tensor scale g_dy: device float) and W^T, X^T quantized as in
+ * snip_qlinear_bwd.  The bf16 dY is never formed here, so this form has no
+ * statistics of it.  The layer's format must be NVFP4; other arguments and
+ * errors as snip_qlinear_bwd. */
+snip_status snip_qlinear_bwd_q(const snip_plan* plan, int layer, const void* X, const void* W,
+                               const uint8_t* dy_codes, const uint8_t* dy_scales, const uint8_t* dyt_codes,
+                               const uint8_t* dyt_scales, const float* g_dy, int64_t T, int64_t K, int64_t N,
+                               float* dX, float* dW, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- a8: statistics */
 

@@ -606,6 +606,120 @@ snip_status snip_qlinear_fwd(const snip_plan* plan, int layer, const void* X, co
                   b + L.op[1].scales_off, gemm_scale(sw, qf), T, N, K, Y, N, ws, sms, st);
 }
 
+namespace {
+constexpr int kMaxMulti = 8;
+// Groups of the layers of a multi-layer forward that share one quantization of X: same forward
+// format and round-to-nearest X_FWD rounding; a stochastic X_FWD rounding is the layer's own group.
+// group[i] = index of layer i's group; first[g] = its first member; returns the number of groups.
+int fwd_groups(const snip_plan* plan, int count, const int* layers, int* group, int* first) {
+  int ng = 0;
+  for (int i = 0; i < count; ++i) {
+    const int l = layers[i], f = forward_fmt(plan->fmt[l]);
+    const bool rtn = plan->rnd[(size_t)l * 6 + SNIP_TAG_X_FWD] == SNIP_RTN;
+    group[i] = -1;
+    for (int g = 0; rtn && g < ng; ++g) {
+      const int l0 = layers[first[g]];
+      if (forward_fmt(plan->fmt[l0]) == f && plan->rnd[(size_t)l0 * 6 + SNIP_TAG_X_FWD] == SNIP_RTN) group[i] = g;
+    }
+    if (group[i] < 0) { first[ng] = i; group[i] = ng++; }
+  }
+  return ng;
+}
+struct MultiLayout {
+  size_t x_codes[kMaxMulti], x_scales[kMaxMulti], w_codes, w_scales, total;
+};
+MultiLayout multi_layout(const snip_plan* plan, int count, const int* layers, int64_t T, int64_t K, const int64_t* N,
+                         const int* first, int ng) {
+  MultiLayout L;
+  size_t off = kSmallWorkspaceRounded;
+  for (int g = 0; g < ng; ++g) {
+    OperandBytes b = operand_bytes(forward_fmt(plan->fmt[layers[first[g]]]), SNIP_LAYOUT_MMA, T, K);
+    L.x_codes[g] = off;
+    off = align_up(off + b.codes, 1024);
+    L.x_scales[g] = off;
+    off = align_up(off + b.scales, 1024);
+  }
+  size_t wc = 0, wsz = 0;
+  for (int i = 0; i < count; ++i) {
+    OperandBytes b = operand_bytes(forward_fmt(plan->fmt[layers[i]]), SNIP_LAYOUT_MMA, N[i], K);
+    wc = b.codes > wc ? b.codes : wc;
+    wsz = b.scales > wsz ? b.scales : wsz;
+  }
+  L.w_codes = off;
+  off = align_up(off + wc, 1024);
+  L.w_scales = off;
+  off = align_up(off + wsz, 1024);
+  L.total = off;
+  return L;
+}
+snip_status check_multi(const snip_plan* plan, int count, const int* layers, int64_t T, int64_t K, const int64_t* N) {
+  if (!plan || count < 1 || count > kMaxMulti || !layers || !N) return SNIP_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    for (int j = 0; j < i; ++j)
+      if (layers[j] == layers[i]) return SNIP_ERR_INVALID_ARG;
+    snip_status s = check_ql(plan, layers[i], T, K, N[i]);
+    if (s != SNIP_OK) return s;
+  }
+  return SNIP_OK;
+}
+}  // namespace
+
+size_t snip_qlinear_fwd_multi_workspace_size(const snip_plan* plan, int count, const int* layers, int64_t T,
+                                             int64_t K, const int64_t* N) {
+  if (check_multi(plan, count, layers, T, K, N) != SNIP_OK) return 0;
+  int group[kMaxMulti], first[kMaxMulti];
+  const int ng = fwd_groups(plan, count, layers, group, first);
+  return multi_layout(plan, count, layers, T, K, N, first, ng).total;
+}
+
+snip_status snip_qlinear_fwd_multi(const snip_plan* plan, int count, const int* layers, const void* X,
+                                   const void* const* W, int64_t T, int64_t K, const int64_t* N, float* const* Y,
+                                   double* stats_x, double* const* stats_w, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if ((s = check_multi(plan, count, layers, T, K, N)) != SNIP_OK) return s;
+  if (!X || !W || !Y) return SNIP_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i)
+    if (!W[i] || !Y[i]) return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < snip_qlinear_fwd_multi_workspace_size(plan, count, layers, T, K, N))
+    return SNIP_ERR_WORKSPACE;
+  if (!aligned16(X) || !aligned16(ws)) return SNIP_ERR_ALIGN;
+  for (int i = 0; i < count; ++i)
+    if (!aligned16(W[i]) || !aligned16(Y[i])) return SNIP_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int group[kMaxMulti], first[kMaxMulti];
+  const int ng = fwd_groups(plan, count, layers, group, first);
+  const MultiLayout L = multi_layout(plan, count, layers, T, K, N, first, ng);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  float* sx = scale_slot(ws, 0);
+  float* sw = scale_slot(ws, 1);
+  if ((s = run_scales(X, T * K, sx, ws, sms, st)) != SNIP_OK) return s;
+  // X once per group; its statistics with the first quantization
+  for (int g = 0; g < ng; ++g) {
+    const int l = layers[first[g]], qf = forward_fmt(plan->fmt[l]);
+    if ((s = run_quantize(qf, X, T, K, SNIP_BLOCKS_ALONG_COLS, plan->rnd[(size_t)l * 6 + SNIP_TAG_X_FWD], plan->seed,
+                          (uint64_t)l * 8 + SNIP_TAG_X_FWD, sx + scale_index(qf), SNIP_LAYOUT_MMA, b + L.x_codes[g],
+                          b + L.x_scales[g], nullptr, nullptr, sms, st, sx, g == 0 ? stats_x : nullptr, ws)) != SNIP_OK)
+      return s;
+  }
+  // each weight: scales, quantization (+ statistics), GEMM; in stream order, so one W region serves all
+  for (int i = 0; i < count; ++i) {
+    const int l = layers[i], qf = forward_fmt(plan->fmt[l]), g = group[i];
+    if ((s = run_scales(W[i], N[i] * K, sw, ws, sms, st)) != SNIP_OK) return s;
+    if ((s = run_quantize(qf, W[i], N[i], K, SNIP_BLOCKS_ALONG_COLS, plan->rnd[(size_t)l * 6 + SNIP_TAG_W_FWD],
+                          plan->seed, (uint64_t)l * 8 + SNIP_TAG_W_FWD, sw + scale_index(qf), SNIP_LAYOUT_MMA,
+                          b + L.w_codes, b + L.w_scales, nullptr, nullptr, sms, st, sw,
+                          stats_w ? stats_w[i] : nullptr, ws)) != SNIP_OK)
+      return s;
+    if ((s = run_gemm(qf, b + L.x_codes[g], b + L.x_scales[g], gemm_scale(sx, qf), b + L.w_codes, b + L.w_scales,
+                      gemm_scale(sw, qf), T, N[i], K, Y[i], N[i], ws, sms, st)) != SNIP_OK)
+      return s;
+  }
+  return SNIP_OK;
+}
+
 snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W, const void* dY,
                              int64_t T, int64_t K, int64_t N, float* dX, float* dW, double* stats_out, void* ws,
                              size_t ws_bytes, void* stream) {
@@ -657,6 +771,127 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
     return s;
   return run_gemm(qg, b + L.op[2].codes_off, b + L.op[2].scales_off, gemm_scale(sd, qg), b + L.op[3].codes_off,
                   b + L.op[3].scales_off, gemm_scale(sx, qf), N, K, T, dW, K, ws, sms, st);
+}
+
+// ---------------------------------------------------------------- NEXT-3: the backward chain
+snip_status snip_qlinear_bwd_chain(const snip_plan* plan, int layer, int prev_layer, const void* X, const void* W,
+                                   const void* dY, int64_t T, int64_t K, int64_t N, float* dX, float* dW,
+                                   double* stats_out, const float* g_prev, uint8_t* prev_codes,
+                                   uint8_t* prev_scales, uint8_t* prev_codes_t, uint8_t* prev_scales_t,
+                                   float* amax_prev, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if ((s = check_ql(plan, layer, T, K, N)) != SNIP_OK) return s;
+  if (prev_layer < 0 || prev_layer >= (int)plan->fmt.size()) return SNIP_ERR_INVALID_ARG;
+  // the preceding layer's gradient operands are what the re-quantizing epilogue writes: NVFP4
+  if (gradient_fmt(plan->fmt[prev_layer]) != SNIP_FMT_NVFP4) return SNIP_ERR_INVALID_ARG;
+  if (!X || !W || !dY || !dW || !g_prev || !prev_codes || !prev_scales || !prev_codes_t || !prev_scales_t)
+    return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < snip_qlinear_workspace_size(plan, layer, T, K, N)) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(dY) || (dX && !aligned16(dX)) || !aligned16(dW) ||
+      !aligned16(ws) || !aligned16(prev_codes) || !aligned16(prev_scales) || !aligned16(prev_codes_t) ||
+      !aligned16(prev_scales_t))
+    return SNIP_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int qg = gradient_fmt(plan->fmt[layer]);
+  const int qf = forward_fmt(plan->fmt[layer]);
+  const int* rnd = &plan->rnd[(size_t)layer * 6];
+  const int* prnd = &plan->rnd[(size_t)prev_layer * 6];
+  const uint64_t sid = (uint64_t)layer * 8, psid = (uint64_t)prev_layer * 8;
+  QlLayout L = ql_layout(qf, T, K, N, true);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  float* sx = scale_slot(ws, 0);
+  float* sw = scale_slot(ws, 1);
+  float* sd = scale_slot(ws, 2);
+  float* sd_out = qg == SNIP_FMT_FP8_E5M2 ? sd + 3 : nullptr;
+  {
+    const void* xs[3] = {dY, W, X};
+    const int64_t ns[3] = {T * N, N * K, T * K};
+    float* outs[3] = {sd, sw, sx};
+    if ((s = run_scales_multi(3, xs, ns, outs, ws, sms, st)) != SNIP_OK) return s;
+  }
+  // dgrad: its product dX (T x K) is the preceding layer's dY, written as that layer's two NVFP4
+  // operands (row blocks along K for its dgrad, column blocks along T for its wgrad) with the given
+  // tensor scale and that layer's roundings and stream ids
+  if ((s = run_quantize(qg, dY, T, N, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_DY_DGRAD], plan->seed,
+                        sid + SNIP_TAG_DY_DGRAD, sd + scale_index(qg), SNIP_LAYOUT_MMA, b + L.op[0].codes_off,
+                        b + L.op[0].scales_off, sd_out, nullptr, sms, st, sd, stats_out, ws)) != SNIP_OK)
+    return s;
+  if ((s = run_quantize(qf, W, N, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_WT_DGRAD], plan->seed,
+                        sid + SNIP_TAG_WT_DGRAD, sw + scale_index(qf), SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
+                        b + L.op[1].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
+    return s;
+  snip_requant rq;
+  rq.g_in = g_prev;
+  rq.rnd = prnd[SNIP_TAG_DY_DGRAD];
+  rq.seed = plan->seed;
+  rq.stream_id = psid + SNIP_TAG_DY_DGRAD;
+  rq.codes = prev_codes;
+  rq.scales = prev_scales;
+  rq.amax_out = amax_prev;
+  rq.rnd_t = prnd[SNIP_TAG_DYT_WGRAD];
+  rq.stream_id_t = psid + SNIP_TAG_DYT_WGRAD;
+  rq.codes_t = prev_codes_t;
+  rq.scales_t = prev_scales_t;
+  if ((s = run_gemm(qg, b + L.op[0].codes_off, b + L.op[0].scales_off, gemm_scale(sd, qg), b + L.op[1].codes_off,
+                    b + L.op[1].scales_off, gemm_scale(sw, qf), T, K, N, dX, K, ws, sms, st, &rq)) != SNIP_OK)
+    return s;
+  // wgrad as in snip_qlinear_bwd
+  if ((s = run_quantize(qg, dY, T, N, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_DYT_WGRAD], plan->seed,
+                        sid + SNIP_TAG_DYT_WGRAD, sd + scale_index(qg), SNIP_LAYOUT_MMA, b + L.op[2].codes_off,
+                        b + L.op[2].scales_off, sd_out, nullptr, sms, st)) != SNIP_OK)
+    return s;
+  if ((s = run_quantize(qf, X, T, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_XT_WGRAD], plan->seed,
+                        sid + SNIP_TAG_XT_WGRAD, sx + scale_index(qf), SNIP_LAYOUT_MMA, b + L.op[3].codes_off,
+                        b + L.op[3].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
+    return s;
+  return run_gemm(qg, b + L.op[2].codes_off, b + L.op[2].scales_off, gemm_scale(sd, qg), b + L.op[3].codes_off,
+                  b + L.op[3].scales_off, gemm_scale(sx, qf), N, K, T, dW, K, ws, sms, st);
+}
+
+snip_status snip_qlinear_bwd_q(const snip_plan* plan, int layer, const void* X, const void* W,
+                               const uint8_t* dy_codes, const uint8_t* dy_scales, const uint8_t* dyt_codes,
+                               const uint8_t* dyt_scales, const float* g_dy, int64_t T, int64_t K, int64_t N,
+                               float* dX, float* dW, void* ws, size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if ((s = check_ql(plan, layer, T, K, N)) != SNIP_OK) return s;
+  if (plan->fmt[layer] != SNIP_FMT_NVFP4) return SNIP_ERR_INVALID_ARG;
+  if (!X || !W || !dy_codes || !dy_scales || !dyt_codes || !dyt_scales || !g_dy || !dX || !dW)
+    return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < snip_qlinear_workspace_size(plan, layer, T, K, N)) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(dy_codes) || !aligned16(dy_scales) || !aligned16(dyt_codes) ||
+      !aligned16(dyt_scales) || !aligned16(dX) || !aligned16(dW) || !aligned16(ws))
+    return SNIP_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int q = SNIP_FMT_NVFP4;
+  const int* rnd = &plan->rnd[(size_t)layer * 6];
+  const uint64_t sid = (uint64_t)layer * 8;
+  QlLayout L = ql_layout(q, T, K, N, true);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  float* sx = scale_slot(ws, 0);
+  float* sw = scale_slot(ws, 1);
+  {
+    const void* xs[2] = {W, X};
+    const int64_t ns[2] = {N * K, T * K};
+    float* outs[2] = {sw, sx};
+    if ((s = run_scales_multi(2, xs, ns, outs, ws, sms, st)) != SNIP_OK) return s;
+  }
+  if ((s = run_quantize(q, W, N, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_WT_DGRAD], plan->seed,
+                        sid + SNIP_TAG_WT_DGRAD, sw + scale_index(q), SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
+                        b + L.op[1].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
+    return s;
+  if ((s = run_gemm(q, dy_codes, dy_scales, g_dy, b + L.op[1].codes_off, b + L.op[1].scales_off,
+                    gemm_scale(sw, q), T, K, N, dX, K, ws, sms, st)) != SNIP_OK)
+    return s;
+  if ((s = run_quantize(q, X, T, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_XT_WGRAD], plan->seed,
+                        sid + SNIP_TAG_XT_WGRAD, sx + scale_index(q), SNIP_LAYOUT_MMA, b + L.op[3].codes_off,
+                        b + L.op[3].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
+    return s;
+  return run_gemm(q, dyt_codes, dyt_scales, g_dy, b + L.op[3].codes_off, b + L.op[3].scales_off,
+                  gemm_scale(sx, q), N, K, T, dW, K, ws, sms, st);
 }
 
 // ---------------------------------------------------------------- statistics

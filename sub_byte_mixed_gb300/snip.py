@@ -37,6 +37,8 @@ EXPORTS = (
     "snip_quantize_e5m2",
     "snip_quantized_bytes", "snip_gemm", "snip_plan_create", "snip_plan_set_rounding", "snip_plan_get",
     "snip_plan_destroy", "snip_qlinear_workspace_size", "snip_qlinear_fwd", "snip_qlinear_bwd",
+    "snip_qlinear_fwd_multi_workspace_size", "snip_qlinear_fwd_multi", "snip_qlinear_bwd_chain",
+    "snip_qlinear_bwd_q",
     "snip_quant_stats", "snip_quantize_stats", "snip_stats_finalize", "snip_plan_costs", "snip_plan_select",
     "snip_dw_noise_workspace_size", "snip_dw_noise", "snip_dw_noise_finalize", "snip_gemm_requant",
 )
@@ -102,6 +104,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "snip_qlinear_workspace_size": (sz, [vp, i32, i64, i64, i64]),
         "snip_qlinear_fwd": (i32, [vp, i32, vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]),
         "snip_qlinear_bwd": (i32, [vp, i32, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, sz, vp]),
+        "snip_qlinear_fwd_multi_workspace_size": (sz, [vp, i32, vp, i64, i64, vp]),
+        "snip_qlinear_fwd_multi": (i32, [vp, i32, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, sz, vp]),
+        "snip_qlinear_bwd_chain": (i32, [vp, i32, i32, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                         vp, vp, sz, vp]),
+        "snip_qlinear_bwd_q": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]),
         "snip_quantize_stats": (i32, [i32, vp, i64, i64, i32, u64, u64, vp, i32, vp, vp, vp, vp, sz, vp]),
         "snip_quant_stats": (i32, [vp, i64, i64, i32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "snip_stats_finalize": (i32, [vp, ctypes.POINTER(SnipStats)]),
@@ -551,6 +558,70 @@ def qlinear_fwd(plan: Plan, layer: int, X, W, ws: Workspace, Y=None, stats=None)
     snip_qlinear_fwd(plan.handle, layer, X.data_ptr(), W.data_ptr(), T, K, N, Y.data_ptr(), _ptr(stats), ws.ptr,
                      ws.nbytes, _stream())
     return Y
+
+
+def _multi_arrays(layers, Ns):
+    n = len(layers)
+    return (ctypes.c_int * n)(*layers), (ctypes.c_int64 * n)(*Ns)
+
+
+def qlinear_fwd_multi_workspace(plan: Plan, layers, T: int, K: int, Ns, device="cuda") -> Workspace:
+    la, na = _multi_arrays(layers, Ns)
+    return Workspace(load().snip_qlinear_fwd_multi_workspace_size(plan.handle, len(layers), la, T, K, na), device)
+
+
+def qlinear_fwd_multi(plan: Plan, layers, X, Ws, ws: Workspace, Ys=None, stats_x=None, stats_w=None):
+    """Forward of the layers `layers` reading one X (Q/K/V, Gate/Up): Ys[i] = Q(X) Q(Ws[i])^T, X's
+    scales, statistics (stats_x) and quantization computed once; stats_w: a list of device float64
+    (STATS_NVALS,) tensors or None for the weights' statistics."""
+    torch = _torch()
+    T, K = X.shape
+    Ns = [w.shape[0] for w in Ws]
+    Ys = Ys if Ys is not None else [torch.empty((T, n), dtype=torch.float32, device=X.device) for n in Ns]
+    la, na = _multi_arrays(layers, Ns)
+    n = len(layers)
+    wa = (ctypes.c_void_p * n)(*[w.data_ptr() for w in Ws])
+    ya = (ctypes.c_void_p * n)(*[y.data_ptr() for y in Ys])
+    sa = (ctypes.c_void_p * n)(*[_ptr(t) for t in stats_w]) if stats_w is not None else None
+    _call("snip_qlinear_fwd_multi", plan.handle, n, la, X.data_ptr(), wa, T, K, na, ya, _ptr(stats_x), sa, ws.ptr,
+          ws.nbytes, _stream())
+    return Ys
+
+
+def qlinear_bwd_chain(plan: Plan, layer: int, prev_layer: int, X, W, dY, g_prev, ws: Workspace, want_dx=False,
+                      stats=None):
+    """The backward of `layer` whose dgrad product is written as prev_layer's NVFP4 gradient operands
+    (row blocks, column blocks; tensor scale g_prev, a device float (1,)) -> (dX fp32 or None, dW,
+    rows QuantNVFP4, columns QuantNVFP4, amax device float (1,))."""
+    torch = _torch()
+    T, K = X.shape
+    N = W.shape[0]
+    dev = X.device
+    dX = torch.empty((T, K), dtype=torch.float32, device=dev) if want_dx else None
+    dW = torch.empty((N, K), dtype=torch.float32, device=dev)
+    cb, sb = snip_quantized_bytes(NVFP4, MMA, T, K)
+    cbt, sbt = snip_quantized_bytes(NVFP4, MMA, K, T)
+    rc, rs = torch.empty(cb, dtype=torch.uint8, device=dev), torch.empty(sb, dtype=torch.uint8, device=dev)
+    tc, ts = torch.empty(cbt, dtype=torch.uint8, device=dev), torch.empty(sbt, dtype=torch.uint8, device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    _call("snip_qlinear_bwd_chain", plan.handle, layer, prev_layer, X.data_ptr(), W.data_ptr(), dY.data_ptr(), T,
+          K, N, _ptr(dX), dW.data_ptr(), _ptr(stats), g_prev.data_ptr(), rc.data_ptr(), rs.data_ptr(),
+          tc.data_ptr(), ts.data_ptr(), amax.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return dX, dW, QuantNVFP4(rc, rs, g_prev, T, K, MMA), QuantNVFP4(tc, ts, g_prev, K, T, MMA), amax
+
+
+def qlinear_bwd_q(plan: Plan, layer: int, X, W, dy_rows, dy_cols, ws: Workspace, dX=None, dW=None):
+    """The backward of an NVFP4 layer from its quantized gradient operands (QuantNVFP4 row and
+    column blocks sharing one tensor scale) -> (dX, dW)."""
+    torch = _torch()
+    T, K = X.shape
+    N = W.shape[0]
+    dX = dX if dX is not None else torch.empty((T, K), dtype=torch.float32, device=X.device)
+    dW = dW if dW is not None else torch.empty((N, K), dtype=torch.float32, device=X.device)
+    _call("snip_qlinear_bwd_q", plan.handle, layer, X.data_ptr(), W.data_ptr(), dy_rows.codes.data_ptr(),
+          dy_rows.scales.data_ptr(), dy_cols.codes.data_ptr(), dy_cols.scales.data_ptr(), dy_rows.g.data_ptr(), T,
+          K, N, dX.data_ptr(), dW.data_ptr(), ws.ptr, ws.nbytes, _stream())
+    return dX, dW
 
 
 def qlinear_bwd(plan: Plan, layer: int, X, W, dY, ws: Workspace, dX=None, dW=None, stats=None):
