@@ -67,6 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--profile-run", action="store_true",
                     help="exactly --warmup untimed steps, no clock settle, e2e or CPU baseline (for ncu)")
     ap.add_argument("--layers", default="", help="comma-separated subset of Q,K,V,O,Gate,Up,Down (profiling)")
+    ap.add_argument("--next4-only", action="store_true",
+                    help="only the dW-level check (bf16 GEMM with fused norms) at the 7B Down shape, one JSON line")
     ap.add_argument("--cpu-sample-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-sample-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -1218,6 +1220,14 @@ def main():
     args = parse_args()
     if args.vs_cublaslt:
         vs_cublaslt()
+        return
+    if args.next4_only:
+        import torch
+        from sub_byte_mixed_gb300 import build, snip
+        build.build()
+        snip.load()
+        snip.snip_device_check()
+        print(json.dumps(dw_noise_time(snip, measured_peaks()["bf16"])), flush=True)
         return
     if args.cpu_sample_only:
         print(json.dumps(cpu_sample(args.cpu_sample_seconds)), flush=True)

@@ -17,6 +17,10 @@
 // Rounding to nearest uses the hardware E2M1/E4M3 conversions; stochastic
 // rounding uses the carry form of the 16-bit rule (snip_device.cuh), with one
 // Philox4x32-10 call per 8 source elements.
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "snip_kernels.cuh"
 #include "snip_quant.cuh"
 
@@ -716,6 +720,32 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
 }
 
 // ------------------------------------------------------------------ host-side launchers
+// CTAs of 256 threads one SM holds at once for a kernel (occupancy query, cached per kernel).
+static int resident_ctas(const void* fn) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& e : cache)
+    if (e.first == fn) return e.second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 256, 0) != cudaSuccess || n < 1) n = 1;
+  cache.emplace_back(fn, n);
+  return n;
+}
+
+// A grid-stride (persistent) kernel: as many CTAs as the work asks for, but no more than one wave of
+// resident CTAs -- every CTA has the same share of the work, so a second, partial wave would run
+// with most SMs idle -- and no more than max_ctas (the partial-result slots).
+template <class P>
+static void launch_persistent(void (*kernel)(P), int64_t want, int max_ctas, int num_sms, cudaStream_t st,
+                              const P& p) {
+  int64_t g = want < 1 ? 1 : want;
+  const int64_t wave = (int64_t)resident_ctas(reinterpret_cast<const void*>(kernel)) * num_sms;
+  if (g > wave) g = wave;
+  if (g > max_ctas) g = max_ctas;
+  kernel<<<(unsigned)g, 256, 0, st>>>(p);
+}
+
 static int fill_grid(int64_t work_items, int per_cta, int max_ctas) {
   int64_t g = (work_items + per_cta - 1) / per_cta;
   if (g < 1) g = 1;
@@ -750,27 +780,31 @@ cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint
   return cudaGetLastError();
 }
 
+// a row-block quantization (persistent: want CTAs at most, cap partial slots)
+#define SNIP_ROWS(...) launch_persistent(quant_rows_kernel<__VA_ARGS__>, want, cap, num_sms, st, p)
+
 template <int FMT>
 static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
                              cudaStream_t st) {
   if (orient == 0) {
     const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
     const bool stats = p.raw_out != nullptr;
-    // with statistics, one partial slot per CTA: keep the grid within them
-    const int grid = fill_grid(segs, 8, stats ? 4 * num_sms : 16 * num_sms);
+    // one warp per 32-block segment at a time; with statistics, one partial slot per CTA
+    const int64_t want = (segs + 7) / 8;
+    const int cap = stats ? kMaxPartials : 16 * num_sms;
     if constexpr (FMT == 1) {
       if (stats && p.group > 1) {   // longer NVFP4 blocks with fused statistics (no block errors)
         if (layout == 0) {
-          if (rnd == 0) quant_rows_kernel<1, 0, 0, false, true, true><<<grid, 256, 0, st>>>(p);
-          else quant_rows_kernel<1, 0, 1, false, true, true><<<grid, 256, 0, st>>>(p);
+          if (rnd == 0) SNIP_ROWS(1, 0, 0, false, true, true);
+          else SNIP_ROWS(1, 0, 1, false, true, true);
         } else {
-          if (rnd == 0) quant_rows_kernel<1, 1, 0, false, true, true><<<grid, 256, 0, st>>>(p);
-          else quant_rows_kernel<1, 1, 1, false, true, true><<<grid, 256, 0, st>>>(p);
+          if (rnd == 0) SNIP_ROWS(1, 1, 0, false, true, true);
+          else SNIP_ROWS(1, 1, 1, false, true, true);
         }
         return;
       }
     }
-#define SNIP_L(LY, RN, ER, SS) quant_rows_kernel<FMT, LY, RN, ER, SS><<<grid, 256, 0, st>>>(p)
+#define SNIP_L(LY, RN, ER, SS) SNIP_ROWS(FMT, LY, RN, ER, SS)
 #define SNIP_LS(LY, RN, ER) do { if (stats) SNIP_L(LY, RN, ER, true); else SNIP_L(LY, RN, ER, false); } while (0)
     if (layout == 0) {
       if (rnd == 0) { if (err) SNIP_LS(0, 0, true); else SNIP_LS(0, 0, false); }
@@ -801,22 +835,22 @@ static void launch_quant_mx(const QuantParams& p, int orient, int layout, int rn
   if (orient == 0) {
     const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
     const bool stats = p.raw_out != nullptr;
-    // with statistics, one partial slot per CTA: keep the grid within them
-    const int grid = fill_grid(segs, 8, stats ? 4 * num_sms : 16 * num_sms);
+    const int64_t want = (segs + 7) / 8;
+    const int cap = stats ? kMaxPartials : 16 * num_sms;
     if (stats) {
       if (layout == 0) {
-        if (rnd == 0) quant_rows_kernel<2, 0, 0, false, true><<<grid, 256, 0, st>>>(p);
-        else quant_rows_kernel<2, 0, 1, false, true><<<grid, 256, 0, st>>>(p);
+        if (rnd == 0) SNIP_ROWS(2, 0, 0, false, true);
+        else SNIP_ROWS(2, 0, 1, false, true);
       } else {
-        if (rnd == 0) quant_rows_kernel<2, 1, 0, false, true><<<grid, 256, 0, st>>>(p);
-        else quant_rows_kernel<2, 1, 1, false, true><<<grid, 256, 0, st>>>(p);
+        if (rnd == 0) SNIP_ROWS(2, 1, 0, false, true);
+        else SNIP_ROWS(2, 1, 1, false, true);
       }
     } else if (layout == 0) {
-      if (rnd == 0) quant_rows_kernel<2, 0, 0, false, false><<<grid, 256, 0, st>>>(p);
-      else quant_rows_kernel<2, 0, 1, false, false><<<grid, 256, 0, st>>>(p);
+      if (rnd == 0) SNIP_ROWS(2, 0, 0, false, false);
+      else SNIP_ROWS(2, 0, 1, false, false);
     } else {
-      if (rnd == 0) quant_rows_kernel<2, 1, 0, false, false><<<grid, 256, 0, st>>>(p);
-      else quant_rows_kernel<2, 1, 1, false, false><<<grid, 256, 0, st>>>(p);
+      if (rnd == 0) SNIP_ROWS(2, 1, 0, false, false);
+      else SNIP_ROWS(2, 1, 1, false, false);
     }
   } else {
     const dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
@@ -835,22 +869,22 @@ static void launch_quant_e5(const QuantParams& p, int orient, int layout, int rn
   if (orient == 0) {
     const int64_t segs = p.orp * (((p.ocp >> 4) + 31) >> 5);
     const bool stats = p.raw_out != nullptr;
-    // with statistics, one partial slot per CTA: keep the grid within them
-    const int grid = fill_grid(segs, 8, stats ? 4 * num_sms : 16 * num_sms);
+    const int64_t want = (segs + 7) / 8;
+    const int cap = stats ? kMaxPartials : 16 * num_sms;
     if (stats) {
       if (layout == 0) {
-        if (rnd == 0) quant_rows_kernel<3, 0, 0, false, true><<<grid, 256, 0, st>>>(p);
-        else quant_rows_kernel<3, 0, 1, false, true><<<grid, 256, 0, st>>>(p);
+        if (rnd == 0) SNIP_ROWS(3, 0, 0, false, true);
+        else SNIP_ROWS(3, 0, 1, false, true);
       } else {
-        if (rnd == 0) quant_rows_kernel<3, 1, 0, false, true><<<grid, 256, 0, st>>>(p);
-        else quant_rows_kernel<3, 1, 1, false, true><<<grid, 256, 0, st>>>(p);
+        if (rnd == 0) SNIP_ROWS(3, 1, 0, false, true);
+        else SNIP_ROWS(3, 1, 1, false, true);
       }
     } else if (layout == 0) {
-      if (rnd == 0) quant_rows_kernel<3, 0, 0, false, false><<<grid, 256, 0, st>>>(p);
-      else quant_rows_kernel<3, 0, 1, false, false><<<grid, 256, 0, st>>>(p);
+      if (rnd == 0) SNIP_ROWS(3, 0, 0, false, false);
+      else SNIP_ROWS(3, 0, 1, false, false);
     } else {
-      if (rnd == 0) quant_rows_kernel<3, 1, 0, false, false><<<grid, 256, 0, st>>>(p);
-      else quant_rows_kernel<3, 1, 1, false, false><<<grid, 256, 0, st>>>(p);
+      if (rnd == 0) SNIP_ROWS(3, 1, 0, false, false);
+      else SNIP_ROWS(3, 1, 1, false, false);
     }
   } else {
     const dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
@@ -875,10 +909,12 @@ cudaError_t launch_quant(int fmt, const QuantParams& p, int orient, int layout, 
 
 cudaError_t launch_stats(const StatsParams& p, int rnd, int num_sms, cudaStream_t st) {
   const int64_t segs = p.rows * (((p.cols >> 4) + 31) >> 5);
-  const int grid = fill_grid(segs, 8 * 4, 4 * num_sms);
+  const int64_t want = (segs + 31) / 32;   // four segments per warp at least
   const bool blk = p.block_err4 || p.block_err8;
-  if (rnd == 0) { if (blk) stats_kernel<0, true><<<grid, 256, 0, st>>>(p); else stats_kernel<0, false><<<grid, 256, 0, st>>>(p); }
-  else { if (blk) stats_kernel<1, true><<<grid, 256, 0, st>>>(p); else stats_kernel<1, false><<<grid, 256, 0, st>>>(p); }
+#define SNIP_ST(RN, BK) launch_persistent(stats_kernel<RN, BK>, want, kMaxPartials, num_sms, st, p)
+  if (rnd == 0) { if (blk) SNIP_ST(0, true); else SNIP_ST(0, false); }
+  else { if (blk) SNIP_ST(1, true); else SNIP_ST(1, false); }
+#undef SNIP_ST
   return cudaGetLastError();
 }
 
