@@ -281,11 +281,16 @@ def measured_peaks():
 
 
 def kernel_source_hash(kind: str) -> str:
+    """Hash of the code (comments and whitespace removed) of a kernel category's sources: a traffic
+    figure measured on one build applies while that code is unchanged."""
     files = {"gemm": ["gemm.cu", "snip_device.cuh", "snip_kernels.cuh", "snip_quant.cuh"],
              "quant": ["quant.cu", "snip_device.cuh", "snip_kernels.cuh", "snip_quant.cuh"]}[kind]
     h = hashlib.sha256()
     for f in files:
-        h.update(open(os.path.join(ROOT, "sub_byte_mixed_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "sub_byte_mixed_gb300", "csrc", f)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,9 +14,10 @@
 // computed once and no shuffles are needed; a warp covers 32 consecutive
 // blocks of a row.  The transposed (column-block) kernels stage a 128 x 64
 // tile in shared memory so that loads and stores both stay coalesced.
-// Rounding to nearest uses the hardware E2M1/E4M3 conversions; stochastic
-// rounding uses the carry form of the 16-bit rule (snip_device.cuh), with one
-// Philox4x32-10 call per 8 source elements.
+// Rounding to nearest and stochastic rounding both run as fp32 additions on
+// the FMA pipe (grid_rn2 / grid_sr2, snip_device.cuh) with one Philox4x32-10
+// call per 8 source elements; codes come from the hardware E2M1/E4M3/E5M2
+// conversions of the exact grid values.
 #include <mutex>
 #include <utility>
 #include <vector>

@@ -51,27 +51,6 @@ __device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
   return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
 }
 
-// Stochastic rounding of y >= 0 (finite) onto the finite E4M3 grid with 16
-// random bits: up iff u16 < floor(frac * 2^16), y >= 448 gives 448.
-// Carry form: with the value's 20 dropped mantissa bits (exponent-aligned
-// fixed point below 2^-6), adding (65535 - u16) << 4 carries into the kept
-// bits exactly when u16 < floor(frac * 2^16).  Returns the magnitude code.
-// Below 2^-6 the fixed point is floor(y * 2^29), read off the mantissa of
-// 2^-6 + y rounded toward zero (its ulp is 2^-29).
-// The two forms are combined without a branch: with T the bottom of the
-// normal range (here 2^-6), bits(y) - bits(T/2) is the larger of the two for
-// y >= T and negative or smaller below it, where bits(T + y rounded toward
-// zero) - bits(T) is the fixed point; so the base is their signed maximum.
-__device__ __forceinline__ uint32_t e4m3_sr_base(float y) {
-  return (uint32_t)max((int32_t)(__float_as_uint(y) - 0x3C000000u),                      // (exp-120)<<23 | mantissa
-                       (int32_t)(__float_as_uint(__fadd_rz(y, 0.015625f)) - 0x3C800000u));
-}
-__device__ __forceinline__ uint32_t e4m3_sr_from_base(uint32_t base, uint32_t u16) {
-  const uint32_t code = (base + ((65535u - u16) << 4)) >> 20;
-  return code < 0x7eu ? code : 0x7eu;
-}
-__device__ __forceinline__ uint32_t e4m3_sr(float y, uint32_t u16) { return e4m3_sr_from_base(e4m3_sr_base(y), u16); }
-
 // ------------------------------------------------------------------ E5M2
 // 1 sign, 5 exponent (bias 15), 2 mantissa bits; largest finite 57344 (0x7b).
 __device__ __forceinline__ uint32_t e5m2x2_rn_sat(float lo, float hi) {
@@ -79,19 +58,6 @@ __device__ __forceinline__ uint32_t e5m2x2_rn_sat(float lo, float hi) {
   asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// Stochastic rounding of y >= 0 onto the finite E5M2 grid, carry form as for
-// E4M3 with 21 dropped mantissa bits; below 2^-14 the fixed point is
-// floor(y * 2^37), the mantissa of 2^-14 + y rounded toward zero.
-__device__ __forceinline__ uint32_t e5m2_sr_base(float y) {
-  return (uint32_t)max((int32_t)(__float_as_uint(y) - 0x38000000u),                      // (exp-112)<<23 | mantissa
-                       (int32_t)(__float_as_uint(__fadd_rz(y, 6.103515625e-05f)) - 0x38800000u));
-}
-__device__ __forceinline__ uint32_t e5m2_sr_from_base(uint32_t base, uint32_t u16) {
-  const uint32_t code = (base + ((65535u - u16) << 5)) >> 21;
-  return code < 0x7bu ? code : 0x7bu;
-}
-__device__ __forceinline__ uint32_t e5m2_sr(float y, uint32_t u16) { return e5m2_sr_from_base(e5m2_sr_base(y), u16); }
-
 // ------------------------------------------------------------------ E2M1
 // Round-to-nearest-even of two signed values to E2M1 (saturating at +-6),
 // hardware cvt: returns one byte, lo in bits 0..3 and hi in bits 4..7.
@@ -108,25 +74,6 @@ __device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
   __half2 h = *reinterpret_cast<__half2*>(&h2);
   return __half22float2(h);
 }
-
-// Stochastic rounding of y >= 0 (finite) onto {0,.5,1,1.5,2,3,4,6} with 16
-// random bits: lo = largest grid value <= y, up iff u16 < floor(frac*2^16)
-// with frac = (y-lo)/(hi-lo); y >= 6 gives 6.  Carry form as in e4m3_sr: the
-// 22 bits below E2M1's one mantissa bit (fixed point 2^-23 below 1) plus
-// (65535 - u16) << 6 carry into the kept bits exactly when the rule rounds
-// up.  Returns the magnitude code 0..7.
-// Below 1 the fixed point is floor(y * 2^23), the mantissa of 1 + y rounded
-// toward zero.
-// (Combined as for E4M3, with T = 1.)
-__device__ __forceinline__ uint32_t e2m1_sr_base(float y) {
-  return (uint32_t)max((int32_t)(__float_as_uint(y) - 0x3F000000u),                      // 2*(exp-126) | m1, << 22
-                       (int32_t)(__float_as_uint(__fadd_rz(y, 1.0f)) - 0x3F800000u));
-}
-__device__ __forceinline__ uint32_t e2m1_sr_from_base(uint32_t base, uint32_t u16) {
-  const uint32_t code = (base + ((65535u - u16) << 6)) >> 22;
-  return code < 7u ? code : 7u;
-}
-__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t u16) { return e2m1_sr_from_base(e2m1_sr_base(y), u16); }
 
 // Value of an E2M1 magnitude code 0..7.
 __device__ __forceinline__ float e2m1_value(uint32_t m) {

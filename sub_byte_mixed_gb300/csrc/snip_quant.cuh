@@ -104,11 +104,6 @@ __device__ __forceinline__ void sr_bits16_rk(int64_t e0, uint64_t sid, const Phi
   u[0] = w0.x; u[1] = w0.y; u[2] = w0.z; u[3] = w0.w;
   u[4] = w1.x; u[5] = w1.y; u[6] = w1.z; u[7] = w1.w;
 }
-// random half of element i from the packed words (element i in half i%2 of word i/2)
-__device__ __forceinline__ uint32_t uhalf(const uint32_t (&u)[8], int i) {
-  return (i & 1) ? (u[i >> 1] >> 16) : (u[i >> 1] & 0xffffu);
-}
-
 // Sources of the 16 random bits of element i of a block, for the encoders:
 // packed two per word (element i in half i%2 of word i/2) ...
 // Each also gives f23(i) = 2^23 + u16 as a float (sr_f23), for the FMA-pipe rounding.
