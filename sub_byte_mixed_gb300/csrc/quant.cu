@@ -195,21 +195,41 @@ __device__ __forceinline__ float e5m2_tensor_scale(float amax) {
 // top (yc) and c = q - yc, the expected SR variance (hi - y)(y - lo) is
 // |c| (h - |c|) whichever neighbour q is, summed as 1/2 sum |c| H - sum c^2
 // (H = twice the E2M1 step; eight times the E4M3 step with 1/8).
-struct BlockStats {
-  float x2, e4, e8, v4, v8;
+// The running sums of one thread over its blocks.  Only the NVFP4 variance is
+// scaled per block (by its p^2); everything else accumulates across blocks
+// (the FP8 variance in units of the tensor scale s8, multiplied at the end).
+struct StatsAcc {
+  float2 x2, e4, e8, S8;
+  float T8, v4;
+  __device__ __forceinline__ void init() {
+    x2 = e4 = e8 = S8 = make_float2(0.f, 0.f);
+    T8 = v4 = 0.f;
+  }
+  // the five sums: ||A||^2, NVFP4 err^2, FP8 err^2, NVFP4 and FP8 expected SR variance
+  __device__ __forceinline__ void finish(float s8, bool special8, float (&out)[5]) const {
+    out[0] = x2.x + x2.y;
+    out[1] = e4.x + e4.y;
+    out[2] = e8.x + e8.y;
+    out[3] = v4;
+    out[4] = special8 ? 0.0f : fmaf(0.125f, T8, -(S8.x + S8.y)) * (s8 * s8);
+  }
 };
-template <int CF, int RND>
-__device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
-                                                    float s8, float inv8, bool special8, uint4& codes) {
-  float2 x2 = make_float2(0.f, 0.f), e4 = x2, e8 = x2, S4 = x2, S8 = x2;
-  float T4 = 0.f, T8 = 0.f, se4 = 0.f, se8 = 0.f;
+// BE: also return the block's two squared errors (per-block error outputs).
+template <int CF, int RND, bool BE = false>
+__device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
+                                              float s8, float inv8, bool special8, uint4& codes, StatsAcc& acc,
+                                              float* be4 = nullptr, float* be8 = nullptr) {
+  float2 S4 = make_float2(0.f, 0.f), b4 = S4, b8 = S4;
+  float T4 = 0.f;
   uint32_t cw[4] = {0u, 0u, 0u, 0u};
   const float2 inv2 = make_float2(bs.inv, bs.inv), np2 = make_float2(-bs.p, -bs.p);
   const float2 i8 = make_float2(inv8, inv8), ns8 = make_float2(-s8, -s8), m1 = make_float2(-1.0f, -1.0f);
+  float2& E4 = BE ? b4 : acc.e4;
+  float2& E8 = BE ? b8 : acc.e8;
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
     const float2 va = make_float2(fabsf(v[i]), fabsf(v[i + 1]));
-    x2 = __ffma2_rn(va, va, x2);
+    acc.x2 = __ffma2_rn(va, va, acc.x2);
     float2 g17 = va, g19 = va;   // random fractions of the pair (stochastic rounding)
     if (RND) {
       const float f0 = sr_f23<false>(u[i >> 1]), f1 = sr_f23<true>(u[i >> 1]);
@@ -222,7 +242,7 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       for (int k = 0; k < 2; ++k) {
         const float q = (bs.p == 0.0f || v[i + k] == 0.0f) ? 0.0f : copysignf(6.0f, v[i + k]);
         const float d = fmaf(q, bs.p, -v[i + k]);
-        se4 = fmaf(d, d, se4);
+        E4.x = fmaf(d, d, E4.x);
       }
     } else {
       const float2 y = __fmul2_rn(va, inv2);
@@ -231,7 +251,7 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       const float2 q = RND ? grid_sr2(yc, H, g17, 4194304.0f) : grid_rn2(yc, H, 4194304.0f);
       if (CF == 1) cw[i >> 3] |= e2m1x2_rn(copysignf(q.x, v[i]), copysignf(q.y, v[i + 1])) << (4 * (i & 7));
       const float2 d = __ffma2_rn(q, np2, va);            // |x| - |x_hat|
-      e4 = __ffma2_rn(d, d, e4);
+      E4 = __ffma2_rn(d, d, E4);
       const float2 c = __ffma2_rn(yc, m1, q);
       S4 = __ffma2_rn(c, c, S4);
       T4 = fmaf(fabsf(c.x), H.x, T4);
@@ -243,7 +263,7 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       for (int k = 0; k < 2; ++k) {
         const float q = v[i + k] == 0.0f ? 0.0f : copysignf(448.0f, v[i + k]);
         const float d = fmaf(q, s8, -v[i + k]);
-        se8 = fmaf(d, d, se8);
+        E8.x = fmaf(d, d, E8.x);
       }
     } else {
       const float2 y = __fmul2_rn(va, i8);
@@ -252,31 +272,30 @@ __device__ __forceinline__ BlockStats stats_block16(const float (&v)[16], const 
       const float2 q = RND ? grid_sr2(yc, H, g19, 1048576.0f) : grid_rn2(yc, H, 1048576.0f);
       if (CF == 0) cw[i >> 2] |= e4m3x2_rn_sat(copysignf(q.x, v[i]), copysignf(q.y, v[i + 1])) << (8 * (i & 3));
       const float2 d = __ffma2_rn(q, ns8, va);
-      e8 = __ffma2_rn(d, d, e8);
+      E8 = __ffma2_rn(d, d, E8);
       const float2 c = __ffma2_rn(yc, m1, q);
-      S8 = __ffma2_rn(c, c, S8);
-      T8 = fmaf(fabsf(c.x), H.x, T8);
-      T8 = fmaf(fabsf(c.y), H.y, T8);
+      acc.S8 = __ffma2_rn(c, c, acc.S8);
+      acc.T8 = fmaf(fabsf(c.x), H.x, acc.T8);
+      acc.T8 = fmaf(fabsf(c.y), H.y, acc.T8);
     }
   }
-  // the variances were summed in units of the scale
-  const float a4 = fmaf(0.5f, T4, -(S4.x + S4.y)), a8 = fmaf(0.125f, T8, -(S8.x + S8.y));
+  // the NVFP4 variance was summed in units of this block's scale
+  if (!bs.special) acc.v4 = fmaf(fmaf(0.5f, T4, -(S4.x + S4.y)), bs.p * bs.p, acc.v4);
+  if (BE) {
+    *be4 = b4.x + b4.y;
+    *be8 = b8.x + b8.y;
+    acc.e4.x += *be4;
+    acc.e8.x += *be8;
+  }
   codes = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-  BlockStats r;
-  r.x2 = x2.x + x2.y;
-  r.e4 = bs.special ? se4 : e4.x + e4.y;
-  r.e8 = special8 ? se8 : e8.x + e8.y;
-  r.v4 = bs.special ? 0.0f : a4 * (bs.p * bs.p);
-  r.v8 = special8 ? 0.0f : a8 * (s8 * s8);
-  return r;
 }
 
 // CTA reduction of the five fp32 per-thread sums into fp64, then the last CTA
 // to finish adds all CTAs' partials and writes the raw statistics vector.
-__device__ __forceinline__ void stats_finish(float sx2, float e4, float e8, float v4, float v8, double* partials,
-                                             uint32_t* counter, double* raw_out, float amax, int64_t count) {
+__device__ __forceinline__ void stats_finish(const float (&sums)[5], double* partials, uint32_t* counter,
+                                             double* raw_out, float amax, int64_t count) {
   // within the CTA in fp32 (256 partial sums: a few ulps), across CTAs in fp64
-  float acc[5] = {sx2, e4, e8, v4, v8};
+  float acc[5] = {sums[0], sums[1], sums[2], sums[3], sums[4]};
   block_sum_f32<5>(acc);
   __shared__ bool s_last;
   if (threadIdx.x == 0) {
@@ -358,7 +377,8 @@ __global__ void __launch_bounds__(256, STATS ? 3 : 4) quant_rows_kernel(QuantPar
   const uint32_t total = (uint32_t)p.orp * spr;
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
-  float sx2 = 0.f, e4 = 0.f, e8 = 0.f, v4 = 0.f, v8 = 0.f;
+  StatsAcc acc;
+  acc.init();
   // segment -> (row, segment in row), stepped without a division per iteration
   const uint32_t seg0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const uint32_t wq = wstride / spr, wr = wstride - wq * spr;
@@ -421,12 +441,7 @@ __global__ void __launch_bounds__(256, STATS ? 3 : 4) quant_rows_kernel(QuantPar
       // statistics of the two candidate formats (16-element NVFP4, E4M3); codes with the scale of
       // the longer NVFP4 block, of the MXFP4 block, or E5M2's tensor scale
       if (real) {
-        const BlockStats st = stats_block16<-1, RND>(v, bs, u, s8, inv8, special8, c);
-        sx2 += st.x2;
-        e4 += st.e4;
-        e8 += st.e8;
-        v4 += st.v4;
-        v8 += st.v8;
+        stats_block16<-1, RND>(v, bs, u, s8, inv8, special8, c, acc);
         if (FMT == 3) {
           c = fp8_encode16<RND, true>(v, inv5, PackedBits{u});
         } else {
@@ -438,12 +453,7 @@ __global__ void __launch_bounds__(256, STATS ? 3 : 4) quant_rows_kernel(QuantPar
     } else if (STATS) {
       // the codes come out of the statistics' own conversions
       if (real) {
-        const BlockStats st = stats_block16<FMT, RND>(v, bs, u, s8, inv8, special8, c);
-        sx2 += st.x2;
-        e4 += st.e4;
-        e8 += st.e8;
-        v4 += st.v4;
-        v8 += st.v8;
+        stats_block16<FMT, RND>(v, bs, u, s8, inv8, special8, c, acc);
         if (FMT == 1 && bs.special) {
           const uint2 e = nvfp4_encode16<RND>(v, bs, PackedBits{u});
           c.x = e.x;
@@ -485,7 +495,11 @@ __global__ void __launch_bounds__(256, STATS ? 3 : 4) quant_rows_kernel(QuantPar
       *reinterpret_cast<uint4*>(p.codes + (int64_t)r * pitch + (int64_t)kb * 16) = c;
     }
   }
-  if (STATS) stats_finish(sx2, e4, e8, v4, v8, p.partials, p.counter, p.raw_out, p.scales3[0], p.rows * p.cols);
+  if (STATS) {
+    float sums[5];
+    acc.finish(s8, special8, sums);
+    stats_finish(sums, p.partials, p.counter, p.raw_out, p.scales3[0], p.rows * p.cols);
+  }
 }
 
 // ------------------------------------------------------------------ a3 / a4: blocks along rows (transposed output)
@@ -673,7 +687,8 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
   const uint32_t total = (uint32_t)p.rows * spr;
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
-  float sx2 = 0.f, e4 = 0.f, e8 = 0.f, v4 = 0.f, v8 = 0.f;
+  StatsAcc acc;
+  acc.init();
   // segment -> (row, segment in row), stepped without a division per iteration
   const uint32_t seg0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const uint32_t wq = wstride / spr, wr = wstride - wq * spr;
@@ -705,19 +720,17 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
     if (RND == 1) sr_bits16_rk(e0, p.stream_id, p.rk, u);
     const BlockScale bs = nvfp4_block_scale_tab(amax16_bits(a, b), six_g, s_tab);
     uint4 unused;
-    const BlockStats st = stats_block16<-1, RND>(v, bs, u, s8, inv8, special8, unused);
-    sx2 += st.x2;
-    e4 += st.e4;
-    e8 += st.e8;
-    v4 += st.v4;
-    v8 += st.v8;
+    float be4 = 0.f, be8 = 0.f;
+    stats_block16<-1, RND, BLK>(v, bs, u, s8, inv8, special8, unused, acc, &be4, &be8);
     if (BLK) {
       const int64_t bi = (int64_t)r * bpr + kb;
-      if (p.block_err4) p.block_err4[bi] = st.e4;
-      if (p.block_err8) p.block_err8[bi] = st.e8;
+      if (p.block_err4) p.block_err4[bi] = be4;
+      if (p.block_err8) p.block_err8[bi] = be8;
     }
   }
-  stats_finish(sx2, e4, e8, v4, v8, p.partials, p.counter, p.raw_out, amax, p.rows * p.cols);
+  float sums[5];
+  acc.finish(s8, special8, sums);
+  stats_finish(sums, p.partials, p.counter, p.raw_out, amax, p.rows * p.cols);
 }
 
 // ------------------------------------------------------------------ host-side launchers
