@@ -503,26 +503,32 @@ __global__ void __launch_bounds__(256, STATS ? 3 : 4) quant_rows_kernel(QuantPar
 }
 
 // ------------------------------------------------------------------ a3 / a4: blocks along rows (transposed output)
-// Tile: 128 source rows (8 blocks of the output contraction) x 64 source
-// columns (64 output rows).  Thread (column pair cp, block b) encodes the two
-// blocks of source columns 2cp and 2cp+1, rows 16b..16b+15.
-constexpr int kTR = 128, kTC = 64;
+// Tile: TR source rows (TR/16 blocks of the output contraction) x 64 source
+// columns (64 output rows), 2 TR threads.  Thread (column pair cp, block b)
+// encodes the two blocks of source columns 2cp and 2cp+1, rows 16b..16b+15.
+// TR = 64 (128 threads, ~22 KB of shared memory) fits on an SM beside a GEMM
+// CTA, so the column quantizations run next to the GEMMs; TR = 128 serves the
+// 128-element NVFP4 blocks, which need all 128 rows of the tile.
+constexpr int kTC = 64;
 constexpr int kXW = kTC / 2 + 4;   // words per staged source row (pairs of bf16), padded
 
 // FMT: 0 FP8, 1 NVFP4, 2 MXFP4 (a 32-row block is split over threads b and
 // b^1, which exchange their half maxima through shared memory).
-template <int FMT, int LAYOUT, int RND, bool ERR>
-__global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
+template <int FMT, int LAYOUT, int RND, bool ERR, int TR>
+__global__ void __launch_bounds__(2 * TR) quant_cols_kernel(QuantParams p) {
   static_assert(FMT < 2 || !ERR, "MXFP4 / E5M2 quantization has no block errors");
+  static_assert(TR == 64 || TR == 128, "tile rows");
   constexpr bool FP4 = FMT == 1 || FMT == 2;
-  constexpr int OB = FP4 ? kTR / 2 : kTR;         // output bytes per row of the tile
+  constexpr int NT = 2 * TR;                      // threads
+  constexpr int NB = TR / 16;                     // 16-row blocks per tile
+  constexpr int OB = FP4 ? TR / 2 : TR;           // output bytes per row of the tile
   constexpr int OW = OB / 4 + 1;                  // staged output row, words (odd: fewer conflicts)
-  __shared__ __align__(16) uint32_t xs[kTR][kXW];
-  __shared__ __align__(16) uint32_t rs[RND ? kTR : 1][RND ? kXW : 4];
+  __shared__ __align__(16) uint32_t xs[TR][kXW];
+  __shared__ __align__(16) uint32_t rs[RND ? TR : 1][RND ? kXW : 4];
   __shared__ uint32_t oc[kTC][OW];
-  __shared__ uint8_t os[FP4 ? kTC : 1][8];
-  __shared__ uint32_t amx[FP4 ? 8 : 1][FP4 ? 32 : 1][2];
-  __shared__ float oe[ERR ? kTC : 1][8];
+  __shared__ uint8_t os[FP4 ? kTC : 1][NB];
+  __shared__ uint32_t amx[FP4 ? NB : 1][FP4 ? 32 : 1][2];
+  __shared__ float oe[ERR ? kTC : 1][NB];
   // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
   const float g = FMT == 3 ? e5m2_tensor_scale(*p.scale) : *p.scale;
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && p.g_out)
@@ -532,12 +538,12 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
   const float inv8 = __frcp_rn(g);
   __shared__ float2 s_tab[FMT == 1 ? kScaleCodes : 1];
   if (FMT == 1) fill_scale_table(s_tab, g);   // ordered before its reads by the staging barrier below
-  const int64_t r0 = (int64_t)blockIdx.x * kTR;   // source row = output contraction index
+  const int64_t r0 = (int64_t)blockIdx.x * TR;    // source row = output contraction index
   const int64_t c0 = (int64_t)blockIdx.y * kTC;   // source col = output row
   const int t = threadIdx.x;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const int row = (t >> 3) + 32 * j, ch = t & 7;
+    const int row = (t >> 3) + (TR / 4) * j, ch = t & 7;   // NT / 8 rows per pass
     const int64_t gr = r0 + row, gc = c0 + ch * 8;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     const bool in = gr < p.rows && gc < p.cols;
@@ -614,8 +620,8 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
   constexpr int BPB = FP4 ? 8 : 16;   // bytes per 16-element block
   if (LAYOUT == 0) {
     // row pitch of the row-major layout is only block-aligned: one store per block
-    for (int idx = t; idx < kTC * 8; idx += 256) {
-      const int row = idx >> 3, b = idx & 7;
+    for (int idx = t; idx < kTC * NB; idx += NT) {
+      const int row = idx / NB, b = idx % NB;
       const int64_t orow = c0 + row;
       if (orow >= p.out_rows || r0 + 16 * b >= p.out_cols) continue;
       uint8_t* dst = p.codes + orow * (p.out_cols * BPB / 16) + (r0 + 16 * b) * BPB / 16;
@@ -625,7 +631,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
     }
   } else {
     constexpr int CH = OB / 16;              // 16-byte chunks per tile row
-    for (int idx = t; idx < kTC * CH; idx += 256) {
+    for (int idx = t; idx < kTC * CH; idx += NT) {
       const int row = idx / CH, ch = idx % CH;
       const int64_t orow = c0 + row;
       if (orow >= p.orp) continue;
@@ -634,17 +640,22 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
     }
   }
   if (FMT == 2 && t < kTC) {
-    // four E8M0 bytes per output row: the tile's 128 contraction elements
+    // NB/2 E8M0 bytes per output row: the tile's TR contraction elements
     const int64_t orow = c0 + t;
     const int64_t kb0 = r0 >> 5;
     if (LAYOUT == 0) {
       if (orow < p.out_rows)
-        for (int b = 0; b < 4 && (kb0 + b) * 32 < p.out_cols; ++b)
+        for (int b = 0; b < NB / 2 && (kb0 + b) * 32 < p.out_cols; ++b)
           p.scales[orow * (p.out_cols >> 5) + kb0 + b] = os[t][b];
     } else if (orow < p.orp) {
-      const uint32_t v = (uint32_t)os[t][0] | ((uint32_t)os[t][1] << 8) | ((uint32_t)os[t][2] << 16) |
-                         ((uint32_t)os[t][3] << 24);
-      *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset_mx(orow, kb0, p.ocp)) = v;
+      if constexpr (NB == 8) {
+        const uint32_t v = (uint32_t)os[t][0] | ((uint32_t)os[t][1] << 8) | ((uint32_t)os[t][2] << 16) |
+                           ((uint32_t)os[t][3] << 24);
+        *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset_mx(orow, kb0, p.ocp)) = v;
+      } else {   // two blocks: a byte pair at an even byte of the chunk word
+        const uint16_t v = (uint16_t)(os[t][0] | (os[t][1] << 8));
+        *reinterpret_cast<uint16_t*>(p.scales + mma_scale_offset_mx(orow, kb0, p.ocp)) = v;
+      }
     }
   }
   if (FMT == 1 && t < kTC) {
@@ -652,18 +663,18 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
     const int64_t kb0 = r0 >> 4;
     if (LAYOUT == 0) {
       if (orow < p.out_rows)
-        for (int b = 0; b < 8 && (kb0 + b) * 16 < p.out_cols; ++b)
+        for (int b = 0; b < NB && (kb0 + b) * 16 < p.out_cols; ++b)
           p.scales[orow * (p.out_cols >> 4) + kb0 + b] = os[t][b];
     } else if (orow < p.orp) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NB / 4; ++h) {
         const uint32_t v = (uint32_t)os[t][4 * h] | ((uint32_t)os[t][4 * h + 1] << 8) |
                            ((uint32_t)os[t][4 * h + 2] << 16) | ((uint32_t)os[t][4 * h + 3] << 24);
         *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(orow, kb0 + 4 * h, p.ocp)) = v;
       }
     }
     if (ERR && p.block_err && orow < p.out_rows)
-      for (int b = 0; b < 8 && (kb0 + b) * 16 < p.out_cols; ++b)
+      for (int b = 0; b < NB && (kb0 + b) * 16 < p.out_cols; ++b)
         p.block_err[orow * (p.out_cols >> 4) + kb0 + b] = oe[t][b];
   }
 }
@@ -797,6 +808,12 @@ cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint
 // a row-block quantization (persistent: want CTAs at most, cap partial slots)
 #define SNIP_ROWS(...) launch_persistent(quant_rows_kernel<__VA_ARGS__>, want, cap, num_sms, st, p)
 
+template <int FMT, int LY, int RN, bool ER, int TR>
+static void launch_cols(const QuantParams& p, cudaStream_t st) {
+  const dim3 grid((unsigned)((p.ocp + TR - 1) / TR), (unsigned)((p.orp + kTC - 1) / kTC));
+  quant_cols_kernel<FMT, LY, RN, ER, TR><<<grid, 2 * TR, 0, st>>>(p);
+}
+
 template <int FMT>
 static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int rnd, bool err, int num_sms,
                              cudaStream_t st) {
@@ -830,9 +847,23 @@ static void launch_quant_fmt(const QuantParams& p, int orient, int layout, int r
 #undef SNIP_LS
 #undef SNIP_L
   } else {
-    // source rows tile the output contraction, source cols the output rows
-    const dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
-#define SNIP_L(LY, RN, ER) quant_cols_kernel<FMT, LY, RN, ER><<<grid, 256, 0, st>>>(p)
+    // source rows tile the output contraction, source cols the output rows; 64-row tiles, except
+    // for blocks of 128 rows
+    if constexpr (FMT == 1) {
+      if (p.group >= 8) {
+#define SNIP_L(LY, RN, ER) launch_cols<FMT, LY, RN, ER, 128>(p, st)
+        if (layout == 0) {
+          if (rnd == 0) { if (err) SNIP_L(0, 0, true); else SNIP_L(0, 0, false); }
+          else { if (err) SNIP_L(0, 1, true); else SNIP_L(0, 1, false); }
+        } else {
+          if (rnd == 0) { if (err) SNIP_L(1, 0, true); else SNIP_L(1, 0, false); }
+          else { if (err) SNIP_L(1, 1, true); else SNIP_L(1, 1, false); }
+        }
+#undef SNIP_L
+        return;
+      }
+    }
+#define SNIP_L(LY, RN, ER) launch_cols<FMT, LY, RN, ER, 64>(p, st)
     if (layout == 0) {
       if (rnd == 0) { if (err) SNIP_L(0, 0, true); else SNIP_L(0, 0, false); }
       else { if (err) SNIP_L(0, 1, true); else SNIP_L(0, 1, false); }
@@ -867,13 +898,12 @@ static void launch_quant_mx(const QuantParams& p, int orient, int layout, int rn
       else SNIP_ROWS(2, 1, 1, false, false);
     }
   } else {
-    const dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
     if (layout == 0) {
-      if (rnd == 0) quant_cols_kernel<2, 0, 0, false><<<grid, 256, 0, st>>>(p);
-      else quant_cols_kernel<2, 0, 1, false><<<grid, 256, 0, st>>>(p);
+      if (rnd == 0) launch_cols<2, 0, 0, false, 64>(p, st);
+      else launch_cols<2, 0, 1, false, 64>(p, st);
     } else {
-      if (rnd == 0) quant_cols_kernel<2, 1, 0, false><<<grid, 256, 0, st>>>(p);
-      else quant_cols_kernel<2, 1, 1, false><<<grid, 256, 0, st>>>(p);
+      if (rnd == 0) launch_cols<2, 1, 0, false, 64>(p, st);
+      else launch_cols<2, 1, 1, false, 64>(p, st);
     }
   }
 }
@@ -901,13 +931,12 @@ static void launch_quant_e5(const QuantParams& p, int orient, int layout, int rn
       else SNIP_ROWS(3, 1, 1, false, false);
     }
   } else {
-    const dim3 grid((unsigned)((p.ocp + kTR - 1) / kTR), (unsigned)((p.orp + kTC - 1) / kTC));
     if (layout == 0) {
-      if (rnd == 0) quant_cols_kernel<3, 0, 0, false><<<grid, 256, 0, st>>>(p);
-      else quant_cols_kernel<3, 0, 1, false><<<grid, 256, 0, st>>>(p);
+      if (rnd == 0) launch_cols<3, 0, 0, false, 64>(p, st);
+      else launch_cols<3, 0, 1, false, 64>(p, st);
     } else {
-      if (rnd == 0) quant_cols_kernel<3, 1, 0, false><<<grid, 256, 0, st>>>(p);
-      else quant_cols_kernel<3, 1, 1, false><<<grid, 256, 0, st>>>(p);
+      if (rnd == 0) launch_cols<3, 1, 0, false, 64>(p, st);
+      else launch_cols<3, 1, 1, false, 64>(p, st);
     }
   }
 }
