@@ -720,18 +720,14 @@ snip_status snip_qlinear_fwd_multi(const snip_plan* plan, int count, const int* 
   return SNIP_OK;
 }
 
-snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W, const void* dY,
-                             int64_t T, int64_t K, int64_t N, float* dX, float* dW, double* stats_out, void* ws,
-                             size_t ws_bytes, void* stream) {
-  int sms;
-  snip_status s = current_device(&sms);
-  if (s != SNIP_OK) return s;
-  if ((s = check_ql(plan, layer, T, K, N)) != SNIP_OK) return s;
-  if (!X || !W || !dY || !dX || !dW) return SNIP_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < snip_qlinear_workspace_size(plan, layer, T, K, N)) return SNIP_ERR_WORKSPACE;
-  if (!aligned16(X) || !aligned16(W) || !aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(ws))
-    return SNIP_ERR_ALIGN;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+namespace {
+// The backward of one layer (snip_qlinear_bwd); with rq, its dgrad GEMM also writes the preceding
+// layer's gradient operands (snip_qlinear_bwd_chain) and dX may be NULL.  Arguments checked by the
+// callers.
+snip_status run_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W, const void* dY,
+                            int64_t T, int64_t K, int64_t N, float* dX, float* dW, double* stats_out, void* ws,
+                            int sms, cudaStream_t st, const snip_requant* rq) {
+  snip_status s;
   const int qg = gradient_fmt(plan->fmt[layer]);   // format of dY and dY^T (the GEMMs' A operands)
   const int qf = forward_fmt(plan->fmt[layer]);    // format of W^T and X^T
   const int* rnd = &plan->rnd[(size_t)layer * 6];
@@ -758,7 +754,7 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
                         b + L.op[1].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
     return s;
   if ((s = run_gemm(qg, b + L.op[0].codes_off, b + L.op[0].scales_off, gemm_scale(sd, qg), b + L.op[1].codes_off,
-                    b + L.op[1].scales_off, gemm_scale(sw, qf), T, K, N, dX, K, ws, sms, st)) != SNIP_OK)
+                    b + L.op[1].scales_off, gemm_scale(sw, qf), T, K, N, dX, K, ws, sms, st, rq)) != SNIP_OK)
     return s;
   // wgrad: dW = Q(dY^T) Q(X^T)^T, contraction T
   if ((s = run_quantize(qg, dY, T, N, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_DYT_WGRAD], plan->seed,
@@ -771,6 +767,22 @@ snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, co
     return s;
   return run_gemm(qg, b + L.op[2].codes_off, b + L.op[2].scales_off, gemm_scale(sd, qg), b + L.op[3].codes_off,
                   b + L.op[3].scales_off, gemm_scale(sx, qf), N, K, T, dW, K, ws, sms, st);
+}
+}  // namespace
+
+snip_status snip_qlinear_bwd(const snip_plan* plan, int layer, const void* X, const void* W, const void* dY,
+                             int64_t T, int64_t K, int64_t N, float* dX, float* dW, double* stats_out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  int sms;
+  snip_status s = current_device(&sms);
+  if (s != SNIP_OK) return s;
+  if ((s = check_ql(plan, layer, T, K, N)) != SNIP_OK) return s;
+  if (!X || !W || !dY || !dX || !dW) return SNIP_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < snip_qlinear_workspace_size(plan, layer, T, K, N)) return SNIP_ERR_WORKSPACE;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(ws))
+    return SNIP_ERR_ALIGN;
+  return run_qlinear_bwd(plan, layer, X, W, dY, T, K, N, dX, dW, stats_out, ws, sms,
+                         static_cast<cudaStream_t>(stream), nullptr);
 }
 
 // ---------------------------------------------------------------- NEXT-3: the backward chain
@@ -793,35 +805,11 @@ snip_status snip_qlinear_bwd_chain(const snip_plan* plan, int layer, int prev_la
       !aligned16(ws) || !aligned16(prev_codes) || !aligned16(prev_scales) || !aligned16(prev_codes_t) ||
       !aligned16(prev_scales_t))
     return SNIP_ERR_ALIGN;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int qg = gradient_fmt(plan->fmt[layer]);
-  const int qf = forward_fmt(plan->fmt[layer]);
-  const int* rnd = &plan->rnd[(size_t)layer * 6];
-  const int* prnd = &plan->rnd[(size_t)prev_layer * 6];
-  const uint64_t sid = (uint64_t)layer * 8, psid = (uint64_t)prev_layer * 8;
-  QlLayout L = ql_layout(qf, T, K, N, true);
-  uint8_t* b = static_cast<uint8_t*>(ws);
-  float* sx = scale_slot(ws, 0);
-  float* sw = scale_slot(ws, 1);
-  float* sd = scale_slot(ws, 2);
-  float* sd_out = qg == SNIP_FMT_FP8_E5M2 ? sd + 3 : nullptr;
-  {
-    const void* xs[3] = {dY, W, X};
-    const int64_t ns[3] = {T * N, N * K, T * K};
-    float* outs[3] = {sd, sw, sx};
-    if ((s = run_scales_multi(3, xs, ns, outs, ws, sms, st)) != SNIP_OK) return s;
-  }
-  // dgrad: its product dX (T x K) is the preceding layer's dY, written as that layer's two NVFP4
+  // the dgrad product dX (T x K) is the preceding layer's dY, written as that layer's two NVFP4
   // operands (row blocks along K for its dgrad, column blocks along T for its wgrad) with the given
   // tensor scale and that layer's roundings and stream ids
-  if ((s = run_quantize(qg, dY, T, N, SNIP_BLOCKS_ALONG_COLS, rnd[SNIP_TAG_DY_DGRAD], plan->seed,
-                        sid + SNIP_TAG_DY_DGRAD, sd + scale_index(qg), SNIP_LAYOUT_MMA, b + L.op[0].codes_off,
-                        b + L.op[0].scales_off, sd_out, nullptr, sms, st, sd, stats_out, ws)) != SNIP_OK)
-    return s;
-  if ((s = run_quantize(qf, W, N, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_WT_DGRAD], plan->seed,
-                        sid + SNIP_TAG_WT_DGRAD, sw + scale_index(qf), SNIP_LAYOUT_MMA, b + L.op[1].codes_off,
-                        b + L.op[1].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
-    return s;
+  const int* prnd = &plan->rnd[(size_t)prev_layer * 6];
+  const uint64_t psid = (uint64_t)prev_layer * 8;
   snip_requant rq;
   rq.g_in = g_prev;
   rq.rnd = prnd[SNIP_TAG_DY_DGRAD];
@@ -834,20 +822,8 @@ snip_status snip_qlinear_bwd_chain(const snip_plan* plan, int layer, int prev_la
   rq.stream_id_t = psid + SNIP_TAG_DYT_WGRAD;
   rq.codes_t = prev_codes_t;
   rq.scales_t = prev_scales_t;
-  if ((s = run_gemm(qg, b + L.op[0].codes_off, b + L.op[0].scales_off, gemm_scale(sd, qg), b + L.op[1].codes_off,
-                    b + L.op[1].scales_off, gemm_scale(sw, qf), T, K, N, dX, K, ws, sms, st, &rq)) != SNIP_OK)
-    return s;
-  // wgrad as in snip_qlinear_bwd
-  if ((s = run_quantize(qg, dY, T, N, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_DYT_WGRAD], plan->seed,
-                        sid + SNIP_TAG_DYT_WGRAD, sd + scale_index(qg), SNIP_LAYOUT_MMA, b + L.op[2].codes_off,
-                        b + L.op[2].scales_off, sd_out, nullptr, sms, st)) != SNIP_OK)
-    return s;
-  if ((s = run_quantize(qf, X, T, K, SNIP_BLOCKS_ALONG_ROWS, rnd[SNIP_TAG_XT_WGRAD], plan->seed,
-                        sid + SNIP_TAG_XT_WGRAD, sx + scale_index(qf), SNIP_LAYOUT_MMA, b + L.op[3].codes_off,
-                        b + L.op[3].scales_off, nullptr, nullptr, sms, st)) != SNIP_OK)
-    return s;
-  return run_gemm(qg, b + L.op[2].codes_off, b + L.op[2].scales_off, gemm_scale(sd, qg), b + L.op[3].codes_off,
-                  b + L.op[3].scales_off, gemm_scale(sx, qf), N, K, T, dW, K, ws, sms, st);
+  return run_qlinear_bwd(plan, layer, X, W, dY, T, K, N, dX, dW, stats_out, ws, sms,
+                         static_cast<cudaStream_t>(stream), &rq);
 }
 
 snip_status snip_qlinear_bwd_q(const snip_plan* plan, int layer, const void* X, const void* W,

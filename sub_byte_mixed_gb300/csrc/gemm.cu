@@ -713,11 +713,7 @@ __global__ void __launch_bounds__(448, 1)
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
+EncodeTiledFn tensor_map_encoder() {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* ptr = nullptr;
@@ -733,7 +729,7 @@ static EncodeTiledFn encode_fn() {
 // 2-D byte tensor rows x row_bytes, loaded in boxes of box_rows x 128 bytes
 // with the 128-byte swizzle the MMA descriptors expect.
 static bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t row_bytes, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
@@ -773,7 +769,7 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
 // box_rows rows (one 128-row group's scales for 256 contraction elements:
 // 2 KB for NVFP4, 1 KB for MXFP4) at a time.
 static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {256u, (cuuint64_t)(bytes / 256)};
   cuuint64_t strides[1] = {256u};

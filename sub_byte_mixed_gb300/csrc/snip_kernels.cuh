@@ -3,6 +3,7 @@
 // (api.cu).  Internal to the library.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "snip_device.cuh"
@@ -175,6 +176,13 @@ cudaError_t launch_dw_noise_gemm(const void* X, const void* dY, int64_t T, int64
 // maps.
 cudaError_t launch_gemm(int fmt, const uint8_t* a_codes, int64_t a_rows_padded, const uint8_t* b_codes,
                         int64_t b_rows_padded, const GemmParams& p, int num_sms, cudaStream_t st);
+
+// The driver's cuTensorMapEncodeTiled (looked up once through the runtime), or null if unavailable.
+// Defined in gemm.cu, used by every kernel launcher that builds TMA tensor maps.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 // Self-check of the bounded wait (waitcheck.cu): out = {completed 0, completed 1, ns}.
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, uint32_t* out, cudaStream_t st);
