@@ -446,9 +446,13 @@ struct Gemm2Cfg {
   static constexpr int SFB_BYTES = FMT ? 2 * CH * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int RQ_BYTES = RQ ? 8 * kRqStageWords * 8 : 0;
+  // Without re-quantization D leaves through TMA stores: each epilogue warp stages a 32 x 32 fp32 box
+  // (4 KB, 128-byte swizzle) in shared memory.
+  static constexpr bool TMA_D = !RQ;
+  static constexpr int STG_BYTES = TMA_D ? 8 * 4096 : 0;
   // NVFP4 five stages (tensor memory holds five stages of scales), else six, or fewer to fit
   static constexpr int BASE_STAGES = FMT == 1 ? 5 : 6;
-  static constexpr int FIT_STAGES = (kMaxSmem - 2048 - RQ_BYTES) / STAGE_BYTES;
+  static constexpr int FIT_STAGES = (kMaxSmem - 2048 - RQ_BYTES - STG_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = BASE_STAGES < FIT_STAGES ? BASE_STAGES : FIT_STAGES;
   static constexpr int ACC_STAGES = (FMT || NS == 2) ? 1 : 2;
   static constexpr int SFA_COLS = 4 * CH;
@@ -459,7 +463,7 @@ struct Gemm2Cfg {
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
   static_assert(STAGE_BYTES % 1024 == 0, "1024-byte aligned stages");
   static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_STAGES + 1;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024 + RQ_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024 + RQ_BYTES + STG_BYTES;
   static_assert(SMEM_BYTES <= kMaxSmem, "shared memory budget");
   static constexpr int SF_WARPS = 4, EPI_WARP0 = 6, EPI_WARPS = 8, EPI_COLS = BN / 2, EPI_ROUND = RQ ? 32 : 64;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
@@ -469,11 +473,13 @@ struct Gemm2Cfg {
           : ((1u << 4) | ((uint32_t)(MMA_N >> 3) << 17) | ((uint32_t)(256 >> 4) << 24));
 };
 
+// 448 threads; 96 registers a thread without re-quantization, so that a 256-thread quantizer CTA of
+// up to 80 registers fits beside the GEMM CTA on its SM when the two streams overlap.
 template <int FMT, bool RQ = false, int NS = 1>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __maxnreg__(RQ ? 128 : 96)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                        GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmD, GemmParams p) {
   using C = Gemm2Cfg<FMT, RQ, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -641,13 +647,18 @@ __global__ void __launch_bounds__(448, 1)
     uint32_t rq_am = 0;
     uint2* rq_stg = reinterpret_cast<uint2*>(smem + C::STAGES * C::STAGE_BYTES + 1024) +
                     (warp - C::EPI_WARP0) * kRqStageWords;
+    // TMA-store staging box of this warp: row i (its lane i's row) at 128 i, 16-byte chunk j of the
+    // row at chunk position j ^ (i & 7) (the 128-byte swizzle; the box is 1024-byte aligned)
+    const uint32_t stg = smem_u32(smem + C::STAGES * C::STAGE_BYTES + 1024 + C::RQ_BYTES) +
+                         (uint32_t)(warp - C::EPI_WARP0) * 4096u;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
       if (!mbar_wait_bounded(tfull(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * C::BN + half * C::EPI_COLS;
-      const int64_t row = (int64_t)(2 * mt + rank) * C::BM + q * 32 + lane;
+      const int64_t row0 = (int64_t)(2 * mt + rank) * C::BM + q * 32;   // the warp's first row
+      const int64_t row = row0 + lane;
       float* drow = p.D ? p.D + row * p.ldd : nullptr;
       const int64_t col0 = (int64_t)nt * C::BN + half * C::EPI_COLS;
 #pragma unroll 1
@@ -673,7 +684,27 @@ __global__ void __launch_bounds__(448, 1)
                                             : requant32_t<0>(r[c], alpha, row, row - lane, col, p, rq_g, rq_six_g, rq_stg));
           }
         }
-        if (p.D && row < p.M) {
+        if constexpr (C::TMA_D) {
+#pragma unroll
+          for (int c = 0; c < C::EPI_ROUND / 32; ++c) {
+            const int64_t col = col0 + rd * C::EPI_ROUND + c * 32;
+            if (lane == 0) bulk_wait_read0();   // the previous box has left the staging buffer
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              st_shared_v4(stg + 128u * lane + 16u * (uint32_t)(k ^ (lane & 7)),
+                           __fmul_rn(alpha, __uint_as_float(r[c][4 * k])),
+                           __fmul_rn(alpha, __uint_as_float(r[c][4 * k + 1])),
+                           __fmul_rn(alpha, __uint_as_float(r[c][4 * k + 2])),
+                           __fmul_rn(alpha, __uint_as_float(r[c][4 * k + 3])));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && row0 < p.M && col < p.N) {   // rows or columns past D are not written
+              tma_store_2d(&tmD, stg, (int32_t)col, (int32_t)row0);
+              bulk_commit();
+            }
+          }
+        } else if (p.D && row < p.M) {   // the re-quantizing kernels: D optional, stored from registers
 #pragma unroll
           for (int c = 0; c < C::EPI_ROUND / 32; ++c)
 #pragma unroll
@@ -701,6 +732,7 @@ __global__ void __launch_bounds__(448, 1)
       if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
     }
     if (RQ && p.rq_amax) requant_publish_amax(rq_am, p.rq_amax);
+    if (C::TMA_D && lane == 0) bulk_wait0();   // every box written before the CTA leaves
   }
   __syncwarp();
   tc_fence_before();
@@ -780,10 +812,29 @@ static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// D (M x N fp32, row stride ldd) for TMA stores of 32 x 32 boxes with the 128-byte swizzle; false when
+// D's base or row stride is not 16-byte aligned (the epilogue then stores from registers).
+static bool make_out_map(CUtensorMap* m, float* D, int64_t M, int64_t N, int64_t ldd) {
+  EncodeTiledFn fn = tensor_map_encoder();
+  if (!fn || !D || reinterpret_cast<uintptr_t>(D) % 16 != 0 || ldd % 4 != 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)ldd * 4u};
+  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, D, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 template <int FMT, bool RQ, int NS = 1>
 static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
                                     GemmParams p, int num_sms, cudaStream_t st) {
   using C = Gemm2Cfg<FMT, RQ, NS>;
+  CUtensorMap td;
+  memset(&td, 0, sizeof td);
+  // a D whose base or row stride does not suit TMA stores goes to the one-CTA kernel
+  if (C::TMA_D && !make_out_map(&td, p.D, p.M, p.N, p.ldd))
+    return launch_gemm_cfg<FMT, 256, RQ>(a_codes, a_rows, b_codes, b_rows, p, num_sms, st);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT, RQ, NS>,
@@ -819,7 +870,7 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT, RQ, NS>, ta, tb, tsa, tsb, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT, RQ, NS>, ta, tb, tsa, tsb, td, p);
 }
 
 // FP8 on 256 x 512 pair tiles for long contractions (measured on GB300: the
