@@ -446,10 +446,11 @@ struct Gemm2Cfg {
   static constexpr int SFB_BYTES = FMT ? 2 * CH * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int RQ_BYTES = RQ ? 8 * kRqStageWords * 8 : 0;
-  // Without re-quantization D leaves through TMA stores: each epilogue warp stages a 32 x 32 fp32 box
-  // (4 KB, 128-byte swizzle) in shared memory.
+  // Without re-quantization D leaves through TMA stores: each epilogue warp stages 32 x 16 fp32 boxes
+  // (2 KB, 64-byte swizzle) in STG_BUFS shared-memory buffers.
   static constexpr bool TMA_D = !RQ;
-  static constexpr int STG_BYTES = TMA_D ? 8 * 4096 : 0;
+  static constexpr int STG_BUFS = 2;
+  static constexpr int STG_BYTES = TMA_D ? 8 * STG_BUFS * 2048 : 0;
   // NVFP4 five stages (tensor memory holds five stages of scales), else six, or fewer to fit
   static constexpr int BASE_STAGES = FMT == 1 ? 5 : 6;
   static constexpr int FIT_STAGES = (kMaxSmem - 2048 - RQ_BYTES - STG_BYTES) / STAGE_BYTES;
@@ -647,10 +648,12 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
     uint32_t rq_am = 0;
     uint2* rq_stg = reinterpret_cast<uint2*>(smem + C::STAGES * C::STAGE_BYTES + 1024) +
                     (warp - C::EPI_WARP0) * kRqStageWords;
-    // TMA-store staging box of this warp: row i (its lane i's row) at 128 i, 16-byte chunk j of the
-    // row at chunk position j ^ (i & 7) (the 128-byte swizzle; the box is 1024-byte aligned)
+    // TMA-store staging of this warp: STG_BUFS 2 KB buffers, each a 32-row x 16-column box with row i
+    // (its lane i's row) at 64 i and 16-byte chunk j of the row at position j ^ ((i >> 1) & 3) (the
+    // 64-byte swizzle; buffers 2048-byte aligned).  A box is staged while earlier ones are being stored.
     const uint32_t stg = smem_u32(smem + C::STAGES * C::STAGE_BYTES + 1024 + C::RQ_BYTES) +
-                         (uint32_t)(warp - C::EPI_WARP0) * 4096u;
+                         (uint32_t)(warp - C::EPI_WARP0) * (uint32_t)(C::STG_BUFS * 2048);
+    uint32_t nbox = 0;   // boxes this warp has stored: picks the buffer
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
@@ -686,24 +689,30 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
         }
         if constexpr (C::TMA_D) {
 #pragma unroll
-          for (int c = 0; c < C::EPI_ROUND / 32; ++c) {
-            const int64_t col = col0 + rd * C::EPI_ROUND + c * 32;
-            if (lane == 0) bulk_wait_read0();   // the previous box has left the staging buffer
-            __syncwarp();
+          for (int c = 0; c < C::EPI_ROUND / 32; ++c)
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              st_shared_v4(stg + 128u * lane + 16u * (uint32_t)(k ^ (lane & 7)),
-                           __fmul_rn(alpha, __uint_as_float(r[c][4 * k])),
-                           __fmul_rn(alpha, __uint_as_float(r[c][4 * k + 1])),
-                           __fmul_rn(alpha, __uint_as_float(r[c][4 * k + 2])),
-                           __fmul_rn(alpha, __uint_as_float(r[c][4 * k + 3])));
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && row0 < p.M && col < p.N) {   // rows or columns past D are not written
-              tma_store_2d(&tmD, stg, (int32_t)col, (int32_t)row0);
-              bulk_commit();
+            for (int h = 0; h < 2; ++h) {
+              const int64_t col = col0 + rd * C::EPI_ROUND + c * 32 + 16 * h;
+              if (row0 < p.M && col < p.N) {   // (warp-uniform) a box wholly past D is skipped
+                const uint32_t buf = stg + 2048u * (nbox % (uint32_t)C::STG_BUFS);
+                if (lane == 0) bulk_wait_read<C::STG_BUFS - 1>();   // this buffer's previous box has left it
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  st_shared_v4(buf + 64u * lane + 16u * (uint32_t)(k ^ ((lane >> 1) & 3)),
+                               __fmul_rn(alpha, __uint_as_float(r[c][16 * h + 4 * k])),
+                               __fmul_rn(alpha, __uint_as_float(r[c][16 * h + 4 * k + 1])),
+                               __fmul_rn(alpha, __uint_as_float(r[c][16 * h + 4 * k + 2])),
+                               __fmul_rn(alpha, __uint_as_float(r[c][16 * h + 4 * k + 3])));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {   // elements past M or N are not written
+                  tma_store_2d(&tmD, buf, (int32_t)col, (int32_t)row0);
+                  bulk_commit();
+                }
+                ++nbox;
+              }
             }
-          }
         } else if (p.D && row < p.M) {   // the re-quantizing kernels: D optional, stored from registers
 #pragma unroll
           for (int c = 0; c < C::EPI_ROUND / 32; ++c)
@@ -812,17 +821,17 @@ static bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t bytes, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// D (M x N fp32, row stride ldd) for TMA stores of 32 x 32 boxes with the 128-byte swizzle; false when
-// D's base or row stride is not 16-byte aligned (the epilogue then stores from registers).
+// D (M x N fp32, row stride ldd) for TMA stores of 32-row x 16-column boxes with the 64-byte swizzle;
+// false when D's base or row stride is not 16-byte aligned.
 static bool make_out_map(CUtensorMap* m, float* D, int64_t M, int64_t N, int64_t ldd) {
   EncodeTiledFn fn = tensor_map_encoder();
   if (!fn || !D || reinterpret_cast<uintptr_t>(D) % 16 != 0 || ldd % 4 != 0) return false;
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
   cuuint64_t strides[1] = {(cuuint64_t)ldd * 4u};
-  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t box[2] = {16u, 32u};
   cuuint32_t estr[2] = {1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, D, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
 
