@@ -539,9 +539,10 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
             const int64_t ga = 2 * mt + rank;
             constexpr int R = C::SFA_BYTES / 256;   // 256-byte rows of one 128-row group's stage scales
             tma_load_2d(smem_u32(sSFA), &tmSFA, 0, (int32_t)(R * (ga * groups_k + kb)), sffull(stage));
-            for (int h = 0; h < 2; ++h)
-              tma_load_2d(smem_u32(sSFB + C::SFA_BYTES * h), &tmSFB, 0,
-                          (int32_t)(R * ((2 * nt + h) * groups_k + kb)), sffull(stage));
+            // both CTAs need the scales of all 256 B rows: each loads its own 128 rows' half and
+            // multicasts it to the pair (the peer's half lands here on this CTA's barrier)
+            tma_load_2d_mc(smem_u32(sSFB + C::SFA_BYTES * rank), &tmSFB, 0,
+                           (int32_t)(R * ((2 * nt + rank) * groups_k + kb)), sffull(stage), (uint16_t)0x3);
           }
           if (rank == 0) mbar_arrive_expect_tx(full(stage), 2 * (C::A_BYTES + C::B_BYTES));
           const uint32_t leader_full = mapa_shared(full(stage), 0);

@@ -294,6 +294,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       "l"(tmap), "r"(c0), "r"(c1), "r"(bar_cluster)
       : "memory");
 }
+// TMA load multicast to the CTAs of `mask` in the cluster: each receives the box at the same shared-memory
+// offset and its completion on its own mbarrier at the same offset.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
