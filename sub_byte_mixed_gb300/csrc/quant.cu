@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(2 * TR) quant_cols_kernel(QuantParams p) {
   {
     const int cp = t & 31, b = t >> 5;
     float v0[16], v1[16];
-    uint32_t m0 = 0, m1 = 0;
+    uint32_t m01 = 0;   // the two columns' maxima of |bf16| bits, as the word's two 16-bit halves
     // random words of rows b*16..b*16+15: column 2cp's bits in the low half, 2cp+1's in the high half
     uint32_t rw[16];
 #pragma unroll
@@ -567,10 +567,10 @@ __global__ void __launch_bounds__(2 * TR) quant_cols_kernel(QuantParams p) {
       const uint32_t w = xs[b * 16 + i][cp];
       v0[i] = __uint_as_float(w << 16);
       v1[i] = __uint_as_float(w & 0xffff0000u);
-      m0 = max(m0, w & 0x7fffu);
-      m1 = max(m1, (w >> 16) & 0x7fffu);
+      m01 = __vmaxu2(m01, w & 0x7fff7fffu);
       rw[i] = RND == 1 ? rs[b * 16 + i][cp] : 0u;
     }
+    uint32_t m0 = m01 & 0xffffu, m1 = m01 >> 16;
     const WordHalfBits<false> u0{rw};
     const WordHalfBits<true> u1{rw};
     if (FMT == 2) {
