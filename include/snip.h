@@ -38,6 +38,12 @@
  *    the sticky device status word; initialise them once with
  *    snip_workspace_init().  Calls that share a workspace must be ordered on
  *    one stream.
+ *  - Sizes: a tensor dimension above 2^31 - 1, or a tensor (operand or GEMM
+ *    output) of more than 2^40 elements, is SNIP_ERR_SHAPE (the kernels count
+ *    tiles and segments in 32 bits and address TMA boxes with 32-bit
+ *    coordinates).  Empty tensors are accepted wherever the entry point's
+ *    text does not require a positive size: nothing is written to their
+ *    outputs, and a tensor scale computed from no elements is 1.
  *  - Random bits for stochastic rounding come from Philox4x32-10 (Salmon et
  *    al., SC'11) keyed by `seed`; source element e (row-major index into the
  *    tensor being quantized, whatever the output orientation) uses 16 bits of

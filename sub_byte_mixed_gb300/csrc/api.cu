@@ -31,6 +31,11 @@ constexpr uint64_t kTimeoutNs = 4000000000ull;   // a GEMM wait that takes 4 s i
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Largest sizes the kernels index with 32-bit tile and segment counts and TMA coordinates: each dimension
+// below 2^31, at most 2^40 elements a tensor (far beyond the device's memory).
+inline bool too_large(int64_t rows, int64_t cols) {
+  return rows > INT32_MAX || cols > INT32_MAX || rows * cols > ((int64_t)1 << 40);
+}
 
 template <typename T>
 inline T* ws_at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off); }
@@ -368,7 +373,7 @@ static snip_status check_quantize_args(int fmt, const void* x, int64_t rows, int
   if (is_fp4(fmt) && !scales) return SNIP_ERR_INVALID_ARG;
   const int64_t be = block_elems(fmt);   // the blocked dim is a whole number of blocks
   if (cols % 16 != 0 || (orient == SNIP_BLOCKS_ALONG_ROWS && rows % be != 0) ||
-      (orient == SNIP_BLOCKS_ALONG_COLS && cols % be != 0))
+      (orient == SNIP_BLOCKS_ALONG_COLS && cols % be != 0) || too_large(rows, cols))
     return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(ws) || (scales && !aligned16(scales))) return SNIP_ERR_ALIGN;
@@ -454,7 +459,8 @@ snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_
   if (fmt != SNIP_FMT_MXFP4 && (!ga || !gb)) return SNIP_ERR_INVALID_ARG;
   if (is_fp4(fmt) && (!a_scales || !b_scales)) return SNIP_ERR_INVALID_ARG;
   if (fmt == SNIP_FMT_MXFP4 && K % 32 != 0) return SNIP_ERR_SHAPE;
-  if (K % 16 != 0 || K == 0 || ldd % 4 != 0) return SNIP_ERR_SHAPE;
+  if (K % 16 != 0 || K == 0 || ldd % 4 != 0 || too_large(M, N) || too_large(M, K) || too_large(N, K))
+    return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < SNIP_WS_HEADER_BYTES) return SNIP_ERR_WORKSPACE;
   if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(D) || !aligned16(ws) ||
       (is_fp4(fmt) && (!aligned16(a_scales) || !aligned16(b_scales))))
@@ -479,7 +485,7 @@ snip_status snip_gemm_requant(snip_format fmt, const uint8_t* a_codes, const uin
   if (fmt != SNIP_FMT_MXFP4 && (!ga || !gb)) return SNIP_ERR_INVALID_ARG;
   if (is_fp4(fmt) && (!a_scales || !b_scales)) return SNIP_ERR_INVALID_ARG;
   if (K % 16 != 0 || K == 0 || N % 16 != 0 || (rq->codes_t && M % 16 != 0) || (D && ldd % 4 != 0) ||
-      (fmt == SNIP_FMT_MXFP4 && K % 32 != 0))
+      (fmt == SNIP_FMT_MXFP4 && K % 32 != 0) || too_large(M, N) || too_large(M, K) || too_large(N, K))
     return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < SNIP_WS_HEADER_BYTES) return SNIP_ERR_WORKSPACE;
   if (!aligned16(a_codes) || !aligned16(b_codes) || (D && !aligned16(D)) || !aligned16(ws) ||
@@ -559,7 +565,7 @@ snip_status check_ql(const snip_plan* plan, int layer, int64_t T, int64_t K, int
   if (!plan || layer < 0 || layer >= (int)plan->fmt.size()) return SNIP_ERR_INVALID_ARG;
   if (T <= 0 || K <= 0 || N <= 0) return SNIP_ERR_INVALID_ARG;
   const int64_t be = block_elems(plan->fmt[layer]);   // every dim is blocked by one of the quantizations
-  if (T % be || K % be || N % be) return SNIP_ERR_SHAPE;
+  if (T % be || K % be || N % be || too_large(T, K) || too_large(T, N) || too_large(N, K)) return SNIP_ERR_SHAPE;
   return SNIP_OK;
 }
 }  // namespace
@@ -878,7 +884,7 @@ snip_status snip_quant_stats(const void* a, int64_t rows, int64_t cols, snip_rou
   snip_status s = current_device(&sms);
   if (s != SNIP_OK) return s;
   if (!valid_enum(rnd, 2) || rows < 0 || cols < 0 || !raw_out || (rows * cols > 0 && !a)) return SNIP_ERR_INVALID_ARG;
-  if (cols % 16 != 0) return SNIP_ERR_SHAPE;
+  if (cols % 16 != 0 || too_large(rows, cols)) return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < kSmallWorkspace) return SNIP_ERR_WORKSPACE;
   if (!aligned16(a) || !aligned16(ws)) return SNIP_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -964,7 +970,7 @@ snip_status snip_dw_noise(const void* X, const void* dY, int64_t T, int64_t K, i
   if (s != SNIP_OK) return s;
   if (!X || !dY || !dW_q || !out2 || T <= 0 || K <= 0 || N <= 0) return SNIP_ERR_INVALID_ARG;
   if (T % 16 || K % 16 || N % 16) return SNIP_ERR_SHAPE;
-  if (T > INT32_MAX || K > INT32_MAX || N > INT32_MAX) return SNIP_ERR_SHAPE;   // TMA coordinates are 32-bit
+  if (too_large(T, K) || too_large(T, N) || too_large(N, K)) return SNIP_ERR_SHAPE;
   if (!ws || ws_bytes < snip_dw_noise_workspace_size(K, N)) return SNIP_ERR_WORKSPACE;
   if (!aligned16(X) || !aligned16(dY) || !aligned16(dW_q) || !aligned16(ws)) return SNIP_ERR_ALIGN;
   return cuda_status(launch_dw_noise_gemm(X, dY, T, K, N, dW_q, ws_at<double>(ws, kOffStatsPartials),

@@ -531,15 +531,19 @@ __global__ void __launch_bounds__(2 * TR) quant_cols_kernel(QuantParams p) {
   __shared__ float oe[ERR ? kTC : 1][NB];
   // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
   const float g = FMT == 3 ? e5m2_tensor_scale(*p.scale) : *p.scale;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && p.g_out)
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out)
     *p.g_out = (FMT == 2 && !isnan(g)) ? 1.0f : g;
   if (isnan(g)) return;
   const float six_g = __fmul_rn(6.0f, g);
   const float inv8 = __frcp_rn(g);
   __shared__ float2 s_tab[FMT == 1 ? kScaleCodes : 1];
   if (FMT == 1) fill_scale_table(s_tab, g);   // ordered before its reads by the staging barrier below
-  const int64_t r0 = (int64_t)blockIdx.x * TR;    // source row = output contraction index
-  const int64_t c0 = (int64_t)blockIdx.y * kTC;   // source col = output row
+  // a one-dimensional grid (a second dimension would cap the output rows at 65535 tiles): tile
+  // (bx, by), bx along the output contraction fastest
+  const uint32_t gx = (uint32_t)((p.ocp + TR - 1) / TR);
+  const uint32_t by = blockIdx.x / gx, bx = blockIdx.x - by * gx;
+  const int64_t r0 = (int64_t)bx * TR;    // source row = output contraction index
+  const int64_t c0 = (int64_t)by * kTC;   // source col = output row
   const int t = threadIdx.x;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -810,8 +814,8 @@ cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint
 
 template <int FMT, int LY, int RN, bool ER, int TR>
 static void launch_cols(const QuantParams& p, cudaStream_t st) {
-  const dim3 grid((unsigned)((p.ocp + TR - 1) / TR), (unsigned)((p.orp + kTC - 1) / kTC));
-  quant_cols_kernel<FMT, LY, RN, ER, TR><<<grid, 2 * TR, 0, st>>>(p);
+  const int64_t tiles = ((p.ocp + TR - 1) / TR) * ((p.orp + kTC - 1) / kTC);   // checked < 2^31 by the API
+  quant_cols_kernel<FMT, LY, RN, ER, TR><<<(unsigned)tiles, 2 * TR, 0, st>>>(p);
 }
 
 template <int FMT>

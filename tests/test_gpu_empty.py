@@ -1,4 +1,4 @@
-"""Empty inputs through the C ABI: every quantizer (each operand format,
+"""Empty and oversized inputs through the C ABI: every quantizer (each operand format,
 both orientations and layouts) on tensors with no rows, no columns or
 neither, the tensor scales and the statistics pass on no elements, and a
 GEMM with no output rows or columns.  Each call returns SNIP_OK, writes
@@ -6,7 +6,9 @@ nothing outside its (empty) outputs -- guard bytes around them keep their
 sentinel -- and still publishes what the oracle gives for an empty tensor:
 amax 0, so g = s = 1 (the NVFP4 / FP8 scale definitions take 1 for an
 all-zero tensor), and statistics sums and count 0.  The layer API has no
-empty layer: T = 0 is SNIP_ERR_INVALID_ARG."""
+empty layer: T = 0 is SNIP_ERR_INVALID_ARG.  Dimensions beyond the kernels'
+32-bit tile counts and TMA coordinates (above 2^31 - 1, or tensors of more
+than 2^40 elements) are SNIP_ERR_SHAPE before anything is read or launched."""
 import numpy as np
 import pytest
 import torch
@@ -129,3 +131,30 @@ def test_layer_without_tokens_is_rejected(snip):
         assert L.snip_qlinear_fwd(plan.handle, layer, X.data_ptr(), X.data_ptr(), 0, 128, 128, Y.data_ptr(), None,
                                   ws.ptr, ws.nbytes, torch.cuda.current_stream().cuda_stream) == \
             snip.SNIP_ERR_INVALID_ARG
+
+
+def test_oversized_dimensions_rejected(snip):
+    L = snip.load()
+    buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")   # never read: the size checks come first
+    P = buf.data_ptr()
+    ws = snip.small_workspace()
+    st = torch.cuda.current_stream().cuda_stream
+    big, wide = 1 << 31, 1 << 26                         # 2^31 rows; 2^26 x 2^26 = 2^52 elements
+    for rows, cols in ((big, 16), (16, big), (wide, wide)):
+        assert L.snip_quantize_nvfp4(P, rows, cols, 0, 0, 0, 0, None, 0, P, P, P, None, ws.ptr, ws.nbytes,
+                                     st) == snip.SNIP_ERR_SHAPE
+        assert L.snip_quantize_fp8(P, rows, cols, 1, 0, 0, 0, None, 1, P, P, ws.ptr, ws.nbytes,
+                                   st) == snip.SNIP_ERR_SHAPE
+        assert L.snip_quant_stats(P, rows, cols, 0, 0, 0, None, P, None, None, ws.ptr, ws.nbytes,
+                                  st) == snip.SNIP_ERR_SHAPE
+    g = torch.ones(1, dtype=torch.float32, device="cuda")
+    for M, N, K in ((big, 256, 256), (256, big, 256), (256, 256, big), (wide, wide, 256)):
+        assert L.snip_gemm(1, P, P, g.data_ptr(), P, P, g.data_ptr(), M, N, K, P, N, ws.ptr, ws.nbytes,
+                           st) == snip.SNIP_ERR_SHAPE
+    plan = snip.Plan([snip.NVFP4])
+    for T, K, N in ((big, 256, 256), (256, big, 256), (wide, wide, 256)):
+        assert L.snip_qlinear_workspace_size(plan.handle, 0, T, K, N) == 0
+        assert L.snip_qlinear_fwd(plan.handle, 0, P, P, T, K, N, P, None, ws.ptr, ws.nbytes, st) == \
+            snip.SNIP_ERR_SHAPE
+    torch.cuda.synchronize()
+    assert ws.status() == snip.SNIP_OK
