@@ -271,13 +271,8 @@ cudaError_t launch_dw_noise_gemm(const void* X, const void* dY, int64_t T, int64
                                  double* partials, uint32_t* counter, double* out2, uint32_t* status,
                                  uint64_t timeout_ns, int num_sms, cudaStream_t st) {
   using C = DwCfg;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(dw_noise_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(dw_noise_gemm_kernel), C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   CUtensorMap ta, tb;
   if (!make_bf16_map(&ta, dY, T, N) || !make_bf16_map(&tb, X, T, K)) return cudaErrorInvalidValue;
   DwParams p;

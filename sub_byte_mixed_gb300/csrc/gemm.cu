@@ -758,15 +758,15 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
 
 // ------------------------------------------------------------------ host side
 EncodeTiledFn tensor_map_encoder() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  static const EncodeTiledFn fn = [] {   // looked up once (thread-safe initialisation)
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return (EncodeTiledFn) nullptr;
+  }();
   return fn;
 }
 
@@ -788,13 +788,8 @@ template <int FMT, int BN, bool RQ>
 static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int64_t b_rows,
                                    GemmParams p, int num_sms, cudaStream_t st) {
   using C = GemmCfg<FMT, BN, RQ>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<FMT, BN, RQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(gemm_tn_kernel<FMT, BN, RQ>), C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   const int64_t row_bytes = FMT ? p.kp / 2 : p.kp;
   CUtensorMap ta, tb;
   if (!make_code_map(&ta, a_codes, a_rows, row_bytes, C::BM) || !make_code_map(&tb, b_codes, b_rows, row_bytes, BN))
@@ -847,13 +842,9 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   // a D whose base or row stride does not suit TMA stores goes to the one-CTA kernel
   if (C::TMA_D && !make_out_map(&td, p.D, p.M, p.N, p.ldd))
     return launch_gemm_cfg<FMT, 256, RQ>(a_codes, a_rows, b_codes, b_rows, p, num_sms, st);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tn_pair_kernel<FMT, RQ, NS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(gemm_tn_pair_kernel<FMT, RQ, NS>),
+                                          C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   const int64_t row_bytes = FMT ? p.kp / 2 : p.kp;
   CUtensorMap ta, tb, tsa, tsb;
   memset(&tsa, 0, sizeof tsa);

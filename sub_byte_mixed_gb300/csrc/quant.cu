@@ -749,17 +749,33 @@ __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
 }
 
 // ------------------------------------------------------------------ host-side launchers
-// CTAs of 256 threads one SM holds at once for a kernel (occupancy query, cached per kernel).
+// CTAs of 256 threads one SM holds at once for a kernel (occupancy query, cached per kernel and device).
 static int resident_ctas(const void* fn) {
   static std::mutex mu;
-  static std::vector<std::pair<const void*, int>> cache;
+  static std::vector<std::pair<std::pair<const void*, int>, int>> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
   for (const auto& e : cache)
-    if (e.first == fn) return e.second;
+    if (e.first.first == fn && e.first.second == dev) return e.second;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 256, 0) != cudaSuccess || n < 1) n = 1;
-  cache.emplace_back(fn, n);
+  cache.emplace_back(std::make_pair(fn, dev), n);
   return n;
+}
+
+cudaError_t ensure_max_dynamic_smem(const void* fn, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;   // (kernel, device) pairs already raised
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& d : done)
+    if (d.first == fn && d.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.emplace_back(fn, dev);
+  return e;
 }
 
 // A grid-stride (persistent) kernel: as many CTAs as the work asks for, but no more than one wave of

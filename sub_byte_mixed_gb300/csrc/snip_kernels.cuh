@@ -184,6 +184,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn tensor_map_encoder();
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device, once per kernel and
+// device (the attribute is per device; thread-safe).  Defined in quant.cu.
+cudaError_t ensure_max_dynamic_smem(const void* fn, int bytes);
+
 // Self-check of the bounded wait (waitcheck.cu): out = {completed 0, completed 1, ns}.
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, uint32_t* out, cudaStream_t st);
 
