@@ -566,6 +566,10 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
     if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
+      // descriptors of stage 0's A and B tiles: a stage or a k-step only moves the 14-bit start address
+      // (16-byte units; shared memory ends below 256 KB, so the field never carries into the next)
+      const uint64_t adesc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
+      const uint64_t bdesc0 = smem_desc(smem_u32(smem) + C::A_BYTES, 16, 1024, 2);
       for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
         if (!mbar_wait_bounded(tempty(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
         tc_fence_after();
@@ -574,16 +578,16 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
           if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           if (FMT && !mbar_wait_bounded(sfready(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t sB = sA + C::A_BYTES;
+          const uint64_t soff = (uint64_t)((stage * (uint32_t)C::STAGE_BYTES) >> 4);
+          const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
           const uint32_t sf = tmem + C::SF_TMEM_BASE + stage * C::SF_COLS;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t adesc = smem_desc(sA + 32 * k, 16, 1024, 2);
+            const uint64_t adesc = ad + (uint64_t)(2 * k);   // 32 bytes: the next 64 FP4 / 32 FP8 elements
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
 #pragma unroll
             for (int h = 0; h < NS; ++h) {   // sub-tile h accumulates in columns [256 h, 256 h + 256)
-              const uint64_t bdesc = smem_desc(sB + h * C::BNC * C::KB + 32 * k, 16, 1024, 2);
+              const uint64_t bdesc = bd + (uint64_t)(((h * C::BNC * C::KB) >> 4) + 2 * k);
               if (FMT == 1)
                 tc_mma_nvf4_pair(d_tmem, adesc, bdesc, C::IDESC, sf + 4 * k, sf + C::SFA_COLS + k * C::SFB_COLS_K,
                                  accum);
