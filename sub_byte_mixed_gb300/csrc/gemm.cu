@@ -23,7 +23,9 @@
 //   warps 6-13  epilogue: each warp drains 32 accumulator rows x BN/2 columns
 //               from TMEM into registers (two rounds), hands the accumulator
 //               back to the MMA warp, then scales by ga*gb and stores fp32
-//               rows while the next tile's MMAs run.
+//               rows while the next tile's MMAs run.  The CTA-pair kernel's
+//               single-accumulator instantiations store through shared memory
+//               with TMA instead (32 x 16 fp32 boxes, two buffers per warp).
 // Every wait is bounded (globaltimer); on expiry the CTA raises the timeout
 // bit of the status word, lets all roles fall through, drains in-flight
 // tensor-core work and frees its tensor memory before returning.
