@@ -364,7 +364,9 @@ snip_status snip_quantized_bytes(snip_format fmt, snip_layout layout, int64_t ou
  * (scale_vec::4X), MXFP4 the same MMA with E8M0 scales (scale_vec::2X), FP8
  * the E4M3 x E4M3 MMA.  NVFP4_B32/_B64/_B128 operands are NVFP4 operands
  * (their repeated scales give the longer blocks' product exactly).  Accumulation is fp32.  Needs K % 16 == 0 (MXFP4:
- * K % 32 == 0), else SNIP_ERR_SHAPE.
+ * K % 32 == 0) and ldd % 4 == 0, else SNIP_ERR_SHAPE; ldd >= N, else SNIP_ERR_INVALID_ARG.  Only D[m, n] with
+ * m < M, n < N is written (a row pitch's padding is left as it was); M == 0 or N == 0 writes nothing and
+ * returns SNIP_OK.
  * ws: at least SNIP_WS_HEADER_BYTES (status word; a timed-out wait raises
  * SNIP_ERR_TIMEOUT there). */
 snip_status snip_gemm(snip_format fmt, const uint8_t* a_codes, const uint8_t* a_scales, const float* ga,
