@@ -1,6 +1,7 @@
 """Quantized operands at the full block sizes, bit for bit: for every linear of
-the 7B block (T = 8192) and of the 70B block (T = 16384) under the seeded
-mixed plan the bench runs, each of the six quantizations the layer makes --
+the TinyLlama block (T = 4096), the 7B block (T = 8192) and the 70B block
+(T = 16384) under the seeded mixed plan the bench runs (its FP4-FLOP target
+for that block), each of the six quantizations the layer makes --
 X, W (forward, round-to-nearest) and dY (dgrad, stochastic) as row blocks
 through the statistics-fused kernel the bench step uses, W^T, dY^T, X^T
 (stochastic) as column blocks -- with the layer's seed and stream ids, in
@@ -65,6 +66,10 @@ def _check_block(snip, cfg):
             del codes, scales
         del X, W, dY, host, dev
         torch.cuda.empty_cache()
+
+
+def test_tinyllama_block_codes(snip):
+    _check_block(snip, inputs.TINYLLAMA)
 
 
 def test_llama7b_block_codes(snip):
