@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/snip.h: argument checks, workspace
 // layout, the per-layer precision plan and the launch sequence of each call.
-// Every compute step runs in the kernels of quant.cu and gemm.cu.
+// Every compute step runs in the kernels of quant.cu, gemm.cu and dw_noise.cu
+// (plan selection over the statistics is host code, plan_select.cu).
 #include <cmath>
 #include <cstdio>
 #include <cstring>
