@@ -131,8 +131,9 @@ __global__ void __launch_bounds__(DwCfg::THREADS, 1)
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
-        // let copies already in flight land before the CTA leaves (bounded)
+      if (!ok || *abort_flag) {
+        // aborted (here or by another role of this CTA): let copies already in flight land before
+        // the CTA leaves (bounded)
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 2000000ull) {}
       }
