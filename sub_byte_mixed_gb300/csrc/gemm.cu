@@ -396,12 +396,18 @@ __global__ void __launch_bounds__(448, 1)
                                 __fmul_rn(alpha, __uint_as_float(rr[7])));
               } else {
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                  if (col + 4 * h < p.N)
-                    st_global_cs_v4(drow + col + 4 * h, __fmul_rn(alpha, __uint_as_float(rr[4 * h])),
+                for (int h = 0; h < 2; ++h) {
+                  const int64_t c4 = col + 4 * h;
+                  if (c4 + 4 <= p.N) {
+                    st_global_cs_v4(drow + c4, __fmul_rn(alpha, __uint_as_float(rr[4 * h])),
                                     __fmul_rn(alpha, __uint_as_float(rr[4 * h + 1])),
                                     __fmul_rn(alpha, __uint_as_float(rr[4 * h + 2])),
                                     __fmul_rn(alpha, __uint_as_float(rr[4 * h + 3])));
+                  } else {   // the row's last 1-3 columns: nothing past N is written
+                    for (int e = 0; e < 4 && c4 + e < p.N; ++e)
+                      drow[c4 + e] = __fmul_rn(alpha, __uint_as_float(rr[4 * h + e]));
+                  }
+                }
               }
             }
         }
@@ -738,12 +744,18 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
                                 __fmul_rn(alpha, __uint_as_float(rr[7])));
               } else {
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                  if (col + 4 * h < p.N)
-                    st_global_cs_v4(drow + col + 4 * h, __fmul_rn(alpha, __uint_as_float(rr[4 * h])),
+                for (int h = 0; h < 2; ++h) {
+                  const int64_t c4 = col + 4 * h;
+                  if (c4 + 4 <= p.N) {
+                    st_global_cs_v4(drow + c4, __fmul_rn(alpha, __uint_as_float(rr[4 * h])),
                                     __fmul_rn(alpha, __uint_as_float(rr[4 * h + 1])),
                                     __fmul_rn(alpha, __uint_as_float(rr[4 * h + 2])),
                                     __fmul_rn(alpha, __uint_as_float(rr[4 * h + 3])));
+                  } else {   // the row's last 1-3 columns: nothing past N is written
+                    for (int e = 0; e < 4 && c4 + e < p.N; ++e)
+                      drow[c4 + e] = __fmul_rn(alpha, __uint_as_float(rr[4 * h + e]));
+                  }
+                }
               }
             }
         }
