@@ -246,3 +246,42 @@ def test_outlier_sweep_full_size(snip):
             q = snip.quantize_fp8(xd)
             ref = oracle.quantize_fp8(x)
             assert np.array_equal(q.codes.cpu().numpy().reshape(ref.codes.shape), ref.codes)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("layout", [0, 1])
+def test_column_blocks_of_a_very_wide_tensor(snip, layout):
+    """16 rows x 4,194,368 columns quantized with blocks along the rows: over
+    65535 x 64 output rows, which a two-dimensional grid of 64-row tiles could
+    not cover.  NVFP4 (SR) and FP8 (SR); sampled output rows, the last ones
+    included, bit-exact vs the oracle."""
+    R, C = 16, 4194368
+    x = inputs.normal_bf16((R, C), 1.0, 5, 31)
+    xd = x.cuda()
+    rng = np.random.default_rng(3)
+    sel = np.unique(np.concatenate([rng.choice(C, 40, replace=False), np.arange(C - 8, C)]))
+    q = snip.quantize_nvfp4(xd, orient=snip.ALONG_ROWS, rnd=snip.SR, seed=2, stream_id=9, layout=layout)
+    ref = oracle.quantize_nvfp4(x, orient=1, rnd=1, seed=2, stream_id=9, rows=sel)
+    if layout == snip.MMA:
+        _, codes = mma_codes_to_rowmajor(q.codes, C, R)
+        # the chunked scale image at the sampled rows only (the whole gather would need GBs of indices)
+        s_all = q.scales.cpu().numpy()
+        r = sel[:, None].astype(np.int64)
+        kb = np.arange(R // 16)[None, :]
+        ocp = 256
+        off = ((r // 128) * (ocp // 64) + kb // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + kb % 4
+        scales = np.zeros((C, R // 16), dtype=np.uint8)
+        scales[sel] = s_all[off]
+    else:
+        codes = q.codes.cpu().numpy().reshape(C, R // 2)
+        scales = q.scales.cpu().numpy().reshape(C, R // 16)
+    np.testing.assert_array_equal(codes[sel], ref.codes)
+    np.testing.assert_array_equal(scales[sel], ref.scales)
+    assert q.g.item() == ref.g
+    f = snip.quantize_fp8(xd, orient=snip.ALONG_ROWS, rnd=snip.SR, seed=2, stream_id=10, layout=layout)
+    fref = oracle.quantize_fp8(x, orient=1, rnd=1, seed=2, stream_id=10, rows=sel)
+    if layout == snip.MMA:
+        _, fcodes = mma_codes_to_rowmajor(f.codes, C, R, fmt_nvfp4=False)
+    else:
+        fcodes = f.codes.cpu().numpy().reshape(C, R)
+    np.testing.assert_array_equal(fcodes[sel], fref.codes)
