@@ -24,6 +24,7 @@ pytestmark = pytest.mark.gpu
 SEED = 3
 T, K1, N1 = 256, 512, 384        # the later layer (layer 1): X1 T x K1, W1 N1 x K1, dY1 T x N1
 K0 = 320                         # the preceding layer (layer 0): X0 T x K0, W0 K1 x K0, its dY = dX1 (T x K1)
+RAGGED = (272, 400, 208, 336)    # T, K1, N1, K0 off every tile boundary
 
 
 @pytest.fixture(scope="module")
@@ -38,7 +39,9 @@ def _lib_operands(snip, dY0, g):
     return rows, cols
 
 
-def test_chain_equals_unfused_library_path(snip):
+@pytest.mark.parametrize("dims", [(T, K1, N1, K0), RAGGED])
+def test_chain_equals_unfused_library_path(snip, dims):
+    T, K1, N1, K0 = dims
     X1 = inputs.normal_bf16((T, K1), 1.0, 21, 1).cuda()
     W1 = inputs.normal_bf16((N1, K1), 0.02, 21, 2).cuda()
     dY1 = inputs.normal_bf16((T, N1), 1e-3, 21, 3).cuda()

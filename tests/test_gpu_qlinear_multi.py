@@ -33,11 +33,12 @@ def _per_layer(snip, plan, layers, X, Ws):
     return Ys, stats
 
 
-@pytest.mark.parametrize("fmts,sr_layer", [((1, 1, 1), None), ((0, 1, 0), None), ((1, 2, 4, 5), None),
-                                           ((1, 1, 0), 1)])
-def test_multi_forward_equals_per_layer(snip, fmts, sr_layer):
-    T, K = 256, 512
-    Ns = [512, 128, 256, 384][:len(fmts)]
+@pytest.mark.parametrize("fmts,sr_layer,shape", [((1, 1, 1), None, None), ((0, 1, 0), None, None),
+                                                 ((1, 2, 4, 5), None, None), ((1, 1, 0), 1, None),
+                                                 ((1, 0), None, (272, 400, [400, 144]))])
+def test_multi_forward_equals_per_layer(snip, fmts, sr_layer, shape):
+    T, K = (256, 512) if shape is None else shape[:2]   # the last case: ragged T, K and N
+    Ns = [512, 128, 256, 384][:len(fmts)] if shape is None else shape[2]
     X = inputs.normal_bf16((T, K), 1.0, 11, 1).cuda()
     Ws = [inputs.normal_bf16((n, K), 0.02, 11, 10 + i).cuda() for i, n in enumerate(Ns)]
     plan = snip.Plan(list(fmts) + [1], seed=5)          # one more layer that the call does not use
