@@ -180,3 +180,38 @@ def _sampled_block_parity(snip, cfg, plan_fmts, seed=0, nrows=48):
 def test_tinyllama_block_sampled(snip):
     cfg = inputs.TINYLLAMA
     _sampled_block_parity(snip, cfg, inputs.seeded_plan(cfg, cfg.fp4_target, seed=0))
+
+
+@pytest.mark.parametrize("fmt,code", FMTS)
+@pytest.mark.parametrize("shape", [(256, 512, 384), (2048, 512, 2560)])
+def test_qlinear_nonfinite_inputs(snip, fmt, code, shape):
+    """A non-finite element in X (forward) or dY (backward) raises SNIP_ERR_NONFINITE in the
+    workspace status and makes that tensor's statistics NaN; after a reset the same workspace gives
+    exactly the results of a fresh one (one-CTA and CTA-pair GEMM shapes)."""
+    T, K, N = shape
+    X, W, dY = (inputs.normal_bf16(s, sg, 55, i).cuda() for i, (s, sg) in
+                enumerate([((T, K), 1.0), ((N, K), 0.02), ((T, N), 1e-3)]))
+    plan = snip.Plan([code], seed=2)
+    ws = snip.qlinear_workspace(plan, 0, T, K, N)
+    st = torch.zeros((3, snip.STATS_NVALS), dtype=torch.float64, device="cuda")
+    Xbad = X.clone()
+    Xbad[T // 2, K // 3] = float("inf")
+    snip.qlinear_fwd(plan, 0, Xbad, W, ws, stats=st[0:2])
+    assert ws.status() == snip.SNIP_ERR_NONFINITE
+    assert np.isnan(st[0].cpu().numpy()).all()
+    ws.reset()
+    dYbad = dY.clone()
+    dYbad[T - 1, N - 1] = float("nan")
+    snip.qlinear_bwd(plan, 0, X, W, dYbad, ws, stats=st[2])
+    assert ws.status() == snip.SNIP_ERR_NONFINITE
+    assert np.isnan(st[2].cpu().numpy()).all()
+    ws.reset()
+    Y = snip.qlinear_fwd(plan, 0, X, W, ws)
+    dX, dW = snip.qlinear_bwd(plan, 0, X, W, dY, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == snip.SNIP_OK
+    fresh = snip.qlinear_workspace(plan, 0, T, K, N)
+    Y2 = snip.qlinear_fwd(plan, 0, X, W, fresh)
+    dX2, dW2 = snip.qlinear_bwd(plan, 0, X, W, dY, fresh)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y2) and torch.equal(dX, dX2) and torch.equal(dW, dW2)
