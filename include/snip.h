@@ -213,10 +213,11 @@ snip_status snip_amax(const void* x, int64_t n, float* amax_out, void* ws, size_
 snip_status snip_tensor_scales(const void* x, int64_t n, float* scales_out, void* ws, size_t ws_bytes,
                                void* stream);
 
-/* The tensor scales of up to 4 tensors in one launch (as snip_tensor_scales
+/* The tensor scales of up to 8 tensors in one launch (as snip_tensor_scales
  * for each; one launch spreads its CTAs over the tensors in proportion to
  * their sizes).  xs[t] (device bf16, 16-byte aligned) holds ns[t] elements;
- * scales_out[t] (device, 3 floats) receives {amax, g, s}.  count in [1, 4].
+ * scales_out[t] (device, 3 floats) receives {amax, g, s}.  count in [1, 8]
+ * (SNIP_ERR_INVALID_ARG otherwise).
  * ws as for snip_tensor_scales; its status word flags non-finite input. */
 snip_status snip_tensor_scales_multi(int count, const void* const* xs, const int64_t* ns, float* const* scales_out,
                                      void* ws, size_t ws_bytes, void* stream);

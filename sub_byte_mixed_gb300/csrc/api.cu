@@ -21,8 +21,9 @@ namespace {
 constexpr size_t kOffStatus = 0;        // uint32 sticky status bits
 constexpr size_t kOffAmaxCounter = 4;   // uint32, self-resetting
 constexpr size_t kOffStatsCounter = 8;  // uint32, self-resetting
-constexpr size_t kOffMultiCounters = 16; // kMaxMultiScales x uint32, self-resetting
+constexpr size_t kOffMultiCounters = 16; // kMaxMultiScales (8) x uint32, self-resetting
 constexpr size_t kOffScaleSlots = 64;   // 8 slots x 4 floats {amax, NVFP4 g, FP8 s, -} (12 bytes used)
+static_assert(kOffMultiCounters + 4 * kMaxMultiScales <= kOffScaleSlots, "multi-scale counters overlap the scale slots");
 constexpr size_t kOffAmaxPartials = SNIP_WS_HEADER_BYTES;                            // kMaxPartials x uint32
 constexpr size_t kOffStatsPartials = kOffAmaxPartials + 4 * kMaxPartials;            // kMaxPartials x 5 doubles
 constexpr size_t kSmallWorkspace = kOffStatsPartials + 8 * 5 * kMaxPartials;         // 45312

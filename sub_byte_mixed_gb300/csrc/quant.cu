@@ -18,6 +18,7 @@
 // the FMA pipe (grid_rn2 / grid_sr2, snip_device.cuh) with one Philox4x32-10
 // call per 8 source elements; codes come from the hardware E2M1/E4M3/E5M2
 // conversions of the exact grid values.
+#include <algorithm>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -141,23 +142,29 @@ __device__ __forceinline__ uint4 fp8_encode16(const float (&v)[16], float inv, B
     }
   } else if (RND == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float a = __fmul_rn(v[2 * i], inv), b = __fmul_rn(v[2 * i + 1], inv);
-      w[i >> 1] |= (E5 ? e5m2x2_rn_sat(a, b) : e4m3x2_rn_sat(a, b)) << (16 * (i & 1));
-    }
+    for (int j = 0; j < 4; ++j)
+      w[j] = fp8x4_rn_sat<E5>(__fmul_rn(v[4 * j], inv), __fmul_rn(v[4 * j + 1], inv), __fmul_rn(v[4 * j + 2], inv),
+                              __fmul_rn(v[4 * j + 3], inv));
   } else {
-    // stochastic rounding on the FMA pipe (grid_sr2), the code converted from the exact grid value
-    constexpr float kTop = E5 ? 57344.0f : 448.0f, kC = E5 ? 2097152.0f : 1048576.0f;
+    // stochastic rounding on the FMA pipe (grid_sr2), the code converted from the exact grid value.
+    // y is not clamped to the grid's top: past it (the tensor scale's rounding) the grid value is the
+    // top or more and the saturating conversion gives the top either way.
+    constexpr float kC = E5 ? 2097152.0f : 1048576.0f;
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const float2 y = __fmul2_rn(make_float2(fabsf(v[i]), fabsf(v[i + 1])), make_float2(inv, inv));
-      const float2 yc = make_float2(fminf(y.x, kTop), fminf(y.y, kTop));
-      const float2 H = E5 ? make_float2(e5m2_step_x4(yc.x), e5m2_step_x4(yc.y))
-                          : make_float2(e4m3_step_x8(yc.x), e4m3_step_x8(yc.y));
-      const float2 g = E5 ? sr_g2<18>(bits.f23(i), bits.f23(i + 1)) : sr_g2<19>(bits.f23(i), bits.f23(i + 1));
-      const float2 q = grid_sr2(yc, H, g, kC);
-      const float a = copysignf(q.x, v[i]), b = copysignf(q.y, v[i + 1]);
-      w[i >> 2] |= (E5 ? e5m2x2_rn_sat(a, b) : e4m3x2_rn_sat(a, b)) << (16 * ((i >> 1) & 1));
+    for (int j = 0; j < 4; ++j) {
+      float a[4];
+#pragma unroll
+      for (int k = 0; k < 4; k += 2) {
+        const int i = 4 * j + k;
+        const float2 y = __fmul2_rn(make_float2(fabsf(v[i]), fabsf(v[i + 1])), make_float2(inv, inv));
+        const float2 H = E5 ? make_float2(e5m2_step_x4(y.x), e5m2_step_x4(y.y))
+                            : make_float2(e4m3_step_x8(y.x), e4m3_step_x8(y.y));
+        const float2 g = E5 ? sr_g2<18>(bits.f23(i), bits.f23(i + 1)) : sr_g2<19>(bits.f23(i), bits.f23(i + 1));
+        const float2 q = grid_sr2(y, H, g, kC);
+        a[k] = copysignf(q.x, v[i]);
+        a[k + 1] = copysignf(q.y, v[i + 1]);
+      }
+      w[j] = fp8x4_rn_sat<E5>(a[0], a[1], a[2], a[3]);
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
@@ -222,6 +229,7 @@ __device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockS
   float2 S4 = make_float2(0.f, 0.f), b4 = S4, b8 = S4;
   float T4 = 0.f;
   uint32_t cw[4] = {0u, 0u, 0u, 0u};
+  float qa[8];   // signed grid values of the CF format awaiting conversion (one word's worth)
   const float2 inv2 = make_float2(bs.inv, bs.inv), np2 = make_float2(-bs.p, -bs.p);
   const float2 i8 = make_float2(inv8, inv8), ns8 = make_float2(-s8, -s8), m1 = make_float2(-1.0f, -1.0f);
   float2& E4 = BE ? b4 : acc.e4;
@@ -249,7 +257,11 @@ __device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockS
       const float2 yc = make_float2(fminf(y.x, 6.0f), fminf(y.y, 6.0f));
       const float2 H = make_float2(e2m1_step_x2(yc.x), e2m1_step_x2(yc.y));
       const float2 q = RND ? grid_sr2(yc, H, g17, 4194304.0f) : grid_rn2(yc, H, 4194304.0f);
-      if (CF == 1) cw[i >> 3] |= e2m1x2_rn(copysignf(q.x, v[i]), copysignf(q.y, v[i + 1])) << (4 * (i & 7));
+      if (CF == 1) {
+        qa[i & 7] = copysignf(q.x, v[i]);
+        qa[(i & 7) + 1] = copysignf(q.y, v[i + 1]);
+        if ((i & 7) == 6) cw[i >> 3] = e2m1x8_rn(qa);
+      }
       const float2 d = __ffma2_rn(q, np2, va);            // |x| - |x_hat|
       E4 = __ffma2_rn(d, d, E4);
       const float2 c = __ffma2_rn(yc, m1, q);
@@ -270,7 +282,11 @@ __device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockS
       const float2 yc = make_float2(fminf(y.x, 448.0f), fminf(y.y, 448.0f));
       const float2 H = make_float2(e4m3_step_x8(yc.x), e4m3_step_x8(yc.y));
       const float2 q = RND ? grid_sr2(yc, H, g19, 1048576.0f) : grid_rn2(yc, H, 1048576.0f);
-      if (CF == 0) cw[i >> 2] |= e4m3x2_rn_sat(copysignf(q.x, v[i]), copysignf(q.y, v[i + 1])) << (8 * (i & 3));
+      if (CF == 0) {
+        qa[i & 3] = copysignf(q.x, v[i]);
+        qa[(i & 3) + 1] = copysignf(q.y, v[i + 1]);
+        if ((i & 3) == 2) cw[i >> 2] = fp8x4_rn_sat(qa[0], qa[1], qa[2], qa[3]);
+      }
       const float2 d = __ffma2_rn(q, ns8, va);
       E8 = __ffma2_rn(d, d, E8);
       const float2 c = __ffma2_rn(yc, m1, q);
@@ -803,7 +819,8 @@ cudaError_t launch_scales_multi(ScalesMulti m, uint32_t* partials, uint32_t* cou
   // CTAs in proportion to each tensor's size, at least one each, within the partial slots
   int64_t total = 0;
   for (int t = 0; t < m.count; ++t) total += m.n[t];
-  const int64_t want = fill_grid(total >> 3, 256 * 4, 4 * num_sms);
+  // rounding each tensor's share up adds at most one CTA a tensor: stay within the partial slots
+  const int64_t want = fill_grid(total >> 3, 256 * 4, std::min(4 * num_sms, kMaxPartials - kMaxMultiScales));
   int c = 0;
   for (int t = 0; t < m.count; ++t) {
     m.cta0[t] = c;
@@ -820,7 +837,7 @@ cudaError_t launch_scales_multi(ScalesMulti m, uint32_t* partials, uint32_t* cou
 
 cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, float* out3,
                           uint32_t* status, int num_sms, cudaStream_t st) {
-  const int grid = fill_grid(n >> 3, 256 * 4, 4 * num_sms);
+  const int grid = fill_grid(n >> 3, 256 * 4, std::min(4 * num_sms, kMaxPartials));
   scales_kernel<<<grid, 256, 0, st>>>(x, n, partials, counter, out3, status);
   return cudaGetLastError();
 }

@@ -31,18 +31,25 @@ __device__ __forceinline__ uint32_t e4m3_rn_sat(float t) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(t), "f"(t));
   return r & 0xffu;
 }
-// Two signed values at once: low byte <- lo, high byte <- hi (sign kept).
-__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+// Four signed values -> one word of E4M3 (E5 false) or E5M2 codes, value k in
+// byte k, nearest even, saturating (E5M2: 1 sign, 5 exponent bits with bias 15,
+// 2 mantissa bits; largest finite 57344, code 0x7b).
+template <bool E5 = false>
+__device__ __forceinline__ uint32_t fp8x4_rn_sat(float a0, float a1, float a2, float a3) {
+  uint32_t r;
+  if (E5)
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 h0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 h1, %4, %3;\n\t"
+        "mov.b32 %0, {h0, h1};\n\t}"
+        : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  else
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
+        "mov.b32 %0, {h0, h1};\n\t}"
+        : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
   return r;
-}
-// Two E4M3 codes (low byte first) -> their values (exact in f16, then f32).
-__device__ __forceinline__ float2 e4m3x2_decode(uint32_t two_codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_codes));
-  __half2 h = *reinterpret_cast<__half2*>(&h2);
-  return __half22float2(h);
 }
 
 // Value of a non-negative E4M3 code (0..0x7e): 2^(e-7)(1+m/8), or m 2^-9.
@@ -51,20 +58,20 @@ __device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
   return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
 }
 
-// ------------------------------------------------------------------ E5M2
-// 1 sign, 5 exponent (bias 15), 2 mantissa bits; largest finite 57344 (0x7b).
-__device__ __forceinline__ uint32_t e5m2x2_rn_sat(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 // ------------------------------------------------------------------ E2M1
-// Round-to-nearest-even of two signed values to E2M1 (saturating at +-6),
-// hardware cvt: returns one byte, lo in bits 0..3 and hi in bits 4..7.
-__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+// Eight signed values -> one word of E2M1 codes, value k in nibble k: round to
+// nearest even, saturating at +-6 (hardware cvt, two values a byte, the first
+// in the low nibble), the four bytes joined by one vector move.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float (&a)[8]) {
   uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r) : "f"(hi), "f"(lo));
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(a[0]), "f"(a[1]), "f"(a[2]), "f"(a[3]), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7]));
   return r;
 }
 // Two E2M1 codes (one byte, low nibble first) -> their values.
@@ -75,10 +82,6 @@ __device__ __forceinline__ float2 e2m1x2_decode(uint32_t byte) {
   return __half22float2(h);
 }
 
-// Value of an E2M1 magnitude code 0..7.
-__device__ __forceinline__ float e2m1_value(uint32_t m) {
-  return m <= 4u ? __fmul_rn((float)m, 0.5f) : (m == 5u ? 3.0f : (m == 6u ? 4.0f : 6.0f));
-}
 
 // ------------------------------------------------------------------ grid rounding on the FMA pipe
 // The E2M1, E4M3 and E5M2 grids have a power-of-two step h at every y >= 0
@@ -94,9 +97,12 @@ __device__ __forceinline__ float e2m1_value(uint32_t m) {
 //    u < floor(frac 2^16): the 16-bit rule.  Rounding toward zero never moves
 //    a sum across a grid value (grid values are fp32 numbers), so the
 //    comparison is exact.
-// Both return the grid value itself (as fp32), and they run on the FMA pipe;
-// the integer forms above use the slower integer pipe.  H is a fixed
-// multiple of h per grid (the *_step_x* helpers) and k = 2^23 h / H.
+// Both return the grid value itself (as fp32), and they run on the FMA pipe,
+// where integer carry forms of the same rules would use the slower ALU pipe.
+// H is a fixed multiple of h per grid (the *_step_x* helpers) and
+// k = 2^23 h / H.  A pass that needs only the code may leave y unclamped: past
+// the top, h is the step of y's own binade and q a multiple of it no smaller
+// than the top, which the saturating conversion maps to the top code.
 __device__ __forceinline__ float2 grid_rn2(float2 yc, float2 H, float k) {
   const float2 C = __fmul2_rn(H, make_float2(k, k));
   return __ffma2_rn(C, make_float2(-1.0f, -1.0f), __fadd2_rn(yc, C));   // exact: the sum is C plus a multiple of h
@@ -137,15 +143,20 @@ __device__ __forceinline__ float e5m2_step_x4(float y) {
 // (SC'11): ten rounds of two 32x32->64-bit products on a 4-word counter, the
 // 2-word key bumped by the Weyl constants between rounds.
 struct U4 { uint32_t x, y, z, w; };
+// The 64-bit product of two words as its low and high words, one wide multiply.
+__device__ __forceinline__ void mul_wide_u32(uint32_t a, uint32_t b, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b64 t;\n\tmul.wide.u32 t, %2, %3;\n\tmov.b64 {%0, %1}, t;\n\t}" : "=r"(lo), "=r"(hi) : "r"(a), "r"(b));
+}
 
 __device__ __forceinline__ U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
                                             uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
-    uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-    uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    uint32_t lo0, hi0, lo1, hi1;
+    mul_wide_u32(0xD2511F53u, c0, lo0, hi0);
+    mul_wide_u32(0xCD9E8D57u, c2, lo1, hi1);
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
     c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
   }
   return U4{c0, c1, c2, c3};
@@ -170,8 +181,9 @@ __host__ __device__ inline PhiloxKey philox_round_keys(uint64_t seed) {
 __device__ __forceinline__ U4 philox4x32_10_rk(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, const PhiloxKey& rk) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    uint32_t lo0, hi0, lo1, hi1;
+    mul_wide_u32(0xD2511F53u, c0, lo0, hi0);
+    mul_wide_u32(0xCD9E8D57u, c2, lo1, hi1);
     const uint32_t n0 = hi1 ^ c1 ^ rk.k[r], n2 = hi0 ^ c3 ^ rk.k[10 + r];
     c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
   }
@@ -188,10 +200,6 @@ __device__ __forceinline__ U4 sr_words_rk(uint64_t group, uint64_t stream_id, co
 __device__ __forceinline__ U4 sr_words(uint64_t group, uint64_t seed, uint64_t stream_id) {
   return philox4x32_10((uint32_t)group, (uint32_t)(group >> 32), (uint32_t)stream_id,
                        (uint32_t)(stream_id >> 32), (uint32_t)seed, (uint32_t)(seed >> 32));
-}
-__device__ __forceinline__ uint32_t sr_half(const U4& w, int i) {
-  uint32_t v = (i >> 1) == 0 ? w.x : (i >> 1) == 1 ? w.y : (i >> 1) == 2 ? w.z : w.w;
-  return (i & 1) ? (v >> 16) : (v & 0xffffu);
 }
 
 // ------------------------------------------------------------------ misc

@@ -151,7 +151,7 @@ __device__ __forceinline__ void block_sum_f64(double (&v)[N]) {
 cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, float* out3,
                           uint32_t* status, int num_sms, cudaStream_t st);
 // Up to kMaxMultiScales tensors' scales in one launch (cta0 filled by the launcher).
-constexpr int kMaxMultiScales = 4;
+constexpr int kMaxMultiScales = 8;
 struct ScalesMulti {
   const uint16_t* x[kMaxMultiScales];
   int64_t n[kMaxMultiScales];

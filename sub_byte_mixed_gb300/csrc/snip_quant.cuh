@@ -136,17 +136,29 @@ __device__ __forceinline__ uint2 nvfp4_encode16(const float (&v)[16], const Bloc
     }
   } else if (RND == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      w[i >> 2] |= e2m1x2_rn(__fmul_rn(v[2 * i], bs.inv), __fmul_rn(v[2 * i + 1], bs.inv)) << (8 * (i & 3));
-  } else {
-    // stochastic rounding on the FMA pipe (grid_sr2), the code converted from the exact grid value
+    for (int h = 0; h < 2; ++h) {
+      float a[8];
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const float2 y = __fmul2_rn(make_float2(fabsf(v[i]), fabsf(v[i + 1])), make_float2(bs.inv, bs.inv));
-      const float2 yc = make_float2(fminf(y.x, 6.0f), fminf(y.y, 6.0f));
-      const float2 H = make_float2(e2m1_step_x2(yc.x), e2m1_step_x2(yc.y));
-      const float2 q = grid_sr2(yc, H, sr_g2<17>(bits.f23(i), bits.f23(i + 1)), 4194304.0f);
-      w[i >> 3] |= e2m1x2_rn(copysignf(q.x, v[i]), copysignf(q.y, v[i + 1])) << (4 * (i & 7));
+      for (int k = 0; k < 8; ++k) a[k] = __fmul_rn(v[8 * h + k], bs.inv);
+      w[h] = e2m1x8_rn(a);
+    }
+  } else {
+    // stochastic rounding on the FMA pipe (grid_sr2), the code converted from the exact grid value.
+    // y is not clamped to the grid's top: above 6 (a block scale rounded down) the grid value is
+    // 6 or more and the saturating conversion gives 6 either way.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float a[8];
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        const int i = 8 * h + k;
+        const float2 y = __fmul2_rn(make_float2(fabsf(v[i]), fabsf(v[i + 1])), make_float2(bs.inv, bs.inv));
+        const float2 H = make_float2(e2m1_step_x2(y.x), e2m1_step_x2(y.y));
+        const float2 q = grid_sr2(y, H, sr_g2<17>(bits.f23(i), bits.f23(i + 1)), 4194304.0f);
+        a[k] = copysignf(q.x, v[i]);
+        a[k + 1] = copysignf(q.y, v[i + 1]);
+      }
+      w[h] = e2m1x8_rn(a);
     }
   }
   return make_uint2(w[0], w[1]);

@@ -2,6 +2,8 @@
 the oracle: bit-exact codes, scales and tensor scales on identical seeded
 inputs, for round-to-nearest and stochastic rounding, in both output layouts,
 at sizes that span several tiles with ragged tails, plus edge cases."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -67,6 +69,31 @@ def test_tensor_scales_multi(snip):
     assert np.isnan(outs2[1].cpu().numpy()).all()
     assert outs2[0].cpu().numpy()[0] == float(xs[3].float().abs().max())
     assert outs2[2].cpu().numpy()[0] == float(xs[2].float().abs().max())
+
+
+def test_tensor_scales_multi_eight_tensors(snip):
+    """The most tensors one launch takes (8: two linears' X, W and dY, one X shared), sizes from a
+    few elements to a few million, each with the scales of its own pass; 0 or 9 tensors are
+    SNIP_ERR_INVALID_ARG before anything is read."""
+    shapes = [(5, 16), (4096, 1024), (1, 8), (2048, 2048), (257, 96), (3000, 1000), (64, 128), (1024, 4096)]
+    xs = [_x(sh, tid=40 + i).cuda() for i, sh in enumerate(shapes)]
+    outs = [torch.full((3,), -1.0, device="cuda") for _ in xs]
+    ws = snip.Workspace(snip.snip_quantize_workspace_size(0, 0))
+    snip.tensor_scales_multi(xs, outs, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == snip.SNIP_OK
+    for x, o in zip(xs, outs):
+        m = float(x.float().abs().max())
+        sc = o.cpu().numpy()
+        assert sc[0] == m and sc[1] == oracle.nvfp4_global_scale(m) and sc[2] == oracle.fp8_tensor_scale(m)
+    L = snip.load()
+    n = 9
+    ptrs = (ctypes.c_void_p * n)(*([xs[0].data_ptr()] * n))
+    ns = (ctypes.c_int64 * n)(*([xs[0].numel()] * n))
+    op = (ctypes.c_void_p * n)(*([outs[0].data_ptr()] * n))
+    st = torch.cuda.current_stream().cuda_stream
+    for count in (0, 9):
+        assert L.snip_tensor_scales_multi(count, ptrs, ns, op, ws.ptr, ws.nbytes, st) == snip.SNIP_ERR_INVALID_ARG
 
 
 def test_precomputed_scales_match(snip):
