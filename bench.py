@@ -66,6 +66,11 @@ def parse_args(argv=None):
                          "block's shapes (builds cublaslt_gemm.cu), one JSON line")
     ap.add_argument("--profile-run", action="store_true",
                     help="exactly --warmup untimed steps, no clock settle, e2e or CPU baseline (for ncu)")
+    ap.add_argument("--scales-per-launch", type=int, default=3,
+                    help="most tensors whose scales one launch computes (3 or less: one launch per linear, "
+                         "the default; packing several linears into one launch measured slower)")
+    ap.add_argument("--order", default="",
+                    help="comma-separated order in which the step runs its linears (default: the model's)")
     ap.add_argument("--layers", default="", help="comma-separated subset of Q,K,V,O,Gate,Up,Down (profiling)")
     ap.add_argument("--next4-only", action="store_true",
                     help="only the dW-level check (bf16 GEMM with fused norms) at the 7B Down shape, one JSON line")
@@ -92,6 +97,10 @@ def workload(args):
     return cfg, plan
 
 
+def linear_order(args):
+    return [n for n in args.order.split(",") if n] or None
+
+
 def config_json(cfg, plan, args):
     from sub_byte_mixed_gb300 import inputs
     return {
@@ -106,7 +115,11 @@ def config_json(cfg, plan, args):
         "schedule": ("one stream" if args.no_overlap else
                      "quantizations and GEMMs on two streams: a linear's quantizations run beside the previous "
                      "linear's GEMMs (events order every GEMM after its operands)")
-                    + ("; the step captured once as a CUDA graph and replayed" if not args.no_graph else ""),
+                    + ("; the step captured once as a CUDA graph and replayed" if not args.no_graph else "")
+                    + (f"; tensor scales of whole linears packed into launches of up to {args.scales_per_launch} "
+                       "tensors (the first linear's alone)" if args.scales_per_launch > 3
+                       else "; one tensor-scale launch per linear")
+                    + (f"; linears run in the order {args.order}" if args.order else ""),
         "plan_source": ("SNIP selection from one step's statistics (snip_plan_select, FP4-FLOP target "
                         f"{cfg.fp4_target})") if args.plan == "snip" else
                        ("seeded plan at the FP4-FLOP target" if args.plan == "mix" else "uniform"),
@@ -336,7 +349,7 @@ class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
     def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True, own_stream=False,
-                 share_x=True):
+                 share_x=True, scales_per_launch=3, order=None):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
@@ -382,6 +395,17 @@ class Step:
         # every sharer's forward GEMM.  The per-linear column-block (stochastic, own stream id)
         # quantizations of X are unchanged.
         active = [j for j, l in enumerate(cfg.linears) if not layers or l.name in layers]
+        # the linears are independent here, so the step may run them in any order (order: their
+        # names, first to last); buffer sets and stream waits go by position in that order, the
+        # random streams and outputs by linear
+        if order:
+            rank = {n: i for i, n in enumerate(order)}
+            missing = [cfg.linears[j].name for j in active if cfg.linears[j].name not in rank]
+            if missing:
+                raise ValueError(f"order leaves out {missing}")
+            active.sort(key=lambda j: rank[cfg.linears[j].name])
+        pos_of = {j: p for p, j in enumerate(active)}
+        self.order = [cfg.linears[j].name for j in active]
         users = {}
         for j in active:
             users.setdefault(cfg.linears[j].x_id, []).append(j)
@@ -389,12 +413,37 @@ class Step:
         shared_ids = {k for k, v in users.items() if len(v) > 1} if share_x else set()
         self.first_user = {k: v[0] for k, v in users.items()}
         xq_owner = {}       # (x_id, format) -> (codes, scales) holding that row-block quantization
-        xbuf = {}           # format -> (codes, scales, last user of its current content)
+        xbuf = {}           # (activation, format) -> (codes, scales, position of its last user)
+        # The tensor-scale passes: the first linear's alone (the first GEMM waits for it), then whole
+        # linears packed in order into launches of at most scales_per_launch tensors (one launch per
+        # linear when that is below 3).  An activation shared by several linears is read once, by
+        # its first user.
+        scale_items = {}
         for j in active:
+            l = cfg.linears[j]
+            src = {l.x_id: self.inp.X[l.x_id], "W": self.inp.W[j], "dY": self.inp.dY[j]}
+            slot = {l.x_id: 0, "W": 1, "dY": 2}
+            sharer = l.x_id in shared_ids and self.first_user[l.x_id] != j
+            names = ("W", "dY") if sharer else (l.x_id, "W", "dY")
+            scale_items[j] = [(src[nm], self.sc[j, slot[nm]].data_ptr()) for nm in names]
+        scale_groups, cur_g = [], []
+        for j in active:
+            fits = sum(len(scale_items[i]) for i in cur_g) + len(scale_items[j]) <= max(scales_per_launch, 3)
+            if cur_g and (not fits or cur_g[0] == active[0]):
+                scale_groups.append(cur_g)
+                cur_g = []
+            cur_g.append(j)
+        if cur_g:
+            scale_groups.append(cur_g)
+        group_of = {g[0]: g for g in scale_groups}
+        self.scale_launches = len(scale_groups)
+        self.wait_at = {}   # call index -> linear whose operand buffers that call (its first quantization) writes
+        for j in active:
+            p = pos_of[j]
             l, f = cfg.linears[j], plan[j]
             X = self.inp.X[l.x_id]
             W, dY = self.inp.W[j], self.inp.dY[j]
-            self.codes, self.scales = codes_sets[j % nsets], scales_sets[j % nsets]
+            self.codes, self.scales = codes_sets[p % nsets], scales_sets[p % nsets]
             src = {l.x_id: X, "W": W, "dY": dY}
             scp = {l.x_id: self.sc[j, 0].data_ptr(), "W": self.sc[j, 1].data_ptr(), "dY": self.sc[j, 2].data_ptr()}
             sid = 8 * j
@@ -408,14 +457,16 @@ class Step:
             sharer = shared and self.first_user[l.x_id] != j
             if sharer:   # X's tensor scales are the first user's
                 scp[l.x_id] = self.sc[self.first_user[l.x_id], 0].data_ptr()
-            # the tensors' scales in one launch (X's only for its first user)
-            names = ("W", "dY") if sharer else (l.x_id, "W", "dY")
-            xs = (ctypes.c_void_p * len(names))(*[src[nm].data_ptr() for nm in names])
-            ns = (ctypes.c_int64 * len(names))(*[src[nm].numel() for nm in names])
-            outs = (ctypes.c_void_p * len(names))(*[scp[nm] for nm in names])
-            self._keep.append((xs, ns, outs))
-            calls.append((L.snip_tensor_scales_multi, (len(names), xs, ns, outs, ws, wsb, stream), "scales",
-                          SCALES_BYTES_PER_ELEM * sum(src[nm].numel() for nm in names), "q", j, -1))
+            # the scales of this linear's group of linears in one launch
+            if j in group_of:
+                items = [it for i in group_of[j] for it in scale_items[i]]
+                xs = (ctypes.c_void_p * len(items))(*[t.data_ptr() for t, _ in items])
+                ns = (ctypes.c_int64 * len(items))(*[t.numel() for t, _ in items])
+                outs = (ctypes.c_void_p * len(items))(*[o for _, o in items])
+                self._keep.append((xs, ns, outs))
+                calls.append((L.snip_tensor_scales_multi, (len(items), xs, ns, outs, ws, wsb, stream), "scales",
+                              SCALES_BYTES_PER_ELEM * sum(t.numel() for t, _ in items), "q", p, -1))
+            self.wait_at[len(calls)] = p
             xcodes = xscales = None      # forward operand of X when it comes from the shared buffers
             for r, (name, orient, orr, occ) in enumerate(roles(l)):
                 t = src[name]
@@ -427,26 +478,26 @@ class Step:
                         xcodes, xscales = xq_owner[key]
                         continue
                     c, sbytes = snip.snip_quantized_bytes(f, snip.MMA, orr, occ)
-                    if f not in xbuf or xbuf[f][0].numel() < c:
-                        xbuf[f] = (torch.empty(c, dtype=torch.uint8, device=device),
-                                   torch.empty(max(sbytes, 16), dtype=torch.uint8, device=device), None)
-                    xc, xsb, last = xbuf[f]
-                    # the buffer's previous content is read by earlier forward GEMMs; this linear's
-                    # quantizations wait for linear j-2's GEMMs, which must cover them
-                    if last is not None and last > j - 2:
+                    if key not in xbuf:
+                        xbuf[key] = (torch.empty(c, dtype=torch.uint8, device=device),
+                                     torch.empty(max(sbytes, 16), dtype=torch.uint8, device=device), None)
+                    xc, xsb, last = xbuf[key]
+                    # a previous content of the buffer is read by earlier forward GEMMs; this linear's
+                    # quantizations wait for the GEMMs two positions back, which must cover them
+                    if last is not None and last > p - 2:
                         raise RuntimeError("shared activations too close together for the two-set schedule")
-                    xbuf[f] = (xc, xsb, max(users[l.x_id]))
+                    xbuf[key] = (xc, xsb, max(pos_of[u] for u in users[l.x_id]))
                     xq_owner[key] = (xc, xsb)
                     xcodes, xscales = xc, xsb
                     dst_c, dst_s = xc.data_ptr(), xsb.data_ptr()
                     if stats and not sharer:
                         args = (f, t.data_ptr(), rows, cols, rnd[r], 0, sid + r, scp[name], snip.MMA, dst_c,
                                 dst_s if f != snip.FP8 else None, self.raw[j, 0].data_ptr(), ws, wsb, stream)
-                        calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", j, -1))
+                        calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", p, -1))
                     else:
                         args = self._plain_quant(L, f, block, t, rows, cols, orient, rnd[r], sid + r, g, dst_c, dst_s,
                                                  ws, wsb, stream)
-                        calls.append((args[0], args[1], qcat, bpe * t.numel(), "q", j, -1))
+                        calls.append((args[0], args[1], qcat, bpe * t.numel(), "q", p, -1))
                     continue
                 if r in (0, 1, 2) and stats:
                     # row-block quantization with SNIP's statistics of the same tensor in one pass
@@ -454,23 +505,23 @@ class Step:
                     args = (f, t.data_ptr(), rows, cols, rnd[r], 0, sid + r, scp[name], snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr() if f != snip.FP8 else None,
                             self.raw[j, k].data_ptr(), ws, wsb, stream)
-                    calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", j, -1))
+                    calls.append((L.snip_quantize_stats, args, "quant_stats", (bpe + 0.0) * t.numel(), "q", p, -1))
                 elif block > 16:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, block, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, ws, wsb, stream)
-                    calls.append((L.snip_quantize_nvfp4_block, args, qcat, bpe * t.numel(), "q", j, -1))
+                    calls.append((L.snip_quantize_nvfp4_block, args, qcat, bpe * t.numel(), "q", p, -1))
                 elif f == snip.NVFP4:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), g, None, ws, wsb, stream)
-                    calls.append((L.snip_quantize_nvfp4, args, qcat, bpe * t.numel(), "q", j, -1))
+                    calls.append((L.snip_quantize_nvfp4, args, qcat, bpe * t.numel(), "q", p, -1))
                 elif f == snip.MXFP4:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, snip.MMA,
                             self.codes[r].data_ptr(), self.scales[r].data_ptr(), ws, wsb, stream)
-                    calls.append((L.snip_quantize_mxfp4, args, qcat, bpe * t.numel(), "q", j, -1))
+                    calls.append((L.snip_quantize_mxfp4, args, qcat, bpe * t.numel(), "q", p, -1))
                 else:
                     args = (t.data_ptr(), rows, cols, orient, rnd[r], 0, sid + r, g, snip.MMA,
                             self.codes[r].data_ptr(), g, ws, wsb, stream)
-                    calls.append((L.snip_quantize_fp8, args, qcat, bpe * t.numel(), "q", j, -1))
+                    calls.append((L.snip_quantize_fp8, args, qcat, bpe * t.numel(), "q", p, -1))
                 if r in (1, 3, 5):   # both operands of a GEMM are ready
                     a, b = r - 1, r
                     M, N, K = {1: (T, l.N, l.K), 3: (T, l.K, l.N), 5: (l.N, l.K, T)}[r]
@@ -485,7 +536,7 @@ class Step:
                     gw = self.gemm_ws
                     args = (f, ac.data_ptr(), sa, ga, self.codes[b].data_ptr(), sb, gb, M, N, K,
                             D.data_ptr(), D.stride(0), gw.ptr, gw.nbytes, gstream)
-                    calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K, "g", j, r // 2))
+                    calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K, "g", p, r // 2))
         self.calls = calls
         # the same calls with every launch on the quantization stream (kernels one after another)
         self.serial_args = [a if k == "q" else a[:-1] + (stream,) for (_, a, _, _, k, _, _) in calls]
@@ -519,8 +570,9 @@ class Step:
 
     def run(self, events=None, serial=False):
         """One step.  With overlap, a GEMM waits for its two operands' quantizations, and the
-        quantizations of linear j wait until linear j-2's GEMMs (the last readers of the same
-        operand buffers) are done; the step ends on the quantization stream after all GEMMs.
+        quantizations of the linear at position p wait until the GEMMs of the linear at p-2 (the
+        last readers of the same operand buffers) are done; the step ends on the quantization
+        stream after all GEMMs.
         serial: every kernel on the quantization stream, one after another (per-kernel timing)."""
         import torch
         ready, gdone = {}, {}
@@ -531,15 +583,15 @@ class Step:
             ev = torch.cuda.Event()
             ev.record(cur)
             self.sQ.wait_event(ev)
-        for i, (fn, args, _, _, kind, j, gi) in enumerate(self.calls):
+        for i, (fn, args, _, _, kind, p, gi) in enumerate(self.calls):
             if serial:
                 args = self.serial_args[i]
             stream = self.sQ if kind == "q" or serial else self.sG
             if overlap:
-                if kind == "q" and gi < 0 and (j - 2) in gdone and fn.__name__ == "snip_tensor_scales_multi":
-                    self.sQ.wait_event(gdone[j - 2])
+                if i in self.wait_at and (p - 2) in gdone:
+                    self.sQ.wait_event(gdone[p - 2])
                 if kind == "g":
-                    self.sG.wait_event(ready[(j, gi)])
+                    self.sG.wait_event(ready[(p, gi)])
             if events is not None:
                 events[i][0].record(stream)
             st = fn(*args)
@@ -556,7 +608,7 @@ class Step:
                 if kind == "g":
                     ev = torch.cuda.Event()
                     ev.record(self.sG)
-                    gdone[j] = ev
+                    gdone[p] = ev
                     last_g = ev
         if overlap and last_g is not None:
             self.sQ.wait_event(last_g)
@@ -938,7 +990,8 @@ def run_ours(args, rank, world, local_rank):
     cfg, plan = workload(args)
     layers = [x for x in args.layers.split(",") if x]
     graph = not args.no_graph
-    step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph)
+    step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph,
+                scales_per_launch=args.scales_per_launch, order=linear_order(args))
     if args.plan == "snip" and layers:
         raise SystemExit("--plan snip selects formats for the whole block; it cannot be combined with --layers")
     if args.plan == "snip":
@@ -949,7 +1002,8 @@ def run_ours(args, rank, world, local_rank):
         flops = [6.0 * cfg.T * l.K * l.N for l in cfg.linears]
         plan, _, _ = snip.snip_plan_select(flops, c8, c4, cfg.fp4_target)
         del step
-        step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph)
+        step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph,
+                scales_per_launch=args.scales_per_launch, order=linear_order(args))
     torch.cuda.synchronize()
     ncalls = len(step.calls)
     sampler = ClockSampler(local_rank) if rank == 0 and not args.profile_run else None
@@ -1015,7 +1069,8 @@ def run_ours(args, rank, world, local_rank):
 
     def time_variant(plan_v, stats_v):
         """Another step of the same block, timed as the headline (K steps after 3 warm-up steps)."""
-        sv = Step(cfg, plan_v, snip, "cuda", layers, overlap=not args.no_overlap, stats=stats_v, own_stream=graph)
+        sv = Step(cfg, plan_v, snip, "cuda", layers, overlap=not args.no_overlap, stats=stats_v, own_stream=graph,
+                  scales_per_launch=args.scales_per_launch, order=linear_order(args))
         for _ in range(3):
             sv.run()
         if graph:

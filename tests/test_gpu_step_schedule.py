@@ -5,8 +5,10 @@ on one stream: Y, dX, dW and the statistics of every linear
 must be identical, so no GEMM reads an operand before its quantization has
 written it or after the next user of its buffer set has overwritten it.  The
 step that computes a shared activation's scales, statistics and forward
-quantization once (Q/K/V, Gate/Up) gives exactly the results of the step that
-recomputes them for every linear."""
+quantization once (Q/K/V, Gate/Up), with the tensor scales of several linears
+in one launch, gives exactly the results of the step that recomputes them for
+every linear with one tensor-scale launch per linear, and so does the step that
+runs the linears in another order."""
 import os
 import sys
 
@@ -28,7 +30,8 @@ def test_two_stream_step_matches_one_stream(plan_kind):
     cfg = inputs.TINYLLAMA
     plan = (inputs.seeded_plan(cfg, cfg.fp4_target, seed=0) if plan_kind == "mix"
             else inputs.all_plan(bench.FORMAT_OF_NAME[plan_kind]))
-    unshared = bench.Step(cfg, plan, snip, "cuda", overlap=False, share_x=False)
+    unshared = bench.Step(cfg, plan, snip, "cuda", overlap=False, share_x=False, scales_per_launch=3)
+    assert unshared.scale_launches == len(cfg.linears)
     unshared.run()
     torch.cuda.synchronize()
     assert unshared.status() == snip.SNIP_OK
@@ -36,7 +39,8 @@ def test_two_stream_step_matches_one_stream(plan_kind):
             unshared.stats_host())
     assert unshared.launches_per_step > 0
     del unshared
-    serial = bench.Step(cfg, plan, snip, "cuda", overlap=False)
+    serial = bench.Step(cfg, plan, snip, "cuda", overlap=False, scales_per_launch=8)
+    assert serial.scale_launches == 3   # Q alone; K, V, O (7 tensors); Gate, Up, Down (8)
     serial.run()
     torch.cuda.synchronize()
     assert serial.status() == snip.SNIP_OK
@@ -58,6 +62,19 @@ def test_two_stream_step_matches_one_stream(plan_kind):
         assert torch.equal(over.dW[j], ref[2][j]), ("dW", j)
     assert torch.equal(over.raw, ref[3])
     del over
+    # the linears in another order (the shared activations' users no longer adjacent)
+    order = ["Q", "Gate", "Up", "Down", "K", "V", "O"]
+    moved = bench.Step(cfg, plan, snip, "cuda", overlap=True, order=order)
+    assert moved.order == order
+    for _ in range(2):
+        moved.run()
+    torch.cuda.synchronize()
+    assert moved.status() == snip.SNIP_OK
+    for j in range(len(cfg.linears)):
+        assert torch.equal(moved.Y[j], ref[0][j]) and torch.equal(moved.dX[j], ref[1][j]), ("order", j)
+        assert torch.equal(moved.dW[j], ref[2][j]), ("order", j)
+    assert torch.equal(moved.raw, ref[3])
+    del moved
     # the same two-stream step captured once as a CUDA graph and replayed
     graph = bench.Step(cfg, plan, snip, "cuda", overlap=True, own_stream=True)
     graph.run()
