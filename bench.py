@@ -69,6 +69,9 @@ def parse_args(argv=None):
     ap.add_argument("--scales-per-launch", type=int, default=3,
                     help="most tensors whose scales one launch computes (3 or less: one launch per linear, "
                          "the default; packing several linears into one launch measured slower)")
+    ap.add_argument("--gemm-streams", type=int, default=3, choices=[1, 2, 3],
+                    help="GEMM streams of the overlapped step: 1; 2, linears alternating; 3 (default), one per "
+                         "GEMM kind")
     ap.add_argument("--order", default="",
                     help="comma-separated order in which the step runs its linears (default: the model's)")
     ap.add_argument("--layers", default="", help="comma-separated subset of Q,K,V,O,Gate,Up,Down (profiling)")
@@ -113,13 +116,16 @@ def config_json(cfg, plan, args):
         "rounding": "RTN forward, SR (Philox4x32-10, 16 bits/elem) backward",
         "stats": "SNIP statistics of X, W (forward rounding) and dY (dgrad rounding) fused into their row-block quantizations",
         "schedule": ("one stream" if args.no_overlap else
-                     "quantizations and GEMMs on two streams: a linear's quantizations run beside the previous "
-                     "linear's GEMMs (events order every GEMM after its operands)")
+                     "quantizations on one stream, GEMMs on others: a linear's quantizations run beside the "
+                     "previous linear's GEMMs (events order every GEMM after its operands)")
                     + ("; the step captured once as a CUDA graph and replayed" if not args.no_graph else "")
                     + (f"; tensor scales of whole linears packed into launches of up to {args.scales_per_launch} "
                        "tensors (the first linear's alone)" if args.scales_per_launch > 3
                        else "; one tensor-scale launch per linear")
-                    + (f"; linears run in the order {args.order}" if args.order else ""),
+                    + (f"; linears run in the order {args.order}" if args.order else "")
+                    + ("" if args.no_overlap else
+                       f"; GEMMs on {args.gemm_streams} stream{'s' if args.gemm_streams > 1 else ''}"
+                       + (" (forward, dgrad, wgrad each on its own)" if args.gemm_streams == 3 else "")),
         "plan_source": ("SNIP selection from one step's statistics (snip_plan_select, FP4-FLOP target "
                         f"{cfg.fp4_target})") if args.plan == "snip" else
                        ("seeded plan at the FP4-FLOP target" if args.plan == "mix" else "uniform"),
@@ -349,7 +355,7 @@ class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
     def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True, own_stream=False,
-                 share_x=True, scales_per_launch=3, order=None):
+                 share_x=True, scales_per_launch=3, order=None, gemm_streams=3):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
@@ -359,7 +365,11 @@ class Step:
         # own_stream: the quantization stream is a stream of its own (a graph cannot be captured on
         # the default stream); run() then joins the caller's stream at both ends
         self.sQ = torch.cuda.Stream() if own_stream else torch.cuda.current_stream()
-        self.sG = torch.cuda.Stream() if overlap else self.sQ
+        # gemm_streams: 1, one GEMM stream; 2, the linears' GEMMs alternate between two streams; 3, the
+        # forward, dgrad and wgrad GEMMs each on a stream of their own (a GEMM's last wave can then
+        # overlap the next GEMM, which reads other operands and writes another output)
+        self.gemm_streams = gemm_streams if overlap else 1
+        self.sGs = [torch.cuda.Stream() for _ in range(self.gemm_streams)] if overlap else [self.sQ]
         self.graph = None
         nsets = 2 if overlap else 1
         L = snip.load()
@@ -384,10 +394,11 @@ class Step:
         codes_sets = [[torch.empty(c, dtype=torch.uint8, device=device) for c in csz] for _ in range(nsets)]
         scales_sets = [[torch.empty(max(s, 16), dtype=torch.uint8, device=device) for s in ssz] for _ in range(nsets)]
         ws, wsb, stream = self.ws.ptr, self.ws.nbytes, self.sQ.cuda_stream
-        gstream = self.sG.cuda_stream
         self.stream = stream
-        calls = []   # (fn, args, category, units, stream kind 'q'/'g', linear, GEMM index or -1)
-        self.gemm_ws = snip.Workspace(snip.WS_HEADER_BYTES, device) if overlap else self.ws
+        calls = []   # (fn, args, category, units, stream kind 'q'/'g', position, GEMM index or -1)
+        self.gsel = {}   # call index of a GEMM -> its GEMM stream
+        self.gemm_wss = ([snip.Workspace(snip.WS_HEADER_BYTES, device) for _ in self.sGs] if overlap
+                         else [self.ws])
         self._keep = []   # ctypes arrays referenced by the calls
         # Activations read by several linears (Q/K/V, Gate/Up: SNIP, Figure 4): with share_x, their
         # tensor scales, statistics and round-to-nearest row-block quantization (forward operand) are
@@ -533,9 +544,11 @@ class Step:
                     sb = self.scales[b].data_ptr() if f != snip.FP8 else None
                     ga = scp[roles(l)[a][0]] + fo if f != snip.MXFP4 else None
                     gb = scp[roles(l)[b][0]] + fo if f != snip.MXFP4 else None
-                    gw = self.gemm_ws
+                    k = (p if self.gemm_streams == 2 else r // 2) % self.gemm_streams
+                    gw = self.gemm_wss[k]
                     args = (f, ac.data_ptr(), sa, ga, self.codes[b].data_ptr(), sb, gb, M, N, K,
-                            D.data_ptr(), D.stride(0), gw.ptr, gw.nbytes, gstream)
+                            D.data_ptr(), D.stride(0), gw.ptr, gw.nbytes, self.sGs[k].cuda_stream)
+                    self.gsel[len(calls)] = k
                     calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K, "g", p, r // 2))
         self.calls = calls
         # the same calls with every launch on the quantization stream (kernels one after another)
@@ -576,7 +589,7 @@ class Step:
         serial: every kernel on the quantization stream, one after another (per-kernel timing)."""
         import torch
         ready, gdone = {}, {}
-        last_g = None
+        last_g = {}
         overlap = self.overlap and not serial
         cur = torch.cuda.current_stream()
         if cur != self.sQ:
@@ -586,12 +599,13 @@ class Step:
         for i, (fn, args, _, _, kind, p, gi) in enumerate(self.calls):
             if serial:
                 args = self.serial_args[i]
-            stream = self.sQ if kind == "q" or serial else self.sG
+            stream = self.sQ if kind == "q" or serial else self.sGs[self.gsel[i]]
             if overlap:
-                if i in self.wait_at and (p - 2) in gdone:
-                    self.sQ.wait_event(gdone[p - 2])
+                if i in self.wait_at:
+                    for ev in gdone.get(p - 2, []):
+                        self.sQ.wait_event(ev)
                 if kind == "g":
-                    self.sG.wait_event(ready[(p, gi)])
+                    stream.wait_event(ready[(p, gi)])
             if events is not None:
                 events[i][0].record(stream)
             st = fn(*args)
@@ -607,11 +621,12 @@ class Step:
                     ready[(nxt[5], nxt[6])] = ev
                 if kind == "g":
                     ev = torch.cuda.Event()
-                    ev.record(self.sG)
-                    gdone[p] = ev
-                    last_g = ev
-        if overlap and last_g is not None:
-            self.sQ.wait_event(last_g)
+                    ev.record(stream)
+                    gdone.setdefault(p, []).append(ev)
+                    last_g[self.gsel[i]] = ev
+        if overlap:
+            for ev in last_g.values():
+                self.sQ.wait_event(ev)
         if cur != self.sQ:
             ev = torch.cuda.Event()
             ev.record(self.sQ)
@@ -633,8 +648,11 @@ class Step:
         self.graph.replay()
 
     def status(self):
-        s = self.ws.status()
-        return s if s != self.snip.SNIP_OK or not self.overlap else self.gemm_ws.status()
+        for w in [self.ws] + self.gemm_wss:
+            s = w.status()
+            if s != self.snip.SNIP_OK:
+                return s
+        return self.snip.SNIP_OK
 
 
 def quantizer_sweep(snip, hbm_gbs: float, reps: int = 10):
@@ -991,7 +1009,8 @@ def run_ours(args, rank, world, local_rank):
     layers = [x for x in args.layers.split(",") if x]
     graph = not args.no_graph
     step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph,
-                scales_per_launch=args.scales_per_launch, order=linear_order(args))
+                scales_per_launch=args.scales_per_launch, order=linear_order(args),
+                gemm_streams=args.gemm_streams)
     if args.plan == "snip" and layers:
         raise SystemExit("--plan snip selects formats for the whole block; it cannot be combined with --layers")
     if args.plan == "snip":
@@ -1003,7 +1022,8 @@ def run_ours(args, rank, world, local_rank):
         plan, _, _ = snip.snip_plan_select(flops, c8, c4, cfg.fp4_target)
         del step
         step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph,
-                scales_per_launch=args.scales_per_launch, order=linear_order(args))
+                scales_per_launch=args.scales_per_launch, order=linear_order(args),
+                gemm_streams=args.gemm_streams)
     torch.cuda.synchronize()
     ncalls = len(step.calls)
     sampler = ClockSampler(local_rank) if rank == 0 and not args.profile_run else None
@@ -1070,7 +1090,8 @@ def run_ours(args, rank, world, local_rank):
     def time_variant(plan_v, stats_v):
         """Another step of the same block, timed as the headline (K steps after 3 warm-up steps)."""
         sv = Step(cfg, plan_v, snip, "cuda", layers, overlap=not args.no_overlap, stats=stats_v, own_stream=graph,
-                  scales_per_launch=args.scales_per_launch, order=linear_order(args))
+                  scales_per_launch=args.scales_per_launch, order=linear_order(args),
+                gemm_streams=args.gemm_streams)
         for _ in range(3):
             sv.run()
         if graph:

@@ -32,7 +32,11 @@
  *    default stream).  Argument errors are returned synchronously and launch
  *    nothing.  Errors found on the device (non-finite input, a kernel wait
  *    that timed out) are OR-ed into the status word of the caller's workspace
- *    and read with snip_workspace_status().
+ *    and read with snip_workspace_status().  The quantizer and GEMM kernels
+ *    are launched with programmatic dependent launch: the next kernel on the
+ *    stream may be scheduled while one ends, but each waits for the work
+ *    before it on the stream to finish before it reads or writes memory, so
+ *    stream order holds as for ordinary launches.
  *  - Workspace: a caller-owned device buffer of at least the size returned by
  *    the matching *_workspace_size() call.  Its first SNIP_WS_HEADER_BYTES hold
  *    the sticky device status word; initialise them once with

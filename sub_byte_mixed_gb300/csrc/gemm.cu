@@ -188,6 +188,7 @@ __device__ __forceinline__ uint32_t requant32_t(const uint32_t (&r)[32], float a
 template <int FMT, int BN, bool RQ = false>
 __global__ void __launch_bounds__(448, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  pdl_enter();
   using C = GemmCfg<FMT, BN, RQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -492,6 +493,7 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const __grid_constant__ CUtensorMap tmD, GemmParams p) {
+  pdl_enter();
   using C = Gemm2Cfg<FMT, RQ, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -819,8 +821,8 @@ static cudaError_t launch_gemm_cfg(const uint8_t* a_codes, int64_t a_rows, const
   p.num_n_tiles = (int)((p.N + BN - 1) / BN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_tn_kernel<FMT, BN, RQ><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_tn_kernel<FMT, BN, RQ>, (unsigned)grid, (unsigned)C::THREADS, (unsigned)C::SMEM_BYTES, 1u,
+                    st, ta, tb, p);
 }
 
 // 2-D byte view of an MMA-layout scale buffer: rows of 256 bytes, loaded
@@ -880,19 +882,8 @@ static cudaError_t launch_gemm_pair(const uint8_t* a_codes, int64_t a_rows, cons
   p.num_n_tiles = (int)((p.N + C::BN - 1) / C::BN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(C::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<FMT, RQ, NS>, ta, tb, tsa, tsb, td, p);
+  return launch_pdl(gemm_tn_pair_kernel<FMT, RQ, NS>, (unsigned)(2 * pairs), (unsigned)C::THREADS,
+                    (unsigned)C::SMEM_BYTES, 2u, st, ta, tb, tsa, tsb, td, p);
 }
 
 // FP8 on 256 x 512 pair tiles for long contractions (measured on GB300: the

@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restri
                                                         uint32_t* __restrict__ partials,
                                                         uint32_t* __restrict__ counter, float* __restrict__ out3,
                                                         uint32_t* __restrict__ status) {
+  pdl_enter();
   scales_body(x, n, blockIdx.x, gridDim.x, partials, counter, out3, status);
 }
 
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(256, 4) scales_kernel(const uint16_t* __restri
 __global__ void __launch_bounds__(256, 4) scales_multi_kernel(ScalesMulti m, uint32_t* __restrict__ partials,
                                                               uint32_t* __restrict__ counters,
                                                               uint32_t* __restrict__ status) {
+  pdl_enter();
   // this CTA's tensor, picked with constant indices (a run-time index into the parameter block would
   // copy it to local memory)
   const uint16_t* x = m.x[0];
@@ -365,6 +367,7 @@ __device__ __forceinline__ void stats_nan(double* raw_out) {
 // time.
 template <int FMT, int LAYOUT, int RND, bool ERR, bool STATS, bool LONG = false>
 __global__ void __launch_bounds__(256, STATS ? 3 : 4) quant_rows_kernel(QuantParams p) {
+  pdl_enter();
   static_assert(!LONG || (FMT == 1 && STATS), "LONG: NVFP4 with fused statistics");
   static_assert(FMT < 2 || !ERR, "MXFP4 / E5M2 quantization has no block errors");
   // FMT 3 (E5M2): p.scale is the amax; MXFP4: read only for the non-finite check
@@ -532,6 +535,7 @@ constexpr int kXW = kTC / 2 + 4;   // words per staged source row (pairs of bf16
 // b^1, which exchange their half maxima through shared memory).
 template <int FMT, int LAYOUT, int RND, bool ERR, int TR>
 __global__ void __launch_bounds__(2 * TR) quant_cols_kernel(QuantParams p) {
+  pdl_enter();
   static_assert(FMT < 2 || !ERR, "MXFP4 / E5M2 quantization has no block errors");
   static_assert(TR == 64 || TR == 128, "tile rows");
   constexpr bool FP4 = FMT == 1 || FMT == 2;
@@ -702,6 +706,7 @@ __global__ void __launch_bounds__(2 * TR) quant_cols_kernel(QuantParams p) {
 // ------------------------------------------------------------------ a8: statistics kernel
 template <int RND, bool BLK>
 __global__ void __launch_bounds__(256) stats_kernel(StatsParams p) {
+  pdl_enter();
   const float amax = p.scales3[0], g = p.scales3[1], s8 = p.scales3[2];
   if (isnan(amax)) {
     stats_nan(p.raw_out);
@@ -804,7 +809,7 @@ static void launch_persistent(void (*kernel)(P), int64_t want, int max_ctas, int
   const int64_t wave = (int64_t)resident_ctas(reinterpret_cast<const void*>(kernel)) * num_sms;
   if (g > wave) g = wave;
   if (g > max_ctas) g = max_ctas;
-  kernel<<<(unsigned)g, 256, 0, st>>>(p);
+  launch_pdl(kernel, (unsigned)g, 256u, 0u, 1u, st, p);
 }
 
 static int fill_grid(int64_t work_items, int per_cta, int max_ctas) {
@@ -831,15 +836,13 @@ cudaError_t launch_scales_multi(ScalesMulti m, uint32_t* partials, uint32_t* cou
     c += (int)k;
   }
   m.cta0[m.count] = c;
-  scales_multi_kernel<<<c, 256, 0, st>>>(m, partials, counters, status);
-  return cudaGetLastError();
+  return launch_pdl(scales_multi_kernel, (unsigned)c, 256u, 0u, 1u, st, m, partials, counters, status);
 }
 
 cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint32_t* counter, float* out3,
                           uint32_t* status, int num_sms, cudaStream_t st) {
   const int grid = fill_grid(n >> 3, 256 * 4, std::min(4 * num_sms, kMaxPartials));
-  scales_kernel<<<grid, 256, 0, st>>>(x, n, partials, counter, out3, status);
-  return cudaGetLastError();
+  return launch_pdl(scales_kernel, (unsigned)grid, 256u, 0u, 1u, st, x, n, partials, counter, out3, status);
 }
 
 // a row-block quantization (persistent: want CTAs at most, cap partial slots)
@@ -848,7 +851,7 @@ cudaError_t launch_scales(const uint16_t* x, int64_t n, uint32_t* partials, uint
 template <int FMT, int LY, int RN, bool ER, int TR>
 static void launch_cols(const QuantParams& p, cudaStream_t st) {
   const int64_t tiles = ((p.ocp + TR - 1) / TR) * ((p.orp + kTC - 1) / kTC);   // checked < 2^31 by the API
-  quant_cols_kernel<FMT, LY, RN, ER, TR><<<(unsigned)tiles, 2 * TR, 0, st>>>(p);
+  launch_pdl(quant_cols_kernel<FMT, LY, RN, ER, TR>, (unsigned)tiles, (unsigned)(2 * TR), 0u, 1u, st, p);
 }
 
 template <int FMT>

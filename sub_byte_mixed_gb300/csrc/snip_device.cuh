@@ -16,6 +16,16 @@
 
 namespace snip {
 
+// Programmatic dependent launch (the kernels of this library are launched with programmatic stream
+// serialization): every kernel first lets the next kernel on its stream be scheduled, then waits
+// until the work it follows on the stream has finished and its writes are visible, before it touches
+// memory; so stream order holds as with ordinary launches, and only the next launch's scheduling
+// overlaps this one's end.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Status bits OR-ed into the workspace status word by kernels.
 constexpr uint32_t kDevNonFinite = 1u;
 constexpr uint32_t kDevTimeout = 2u;

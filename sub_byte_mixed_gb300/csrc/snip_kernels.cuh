@@ -188,6 +188,28 @@ EncodeTiledFn tensor_map_encoder();
 // device (the attribute is per device; thread-safe).  Defined in quant.cu.
 cudaError_t ensure_max_dynamic_smem(const void* fn, int bytes);
 
+// Launch with programmatic stream serialization (the kernel starts with pdl_enter) and, for cluster > 1,
+// thread-block clusters of that many CTAs along x.
+template <class... K, class... A>
+cudaError_t launch_pdl(void (*kernel)(K...), unsigned grid, unsigned block, unsigned smem, unsigned cluster,
+                       cudaStream_t st, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Self-check of the bounded wait (waitcheck.cu): out = {completed 0, completed 1, ns}.
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, uint32_t* out, cudaStream_t st);
 

@@ -7,8 +7,11 @@ written it or after the next user of its buffer set has overwritten it.  The
 step that computes a shared activation's scales, statistics and forward
 quantization once (Q/K/V, Gate/Up), with the tensor scales of several linears
 in one launch, gives exactly the results of the step that recomputes them for
-every linear with one tensor-scale launch per linear, and so does the step that
-runs the linears in another order."""
+every linear with one tensor-scale launch per linear, and so do the steps that
+run the linears in another order and spread the GEMMs over one, two (linears
+alternating) or three (forward, dgrad, wgrad) streams.  Every kernel is
+launched with programmatic stream serialization, so this also checks that each
+waits for the work it follows on its stream."""
 import os
 import sys
 
@@ -51,7 +54,7 @@ def test_two_stream_step_matches_one_stream(plan_kind):
         assert torch.equal(ref[2][j], ref0[2][j]), ("shared X", j)
     assert (serial.stats_host() == ref0[3]).all()
     del serial
-    over = bench.Step(cfg, plan, snip, "cuda", overlap=True)
+    over = bench.Step(cfg, plan, snip, "cuda", overlap=True, gemm_streams=1)
     for _ in range(2):   # the second step also reuses both buffer sets across the step boundary
         over.run()
     torch.cuda.synchronize()
@@ -64,7 +67,7 @@ def test_two_stream_step_matches_one_stream(plan_kind):
     del over
     # the linears in another order (the shared activations' users no longer adjacent)
     order = ["Q", "Gate", "Up", "Down", "K", "V", "O"]
-    moved = bench.Step(cfg, plan, snip, "cuda", overlap=True, order=order)
+    moved = bench.Step(cfg, plan, snip, "cuda", overlap=True, order=order, gemm_streams=2)
     assert moved.order == order
     for _ in range(2):
         moved.run()
