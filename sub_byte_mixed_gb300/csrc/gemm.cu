@@ -188,7 +188,9 @@ __device__ __forceinline__ uint32_t requant32_t(const uint32_t (&r)[32], float a
 template <int FMT, int BN, bool RQ = false>
 __global__ void __launch_bounds__(448, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
-  pdl_enter();
+  // the set-up below touches no memory that earlier work on the stream writes: it overlaps that
+  // work's end, and the wait comes before the first operand load, scale read or store
+  pdl_launch_dependents();
   using C = GemmCfg<FMT, BN, RQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -217,6 +219,7 @@ __global__ void __launch_bounds__(448, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();
   const uint32_t tmem = *tmem_slot;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
   const int64_t sf_chunks_per_group = p.kp >> (FMT == 2 ? 7 : 6);   // 512-byte scale chunks per 128-row group
@@ -493,7 +496,9 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const __grid_constant__ CUtensorMap tmD, GemmParams p) {
-  pdl_enter();
+  // the set-up below touches no memory that earlier work on the stream writes: it overlaps that
+  // work's end, and the wait comes before the first operand load, scale read or store
+  pdl_launch_dependents();
   using C = Gemm2Cfg<FMT, RQ, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -529,6 +534,7 @@ __global__ void __maxnreg__(RQ ? 128 : 96)
   __syncthreads();
   cluster_sync();   // both CTAs' barriers and tensor memory exist before any cross-CTA traffic
   tc_fence_after();
+  pdl_wait();
   const uint32_t tmem = *tmem_slot;
   const int num_pairs = gridDim.x >> 1, pair = blockIdx.x >> 1;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;   // 256 x 256 tiles

@@ -21,9 +21,11 @@ namespace snip {
 // until the work it follows on the stream has finished and its writes are visible, before it touches
 // memory; so stream order holds as with ordinary launches, and only the next launch's scheduling
 // overlaps this one's end.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_enter() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_launch_dependents();
+  pdl_wait();
 }
 
 // Status bits OR-ed into the workspace status word by kernels.
