@@ -224,10 +224,12 @@ struct StatsAcc {
   }
 };
 // BE: also return the block's two squared errors (per-block error outputs).
-template <int CF, int RND, bool BE = false>
-__device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
-                                              float s8, float inv8, bool special8, uint4& codes, StatsAcc& acc,
-                                              float* be4 = nullptr, float* be8 = nullptr) {
+// GEN: the general form, which handles a special NVFP4 block scale or FP8 tensor scale; without it
+// both are taken as ordinary, and the unrolled body has no branch (stats_block16 picks the form).
+template <int CF, int RND, bool BE, bool GEN>
+__device__ __forceinline__ void stats_block16_form(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
+                                                   float s8, float inv8, bool special8, uint4& codes, StatsAcc& acc,
+                                                   float* be4, float* be8) {
   float2 S4 = make_float2(0.f, 0.f), b4 = S4, b8 = S4;
   float T4 = 0.f;
   uint32_t cw[4] = {0u, 0u, 0u, 0u};
@@ -247,7 +249,7 @@ __device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockS
       g19 = sr_g2<19>(f0, f1);
     }
     // ---------------- NVFP4
-    if (bs.special) {
+    if (GEN && bs.special) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const float q = (bs.p == 0.0f || v[i + k] == 0.0f) ? 0.0f : copysignf(6.0f, v[i + k]);
@@ -272,7 +274,7 @@ __device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockS
       T4 = fmaf(fabsf(c.y), H.y, T4);
     }
     // ---------------- FP8
-    if (special8) {
+    if (GEN && special8) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const float q = v[i + k] == 0.0f ? 0.0f : copysignf(448.0f, v[i + k]);
@@ -298,7 +300,7 @@ __device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockS
     }
   }
   // the NVFP4 variance was summed in units of this block's scale
-  if (!bs.special) acc.v4 = fmaf(fmaf(0.5f, T4, -(S4.x + S4.y)), bs.p * bs.p, acc.v4);
+  if (!(GEN && bs.special)) acc.v4 = fmaf(fmaf(0.5f, T4, -(S4.x + S4.y)), bs.p * bs.p, acc.v4);
   if (BE) {
     *be4 = b4.x + b4.y;
     *be8 = b8.x + b8.y;
@@ -306,6 +308,15 @@ __device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockS
     acc.e8.x += *be8;
   }
   codes = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+}
+template <int CF, int RND, bool BE = false>
+__device__ __forceinline__ void stats_block16(const float (&v)[16], const BlockScale& bs, const uint32_t (&u)[8],
+                                              float s8, float inv8, bool special8, uint4& codes, StatsAcc& acc,
+                                              float* be4 = nullptr, float* be8 = nullptr) {
+  if (bs.special || special8)
+    stats_block16_form<CF, RND, BE, true>(v, bs, u, s8, inv8, special8, codes, acc, be4, be8);
+  else
+    stats_block16_form<CF, RND, BE, false>(v, bs, u, s8, inv8, special8, codes, acc, be4, be8);
 }
 
 // CTA reduction of the five fp32 per-thread sums into fp64, then the last CTA
