@@ -72,6 +72,9 @@ def parse_args(argv=None):
     ap.add_argument("--gemm-streams", type=int, default=3, choices=[1, 2, 3],
                     help="GEMM streams of the overlapped step: 1; 2, linears alternating; 3 (default), one per "
                          "GEMM kind")
+    ap.add_argument("--no-scales-stream", action="store_true",
+                    help="tensor-scale passes on the quantization stream (default: a stream of their own, "
+                         "two linears ahead)")
     ap.add_argument("--order", default="",
                     help="comma-separated order in which the step runs its linears (default: the model's)")
     ap.add_argument("--layers", default="", help="comma-separated subset of Q,K,V,O,Gate,Up,Down (profiling)")
@@ -125,7 +128,10 @@ def config_json(cfg, plan, args):
                     + (f"; linears run in the order {args.order}" if args.order else "")
                     + ("" if args.no_overlap else
                        f"; GEMMs on {args.gemm_streams} stream{'s' if args.gemm_streams > 1 else ''}"
-                       + (" (forward, dgrad, wgrad each on its own)" if args.gemm_streams == 3 else "")),
+                       + (" (forward, dgrad, wgrad each on its own)" if args.gemm_streams == 3 else "")
+                       + ("" if args.no_scales_stream else
+                          "; tensor-scale passes on a stream of their own, each after the quantizations two "
+                          "linears back")),
         "plan_source": ("SNIP selection from one step's statistics (snip_plan_select, FP4-FLOP target "
                         f"{cfg.fp4_target})") if args.plan == "snip" else
                        ("seeded plan at the FP4-FLOP target" if args.plan == "mix" else "uniform"),
@@ -355,7 +361,7 @@ class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
     def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True, own_stream=False,
-                 share_x=True, scales_per_launch=3, order=None, gemm_streams=3):
+                 share_x=True, scales_per_launch=3, order=None, gemm_streams=3, scales_stream=True):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
@@ -370,6 +376,10 @@ class Step:
         # overlap the next GEMM, which reads other operands and writes another output)
         self.gemm_streams = gemm_streams if overlap else 1
         self.sGs = [torch.cuda.Stream() for _ in range(self.gemm_streams)] if overlap else [self.sQ]
+        # scales_stream: the tensor-scale passes on a stream of their own, each started once the
+        # quantizations two positions back are done, so that it can run beside the GEMMs (which
+        # leave registers and bandwidth to spare on their SMs) instead of on the quantization stream
+        self.sS = torch.cuda.Stream() if overlap and scales_stream else None
         self.graph = None
         nsets = 2 if overlap else 1
         L = snip.load()
@@ -399,6 +409,8 @@ class Step:
         self.gsel = {}   # call index of a GEMM -> its GEMM stream
         self.gemm_wss = ([snip.Workspace(snip.WS_HEADER_BYTES, device) for _ in self.sGs] if overlap
                          else [self.ws])
+        self.ws_s = snip.Workspace(snip.snip_quantize_workspace_size(0, 0), device) if self.sS is not None else None
+        self.scale_call = {}   # call index of a scale pass -> its arguments on the scales stream
         self._keep = []   # ctypes arrays referenced by the calls
         # Activations read by several linears (Q/K/V, Gate/Up: SNIP, Figure 4): with share_x, their
         # tensor scales, statistics and round-to-nearest row-block quantization (forward operand) are
@@ -475,6 +487,9 @@ class Step:
                 ns = (ctypes.c_int64 * len(items))(*[t.numel() for t, _ in items])
                 outs = (ctypes.c_void_p * len(items))(*[o for _, o in items])
                 self._keep.append((xs, ns, outs))
+                if self.sS is not None:
+                    self.scale_call[len(calls)] = (len(items), xs, ns, outs, self.ws_s.ptr, self.ws_s.nbytes,
+                                                   self.sS.cuda_stream)
                 calls.append((L.snip_tensor_scales_multi, (len(items), xs, ns, outs, ws, wsb, stream), "scales",
                               SCALES_BYTES_PER_ELEM * sum(t.numel() for t, _ in items), "q", p, -1))
             self.wait_at[len(calls)] = p
@@ -551,6 +566,10 @@ class Step:
                     self.gsel[len(calls)] = k
                     calls.append((L.snip_gemm, args, gcat, 2.0 * M * N * K, "g", p, r // 2))
         self.calls = calls
+        self.last_q = {}   # position -> index of its last quantization (tensor-scale passes excluded)
+        for i, c in enumerate(calls):
+            if c[4] == "q" and c[2] != "scales":
+                self.last_q[c[5]] = i
         # the same calls with every launch on the quantization stream (kernels one after another)
         self.serial_args = [a if k == "q" else a[:-1] + (stream,) for (_, a, _, _, k, _, _) in calls]
         # one kernel per call (the scales are computed once per tensor and passed in; every plan
@@ -590,6 +609,8 @@ class Step:
         import torch
         ready, gdone = {}, {}
         last_g = {}
+        qdone, sdone = {}, {}   # position -> event: its last quantization; its scale pass
+        last_s = None
         overlap = self.overlap and not serial
         cur = torch.cuda.current_stream()
         if cur != self.sQ:
@@ -600,10 +621,21 @@ class Step:
             if serial:
                 args = self.serial_args[i]
             stream = self.sQ if kind == "q" or serial else self.sGs[self.gsel[i]]
+            on_s = overlap and i in self.scale_call
+            if on_s:
+                args, stream = self.scale_call[i], self.sS
+                if (p - 2) in qdone:
+                    self.sS.wait_event(qdone[p - 2])
+                elif last_s is None:   # the first pass follows the caller's work
+                    ev = torch.cuda.Event()
+                    ev.record(self.sQ)
+                    self.sS.wait_event(ev)
             if overlap:
                 if i in self.wait_at:
                     for ev in gdone.get(p - 2, []):
                         self.sQ.wait_event(ev)
+                    if p in sdone:
+                        self.sQ.wait_event(sdone[p])
                 if kind == "g":
                     stream.wait_event(ready[(p, gi)])
             if events is not None:
@@ -613,8 +645,17 @@ class Step:
                 raise RuntimeError(f"{fn.__name__} failed with status {st}")
             if events is not None:
                 events[i][1].record(stream)
+            if on_s:
+                ev = torch.cuda.Event()
+                ev.record(self.sS)
+                sdone[p] = ev
+                last_s = ev
             if overlap:
                 nxt = self.calls[i + 1] if i + 1 < len(self.calls) else None
+                if self.scale_call and i == self.last_q.get(p):   # the last quantization of position p
+                    ev = torch.cuda.Event()
+                    ev.record(self.sQ)
+                    qdone[p] = ev
                 if kind == "q" and nxt is not None and nxt[4] == "g":   # both operands of the next GEMM written
                     ev = torch.cuda.Event()
                     ev.record(self.sQ)
@@ -627,6 +668,8 @@ class Step:
         if overlap:
             for ev in last_g.values():
                 self.sQ.wait_event(ev)
+            if last_s is not None:
+                self.sQ.wait_event(last_s)
         if cur != self.sQ:
             ev = torch.cuda.Event()
             ev.record(self.sQ)
@@ -648,7 +691,7 @@ class Step:
         self.graph.replay()
 
     def status(self):
-        for w in [self.ws] + self.gemm_wss:
+        for w in [self.ws] + self.gemm_wss + ([self.ws_s] if self.ws_s is not None else []):
             s = w.status()
             if s != self.snip.SNIP_OK:
                 return s
@@ -1010,7 +1053,7 @@ def run_ours(args, rank, world, local_rank):
     graph = not args.no_graph
     step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph,
                 scales_per_launch=args.scales_per_launch, order=linear_order(args),
-                gemm_streams=args.gemm_streams)
+                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream)
     if args.plan == "snip" and layers:
         raise SystemExit("--plan snip selects formats for the whole block; it cannot be combined with --layers")
     if args.plan == "snip":
@@ -1023,7 +1066,7 @@ def run_ours(args, rank, world, local_rank):
         del step
         step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph,
                 scales_per_launch=args.scales_per_launch, order=linear_order(args),
-                gemm_streams=args.gemm_streams)
+                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream)
     torch.cuda.synchronize()
     ncalls = len(step.calls)
     sampler = ClockSampler(local_rank) if rank == 0 and not args.profile_run else None
@@ -1091,7 +1134,7 @@ def run_ours(args, rank, world, local_rank):
         """Another step of the same block, timed as the headline (K steps after 3 warm-up steps)."""
         sv = Step(cfg, plan_v, snip, "cuda", layers, overlap=not args.no_overlap, stats=stats_v, own_stream=graph,
                   scales_per_launch=args.scales_per_launch, order=linear_order(args),
-                gemm_streams=args.gemm_streams)
+                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream)
         for _ in range(3):
             sv.run()
         if graph:

@@ -8,8 +8,9 @@ step that computes a shared activation's scales, statistics and forward
 quantization once (Q/K/V, Gate/Up), with the tensor scales of several linears
 in one launch, gives exactly the results of the step that recomputes them for
 every linear with one tensor-scale launch per linear, and so do the steps that
-run the linears in another order and spread the GEMMs over one, two (linears
-alternating) or three (forward, dgrad, wgrad) streams.  Every kernel is
+run the linears in another order, spread the GEMMs over one, two (linears
+alternating) or three (forward, dgrad, wgrad) streams, and put the tensor-scale
+passes on a stream of their own.  Every kernel is
 launched with programmatic stream serialization, so this also checks that each
 waits for the work it follows on its stream."""
 import os
@@ -54,7 +55,7 @@ def test_two_stream_step_matches_one_stream(plan_kind):
         assert torch.equal(ref[2][j], ref0[2][j]), ("shared X", j)
     assert (serial.stats_host() == ref0[3]).all()
     del serial
-    over = bench.Step(cfg, plan, snip, "cuda", overlap=True, gemm_streams=1)
+    over = bench.Step(cfg, plan, snip, "cuda", overlap=True, gemm_streams=1, scales_stream=False)
     for _ in range(2):   # the second step also reuses both buffer sets across the step boundary
         over.run()
     torch.cuda.synchronize()
@@ -67,7 +68,7 @@ def test_two_stream_step_matches_one_stream(plan_kind):
     del over
     # the linears in another order (the shared activations' users no longer adjacent)
     order = ["Q", "Gate", "Up", "Down", "K", "V", "O"]
-    moved = bench.Step(cfg, plan, snip, "cuda", overlap=True, order=order, gemm_streams=2)
+    moved = bench.Step(cfg, plan, snip, "cuda", overlap=True, order=order, gemm_streams=2, scales_stream=True)
     assert moved.order == order
     for _ in range(2):
         moved.run()
