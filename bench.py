@@ -66,9 +66,9 @@ def parse_args(argv=None):
                          "block's shapes (builds cublaslt_gemm.cu), one JSON line")
     ap.add_argument("--profile-run", action="store_true",
                     help="exactly --warmup untimed steps, no clock settle, e2e or CPU baseline (for ncu)")
-    ap.add_argument("--scales-per-launch", type=int, default=3,
-                    help="most tensors whose scales one launch computes (3 or less: one launch per linear, "
-                         "the default; packing several linears into one launch measured slower)")
+    ap.add_argument("--scales-per-launch", type=int, default=5,
+                    help="most tensors whose scales one launch computes, whole linears packed in order "
+                         "(3 or less: one launch per linear)")
     ap.add_argument("--gemm-streams", type=int, default=3, choices=[1, 2, 3],
                     help="GEMM streams of the overlapped step: 1; 2, linears alternating; 3 (default), one per "
                          "GEMM kind")
@@ -361,7 +361,7 @@ class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
     def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True, own_stream=False,
-                 share_x=True, scales_per_launch=3, order=None, gemm_streams=3, scales_stream=True):
+                 share_x=True, scales_per_launch=5, order=None, gemm_streams=3, scales_stream=True):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
