@@ -75,6 +75,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-scales-stream", action="store_true",
                     help="tensor-scale passes on the quantization stream (default: a stream of their own, "
                          "two linears ahead)")
+    ap.add_argument("--scales-lead", type=int, default=2,
+                    help="a linear's scale pass starts after the quantizations this many linears back")
     ap.add_argument("--order", default="",
                     help="comma-separated order in which the step runs its linears (default: the model's)")
     ap.add_argument("--layers", default="", help="comma-separated subset of Q,K,V,O,Gate,Up,Down (profiling)")
@@ -361,7 +363,8 @@ class Step:
     """Pre-marshalled C-ABI calls of one step (ctypes function + fixed args)."""
 
     def __init__(self, cfg, plan, snip, device, layers=None, overlap=True, stats=True, own_stream=False,
-                 share_x=True, scales_per_launch=5, order=None, gemm_streams=3, scales_stream=True):
+                 share_x=True, scales_per_launch=5, order=None, gemm_streams=3, scales_stream=True,
+                 scales_lead=2):
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
@@ -380,6 +383,7 @@ class Step:
         # quantizations two positions back are done, so that it can run beside the GEMMs (which
         # leave registers and bandwidth to spare on their SMs) instead of on the quantization stream
         self.sS = torch.cuda.Stream() if overlap and scales_stream else None
+        self.scales_lead = scales_lead   # the pass of position p waits for the quantizations of p - scales_lead
         self.graph = None
         nsets = 2 if overlap else 1
         L = snip.load()
@@ -624,8 +628,8 @@ class Step:
             on_s = overlap and i in self.scale_call
             if on_s:
                 args, stream = self.scale_call[i], self.sS
-                if (p - 2) in qdone:
-                    self.sS.wait_event(qdone[p - 2])
+                if (p - self.scales_lead) in qdone:
+                    self.sS.wait_event(qdone[p - self.scales_lead])
                 elif last_s is None:   # the first pass follows the caller's work
                     ev = torch.cuda.Event()
                     ev.record(self.sQ)
@@ -1053,7 +1057,8 @@ def run_ours(args, rank, world, local_rank):
     graph = not args.no_graph
     step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph,
                 scales_per_launch=args.scales_per_launch, order=linear_order(args),
-                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream)
+                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream,
+                scales_lead=args.scales_lead)
     if args.plan == "snip" and layers:
         raise SystemExit("--plan snip selects formats for the whole block; it cannot be combined with --layers")
     if args.plan == "snip":
@@ -1066,7 +1071,8 @@ def run_ours(args, rank, world, local_rank):
         del step
         step = Step(cfg, plan, snip, "cuda", layers, overlap=not args.no_overlap, own_stream=graph,
                 scales_per_launch=args.scales_per_launch, order=linear_order(args),
-                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream)
+                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream,
+                scales_lead=args.scales_lead)
     torch.cuda.synchronize()
     ncalls = len(step.calls)
     sampler = ClockSampler(local_rank) if rank == 0 and not args.profile_run else None
@@ -1134,7 +1140,8 @@ def run_ours(args, rank, world, local_rank):
         """Another step of the same block, timed as the headline (K steps after 3 warm-up steps)."""
         sv = Step(cfg, plan_v, snip, "cuda", layers, overlap=not args.no_overlap, stats=stats_v, own_stream=graph,
                   scales_per_launch=args.scales_per_launch, order=linear_order(args),
-                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream)
+                gemm_streams=args.gemm_streams, scales_stream=not args.no_scales_stream,
+                scales_lead=args.scales_lead)
         for _ in range(3):
             sv.run()
         if graph:
