@@ -26,8 +26,8 @@ constexpr size_t kOffScaleSlots = 64;   // 8 slots x 4 floats {amax, NVFP4 g, FP
 static_assert(kOffMultiCounters + 4 * kMaxMultiScales <= kOffScaleSlots, "multi-scale counters overlap the scale slots");
 constexpr size_t kOffAmaxPartials = SNIP_WS_HEADER_BYTES;                            // kMaxPartials x uint32
 constexpr size_t kOffStatsPartials = kOffAmaxPartials + 4 * kMaxPartials;            // kMaxPartials x 5 doubles
-constexpr size_t kSmallWorkspace = kOffStatsPartials + 8 * 5 * kMaxPartials;         // 45312
-constexpr size_t kSmallWorkspaceRounded = (kSmallWorkspace + 4095) / 4096 * 4096;   // 49152
+constexpr size_t kSmallWorkspace = kOffStatsPartials + 8 * 5 * kMaxPartials;         // 90368
+constexpr size_t kSmallWorkspaceRounded = (kSmallWorkspace + 4095) / 4096 * 4096;   // 94208
 
 constexpr uint64_t kTimeoutNs = 4000000000ull;   // a GEMM wait that takes 4 s is a fault
 

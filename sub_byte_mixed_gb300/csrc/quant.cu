@@ -810,15 +810,18 @@ cudaError_t ensure_max_dynamic_smem(const void* fn, int bytes) {
   return e;
 }
 
-// A grid-stride (persistent) kernel: as many CTAs as the work asks for, but no more than one wave of
-// resident CTAs -- every CTA has the same share of the work, so a second, partial wave would run
-// with most SMs idle -- and no more than max_ctas (the partial-result slots).
+// A grid-stride kernel: as many CTAs as the work asks for, but no more than two waves of resident
+// CTAs, and no more than max_ctas (the partial-result slots).  Every CTA has the same share of the
+// work.  Alone on the GPU the two waves run one after the other at the speed of one; beside another
+// kernel that holds part of every SM (a GEMM's CTA) only some CTAs are resident at a time, and
+// shares half the size let the CTAs that start late finish sooner (measured on the 7B step: one wave
+// 2337, two 2361, four 2327 TFLOP/s).
 template <class P>
 static void launch_persistent(void (*kernel)(P), int64_t want, int max_ctas, int num_sms, cudaStream_t st,
                               const P& p) {
   int64_t g = want < 1 ? 1 : want;
   const int64_t wave = (int64_t)resident_ctas(reinterpret_cast<const void*>(kernel)) * num_sms;
-  if (g > wave) g = wave;
+  if (g > 2 * wave) g = 2 * wave;
   if (g > max_ctas) g = max_ctas;
   launch_pdl(kernel, (unsigned)g, 256u, 0u, 1u, st, p);
 }

@@ -214,7 +214,7 @@ cudaError_t launch_pdl(void (*kernel)(K...), unsigned grid, unsigned block, unsi
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, uint32_t* out, cudaStream_t st);
 
 // Upper bound on the number of amax / stats partial slots any launch uses.
-constexpr int kMaxPartials = 1024;
+constexpr int kMaxPartials = 2048;
 
 __device__ __forceinline__ U4 make_zero_u4() { return U4{0u, 0u, 0u, 0u}; }
 
