@@ -368,8 +368,8 @@ class Step:
         import torch
         from sub_byte_mixed_gb300 import inputs
         self.cfg, self.plan, self.snip = cfg, plan, snip
-        # overlap: quantizations on one stream, GEMMs on another, so that a linear's quantizations run
-        # beside the previous linear's GEMMs; operand buffers alternate between two sets by linear
+        # overlap: quantizations on one stream, GEMMs on others, so that a linear's quantizations run
+        # beside the previous linear's GEMMs; operand buffers alternate between two sets by position
         self.overlap = overlap
         # own_stream: the quantization stream is a stream of its own (a graph cannot be captured on
         # the default stream); run() then joins the caller's stream at both ends
@@ -380,8 +380,9 @@ class Step:
         self.gemm_streams = gemm_streams if overlap else 1
         self.sGs = [torch.cuda.Stream() for _ in range(self.gemm_streams)] if overlap else [self.sQ]
         # scales_stream: the tensor-scale passes on a stream of their own, each started once the
-        # quantizations two positions back are done, so that it can run beside the GEMMs (which
-        # leave registers and bandwidth to spare on their SMs) instead of on the quantization stream
+        # quantizations scales_lead positions back are done, so that it can run beside the GEMMs
+        # (which leave registers and bandwidth to spare on their SMs) instead of on the quantization
+        # stream
         self.sS = torch.cuda.Stream() if overlap and scales_stream else None
         self.scales_lead = scales_lead   # the pass of position p waits for the quantizations of p - scales_lead
         self.graph = None
