@@ -282,8 +282,12 @@ __device__ __forceinline__ void stats_block16_form(const float (&v)[16], const B
         E8.x = fmaf(d, d, E8.x);
       }
     } else {
-      const float2 y = __fmul2_rn(va, i8);
-      const float2 yc = make_float2(fminf(y.x, 448.0f), fminf(y.y, 448.0f));
+      // y is not clamped to 448: under the tensor scale only an element equal to the tensor's amax
+      // can pass 448 (any other bf16 value is smaller by a factor of at most 1 - 2^-8), and only by the
+      // roundings of amax / 448, its inverse and the product (under 2^-21 relative); its grid value
+      // is 448 either way, so codes and error sums are those of the clamped form, and its SR-variance
+      // term moves by under 2^-21 * 448 * H
+      const float2 yc = __fmul2_rn(va, i8);
       const float2 H = make_float2(e4m3_step_x8(yc.x), e4m3_step_x8(yc.y));
       const float2 q = RND ? grid_sr2(yc, H, g19, 1048576.0f) : grid_rn2(yc, H, 1048576.0f);
       if (CF == 0) {
