@@ -201,9 +201,10 @@ __device__ __forceinline__ float e5m2_tensor_scale(float amax) {
 // and each candidate's rounding is the FMA-pipe form (grid_rn2 / grid_sr2),
 // which gives the grid value q of the code the rule picks; the code is then
 // the hardware conversion of that exact value.  With y clamped to the grid's
-// top (yc) and c = q - yc, the expected SR variance (hi - y)(y - lo) is
-// |c| (h - |c|) whichever neighbour q is, summed as 1/2 sum |c| H - sum c^2
-// (H = twice the E2M1 step; eight times the E4M3 step with 1/8).
+// top (yc; the FP8 candidate needs no clamp, see there) and c = q - yc, the
+// expected SR variance (hi - y)(y - lo) is |c| (h - |c|) whichever neighbour
+// q is, summed as 1/2 sum |c| H - sum c^2 (H = twice the E2M1 step; eight
+// times the E4M3 step with 1/8).
 // The running sums of one thread over its blocks.  Only the NVFP4 variance is
 // scaled per block (by its p^2); everything else accumulates across blocks
 // (the FP8 variance in units of the tensor scale s8, multiplied at the end).
